@@ -1,0 +1,214 @@
+"""CPU oracle for batch-1 greedy decoding (TEST INFRASTRUCTURE ONLY).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The product path never does, and this
+package imports nothing from it: the two share only the seeded input
+generators in ``synthetic``.
+
+The arithmetic lives in ``oracle.c`` (plain C, FP32 math, BF16 weights and
+BF16 activations at the rounding points stated in that file's header); this
+module builds it with gcc and marshals numpy arrays through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class OrcModel(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab",
+                 "max_pos", "qk_norm", "rope_scaling")] + \
+               [(n, ctypes.c_double) for n in
+                ("rope_theta", "rs_factor", "rs_low", "rs_high", "rs_orig_max")] + \
+               [("rms_eps", ctypes.c_float)]
+
+
+_SLOTS = ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "ffn_norm", "w_gate",
+          "w_up", "w_down")
+
+
+class OrcLayer(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _SLOTS]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc -O2, OpenMP, no FP contraction)."""
+    if not force and os.path.exists(_LIB_PATH) and \
+            os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+                           "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB_PATH)
+            vp, i32, f32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int64
+            L.orc_bf16_from_f32.argtypes = [f32]
+            L.orc_bf16_from_f32.restype = ctypes.c_uint16
+            L.orc_f32_from_bf16.argtypes = [ctypes.c_uint16]
+            L.orc_f32_from_bf16.restype = f32
+            L.orc_bf16_round_array.argtypes = [vp, vp, i64]
+            L.orc_rmsnorm.argtypes = [vp, vp, i32, f32, vp]
+            L.orc_rope_inv_freq.argtypes = [ctypes.POINTER(OrcModel), vp]
+            L.orc_rope_cos_sin.argtypes = [ctypes.POINTER(OrcModel), i32, vp, vp]
+            L.orc_rope_apply.argtypes = [vp, i32, vp, vp]
+            L.orc_gemv.argtypes = [vp, i32, i32, vp, vp]
+            L.orc_attention.argtypes = [vp, vp, vp, i32, i32, f32, vp]
+            L.orc_attention_split.argtypes = [vp, vp, vp, i32, i32, f32, i32, vp, vp]
+            L.orc_decode.argtypes = [ctypes.POINTER(OrcModel), ctypes.POINTER(OrcLayer), vp, vp,
+                                     vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32]
+            L.orc_decode.restype = i32
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ------------------------------------------------------------- elementary ops
+def bf16_from_f32(x) -> np.ndarray:
+    x = _c(np.atleast_1d(x), np.float32)
+    out = np.empty(x.shape, np.uint16)
+    lib().orc_bf16_round_array(x.ctypes.data, out.ctypes.data, x.size)
+    return out
+
+
+def f32_from_bf16(b) -> np.ndarray:
+    b = _c(np.atleast_1d(b), np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def rmsnorm(x, g_bf16, eps: float) -> np.ndarray:
+    x = _c(x, np.float32)
+    g = _c(g_bf16, np.uint16)
+    out = np.empty_like(x)
+    lib().orc_rmsnorm(x.ctypes.data, g.ctypes.data, x.size, eps, out.ctypes.data)
+    return out
+
+
+def model_struct(cfg) -> OrcModel:
+    return OrcModel(n_layers=cfg.n_layers, hidden=cfg.hidden, n_q_heads=cfg.n_q_heads,
+                    n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim, ffn=cfg.ffn,
+                    vocab=cfg.vocab, max_pos=cfg.max_pos, qk_norm=int(cfg.qk_norm),
+                    rope_scaling=int(cfg.rope_scaling), rope_theta=cfg.rope_theta,
+                    rs_factor=cfg.rs_factor, rs_low=cfg.rs_low, rs_high=cfg.rs_high,
+                    rs_orig_max=float(cfg.rs_orig_max), rms_eps=cfg.rms_eps)
+
+
+def rope_inv_freq(cfg) -> np.ndarray:
+    m = model_struct(cfg)
+    out = np.empty(cfg.head_dim // 2, np.float64)
+    lib().orc_rope_inv_freq(ctypes.byref(m), out.ctypes.data)
+    return out
+
+
+def rope_cos_sin(cfg, pos: int):
+    m = model_struct(cfg)
+    c = np.empty(cfg.head_dim // 2, np.float32)
+    s = np.empty(cfg.head_dim // 2, np.float32)
+    lib().orc_rope_cos_sin(ctypes.byref(m), pos, c.ctypes.data, s.ctypes.data)
+    return c, s
+
+
+def rope_apply(v, cos, sin) -> np.ndarray:
+    v = _c(v, np.float32).copy()
+    cos = _c(cos, np.float32)
+    sin = _c(sin, np.float32)
+    lib().orc_rope_apply(v.ctypes.data, v.size, cos.ctypes.data, sin.ctypes.data)
+    return v
+
+
+def gemv(W_bf16, x) -> np.ndarray:
+    W = _c(W_bf16, np.uint16)
+    x = _c(x, np.float32)
+    y = np.empty(W.shape[0], np.float32)
+    lib().orc_gemv(W.ctypes.data, W.shape[0], W.shape[1], x.ctypes.data, y.ctypes.data)
+    return y
+
+
+def attention(q, K_bf16, V_bf16, scale: float) -> np.ndarray:
+    q = _c(q, np.float32)
+    K = _c(K_bf16, np.uint16)
+    V = _c(V_bf16, np.uint16)
+    out = np.empty(q.size, np.float32)
+    lib().orc_attention(q.ctypes.data, K.ctypes.data, V.ctypes.data, K.shape[0], q.size, scale,
+                        out.ctypes.data)
+    return out
+
+
+def attention_split(q, K_bf16, V_bf16, scale: float, bounds) -> np.ndarray:
+    q = _c(q, np.float32)
+    K = _c(K_bf16, np.uint16)
+    V = _c(V_bf16, np.uint16)
+    b = _c(bounds, np.int32)
+    out = np.empty(q.size, np.float32)
+    lib().orc_attention_split(q.ctypes.data, K.ctypes.data, V.ctypes.data, K.shape[0], q.size,
+                              scale, b.size - 1, b.ctypes.data, out.ctypes.data)
+    return out
+
+
+# ------------------------------------------------------------- whole decoder
+class DecodeResult:
+    def __init__(self, tokens, logits, gaps):
+        self.tokens = tokens
+        self.logits = logits
+        self.gaps = gaps
+
+
+def decode(cfg, weights, k_cache, v_cache, prompt, start_pos: int, n_new: int,
+           force_tokens=None, want_logits: bool = True, n_threads: int = 0) -> DecodeResult:
+    """Run the oracle. ``weights`` is a ``synthetic.ModelWeights``; ``k_cache`` and
+    ``v_cache`` are [L][n_kv][max_pos][d] uint16 arrays updated in place."""
+    prompt = _c(prompt, np.int32)
+    n_prompt = prompt.size
+    steps = n_prompt - 1 + n_new
+    layers = (OrcLayer * cfg.n_layers)()
+    keep = []
+    for l, w in enumerate(weights.layers):
+        for slot in _SLOTS:
+            a = w.get(slot)
+            if a is not None:
+                a = _c(a, np.uint16)
+                keep.append(a)
+                setattr(layers[l], slot, a.ctypes.data)
+            else:
+                setattr(layers[l], slot, None)
+    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous
+    assert v_cache.dtype == np.uint16 and v_cache.flags.c_contiguous
+    embed = _c(weights.embed, np.uint16)
+    fnorm = _c(weights.final_norm, np.uint16)
+    out_tokens = np.zeros(max(n_new, 1), np.int32)
+    logits = np.empty((steps, cfg.vocab), np.float32) if want_logits else None
+    gaps = np.empty(max(steps, 1), np.float32)
+    force = None if force_tokens is None else _c(force_tokens, np.int32)
+    m = model_struct(cfg)
+    rc = lib().orc_decode(ctypes.byref(m), layers, embed.ctypes.data, fnorm.ctypes.data,
+                          k_cache.ctypes.data, v_cache.ctypes.data, prompt.ctypes.data, n_prompt,
+                          start_pos, n_new, _ptr(force), out_tokens.ctypes.data, _ptr(logits),
+                          gaps.ctypes.data, n_threads)
+    if rc != 0:
+        raise ValueError(f"orc_decode rejected its arguments (rc={rc})")
+    return DecodeResult(out_tokens[:n_new], logits, gaps[:steps])

@@ -1,0 +1,355 @@
+"""Pins of the CPU oracle to facts other than itself.
+
+The pages print no worked numeric example of the forward pass, so the oracle is
+pinned by the BF16 rounding definition (hand-derived bit patterns), closed forms,
+invariants, special cases that reduce to a known value, and brute force in FP64
+on tiny inputs. Each test names the plausible mistake it would catch.
+"""
+import os
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synthetic as S
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- BF16 rounding
+def _golden_bf16():
+    rows = []
+    with open(os.path.join(GOLDEN, "bf16_rne.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            a, b = line.split()[:2]
+            rows.append((int(a, 16), b))
+    return rows
+
+
+def test_bf16_rne_golden_bit_patterns():
+    rows = _golden_bf16()
+    f = np.array([r[0] for r in rows], np.uint32).view(np.float32)
+    got = O.bf16_from_f32(f)
+    for (src, want), g in zip(rows, got):
+        if want == "nan":
+            assert (g & 0x7F80) == 0x7F80 and (g & 0x007F) != 0, hex(src)
+        else:
+            assert int(g) == int(want, 16), (hex(src), hex(int(g)), want)
+
+
+def test_bf16_widening_is_exact():
+    b = np.arange(0, 1 << 16, dtype=np.uint16)
+    fin = (b & 0x7F80) != 0x7F80
+    f = O.f32_from_bf16(b[fin])
+    assert np.array_equal(O.bf16_from_f32(f), b[fin])      # round trip is the identity
+
+
+# ----------------------------------------------------------------- GEMV
+def test_gemv_small_integers_is_exact():
+    """Integer weights/activations in [-4, 4]: every partial sum is an integer below
+    2^24, so FP32 is exact and the result must equal the integer dot product.
+    Catches a transposed W, a dropped column, a wrong row stride."""
+    rng = np.random.default_rng(7)
+    for rows, cols in [(5, 7), (33, 2048), (17, 8192)]:
+        Wi = rng.integers(-4, 5, size=(rows, cols))
+        xi = rng.integers(-4, 5, size=cols)
+        W = O.bf16_from_f32(Wi.astype(np.float32)).reshape(rows, cols)
+        y = O.gemv(W, xi.astype(np.float32))
+        assert np.array_equal(y.astype(np.int64), Wi @ xi)
+
+
+# ----------------------------------------------------------------- RMSNorm
+def test_rmsnorm_constant_vector_closed_form():
+    """x = c * 1 gives g / sqrt(1 + eps / c^2)."""
+    n, eps = 2048, 1e-5
+    g = O.bf16_from_f32(np.linspace(-2, 2, n).astype(np.float32))
+    for c in (0.5, 3.0, -0.125):
+        out = O.rmsnorm(np.full(n, c, np.float32), g, eps)
+        want = O.f32_from_bf16(g).astype(np.float64) * np.sign(c) / np.sqrt(1 + eps / c ** 2)
+        np.testing.assert_allclose(out, want, rtol=2e-6, atol=1e-7)
+
+
+def test_rmsnorm_power_of_two_scale_invariance_bitwise():
+    """With eps = 0, scaling x by 2^k leaves every output bit unchanged."""
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(1024).astype(np.float32)
+    g = O.bf16_from_f32(rng.standard_normal(1024).astype(np.float32))
+    base = O.rmsnorm(x, g, 0.0)
+    for k in (-3, 1, 5):
+        assert np.array_equal(O.rmsnorm(x * np.float32(2.0 ** k), g, 0.0), base)
+
+
+def test_rmsnorm_unit_gain_has_unit_rms():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal(4096).astype(np.float32) * 3
+    out = O.rmsnorm(x, S.ones_bf16(4096), 0.0).astype(np.float64)
+    assert abs(np.sqrt(np.mean(out ** 2)) - 1.0) < 1e-5
+
+
+# ----------------------------------------------------------------- RoPE
+def test_rope_frequencies_geometric_without_scaling():
+    cfg = S.CONFIGS["qwen3_0_6b"]
+    w = O.rope_inv_freq(cfg)
+    assert w[0] == 1.0
+    ratio = w[1:] / w[:-1]
+    np.testing.assert_allclose(ratio, cfg.rope_theta ** (-2.0 / cfg.head_dim), rtol=1e-12)
+
+
+def test_rope_llama3_scaling_regions():
+    """High-frequency pairs unchanged, low-frequency pairs divided by the factor,
+    the band between strictly between the two and continuous at both edges."""
+    cfg = S.CONFIGS["llama1b"]
+    base = O.rope_inv_freq(replace(cfg, rope_scaling=False))
+    sc = O.rope_inv_freq(cfg)
+    lam = 2 * np.pi / base
+    hi = lam < cfg.rs_orig_max / cfg.rs_high
+    lo = lam > cfg.rs_orig_max / cfg.rs_low
+    mid = ~hi & ~lo
+    assert hi.any() and lo.any() and mid.any()
+    assert np.array_equal(sc[hi], base[hi])
+    np.testing.assert_allclose(sc[lo], base[lo] / cfg.rs_factor, rtol=1e-15)
+    assert np.all(sc[mid] < base[mid]) and np.all(sc[mid] > base[mid] / cfg.rs_factor)
+    # the smoothing weight goes to 0 at lambda = orig/low and to 1 at orig/high
+    sw = (sc[mid] - base[mid] / cfg.rs_factor) / (base[mid] - base[mid] / cfg.rs_factor)
+    want = (cfg.rs_orig_max / lam[mid] - cfg.rs_low) / (cfg.rs_high - cfg.rs_low)
+    np.testing.assert_allclose(sw, want, rtol=1e-9)
+    assert np.all(np.diff(sc) < 0)                       # still strictly decreasing
+
+
+def test_rope_position_zero_is_identity_bitwise():
+    cfg = S.CONFIGS["llama1b"]
+    c, s = O.rope_cos_sin(cfg, 0)
+    v = np.random.default_rng(3).standard_normal(cfg.head_dim).astype(np.float32)
+    assert np.array_equal(O.rope_apply(v, c, s), v)
+
+
+def test_rope_rotate_half_pairing():
+    """A unit vector on element j lands on (cos, sin) at elements (j, j + d/2):
+    an interleaved (j, j+1) pairing or a flipped sign fails this."""
+    cfg = S.CONFIGS["tiny"]
+    d = cfg.head_dim
+    c, s = O.rope_cos_sin(cfg, 7)
+    for j in (0, 5, d // 2 - 1):
+        e = np.zeros(d, np.float32)
+        e[j] = 1.0
+        r = O.rope_apply(e, c, s)
+        assert r[j] == c[j] and r[j + d // 2] == s[j]
+        assert np.count_nonzero(r) <= 2
+
+
+def test_rope_preserves_pair_norms_and_relative_positions():
+    cfg = S.CONFIGS["llama1b"]
+    d = cfg.head_dim
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal(d).astype(np.float32)
+    k = rng.standard_normal(d).astype(np.float32)
+
+    def rot(v, p):
+        c, s = O.rope_cos_sin(cfg, p)
+        return O.rope_apply(v, c, s).astype(np.float64)
+
+    r = rot(q, 1234)
+    n0 = q[: d // 2].astype(np.float64) ** 2 + q[d // 2:].astype(np.float64) ** 2
+    n1 = r[: d // 2] ** 2 + r[d // 2:] ** 2
+    np.testing.assert_allclose(n1, n0, rtol=1e-5)
+    a = rot(q, 100) @ rot(k, 40)
+    b = rot(q, 1100) @ rot(k, 1040)
+    assert abs(a - b) < 1e-4 * (1 + abs(a))
+
+
+# ----------------------------------------------------------------- attention
+def _fp64_attention(q, K, V, scale):
+    s = (K.astype(np.float64) @ q.astype(np.float64)) * scale
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    return p @ V.astype(np.float64)
+
+
+@pytest.mark.parametrize("n,d", [(1, 4), (3, 8), (5, 8), (5, 2)])
+def test_attention_matches_fp64_brute_force(n, d):
+    rng = np.random.default_rng(10 * n + d)
+    q = O.f32_from_bf16(O.bf16_from_f32(rng.standard_normal(d).astype(np.float32)))
+    K = O.bf16_from_f32(rng.standard_normal((n, d)).astype(np.float32)).reshape(n, d)
+    V = O.bf16_from_f32(rng.standard_normal((n, d)).astype(np.float32)).reshape(n, d)
+    got = O.attention(q, K, V, 0.5)
+    want = _fp64_attention(q, O.f32_from_bf16(K).reshape(n, d), O.f32_from_bf16(V).reshape(n, d), 0.5)
+    np.testing.assert_allclose(got, want, rtol=1e-5, atol=1e-6)
+
+
+def test_attention_single_position_returns_value_bitwise():
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal(64).astype(np.float32)
+    K = O.bf16_from_f32(rng.standard_normal(64).astype(np.float32)).reshape(1, 64)
+    V = O.bf16_from_f32(rng.standard_normal(64).astype(np.float32)).reshape(1, 64)
+    assert np.array_equal(O.attention(q, K, V, 0.125), O.f32_from_bf16(V).reshape(64))
+
+
+def test_attention_equal_keys_average_values():
+    rng = np.random.default_rng(12)
+    n, d = 9, 64
+    q = rng.standard_normal(d).astype(np.float32)
+    K = np.tile(O.bf16_from_f32(rng.standard_normal(d).astype(np.float32)), (n, 1))
+    V = O.bf16_from_f32(rng.standard_normal((n, d)).astype(np.float32)).reshape(n, d)
+    got = O.attention(q, K, V, 0.125)
+    np.testing.assert_allclose(got, O.f32_from_bf16(V).reshape(n, d).astype(np.float64).mean(0),
+                               rtol=1e-5, atol=1e-6)
+
+
+def test_split_partials_and_combine_equal_unsplit():
+    rng = np.random.default_rng(13)
+    n, d = 200, 64
+    q = O.f32_from_bf16(O.bf16_from_f32(rng.standard_normal(d).astype(np.float32)))
+    K = O.bf16_from_f32(rng.standard_normal((n, d)).astype(np.float32)).reshape(n, d)
+    V = O.bf16_from_f32(rng.standard_normal((n, d)).astype(np.float32)).reshape(n, d)
+    full = O.attention(q, K, V, 0.125)
+    for bounds in ([0, 200], [0, 64, 128, 192, 200], [0, 0, 50, 50, 200], [0, 199, 200]):
+        np.testing.assert_allclose(O.attention_split(q, K, V, 0.125, bounds), full,
+                                   rtol=2e-5, atol=2e-6)
+
+
+# ----------------------------------------------------------------- whole decoder
+def _tiny_inputs(cfg):
+    return S.model_weights(cfg), *S.kv_prefill(cfg), S.prompt(cfg)
+
+
+def test_decoder_causal_invariance_bitwise(tiny_cfg):
+    """Appending steps leaves the logits of earlier steps bit-for-bit unchanged."""
+    w, k, v, p = _tiny_inputs(tiny_cfg)
+    a = O.decode(tiny_cfg, w, k.copy(), v.copy(), p, 0, 4)
+    b = O.decode(tiny_cfg, w, k.copy(), v.copy(), p, 0, 9)
+    assert np.array_equal(b.logits[: a.logits.shape[0]], a.logits)
+    assert np.array_equal(b.tokens[:4], a.tokens)
+
+
+def test_decoder_resume_from_own_cache_equals_continuous_bitwise(tiny_cfg):
+    w, k, v, p = _tiny_inputs(tiny_cfg)
+    full = O.decode(tiny_cfg, w, k.copy(), v.copy(), p, 0, 10)
+    k2, v2 = k.copy(), v.copy()
+    first = O.decode(tiny_cfg, w, k2, v2, p[:20], 0, 1)
+    second = O.decode(tiny_cfg, w, k2, v2, p[19:], 19, 10)
+    assert np.array_equal(np.concatenate([first.logits, second.logits[1:]]), full.logits)
+    assert np.array_equal(second.tokens, full.tokens)
+
+
+def test_decoder_thread_count_does_not_change_bits(tiny_cfg):
+    w, k, v, p = _tiny_inputs(tiny_cfg)
+    a = O.decode(tiny_cfg, w, k.copy(), v.copy(), p, 0, 6, n_threads=1)
+    b = O.decode(tiny_cfg, w, k.copy(), v.copy(), p, 0, 6, n_threads=4)
+    assert np.array_equal(a.logits, b.logits)
+
+
+def test_decoder_greedy_is_first_argmax_and_forcing_own_tokens_is_neutral(tiny_cfg):
+    w, k, v, p = _tiny_inputs(tiny_cfg)
+    r = O.decode(tiny_cfg, w, k.copy(), v.copy(), p, 0, 8)
+    n_prompt = p.size
+    assert np.array_equal(r.tokens, r.logits[n_prompt - 1:].argmax(1))
+    srt = np.sort(r.logits, 1)
+    np.testing.assert_array_equal(r.gaps, srt[:, -1] - srt[:, -2])
+    f = O.decode(tiny_cfg, w, k.copy(), v.copy(), p, 0, 8, force_tokens=r.tokens[:-1])
+    assert np.array_equal(f.logits, r.logits)
+
+
+def _zero_like(a):
+    return np.zeros_like(a)
+
+
+def _perm_matrix(n_out, n_in, perm, value=1.0):
+    W = np.zeros((n_out, n_in), np.uint16)
+    W[np.arange(n_out), perm] = O.bf16_from_f32(np.float32(value))[0]
+    return W
+
+
+def test_decoder_attention_special_case_closed_form(tiny_cfg):
+    """Keys all zero -> uniform softmax over positions 0..P; cached values are a
+    constant vector per KV head, the new value is zero; Wo is a permutation;
+    the FFN is zero. Then every layer adds R(P/(P+1) c_{i//G}) permuted, and the
+    logits follow in closed form. A wrong GQA head mapping, an exclusive causal
+    range, a transposed Wo or a wrong tied head fails it."""
+    cfg = tiny_cfg
+    rng = np.random.default_rng(21)
+    w = S.model_weights(cfg)
+    H, d, nkv, G = cfg.hidden, cfg.head_dim, cfg.n_kv_heads, cfg.n_q_heads // cfg.n_kv_heads
+    perm = rng.permutation(H)
+    for lw in w.layers:
+        lw["wk"] = _zero_like(lw["wk"])
+        lw["wv"] = _zero_like(lw["wv"])
+        lw["wo"] = _perm_matrix(H, cfg.q_dim, perm)
+        lw["w_gate"] = _zero_like(lw["w_gate"])
+        lw["w_up"] = _zero_like(lw["w_up"])
+        lw["w_down"] = _zero_like(lw["w_down"])
+    P = 5
+    k = np.zeros((cfg.n_layers, nkv, cfg.max_pos, d), np.uint16)
+    v = np.zeros_like(k)
+    consts = O.bf16_from_f32(rng.standard_normal((nkv, d)).astype(np.float32)).reshape(nkv, d)
+    v[:, :, :P, :] = consts[None, :, None, :]
+    tok = np.array([17], np.int32)
+    r = O.decode(cfg, w, k, v, tok, P, 1)
+    # closed form in float64, rounding to bf16 where the definition does
+    c = O.f32_from_bf16(consts).reshape(nkv, d).astype(np.float64)
+    o = np.concatenate([c[i // G] * P / (P + 1) for i in range(cfg.n_q_heads)])
+    o = O.f32_from_bf16(O.bf16_from_f32(o.astype(np.float32))).astype(np.float64)
+    x = O.f32_from_bf16(w.embed[tok[0]]).astype(np.float64)
+    for _ in range(cfg.n_layers):
+        x = O.f32_from_bf16(O.bf16_from_f32((x + o[perm]).astype(np.float32))).astype(np.float64)
+    hf = x / np.sqrt(np.mean(x ** 2) + cfg.rms_eps)
+    hf = O.f32_from_bf16(O.bf16_from_f32(hf.astype(np.float32))).astype(np.float64)
+    logits = O.f32_from_bf16(w.embed).reshape(cfg.vocab, H).astype(np.float64) @ hf
+    np.testing.assert_allclose(r.logits[0], logits, atol=2e-4)
+    assert r.tokens[0] == int(np.argmax(logits))
+    # the new K/V position was written (as zeros here) and nothing else moved
+    assert np.array_equal(v[:, :, :P], np.broadcast_to(consts[None, :, None, :], v[:, :, :P].shape))
+
+
+def test_decoder_ffn_special_case_closed_form(tiny_cfg):
+    """Attention output projection zero; gate = rows 0..H-1 identity, up = 2x
+    identity, down = a permutation: each layer adds R(silu(h) * 2h) permuted.
+    Swapped gate/up, a wrong SiLU or a transposed down projection fails it."""
+    cfg = tiny_cfg
+    rng = np.random.default_rng(22)
+    w = S.model_weights(cfg)
+    H, F = cfg.hidden, cfg.ffn
+    perm = rng.permutation(H)
+    eye_g = np.zeros((F, H), np.uint16)
+    eye_g[np.arange(H), np.arange(H)] = 0x3F80          # 1.0
+    eye_u = np.zeros((F, H), np.uint16)
+    eye_u[np.arange(H), np.arange(H)] = 0x4000          # 2.0
+    down = np.zeros((H, F), np.uint16)
+    down[np.arange(H), perm] = 0x3F80
+    for lw in w.layers:
+        lw["wo"] = _zero_like(lw["wo"])
+        lw["w_gate"], lw["w_up"], lw["w_down"] = eye_g, eye_u, down
+    k, v = S.kv_prefill(cfg, n_pos=3)
+    tok = np.array([5], np.int32)
+    r = O.decode(cfg, w, k, v, tok, 3, 1)
+
+    def rb(a):
+        return O.f32_from_bf16(O.bf16_from_f32(np.asarray(a, np.float32))).astype(np.float64)
+
+    x = rb(O.f32_from_bf16(w.embed[tok[0]]))
+    for _ in range(cfg.n_layers):
+        h = rb(x / np.sqrt(np.mean(x ** 2) + cfg.rms_eps))
+        a = rb(h / (1 + np.exp(-h)) * 2 * h)
+        x = rb(x + a[perm])
+    hf = rb(x / np.sqrt(np.mean(x ** 2) + cfg.rms_eps))
+    logits = O.f32_from_bf16(w.embed).reshape(cfg.vocab, H).astype(np.float64) @ hf
+    np.testing.assert_allclose(r.logits[0], logits, atol=2e-3)
+    assert r.tokens[0] == int(np.argmax(logits))
+
+
+def test_decoder_writes_kv_at_position_only(tiny_cfg):
+    w, k, v, p = _tiny_inputs(tiny_cfg)
+    k0, v0 = k.copy(), v.copy()
+    O.decode(tiny_cfg, w, k, v, p[:3], 0, 1)
+    changed = np.any(k != k0, axis=(0, 1, 3))
+    assert set(np.nonzero(changed)[0]) <= {0, 1, 2}
+    assert changed[:3].all()
+
+
+def test_decoder_rejects_capacity_overflow(tiny_cfg):
+    w, k, v, p = _tiny_inputs(tiny_cfg)
+    with pytest.raises(ValueError):
+        O.decode(tiny_cfg, w, k, v, p, tiny_cfg.max_pos - 2, 8)

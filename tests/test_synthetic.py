@@ -1,0 +1,57 @@
+"""The shared seeded input generator: definition, determinism, distribution."""
+import numpy as np
+
+import synthetic as S
+
+
+def test_splitmix64_reference_outputs():
+    """First outputs of SplitMix64 from state 1234567, the test vector that ships
+    with the reference C implementation of the generator (Vigna, splitmix64.c)."""
+    want = [6457827717110365317, 3203168211198807973, 9817491932198370423,
+            4593380528125082431, 16408922859458223821]
+    assert [int(v) for v in S.splitmix64_stream(1234567, 5)] == want
+
+
+def test_counter_based_elements_are_position_independent():
+    whole = S.normal_f32(0, 5, 1000, 1.0)
+    part = S.normal_f32(0, 5, 300, 1.0, i0=401)
+    assert np.array_equal(whole[401:701], part)
+    assert not np.array_equal(S.normal_f32(0, 6, 1000), whole)   # other tensor id
+    assert not np.array_equal(S.normal_f32(1, 5, 1000), whole)   # other seed
+
+
+def test_normal_statistics():
+    x = S.normal_f32(3, 9, 1 << 20, 0.02).astype(np.float64)
+    assert abs(x.mean()) < 1e-4
+    assert abs(x.std() - 0.02) < 1e-4
+    assert abs(np.mean(np.abs(x) < 0.02) - 0.6827) < 3e-3       # one-sigma mass
+
+
+def test_bf16_generation_rounds_the_float_values():
+    f = S.normal_f32(0, 11, 4096, 0.02)
+    b = S.normal_bf16(0, 11, (4096,), 0.02)
+    back = S.bf16_to_f32(b)
+    assert np.all(np.abs(back - f) <= np.abs(f) * 2.0 ** -8)
+
+
+def test_tokens_in_range_and_spread():
+    t = S.tokens(2, 0, 20000, 1024)
+    assert t.min() >= 0 and t.max() < 1024
+    assert len(np.unique(t)) > 1000
+
+
+def test_kv_prefill_layout_and_tail_zero():
+    cfg = S.CONFIGS["tiny"].with_workload(start_pos=10, max_pos=16)
+    k, v = S.kv_prefill(cfg, n_pos=10)
+    assert k.shape == (2, 2, 16, 64)
+    assert not k[:, :, 10:].any() and not v[:, :, 10:].any()
+    # element (h, p, j) of layer l is element (h * n_pos + p) * d + j of tensor 2l
+    flat = S.normal_bf16(S.SEED_KV, 2 * 1, (2 * 10 * 64,), 1.0).reshape(2, 10, 64)
+    assert np.array_equal(k[1, :, :10], flat)
+
+
+def test_config_byte_counts():
+    c = S.CONFIGS["llama1b"]
+    assert c.weight_bytes() == 2 * (16 * (3072 * 2048 + 2048 * 2048 + 3 * 8192 * 2048 + 2 * 2048)
+                                    + 128256 * 2048 + 2048)
+    assert abs(c.algorithmic_bytes_per_token() - 2.5063e9) < 1e6
