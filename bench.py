@@ -1,0 +1,383 @@
+"""Benchmark: batch-1 greedy decode tok/s on one GB300 and the fraction of the
+HBM roofline it reaches.
+
+Workload (default): the Llama-3.2-1B-shaped decoder (16 layers, hidden 2048,
+32/8 heads, head_dim 64, FFN 8192, vocab 128256, tied embeddings, llama3 RoPE)
+with seed-generated BF16 weights N(0, 0.02), a KV cache pre-filled with 1,023
+positions of N(0, 1), one seeded input token, 64 greedy tokens. One "step" is
+one decode call of those 64 tokens (one cooperative launch of the persistent
+kernel); each call rewrites positions 1023..1086, so repeats are identical and
+are checked bit for bit.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                  [--scheduler counters|waves] [--impl ours|reference]
+
+With N > 1 (launched by torchrun) every rank runs an independent replica: a
+batch-1 decode has no exchange step to shard (replicas only). `--impl
+reference` times the CPU oracle on the host cores on a bounded sample of the
+same workload. Prints one JSON line on stdout.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 decode tok/s on 1 GB300; % of HBM roofline (weight+KV bytes/token)"
+UNIT = "tok/s"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "megakernel_traffic.json")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload_config(cfg):
+    return {"workload": f"{cfg.name}: {cfg.n_layers} layers, hidden {cfg.hidden}, "
+                        f"{cfg.n_q_heads}/{cfg.n_kv_heads} heads x {cfg.head_dim}, ffn {cfg.ffn}, "
+                        f"vocab {cfg.vocab}, {cfg.start_pos} cached positions, "
+                        f"{cfg.n_new} greedy tokens per step",
+            "tokens_per_step": cfg.n_new, "cached_positions": cfg.start_pos,
+            "bytes_per_token": int(round(cfg.algorithmic_bytes_per_token())),
+            "l2": "inputs larger than L2 (every token streams all weights, >1 GB)"}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tile_scheduled_persistent_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config_name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(config_name)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- CPU oracle arm
+def oracle_sample(cfg, w, k, v, prompt, n_tokens):
+    """Time the oracle on n_tokens decode steps of the workload (all host cores)."""
+    import oracle
+    kk, vv = k.copy(), v.copy()
+    t0 = time.perf_counter()
+    oracle.decode(cfg, w, kk, vv, prompt, cfg.start_pos, n_tokens, want_logits=False)
+    return time.perf_counter() - t0
+
+
+def run_reference(args):
+    import synthetic as S
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = S.CONFIGS[args.config]
+    log(f"[reference] generating {cfg.name} inputs ...")
+    w = S.model_weights(cfg)
+    k, v = S.kv_prefill(cfg)
+    prompt = S.prompt(cfg)
+    n_tok = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_sample(cfg, w, k, v, prompt, n_tok)
+    times = [oracle_sample(cfg, w, k, v, prompt, n_tok) for _ in range(args.steps)]
+    tot = sum(times)
+    value = n_tok * args.steps / tot
+    cores = os.cpu_count()
+    sample = (f"{n_tok} decode tokens of the workload from position {cfg.start_pos} per step "
+              f"(of {cfg.n_new}), OpenMP over output rows and heads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(cfg),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import synthetic as S
+    import tile_scheduled_persistent_gb300 as tsp
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    tsp.build()
+    cfg = S.CONFIGS[args.config]
+    log(f"[rank {rank}] generating {cfg.name} inputs ...")
+    t0 = time.time()
+    w = S.model_weights(cfg)
+    k_np, v_np = S.kv_prefill(cfg)
+    prompt_np = S.prompt(cfg)
+    log(f"[rank {rank}] generated in {time.time() - t0:.1f}s; uploading")
+    dw = tsp.upload_weights(w)
+    kc = tsp.to_device_bf16(k_np)
+    vc = tsp.to_device_bf16(v_np)
+    dprompt = torch.from_numpy(prompt_np).cuda()
+    stream = torch.cuda.current_stream()
+
+    # HBM copy peak measured in this run (read + write bytes, best of 10)
+    n_copy = 1 << 30
+    a = torch.empty(n_copy, dtype=torch.int16, device="cuda")
+    b = torch.empty_like(a)
+    a.fill_(1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 1e30
+    for _ in range(12):
+        e0.record()
+        tsp.copy_bw(b, a)
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1) / 1e3)
+    copy_gbs = 2 * a.numel() * 2 / best / 1e9
+    del a, b
+    torch.cuda.empty_cache()
+    try:
+        barrier_ns = tsp.barrier_cost(0, 2000)
+    except tsp.TilesError:
+        barrier_ns = None
+
+    bytes_per_token = cfg.algorithmic_bytes_per_token()
+    results = {}
+    scheds = ["counters", "waves"] if args.scheduler == "both" else [args.scheduler]
+    for sname in scheds:
+        plan = tsp.Plan(tsp.ModelDesc.from_config(cfg), dw,
+                        tsp.make_opts(scheduler=tsp.SCHED_COUNTERS if sname == "counters" else tsp.SCHED_WAVES))
+        info = plan.info()
+        toks = torch.zeros(cfg.n_new, dtype=torch.int32, device="cuda")
+        ref_toks = None
+        for _ in range(args.warmup):
+            plan.decode(kc, vc, dprompt, cfg.start_pos, cfg.n_new, toks)
+        plan.check()
+        ref_toks = toks.clone()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        all_toks = torch.zeros((args.steps, cfg.n_new), dtype=torch.int32, device="cuda")
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(dev) as clk:
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            for i in range(args.steps):
+                starts[i].record(stream)
+                plan.decode(kc, vc, dprompt, cfg.start_pos, cfg.n_new, all_toks[i])
+                ends[i].record(stream)
+            g1.record(stream)
+            torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        plan.check()
+        total_s = g0.elapsed_time(g1) / 1e3
+        per_launch = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
+        bitwise = bool((all_toks == ref_toks[None, :]).all().item())
+        results[sname] = dict(total_s=total_s, per_launch=per_launch, clocks=clk.summary(),
+                              bitwise=bitwise, info=info, plan=plan,
+                              tokens=ref_toks.cpu().numpy())
+        log(f"[rank {rank}] {sname}: {args.steps * cfg.n_new / total_s:.1f} tok/s, "
+            f"launch {statistics.mean(per_launch) * 1e6:.0f} us, bitwise {bitwise}")
+    # keep the faster scheduler on evidence
+    chosen = min(results, key=lambda s: results[s]["total_s"])
+    if args.scheduler != "both":
+        chosen = args.scheduler
+    r = results[chosen]
+    total_s = r["total_s"]
+    if ws > 1:
+        t = torch.tensor([total_s], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+    tokens_all = args.steps * cfg.n_new * ws
+    value = tokens_all / total_s
+    launch_s = statistics.mean(r["per_launch"])
+    achieved_gbs = bytes_per_token * cfg.n_new / launch_s / 1e9
+    peaks = measured_peaks()
+    if peaks and peaks.get("hbm_gbs"):
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    else:
+        peak, peak_src = 6800.0, "fallback 6.8 TB/s"
+    traffic = recorded_traffic(cfg.name)
+
+    # end to end through the host-buffer entry point (copies inside the timed region)
+    plan = r["plan"]
+    pin_prompt = torch.from_numpy(prompt_np.copy()).pin_memory().numpy()
+    host_toks = torch.zeros(cfg.n_new, dtype=torch.int32).pin_memory().numpy()
+    plan.decode_host(kc, vc, pin_prompt, cfg.start_pos, cfg.n_new, host_toks)
+    if ws > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        plan.decode_host(kc, vc, pin_prompt, cfg.start_pos, cfg.n_new, host_toks)
+    e2e_s = time.perf_counter() - t0
+    if ws > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_same = bool(np.array_equal(host_toks, r["tokens"]))
+    e2e_value = tokens_all / e2e_s
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n_tok = args.ref_tokens
+        secs = oracle_sample(cfg, w, k_np, v_np, prompt_np, n_tok)
+        cpu = {"value": n_tok / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"first {n_tok} of the {cfg.n_new} decode tokens from position "
+                         f"{cfg.start_pos}, OpenMP over output rows and heads on all host cores"}
+
+    if rank == 0:
+        conf = workload_config(cfg)
+        conf.update({"scheduler": chosen, "ctas": r["info"]["n_ctas"],
+                     "ring": f"{r['info']['ring_slots']} x {r['info']['slot_bytes']} B",
+                     "kv_splits": r["info"]["kv_splits"], "parallelism": f"replicas x{ws}"})
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1000 * total_s / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": conf,
+                "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak,
+                             "unit": "GB/s", "frac": achieved_gbs / peak,
+                             "traffic": traffic, "peak_source": peak_src,
+                             "kernel": "tiles_megakernel",
+                             "copy_kernel_gbs_this_run": copy_gbs,
+                             "frac_of_copy_this_run": achieved_gbs / copy_gbs},
+                "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 4 * prompt_np.size,
+                        "d2h_bytes_per_step": 4 * cfg.n_new, "same_tokens": e2e_same},
+                "gpu_launches": args.steps,
+                "clocks": r["clocks"],
+                "bitwise_repeat": r["bitwise"],
+                "us_per_token": 1e6 * launch_s / cfg.n_new,
+                "grid_barrier_ns": barrier_ns,
+                "schedulers": {s: {"tok_s": args.steps * cfg.n_new / results[s]["total_s"],
+                                   "bitwise_repeat": results[s]["bitwise"]} for s in results}}
+        print(json.dumps(line), flush=True)
+    for s in results:
+        results[s]["plan"].close()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="llama1b")
+    ap.add_argument("--scheduler", default="both", choices=["counters", "waves", "both"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=2,
+                    help="oracle decode tokens per timed step (CPU arms)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        log("warm-up raised to 3 steps")
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

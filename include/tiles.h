@@ -1,0 +1,239 @@
+/*
+ * tiles.h -- C ABI of the tile-scheduled persistent decoder for GB300 (sm_103a).
+ *
+ * The operation: batch-size-1 greedy decoding of a Llama/Qwen-style dense BF16
+ * decoder in which every operator is cut into tiles (a range of output rows
+ * plus the small fused work that produces them), an offline planner assigns
+ * every tile to one persistent worker CTA per SM, balances the bytes each
+ * worker streams and orders the tiles, and one persistent kernel executes the
+ * whole schedule for a run of up to 64 tokens, with greedy selection inside
+ * the kernel.  Sources: "Tiles: Scheduling LLM Decoding as a Graph of Tiles"
+ * (intro; "What the code contains": the planner validates the schedule, the
+ * runtime re-validates it, checks it was made for this binary and GPU, and runs
+ * up to 64 tokens per cooperative launch with greedy selection in the kernel;
+ * "Scope": prefill one token per step).
+ *
+ * Conventions for every function below:
+ *   - All pointers are plain addresses. "device" means CUDA device memory of
+ *     the GPU the plan was made on; "host" means ordinary host memory.
+ *   - Matrices are row-major [out][in] bfloat16 (uint16 bit patterns).
+ *   - The caller owns every buffer it passes in (weights, caches, prompts,
+ *     outputs); they must stay valid while a plan or call uses them. A plan
+ *     owns only what it allocates itself (its tables and scratch).
+ *   - Functions return TILES_OK or a negative tiles_status_t and never abort
+ *     the process. A NULL required pointer gives TILES_ERR_INVALID_ARG.
+ *   - A plan is not thread-safe: one decode in flight per plan.
+ */
+#ifndef TILES_H
+#define TILES_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TILES_OK = 0,
+    TILES_ERR_INVALID_ARG = -1,     /* bad pointer, size or option                    */
+    TILES_ERR_UNSUPPORTED = -2,     /* shape outside what the kernel handles          */
+    TILES_ERR_PLAN_INVALID = -3,    /* schedule failed validation                     */
+    TILES_ERR_DEVICE_MISMATCH = -4, /* plan used on another GPU / SM count / binary   */
+    TILES_ERR_CAPACITY = -5,        /* start_pos + steps exceeds max_pos              */
+    TILES_ERR_CUDA = -6,            /* a CUDA runtime call failed                     */
+    TILES_ERR_TIMEOUT = -7,         /* a bounded in-kernel wait expired               */
+    TILES_ERR_DEVICE_BOUNDS = -8    /* the kernel rejected an out-of-range index      */
+} tiles_status_t;
+
+/* Model shape.  Llama-style when qk_norm == 0, Qwen3-style (per-head RMSNorm on
+ * q and k before RoPE) when qk_norm == 1.  Embeddings must be tied (the LM head
+ * is the embedding matrix).  RoPE pairs element j with j + head_dim/2; inverse
+ * frequencies theta^(-2j/d) with optional llama3 scaling (rope_scaling == 1,
+ * factor / low / high / original context), angles and tables in FP64 rounded
+ * to FP32. */
+typedef struct {
+    int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, max_pos;
+    int32_t qk_norm;          /* 0 or 1                                   */
+    int32_t rope_scaling;     /* 0 none, 1 llama3                          */
+    int32_t tied_embeddings;  /* must be 1                                */
+    int32_t rs_orig_max;      /* llama3: original context length          */
+    double rope_theta;
+    double rs_factor, rs_low, rs_high;
+    float rms_eps;            /* RMSNorm epsilon, also for the q/k norms  */
+} tiles_model_desc;
+
+/* Device pointers to one layer's weights. q_norm / k_norm are [head_dim] and
+ * may be NULL when qk_norm == 0. */
+typedef struct {
+    const void *attn_norm;  /* [hidden]                       */
+    const void *wq;         /* [n_q_heads*head_dim][hidden]   */
+    const void *wk;         /* [n_kv_heads*head_dim][hidden]  */
+    const void *wv;         /* [n_kv_heads*head_dim][hidden]  */
+    const void *q_norm;     /* [head_dim] or NULL             */
+    const void *k_norm;     /* [head_dim] or NULL             */
+    const void *wo;         /* [hidden][n_q_heads*head_dim]   */
+    const void *ffn_norm;   /* [hidden]                       */
+    const void *w_gate;     /* [ffn][hidden]                  */
+    const void *w_up;       /* [ffn][hidden]                  */
+    const void *w_down;     /* [hidden][ffn]                  */
+} tiles_layer_weights;
+
+/* Device weight pointers; every pointer 16-byte aligned. `layers` itself is a
+ * HOST array of n_layers entries (copied by tiles_plan_create). */
+typedef struct {
+    const void *embed;       /* [vocab][hidden], also the LM head */
+    const void *final_norm;  /* [hidden]                          */
+    const tiles_layer_weights *layers;
+} tiles_weights;
+
+enum { TILES_SCHED_WAVES = 0, TILES_SCHED_COUNTERS = 1 };
+
+/* Planner options; pass NULL to tiles_plan_create for the defaults (shown). */
+typedef struct {
+    int32_t scheduler;    /* TILES_SCHED_COUNTERS (default) or TILES_SCHED_WAVES        */
+    int32_t n_ctas;       /* 0 = one worker CTA per SM                                  */
+    int32_t slot_bytes;   /* 0 = auto: bytes per shared-memory ring slot (mult. of 1024) */
+    int32_t ring_slots;   /* 0 = as many as fit in shared memory                         */
+    int32_t kv_splits;    /* 0 = auto: split-KV ranges per KV head                       */
+    int32_t timeout_ms;   /* bound on every in-kernel wait; 0 = 2000 ms                  */
+    uint32_t flags;       /* reserved, must be 0                                         */
+} tiles_plan_opts;
+
+typedef struct tiles_plan_s *tiles_plan_t;
+
+/* Builds, validates and uploads a schedule for `desc` on the current CUDA
+ * device. Query the device (SM count, shared memory, cooperative launch,
+ * occupancy of the worker kernel at the chosen shared-memory size), build the
+ * tile graph, assign tiles to CTAs balancing streamed bytes, order them into
+ * waves or dependency-counter chains, validate, and allocate the plan's own
+ * device tables and scratch.  On success *out owns those allocations.
+ * Errors: INVALID_ARG, UNSUPPORTED (shape), PLAN_INVALID, CUDA. */
+tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weights *weights,
+                                 const tiles_plan_opts *opts, tiles_plan_t *out);
+
+/* Frees everything the plan allocated. NULL is allowed. The caller must make
+ * sure no decode using the plan is still running. */
+void tiles_plan_destroy(tiles_plan_t plan);
+
+/*
+ * Greedy decoding, asynchronous on `stream` (a cudaStream_t, NULL = legacy).
+ *
+ * Runs n_prompt - 1 + n_new steps; step s runs at position start_pos + s. Its
+ * input token is prompt[s] when s < n_prompt, else the token chosen at step
+ * s - 1. Steps s >= n_prompt - 1 write out_tokens[s - (n_prompt - 1)]. Every
+ * step writes K and V of its position into the caches and reads positions
+ * 0..start_pos + s. Steps are split into cooperative launches of <= 64.
+ *
+ *   k_cache, v_cache  device, [n_layers][n_kv_heads][max_pos][head_dim] bf16,
+ *                     positions < start_pos already filled by the caller
+ *   prompt            device, n_prompt >= 1 token ids in [0, vocab)
+ *   out_tokens        device, n_new int32
+ *   out_logits        device, [n_prompt - 1 + n_new][vocab] float32, or NULL
+ *
+ * The return value covers argument, capacity and launch errors; errors raised
+ * inside the kernel (timeout, bad token id) are read by tiles_status.
+ * Errors: INVALID_ARG, CAPACITY, DEVICE_MISMATCH, CUDA.
+ */
+tiles_status_t tiles_decode(tiles_plan_t plan, void *k_cache, void *v_cache,
+                            const int32_t *prompt, int32_t n_prompt, int32_t start_pos,
+                            int32_t n_new, void *stream, int32_t *out_tokens, float *out_logits);
+
+/*
+ * Same as tiles_decode, but prompt, out_tokens and out_logits are HOST
+ * buffers: the call copies the prompt in, decodes, copies the results out and
+ * synchronises `stream` before returning (so it also reports kernel errors).
+ * out_logits may be NULL. Uses the plan's own device staging buffers.
+ */
+tiles_status_t tiles_decode_host(tiles_plan_t plan, void *k_cache, void *v_cache,
+                                 const int32_t *prompt_host, int32_t n_prompt, int32_t start_pos,
+                                 int32_t n_new, void *stream, int32_t *out_tokens_host,
+                                 float *out_logits_host);
+
+/* Synchronises `stream` and reads the plan's device status word, then clears
+ * it. Returns TILES_OK, TILES_ERR_TIMEOUT, TILES_ERR_DEVICE_BOUNDS or CUDA. */
+tiles_status_t tiles_status(tiles_plan_t plan, void *stream);
+
+/* Static string naming a status code. Never NULL. */
+const char *tiles_status_string(tiles_status_t status);
+
+/* Facts about a built plan, for reports and tests. */
+typedef struct {
+    int32_t n_ctas, threads_per_cta, smem_bytes, slot_bytes, ring_slots, kv_splits;
+    int32_t scheduler, n_tasks, n_counters, phases_per_step;
+    int64_t weight_bytes_per_token;     /* every weight byte the kernel streams per step */
+    int64_t max_cta_bytes, min_cta_bytes; /* per-step streamed weight bytes, busiest/idlest CTA */
+} tiles_plan_info;
+
+tiles_status_t tiles_plan_get_info(tiles_plan_t plan, tiles_plan_info *info);
+
+/* ------------------------------------------------------------------------ */
+/* Schedule inspection without a GPU (planner and validator tests).          */
+
+enum {
+    TILES_OP_QKV = 1,      /* RMSNorm prologue, rows of [Wq; Wk; Wv] -> FP32 q,k,v        */
+    TILES_OP_ATTN = 2,     /* q/k norm + RoPE + KV write, split-KV partials (item = kv head * splits + split) */
+    TILES_OP_COMBINE = 3,  /* merge split partials of q heads [begin, end) -> bf16 o      */
+    TILES_OP_OPROJ = 4,    /* rows of Wo, residual add                                    */
+    TILES_OP_GATEUP = 5,   /* RMSNorm prologue, rows of Wg and Wu, SwiGLU epilogue        */
+    TILES_OP_DOWN = 6,     /* rows of Wd, residual add                                    */
+    TILES_OP_LMHEAD = 7,   /* final RMSNorm, rows of the tied embedding, argmax           */
+    TILES_OP_SYNC = 8      /* no work: barrier arrival only (wave scheduler)              */
+};
+
+#define TILES_NO_COUNTER 0xFFFFu
+
+/* One scheduled tile task. A CTA runs its task list once per step. Before a
+ * task, the CTA waits until counter `wait_ctr` reaches
+ * wait_mul * step + wait_add (step counted from the launch's first step);
+ * after it, the CTA adds 1 to `signal_ctr`. */
+typedef struct {
+    uint8_t op;
+    uint8_t phase_kind;      /* position of the op within its layer (0..5), 6 = LM head */
+    uint16_t layer;
+    uint32_t begin, end;     /* output rows or items                                     */
+    uint16_t wait_ctr, signal_ctr;
+    uint32_t wait_mul, wait_add;
+} tiles_task;
+
+typedef struct tiles_schedule_s *tiles_schedule_t;
+
+/* Builds (but does not validate) the schedule the planner would make for
+ * n_ctas CTAs, a ring of ring_slots slots of slot_bytes bytes. Host only. */
+tiles_status_t tiles_schedule_build(const tiles_model_desc *desc, const tiles_plan_opts *opts,
+                                    int32_t n_ctas, tiles_schedule_t *out);
+
+/* Validates a schedule: every output row / item covered exactly once per step,
+ * indices in range, each wait satisfiable by earlier signals and covering all
+ * of them, copy sizes and ring slots 16-byte aligned. Returns TILES_OK or
+ * TILES_ERR_PLAN_INVALID; `why` (may be NULL) receives a message. */
+tiles_status_t tiles_schedule_validate(tiles_schedule_t sched, char *why, size_t why_len);
+
+/* Mutable view of the task table: tasks of CTA c are
+ * tasks[offsets[c] .. offsets[c+1]). Valid until the schedule is destroyed. */
+tiles_status_t tiles_schedule_tasks(tiles_schedule_t sched, tiles_task **tasks,
+                                    int32_t *n_tasks, const int32_t **offsets, int32_t *n_ctas);
+
+/* Per-CTA weight+KV bytes streamed in one step at context position `pos`. */
+tiles_status_t tiles_schedule_cta_bytes(tiles_schedule_t sched, int32_t pos, int64_t *bytes);
+
+void tiles_schedule_destroy(tiles_schedule_t sched);
+
+/* ------------------------------------------------------------------------ */
+/* Measurement helpers.                                                       */
+
+/* Device-to-device copy of `bytes` (multiple of 16, both pointers 16-byte
+ * aligned) by a grid of n_ctas CTAs (0 = 2 per SM), asynchronous on stream.
+ * The HBM peak the roofline fraction is taken against. */
+tiles_status_t tiles_copy_bw(void *dst, const void *src, size_t bytes, int32_t n_ctas,
+                             void *stream);
+
+/* Grid-barrier round trip: one cooperative launch of n_ctas CTAs that crosses
+ * `rounds` grid barriers; *ns_per_barrier receives the mean cost measured
+ * inside the kernel with the global timer. Synchronous. */
+tiles_status_t tiles_barrier_cost(int32_t n_ctas, int32_t rounds, double *ns_per_barrier);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TILES_H */

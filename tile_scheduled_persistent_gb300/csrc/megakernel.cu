@@ -1,0 +1,1088 @@
+// The persistent decode kernel for sm_103a.
+//
+// One CTA per SM runs its static task list once per step, for up to 64 steps
+// per cooperative launch ("Tiles: Scheduling LLM Decoding as a Graph of
+// Tiles", intro and "What the code contains": a fixed worker per SM executes a
+// planned schedule, greedy selection inside the kernel, up to 64 tokens per
+// launch). Each CTA has
+//   - one producer warp: a single lane walks the same task list as the
+//     consumers and streams every tile's weight rows (or K/V positions) into a
+//     shared-memory ring with cp.async.bulk (TMA) copies, completing on per-slot
+//     mbarriers. Weights never depend on activations, so the stream runs ahead
+//     across phase boundaries and keeps HBM busy while the consumers wait
+//     (the megakernel paragraph of the same page: load the next weights while
+//     the current work finishes).
+//   - eight consumer warps: chunk j of the CTA's stream goes to ring slot
+//     j % slots, and each slot has one owning warp, (j % slots) % 8. GEMV chunks: 16-byte bf16 loads from shared memory,
+//     FP32 FMA, warp-shuffle reductions. Attention chunks: split-KV online
+//     softmax over up to kv_block positions per chunk.
+// Phases are ordered by counters in global memory (one grid barrier per phase
+// in the wave schedule, or per-phase dependency counters): release-add after a
+// task, acquire-spin before one. Every spin is bounded by the global timer;
+// on expiry the CTA records an error in the status word, drains its copies in
+// flight and returns, and every other CTA leaves at its next wait.
+//
+// Fused work (same page, intro: norms and activations fold into the tiles
+// next to them; "History and roadmap", "M8 so far": q/k norm + RoPE + KV
+// write, residual + RMSNorm and SwiGLU-in-GEMV fusions):
+//   QKV tiles     RMSNorm of the residual in the prologue
+//   ATTN tiles    per-head q/k RMSNorm, RoPE, KV write at the new position
+//   O / DOWN      residual add in the epilogue
+//   GATE/UP       RMSNorm prologue, SwiGLU epilogue
+//   LM head       final RMSNorm prologue, argmax epilogue (packed 64-bit
+//                 atomicMax: ordered logit bits high, inverted row low, so the
+//                 lowest row wins ties)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tiles_internal.h"
+
+namespace tiles {
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         unsigned long long policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_nohint(void *dst, const void *src, uint32_t bytes,
+                                                uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_volatile(const uint32_t *p) {
+    return *(const volatile uint32_t *)p;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_release_cta(int *p, int v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_cta(const int *p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// Consumer barrier that also ORs a flag over all consumer threads: every thread
+// gets the same answer, so leaving on it keeps the barrier sequence aligned.
+__device__ __forceinline__ bool consumer_sync_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kConsumerWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
+// ------------------------------------------------------------------ numerics
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// float -> bfloat16, round to nearest even (finite inputs; NaN kept as NaN)
+__device__ __forceinline__ uint16_t f2bf(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+__device__ __forceinline__ float round_bf(float f) { return bf2f(f2bf(f)); }
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+    f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
+    f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
+}
+
+__device__ __forceinline__ float dot8(const uint4 &w, const float (&x)[8], float acc) {
+    acc = fmaf(bf_lo(w.x), x[0], acc); acc = fmaf(bf_hi(w.x), x[1], acc);
+    acc = fmaf(bf_lo(w.y), x[2], acc); acc = fmaf(bf_hi(w.y), x[3], acc);
+    acc = fmaf(bf_lo(w.z), x[4], acc); acc = fmaf(bf_hi(w.z), x[5], acc);
+    acc = fmaf(bf_lo(w.w), x[6], acc); acc = fmaf(bf_hi(w.w), x[7], acc);
+    return acc;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+// order-preserving key of (logit, row): bigger logit first, lower row on ties
+__device__ __forceinline__ unsigned long long argmax_key(float f, uint32_t row) {
+    uint32_t u = __float_as_uint(f);
+    uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - row);
+}
+__device__ __forceinline__ int key_row(unsigned long long k) {
+    return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+}
+
+// ------------------------------------------------------------------ shared state
+struct Ctl {
+    int unused;
+    int token;
+    int step_ready;  // consumers passed the first wait of this step (KV of earlier steps visible)
+    int pad;
+    float red[kConsumerWarps];
+    unsigned long long warp_key[kConsumerWarps];
+};
+
+struct Smem {
+    uint64_t *full, *empty;
+    Ctl *ctl;
+    uint8_t *ring;
+    uint8_t *vec;
+};
+
+__device__ __forceinline__ Smem smem_layout(uint8_t *base, const KernelParams &p) {
+    Smem s;
+    s.full = reinterpret_cast<uint64_t *>(base);
+    s.empty = s.full + kMaxSlots;
+    s.ctl = reinterpret_cast<Ctl *>(base + 2 * kMaxSlots * 8);
+    s.ring = base + p.ring_off;
+    s.vec = base + p.vec_off;
+    return s;
+}
+
+__device__ __forceinline__ bool failed(const KernelParams &p) { return ld_volatile(p.status) != 0; }
+
+// Bounded spin until counter >= target. false when the run is aborting.
+__device__ bool wait_counter(const KernelParams &p, const uint32_t *ctr, uint32_t target) {
+    if (ld_acquire(ctr) >= target) return true;
+    unsigned long long t0 = global_timer();
+    for (uint32_t spin = 1;; ++spin) {
+        if (ld_acquire(ctr) >= target) return true;
+        if ((spin & 31u) == 0) {
+            if (failed(p)) return false;
+            if (global_timer() - t0 > p.timeout_ns) {
+                atomicOr(p.status, kDevTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded mbarrier wait. false on timeout or when the run is aborting.
+__device__ bool wait_mbar(const KernelParams &p, uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0 = global_timer();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 15u) == 0) {
+            if (failed(p)) return false;
+            if (global_timer() - t0 > p.timeout_ns) {
+                atomicOr(p.status, kDevTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ producer
+struct Producer {
+    const KernelParams &p;
+    Smem &s;
+    uint32_t j = 0;  // chunks issued
+    bool ok = true;
+    unsigned long long pol_weights;  // L2 evict-first: weights are streamed once per step
+
+    __device__ Producer(const KernelParams &p_, Smem &s_) : p(p_), s(s_) {
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_weights));
+    }
+
+    // Reserve the next slot: wait until its previous chunk was consumed.
+    __device__ uint8_t *acquire(uint64_t **bar) {
+        const uint32_t ns = (uint32_t)p.g.ring_slots;
+        uint32_t slot = j % ns;
+        if (j >= ns && !wait_mbar(p, &s.empty[slot], ((j / ns) - 1u) & 1u)) {
+            ok = false;
+            return nullptr;
+        }
+        *bar = &s.full[slot];
+        return s.ring + (size_t)slot * p.g.slot_bytes;
+    }
+
+    __device__ void gemv_chunk(int op, int layer, uint32_t r0, uint32_t nr) {
+        uint64_t *bar;
+        uint8_t *dst = acquire(&bar);
+        if (!dst) return;
+        const Geom &g = p.g;
+        const LayerPtrs &lw = p.layers[layer];
+        const int in = op_in_dim(g, op);
+        const uint32_t rb = (uint32_t)in * 2u;
+        const int rpc = op_rows_per_chunk(g, op);
+        const uint32_t bytes = nr * rb * (uint32_t)op_mats(op);
+        mbar_expect_tx(bar, bytes);
+        const unsigned long long pol = pol_weights;
+        switch (op) {
+            case TILES_OP_QKV: {
+                // rows of the concatenation [Wq; Wk; Wv]
+                uint32_t r = r0, end = r0 + nr;
+                while (r < end) {
+                    const uint16_t *base;
+                    uint32_t lo, hi;
+                    if (r < (uint32_t)g.qd) { base = lw.wq; lo = 0; hi = g.qd; }
+                    else if (r < (uint32_t)(g.qd + g.kvd)) { base = lw.wk; lo = g.qd; hi = g.qd + g.kvd; }
+                    else { base = lw.wv; lo = g.qd + g.kvd; hi = g.qkv_rows; }
+                    uint32_t e = end < hi ? end : hi;
+                    bulk_g2s(dst + (size_t)(r - r0) * rb, base + (size_t)(r - lo) * in, (e - r) * rb,
+                             bar, pol);
+                    r = e;
+                }
+                break;
+            }
+            case TILES_OP_OPROJ:
+                bulk_g2s(dst, lw.wo + (size_t)r0 * in, nr * rb, bar, pol);
+                break;
+            case TILES_OP_GATEUP:
+                bulk_g2s(dst, lw.w_gate + (size_t)r0 * in, nr * rb, bar, pol);
+                bulk_g2s(dst + (size_t)rpc * rb, lw.w_up + (size_t)r0 * in, nr * rb, bar, pol);
+                break;
+            case TILES_OP_DOWN:
+                bulk_g2s(dst, lw.w_down + (size_t)r0 * in, nr * rb, bar, pol);
+                break;
+            case TILES_OP_LMHEAD:
+                bulk_g2s(dst, p.embed + (size_t)r0 * in, nr * rb, bar, pol);
+                break;
+        }
+        ++j;
+    }
+
+    // K and V of positions [p0, p1) (all < P) of kv head `h`, layer `layer`.
+    __device__ void kv_chunk(int layer, int h, int p0, int p1) {
+        uint64_t *bar;
+        uint8_t *dst = acquire(&bar);
+        if (!dst) return;
+        const Geom &g = p.g;
+        const int n = p1 > p0 ? p1 - p0 : 0;
+        const uint32_t bytes = (uint32_t)n * g.d * 2u;
+        mbar_expect_tx(bar, 2u * bytes);
+        if (n > 0) {
+            size_t off = ((size_t)(layer * g.nkv + h) * g.max_pos + p0) * g.d;
+            bulk_g2s_nohint(dst, p.k_cache + off, bytes, bar);
+            bulk_g2s_nohint(dst + (size_t)g.kv_block * g.d * 2, p.v_cache + off, bytes, bar);
+        }
+        ++j;
+    }
+
+    // K/V of positions written by step st-1 may be read only after this CTA's
+    // consumers acquired the end of step st-1 (they publish that in step_ready).
+    int ready = 0;
+    __device__ bool kv_ready(int st) {
+        if (ready >= st) return true;
+        unsigned long long t0 = global_timer();
+        for (uint32_t spin = 0;; ++spin) {
+            ready = ld_acquire_cta(&s.ctl->step_ready);
+            if (ready >= st) break;
+            if ((spin & 15u) == 15u) {
+                if (failed(p)) return false;
+                if (global_timer() - t0 > p.timeout_ns) {
+                    atomicOr(p.status, kDevTimeout);
+                    return false;
+                }
+            }
+        }
+        // generic-proxy K/V writes of earlier steps, then async-proxy reads
+        fence_proxy_async_global();
+        return true;
+    }
+
+    __device__ void run(int cta) {
+        const Geom &g = p.g;
+        const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
+        fence_proxy_async_global();
+        for (int st = 0; st < p.n_steps && ok; ++st) {
+            const int P = p.pos0 + st;
+            for (int ti = t0; ti < t1 && ok; ++ti) {
+                const tiles_task t = p.tasks[ti];
+                if (op_is_gemv(t.op)) {
+                    const uint32_t rpc = (uint32_t)op_rows_per_chunk(g, t.op);
+                    for (uint32_t r = t.begin; r < t.end && ok; r += rpc) {
+                        uint32_t nr = t.end - r < rpc ? t.end - r : rpc;
+                        gemv_chunk(t.op, t.layer, r, nr);
+                    }
+                } else if (t.op == TILES_OP_ATTN) {
+                    if (!kv_ready(st)) { ok = false; break; }
+                    for (uint32_t it = t.begin; it < t.end && ok; ++it) {
+                        const int h = (int)(it / (uint32_t)g.kv_splits);
+                        const int c = (int)(it % (uint32_t)g.kv_splits);
+                        int b0, b1;
+                        attn_split_blocks(g, P + 1, c, &b0, &b1);
+                        for (int b = b0; b < b1 && ok; ++b) {
+                            int q0 = b * g.kv_block, q1 = q0 + g.kv_block;
+                            if (q1 > P) q1 = P;  // position P itself is computed in this step
+                            kv_chunk(t.layer, h, q0, q1);
+                        }
+                    }
+                }
+            }
+        }
+        // drain: wait for every copy still in flight so no bulk copy outlives the CTA
+        const uint32_t ns = (uint32_t)g.ring_slots;
+        uint32_t first = j > ns ? j - ns : 0;
+        for (uint32_t k = first; k < j; ++k) {
+            unsigned long long t0n = global_timer();
+            while (!mbar_try_wait(&s.full[k % ns], (k / ns) & 1u)) {
+                if (global_timer() - t0n > p.timeout_ns) break;
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------ consumers
+struct Consumer {
+    const KernelParams &p;
+    Smem &s;
+    const int tid, warp, lane;
+    uint32_t j = 0;  // chunks consumed by the CTA (all warps keep the same count)
+    int step = 0, P = 0;
+    bool bad = false;  // this thread saw a timeout, an abort or a bad index
+
+    __device__ Consumer(const KernelParams &p_, Smem &s_, int tid_)
+        : p(p_), s(s_), tid(tid_), warp(tid_ >> 5), lane(tid_ & 31) {}
+
+    // Chunk k lives in ring slot k % slots and is consumed by the warp that owns
+    // that slot, (k % slots) % 8. One owner per slot means a warp only waits on
+    // a slot after it released the slot's previous chunk itself, so the
+    // mbarrier parity can never alias a chunk two ring laps ahead.
+    __device__ bool mine(uint32_t k) const {
+        return (int)((k % (uint32_t)p.g.ring_slots) % kConsumerWarps) == warp;
+    }
+
+    // slot of CTA chunk k, after its data landed; nullptr when aborting
+    __device__ uint8_t *wait_chunk(uint32_t k) {
+        const uint32_t ns = (uint32_t)p.g.ring_slots;
+        uint32_t slot = k % ns;
+        const bool ok = wait_mbar(p, &s.full[slot], (k / ns) & 1u);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {  // warp-uniform decision
+            bad = true;
+            return nullptr;
+        }
+        return s.ring + (size_t)slot * p.g.slot_bytes;
+    }
+    __device__ void release_chunk(uint32_t k) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.empty[k % (uint32_t)p.g.ring_slots]);
+    }
+
+    __device__ int token_of_step(int st) {
+        const int sg = p.step0 + st;
+        int tok;
+        if (sg < p.n_prompt) tok = p.prompt[sg];
+        else if (st > 0) tok = key_row(__ldcg(&p.keys[st - 1]));
+        else tok = __ldcg(&p.out_tokens[sg - p.n_prompt]);
+        return tok;
+    }
+
+    // ---------------------------------------------------------- prologues
+    // vec <- bf16(rmsnorm(src) * gain), src bf16 [n]; sum of squares in a fixed
+    // order, so every CTA computes the same scale.
+    __device__ void rmsnorm_to_vec(const uint16_t *src, const uint16_t *gain, int n) {
+        const int nu4 = n >> 3;
+        float ss = 0.f;
+        for (int c = tid; c < nu4; c += kConsumerWarps * 32) {
+            uint4 v = __ldcg(reinterpret_cast<const uint4 *>(src) + c);
+            float f[8];
+            unpack8(v, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) s.ctl->red[warp] = ss;
+        consumer_sync();
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) tot += s.ctl->red[w];
+        const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)n), p.eps)));
+        uint4 *dst = reinterpret_cast<uint4 *>(s.vec);
+        for (int c = tid; c < nu4; c += kConsumerWarps * 32) {
+            uint4 v = __ldcg(reinterpret_cast<const uint4 *>(src) + c);
+            uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gain) + c);
+            float f[8], gf[8];
+            unpack8(v, f);
+            unpack8(gv, gf);
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                uint16_t lo = f2bf(__fmul_rn(__fmul_rn(f[2 * e], r), gf[2 * e]));
+                uint16_t hi = f2bf(__fmul_rn(__fmul_rn(f[2 * e + 1], r), gf[2 * e + 1]));
+                o[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+            dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+
+    __device__ void copy_to_vec(const uint16_t *src, int n) {
+        const int nu4 = n >> 3;
+        uint4 *dst = reinterpret_cast<uint4 *>(s.vec);
+        for (int c = tid; c < nu4; c += kConsumerWarps * 32)
+            dst[c] = __ldcg(reinterpret_cast<const uint4 *>(src) + c);
+    }
+
+    // ---------------------------------------------------------- GEMV tasks
+    template <int MATS>
+    __device__ void gemv_task(const tiles_task &t) {
+        const Geom &g = p.g;
+        const int op = t.op;
+        const int in = op_in_dim(g, op);
+        const int nu4 = in >> 3;
+        const uint32_t rpc = (uint32_t)op_rows_per_chunk(g, op);
+        const uint32_t nchunks = (t.end - t.begin + rpc - 1) / rpc;
+        const uint4 *vec = reinterpret_cast<const uint4 *>(s.vec);
+        unsigned long long best = 0;
+        const int sg = p.step0 + step;
+        (void)sg;
+        for (uint32_t k = 0; k < nchunks; ++k) {
+            const uint32_t jj = j + k;
+            if (!mine(jj)) continue;
+            const uint32_t r0 = t.begin + k * rpc;
+            const uint32_t nr = t.end - r0 < rpc ? t.end - r0 : rpc;
+            const uint8_t *slot = wait_chunk(jj);
+            if (!slot) break;
+            float acc[kMaxRowsPerChunk][MATS];
+#pragma unroll
+            for (int r = 0; r < kMaxRowsPerChunk; ++r)
+#pragma unroll
+                for (int m = 0; m < MATS; ++m) acc[r][m] = 0.f;
+            for (int c = lane; c < nu4; c += 32) {
+                float xf[8];
+                unpack8(vec[c], xf);
+#pragma unroll
+                for (int r = 0; r < kMaxRowsPerChunk; ++r) {
+                    if ((uint32_t)r < nr) {
+#pragma unroll
+                        for (int m = 0; m < MATS; ++m) {
+                            const uint4 w = reinterpret_cast<const uint4 *>(
+                                slot + ((size_t)m * rpc + r) * (size_t)in * 2)[c];
+                            acc[r][m] = dot8(w, xf, acc[r][m]);
+                        }
+                    }
+                }
+            }
+            release_chunk(jj);
+            float mine[MATS];
+#pragma unroll
+            for (int m = 0; m < MATS; ++m) mine[m] = 0.f;
+#pragma unroll
+            for (int r = 0; r < kMaxRowsPerChunk; ++r) {
+                if ((uint32_t)r < nr) {
+#pragma unroll
+                    for (int m = 0; m < MATS; ++m) {
+                        float v = warp_sum(acc[r][m]);
+                        if (lane == r) mine[m] = v;
+                    }
+                }
+            }
+            if ((uint32_t)lane < nr) {
+                const uint32_t row = r0 + lane;
+                switch (op) {
+                    case TILES_OP_QKV:
+                        __stcg(&p.qkv[row], mine[0]);
+                        break;
+                    case TILES_OP_OPROJ: {
+                        const uint16_t xb = (t.layer == 0)
+                                                ? p.embed[(size_t)s.ctl->token * g.H + row]
+                                                : __ldcg(&p.x[row]);
+                        __stcg(&p.x[row], f2bf(__fadd_rn(bf2f(xb), mine[0])));
+                        break;
+                    }
+                    case TILES_OP_DOWN: {
+                        const uint16_t xb = __ldcg(&p.x[row]);
+                        __stcg(&p.x[row], f2bf(__fadd_rn(bf2f(xb), mine[0])));
+                        break;
+                    }
+                    case TILES_OP_GATEUP: {
+                        const float gt = mine[0];
+                        const float silu = __fdiv_rn(gt, __fadd_rn(1.0f, expf(-gt)));
+                        __stcg(&p.a[row], f2bf(__fmul_rn(silu, mine[MATS - 1])));
+                        break;
+                    }
+                    case TILES_OP_LMHEAD: {
+                        if (p.out_logits) __stcg(&p.out_logits[(size_t)sg * g.V + row], mine[0]);
+                        break;
+                    }
+                }
+            }
+            if (op == TILES_OP_LMHEAD) {
+                unsigned long long key = (uint32_t)lane < nr ? argmax_key(mine[0], r0 + lane) : 0ull;
+                key = warp_max_u64(key);
+                best = key > best ? key : best;
+            }
+        }
+        j += nchunks;
+        if (op == TILES_OP_LMHEAD) {
+            if (lane == 0) s.ctl->warp_key[warp] = best;
+            consumer_sync();
+            if (tid == 0) {
+                unsigned long long b = 0;
+                for (int w = 0; w < kConsumerWarps; ++w) b = s.ctl->warp_key[w] > b ? s.ctl->warp_key[w] : b;
+                atomicMax(&p.keys[step], b);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------- attention
+    // Layout of the vec region during attention tasks.
+    struct AttnSmem {
+        float *q;          // [G][d] f32 (bf16-valued)
+        uint16_t *knew;    // [d]
+        uint16_t *vnew;    // [d]
+        float *prob;       // [warps][32][G]
+        float *wstate;     // [warps][G][4 + d]
+    };
+    __device__ AttnSmem attn_smem() const {
+        const Geom &g = p.g;
+        AttnSmem a;
+        uint8_t *b = s.vec;
+        a.q = reinterpret_cast<float *>(b);
+        b += (size_t)g.G * g.d * 4;
+        a.knew = reinterpret_cast<uint16_t *>(b);
+        b += (size_t)g.d * 2;
+        a.vnew = reinterpret_cast<uint16_t *>(b);
+        b += (size_t)g.d * 2;
+        a.prob = reinterpret_cast<float *>(b);
+        b += (size_t)kConsumerWarps * 32 * g.G * 4;
+        a.wstate = reinterpret_cast<float *>(b);
+        return a;
+    }
+
+    // q heads of kv head h (and k, v of head h): optional RMSNorm over the head,
+    // RoPE at position P, rounding to bf16. One warp per head.
+    template <int D>
+    __device__ void prep_qkv(int h, const AttnSmem &a) {
+        const Geom &g = p.g;
+        const LayerPtrs &lw = p.layers[cur_layer];
+        const float *cs = p.rope_cos + (size_t)P * (D / 2);
+        const float *sn = p.rope_sin + (size_t)P * (D / 2);
+        constexpr int E = D / 32;  // elements per lane: lane, lane+32, ...
+        for (int hh = warp; hh < g.G + 2; hh += kConsumerWarps) {
+            const bool is_q = hh < g.G, is_k = hh == g.G;
+            const int row0 = is_q ? (h * g.G + hh) * D
+                                  : (is_k ? g.qd + h * D : g.qd + g.kvd + h * D);
+            float v[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[e] = __ldcg(&p.qkv[row0 + lane + 32 * e]);
+            if (!is_q && !is_k) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) a.vnew[lane + 32 * e] = f2bf(v[e]);
+                continue;
+            }
+            if (p.qk_norm) {
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
+                ss = warp_sum(ss);
+                const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)D), p.eps)));
+                const uint16_t *gn = is_q ? lw.q_norm : lw.k_norm;
+#pragma unroll
+                for (int e = 0; e < E; ++e) v[e] = __fmul_rn(__fmul_rn(v[e], r), bf2f(gn[lane + 32 * e]));
+            }
+            // rotate-half: element j pairs with j + D/2 (both held by this lane)
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) {
+                const int jx = lane + 32 * e;
+                const float c = cs[jx], sv = sn[jx];
+                const float x0 = v[e], x1 = v[e + E / 2];
+                v[e] = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sv));
+                v[e + E / 2] = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, sv));
+            }
+            if (is_q) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) a.q[hh * D + lane + 32 * e] = round_bf(v[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) a.knew[lane + 32 * e] = f2bf(v[e]);
+            }
+        }
+    }
+
+    int cur_layer = 0;
+
+    // one chunk of positions [q0, q0 + npos) for the G q heads of one kv head
+    template <int D, int G>
+    __device__ void attn_chunk(const uint8_t *slot, int npos, const AttnSmem &a, float (&m)[G],
+                               float (&l)[G], float (&o)[G][D / 32]) {
+        constexpr int NC = D / 8;   // 16-byte columns per row
+        constexpr int DPL = D / 32; // dims per lane in the PV product
+        const Geom &g = p.g;
+        const uint8_t *Kb = slot;
+        const uint8_t *Vb = slot + (size_t)g.kv_block * D * 2;
+        float *prob = a.prob + (size_t)warp * 32 * G;
+        for (int t0 = 0; t0 < npos; t0 += 32) {
+            const int t = t0 + lane;
+            const bool valid = t < npos;
+            float sc[G];
+#pragma unroll
+            for (int i = 0; i < G; ++i) sc[i] = 0.f;
+            if (valid) {
+                const uint4 *krow = reinterpret_cast<const uint4 *>(Kb + (size_t)t * D * 2);
+#pragma unroll
+                for (int jj = 0; jj < NC; ++jj) {
+                    const int col = (jj + lane) & (NC - 1);  // rotated: no bank conflicts
+                    float kf[8];
+                    unpack8(krow[col], kf);
+#pragma unroll
+                    for (int i = 0; i < G; ++i) {
+                        const float4 qa = reinterpret_cast<const float4 *>(a.q + i * D + col * 8)[0];
+                        const float4 qb = reinterpret_cast<const float4 *>(a.q + i * D + col * 8)[1];
+                        float acc = sc[i];
+                        acc = fmaf(kf[0], qa.x, acc); acc = fmaf(kf[1], qa.y, acc);
+                        acc = fmaf(kf[2], qa.z, acc); acc = fmaf(kf[3], qa.w, acc);
+                        acc = fmaf(kf[4], qb.x, acc); acc = fmaf(kf[5], qb.y, acc);
+                        acc = fmaf(kf[6], qb.z, acc); acc = fmaf(kf[7], qb.w, acc);
+                        sc[i] = acc;
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+                const float si = valid ? sc[i] * p.attn_scale : -INFINITY;
+                const float bm = warp_max(si);
+                const float mn = fmaxf(m[i], bm);
+                const float corr = expf(m[i] - mn);
+                const float pi = valid ? expf(si - mn) : 0.f;
+                const float ps = warp_sum(pi);
+                l[i] = fmaf(l[i], corr, ps);
+                m[i] = mn;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o[i][e] *= corr;
+                prob[lane * G + i] = pi;
+            }
+            __syncwarp();
+            const int nv = npos - t0 < 32 ? npos - t0 : 32;
+            for (int tt = 0; tt < nv; ++tt) {
+                float pv[G];
+#pragma unroll
+                for (int i = 0; i < G; ++i) pv[i] = prob[tt * G + i];
+                const uint8_t *vrow = Vb + (size_t)(t0 + tt) * D * 2;
+                float vf[DPL];
+                if (DPL == 2) {
+                    const uint32_t w = reinterpret_cast<const uint32_t *>(vrow)[lane];
+                    vf[0] = bf_lo(w);
+                    vf[1] = bf_hi(w);
+                } else {
+                    const uint2 w = reinterpret_cast<const uint2 *>(vrow)[lane];
+                    vf[0] = bf_lo(w.x);
+                    vf[1] = bf_hi(w.x);
+                    vf[DPL > 2 ? 2 : 0] = bf_lo(w.y);
+                    vf[DPL > 3 ? 3 : 1] = bf_hi(w.y);
+                }
+#pragma unroll
+                for (int i = 0; i < G; ++i)
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) o[i][e] = fmaf(pv[i], vf[e], o[i][e]);
+            }
+            __syncwarp();
+        }
+    }
+
+    template <int D, int G>
+    __device__ void attn_task(const tiles_task &t) {
+        const Geom &g = p.g;
+        const AttnSmem a = attn_smem();
+        constexpr int DPL = D / 32;
+        int prepared = -1;
+        for (uint32_t it = t.begin; it < t.end; ++it) {
+            const int h = (int)(it / (uint32_t)g.kv_splits);
+            const int c = (int)(it % (uint32_t)g.kv_splits);
+            if (h != prepared) {
+                consumer_sync();  // previous item finished reading q / knew / vnew
+                prep_qkv<D>(h, a);
+                consumer_sync();
+                prepared = h;
+            }
+            int b0, b1;
+            attn_split_blocks(g, P + 1, c, &b0, &b1);
+            const int pb = P / g.kv_block;
+            const bool has_new = pb >= b0 && pb < b1;
+            if (has_new && tid < D) {
+                // the one tile whose range holds position P writes the new K/V
+                const size_t off = ((size_t)(cur_layer * g.nkv + h) * g.max_pos + P) * D + tid;
+                p.k_cache[off] = a.knew[tid];
+                p.v_cache[off] = a.vnew[tid];
+                fence_proxy_async_global();
+            }
+            float m[G], l[G], o[G][DPL];
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+                m[i] = -INFINITY;
+                l[i] = 0.f;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
+            }
+            const uint32_t nch = (uint32_t)(b1 - b0);
+            for (uint32_t k = 0; k < nch; ++k) {
+                const uint32_t jj = j + k;
+                if (!mine(jj)) continue;
+                uint8_t *slot = wait_chunk(jj);
+                if (!slot) break;
+                const int q0 = (b0 + (int)k) * g.kv_block;
+                int q1 = q0 + g.kv_block;
+                if (q1 > P + 1) q1 = P + 1;
+                if (q0 <= P && P < q1) {
+                    // position P was not loaded; place the fresh K/V into the slot
+                    uint16_t *kd = reinterpret_cast<uint16_t *>(slot + (size_t)(P - q0) * D * 2);
+                    uint16_t *vd = reinterpret_cast<uint16_t *>(slot + (size_t)g.kv_block * D * 2 +
+                                                                (size_t)(P - q0) * D * 2);
+                    for (int e = lane; e < D; e += 32) {
+                        kd[e] = a.knew[e];
+                        vd[e] = a.vnew[e];
+                    }
+                    __syncwarp();
+                }
+                attn_chunk<D, G>(slot, q1 - q0, a, m, l, o);
+                fence_proxy_async_smem();  // generic writes to the slot before the TMA reuses it
+                release_chunk(jj);
+            }
+            j += nch;
+            // per-warp states -> shared memory -> one partial for (q heads, split c)
+            float *ws = a.wstate + (size_t)warp * G * (kPartialPad + D);
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+                if (lane == 0) {
+                    ws[i * (kPartialPad + D) + 0] = m[i];
+                    ws[i * (kPartialPad + D) + 1] = l[i];
+                }
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) ws[i * (kPartialPad + D) + kPartialPad + lane * DPL + e] = o[i][e];
+            }
+            consumer_sync();
+            for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
+                const int i = idx / D, dd = idx % D;
+                float M = -INFINITY;
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    M = fmaxf(M, a.wstate[((size_t)w * G + i) * (kPartialPad + D)]);
+                float L = 0.f, O = 0.f;
+                if (M != -INFINITY) {
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        const float *st = a.wstate + ((size_t)w * G + i) * (kPartialPad + D);
+                        const float sc = expf(st[0] - M);
+                        L = fmaf(sc, st[1], L);
+                        O = fmaf(sc, st[kPartialPad + dd], O);
+                    }
+                }
+                float *dst = p.partials + ((size_t)(h * G + i) * g.kv_splits + c) * (kPartialPad + D);
+                if (dd == 0) {
+                    __stcg(&dst[0], M);
+                    __stcg(&dst[1], L);
+                }
+                __stcg(&dst[kPartialPad + dd], O);
+            }
+            // wstate is reused by the next item; leave together on any failure
+            if (consumer_sync_or(bad)) return;
+        }
+    }
+
+    // merge the split partials of q heads [begin, end): one thread per element
+    __device__ void combine_task(const tiles_task &t) {
+        const Geom &g = p.g;
+        const int D = g.d, S = g.kv_splits;
+        const int n = (int)(t.end - t.begin) * D;
+        for (int idx = tid; idx < n; idx += kConsumerWarps * 32) {
+            const int hq = (int)t.begin + idx / D, dd = idx % D;
+            const float *base = p.partials + (size_t)hq * S * (kPartialPad + D);
+            float M = -INFINITY;
+            for (int c = 0; c < S; ++c) M = fmaxf(M, __ldcg(&base[(size_t)c * (kPartialPad + D)]));
+            float L = 0.f, O = 0.f;
+            for (int c = 0; c < S; ++c) {
+                const float *pc = base + (size_t)c * (kPartialPad + D);
+                const float mc = __ldcg(&pc[0]);
+                if (mc == -INFINITY) continue;
+                const float w = expf(mc - M);
+                L = fmaf(w, __ldcg(&pc[1]), L);
+                O = fmaf(w, __ldcg(&pc[kPartialPad + dd]), O);
+            }
+            __stcg(&p.o[(size_t)hq * D + dd], f2bf(__fdiv_rn(O, L)));
+        }
+    }
+
+    __device__ void attn_dispatch(const tiles_task &t) {
+        const int D = p.g.d, G = p.g.G;
+#define TILES_ATTN_CASE(DD, GG) \
+    if (D == DD && G == GG) { attn_task<DD, GG>(t); return; }
+        TILES_ATTN_CASE(64, 1) TILES_ATTN_CASE(64, 2) TILES_ATTN_CASE(64, 4) TILES_ATTN_CASE(64, 8)
+        TILES_ATTN_CASE(128, 1) TILES_ATTN_CASE(128, 2) TILES_ATTN_CASE(128, 4) TILES_ATTN_CASE(128, 8)
+#undef TILES_ATTN_CASE
+    }
+
+    __device__ void prep_dispatch(int h, const AttnSmem &a) {
+        if (p.g.d == 64) prep_qkv<64>(h, a);
+        else prep_qkv<128>(h, a);
+    }
+
+    // ---------------------------------------------------------- main loop
+    __device__ void run(int cta) {
+        const Geom &g = p.g;
+        const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
+        for (step = 0; step < p.n_steps; ++step) {
+            P = p.pos0 + step;
+            for (int ti = t0; ti < t1; ++ti) {
+                const tiles_task t = p.tasks[ti];
+                cur_layer = t.layer;
+                // ---- wait for the inputs
+                if (tid == 0) {
+                    const uint32_t target = t.wait_mul * (uint32_t)step + t.wait_add;
+                    if (t.wait_ctr != TILES_NO_COUNTER &&
+                        !wait_counter(p, p.counters + (size_t)t.wait_ctr * kCounterStride, target))
+                        bad = true;
+                    if (ti == t0 && !bad) st_release_cta(&s.ctl->step_ready, step);
+                    if (!bad && (t.op == TILES_OP_QKV || t.op == TILES_OP_OPROJ) && t.layer == 0) {
+                        int tok = token_of_step(step);
+                        if (tok < 0 || tok >= g.V) {
+                            atomicOr(p.status, kDevBounds);
+                            bad = true;
+                            tok = 0;
+                        }
+                        s.ctl->token = tok;
+                    }
+                }
+                if (consumer_sync_or(bad)) return;
+                // ---- work
+                switch (t.op) {
+                    case TILES_OP_QKV:
+                        rmsnorm_to_vec(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : p.x,
+                                       p.layers[t.layer].attn_norm, g.H);
+                        consumer_sync();
+                        gemv_task<1>(t);
+                        break;
+                    case TILES_OP_ATTN:
+                        attn_dispatch(t);
+                        break;
+                    case TILES_OP_COMBINE:
+                        combine_task(t);
+                        break;
+                    case TILES_OP_OPROJ:
+                        copy_to_vec(p.o, g.qd);
+                        consumer_sync();
+                        gemv_task<1>(t);
+                        break;
+                    case TILES_OP_GATEUP:
+                        rmsnorm_to_vec(p.x, p.layers[t.layer].ffn_norm, g.H);
+                        consumer_sync();
+                        gemv_task<2>(t);
+                        break;
+                    case TILES_OP_DOWN:
+                        copy_to_vec(p.a, g.F);
+                        consumer_sync();
+                        gemv_task<1>(t);
+                        break;
+                    case TILES_OP_LMHEAD:
+                        rmsnorm_to_vec(p.x, p.final_norm, g.H);
+                        consumer_sync();
+                        gemv_task<1>(t);
+                        break;
+                    default:
+                        break;
+                }
+                // ---- publish
+                if (consumer_sync_or(bad)) return;
+                if (tid == 0 && t.signal_ctr != TILES_NO_COUNTER) {
+                    __threadfence();
+                    red_release_add(p.counters + (size_t)t.signal_ctr * kCounterStride, 1u);
+                }
+            }
+        }
+        // the chosen tokens of this launch
+        if (cta == 0 && tid == 0) {
+            const uint32_t target = p.final_mul * (uint32_t)p.n_steps;
+            if (wait_counter(p, p.counters + (size_t)p.final_ctr * kCounterStride, target)) {
+                for (int st = 0; st < p.n_steps; ++st) {
+                    const int sg = p.step0 + st;
+                    if (sg >= p.n_prompt - 1)
+                        p.out_tokens[sg - (p.n_prompt - 1)] = key_row(__ldcg(&p.keys[st]));
+                }
+            }
+        }
+    }
+};
+
+__global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_constant__ KernelParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    Smem s = smem_layout(smem_raw, p);
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int i = 0; i < p.g.ring_slots; ++i) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], 1);
+        }
+        s.ctl->unused = 0;
+        s.ctl->token = 0;
+        s.ctl->step_ready = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid >= kConsumerWarps * 32) {
+        if (tid == kConsumerWarps * 32) {
+            Producer prod(p, s);
+            prod.run(blockIdx.x);
+        }
+        return;
+    }
+    Consumer cons(p, s, tid);
+    cons.run(blockIdx.x);
+}
+
+// ------------------------------------------------------------------ launchers
+cudaError_t megakernel_configure(int smem_bytes) {
+    return cudaFuncSetAttribute(tiles_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_bytes);
+}
+
+cudaError_t megakernel_occupancy(int smem_bytes, int *blocks_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tiles_megakernel, kThreads,
+                                                         smem_bytes);
+}
+
+cudaError_t megakernel_launch(const KernelParams &p, int n_ctas, int smem_bytes, cudaStream_t st) {
+    void *args[] = {const_cast<KernelParams *>(&p)};
+    return cudaLaunchCooperativeKernel((const void *)tiles_megakernel, dim3(n_ctas), dim3(kThreads),
+                                       args, (size_t)smem_bytes, st);
+}
+
+// ------------------------------------------------------------------ measurement kernels
+__global__ void __launch_bounds__(512) copy_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src,
+                                                   size_t n) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (; i + 3 * stride < n; i += 4 * stride) {
+        uint4 a = __ldcs(src + i), b = __ldcs(src + i + stride), c = __ldcs(src + i + 2 * stride),
+              d = __ldcs(src + i + 3 * stride);
+        __stcs(dst + i, a);
+        __stcs(dst + i + stride, b);
+        __stcs(dst + i + 2 * stride, c);
+        __stcs(dst + i + 3 * stride, d);
+    }
+    for (; i < n; i += stride) __stcs(dst + i, __ldcs(src + i));
+}
+
+cudaError_t copy_launch(void *dst, const void *src, size_t bytes, int n_ctas, cudaStream_t st) {
+    copy_kernel<<<n_ctas, 512, 0, st>>>(reinterpret_cast<uint4 *>(dst),
+                                        reinterpret_cast<const uint4 *>(src), bytes / 16);
+    return cudaGetLastError();
+}
+
+// rounds of grid barriers; CTA 0 reports the elapsed global-timer nanoseconds
+__global__ void barrier_kernel(uint32_t *ctr, int rounds, unsigned long long *elapsed,
+                               uint32_t *status, unsigned long long timeout_ns) {
+    __shared__ int abort_flag;
+    const uint32_t n = gridDim.x;
+    unsigned long long t0 = 0;
+    if (threadIdx.x == 0) abort_flag = 0;
+    __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x == 0) t0 = global_timer();
+    for (int r = 0; r < rounds; ++r) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            red_release_add(ctr, 1u);
+            const uint32_t target = n * (uint32_t)(r + 1);
+            unsigned long long ts = global_timer();
+            while (ld_acquire(ctr) < target) {
+                if (global_timer() - ts > timeout_ns) {
+                    atomicOr(status, kDevTimeout);
+                    abort_flag = 1;
+                    break;
+                }
+            }
+        }
+        __syncthreads();
+        if (abort_flag) return;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *elapsed = global_timer() - t0;
+}
+
+cudaError_t barrier_launch(uint32_t *ctr, int rounds, unsigned long long *elapsed, uint32_t *status,
+                           int n_ctas, cudaStream_t st) {
+    unsigned long long timeout = 2000000000ull;
+    void *args[] = {&ctr, &rounds, &elapsed, &status, &timeout};
+    return cudaLaunchCooperativeKernel((const void *)barrier_kernel, dim3(n_ctas), dim3(128), args, 0,
+                                       st);
+}
+
+}  // namespace tiles

@@ -1,0 +1,501 @@
+// Offline planner and validator (host only, no CUDA calls).
+//
+// Builds the tile graph of one decode step, assigns every tile to one of the
+// persistent worker CTAs so that the bytes each CTA streams stay balanced,
+// orders the tiles into waves (one grid barrier per phase) or dependency-
+// counter chains, and validates the result before anything runs on the GPU.
+// Source: "Tiles: Scheduling LLM Decoding as a Graph of Tiles", intro (tiles
+// are output-row ranges with their fused work; a planner assigns every tile to
+// a fixed worker, balances the bytes each worker streams, groups tiles into
+// waves separated by grid barriers; the whole schedule is validated before
+// launch) and the Hazy-megakernel paragraph (start work once its inputs are
+// ready: the dependency-counter variant).
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "tiles_internal.h"
+
+namespace tiles {
+
+tiles_plan_opts default_opts() {
+    tiles_plan_opts o;
+    std::memset(&o, 0, sizeof(o));
+    o.scheduler = TILES_SCHED_COUNTERS;
+    return o;
+}
+
+static bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+static int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+// Attention scratch in the vec region: q [G][d] f32, new k and v [d] bf16,
+// per-warp probabilities [32][G] f32, per-warp states [G][4 + d] f32.
+static int attn_vec_bytes(int G, int d) {
+    return G * d * 4 + 2 * d * 2 + kConsumerWarps * 32 * G * 4 +
+           kConsumerWarps * G * (kPartialPad + d) * 4;
+}
+
+tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o, int n_ctas,
+                            int smem_limit, Geom *g, std::string *why) {
+    auto fail = [&](tiles_status_t st, const char *msg) {
+        if (why) *why = msg;
+        return st;
+    };
+    if (d.n_layers < 1 || d.hidden < 8 || d.n_q_heads < 1 || d.n_kv_heads < 1 || d.ffn < 8 ||
+        d.vocab < 1 || d.max_pos < 1 || d.head_dim < 1)
+        return fail(TILES_ERR_INVALID_ARG, "non-positive model dimension");
+    if (d.tied_embeddings != 1) return fail(TILES_ERR_UNSUPPORTED, "embeddings must be tied");
+    if (d.head_dim != 64 && d.head_dim != 128)
+        return fail(TILES_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (d.n_q_heads % d.n_kv_heads) return fail(TILES_ERR_UNSUPPORTED, "n_q_heads % n_kv_heads");
+    int G = d.n_q_heads / d.n_kv_heads;
+    if (!pow2(G) || G > 8) return fail(TILES_ERR_UNSUPPORTED, "GQA group must be 1, 2, 4 or 8");
+    if (d.hidden % 8 || d.ffn % 8) return fail(TILES_ERR_UNSUPPORTED, "hidden, ffn multiples of 8");
+    if (d.qk_norm != 0 && d.qk_norm != 1) return fail(TILES_ERR_INVALID_ARG, "qk_norm 0/1");
+    if (d.rope_scaling != 0 && d.rope_scaling != 1)
+        return fail(TILES_ERR_INVALID_ARG, "rope_scaling 0/1");
+    if (!(d.rope_theta > 1.0)) return fail(TILES_ERR_INVALID_ARG, "rope_theta");
+    if (!(d.rms_eps >= 0.0f)) return fail(TILES_ERR_INVALID_ARG, "rms_eps");
+    if (d.rope_scaling == 1 && (!(d.rs_factor > 0) || !(d.rs_high > d.rs_low) ||
+                                !(d.rs_low > 0) || d.rs_orig_max < 1))
+        return fail(TILES_ERR_INVALID_ARG, "llama3 scaling parameters");
+    if ((long long)d.n_q_heads * d.head_dim > 65536 || d.hidden > 65536 || d.ffn > 65536)
+        return fail(TILES_ERR_UNSUPPORTED, "dimension too large");
+    if (n_ctas < 1 || n_ctas > 4096) return fail(TILES_ERR_INVALID_ARG, "n_ctas");
+    if (o.flags != 0) return fail(TILES_ERR_INVALID_ARG, "flags must be 0");
+    if (o.scheduler != TILES_SCHED_WAVES && o.scheduler != TILES_SCHED_COUNTERS)
+        return fail(TILES_ERR_INVALID_ARG, "scheduler");
+
+    Geom &G_ = *g;
+    std::memset(&G_, 0, sizeof(G_));
+    G_.L = d.n_layers;
+    G_.H = d.hidden;
+    G_.nq = d.n_q_heads;
+    G_.nkv = d.n_kv_heads;
+    G_.d = d.head_dim;
+    G_.F = d.ffn;
+    G_.V = d.vocab;
+    G_.max_pos = d.max_pos;
+    G_.G = G;
+    G_.qd = d.n_q_heads * d.head_dim;
+    G_.kvd = d.n_kv_heads * d.head_dim;
+    G_.qkv_rows = G_.qd + 2 * G_.kvd;
+
+    // slot: large enough for one row of every GEMV (two for gate/up), >= 16 KB
+    int need = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, 2 * 2 * G_.H, 16384});
+    int slot = o.slot_bytes > 0 ? o.slot_bytes : round_up(need, 1024);
+    if (slot % 1024 || slot < need) return fail(TILES_ERR_INVALID_ARG, "slot_bytes too small or not a multiple of 1024");
+    G_.slot_bytes = slot;
+    auto rpc = [&](int in, int mats) {
+        return std::min(kMaxRowsPerChunk, slot / (in * 2 * mats));
+    };
+    G_.rpc_qkv = rpc(G_.H, 1);
+    G_.rpc_o = rpc(G_.qd, 1);
+    G_.rpc_gateup = rpc(G_.H, 2);
+    G_.rpc_down = rpc(G_.F, 1);
+    G_.rpc_lm = rpc(G_.H, 1);
+    int kb = slot / (2 * G_.d * 2);
+    kb = kb >= 32 ? kb / 32 * 32 : kb;
+    if (kb < 1) return fail(TILES_ERR_UNSUPPORTED, "slot too small for one KV position");
+    G_.kv_block = kb;
+    int nb_max = ceil_div(G_.max_pos, kb);
+    int splits = o.kv_splits > 0 ? o.kv_splits : std::max(1, std::min(nb_max, n_ctas / G_.nkv));
+    if (splits < 1 || splits > 4096) return fail(TILES_ERR_INVALID_ARG, "kv_splits");
+    G_.kv_splits = splits;
+
+    int vec = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, attn_vec_bytes(G, G_.d)});
+    G_.vec_bytes = round_up(vec, 128);
+    int avail = smem_limit - kCtlBytes - G_.vec_bytes;
+    int slots = o.ring_slots > 0 ? o.ring_slots : std::min(kMaxSlots, avail / slot);
+    if (slots < 2 || slots > kMaxSlots) return fail(TILES_ERR_UNSUPPORTED, "ring needs 2..32 slots");
+    G_.ring_slots = slots;
+    G_.smem_bytes = kCtlBytes + slots * slot + G_.vec_bytes;
+    if (G_.smem_bytes > smem_limit) return fail(TILES_ERR_UNSUPPORTED, "shared memory exceeds the limit");
+    return TILES_OK;
+}
+
+namespace {
+
+struct Assign {
+    int cta;
+    uint32_t begin, end;
+};
+
+// Contiguous row ranges, one per CTA, sized so cumulative streamed bytes stay
+// balanced: each CTA gets floor(R/N) rows and the R mod N extra rows go to the
+// CTAs that have streamed least so far (ties to the lower index).
+std::vector<Assign> assign_rows(int R, long long row_bytes, int N, std::vector<long long> &cum) {
+    std::vector<int> cnt(N, R / N);
+    int extra = R % N;
+    if (extra) {
+        std::vector<int> order(N);
+        std::iota(order.begin(), order.end(), 0);
+        std::stable_sort(order.begin(), order.end(),
+                         [&](int a, int b) { return cum[a] < cum[b]; });
+        for (int i = 0; i < extra; ++i) cnt[order[i]] += 1;
+    }
+    std::vector<Assign> out;
+    uint32_t r = 0;
+    for (int c = 0; c < N; ++c) {
+        if (cnt[c] == 0) continue;
+        out.push_back({c, r, r + (uint32_t)cnt[c]});
+        r += cnt[c];
+        cum[c] += cnt[c] * row_bytes;
+    }
+    return out;
+}
+
+// Single items (attention splits, combine heads) to the least-loaded CTAs,
+// consecutive items merged when they land on the same CTA.
+std::vector<Assign> assign_items(int n_items, const std::vector<long long> &item_bytes, int N,
+                                 std::vector<long long> &cum) {
+    std::vector<Assign> out;
+    for (int it = 0; it < n_items; ++it) {
+        int best = 0;
+        for (int c = 1; c < N; ++c)
+            if (cum[c] < cum[best]) best = c;
+        cum[best] += item_bytes[it];
+        if (!out.empty() && out.back().cta == best && out.back().end == (uint32_t)it)
+            out.back().end += 1;
+        else
+            out.push_back({best, (uint32_t)it, (uint32_t)it + 1});
+    }
+    return out;
+}
+
+}  // namespace
+
+tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &o, int N,
+                              int smem_limit, tiles_schedule_s *s, std::string *why) {
+    tiles_status_t st = resolve_geom(d, o, N, smem_limit, &s->geom, why);
+    if (st != TILES_OK) return st;
+    const Geom &g = s->geom;
+    s->desc = d;
+    s->opts = o;
+    s->n_ctas = N;
+    s->scheduler = o.scheduler;
+    const int PPS = phases_per_step(g);
+
+    // per phase, the (cta, range) tasks
+    std::vector<std::vector<Assign>> phase_tasks(PPS);
+    std::vector<int> phase_op(PPS), phase_layer(PPS);
+    std::vector<long long> cum(N, 0);
+    // attention bytes for balancing: split sizes at the largest position
+    for (int l = 0; l <= g.L; ++l) {
+        for (int k = 0; k < (l < g.L ? kPhaseKinds : 1); ++k) {
+            int kind = l < g.L ? k : 6;
+            int phi = phase_index(g, l < g.L ? l : 0, kind);
+            static const int ops[7] = {TILES_OP_QKV,  TILES_OP_ATTN,   TILES_OP_COMBINE,
+                                       TILES_OP_OPROJ, TILES_OP_GATEUP, TILES_OP_DOWN,
+                                       TILES_OP_LMHEAD};
+            int op = ops[kind];
+            phase_op[phi] = op;
+            phase_layer[phi] = l < g.L ? l : 0;
+            if (op_is_gemv(op)) {
+                phase_tasks[phi] = assign_rows(op_extent(g, op),
+                                               (long long)op_in_dim(g, op) * 2 * op_mats(op), N,
+                                               cum);
+            } else if (op == TILES_OP_ATTN) {
+                int n = op_extent(g, op);
+                std::vector<long long> b(n);
+                for (int it = 0; it < n; ++it) {
+                    tiles_task t{};
+                    t.op = TILES_OP_ATTN;
+                    t.begin = it;
+                    t.end = it + 1;
+                    b[it] = task_bytes(g, t, g.max_pos - 1);
+                }
+                phase_tasks[phi] = assign_items(n, b, N, cum);
+            } else {  // combine: cheap; spread one head per CTA
+                int n = op_extent(g, op);
+                std::vector<long long> b(n, 1);
+                phase_tasks[phi] = assign_items(n, b, N, cum);
+            }
+        }
+    }
+
+    // counters and waits
+    std::vector<std::vector<tiles_task>> per_cta(N);
+    if (o.scheduler == TILES_SCHED_WAVES) {
+        s->n_counters = 1;
+        for (int phi = 0; phi < PPS; ++phi) {
+            std::vector<bool> has(N, false);
+            std::vector<int> last(N, -1);
+            for (size_t k = 0; k < phase_tasks[phi].size(); ++k) last[phase_tasks[phi][k].cta] = (int)k;
+            for (size_t k = 0; k < phase_tasks[phi].size(); ++k) {
+                const Assign &a = phase_tasks[phi][k];
+                tiles_task t{};
+                t.op = (uint8_t)phase_op[phi];
+                t.phase_kind = (uint8_t)phase_of_op(phase_op[phi]);
+                t.layer = (uint16_t)phase_layer[phi];
+                t.begin = a.begin;
+                t.end = a.end;
+                t.wait_ctr = 0;
+                // one arrival per CTA and phase, after its last task of the phase
+                t.signal_ctr = last[a.cta] == (int)k ? 0 : TILES_NO_COUNTER;
+                t.wait_mul = (uint32_t)(N * PPS);
+                t.wait_add = (uint32_t)(N * phi);
+                has[a.cta] = true;
+                per_cta[a.cta].push_back(t);
+            }
+            for (int c = 0; c < N; ++c) {
+                if (has[c]) continue;
+                tiles_task t{};
+                t.op = TILES_OP_SYNC;
+                t.phase_kind = (uint8_t)phase_of_op(phase_op[phi]);
+                t.layer = (uint16_t)phase_layer[phi];
+                t.wait_ctr = 0;
+                t.signal_ctr = 0;
+                t.wait_mul = (uint32_t)(N * PPS);
+                t.wait_add = (uint32_t)(N * phi);
+                per_cta[c].push_back(t);
+            }
+        }
+        s->final_ctr = 0;
+        s->final_mul = (uint32_t)(N * PPS);
+    } else {
+        s->n_counters = PPS;
+        // previous non-empty phase, cyclically (phase 0 depends on the last of the step before)
+        std::vector<int> prev(PPS, -1);
+        int last_nonempty = -1;
+        for (int phi = PPS - 1; phi >= 0 && last_nonempty < 0; --phi)
+            if (!phase_tasks[phi].empty()) last_nonempty = phi;
+        int p = last_nonempty;
+        for (int phi = 0; phi < PPS; ++phi) {
+            prev[phi] = p;
+            if (!phase_tasks[phi].empty()) p = phi;
+        }
+        for (int phi = 0; phi < PPS; ++phi) {
+            int pp = prev[phi];
+            uint32_t npp = pp >= 0 ? (uint32_t)phase_tasks[pp].size() : 0;
+            for (auto &a : phase_tasks[phi]) {
+                tiles_task t{};
+                t.op = (uint8_t)phase_op[phi];
+                t.phase_kind = (uint8_t)phase_of_op(phase_op[phi]);
+                t.layer = (uint16_t)phase_layer[phi];
+                t.begin = a.begin;
+                t.end = a.end;
+                t.signal_ctr = (uint16_t)phi;
+                t.wait_ctr = (uint16_t)pp;
+                t.wait_mul = npp;
+                t.wait_add = pp < phi ? npp : 0;  // same step, or the step before
+                per_cta[a.cta].push_back(t);
+            }
+        }
+        s->final_ctr = last_nonempty;
+        s->final_mul = (uint32_t)phase_tasks[last_nonempty].size();
+    }
+    s->tasks.clear();
+    s->offsets.assign(N + 1, 0);
+    for (int c = 0; c < N; ++c) {
+        s->offsets[c] = (int32_t)s->tasks.size();
+        s->tasks.insert(s->tasks.end(), per_cta[c].begin(), per_cta[c].end());
+    }
+    s->offsets[N] = (int32_t)s->tasks.size();
+    return TILES_OK;
+}
+
+tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
+    char buf[256];
+    auto fail = [&](const char *msg) {
+        if (why) *why = msg;
+        return TILES_ERR_PLAN_INVALID;
+    };
+    const Geom &g = s.geom;
+    const int N = s.n_ctas, PPS = phases_per_step(g);
+    if ((int)s.offsets.size() != N + 1 || s.offsets[0] != 0 ||
+        s.offsets[N] != (int32_t)s.tasks.size())
+        return fail("task offsets inconsistent");
+    // geometry: every copy is a whole number of 16-byte units into 128-byte aligned slots
+    if (g.slot_bytes % 1024 || g.ring_slots < 2 || g.ring_slots > kMaxSlots)
+        return fail("ring geometry");
+    if ((2 * g.H) % 16 || (2 * g.F) % 16 || (2 * g.qd) % 16 || (2 * g.d) % 16)
+        return fail("row bytes not a multiple of 16");
+    for (int op = TILES_OP_QKV; op <= TILES_OP_LMHEAD; ++op) {
+        if (!op_is_gemv(op)) continue;
+        int r = op_rows_per_chunk(g, op);
+        if (r < 1 || (long long)r * op_in_dim(g, op) * 2 * op_mats(op) > g.slot_bytes)
+            return fail("rows per chunk do not fit a slot");
+    }
+    if (g.kv_block < 1 || 2LL * g.kv_block * g.d * 2 > g.slot_bytes) return fail("kv block");
+    if (g.smem_bytes > kSmemLimit) return fail("shared memory");
+    if (s.n_counters < 1 || s.n_counters > 0xFFFE) return fail("counter count");
+
+    // per phase coverage, per CTA order, signal accounting
+    std::vector<std::vector<std::pair<uint32_t, uint32_t>>> cover(PPS);
+    std::vector<int> phase_op(PPS, 0);
+    std::vector<std::vector<int>> sig_by_phase(PPS, std::vector<int>(s.n_counters, 0));
+    for (int c = 0; c < N; ++c) {
+        int last_phi = -1;
+        for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i) {
+            if (i < s.offsets[c] || i >= (int)s.tasks.size()) return fail("task index");
+            const tiles_task &t = s.tasks[i];
+            if (t.op < TILES_OP_QKV || t.op > TILES_OP_SYNC) return fail("unknown op");
+            int kind = t.op == TILES_OP_SYNC ? t.phase_kind : phase_of_op(t.op);
+            if (kind < 0 || kind > 6 || t.phase_kind != kind) return fail("phase kind mismatch");
+            if (kind < 6 && t.layer >= g.L) return fail("layer out of range");
+            int phi = phase_index(g, kind == 6 ? 0 : t.layer, kind);
+            if (phi < last_phi) return fail("tasks of a CTA out of phase order");
+            last_phi = phi;
+            if (t.op != TILES_OP_SYNC) {
+                if (phase_op[phi] && phase_op[phi] != t.op) return fail("two ops in one phase");
+                phase_op[phi] = t.op;
+                if (t.begin >= t.end || t.end > (uint32_t)op_extent(g, t.op))
+                    return fail("task range out of bounds");
+                cover[phi].push_back({t.begin, t.end});
+            }
+            if (t.signal_ctr != TILES_NO_COUNTER) {
+                if (t.signal_ctr >= s.n_counters) return fail("signal counter out of range");
+                sig_by_phase[phi][t.signal_ctr] += 1;
+            }
+            if (t.wait_ctr != TILES_NO_COUNTER && t.wait_ctr >= s.n_counters)
+                return fail("wait counter out of range");
+        }
+    }
+    for (int phi = 0; phi < PPS; ++phi) {
+        auto &v = cover[phi];
+        std::sort(v.begin(), v.end());
+        int kind = phi == PPS - 1 ? 6 : phi % kPhaseKinds;
+        static const int ops[7] = {TILES_OP_QKV,  TILES_OP_ATTN,   TILES_OP_COMBINE,
+                                   TILES_OP_OPROJ, TILES_OP_GATEUP, TILES_OP_DOWN,
+                                   TILES_OP_LMHEAD};
+        uint32_t want = (uint32_t)op_extent(g, ops[kind]);
+        uint32_t at = 0;
+        for (auto &r : v) {
+            if (r.first != at) {
+                std::snprintf(buf, sizeof buf, "phase %d: rows/items [%u, %u) %s", phi, at,
+                              r.first, r.first > at ? "not covered" : "covered twice");
+                if (why) *why = buf;
+                return TILES_ERR_PLAN_INVALID;
+            }
+            at = r.second;
+        }
+        if (at != want) {
+            std::snprintf(buf, sizeof buf, "phase %d: covers %u of %u rows/items", phi, at, want);
+            if (why) *why = buf;
+            return TILES_ERR_PLAN_INVALID;
+        }
+    }
+    // signals per step on each counter; per CTA, the counter its last task of each phase signals
+    std::vector<long long> per_step(s.n_counters, 0);
+    for (int phi = 0; phi < PPS; ++phi)
+        for (int c = 0; c < s.n_counters; ++c) per_step[c] += sig_by_phase[phi][c];
+    std::vector<int> last_sig((size_t)N * PPS, -2);  // -2: no task of the CTA in that phase
+    std::vector<int> phase_ntasks(PPS, 0);
+    for (int c = 0; c < N; ++c)
+        for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i) {
+            const tiles_task &t = s.tasks[i];
+            int kind = t.op == TILES_OP_SYNC ? t.phase_kind : phase_of_op(t.op);
+            int phi = phase_index(g, kind == 6 ? 0 : t.layer, kind);
+            phase_ntasks[phi] += 1;
+            last_sig[(size_t)c * PPS + phi] =
+                t.signal_ctr == TILES_NO_COUNTER ? -1 : (int)t.signal_ctr;
+        }
+    for (int c = 0; c < N; ++c) {
+        for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i) {
+            const tiles_task &t = s.tasks[i];
+            int kind = t.op == TILES_OP_SYNC ? t.phase_kind : phase_of_op(t.op);
+            int phi = phase_index(g, kind == 6 ? 0 : t.layer, kind);
+            if (t.wait_ctr == TILES_NO_COUNTER) return fail("task without a wait");
+            int ctr = t.wait_ctr;
+            long long before = 0;
+            for (int q = 0; q < phi; ++q) before += sig_by_phase[q][ctr];
+            if ((long long)t.wait_mul != per_step[ctr])
+                return fail("wait multiplier differs from the counter's signals per step");
+            if ((long long)t.wait_add != before)
+                return fail("wait target is not exactly the signals issued before this phase");
+            // the wait must cover the nearest earlier non-empty phase (cyclically): every CTA
+            // with work there signals this counter after its last task of that phase
+            int prev = -1;
+            for (int q = phi - 1; q >= 0 && prev < 0; --q)
+                if (phase_ntasks[q]) prev = q;
+            for (int q = PPS - 1; q > phi && prev < 0; --q)
+                if (phase_ntasks[q]) prev = q;
+            if (prev < 0) continue;
+            for (int c2 = 0; c2 < N; ++c2) {
+                int ls = last_sig[(size_t)c2 * PPS + prev];
+                if (ls != -2 && ls != ctr)
+                    return fail("wait does not cover every task of the previous phase");
+            }
+        }
+    }
+    if (s.final_ctr < 0 || s.final_ctr >= s.n_counters || (long long)s.final_mul != per_step[s.final_ctr])
+        return fail("final wait");
+    return TILES_OK;
+}
+
+}  // namespace tiles
+
+using namespace tiles;
+
+extern "C" {
+
+tiles_status_t tiles_schedule_build(const tiles_model_desc *desc, const tiles_plan_opts *opts,
+                                    int32_t n_ctas, tiles_schedule_t *out) {
+    if (!desc || !out) return TILES_ERR_INVALID_ARG;
+    *out = nullptr;
+    tiles_plan_opts o = opts ? *opts : default_opts();
+    auto *s = new tiles_schedule_s();
+    std::string why;
+    tiles_status_t st = build_schedule(*desc, o, n_ctas, kSmemLimit, s, &why);
+    if (st != TILES_OK) {
+        delete s;
+        return st;
+    }
+    *out = s;
+    return TILES_OK;
+}
+
+tiles_status_t tiles_schedule_validate(tiles_schedule_t sched, char *why, size_t why_len) {
+    if (!sched) return TILES_ERR_INVALID_ARG;
+    std::string w;
+    tiles_status_t st = validate_schedule(*sched, &w);
+    if (why && why_len) {
+        std::snprintf(why, why_len, "%s", st == TILES_OK ? "ok" : w.c_str());
+    }
+    return st;
+}
+
+tiles_status_t tiles_schedule_tasks(tiles_schedule_t sched, tiles_task **tasks, int32_t *n_tasks,
+                                    const int32_t **offsets, int32_t *n_ctas) {
+    if (!sched || !tasks || !n_tasks || !offsets || !n_ctas) return TILES_ERR_INVALID_ARG;
+    *tasks = sched->tasks.data();
+    *n_tasks = (int32_t)sched->tasks.size();
+    *offsets = sched->offsets.data();
+    *n_ctas = sched->n_ctas;
+    return TILES_OK;
+}
+
+tiles_status_t tiles_schedule_cta_bytes(tiles_schedule_t sched, int32_t pos, int64_t *bytes) {
+    if (!sched || !bytes || pos < 0 || pos >= sched->geom.max_pos) return TILES_ERR_INVALID_ARG;
+    for (int c = 0; c < sched->n_ctas; ++c) {
+        long long b = 0;
+        for (int i = sched->offsets[c]; i < sched->offsets[c + 1]; ++i)
+            b += task_bytes(sched->geom, sched->tasks[i], pos);
+        bytes[c] = b;
+    }
+    return TILES_OK;
+}
+
+void tiles_schedule_destroy(tiles_schedule_t sched) { delete sched; }
+
+const char *tiles_status_string(tiles_status_t st) {
+    switch (st) {
+        case TILES_OK: return "ok";
+        case TILES_ERR_INVALID_ARG: return "invalid argument";
+        case TILES_ERR_UNSUPPORTED: return "unsupported model shape";
+        case TILES_ERR_PLAN_INVALID: return "plan failed validation";
+        case TILES_ERR_DEVICE_MISMATCH: return "plan made for another device or binary";
+        case TILES_ERR_CAPACITY: return "start_pos + steps exceeds max_pos";
+        case TILES_ERR_CUDA: return "CUDA runtime error";
+        case TILES_ERR_TIMEOUT: return "in-kernel wait timed out";
+        case TILES_ERR_DEVICE_BOUNDS: return "kernel rejected an out-of-range index";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,392 @@
+// Runtime side of the C ABI: plan creation (device query, schedule build and
+// validation, upload of tables and RoPE angles, scratch allocation), decode
+// launches of up to 64 steps, status readback and the measurement helpers.
+// "Tiles: Scheduling LLM Decoding as a Graph of Tiles", "What the code
+// contains": the runtime re-validates a plan, checks it was made for this
+// worker binary and GPU, and runs up to 64 tokens per cooperative launch.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "tiles_internal.h"
+
+namespace tiles {
+cudaError_t megakernel_configure(int smem_bytes);
+cudaError_t megakernel_occupancy(int smem_bytes, int *blocks_per_sm);
+cudaError_t megakernel_launch(const KernelParams &p, int n_ctas, int smem_bytes, cudaStream_t st);
+cudaError_t copy_launch(void *dst, const void *src, size_t bytes, int n_ctas, cudaStream_t st);
+cudaError_t barrier_launch(uint32_t *ctr, int rounds, unsigned long long *elapsed, uint32_t *status,
+                           int n_ctas, cudaStream_t st);
+}  // namespace tiles
+
+using namespace tiles;
+
+struct tiles_plan_s {
+    tiles_schedule_s sched;
+    int device = -1, sm_count = 0, cc_major = 0, cc_minor = 0;
+    std::vector<void *> allocs;
+    KernelParams base{};
+    unsigned long long *d_keys = nullptr;  // keys then counters: one memset per launch
+    size_t sync_bytes = 0;
+    int32_t *d_prompt_stage = nullptr, *d_tokens_stage = nullptr;
+    float *d_logits_stage = nullptr;
+    size_t logits_stage_elems = 0;
+};
+
+namespace {
+
+template <typename T>
+cudaError_t dalloc(tiles_plan_s *p, T **ptr, size_t bytes) {
+    void *v = nullptr;
+    cudaError_t e = cudaMalloc(&v, bytes ? bytes : 16);
+    if (e != cudaSuccess) return e;
+    p->allocs.push_back(v);
+    *ptr = reinterpret_cast<T *>(v);
+    return cudaSuccess;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// RoPE inverse frequencies theta^(-2j/d) in FP64, with the published llama3
+// rule when enabled: wavelength 2 pi / w below orig/high keeps w, above
+// orig/low divides it by the factor, between the two blends linearly in
+// orig/wavelength.
+void rope_inv_freq(const tiles_model_desc &d, std::vector<double> &w) {
+    const int h = d.head_dim / 2;
+    w.resize(h);
+    for (int j = 0; j < h; ++j) {
+        double f = std::pow(d.rope_theta, -(2.0 * j) / d.head_dim);
+        if (d.rope_scaling == 1) {
+            const double wl = 2.0 * M_PI / f;
+            const double lo_wl = d.rs_orig_max / d.rs_low, hi_wl = d.rs_orig_max / d.rs_high;
+            if (wl > lo_wl) {
+                f = f / d.rs_factor;
+            } else if (wl >= hi_wl) {
+                const double sm = (d.rs_orig_max / wl - d.rs_low) / (d.rs_high - d.rs_low);
+                f = (1.0 - sm) * (f / d.rs_factor) + sm * f;
+            }
+        }
+        w[j] = f;
+    }
+}
+
+tiles_status_t cuda_fail(cudaError_t e) {
+    (void)e;
+    return TILES_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weights *w,
+                                 const tiles_plan_opts *opts, tiles_plan_t *out) {
+    if (!desc || !w || !out || !w->embed || !w->final_norm || !w->layers) return TILES_ERR_INVALID_ARG;
+    *out = nullptr;
+    tiles_plan_opts o = opts ? *opts : default_opts();
+    if (o.timeout_ms < 0) return TILES_ERR_INVALID_ARG;
+    // weights: present, 16-byte aligned
+    if (!aligned16(w->embed) || !aligned16(w->final_norm)) return TILES_ERR_INVALID_ARG;
+    for (int l = 0; l < desc->n_layers; ++l) {
+        const tiles_layer_weights &lw = w->layers[l];
+        const void *req[] = {lw.attn_norm, lw.wq, lw.wk, lw.wv, lw.wo, lw.ffn_norm, lw.w_gate, lw.w_up, lw.w_down};
+        for (const void *q : req)
+            if (!q || !aligned16(q)) return TILES_ERR_INVALID_ARG;
+        if (desc->qk_norm && (!lw.q_norm || !lw.k_norm)) return TILES_ERR_INVALID_ARG;
+    }
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (!prop.cooperativeLaunch) return TILES_ERR_UNSUPPORTED;
+    int smem_limit = (int)prop.sharedMemPerBlockOptin;
+    if (smem_limit > kSmemLimit) smem_limit = kSmemLimit;
+    int n_ctas = o.n_ctas > 0 ? o.n_ctas : prop.multiProcessorCount;
+    if (n_ctas > prop.multiProcessorCount) return TILES_ERR_INVALID_ARG;
+
+    auto *plan = new tiles_plan_s();
+    plan->device = dev;
+    plan->sm_count = prop.multiProcessorCount;
+    plan->cc_major = prop.major;
+    plan->cc_minor = prop.minor;
+    std::string why;
+    tiles_status_t st = build_schedule(*desc, o, n_ctas, smem_limit, &plan->sched, &why);
+    if (st == TILES_OK) st = validate_schedule(plan->sched, &why);
+    if (st != TILES_OK) {
+        delete plan;
+        return st;
+    }
+    const Geom &g = plan->sched.geom;
+
+    // the worker must fit one CTA per SM at this shared-memory size (co-residency)
+    e = megakernel_configure(g.smem_bytes);
+    int occ = 0;
+    if (e == cudaSuccess) e = megakernel_occupancy(g.smem_bytes, &occ);
+    if (e != cudaSuccess || occ < 1) {
+        delete plan;
+        return e != cudaSuccess ? TILES_ERR_CUDA : TILES_ERR_UNSUPPORTED;
+    }
+
+    KernelParams &p = plan->base;
+    std::memset(&p, 0, sizeof(p));
+    p.g = g;
+    p.eps = desc->rms_eps;
+    p.attn_scale = (float)(1.0 / std::sqrt((double)g.d));
+    p.qk_norm = desc->qk_norm;
+    p.final_ctr = plan->sched.final_ctr;
+    p.final_mul = plan->sched.final_mul;
+    p.embed = reinterpret_cast<const uint16_t *>(w->embed);
+    p.final_norm = reinterpret_cast<const uint16_t *>(w->final_norm);
+    p.timeout_ns = (unsigned long long)(o.timeout_ms > 0 ? o.timeout_ms : 2000) * 1000000ull;
+    p.ring_off = kCtlBytes;
+    p.vec_off = kCtlBytes + g.ring_slots * g.slot_bytes;
+    auto fail = [&](cudaError_t ce) {
+        tiles_plan_destroy(plan);
+        return cuda_fail(ce);
+    };
+    tiles_task *d_tasks;
+    int32_t *d_off;
+    LayerPtrs *d_layers;
+    if ((e = dalloc(plan, &d_tasks, plan->sched.tasks.size() * sizeof(tiles_task))) != cudaSuccess) return fail(e);
+    if ((e = dalloc(plan, &d_off, plan->sched.offsets.size() * sizeof(int32_t))) != cudaSuccess) return fail(e);
+    if ((e = dalloc(plan, &d_layers, (size_t)g.L * sizeof(LayerPtrs))) != cudaSuccess) return fail(e);
+    std::vector<LayerPtrs> lp(g.L);
+    for (int l = 0; l < g.L; ++l) {
+        const tiles_layer_weights &lw = w->layers[l];
+        lp[l] = LayerPtrs{(const uint16_t *)lw.attn_norm, (const uint16_t *)lw.wq, (const uint16_t *)lw.wk,
+                          (const uint16_t *)lw.wv,        (const uint16_t *)lw.q_norm, (const uint16_t *)lw.k_norm,
+                          (const uint16_t *)lw.wo,        (const uint16_t *)lw.ffn_norm, (const uint16_t *)lw.w_gate,
+                          (const uint16_t *)lw.w_up,      (const uint16_t *)lw.w_down};
+    }
+    e = cudaMemcpy(d_tasks, plan->sched.tasks.data(), plan->sched.tasks.size() * sizeof(tiles_task),
+                   cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(d_off, plan->sched.offsets.data(), plan->sched.offsets.size() * sizeof(int32_t),
+                       cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(d_layers, lp.data(), (size_t)g.L * sizeof(LayerPtrs), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail(e);
+    p.tasks = d_tasks;
+    p.offsets = d_off;
+    p.layers = d_layers;
+
+    // RoPE cos/sin [max_pos][d/2]: angle pos * w_j in FP64, rounded to FP32
+    {
+        std::vector<double> inv;
+        rope_inv_freq(*desc, inv);
+        const int h = g.d / 2;
+        std::vector<float> c((size_t)g.max_pos * h), s((size_t)g.max_pos * h);
+        for (int pos = 0; pos < g.max_pos; ++pos)
+            for (int j = 0; j < h; ++j) {
+                const double a = (double)pos * inv[j];
+                c[(size_t)pos * h + j] = (float)std::cos(a);
+                s[(size_t)pos * h + j] = (float)std::sin(a);
+            }
+        float *dc, *ds;
+        if ((e = dalloc(plan, &dc, c.size() * 4)) != cudaSuccess) return fail(e);
+        if ((e = dalloc(plan, &ds, s.size() * 4)) != cudaSuccess) return fail(e);
+        if ((e = cudaMemcpy(dc, c.data(), c.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess) return fail(e);
+        if ((e = cudaMemcpy(ds, s.data(), s.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess) return fail(e);
+        p.rope_cos = dc;
+        p.rope_sin = ds;
+    }
+    // scratch
+    if ((e = dalloc(plan, &p.qkv, (size_t)g.qkv_rows * 4)) != cudaSuccess) return fail(e);
+    if ((e = dalloc(plan, &p.partials, (size_t)g.nq * g.kv_splits * (kPartialPad + g.d) * 4)) != cudaSuccess) return fail(e);
+    if ((e = dalloc(plan, &p.o, (size_t)g.qd * 2)) != cudaSuccess) return fail(e);
+    if ((e = dalloc(plan, &p.x, (size_t)g.H * 2)) != cudaSuccess) return fail(e);
+    if ((e = dalloc(plan, &p.a, (size_t)g.F * 2)) != cudaSuccess) return fail(e);
+    plan->sync_bytes = kMaxStepsPerLaunch * 8 + (size_t)plan->sched.n_counters * kCounterStride * 4;
+    uint8_t *sync;
+    if ((e = dalloc(plan, &sync, plan->sync_bytes)) != cudaSuccess) return fail(e);
+    plan->d_keys = reinterpret_cast<unsigned long long *>(sync);
+    p.keys = plan->d_keys;
+    p.counters = reinterpret_cast<uint32_t *>(sync + kMaxStepsPerLaunch * 8);
+    if ((e = dalloc(plan, &p.status, 16)) != cudaSuccess) return fail(e);
+    if ((e = cudaMemset(p.status, 0, 16)) != cudaSuccess) return fail(e);
+    if ((e = dalloc(plan, &plan->d_prompt_stage, (size_t)g.max_pos * 4)) != cudaSuccess) return fail(e);
+    if ((e = dalloc(plan, &plan->d_tokens_stage, (size_t)g.max_pos * 4)) != cudaSuccess) return fail(e);
+    *out = plan;
+    return TILES_OK;
+}
+
+void tiles_plan_destroy(tiles_plan_t plan) {
+    if (!plan) return;
+    for (void *v : plan->allocs) cudaFree(v);
+    delete plan;
+}
+
+tiles_status_t tiles_plan_get_info(tiles_plan_t plan, tiles_plan_info *info) {
+    if (!plan || !info) return TILES_ERR_INVALID_ARG;
+    const tiles_schedule_s &s = plan->sched;
+    const Geom &g = s.geom;
+    std::memset(info, 0, sizeof(*info));
+    info->n_ctas = s.n_ctas;
+    info->threads_per_cta = kThreads;
+    info->smem_bytes = g.smem_bytes;
+    info->slot_bytes = g.slot_bytes;
+    info->ring_slots = g.ring_slots;
+    info->kv_splits = g.kv_splits;
+    info->scheduler = s.scheduler;
+    info->n_tasks = (int32_t)s.tasks.size();
+    info->n_counters = s.n_counters;
+    info->phases_per_step = phases_per_step(g);
+    long long tot = 0, mx = 0, mn = -1;
+    for (int c = 0; c < s.n_ctas; ++c) {
+        long long b = 0;
+        for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i)
+            if (op_is_gemv(s.tasks[i].op)) b += task_bytes(g, s.tasks[i], 0);
+        tot += b;
+        mx = b > mx ? b : mx;
+        mn = (mn < 0 || b < mn) ? b : mn;
+    }
+    info->weight_bytes_per_token = tot;
+    info->max_cta_bytes = mx;
+    info->min_cta_bytes = mn;
+    return TILES_OK;
+}
+
+static tiles_status_t check_device(tiles_plan_t plan) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TILES_ERR_CUDA;
+    if (dev != plan->device) return TILES_ERR_DEVICE_MISMATCH;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return TILES_ERR_CUDA;
+    if (sms != plan->sm_count) return TILES_ERR_DEVICE_MISMATCH;
+    return TILES_OK;
+}
+
+tiles_status_t tiles_decode(tiles_plan_t plan, void *k_cache, void *v_cache, const int32_t *prompt,
+                            int32_t n_prompt, int32_t start_pos, int32_t n_new, void *stream,
+                            int32_t *out_tokens, float *out_logits) {
+    if (!plan || !k_cache || !v_cache || !prompt || n_prompt < 1 || n_new < 0 || start_pos < 0)
+        return TILES_ERR_INVALID_ARG;
+    if (n_new > 0 && !out_tokens) return TILES_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return TILES_ERR_INVALID_ARG;
+    const Geom &g = plan->sched.geom;
+    const long long steps = (long long)n_prompt - 1 + n_new;
+    if (steps == 0) return TILES_OK;
+    if ((long long)start_pos + steps > g.max_pos) return TILES_ERR_CAPACITY;
+    tiles_status_t st = check_device(plan);
+    if (st != TILES_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    KernelParams p = plan->base;
+    p.k_cache = reinterpret_cast<uint16_t *>(k_cache);
+    p.v_cache = reinterpret_cast<uint16_t *>(v_cache);
+    p.prompt = prompt;
+    p.n_prompt = n_prompt;
+    p.out_tokens = out_tokens;
+    p.out_logits = out_logits;
+    for (long long s0 = 0; s0 < steps; s0 += kMaxStepsPerLaunch) {
+        const int n = (int)(steps - s0 < kMaxStepsPerLaunch ? steps - s0 : kMaxStepsPerLaunch);
+        p.step0 = (int)s0;
+        p.pos0 = start_pos + (int)s0;
+        p.n_steps = n;
+        cudaError_t e = cudaMemsetAsync(plan->d_keys, 0, plan->sync_bytes, cs);
+        if (e == cudaSuccess) e = megakernel_launch(p, plan->sched.n_ctas, g.smem_bytes, cs);
+        if (e != cudaSuccess) return TILES_ERR_CUDA;
+    }
+    return TILES_OK;
+}
+
+tiles_status_t tiles_status(tiles_plan_t plan, void *stream) {
+    if (!plan) return TILES_ERR_INVALID_ARG;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return TILES_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, plan->base.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return TILES_ERR_CUDA;
+    if (word) {
+        if (cudaMemset(plan->base.status, 0, 4) != cudaSuccess) return TILES_ERR_CUDA;
+    }
+    if (word & kDevBounds) return TILES_ERR_DEVICE_BOUNDS;
+    if (word & kDevTimeout) return TILES_ERR_TIMEOUT;
+    return TILES_OK;
+}
+
+tiles_status_t tiles_decode_host(tiles_plan_t plan, void *k_cache, void *v_cache,
+                                 const int32_t *prompt_host, int32_t n_prompt, int32_t start_pos,
+                                 int32_t n_new, void *stream, int32_t *out_tokens_host,
+                                 float *out_logits_host) {
+    if (!plan || !prompt_host || n_prompt < 1 || n_new < 0 || start_pos < 0) return TILES_ERR_INVALID_ARG;
+    if (n_new > 0 && !out_tokens_host) return TILES_ERR_INVALID_ARG;
+    const Geom &g = plan->sched.geom;
+    const long long steps = (long long)n_prompt - 1 + n_new;
+    if ((long long)start_pos + steps > g.max_pos) return TILES_ERR_CAPACITY;
+    if (n_prompt > g.max_pos) return TILES_ERR_CAPACITY;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    float *dlog = nullptr;
+    if (out_logits_host && steps > 0) {
+        const size_t need = (size_t)steps * g.V;
+        if (plan->logits_stage_elems < need) {
+            if (plan->d_logits_stage) cudaFree(plan->d_logits_stage);
+            plan->d_logits_stage = nullptr;
+            plan->logits_stage_elems = 0;
+            if (cudaMalloc(&plan->d_logits_stage, need * 4) != cudaSuccess) return TILES_ERR_CUDA;
+            plan->logits_stage_elems = need;
+        }
+        dlog = plan->d_logits_stage;
+    }
+    if (cudaMemcpyAsync(plan->d_prompt_stage, prompt_host, (size_t)n_prompt * 4, cudaMemcpyHostToDevice, cs) !=
+        cudaSuccess)
+        return TILES_ERR_CUDA;
+    tiles_status_t st = tiles_decode(plan, k_cache, v_cache, plan->d_prompt_stage, n_prompt, start_pos, n_new,
+                                     stream, plan->d_tokens_stage, dlog);
+    if (st != TILES_OK) return st;
+    if (n_new > 0 && cudaMemcpyAsync(out_tokens_host, plan->d_tokens_stage, (size_t)n_new * 4,
+                                     cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return TILES_ERR_CUDA;
+    if (dlog && cudaMemcpyAsync(out_logits_host, dlog, (size_t)steps * g.V * 4, cudaMemcpyDeviceToHost, cs) !=
+                    cudaSuccess)
+        return TILES_ERR_CUDA;
+    return tiles_status(plan, stream);
+}
+
+tiles_status_t tiles_copy_bw(void *dst, const void *src, size_t bytes, int32_t n_ctas, void *stream) {
+    if (!dst || !src || bytes % 16 || !aligned16(dst) || !aligned16(src) || n_ctas < 0) return TILES_ERR_INVALID_ARG;
+    if (bytes == 0) return TILES_OK;
+    if (n_ctas == 0) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TILES_ERR_CUDA;
+        n_ctas = 2 * sms;
+    }
+    return copy_launch(dst, src, bytes, n_ctas, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? TILES_OK
+               : TILES_ERR_CUDA;
+}
+
+tiles_status_t tiles_barrier_cost(int32_t n_ctas, int32_t rounds, double *ns_per_barrier) {
+    if (!ns_per_barrier || rounds < 1 || n_ctas < 0) return TILES_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return TILES_ERR_CUDA;
+    if (n_ctas == 0) n_ctas = sms;
+    if (n_ctas > sms) return TILES_ERR_INVALID_ARG;
+    uint32_t *buf = nullptr;
+    if (cudaMalloc(&buf, 64) != cudaSuccess) return TILES_ERR_CUDA;
+    tiles_status_t st = TILES_OK;
+    unsigned long long elapsed = 0;
+    uint32_t status = 0;
+    if (cudaMemset(buf, 0, 64) != cudaSuccess ||
+        barrier_launch(buf, rounds, reinterpret_cast<unsigned long long *>(buf + 8), buf + 4, n_ctas, 0) !=
+            cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&elapsed, buf + 8, 8, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(&status, buf + 4, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+        st = TILES_ERR_CUDA;
+    else if (status)
+        st = TILES_ERR_TIMEOUT;
+    cudaFree(buf);
+    if (st == TILES_OK) *ns_per_barrier = (double)elapsed / rounds;
+    return st;
+}
+
+}  // extern "C"
