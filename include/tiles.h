@@ -157,10 +157,20 @@ tiles_status_t tiles_status(tiles_plan_t plan, void *stream);
 /* Static string naming a status code. Never NULL. */
 const char *tiles_status_string(tiles_status_t status);
 
+/* Diagnostics: makes later tiles_decode calls on this plan record a per-task
+ * timeline of their first `steps` steps into `trace` (device memory, caller
+ * owned, at least n_ctas * steps * max_tasks_per_cta * 8 uint64 words, see
+ * tiles_plan_info.max_tasks_per_cta). Word layout per task record: consumer
+ * wait start, inputs ready, task end, producer first issue, producer last
+ * issue, producer ns stalled on a full ring, op | layer << 8 | chunks << 32.
+ * Times are %globaltimer nanoseconds. trace == NULL or steps == 0 turns it off.
+ * Errors: INVALID_ARG. */
+tiles_status_t tiles_plan_set_trace(tiles_plan_t plan, void *trace, int32_t steps);
+
 /* Facts about a built plan, for reports and tests. */
 typedef struct {
     int32_t n_ctas, threads_per_cta, smem_bytes, slot_bytes, ring_slots, kv_splits;
-    int32_t scheduler, n_tasks, n_counters, phases_per_step;
+    int32_t scheduler, n_tasks, n_counters, phases_per_step, max_tasks_per_cta;
     int64_t weight_bytes_per_token;     /* every weight byte the kernel streams per step */
     int64_t max_cta_bytes, min_cta_bytes; /* per-step streamed weight bytes, busiest/idlest CTA */
 } tiles_plan_info;

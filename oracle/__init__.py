@@ -21,8 +21,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_ALT_LIB_PATH = os.path.join(_HERE, "liboracle_alt.so")
 _lock = threading.Lock()
-_lib = None
+_libs = {}
 
 
 class OrcModel(ctypes.Structure):
@@ -42,24 +43,29 @@ class OrcLayer(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in _SLOTS]
 
 
-def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so (gcc -O2, OpenMP, no FP contraction)."""
-    if not force and os.path.exists(_LIB_PATH) and \
-            os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
-        return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+def _build_one(path, extra, force):
+    if not force and os.path.exists(path) and os.path.getmtime(path) >= os.path.getmtime(_SRC):
+        return path
+    tmp = path + f".tmp{os.getpid()}"
     subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
-                           "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+                           "-fno-fast-math", *extra, "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, path)
+    return path
 
 
-def lib():
-    global _lib
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc -O2, OpenMP, no FP contraction) and
+    the alternative-summation-order build liboracle_alt.so (noise-floor reference)."""
+    _build_one(_ALT_LIB_PATH, ["-DORC_ALT_SUM_ORDER"], force)
+    return _build_one(_LIB_PATH, [], force)
+
+
+def lib(variant: str = "seq"):
+    """The oracle library; variant "alt" is the build with the other GEMV summation order."""
     with _lock:
-        if _lib is None:
+        if variant not in _libs:
             build()
-            L = ctypes.CDLL(_LIB_PATH)
+            L = ctypes.CDLL(_ALT_LIB_PATH if variant == "alt" else _LIB_PATH)
             vp, i32, f32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int64
             L.orc_bf16_from_f32.argtypes = [f32]
             L.orc_bf16_from_f32.restype = ctypes.c_uint16
@@ -76,8 +82,8 @@ def lib():
             L.orc_decode.argtypes = [ctypes.POINTER(OrcModel), ctypes.POINTER(OrcLayer), vp, vp,
                                      vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32]
             L.orc_decode.restype = i32
-            _lib = L
-    return _lib
+            _libs[variant] = L
+    return _libs[variant]
 
 
 def _ptr(a):
@@ -179,9 +185,11 @@ class DecodeResult:
 
 
 def decode(cfg, weights, k_cache, v_cache, prompt, start_pos: int, n_new: int,
-           force_tokens=None, want_logits: bool = True, n_threads: int = 0) -> DecodeResult:
+           force_tokens=None, want_logits: bool = True, n_threads: int = 0,
+           variant: str = "seq") -> DecodeResult:
     """Run the oracle. ``weights`` is a ``synthetic.ModelWeights``; ``k_cache`` and
-    ``v_cache`` are [L][n_kv][max_pos][d] uint16 arrays updated in place."""
+    ``v_cache`` are [L][n_kv][max_pos][d] uint16 arrays updated in place.
+    ``variant="alt"`` runs the build with the other GEMV summation order."""
     prompt = _c(prompt, np.int32)
     n_prompt = prompt.size
     steps = n_prompt - 1 + n_new
@@ -205,7 +213,7 @@ def decode(cfg, weights, k_cache, v_cache, prompt, start_pos: int, n_new: int,
     gaps = np.empty(max(steps, 1), np.float32)
     force = None if force_tokens is None else _c(force_tokens, np.int32)
     m = model_struct(cfg)
-    rc = lib().orc_decode(ctypes.byref(m), layers, embed.ctypes.data, fnorm.ctypes.data,
+    rc = lib(variant).orc_decode(ctypes.byref(m), layers, embed.ctypes.data, fnorm.ctypes.data,
                           k_cache.ctypes.data, v_cache.ctypes.data, prompt.ctypes.data, n_prompt,
                           start_pos, n_new, _ptr(force), out_tokens.ctypes.data, _ptr(logits),
                           gaps.ctypes.data, n_threads)

@@ -155,14 +155,26 @@ void orc_rope_apply(float *v, int d, const float *c, const float *s) {
 
 /* ------------------------------------------------------------------ GEMV */
 
-/* y[r] = sum_j W[r][j] x[j], W bf16 row-major [rows][cols], sum left to right. */
+/* y[r] = sum_j W[r][j] x[j], W bf16 row-major [rows][cols], sum left to right.
+ *
+ * Built with -DORC_ALT_SUM_ORDER, the same sum is taken in another order
+ * (eight interleaved partial sums, then added pairwise). That build is not a
+ * second definition: it measures how far an equally valid FP32 summation order
+ * moves the whole decoder (the floating-point noise floor the GPU path is held
+ * to on deep models), nothing else. */
 void orc_gemv(const uint16_t *W, int rows, int cols, const float *x, float *y) {
 #pragma omp parallel for schedule(static)
     for (int r = 0; r < rows; ++r) {
         const uint16_t *w = W + (int64_t)r * cols;
+#ifdef ORC_ALT_SUM_ORDER
+        float pa[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int j = 0; j < cols; ++j) pa[j & 7] += orc_f32_from_bf16(w[j]) * x[j];
+        y[r] = ((pa[0] + pa[1]) + (pa[2] + pa[3])) + ((pa[4] + pa[5]) + (pa[6] + pa[7]));
+#else
         float acc = 0.0f;
         for (int j = 0; j < cols; ++j) acc += orc_f32_from_bf16(w[j]) * x[j];
         y[r] = acc;
+#endif
     }
 }
 

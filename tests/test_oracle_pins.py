@@ -353,3 +353,23 @@ def test_decoder_rejects_capacity_overflow(tiny_cfg):
     w, k, v, p = _tiny_inputs(tiny_cfg)
     with pytest.raises(ValueError):
         O.decode(tiny_cfg, w, k, v, p, tiny_cfg.max_pos - 2, 8)
+
+
+def test_alternative_sum_order_build_is_the_same_function():
+    """The noise-floor build differs only in rounding: exact on small integers,
+    close on a small model (its rounding flips stay far inside the tolerance)."""
+    rng = np.random.default_rng(31)
+    Wi = rng.integers(-4, 5, size=(9, 1000))
+    xi = rng.integers(-4, 5, size=1000)
+    W = O.bf16_from_f32(Wi.astype(np.float32)).reshape(9, 1000)
+    import ctypes
+    y = np.empty(9, np.float32)
+    xf = xi.astype(np.float32)
+    O.lib("alt").orc_gemv(W.ctypes.data, 9, 1000, xf.ctypes.data, y.ctypes.data)
+    assert np.array_equal(y.astype(np.int64), Wi @ xi)
+    cfg = S.CONFIGS["tiny"]
+    w, (k, v), p = S.model_weights(cfg), S.kv_prefill(cfg), S.prompt(cfg)
+    a = O.decode(cfg, w, k.copy(), v.copy(), p, 0, 4)
+    b = O.decode(cfg, w, k.copy(), v.copy(), p, 0, 4, variant="alt")
+    assert np.abs(a.logits - b.logits).max() < 1e-2      # well inside 3e-2 at two layers
+    del ctypes

@@ -71,7 +71,8 @@ class PlanOpts(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("n_ctas", "threads_per_cta", "smem_bytes", "slot_bytes", "ring_slots",
-                 "kv_splits", "scheduler", "n_tasks", "n_counters", "phases_per_step")] + \
+                 "kv_splits", "scheduler", "n_tasks", "n_counters", "phases_per_step",
+                 "max_tasks_per_cta")] + \
                [(n, ctypes.c_int64) for n in
                 ("weight_bytes_per_token", "max_cta_bytes", "min_cta_bytes")]
 
@@ -92,7 +93,7 @@ assert ctypes.sizeof(Task) == 24
 EXPORTS = ("tiles_plan_create", "tiles_plan_destroy", "tiles_decode", "tiles_decode_host",
            "tiles_status", "tiles_status_string", "tiles_plan_get_info", "tiles_schedule_build",
            "tiles_schedule_validate", "tiles_schedule_tasks", "tiles_schedule_cta_bytes",
-           "tiles_schedule_destroy", "tiles_copy_bw", "tiles_barrier_cost")
+           "tiles_schedule_destroy", "tiles_copy_bw", "tiles_barrier_cost", "tiles_plan_set_trace")
 
 _lib_handle = None
 
@@ -119,6 +120,8 @@ def _lib():
         L.tiles_status.restype = st
         L.tiles_status_string.argtypes = [st]
         L.tiles_status_string.restype = ctypes.c_char_p
+        L.tiles_plan_set_trace.argtypes = [vp, vp, i32]
+        L.tiles_plan_set_trace.restype = st
         L.tiles_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
         L.tiles_plan_get_info.restype = st
         L.tiles_schedule_build.argtypes = [ctypes.POINTER(ModelDesc), ctypes.POINTER(PlanOpts), i32,
@@ -249,6 +252,11 @@ class Plan:
         inf = PlanInfo()
         _check(_lib().tiles_plan_get_info(self._h, ctypes.byref(inf)), "tiles_plan_get_info")
         return inf.as_dict()
+
+    def set_trace(self, buf, steps: int) -> None:
+        """Record a per-task timeline of the first `steps` steps of later decodes into
+        `buf` (int64 CUDA tensor of n_ctas * steps * max_tasks_per_cta * 8 words)."""
+        _check(_lib().tiles_plan_set_trace(self._h, _ptr(buf), steps), "tiles_plan_set_trace")
 
     def decode(self, k_cache, v_cache, prompt, start_pos: int, n_new: int, out_tokens,
                out_logits=None, stream=None) -> None:

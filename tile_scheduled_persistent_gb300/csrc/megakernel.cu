@@ -208,7 +208,7 @@ struct Ctl {
     int unused;
     int token;
     int step_ready;  // consumers passed the first wait of this step (KV of earlier steps visible)
-    int pad;
+    int merge;       // this CTA holds the last split of a KV head and merges its partials
     float red[kConsumerWarps];
     unsigned long long warp_key[kConsumerWarps];
 };
@@ -231,6 +231,12 @@ __device__ __forceinline__ Smem smem_layout(uint8_t *base, const KernelParams &p
 }
 
 __device__ __forceinline__ bool failed(const KernelParams &p) { return ld_volatile(p.status) != 0; }
+
+__device__ __forceinline__ unsigned long long *trace_rec(const KernelParams &p, int cta, int step,
+                                                         int task) {
+    if (!p.trace || step >= p.trace_steps) return nullptr;
+    return p.trace + (((size_t)cta * p.trace_steps + step) * p.trace_tasks + task) * kTraceWords;
+}
 
 // Bounded spin until counter >= target. false when the run is aborting.
 __device__ bool wait_counter(const KernelParams &p, const uint32_t *ctr, uint32_t target) {
@@ -271,6 +277,8 @@ struct Producer {
     uint32_t j = 0;  // chunks issued
     bool ok = true;
     unsigned long long pol_weights;  // L2 evict-first: weights are streamed once per step
+    unsigned long long stall = 0;    // ns spent waiting for a free slot (traced runs)
+    bool tracing = false;
 
     __device__ Producer(const KernelParams &p_, Smem &s_) : p(p_), s(s_) {
         asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_weights));
@@ -280,9 +288,13 @@ struct Producer {
     __device__ uint8_t *acquire(uint64_t **bar) {
         const uint32_t ns = (uint32_t)p.g.ring_slots;
         uint32_t slot = j % ns;
-        if (j >= ns && !wait_mbar(p, &s.empty[slot], ((j / ns) - 1u) & 1u)) {
-            ok = false;
-            return nullptr;
+        if (j >= ns) {
+            unsigned long long t0 = tracing ? global_timer() : 0;
+            if (!wait_mbar(p, &s.empty[slot], ((j / ns) - 1u) & 1u)) {
+                ok = false;
+                return nullptr;
+            }
+            if (tracing) stall += global_timer() - t0;
         }
         *bar = &s.full[slot];
         return s.ring + (size_t)slot * p.g.slot_bytes;
@@ -381,6 +393,10 @@ struct Producer {
             const int P = p.pos0 + st;
             for (int ti = t0; ti < t1 && ok; ++ti) {
                 const tiles_task t = p.tasks[ti];
+                unsigned long long *tr = trace_rec(p, cta, st, ti - t0);
+                tracing = tr != nullptr;
+                stall = 0;
+                if (tr) tr[kTrProdFirst] = global_timer();
                 if (op_is_gemv(t.op)) {
                     const uint32_t rpc = (uint32_t)op_rows_per_chunk(g, t.op);
                     for (uint32_t r = t.begin; r < t.end && ok; r += rpc) {
@@ -401,6 +417,12 @@ struct Producer {
                         }
                     }
                 }
+                if (tr) {
+                    tr[kTrProdLast] = global_timer();
+                    tr[kTrProdStall] = stall;
+                    tr[kTrOpInfo] = (unsigned long long)t.op | ((unsigned long long)t.layer << 8) |
+                                    ((unsigned long long)task_chunks(g, t, P) << 32);
+                }
             }
         }
         // drain: wait for every copy still in flight so no bulk copy outlives the CTA
@@ -414,6 +436,57 @@ struct Producer {
         }
     }
 };
+
+// ------------------------------------------------------------------ GEMV rows
+// NR rows (x MATS matrices) of one chunk against the input vector in shared
+// memory: lane c reads 16-byte columns c, c+32, ... of every row, FP32 FMA,
+// then an xor-shuffle reduction; lane r returns row r's sums. The row count is
+// a compile-time constant so no predicated-off rows are issued.
+template <int MATS, int NR>
+__device__ __forceinline__ void gemv_rows(const uint8_t *slot, const uint4 *vec, int nu4,
+                                          size_t row_bytes, int rpc, float (&res)[MATS]) {
+    const int lane = threadIdx.x & 31;
+    float acc[NR][MATS];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int m = 0; m < MATS; ++m) acc[r][m] = 0.f;
+    for (int c = lane; c < nu4; c += 32) {
+        float xf[8];
+        unpack8(vec[c], xf);
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int m = 0; m < MATS; ++m) {
+                const uint4 w = reinterpret_cast<const uint4 *>(slot + ((size_t)m * rpc + r) * row_bytes)[c];
+                acc[r][m] = dot8(w, xf, acc[r][m]);
+            }
+    }
+#pragma unroll
+    for (int m = 0; m < MATS; ++m) res[m] = 0.f;
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int m = 0; m < MATS; ++m) {
+            const float v = warp_sum(acc[r][m]);
+            if (lane == r) res[m] = v;
+        }
+}
+
+template <int MATS>
+__device__ __forceinline__ void gemv_rows_n(uint32_t nr, const uint8_t *slot, const uint4 *vec, int nu4,
+                                            size_t row_bytes, int rpc, float (&res)[MATS]) {
+    switch (nr) {
+        case 1: gemv_rows<MATS, 1>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 2: gemv_rows<MATS, 2>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 3: gemv_rows<MATS, 3>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 4: gemv_rows<MATS, 4>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 5: gemv_rows<MATS, 5>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 6: gemv_rows<MATS, 6>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 7: gemv_rows<MATS, 7>(slot, vec, nu4, row_bytes, rpc, res); break;
+        default: gemv_rows<MATS, 8>(slot, vec, nu4, row_bytes, rpc, res); break;
+    }
+}
 
 // ------------------------------------------------------------------ consumers
 struct Consumer {
@@ -525,40 +598,9 @@ struct Consumer {
             const uint32_t nr = t.end - r0 < rpc ? t.end - r0 : rpc;
             const uint8_t *slot = wait_chunk(jj);
             if (!slot) break;
-            float acc[kMaxRowsPerChunk][MATS];
-#pragma unroll
-            for (int r = 0; r < kMaxRowsPerChunk; ++r)
-#pragma unroll
-                for (int m = 0; m < MATS; ++m) acc[r][m] = 0.f;
-            for (int c = lane; c < nu4; c += 32) {
-                float xf[8];
-                unpack8(vec[c], xf);
-#pragma unroll
-                for (int r = 0; r < kMaxRowsPerChunk; ++r) {
-                    if ((uint32_t)r < nr) {
-#pragma unroll
-                        for (int m = 0; m < MATS; ++m) {
-                            const uint4 w = reinterpret_cast<const uint4 *>(
-                                slot + ((size_t)m * rpc + r) * (size_t)in * 2)[c];
-                            acc[r][m] = dot8(w, xf, acc[r][m]);
-                        }
-                    }
-                }
-            }
-            release_chunk(jj);
             float mine[MATS];
-#pragma unroll
-            for (int m = 0; m < MATS; ++m) mine[m] = 0.f;
-#pragma unroll
-            for (int r = 0; r < kMaxRowsPerChunk; ++r) {
-                if ((uint32_t)r < nr) {
-#pragma unroll
-                    for (int m = 0; m < MATS; ++m) {
-                        float v = warp_sum(acc[r][m]);
-                        if (lane == r) mine[m] = v;
-                    }
-                }
-            }
+            gemv_rows_n<MATS>(nr, slot, vec, nu4, (size_t)in * 2, (int)rpc, mine);
+            release_chunk(jj);
             if ((uint32_t)lane < nr) {
                 const uint32_t row = r0 + lane;
                 switch (op) {
@@ -762,6 +804,86 @@ struct Consumer {
         }
     }
 
+    // Cooperative form: this warp handles one q head (hi) and the 32-position
+    // sub-blocks sb_first, sb_first + sb_step, ... of a chunk all warps share.
+    template <int D>
+    __device__ void attn_chunk_one(const uint8_t *slot, int npos, const AttnSmem &a, int hi,
+                                   int sb_first, int sb_step, float &m, float &l,
+                                   float (&o)[D / 32]) {
+        constexpr int NC = D / 8;
+        constexpr int DPL = D / 32;
+        const Geom &g = p.g;
+        const uint8_t *Kb = slot;
+        const uint8_t *Vb = slot + (size_t)g.kv_block * D * 2;
+        const float *q = a.q + hi * D;
+        float *prob = a.prob + (size_t)warp * 32 * g.G;
+        for (int t0 = sb_first * 32; t0 < npos; t0 += sb_step * 32) {
+            const int t = t0 + lane;
+            const bool valid = t < npos;
+            float sc = 0.f;
+            if (valid) {
+                const uint4 *krow = reinterpret_cast<const uint4 *>(Kb + (size_t)t * D * 2);
+#pragma unroll
+                for (int jj = 0; jj < NC; ++jj) {
+                    const int col = (jj + lane) & (NC - 1);
+                    float kf[8];
+                    unpack8(krow[col], kf);
+                    const float4 qa = reinterpret_cast<const float4 *>(q + col * 8)[0];
+                    const float4 qb = reinterpret_cast<const float4 *>(q + col * 8)[1];
+                    sc = fmaf(kf[0], qa.x, sc); sc = fmaf(kf[1], qa.y, sc);
+                    sc = fmaf(kf[2], qa.z, sc); sc = fmaf(kf[3], qa.w, sc);
+                    sc = fmaf(kf[4], qb.x, sc); sc = fmaf(kf[5], qb.y, sc);
+                    sc = fmaf(kf[6], qb.z, sc); sc = fmaf(kf[7], qb.w, sc);
+                }
+            }
+            const float si = valid ? sc * p.attn_scale : -INFINITY;
+            const float bm = warp_max(si);
+            const float mn = fmaxf(m, bm);
+            const float corr = expf(m - mn);
+            const float pi = valid ? expf(si - mn) : 0.f;
+            const float ps = warp_sum(pi);
+            l = fmaf(l, corr, ps);
+            m = mn;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[e] *= corr;
+            prob[lane] = pi;
+            __syncwarp();
+            const int nv = npos - t0 < 32 ? npos - t0 : 32;
+            for (int tt = 0; tt < nv; ++tt) {
+                const float pv = prob[tt];
+                const uint8_t *vrow = Vb + (size_t)(t0 + tt) * D * 2;
+                if (DPL == 2) {
+                    const uint32_t w = reinterpret_cast<const uint32_t *>(vrow)[lane];
+                    o[0] = fmaf(pv, bf_lo(w), o[0]);
+                    o[DPL > 1 ? 1 : 0] = fmaf(pv, bf_hi(w), o[DPL > 1 ? 1 : 0]);
+                } else {
+                    const uint2 w = reinterpret_cast<const uint2 *>(vrow)[lane];
+                    o[0] = fmaf(pv, bf_lo(w.x), o[0]);
+                    o[1] = fmaf(pv, bf_hi(w.x), o[1]);
+                    o[DPL > 2 ? 2 : 0] = fmaf(pv, bf_lo(w.y), o[DPL > 2 ? 2 : 0]);
+                    o[DPL > 3 ? 3 : 1] = fmaf(pv, bf_hi(w.y), o[DPL > 3 ? 3 : 1]);
+                }
+            }
+            __syncwarp();
+        }
+    }
+
+    // Put the freshly computed K/V of position P into the chunk's slot (the
+    // producer loaded only positions < P), then order these generic writes
+    // before the async-proxy copy that will later refill the slot.
+    template <int D>
+    __device__ void place_new_kv(uint8_t *slot, int q0, const AttnSmem &a) {
+        const Geom &g = p.g;
+        uint16_t *kd = reinterpret_cast<uint16_t *>(slot + (size_t)(P - q0) * D * 2);
+        uint16_t *vd = reinterpret_cast<uint16_t *>(slot + (size_t)g.kv_block * D * 2 + (size_t)(P - q0) * D * 2);
+        for (int e = lane; e < D; e += 32) {
+            kd[e] = a.knew[e];
+            vd[e] = a.vnew[e];
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
     template <int D, int G>
     __device__ void attn_task(const tiles_task &t) {
         const Geom &g = p.g;
@@ -797,28 +919,45 @@ struct Consumer {
                 for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
             }
             const uint32_t nch = (uint32_t)(b1 - b0);
-            for (uint32_t k = 0; k < nch; ++k) {
-                const uint32_t jj = j + k;
-                if (!mine(jj)) continue;
-                uint8_t *slot = wait_chunk(jj);
-                if (!slot) break;
-                const int q0 = (b0 + (int)k) * g.kv_block;
-                int q1 = q0 + g.kv_block;
-                if (q1 > P + 1) q1 = P + 1;
-                if (q0 <= P && P < q1) {
-                    // position P was not loaded; place the fresh K/V into the slot
-                    uint16_t *kd = reinterpret_cast<uint16_t *>(slot + (size_t)(P - q0) * D * 2);
-                    uint16_t *vd = reinterpret_cast<uint16_t *>(slot + (size_t)g.kv_block * D * 2 +
-                                                                (size_t)(P - q0) * D * 2);
-                    for (int e = lane; e < D; e += 32) {
-                        kd[e] = a.knew[e];
-                        vd[e] = a.vnew[e];
-                    }
-                    __syncwarp();
+            if (nch < (uint32_t)kConsumerWarps) {
+                // few chunks: every warp works on every chunk (one q head, some sub-blocks)
+                const int hi = warp % G, sb0 = warp / G, sbs = kConsumerWarps / G;
+                float m1 = -INFINITY, l1 = 0.f, o1[DPL];
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o1[e] = 0.f;
+                for (uint32_t k = 0; k < nch; ++k) {
+                    const uint32_t jj = j + k;
+                    uint8_t *slot = wait_chunk(jj);
+                    const int q0 = (b0 + (int)k) * g.kv_block;
+                    int q1 = q0 + g.kv_block;
+                    if (q1 > P + 1) q1 = P + 1;
+                    if (slot && warp == 0 && q0 <= P && P < q1) place_new_kv<D>(slot, q0, a);
+                    if (consumer_sync_or(bad)) break;
+                    attn_chunk_one<D>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1);
+                    consumer_sync();
+                    if (tid == 0) mbar_arrive(&s.empty[jj % (uint32_t)g.ring_slots]);
                 }
-                attn_chunk<D, G>(slot, q1 - q0, a, m, l, o);
-                fence_proxy_async_smem();  // generic writes to the slot before the TMA reuses it
-                release_chunk(jj);
+#pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    m[i] = i == hi ? m1 : -INFINITY;
+                    l[i] = i == hi ? l1 : 0.f;
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) o[i][e] = i == hi ? o1[e] : 0.f;
+                }
+            } else {
+                // many chunks: each chunk goes to its slot's owner warp, all q heads
+                for (uint32_t k = 0; k < nch; ++k) {
+                    const uint32_t jj = j + k;
+                    if (!mine(jj)) continue;
+                    uint8_t *slot = wait_chunk(jj);
+                    if (!slot) break;
+                    const int q0 = (b0 + (int)k) * g.kv_block;
+                    int q1 = q0 + g.kv_block;
+                    if (q1 > P + 1) q1 = P + 1;
+                    if (q0 <= P && P < q1) place_new_kv<D>(slot, q0, a);
+                    attn_chunk<D, G>(slot, q1 - q0, a, m, l, o);
+                    release_chunk(jj);
+                }
             }
             j += nch;
             // per-warp states -> shared memory -> one partial for (q heads, split c)
@@ -856,29 +995,67 @@ struct Consumer {
             }
             // wstate is reused by the next item; leave together on any failure
             if (consumer_sync_or(bad)) return;
+            // arrival of this split; the last of the S splits of head h merges them
+            // (release: fence then atomic; acquire: atomic then fence)
+            if (tid == 0) {
+                __threadfence();
+                const uint32_t old =
+                    atomicAdd(p.attn_arrive + (size_t)(cur_layer * g.nkv + h) * kCounterStride, 1u);
+                const bool last = old + 1u == (uint32_t)g.kv_splits * (uint32_t)(step + 1);
+                if (last) __threadfence();
+                s.ctl->merge = last ? 1 : 0;
+            }
+            consumer_sync();
+            if (s.ctl->merge) {
+                merge_heads(h * G, (h + 1) * G);
+                consumer_sync();
+                if (tid == 0 && p.attn_head_signals) {
+                    __threadfence();
+                    red_release_add(p.counters + (size_t)t.signal_ctr * kCounterStride, 1u);
+                }
+            }
         }
     }
 
-    // merge the split partials of q heads [begin, end): one thread per element
-    __device__ void combine_task(const tiles_task &t) {
+    // Merge the split partials of q heads [h0, h1), in split order:
+    //   M = max_c m_c, w_c = e^(m_c - M), out = sum_c w_c o_c / sum_c w_c l_c.
+    // Three stages so the L2 reads go out in parallel: split maxima and sums to
+    // shared memory, one thread per head for the weights, then every output
+    // element with its S independent loads.
+    __device__ void merge_heads(int h0, int h1) {
         const Geom &g = p.g;
-        const int D = g.d, S = g.kv_splits;
-        const int n = (int)(t.end - t.begin) * D;
-        for (int idx = tid; idx < n; idx += kConsumerWarps * 32) {
-            const int hq = (int)t.begin + idx / D, dd = idx % D;
-            const float *base = p.partials + (size_t)hq * S * (kPartialPad + D);
+        const int D = g.d, S = g.kv_splits, nh = h1 - h0;
+        const AttnSmem a = attn_smem();
+        float *ms = a.wstate;              // [nh][S] split maxima, then weights
+        float *ls = ms + (size_t)nh * S;   // [nh][S] split sums
+        float *Ls = ls + (size_t)nh * S;   // [nh] merged sums
+        const float *base = p.partials + (size_t)h0 * S * (kPartialPad + D);
+        for (int idx = tid; idx < nh * S; idx += kConsumerWarps * 32) {
+            ms[idx] = __ldcg(&base[(size_t)idx * (kPartialPad + D)]);
+            ls[idx] = __ldcg(&base[(size_t)idx * (kPartialPad + D) + 1]);
+        }
+        consumer_sync();
+        if (tid < nh) {
             float M = -INFINITY;
-            for (int c = 0; c < S; ++c) M = fmaxf(M, __ldcg(&base[(size_t)c * (kPartialPad + D)]));
-            float L = 0.f, O = 0.f;
+            for (int c = 0; c < S; ++c) M = fmaxf(M, ms[tid * S + c]);
+            float L = 0.f;
             for (int c = 0; c < S; ++c) {
-                const float *pc = base + (size_t)c * (kPartialPad + D);
-                const float mc = __ldcg(&pc[0]);
-                if (mc == -INFINITY) continue;
-                const float w = expf(mc - M);
-                L = fmaf(w, __ldcg(&pc[1]), L);
-                O = fmaf(w, __ldcg(&pc[kPartialPad + dd]), O);
+                const float mc = ms[tid * S + c];
+                const float w = mc == -INFINITY ? 0.f : expf(mc - M);
+                ms[tid * S + c] = w;
+                L = fmaf(w, ls[tid * S + c], L);
             }
-            __stcg(&p.o[(size_t)hq * D + dd], f2bf(__fdiv_rn(O, L)));
+            Ls[tid] = L;
+        }
+        consumer_sync();
+        for (int idx = tid; idx < nh * D; idx += kConsumerWarps * 32) {
+            const int i = idx / D, dd = idx % D;
+            const float *pc = base + (size_t)i * S * (kPartialPad + D) + kPartialPad + dd;
+            const float *wi = ms + (size_t)i * S;
+            float O = 0.f;
+#pragma unroll 4
+            for (int c = 0; c < S; ++c) O = fmaf(wi[c], __ldcg(&pc[(size_t)c * (kPartialPad + D)]), O);
+            __stcg(&p.o[(size_t)(h0 + i) * D + dd], f2bf(__fdiv_rn(O, Ls[i])));
         }
     }
 
@@ -906,6 +1083,8 @@ struct Consumer {
                 const tiles_task t = p.tasks[ti];
                 cur_layer = t.layer;
                 // ---- wait for the inputs
+                unsigned long long *tr = tid == 0 ? trace_rec(p, cta, step, ti - t0) : nullptr;
+                if (tr) tr[kTrWaitStart] = global_timer();
                 if (tid == 0) {
                     const uint32_t target = t.wait_mul * (uint32_t)step + t.wait_add;
                     if (t.wait_ctr != TILES_NO_COUNTER &&
@@ -923,6 +1102,7 @@ struct Consumer {
                     }
                 }
                 if (consumer_sync_or(bad)) return;
+                if (tr) tr[kTrWaitEnd] = global_timer();
                 // ---- work
                 switch (t.op) {
                     case TILES_OP_QKV:
@@ -933,9 +1113,6 @@ struct Consumer {
                         break;
                     case TILES_OP_ATTN:
                         attn_dispatch(t);
-                        break;
-                    case TILES_OP_COMBINE:
-                        combine_task(t);
                         break;
                     case TILES_OP_OPROJ:
                         copy_to_vec(p.o, g.qd);
@@ -962,7 +1139,9 @@ struct Consumer {
                 }
                 // ---- publish
                 if (consumer_sync_or(bad)) return;
-                if (tid == 0 && t.signal_ctr != TILES_NO_COUNTER) {
+                if (tr) tr[kTrTaskEnd] = global_timer();
+                if (tid == 0 && t.signal_ctr != TILES_NO_COUNTER &&
+                    !(t.op == TILES_OP_ATTN && p.attn_head_signals)) {
                     __threadfence();
                     red_release_add(p.counters + (size_t)t.signal_ctr * kCounterStride, 1u);
                 }
@@ -994,6 +1173,7 @@ __global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_con
         s.ctl->unused = 0;
         s.ctl->token = 0;
         s.ctl->step_ready = 0;
+        s.ctl->merge = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();

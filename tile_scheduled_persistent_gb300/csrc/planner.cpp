@@ -107,7 +107,12 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     if (splits < 1 || splits > 4096) return fail(TILES_ERR_INVALID_ARG, "kv_splits");
     G_.kv_splits = splits;
 
-    int vec = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, attn_vec_bytes(G, G_.d)});
+    // the split merge keeps 2 * G * S + G floats in the per-warp state area
+    int merge_need = (2 * G * splits + G) * 4;
+    int attn_need = attn_vec_bytes(G, G_.d);
+    int wstate_off = G * G_.d * 4 + 2 * G_.d * 2 + kConsumerWarps * 32 * G * 4;
+    if (wstate_off + merge_need > attn_need) attn_need = wstate_off + merge_need;
+    int vec = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, attn_need});
     G_.vec_bytes = round_up(vec, 128);
     int avail = smem_limit - kCtlBytes - G_.vec_bytes;
     int slots = o.ring_slots > 0 ? o.ring_slots : std::min(kMaxSlots, avail / slot);
@@ -210,19 +215,24 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
                     b[it] = task_bytes(g, t, g.max_pos - 1);
                 }
                 phase_tasks[phi] = assign_items(n, b, N, cum);
-            } else {  // combine: cheap; spread one head per CTA
-                int n = op_extent(g, op);
-                std::vector<long long> b(n, 1);
-                phase_tasks[phi] = assign_items(n, b, N, cum);
             }
+            // the combine phase stays empty: the last split tile of each KV head
+            // merges the partials inside the attention phase
         }
     }
 
     // counters and waits
     std::vector<std::vector<tiles_task>> per_cta(N);
+    std::vector<int> ord(PPS, 0);  // index among non-empty phases
+    int n_nonempty = 0;
+    for (int phi = 0; phi < PPS; ++phi) {
+        ord[phi] = n_nonempty;
+        if (!phase_tasks[phi].empty()) ++n_nonempty;
+    }
     if (o.scheduler == TILES_SCHED_WAVES) {
         s->n_counters = 1;
         for (int phi = 0; phi < PPS; ++phi) {
+            if (phase_tasks[phi].empty()) continue;
             std::vector<bool> has(N, false);
             std::vector<int> last(N, -1);
             for (size_t k = 0; k < phase_tasks[phi].size(); ++k) last[phase_tasks[phi][k].cta] = (int)k;
@@ -237,8 +247,8 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
                 t.wait_ctr = 0;
                 // one arrival per CTA and phase, after its last task of the phase
                 t.signal_ctr = last[a.cta] == (int)k ? 0 : TILES_NO_COUNTER;
-                t.wait_mul = (uint32_t)(N * PPS);
-                t.wait_add = (uint32_t)(N * phi);
+                t.wait_mul = (uint32_t)(N * n_nonempty);
+                t.wait_add = (uint32_t)(N * ord[phi]);
                 has[a.cta] = true;
                 per_cta[a.cta].push_back(t);
             }
@@ -250,13 +260,13 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
                 t.layer = (uint16_t)phase_layer[phi];
                 t.wait_ctr = 0;
                 t.signal_ctr = 0;
-                t.wait_mul = (uint32_t)(N * PPS);
-                t.wait_add = (uint32_t)(N * phi);
+                t.wait_mul = (uint32_t)(N * n_nonempty);
+                t.wait_add = (uint32_t)(N * ord[phi]);
                 per_cta[c].push_back(t);
             }
         }
         s->final_ctr = 0;
-        s->final_mul = (uint32_t)(N * PPS);
+        s->final_mul = (uint32_t)(N * n_nonempty);
     } else {
         s->n_counters = PPS;
         // previous non-empty phase, cyclically (phase 0 depends on the last of the step before)
@@ -269,9 +279,15 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
             prev[phi] = p;
             if (!phase_tasks[phi].empty()) p = phi;
         }
+        // signals per step: one per task, except the attention phase, which the
+        // merging tile of each KV head signals once (n_kv per step)
+        auto per_step = [&](int phi) -> uint32_t {
+            if (phi < 0) return 0;
+            return phase_op[phi] == TILES_OP_ATTN ? (uint32_t)g.nkv : (uint32_t)phase_tasks[phi].size();
+        };
         for (int phi = 0; phi < PPS; ++phi) {
             int pp = prev[phi];
-            uint32_t npp = pp >= 0 ? (uint32_t)phase_tasks[pp].size() : 0;
+            uint32_t npp = per_step(pp);
             for (auto &a : phase_tasks[phi]) {
                 tiles_task t{};
                 t.op = (uint8_t)phase_op[phi];
@@ -287,7 +303,7 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
             }
         }
         s->final_ctr = last_nonempty;
-        s->final_mul = (uint32_t)phase_tasks[last_nonempty].size();
+        s->final_mul = per_step(last_nonempty);
     }
     s->tasks.clear();
     s->offsets.assign(N + 1, 0);
@@ -329,6 +345,7 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
     std::vector<std::vector<std::pair<uint32_t, uint32_t>>> cover(PPS);
     std::vector<int> phase_op(PPS, 0);
     std::vector<std::vector<int>> sig_by_phase(PPS, std::vector<int>(s.n_counters, 0));
+    std::vector<int> attn_sig(PPS, -1);
     for (int c = 0; c < N; ++c) {
         int last_phi = -1;
         for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i) {
@@ -350,7 +367,14 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
             }
             if (t.signal_ctr != TILES_NO_COUNTER) {
                 if (t.signal_ctr >= s.n_counters) return fail("signal counter out of range");
-                sig_by_phase[phi][t.signal_ctr] += 1;
+                if (t.op == TILES_OP_ATTN && s.scheduler == TILES_SCHED_COUNTERS) {
+                    // counted once per phase below: n_kv merges per step
+                    int &seen = attn_sig[phi];
+                    if (seen == -1) seen = t.signal_ctr;
+                    else if (seen != (int)t.signal_ctr) return fail("attention tiles signal different counters");
+                } else {
+                    sig_by_phase[phi][t.signal_ctr] += 1;
+                }
             }
             if (t.wait_ctr != TILES_NO_COUNTER && t.wait_ctr >= s.n_counters)
                 return fail("wait counter out of range");
@@ -380,6 +404,8 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
             return TILES_ERR_PLAN_INVALID;
         }
     }
+    for (int phi = 0; phi < PPS; ++phi)
+        if (attn_sig[phi] >= 0) sig_by_phase[phi][attn_sig[phi]] += g.nkv;
     // signals per step on each counter; per CTA, the counter its last task of each phase signals
     std::vector<long long> per_step(s.n_counters, 0);
     for (int phi = 0; phi < PPS; ++phi)

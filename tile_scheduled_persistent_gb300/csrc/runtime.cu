@@ -6,6 +6,7 @@
 // worker binary and GPU, and runs up to 64 tokens per cooperative launch.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -202,12 +203,17 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
     if ((e = dalloc(plan, &p.o, (size_t)g.qd * 2)) != cudaSuccess) return fail(e);
     if ((e = dalloc(plan, &p.x, (size_t)g.H * 2)) != cudaSuccess) return fail(e);
     if ((e = dalloc(plan, &p.a, (size_t)g.F * 2)) != cudaSuccess) return fail(e);
-    plan->sync_bytes = kMaxStepsPerLaunch * 8 + (size_t)plan->sched.n_counters * kCounterStride * 4;
+    // one memset per launch clears: argmax keys | phase counters | split arrivals
+    const size_t ctr_bytes = (size_t)plan->sched.n_counters * kCounterStride * 4;
+    const size_t arrive_bytes = (size_t)g.L * g.nkv * kCounterStride * 4;
+    plan->sync_bytes = kMaxStepsPerLaunch * 8 + ctr_bytes + arrive_bytes;
     uint8_t *sync;
     if ((e = dalloc(plan, &sync, plan->sync_bytes)) != cudaSuccess) return fail(e);
     plan->d_keys = reinterpret_cast<unsigned long long *>(sync);
     p.keys = plan->d_keys;
     p.counters = reinterpret_cast<uint32_t *>(sync + kMaxStepsPerLaunch * 8);
+    p.attn_arrive = reinterpret_cast<uint32_t *>(sync + kMaxStepsPerLaunch * 8 + ctr_bytes);
+    p.attn_head_signals = plan->sched.scheduler == TILES_SCHED_COUNTERS ? 1 : 0;
     if ((e = dalloc(plan, &p.status, 16)) != cudaSuccess) return fail(e);
     if ((e = cudaMemset(p.status, 0, 16)) != cudaSuccess) return fail(e);
     if ((e = dalloc(plan, &plan->d_prompt_stage, (size_t)g.max_pos * 4)) != cudaSuccess) return fail(e);
@@ -220,6 +226,17 @@ void tiles_plan_destroy(tiles_plan_t plan) {
     if (!plan) return;
     for (void *v : plan->allocs) cudaFree(v);
     delete plan;
+}
+
+tiles_status_t tiles_plan_set_trace(tiles_plan_t plan, void *trace, int32_t steps) {
+    if (!plan || steps < 0 || (steps > 0 && !trace)) return TILES_ERR_INVALID_ARG;
+    int mt = 0;
+    for (int c = 0; c < plan->sched.n_ctas; ++c)
+        mt = std::max(mt, plan->sched.offsets[c + 1] - plan->sched.offsets[c]);
+    plan->base.trace = steps > 0 ? reinterpret_cast<unsigned long long *>(trace) : nullptr;
+    plan->base.trace_steps = steps;
+    plan->base.trace_tasks = mt;
+    return TILES_OK;
 }
 
 tiles_status_t tiles_plan_get_info(tiles_plan_t plan, tiles_plan_info *info) {
@@ -237,6 +254,9 @@ tiles_status_t tiles_plan_get_info(tiles_plan_t plan, tiles_plan_info *info) {
     info->n_tasks = (int32_t)s.tasks.size();
     info->n_counters = s.n_counters;
     info->phases_per_step = phases_per_step(g);
+    int mt = 0;
+    for (int c = 0; c < s.n_ctas; ++c) mt = std::max(mt, s.offsets[c + 1] - s.offsets[c]);
+    info->max_tasks_per_cta = mt;
     long long tot = 0, mx = 0, mn = -1;
     for (int c = 0; c < s.n_ctas; ++c) {
         long long b = 0;

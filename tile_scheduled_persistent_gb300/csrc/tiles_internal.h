@@ -68,7 +68,7 @@ TILES_HD int op_extent(const Geom &g, int op) {
     switch (op) {
         case TILES_OP_QKV: return g.qkv_rows;
         case TILES_OP_ATTN: return g.nkv * g.kv_splits;
-        case TILES_OP_COMBINE: return g.nq;
+        case TILES_OP_COMBINE: return 0;  // merged into the attention phase (last split merges)
         case TILES_OP_OPROJ: return g.H;
         case TILES_OP_GATEUP: return g.F;
         case TILES_OP_DOWN: return g.H;
@@ -172,6 +172,9 @@ struct KernelParams {
     uint16_t *o, *x, *a;
     unsigned long long *keys;
     uint32_t *counters, *status;
+    // per (layer, kv head) arrivals of split tiles; the last one merges the splits
+    uint32_t *attn_arrive;
+    int attn_head_signals;  // 1: the merging tile signals the attention counter (counter chains)
     // run
     const int32_t *prompt;
     int n_prompt, step0, pos0, n_steps;
@@ -179,7 +182,15 @@ struct KernelParams {
     float *out_logits;
     unsigned long long timeout_ns;
     int vec_off, ring_off;
+    // optional per-task timeline: [cta][step < trace_steps][task][kTraceWords]
+    unsigned long long *trace;
+    int trace_steps, trace_tasks;
 };
+
+// trace record words
+constexpr int kTraceWords = 8;
+enum { kTrWaitStart = 0, kTrWaitEnd, kTrTaskEnd, kTrProdFirst, kTrProdLast, kTrProdStall,
+       kTrOpInfo };
 
 }  // namespace tiles
 
