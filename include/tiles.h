@@ -93,10 +93,11 @@ enum { TILES_SCHED_WAVES = 0, TILES_SCHED_COUNTERS = 1 };
 typedef struct {
     int32_t scheduler;    /* TILES_SCHED_COUNTERS (default) or TILES_SCHED_WAVES        */
     int32_t n_ctas;       /* 0 = one worker CTA per SM                                  */
-    int32_t slot_bytes;   /* 0 = auto: bytes per shared-memory ring slot (mult. of 1024) */
+    int32_t slot_bytes;   /* 0 = auto (32 KB or the longest row): ring slot bytes, mult. of 1024 */
     int32_t ring_slots;   /* 0 = as many as fit in shared memory                         */
     int32_t kv_splits;    /* 0 = auto: split-KV ranges per KV head                       */
     int32_t timeout_ms;   /* bound on every in-kernel wait; 0 = 2000 ms                  */
+    int32_t l2_prefetch_kb; /* L2 lookahead of the weight stream per CTA, KB; <= 0 = off */
     uint32_t flags;       /* reserved, must be 0                                         */
 } tiles_plan_opts;
 
@@ -107,8 +108,11 @@ typedef struct tiles_plan_s *tiles_plan_t;
  * occupancy of the worker kernel at the chosen shared-memory size), build the
  * tile graph, assign tiles to CTAs balancing streamed bytes, order them into
  * waves or dependency-counter chains, validate, and allocate the plan's own
- * device tables and scratch.  On success *out owns those allocations.
- * Errors: INVALID_ARG, UNSUPPORTED (shape), PLAN_INVALID, CUDA. */
+ * device tables and scratch. The plan also packs its own copies of
+ * [Wq; Wk; Wv] and of Wg/Wu interleaved by row (the kernel streams those);
+ * wq/wk/wv/w_gate/w_up are only read during this call, the other weight
+ * pointers must stay valid for the plan's lifetime. On success *out owns its
+ * allocations. Errors: INVALID_ARG, UNSUPPORTED (shape), PLAN_INVALID, CUDA. */
 tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weights *weights,
                                  const tiles_plan_opts *opts, tiles_plan_t *out);
 

@@ -96,6 +96,10 @@ __device__ __forceinline__ void bulk_g2s_nohint(void *dst, const void *src, uint
         : "memory");
 }
 
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -279,18 +283,80 @@ struct Producer {
     unsigned long long pol_weights;  // L2 evict-first: weights are streamed once per step
     unsigned long long stall = 0;    // ns spent waiting for a free slot (traced runs)
     bool tracing = false;
+    int pid = 0;                     // this producer issues chunks of slots with slot % 2 == pid
 
-    __device__ Producer(const KernelParams &p_, Smem &s_) : p(p_), s(s_) {
+    __device__ Producer(const KernelParams &p_, Smem &s_, int pid_) : p(p_), s(s_), pid(pid_) {
         asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_weights));
     }
 
-    // Reserve the next slot: wait until its previous chunk was consumed.
+    // Weight rows [r0, ...) of a GEMV tile: where they start in HBM.
+    __device__ const uint16_t *gemv_src(int op, int layer, uint32_t r0) const {
+        const LayerPtrs &lw = p.layers[layer];
+        const size_t in = (size_t)op_in_dim(p.g, op);
+        switch (op) {
+            case TILES_OP_QKV: return lw.wqkv + r0 * in;
+            case TILES_OP_OPROJ: return lw.wo + r0 * in;
+            case TILES_OP_GATEUP: return lw.wgu + r0 * 2 * in;
+            case TILES_OP_DOWN: return lw.w_down + r0 * in;
+            default: return p.embed + r0 * in;
+        }
+    }
+
+    // L2 lookahead (producer 0 only): walks the weight rows of this CTA's stream
+    // ahead of the ring and prefetches them into L2 in pieces of up to 64 KB, at
+    // most l2_prefetch_bytes ahead of the bytes already handed to the ring. HBM
+    // keeps streaming while the consumers wait at a phase boundary and the ring
+    // is full; the ring then refills from L2.
+    unsigned long long stream_bytes = 0;  // weight bytes of every chunk passed so far
+    unsigned long long look_bytes = 0;
+    int look_st = 0, look_ti = -1;
+    uint32_t look_r = 0;
+    bool look_done = false;
+
+    __device__ void lookahead(int t0, int t1) {
+        const unsigned long long limit = stream_bytes + p.l2_prefetch_bytes;
+        while (!look_done && look_bytes < limit) {
+            if (look_ti < t0 || look_ti >= t1) {
+                if (look_ti >= t1 && ++look_st >= p.n_steps) {
+                    look_done = true;
+                    break;
+                }
+                look_ti = t0;
+                look_r = p.tasks[t0].begin;
+            }
+            const tiles_task t = p.tasks[look_ti];
+            if (!op_is_gemv(t.op) || look_r >= t.end) {
+                if (++look_ti < t1) look_r = p.tasks[look_ti].begin;
+                continue;
+            }
+            const uint32_t row_bytes = (uint32_t)op_in_dim(p.g, t.op) * 2u * (uint32_t)op_mats(t.op);
+            uint32_t n = 65536u / row_bytes;
+            if (n < 1) n = 1;
+            if (n > t.end - look_r) n = t.end - look_r;
+            bulk_prefetch_l2(gemv_src(t.op, t.layer, look_r), n * row_bytes);
+            look_bytes += (unsigned long long)n * row_bytes;
+            look_r += n;
+        }
+    }
+
+    // Chunk j's slot belongs to this producer?
+    __device__ bool owns(uint32_t jj) const {
+        return (int)((jj % (uint32_t)p.g.ring_slots) % kProducerWarps) == pid;
+    }
+
+    // Reserve the next slot: wait until its previous chunk was consumed. While
+    // the ring is full (consumers held at a phase boundary), producer 0 spends
+    // the wait prefetching the upcoming weight rows into L2.
+    int lt0 = 0, lt1 = 0;  // this CTA's task range (for the lookahead)
     __device__ uint8_t *acquire(uint64_t **bar) {
         const uint32_t ns = (uint32_t)p.g.ring_slots;
         uint32_t slot = j % ns;
         if (j >= ns) {
             unsigned long long t0 = tracing ? global_timer() : 0;
-            if (!wait_mbar(p, &s.empty[slot], ((j / ns) - 1u) & 1u)) {
+            const uint32_t par = ((j / ns) - 1u) & 1u;
+            if (pid == 0 && p.l2_prefetch_bytes && !mbar_try_wait(&s.empty[slot], par))
+                lookahead(lt0, lt1);
+            if (!wait_mbar(p, &s.empty[slot], par)) {
                 ok = false;
                 return nullptr;
             }
@@ -301,6 +367,11 @@ struct Producer {
     }
 
     __device__ void gemv_chunk(int op, int layer, uint32_t r0, uint32_t nr) {
+        stream_bytes += (unsigned long long)nr * op_in_dim(p.g, op) * 2u * op_mats(op);
+        if (!owns(j)) {
+            ++j;
+            return;
+        }
         uint64_t *bar;
         uint8_t *dst = acquire(&bar);
         if (!dst) return;
@@ -308,33 +379,18 @@ struct Producer {
         const LayerPtrs &lw = p.layers[layer];
         const int in = op_in_dim(g, op);
         const uint32_t rb = (uint32_t)in * 2u;
-        const int rpc = op_rows_per_chunk(g, op);
         const uint32_t bytes = nr * rb * (uint32_t)op_mats(op);
         mbar_expect_tx(bar, bytes);
         const unsigned long long pol = pol_weights;
         switch (op) {
-            case TILES_OP_QKV: {
-                // rows of the concatenation [Wq; Wk; Wv]
-                uint32_t r = r0, end = r0 + nr;
-                while (r < end) {
-                    const uint16_t *base;
-                    uint32_t lo, hi;
-                    if (r < (uint32_t)g.qd) { base = lw.wq; lo = 0; hi = g.qd; }
-                    else if (r < (uint32_t)(g.qd + g.kvd)) { base = lw.wk; lo = g.qd; hi = g.qd + g.kvd; }
-                    else { base = lw.wv; lo = g.qd + g.kvd; hi = g.qkv_rows; }
-                    uint32_t e = end < hi ? end : hi;
-                    bulk_g2s(dst + (size_t)(r - r0) * rb, base + (size_t)(r - lo) * in, (e - r) * rb,
-                             bar, pol);
-                    r = e;
-                }
+            case TILES_OP_QKV:  // rows of the packed [Wq; Wk; Wv]
+                bulk_g2s(dst, lw.wqkv + (size_t)r0 * in, nr * rb, bar, pol);
                 break;
-            }
             case TILES_OP_OPROJ:
                 bulk_g2s(dst, lw.wo + (size_t)r0 * in, nr * rb, bar, pol);
                 break;
-            case TILES_OP_GATEUP:
-                bulk_g2s(dst, lw.w_gate + (size_t)r0 * in, nr * rb, bar, pol);
-                bulk_g2s(dst + (size_t)rpc * rb, lw.w_up + (size_t)r0 * in, nr * rb, bar, pol);
+            case TILES_OP_GATEUP:  // rows of the packed [Wg | Wu] (gate row, up row, ...)
+                bulk_g2s(dst, lw.wgu + (size_t)r0 * 2 * in, 2 * nr * rb, bar, pol);
                 break;
             case TILES_OP_DOWN:
                 bulk_g2s(dst, lw.w_down + (size_t)r0 * in, nr * rb, bar, pol);
@@ -348,6 +404,10 @@ struct Producer {
 
     // K and V of positions [p0, p1) (all < P) of kv head `h`, layer `layer`.
     __device__ void kv_chunk(int layer, int h, int p0, int p1) {
+        if (!owns(j)) {
+            ++j;
+            return;
+        }
         uint64_t *bar;
         uint8_t *dst = acquire(&bar);
         if (!dst) return;
@@ -388,12 +448,14 @@ struct Producer {
     __device__ void run(int cta) {
         const Geom &g = p.g;
         const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
+        lt0 = t0;
+        lt1 = t1;
         fence_proxy_async_global();
         for (int st = 0; st < p.n_steps && ok; ++st) {
             const int P = p.pos0 + st;
             for (int ti = t0; ti < t1 && ok; ++ti) {
                 const tiles_task t = p.tasks[ti];
-                unsigned long long *tr = trace_rec(p, cta, st, ti - t0);
+                unsigned long long *tr = pid == 0 ? trace_rec(p, cta, st, ti - t0) : nullptr;
                 tracing = tr != nullptr;
                 stall = 0;
                 if (tr) tr[kTrProdFirst] = global_timer();
@@ -429,6 +491,7 @@ struct Producer {
         const uint32_t ns = (uint32_t)g.ring_slots;
         uint32_t first = j > ns ? j - ns : 0;
         for (uint32_t k = first; k < j; ++k) {
+            if (!owns(k)) continue;
             unsigned long long t0n = global_timer();
             while (!mbar_try_wait(&s.full[k % ns], (k / ns) & 1u)) {
                 if (global_timer() - t0n > p.timeout_ns) break;
@@ -458,7 +521,8 @@ __device__ __forceinline__ void gemv_rows(const uint8_t *slot, const uint4 *vec,
         for (int r = 0; r < NR; ++r)
 #pragma unroll
             for (int m = 0; m < MATS; ++m) {
-                const uint4 w = reinterpret_cast<const uint4 *>(slot + ((size_t)m * rpc + r) * row_bytes)[c];
+                // MATS == 2: gate row r at 2r, up row r at 2r + 1 (packed layout)
+                const uint4 w = reinterpret_cast<const uint4 *>(slot + ((size_t)r * MATS + m) * row_bytes)[c];
                 acc[r][m] = dot8(w, xf, acc[r][m]);
             }
     }
@@ -1178,8 +1242,8 @@ __global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_con
     }
     __syncthreads();
     if (tid >= kConsumerWarps * 32) {
-        if (tid == kConsumerWarps * 32) {
-            Producer prod(p, s);
+        if ((tid & 31) == 0) {
+            Producer prod(p, s, (tid >> 5) - kConsumerWarps);
             prod.run(blockIdx.x);
         }
         return;

@@ -85,9 +85,13 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     G_.kvd = d.n_kv_heads * d.head_dim;
     G_.qkv_rows = G_.qd + 2 * G_.kvd;
 
-    // slot: large enough for one row of every GEMV (two for gate/up), >= 16 KB
-    int need = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, 2 * 2 * G_.H, 16384});
-    int slot = o.slot_bytes > 0 ? o.slot_bytes : round_up(need, 1024);
+    // slot: large enough for one row of every GEMV (two for gate/up). A bulk
+    // copy costs about the same TMA time whatever its size up to tens of KB
+    // (measured on GB300: two issuing lanes reach ~45 GB/s per SM with 16 KB
+    // copies and ~85 GB/s with 32 KB ones), so the default is 32 KB or the
+    // largest row, whichever is bigger.
+    int need = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, 2 * 2 * G_.H});
+    int slot = o.slot_bytes > 0 ? o.slot_bytes : round_up(std::max(need, 32768), 1024);
     if (slot % 1024 || slot < need) return fail(TILES_ERR_INVALID_ARG, "slot_bytes too small or not a multiple of 1024");
     G_.slot_bytes = slot;
     auto rpc = [&](int in, int mats) {

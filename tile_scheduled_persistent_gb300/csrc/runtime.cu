@@ -146,6 +146,9 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
     p.embed = reinterpret_cast<const uint16_t *>(w->embed);
     p.final_norm = reinterpret_cast<const uint16_t *>(w->final_norm);
     p.timeout_ns = (unsigned long long)(o.timeout_ms > 0 ? o.timeout_ms : 2000) * 1000000ull;
+    // L2 lookahead is off unless asked for: on GB300 it competes with the ring
+    // copies for the TMA unit and measured slower at every distance tried
+    p.l2_prefetch_bytes = o.l2_prefetch_kb > 0 ? (unsigned long long)o.l2_prefetch_kb * 1024ull : 0ull;
     p.ring_off = kCtlBytes;
     p.vec_off = kCtlBytes + g.ring_slots * g.slot_bytes;
     auto fail = [&](cudaError_t ce) {
@@ -164,7 +167,24 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
         lp[l] = LayerPtrs{(const uint16_t *)lw.attn_norm, (const uint16_t *)lw.wq, (const uint16_t *)lw.wk,
                           (const uint16_t *)lw.wv,        (const uint16_t *)lw.q_norm, (const uint16_t *)lw.k_norm,
                           (const uint16_t *)lw.wo,        (const uint16_t *)lw.ffn_norm, (const uint16_t *)lw.w_gate,
-                          (const uint16_t *)lw.w_up,      (const uint16_t *)lw.w_down};
+                          (const uint16_t *)lw.w_up,      (const uint16_t *)lw.w_down, nullptr, nullptr};
+        // packed copies ("TilePlan ... packs the weights"): [Wq; Wk; Wv] contiguous,
+        // and Wg / Wu interleaved by row, so each ring chunk is one bulk copy
+        const size_t H2 = (size_t)g.H * 2;
+        uint16_t *qkv, *gu;
+        if ((e = dalloc(plan, &qkv, (size_t)g.qkv_rows * H2)) != cudaSuccess) return fail(e);
+        if ((e = dalloc(plan, &gu, (size_t)g.F * 2 * H2)) != cudaSuccess) return fail(e);
+        uint8_t *q8 = reinterpret_cast<uint8_t *>(qkv);
+        if ((e = cudaMemcpy(q8, lw.wq, (size_t)g.qd * H2, cudaMemcpyDeviceToDevice)) != cudaSuccess ||
+            (e = cudaMemcpy(q8 + (size_t)g.qd * H2, lw.wk, (size_t)g.kvd * H2, cudaMemcpyDeviceToDevice)) != cudaSuccess ||
+            (e = cudaMemcpy(q8 + (size_t)(g.qd + g.kvd) * H2, lw.wv, (size_t)g.kvd * H2, cudaMemcpyDeviceToDevice)) !=
+                cudaSuccess ||
+            (e = cudaMemcpy2D(gu, 2 * H2, lw.w_gate, H2, H2, g.F, cudaMemcpyDeviceToDevice)) != cudaSuccess ||
+            (e = cudaMemcpy2D(reinterpret_cast<uint8_t *>(gu) + H2, 2 * H2, lw.w_up, H2, H2, g.F,
+                              cudaMemcpyDeviceToDevice)) != cudaSuccess)
+            return fail(e);
+        lp[l].wqkv = qkv;
+        lp[l].wgu = gu;
     }
     e = cudaMemcpy(d_tasks, plan->sched.tasks.data(), plan->sched.tasks.size() * sizeof(tiles_task),
                    cudaMemcpyHostToDevice);

@@ -18,7 +18,8 @@
 namespace tiles {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kProducerWarps = 2;  // lane 0 of each issues the copies of every other ring slot
+constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 constexpr int kMaxRowsPerChunk = 8;                   // GEMV rows a warp handles per chunk
 constexpr int kMaxSlots = 32;
 constexpr int kSmemLimit = 232448;                    // 227 KB dynamic shared memory per CTA
@@ -148,9 +149,13 @@ TILES_HD long long task_bytes(const Geom &g, const tiles_task &t, int P) {
 }
 
 // Device copy of one layer's weight pointers.
+// wqkv and wgu are the plan's packed copies: [Wq; Wk; Wv] as one [qd + 2 kvd][H]
+// matrix, and Wg / Wu interleaved by row ([F][2][H]: gate row r, then up row
+// r), so every ring chunk of those tiles is a single contiguous bulk copy.
 struct LayerPtrs {
     const uint16_t *attn_norm, *wq, *wk, *wv, *q_norm, *k_norm, *wo, *ffn_norm, *w_gate, *w_up,
         *w_down;
+    const uint16_t *wqkv, *wgu;
 };
 
 struct KernelParams {
@@ -181,6 +186,7 @@ struct KernelParams {
     int32_t *out_tokens;
     float *out_logits;
     unsigned long long timeout_ns;
+    unsigned long long l2_prefetch_bytes;  // L2 lookahead of the weight stream per CTA (0: off)
     int vec_off, ring_off;
     // optional per-task timeline: [cta][step < trace_steps][task][kTraceWords]
     unsigned long long *trace;
