@@ -154,6 +154,33 @@ tiles_status_t tiles_decode_host(tiles_plan_t plan, void *k_cache, void *v_cache
                                  int32_t n_new, void *stream, int32_t *out_tokens_host,
                                  float *out_logits_host);
 
+/*
+ * tiles_decode without any device allocation. The pages have no counterpart:
+ * this exists for callers that may not allocate GPU memory when they decode
+ * (a process whose device memory is all handed to its own allocator, or a
+ * runtime that forbids allocation after start-up), so the kernel's per-call
+ * working memory comes from one fixed array compiled into the library instead
+ * of the plan's own buffers. Same arguments, ownership, results and errors as
+ * tiles_decode; device-side errors still go to the plan's status word
+ * (read with tiles_status).
+ *
+ *   - The array is 1 MiB of device memory, held by every GPU that loads the
+ *     library until the process exits. A plan whose working memory does not
+ *     fit (q/k/v, split partials, attention output, residual, FFN activation,
+ *     argmax keys and counters) is rejected with TILES_ERR_CAPACITY.
+ *   - The first call on a device looks up the array's device address once;
+ *     make that first call before any stream capture.
+ *   - Every call on a device shares the one array and finds it as the previous
+ *     call left it; the call clears what must start at zero. Calls whose work
+ *     overlaps on the GPU (other streams, other plans) race on it: keep them
+ *     ordered.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache, void *v_cache,
+                                    const int32_t *prompt, int32_t n_prompt, int32_t start_pos,
+                                    int32_t n_new, void *stream, int32_t *out_tokens,
+                                    float *out_logits);
+
 /* Synchronises `stream` and reads the plan's device status word, then clears
  * it. Returns TILES_OK, TILES_ERR_TIMEOUT, TILES_ERR_DEVICE_BOUNDS or CUDA. */
 tiles_status_t tiles_status(tiles_plan_t plan, void *stream);

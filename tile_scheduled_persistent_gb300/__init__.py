@@ -94,7 +94,8 @@ assert ctypes.sizeof(Task) == 24
 EXPORTS = ("tiles_plan_create", "tiles_plan_destroy", "tiles_decode", "tiles_decode_host",
            "tiles_status", "tiles_status_string", "tiles_plan_get_info", "tiles_schedule_build",
            "tiles_schedule_validate", "tiles_schedule_tasks", "tiles_schedule_cta_bytes",
-           "tiles_schedule_destroy", "tiles_copy_bw", "tiles_barrier_cost", "tiles_plan_set_trace")
+           "tiles_schedule_destroy", "tiles_copy_bw", "tiles_barrier_cost", "tiles_plan_set_trace",
+           "tiles_decode_noalloc")
 
 _lib_handle = None
 
@@ -116,6 +117,8 @@ def _lib():
         L.tiles_decode.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.tiles_decode.restype = st
         L.tiles_decode_host.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
+        L.tiles_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
+        L.tiles_decode_noalloc.restype = st
         L.tiles_decode_host.restype = st
         L.tiles_status.argtypes = [vp, vp]
         L.tiles_status.restype = st
@@ -267,6 +270,16 @@ class Plan:
         _check(_lib().tiles_decode(self._h, _ptr(k_cache), _ptr(v_cache), _ptr(prompt),
                                    int(prompt.numel()), start_pos, n_new, _stream_ptr(stream),
                                    _ptr(out_tokens), _ptr(out_logits)), "tiles_decode")
+
+    def decode_noalloc(self, k_cache, v_cache, prompt, start_pos: int, n_new: int, out_tokens,
+                       out_logits=None, stream=None) -> None:
+        """Same as decode, but the kernel's working memory comes from the library's
+        fixed 1 MiB device array instead of the plan's buffers (nothing is allocated;
+        calls that overlap on the GPU must not share it)."""
+        _check(_lib().tiles_decode_noalloc(self._h, _ptr(k_cache), _ptr(v_cache), _ptr(prompt),
+                                           int(prompt.numel()), start_pos, n_new,
+                                           _stream_ptr(stream), _ptr(out_tokens), _ptr(out_logits)),
+               "tiles_decode_noalloc")
 
     def decode_host(self, k_cache, v_cache, prompt_np, start_pos: int, n_new: int,
                     out_tokens_np, out_logits_np=None, stream=None) -> None:

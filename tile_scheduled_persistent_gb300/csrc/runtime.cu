@@ -430,3 +430,94 @@ tiles_status_t tiles_barrier_cost(int32_t n_ctas, int32_t rounds, double *ns_per
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without any allocation: the per-call working memory of the kernel
+// (q/k/v, split partials, attention output, residual, FFN activation, argmax
+// keys, phase counters, split arrivals) lives in one file-scope device array
+// instead of the plan's own buffers. For callers that must not allocate device
+// memory at the point of the call. The plan's tables, weights and status word
+// are still the plan's.
+
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 1u << 20;  // 1 MiB, held by every GPU that loads the library
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kNoAllocMaxDevices];  // device address of g_noalloc_scratch, per device
+
+size_t align256(size_t v) { return (v + 255u) & ~(size_t)255u; }
+
+// Device address of the array on `dev` (current device); looked up once per device.
+tiles_status_t noalloc_scratch(int dev, unsigned char **out) {
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return TILES_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return TILES_ERR_CUDA;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = reinterpret_cast<unsigned char *>(g_noalloc_ptr[dev]);
+    return TILES_OK;
+}
+
+}  // namespace
+
+extern "C" tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache, void *v_cache,
+                                               const int32_t *prompt, int32_t n_prompt, int32_t start_pos,
+                                               int32_t n_new, void *stream, int32_t *out_tokens,
+                                               float *out_logits) {
+    if (!plan || !k_cache || !v_cache || !prompt || n_prompt < 1 || n_new < 0 || start_pos < 0)
+        return TILES_ERR_INVALID_ARG;
+    if (n_new > 0 && !out_tokens) return TILES_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return TILES_ERR_INVALID_ARG;
+    const Geom &g = plan->sched.geom;
+    // layout in the array: sync block (zeroed per launch) | qkv | partials | o | x | a
+    const size_t off_qkv = align256(plan->sync_bytes);
+    const size_t off_part = off_qkv + align256((size_t)g.qkv_rows * 4);
+    const size_t off_o = off_part + align256((size_t)g.nq * g.kv_splits * (kPartialPad + g.d) * 4);
+    const size_t off_x = off_o + align256((size_t)g.qd * 2);
+    const size_t off_a = off_x + align256((size_t)g.H * 2);
+    const size_t need = off_a + align256((size_t)g.F * 2);
+    if (need > kNoAllocScratchBytes) return TILES_ERR_CAPACITY;
+    const long long steps = (long long)n_prompt - 1 + n_new;
+    if (steps == 0) return TILES_OK;
+    if ((long long)start_pos + steps > g.max_pos) return TILES_ERR_CAPACITY;
+    tiles_status_t st = check_device(plan);
+    if (st != TILES_OK) return st;
+    unsigned char *base = nullptr;
+    if ((st = noalloc_scratch(plan->device, &base)) != TILES_OK) return st;
+    const size_t ctr_bytes = (size_t)plan->sched.n_counters * kCounterStride * 4;
+    KernelParams p = plan->base;
+    p.keys = reinterpret_cast<unsigned long long *>(base);
+    p.counters = reinterpret_cast<uint32_t *>(base + kMaxStepsPerLaunch * 8);
+    p.attn_arrive = reinterpret_cast<uint32_t *>(base + kMaxStepsPerLaunch * 8 + ctr_bytes);
+    p.qkv = reinterpret_cast<float *>(base + off_qkv);
+    p.partials = reinterpret_cast<float *>(base + off_part);
+    p.o = reinterpret_cast<uint16_t *>(base + off_o);
+    p.x = reinterpret_cast<uint16_t *>(base + off_x);
+    p.a = reinterpret_cast<uint16_t *>(base + off_a);
+    p.k_cache = reinterpret_cast<uint16_t *>(k_cache);
+    p.v_cache = reinterpret_cast<uint16_t *>(v_cache);
+    p.prompt = prompt;
+    p.n_prompt = n_prompt;
+    p.out_tokens = out_tokens;
+    p.out_logits = out_logits;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    for (long long s0 = 0; s0 < steps; s0 += kMaxStepsPerLaunch) {
+        const int n = (int)(steps - s0 < kMaxStepsPerLaunch ? steps - s0 : kMaxStepsPerLaunch);
+        p.step0 = (int)s0;
+        p.pos0 = start_pos + (int)s0;
+        p.n_steps = n;
+        // the array keeps the previous call's contents: the counters and keys must start at zero
+        cudaError_t e = cudaMemsetAsync(base, 0, plan->sync_bytes, cs);
+        if (e == cudaSuccess) e = megakernel_launch(p, plan->sched.n_ctas, g.smem_bytes, cs);
+        if (e != cudaSuccess) return TILES_ERR_CUDA;
+    }
+    return TILES_OK;
+}
