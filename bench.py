@@ -10,7 +10,7 @@ kernel); each call rewrites positions 1023..1086, so repeats are identical and
 are checked bit for bit.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
-                  [--scheduler counters|waves] [--impl ours|reference]
+                  [--scheduler counters|waves] [--impl ours|reference] [--tokens T]
 
 With N > 1 (launched by torchrun) every rank runs an independent replica: a
 batch-1 decode has no exchange step to shard (replicas only). `--impl
@@ -76,9 +76,11 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config_name):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel source; else None."""
+def recorded_traffic(config_name, n_tokens):
+    """DRAM bytes per launch of `n_tokens` tokens, from the per-token figure of a
+    committed ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of one
+    launch over its token count), if it was taken on the current kernel
+    source; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
@@ -87,7 +89,8 @@ def recorded_traffic(config_name):
     e = d.get(config_name)
     if not e or e.get("source_hash") != kernel_source_hash():
         return None
-    return e.get("dram_bytes_per_launch")
+    per_token = e.get("dram_bytes_per_token")
+    return None if per_token is None else per_token * n_tokens
 
 
 class ClockSampler:
@@ -205,6 +208,9 @@ def run_ours(args):
     dev = torch.cuda.current_device()
     tsp.build()
     cfg = S.CONFIGS[args.config]
+    if args.tokens:
+        from dataclasses import replace
+        cfg = replace(cfg, n_new=args.tokens)
     log(f"[rank {rank}] generating {cfg.name} inputs ...")
     t0 = time.time()
     w = S.model_weights(cfg)
@@ -297,7 +303,7 @@ def run_ours(args):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
     else:
         peak, peak_src = 6800.0, "fallback 6.8 TB/s"
-    traffic = recorded_traffic(cfg.name)
+    traffic = recorded_traffic(cfg.name, cfg.n_new)
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     plan = r["plan"]
@@ -370,6 +376,9 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=2,
                     help="oracle decode tokens per timed step (CPU arms)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="decode tokens per step (default: the workload's 64); a smaller "
+                         "launch of the same kernel, for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         log("warm-up raised to 3 steps")

@@ -217,6 +217,8 @@ struct Ctl {
     unsigned long long warp_key[kConsumerWarps];
 };
 
+static_assert(2 * kMaxSlots * 8 + sizeof(Ctl) <= (size_t)kCtlBytes, "control block overflows its region");
+
 struct Smem {
     uint64_t *full, *empty;
     Ctl *ctl;
@@ -445,7 +447,7 @@ struct Producer {
         return true;
     }
 
-    __device__ void run(int cta) {
+    __device__ __forceinline__ void run(int cta) {
         const Geom &g = p.g;
         const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
         lt0 = t0;
@@ -598,17 +600,24 @@ struct Consumer {
     }
 
     // ---------------------------------------------------------- prologues
-    // vec <- bf16(rmsnorm(src) * gain), src bf16 [n]; sum of squares in a fixed
-    // order, so every CTA computes the same scale.
+    // vec <- bf16(rmsnorm(src) * gain), src bf16 [n <= 8192]; sum of squares in a
+    // fixed order, so every CTA computes the same scale. One pass over src: each
+    // thread keeps its (at most four) 16-byte pieces in registers.
     __device__ void rmsnorm_to_vec(const uint16_t *src, const uint16_t *gain, int n) {
+        constexpr int kMaxU = 4;
         const int nu4 = n >> 3;
+        uint4 v[kMaxU];
         float ss = 0.f;
-        for (int c = tid; c < nu4; c += kConsumerWarps * 32) {
-            uint4 v = __ldcg(reinterpret_cast<const uint4 *>(src) + c);
-            float f[8];
-            unpack8(v, f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+        for (int k = 0; k < kMaxU; ++k) {
+            const int c = tid + k * kConsumerWarps * 32;
+            if (c < nu4) {
+                v[k] = __ldcg(reinterpret_cast<const uint4 *>(src) + c);
+                float f[8];
+                unpack8(v[k], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+            }
         }
         ss = warp_sum(ss);
         if (lane == 0) s.ctl->red[warp] = ss;
@@ -618,21 +627,30 @@ struct Consumer {
         for (int w = 0; w < kConsumerWarps; ++w) tot += s.ctl->red[w];
         const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)n), p.eps)));
         uint4 *dst = reinterpret_cast<uint4 *>(s.vec);
-        for (int c = tid; c < nu4; c += kConsumerWarps * 32) {
-            uint4 v = __ldcg(reinterpret_cast<const uint4 *>(src) + c);
-            uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gain) + c);
-            float f[8], gf[8];
-            unpack8(v, f);
-            unpack8(gv, gf);
-            uint32_t o[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                uint16_t lo = f2bf(__fmul_rn(__fmul_rn(f[2 * e], r), gf[2 * e]));
-                uint16_t hi = f2bf(__fmul_rn(__fmul_rn(f[2 * e + 1], r), gf[2 * e + 1]));
-                o[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+        for (int k = 0; k < kMaxU; ++k) {
+            const int c = tid + k * kConsumerWarps * 32;
+            if (c < nu4) {
+                const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gain) + c);
+                float f[8], gf[8];
+                unpack8(v[k], f);
+                unpack8(gv, gf);
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint16_t lo = f2bf(__fmul_rn(__fmul_rn(f[2 * e], r), gf[2 * e]));
+                    const uint16_t hi = f2bf(__fmul_rn(__fmul_rn(f[2 * e + 1], r), gf[2 * e + 1]));
+                    o[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                }
+                dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
             }
-            dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
         }
+    }
+
+    // residual rows [begin, end) of `base` into shared memory, for the epilogue
+    __device__ void load_residual(const uint16_t *base, uint32_t begin, uint32_t end) {
+        uint16_t *res = reinterpret_cast<uint16_t *>(s.vec + p.res_off);
+        for (uint32_t r = begin + tid; r < end; r += kConsumerWarps * 32) res[r - begin] = __ldcg(&base[r]);
     }
 
     __device__ void copy_to_vec(const uint16_t *src, int n) {
@@ -643,6 +661,34 @@ struct Consumer {
     }
 
     // ---------------------------------------------------------- GEMV tasks
+    // One output row of a GEMV task, from its MATS dot products: the fused
+    // epilogue of the op (residual add, SwiGLU, logits store).
+    template <int MATS>
+    __device__ void emit_row(int op, const tiles_task &t, uint32_t row, const float (&v)[MATS]) {
+        switch (op) {
+            case TILES_OP_QKV:
+                __stcg(&p.qkv[row], v[0]);
+                break;
+            case TILES_OP_OPROJ:
+            case TILES_OP_DOWN: {  // residual rows were loaded in the prologue
+                const uint16_t xb = reinterpret_cast<const uint16_t *>(s.vec + p.res_off)[row - t.begin];
+                __stcg(&p.x[row], f2bf(__fadd_rn(bf2f(xb), v[0])));
+                break;
+            }
+            case TILES_OP_GATEUP: {
+                const float gt = v[0];
+                const float silu = __fdiv_rn(gt, __fadd_rn(1.0f, expf(-gt)));
+                __stcg(&p.a[row], f2bf(__fmul_rn(silu, v[MATS - 1])));
+                break;
+            }
+            case TILES_OP_LMHEAD:
+                if (p.out_logits) __stcg(&p.out_logits[(size_t)(p.step0 + step) * p.g.V + row], v[0]);
+                break;
+        }
+    }
+
+    // Chunk k goes to the warp that owns its slot, which reduces it alone; the
+    // warps work on different chunks at once.
     template <int MATS>
     __device__ void gemv_task(const tiles_task &t) {
         const Geom &g = p.g;
@@ -653,8 +699,6 @@ struct Consumer {
         const uint32_t nchunks = (t.end - t.begin + rpc - 1) / rpc;
         const uint4 *vec = reinterpret_cast<const uint4 *>(s.vec);
         unsigned long long best = 0;
-        const int sg = p.step0 + step;
-        (void)sg;
         for (uint32_t k = 0; k < nchunks; ++k) {
             const uint32_t jj = j + k;
             if (!mine(jj)) continue;
@@ -665,36 +709,7 @@ struct Consumer {
             float mine[MATS];
             gemv_rows_n<MATS>(nr, slot, vec, nu4, (size_t)in * 2, (int)rpc, mine);
             release_chunk(jj);
-            if ((uint32_t)lane < nr) {
-                const uint32_t row = r0 + lane;
-                switch (op) {
-                    case TILES_OP_QKV:
-                        __stcg(&p.qkv[row], mine[0]);
-                        break;
-                    case TILES_OP_OPROJ: {
-                        const uint16_t xb = (t.layer == 0)
-                                                ? p.embed[(size_t)s.ctl->token * g.H + row]
-                                                : __ldcg(&p.x[row]);
-                        __stcg(&p.x[row], f2bf(__fadd_rn(bf2f(xb), mine[0])));
-                        break;
-                    }
-                    case TILES_OP_DOWN: {
-                        const uint16_t xb = __ldcg(&p.x[row]);
-                        __stcg(&p.x[row], f2bf(__fadd_rn(bf2f(xb), mine[0])));
-                        break;
-                    }
-                    case TILES_OP_GATEUP: {
-                        const float gt = mine[0];
-                        const float silu = __fdiv_rn(gt, __fadd_rn(1.0f, expf(-gt)));
-                        __stcg(&p.a[row], f2bf(__fmul_rn(silu, mine[MATS - 1])));
-                        break;
-                    }
-                    case TILES_OP_LMHEAD: {
-                        if (p.out_logits) __stcg(&p.out_logits[(size_t)sg * g.V + row], mine[0]);
-                        break;
-                    }
-                }
-            }
+            if ((uint32_t)lane < nr) emit_row<MATS>(op, t, r0 + lane, mine);
             if (op == TILES_OP_LMHEAD) {
                 unsigned long long key = (uint32_t)lane < nr ? argmax_key(mine[0], r0 + lane) : 0ull;
                 key = warp_max_u64(key);
@@ -1138,7 +1153,7 @@ struct Consumer {
     }
 
     // ---------------------------------------------------------- main loop
-    __device__ void run(int cta) {
+    __device__ __forceinline__ void run(int cta) {
         const Geom &g = p.g;
         const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
         for (step = 0; step < p.n_steps; ++step) {
@@ -1180,6 +1195,7 @@ struct Consumer {
                         break;
                     case TILES_OP_OPROJ:
                         copy_to_vec(p.o, g.qd);
+                        load_residual(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : p.x, t.begin, t.end);
                         consumer_sync();
                         gemv_task<1>(t);
                         break;
@@ -1190,6 +1206,7 @@ struct Consumer {
                         break;
                     case TILES_OP_DOWN:
                         copy_to_vec(p.a, g.F);
+                        load_residual(p.x, t.begin, t.end);
                         consumer_sync();
                         gemv_task<1>(t);
                         break;

@@ -55,6 +55,7 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     int G = d.n_q_heads / d.n_kv_heads;
     if (!pow2(G) || G > 8) return fail(TILES_ERR_UNSUPPORTED, "GQA group must be 1, 2, 4 or 8");
     if (d.hidden % 8 || d.ffn % 8) return fail(TILES_ERR_UNSUPPORTED, "hidden, ffn multiples of 8");
+    if (d.hidden > 8192) return fail(TILES_ERR_UNSUPPORTED, "hidden above 8192");
     if (d.qk_norm != 0 && d.qk_norm != 1) return fail(TILES_ERR_INVALID_ARG, "qk_norm 0/1");
     if (d.rope_scaling != 0 && d.rope_scaling != 1)
         return fail(TILES_ERR_INVALID_ARG, "rope_scaling 0/1");
@@ -117,7 +118,9 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     int wstate_off = G * G_.d * 4 + 2 * G_.d * 2 + kConsumerWarps * 32 * G * 4;
     if (wstate_off + merge_need > attn_need) attn_need = wstate_off + merge_need;
     int vec = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, attn_need});
-    G_.vec_bytes = round_up(vec, 128);
+    // residual rows of an O-proj / down tile follow (a tile has at most H rows)
+    G_.res_off = round_up(vec, 16);
+    G_.vec_bytes = round_up(G_.res_off + 2 * G_.H, 128);
     int avail = smem_limit - kCtlBytes - G_.vec_bytes;
     int slots = o.ring_slots > 0 ? o.ring_slots : std::min(kMaxSlots, avail / slot);
     if (slots < 2 || slots > kMaxSlots) return fail(TILES_ERR_UNSUPPORTED, "ring needs 2..32 slots");

@@ -151,6 +151,7 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
     p.l2_prefetch_bytes = o.l2_prefetch_kb > 0 ? (unsigned long long)o.l2_prefetch_kb * 1024ull : 0ull;
     p.ring_off = kCtlBytes;
     p.vec_off = kCtlBytes + g.ring_slots * g.slot_bytes;
+    p.res_off = g.res_off;
     auto fail = [&](cudaError_t ce) {
         tiles_plan_destroy(plan);
         return cuda_fail(ce);

@@ -39,6 +39,7 @@ struct Geom {
     int slot_bytes, ring_slots, kv_splits, kv_block;
     int rpc_qkv, rpc_o, rpc_gateup, rpc_down, rpc_lm;
     int vec_bytes;  // shared-memory region for the input vector / attention scratch
+    int res_off;    // in the vec region: residual rows of an O-proj / down tile
     int smem_bytes;
 };
 
@@ -187,7 +188,7 @@ struct KernelParams {
     float *out_logits;
     unsigned long long timeout_ns;
     unsigned long long l2_prefetch_bytes;  // L2 lookahead of the weight stream per CTA (0: off)
-    int vec_off, ring_off;
+    int vec_off, ring_off, res_off;
     // optional per-task timeline: [cta][step < trace_steps][task][kTraceWords]
     unsigned long long *trace;
     int trace_steps, trace_tasks;
