@@ -48,6 +48,27 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device="cpu"):
+    """Element-wise maximum of a list of timings over all ranks (the list
+    unchanged when no process group is up). Every rank gets the same list."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(units_per_rank, seconds, device="cpu"):
+    """(units all ranks processed / the slowest rank's seconds, that time):
+    the replicas' aggregate throughput over the wall time of the whole job."""
+    import torch.distributed as dist
+    ws = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    (slowest,) = max_over_ranks([seconds], device)
+    return units_per_rank * ws / slowest, slowest
+
+
 def workload_config(cfg):
     return {"workload": f"{cfg.name}: {cfg.n_layers} layers, hidden {cfg.hidden}, "
                         f"{cfg.n_q_heads}/{cfg.n_kv_heads} heads x {cfg.head_dim}, ffn {cfg.ffn}, "
@@ -284,18 +305,12 @@ def run_ours(args):
                               tokens=ref_toks.cpu().numpy())
         log(f"[rank {rank}] {sname}: {args.steps * cfg.n_new / total_s:.1f} tok/s, "
             f"launch {statistics.mean(per_launch) * 1e6:.0f} us, bitwise {bitwise}")
-    # keep the faster scheduler on evidence
-    chosen = min(results, key=lambda s: results[s]["total_s"])
-    if args.scheduler != "both":
-        chosen = args.scheduler
+    # keep the faster scheduler on evidence: its slowest rank decides
+    names = list(results)
+    slowest = dict(zip(names, max_over_ranks([results[s]["total_s"] for s in names], "cuda")))
+    chosen = min(names, key=lambda s: slowest[s])
     r = results[chosen]
-    total_s = r["total_s"]
-    if ws > 1:
-        t = torch.tensor([total_s], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
-    tokens_all = args.steps * cfg.n_new * ws
-    value = tokens_all / total_s
+    value, total_s = whole_job_rate(args.steps * cfg.n_new, r["total_s"], "cuda")
     launch_s = statistics.mean(r["per_launch"])
     achieved_gbs = bytes_per_token * cfg.n_new / launch_s / 1e9
     peaks = measured_peaks()
@@ -315,13 +330,8 @@ def run_ours(args):
     t0 = time.perf_counter()
     for _ in range(args.steps):
         plan.decode_host(kc, vc, pin_prompt, cfg.start_pos, cfg.n_new, host_toks)
-    e2e_s = time.perf_counter() - t0
-    if ws > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_value, _ = whole_job_rate(args.steps * cfg.n_new, time.perf_counter() - t0, "cuda")
     e2e_same = bool(np.array_equal(host_toks, r["tokens"]))
-    e2e_value = tokens_all / e2e_s
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -355,7 +365,7 @@ def run_ours(args):
                 "bitwise_repeat": r["bitwise"],
                 "us_per_token": 1e6 * launch_s / cfg.n_new,
                 "grid_barrier_ns": barrier_ns,
-                "schedulers": {s: {"tok_s": args.steps * cfg.n_new / results[s]["total_s"],
+                "schedulers": {s: {"tok_s": args.steps * cfg.n_new * ws / slowest[s],
                                    "bitwise_repeat": results[s]["bitwise"]} for s in results}}
         print(json.dumps(line), flush=True)
     for s in results:
