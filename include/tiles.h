@@ -97,7 +97,8 @@ typedef struct {
     int32_t ring_slots;   /* 0 = as many as fit in shared memory                         */
     int32_t kv_splits;    /* 0 = auto: split-KV ranges per KV head                       */
     int32_t timeout_ms;   /* bound on every in-kernel wait; 0 = 2000 ms                  */
-    int32_t l2_prefetch_kb; /* L2 lookahead of the weight stream per CTA, KB; <= 0 = off */
+    int32_t l2_prefetch_kb; /* L2 prefetch warp: weight bytes it may run ahead of the ring, KB per CTA; <= 0 = off */
+    int32_t l2_prefetch_gbs; /* its issue rate per CTA, GB/s (token bucket); <= 0 = unpaced */
     uint32_t flags;       /* reserved, must be 0                                         */
 } tiles_plan_opts;
 

@@ -136,6 +136,24 @@ def test_few_ctas_and_small_ring(tsp):
     plan.close()
 
 
+@pytest.mark.parametrize("name", ["tiny", "g2_cache"])
+@pytest.mark.parametrize("gbs", [0, 40])
+def test_l2_prefetch_warp_leaves_results_bit_identical(tsp, name, gbs):
+    """The L2 prefetch warp only warms the cache: tokens, logits and the cache
+    it writes are bit-identical with and without it, paced or not."""
+    cfg = S.CONFIGS["tiny"] if name == "tiny" else VARIANTS[name]
+    w, k, v, prompt = inputs(cfg)
+    prompt = prompt[: cfg.n_prompt]
+    outs = []
+    for kb in (0, 64):
+        plan = _plan(tsp, cfg, w, l2_prefetch_kb=kb, l2_prefetch_gbs=gbs)
+        outs.append(gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, cfg.n_new))
+        plan.close()
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1].view(np.uint32), outs[1][1].view(np.uint32))
+    assert np.array_equal(outs[0][2], outs[1][2]) and np.array_equal(outs[0][3], outs[1][3])
+
+
 # ------------------------------------------------------------------ edge cases
 def test_edges_empty_and_single_step(tsp, tiny):
     import torch

@@ -65,7 +65,7 @@ class Weights(ctypes.Structure):
 class PlanOpts(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("scheduler", "n_ctas", "slot_bytes", "ring_slots", "kv_splits", "timeout_ms",
-                 "l2_prefetch_kb")] + \
+                 "l2_prefetch_kb", "l2_prefetch_gbs")] + \
                [("flags", ctypes.c_uint32)]
 
 
@@ -160,10 +160,10 @@ def _check(status: int, what: str):
 
 
 def make_opts(scheduler=SCHED_COUNTERS, n_ctas=0, slot_bytes=0, ring_slots=0, kv_splits=0,
-              timeout_ms=0, l2_prefetch_kb=0) -> PlanOpts:
+              timeout_ms=0, l2_prefetch_kb=0, l2_prefetch_gbs=0) -> PlanOpts:
     return PlanOpts(scheduler=scheduler, n_ctas=n_ctas, slot_bytes=slot_bytes,
                     ring_slots=ring_slots, kv_splits=kv_splits, timeout_ms=timeout_ms,
-                    l2_prefetch_kb=l2_prefetch_kb, flags=0)
+                    l2_prefetch_kb=l2_prefetch_kb, l2_prefetch_gbs=l2_prefetch_gbs, flags=0)
 
 
 # ------------------------------------------------------------------ schedule (host only)

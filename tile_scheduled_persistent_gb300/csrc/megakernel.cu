@@ -96,14 +96,28 @@ __device__ __forceinline__ void bulk_g2s_nohint(void *dst, const void *src, uint
         : "memory");
 }
 
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+__device__ __forceinline__ void prefetch_l2(const void *src) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+}
+__device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"((uint32_t)__cvta_generic_to_shared(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_volatile_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.volatile.shared.u64 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(p)), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
     uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 
 __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
@@ -212,9 +226,9 @@ struct Ctl {
     int unused;
     int token;
     int step_ready;  // consumers passed the first wait of this step (KV of earlier steps visible)
-    int merge;       // this CTA holds the last split of a KV head and merges its partials
     float red[kConsumerWarps];
     unsigned long long warp_key[kConsumerWarps];
+    unsigned long long stream_pos;  // weight bytes the producers have handed to the ring
 };
 
 static_assert(2 * kMaxSlots * 8 + sizeof(Ctl) <= (size_t)kCtlBytes, "control block overflows its region");
@@ -245,11 +259,20 @@ __device__ __forceinline__ unsigned long long *trace_rec(const KernelParams &p, 
 }
 
 // Bounded spin until counter >= target. false when the run is aborting.
+// Acquire side of a dependency counter: relaxed polls, one acquire fence once
+// the target is seen (the signal side is a release reduction after a CTA
+// barrier, which orders every thread's writes of the tile before it).
 __device__ bool wait_counter(const KernelParams &p, const uint32_t *ctr, uint32_t target) {
-    if (ld_acquire(ctr) >= target) return true;
+    if (ld_relaxed(ctr) >= target) {
+        fence_acquire_gpu();
+        return true;
+    }
     unsigned long long t0 = global_timer();
     for (uint32_t spin = 1;; ++spin) {
-        if (ld_acquire(ctr) >= target) return true;
+        if (ld_relaxed(ctr) >= target) {
+            fence_acquire_gpu();
+            return true;
+        }
         if ((spin & 31u) == 0) {
             if (failed(p)) return false;
             if (global_timer() - t0 > p.timeout_ns) {
@@ -304,60 +327,20 @@ struct Producer {
         }
     }
 
-    // L2 lookahead (producer 0 only): walks the weight rows of this CTA's stream
-    // ahead of the ring and prefetches them into L2 in pieces of up to 64 KB, at
-    // most l2_prefetch_bytes ahead of the bytes already handed to the ring. HBM
-    // keeps streaming while the consumers wait at a phase boundary and the ring
-    // is full; the ring then refills from L2.
     unsigned long long stream_bytes = 0;  // weight bytes of every chunk passed so far
-    unsigned long long look_bytes = 0;
-    int look_st = 0, look_ti = -1;
-    uint32_t look_r = 0;
-    bool look_done = false;
-
-    __device__ void lookahead(int t0, int t1) {
-        const unsigned long long limit = stream_bytes + p.l2_prefetch_bytes;
-        while (!look_done && look_bytes < limit) {
-            if (look_ti < t0 || look_ti >= t1) {
-                if (look_ti >= t1 && ++look_st >= p.n_steps) {
-                    look_done = true;
-                    break;
-                }
-                look_ti = t0;
-                look_r = p.tasks[t0].begin;
-            }
-            const tiles_task t = p.tasks[look_ti];
-            if (!op_is_gemv(t.op) || look_r >= t.end) {
-                if (++look_ti < t1) look_r = p.tasks[look_ti].begin;
-                continue;
-            }
-            const uint32_t row_bytes = (uint32_t)op_in_dim(p.g, t.op) * 2u * (uint32_t)op_mats(t.op);
-            uint32_t n = 65536u / row_bytes;
-            if (n < 1) n = 1;
-            if (n > t.end - look_r) n = t.end - look_r;
-            bulk_prefetch_l2(gemv_src(t.op, t.layer, look_r), n * row_bytes);
-            look_bytes += (unsigned long long)n * row_bytes;
-            look_r += n;
-        }
-    }
 
     // Chunk j's slot belongs to this producer?
     __device__ bool owns(uint32_t jj) const {
         return (int)((jj % (uint32_t)p.g.ring_slots) % kProducerWarps) == pid;
     }
 
-    // Reserve the next slot: wait until its previous chunk was consumed. While
-    // the ring is full (consumers held at a phase boundary), producer 0 spends
-    // the wait prefetching the upcoming weight rows into L2.
-    int lt0 = 0, lt1 = 0;  // this CTA's task range (for the lookahead)
+    // Reserve the next slot: wait until its previous chunk was consumed.
     __device__ uint8_t *acquire(uint64_t **bar) {
         const uint32_t ns = (uint32_t)p.g.ring_slots;
         uint32_t slot = j % ns;
         if (j >= ns) {
             unsigned long long t0 = tracing ? global_timer() : 0;
             const uint32_t par = ((j / ns) - 1u) & 1u;
-            if (pid == 0 && p.l2_prefetch_bytes && !mbar_try_wait(&s.empty[slot], par))
-                lookahead(lt0, lt1);
             if (!wait_mbar(p, &s.empty[slot], par)) {
                 ok = false;
                 return nullptr;
@@ -370,6 +353,7 @@ struct Producer {
 
     __device__ void gemv_chunk(int op, int layer, uint32_t r0, uint32_t nr) {
         stream_bytes += (unsigned long long)nr * op_in_dim(p.g, op) * 2u * op_mats(op);
+        if (pid == 0) st_volatile_u64(&s.ctl->stream_pos, stream_bytes);
         if (!owns(j)) {
             ++j;
             return;
@@ -450,8 +434,6 @@ struct Producer {
     __device__ __forceinline__ void run(int cta) {
         const Geom &g = p.g;
         const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
-        lt0 = t0;
-        lt1 = t1;
         fence_proxy_async_global();
         for (int st = 0; st < p.n_steps && ok; ++st) {
             const int P = p.pos0 + st;
@@ -489,6 +471,7 @@ struct Producer {
                 }
             }
         }
+        if (pid == 0) st_volatile_u64(&s.ctl->stream_pos, ~0ull);  // releases the prefetch warp
         // drain: wait for every copy still in flight so no bulk copy outlives the CTA
         const uint32_t ns = (uint32_t)g.ring_slots;
         uint32_t first = j > ns ? j - ns : 0;
@@ -497,6 +480,103 @@ struct Producer {
             unsigned long long t0n = global_timer();
             while (!mbar_try_wait(&s.full[k % ns], (k / ns) & 1u)) {
                 if (global_timer() - t0n > p.timeout_ns) break;
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------ L2 prefetch warp
+// Keeps HBM streaming while the ring is full and the consumers wait on a
+// dependency. The warp walks this CTA's tasks in the producers' order and
+// prefetches into L2, one 128-byte line per lane, the weight rows of each GEMV
+// tile and the cached K/V of each attention tile, at most l2_prefetch_bytes of
+// weights ahead of what the producers have handed to the ring. Issue is paced
+// (a token bucket in global-timer nanoseconds) so the warp does not queue more
+// requests than this SM's share of HBM bandwidth drains. It never makes the
+// kernel wait: when the producers finish or anything fails, it stops.
+struct Prefetcher {
+    const KernelParams &p;
+    Smem &s;
+    const int lane;
+    unsigned long long next_ns = 0;
+
+    __device__ Prefetcher(const KernelParams &p_, Smem &s_) : p(p_), s(s_), lane(threadIdx.x & 31) {}
+
+    // false: stop prefetching (failure, or the producers stopped moving)
+    __device__ bool wait_window(unsigned long long pos) {
+        if (pos < ld_volatile_u64(&s.ctl->stream_pos) + p.l2_prefetch_bytes) return true;
+        const unsigned long long t0 = global_timer();
+        for (uint32_t spin = 1;; ++spin) {
+            __nanosleep(64);
+            const unsigned long long sp = ld_volatile_u64(&s.ctl->stream_pos);
+            if (sp == ~0ull) return false;
+            if (pos < sp + p.l2_prefetch_bytes) return true;
+            if ((spin & 63u) == 0 && (failed(p) || global_timer() - t0 > p.timeout_ns)) return false;
+        }
+    }
+
+    // lines [a, a + bytes) of one range, 4 KB per warp instruction
+    __device__ bool range(const uint8_t *a, unsigned long long bytes, unsigned long long pos) {
+        for (unsigned long long off = 0; off < bytes; off += 4096) {
+            if (!wait_window(pos + off)) return false;
+            if (p.l2_prefetch_ns_per_4k) {
+                unsigned long long now = global_timer();
+                const unsigned long long floor = now > 8ull * p.l2_prefetch_ns_per_4k ? now - 8ull * p.l2_prefetch_ns_per_4k : 0ull;
+                if (next_ns < floor) next_ns = floor;  // at most 32 KB of burst credit
+                while (now < next_ns) now = global_timer();
+                next_ns += p.l2_prefetch_ns_per_4k;
+            }
+            const unsigned long long o = off + (unsigned long long)lane * 128u;
+            if (o < bytes) prefetch_l2(a + o);
+        }
+        return true;
+    }
+
+    __device__ void run(int cta) {
+        const Geom &g = p.g;
+        const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
+        unsigned long long pos = 0;  // weight bytes of the tasks walked so far
+        for (int st = 0; st < p.n_steps; ++st) {
+            const int P = p.pos0 + st;
+            for (int ti = t0; ti < t1; ++ti) {
+                const tiles_task t = p.tasks[ti];
+                if (failed(p)) return;
+                if (op_is_gemv(t.op)) {
+                    const unsigned long long rb = (unsigned long long)op_in_dim(g, t.op) * 2u * op_mats(t.op);
+                    const unsigned long long bytes = (unsigned long long)(t.end - t.begin) * rb;
+                    const unsigned long long sp = ld_volatile_u64(&s.ctl->stream_pos);
+                    if (sp == ~0ull) return;
+                    // skip what the producers already handed to the ring
+                    unsigned long long skip = sp > pos ? (sp - pos) & ~4095ull : 0ull;
+                    if (skip < bytes) {
+                        const LayerPtrs &lw = p.layers[t.layer];
+                        const uint16_t *src;
+                        switch (t.op) {
+                            case TILES_OP_QKV: src = lw.wqkv; break;
+                            case TILES_OP_OPROJ: src = lw.wo; break;
+                            case TILES_OP_GATEUP: src = lw.wgu; break;
+                            case TILES_OP_DOWN: src = lw.w_down; break;
+                            default: src = p.embed; break;
+                        }
+                        const uint8_t *a = reinterpret_cast<const uint8_t *>(src) + (size_t)t.begin * rb;
+                        if (!range(a + skip, bytes - skip, pos + skip)) return;
+                    }
+                    pos += bytes;
+                } else if (t.op == TILES_OP_ATTN) {
+                    // cached positions only: position P is written in this step
+                    for (uint32_t it = t.begin; it < t.end; ++it) {
+                        const int h = (int)(it / (uint32_t)g.kv_splits);
+                        int b0, b1;
+                        attn_split_blocks(g, P + 1, (int)(it % (uint32_t)g.kv_splits), &b0, &b1);
+                        int q0 = b0 * g.kv_block, q1 = b1 * g.kv_block;
+                        if (q1 > P) q1 = P;
+                        if (q1 <= q0) continue;
+                        const size_t off = ((size_t)(t.layer * g.nkv + h) * g.max_pos + q0) * g.d;
+                        const unsigned long long n = (unsigned long long)(q1 - q0) * g.d * 2u;
+                        if (!range(reinterpret_cast<const uint8_t *>(p.k_cache + off), n, pos)) return;
+                        if (!range(reinterpret_cast<const uint8_t *>(p.v_cache + off), n, pos)) return;
+                    }
+                }
             }
         }
     }
@@ -551,6 +631,23 @@ __device__ __forceinline__ void gemv_rows_n(uint32_t nr, const uint8_t *slot, co
         case 6: gemv_rows<MATS, 6>(slot, vec, nu4, row_bytes, rpc, res); break;
         case 7: gemv_rows<MATS, 7>(slot, vec, nu4, row_bytes, rpc, res); break;
         default: gemv_rows<MATS, 8>(slot, vec, nu4, row_bytes, rpc, res); break;
+    }
+}
+
+// this lane's DPL elements (2 or 4 consecutive dims) of one bf16 V row
+template <int DPL>
+__device__ __forceinline__ void v_piece(const uint8_t *vrow, float (&vf)[DPL]) {
+    const int lane = threadIdx.x & 31;
+    if constexpr (DPL == 2) {
+        const uint32_t w = reinterpret_cast<const uint32_t *>(vrow)[lane];
+        vf[0] = bf_lo(w);
+        vf[1] = bf_hi(w);
+    } else {
+        const uint2 w = reinterpret_cast<const uint2 *>(vrow)[lane];
+        vf[0] = bf_lo(w.x);
+        vf[1] = bf_hi(w.x);
+        vf[2] = bf_lo(w.y);
+        vf[3] = bf_hi(w.y);
     }
 }
 
@@ -899,22 +996,26 @@ struct Consumer {
         for (int t0 = sb_first * 32; t0 < npos; t0 += sb_step * 32) {
             const int t = t0 + lane;
             const bool valid = t < npos;
-            float sc = 0.f;
+            // q . k over four independent partial sums (16-byte columns mod 4)
+            float sc4[4] = {0.f, 0.f, 0.f, 0.f};
             if (valid) {
                 const uint4 *krow = reinterpret_cast<const uint4 *>(Kb + (size_t)t * D * 2);
 #pragma unroll
                 for (int jj = 0; jj < NC; ++jj) {
-                    const int col = (jj + lane) & (NC - 1);
+                    const int col = (jj + lane) & (NC - 1);  // rotated: no bank conflicts
                     float kf[8];
                     unpack8(krow[col], kf);
                     const float4 qa = reinterpret_cast<const float4 *>(q + col * 8)[0];
                     const float4 qb = reinterpret_cast<const float4 *>(q + col * 8)[1];
+                    float sc = sc4[jj & 3];
                     sc = fmaf(kf[0], qa.x, sc); sc = fmaf(kf[1], qa.y, sc);
                     sc = fmaf(kf[2], qa.z, sc); sc = fmaf(kf[3], qa.w, sc);
                     sc = fmaf(kf[4], qb.x, sc); sc = fmaf(kf[5], qb.y, sc);
                     sc = fmaf(kf[6], qb.z, sc); sc = fmaf(kf[7], qb.w, sc);
+                    sc4[jj & 3] = sc;
                 }
             }
+            const float sc = __fadd_rn(__fadd_rn(sc4[0], sc4[1]), __fadd_rn(sc4[2], sc4[3]));
             const float si = valid ? sc * p.attn_scale : -INFINITY;
             const float bm = warp_max(si);
             const float mn = fmaxf(m, bm);
@@ -923,26 +1024,36 @@ struct Consumer {
             const float ps = warp_sum(pi);
             l = fmaf(l, corr, ps);
             m = mn;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) o[e] *= corr;
             prob[lane] = pi;
             __syncwarp();
+            // p . V over the block's positions, four positions in flight
             const int nv = npos - t0 < 32 ? npos - t0 : 32;
-            for (int tt = 0; tt < nv; ++tt) {
-                const float pv = prob[tt];
-                const uint8_t *vrow = Vb + (size_t)(t0 + tt) * D * 2;
-                if (DPL == 2) {
-                    const uint32_t w = reinterpret_cast<const uint32_t *>(vrow)[lane];
-                    o[0] = fmaf(pv, bf_lo(w), o[0]);
-                    o[DPL > 1 ? 1 : 0] = fmaf(pv, bf_hi(w), o[DPL > 1 ? 1 : 0]);
-                } else {
-                    const uint2 w = reinterpret_cast<const uint2 *>(vrow)[lane];
-                    o[0] = fmaf(pv, bf_lo(w.x), o[0]);
-                    o[1] = fmaf(pv, bf_hi(w.x), o[1]);
-                    o[DPL > 2 ? 2 : 0] = fmaf(pv, bf_lo(w.y), o[DPL > 2 ? 2 : 0]);
-                    o[DPL > 3 ? 3 : 1] = fmaf(pv, bf_hi(w.y), o[DPL > 3 ? 3 : 1]);
+            float acc[4][DPL];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[u][e] = 0.f;
+            int tt = 0;
+            for (; tt + 4 <= nv; tt += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float vf[DPL];
+                    v_piece<DPL>(Vb + (size_t)(t0 + tt + u) * D * 2, vf);
+                    const float pv = prob[tt + u];
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) acc[u][e] = fmaf(pv, vf[e], acc[u][e]);
                 }
             }
+            for (; tt < nv; ++tt) {
+                float vf[DPL];
+                v_piece<DPL>(Vb + (size_t)(t0 + tt) * D * 2, vf);
+                const float pv = prob[tt];
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[0][e] = fmaf(pv, vf[e], acc[0][e]);
+            }
+#pragma unroll
+            for (int e = 0; e < DPL; ++e)
+                o[e] = fmaf(o[e], corr, __fadd_rn(__fadd_rn(acc[0][e], acc[1][e]), __fadd_rn(acc[2][e], acc[3][e])));
             __syncwarp();
         }
     }
@@ -1074,67 +1185,102 @@ struct Consumer {
             }
             // wstate is reused by the next item; leave together on any failure
             if (consumer_sync_or(bad)) return;
-            // arrival of this split; the last of the S splits of head h merges them
-            // (release: fence then atomic; acquire: atomic then fence)
-            if (tid == 0) {
-                __threadfence();
-                const uint32_t old =
-                    atomicAdd(p.attn_arrive + (size_t)(cur_layer * g.nkv + h) * kCounterStride, 1u);
-                const bool last = old + 1u == (uint32_t)g.kv_splits * (uint32_t)(step + 1);
-                if (last) __threadfence();
-                s.ctl->merge = last ? 1 : 0;
-            }
-            consumer_sync();
-            if (s.ctl->merge) {
-                merge_heads(h * G, (h + 1) * G);
-                consumer_sync();
-                if (tid == 0 && p.attn_head_signals) {
-                    __threadfence();
-                    red_release_add(p.counters + (size_t)t.signal_ctr * kCounterStride, 1u);
-                }
-            }
         }
     }
 
-    // Merge the split partials of q heads [h0, h1), in split order:
-    //   M = max_c m_c, w_c = e^(m_c - M), out = sum_c w_c o_c / sum_c w_c l_c.
-    // Three stages so the L2 reads go out in parallel: split maxima and sums to
-    // shared memory, one thread per head for the weights, then every output
-    // element with its S independent loads.
-    __device__ void merge_heads(int h0, int h1) {
+    // O-proj prologue: vec <- bf16 attention output of every q head, merged
+    // from the S split partials in split order:
+    //   M = max_c m_c, w_c = e^(m_c - M), o = sum_c w_c o_c / sum_c w_c l_c.
+    // Every O-proj tile merges all heads itself, straight from the partials, so
+    // no tile waits on another tile's merge. Per group of heads: split maxima
+    // and sums to shared memory, one thread per head for the weights, then
+    // every output element with its S independent loads.
+    // The same merge with S known at compile time: a thread takes 4 dims of
+    // one head and issues all its loads (S maxima, S sums, S 16-byte pieces of
+    // o) at once, so the whole prologue costs about one L2 round trip per
+    // group of outputs instead of one per split batch.
+    template <int S>
+    __device__ void merge_to_vec_fixed() {
         const Geom &g = p.g;
-        const int D = g.d, S = g.kv_splits, nh = h1 - h0;
-        const AttnSmem a = attn_smem();
-        float *ms = a.wstate;              // [nh][S] split maxima, then weights
-        float *ls = ms + (size_t)nh * S;   // [nh][S] split sums
-        float *Ls = ls + (size_t)nh * S;   // [nh] merged sums
-        const float *base = p.partials + (size_t)h0 * S * (kPartialPad + D);
-        for (int idx = tid; idx < nh * S; idx += kConsumerWarps * 32) {
-            ms[idx] = __ldcg(&base[(size_t)idx * (kPartialPad + D)]);
-            ls[idx] = __ldcg(&base[(size_t)idx * (kPartialPad + D) + 1]);
-        }
-        consumer_sync();
-        if (tid < nh) {
-            float M = -INFINITY;
-            for (int c = 0; c < S; ++c) M = fmaxf(M, ms[tid * S + c]);
-            float L = 0.f;
+        const int D = g.d, q4 = D / 4, n = g.nq * q4;
+        uint16_t *out = reinterpret_cast<uint16_t *>(s.vec);
+        for (int idx = tid; idx < n; idx += kConsumerWarps * 32) {
+            const int i = idx / q4, k = idx % q4;
+            const float *hb = p.partials + (size_t)i * S * (kPartialPad + D);
+            float mc[S], lc[S];
+            float4 oc[S];
+#pragma unroll
             for (int c = 0; c < S; ++c) {
-                const float mc = ms[tid * S + c];
-                const float w = mc == -INFINITY ? 0.f : expf(mc - M);
-                ms[tid * S + c] = w;
-                L = fmaf(w, ls[tid * S + c], L);
+                const float *pc = hb + (size_t)c * (kPartialPad + D);
+                mc[c] = __ldcg(pc);
+                lc[c] = __ldcg(pc + 1);
+                oc[c] = __ldcg(reinterpret_cast<const float4 *>(pc + kPartialPad) + k);
             }
-            Ls[tid] = L;
+            float M = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < S; ++c) M = fmaxf(M, mc[c]);
+            float L = 0.f;
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < S; ++c) {
+                const float w = mc[c] == -INFINITY ? 0.f : expf(mc[c] - M);
+                L = fmaf(w, lc[c], L);
+                O.x = fmaf(w, oc[c].x, O.x);
+                O.y = fmaf(w, oc[c].y, O.y);
+                O.z = fmaf(w, oc[c].z, O.z);
+                O.w = fmaf(w, oc[c].w, O.w);
+            }
+            const uint32_t lo = (uint32_t)f2bf(__fdiv_rn(O.x, L)) | ((uint32_t)f2bf(__fdiv_rn(O.y, L)) << 16);
+            const uint32_t hi = (uint32_t)f2bf(__fdiv_rn(O.z, L)) | ((uint32_t)f2bf(__fdiv_rn(O.w, L)) << 16);
+            reinterpret_cast<uint2 *>(out + (size_t)i * D)[k] = make_uint2(lo, hi);
         }
-        consumer_sync();
-        for (int idx = tid; idx < nh * D; idx += kConsumerWarps * 32) {
-            const int i = idx / D, dd = idx % D;
-            const float *pc = base + (size_t)i * S * (kPartialPad + D) + kPartialPad + dd;
-            const float *wi = ms + (size_t)i * S;
-            float O = 0.f;
+    }
+
+    __device__ void merge_to_vec() {
+        switch (p.g.kv_splits) {  // the split counts the default plans pick
+            case 8: merge_to_vec_fixed<8>(); return;
+            case 9: merge_to_vec_fixed<9>(); return;
+            case 17: merge_to_vec_fixed<17>(); return;
+            case 19: merge_to_vec_fixed<19>(); return;
+            default: break;
+        }
+        const Geom &g = p.g;
+        const int D = g.d, S = g.kv_splits;
+        float *ms = reinterpret_cast<float *>(s.vec + g.merge_off);
+        uint16_t *out = reinterpret_cast<uint16_t *>(s.vec);
+        for (int h0 = 0; h0 < g.nq; h0 += g.merge_heads) {
+            const int nh = g.nq - h0 < g.merge_heads ? g.nq - h0 : g.merge_heads;
+            float *ls = ms + (size_t)nh * S;   // [nh][S] split sums
+            float *Ls = ls + (size_t)nh * S;   // [nh] merged sums
+            const float *base = p.partials + (size_t)h0 * S * (kPartialPad + D);
+            if (h0 > 0) consumer_sync();       // the previous group is done with the scratch
+            for (int idx = tid; idx < nh * S; idx += kConsumerWarps * 32) {
+                ms[idx] = __ldcg(&base[(size_t)idx * (kPartialPad + D)]);
+                ls[idx] = __ldcg(&base[(size_t)idx * (kPartialPad + D) + 1]);
+            }
+            consumer_sync();
+            for (int i = tid; i < nh; i += kConsumerWarps * 32) {
+                float M = -INFINITY;
+                for (int c = 0; c < S; ++c) M = fmaxf(M, ms[i * S + c]);
+                float L = 0.f;
+                for (int c = 0; c < S; ++c) {
+                    const float mc = ms[i * S + c];
+                    const float w = mc == -INFINITY ? 0.f : expf(mc - M);
+                    ms[i * S + c] = w;
+                    L = fmaf(w, ls[i * S + c], L);
+                }
+                Ls[i] = L;
+            }
+            consumer_sync();
+            for (int idx = tid; idx < nh * D; idx += kConsumerWarps * 32) {
+                const int i = idx / D, dd = idx % D;
+                const float *pc = base + (size_t)i * S * (kPartialPad + D) + kPartialPad + dd;
+                const float *wi = ms + (size_t)i * S;
+                float O = 0.f;
 #pragma unroll 4
-            for (int c = 0; c < S; ++c) O = fmaf(wi[c], __ldcg(&pc[(size_t)c * (kPartialPad + D)]), O);
-            __stcg(&p.o[(size_t)(h0 + i) * D + dd], f2bf(__fdiv_rn(O, Ls[i])));
+                for (int c = 0; c < S; ++c) O = fmaf(wi[c], __ldcg(&pc[(size_t)c * (kPartialPad + D)]), O);
+                out[(size_t)(h0 + i) * D + dd] = f2bf(__fdiv_rn(O, Ls[i]));
+            }
         }
     }
 
@@ -1194,7 +1340,7 @@ struct Consumer {
                         attn_dispatch(t);
                         break;
                     case TILES_OP_OPROJ:
-                        copy_to_vec(p.o, g.qd);
+                        merge_to_vec();
                         load_residual(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : p.x, t.begin, t.end);
                         consumer_sync();
                         gemv_task<1>(t);
@@ -1221,9 +1367,7 @@ struct Consumer {
                 // ---- publish
                 if (consumer_sync_or(bad)) return;
                 if (tr) tr[kTrTaskEnd] = global_timer();
-                if (tid == 0 && t.signal_ctr != TILES_NO_COUNTER &&
-                    !(t.op == TILES_OP_ATTN && p.attn_head_signals)) {
-                    __threadfence();
+                if (tid == 0 && t.signal_ctr != TILES_NO_COUNTER) {
                     red_release_add(p.counters + (size_t)t.signal_ctr * kCounterStride, 1u);
                 }
             }
@@ -1254,10 +1398,17 @@ __global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_con
         s.ctl->unused = 0;
         s.ctl->token = 0;
         s.ctl->step_ready = 0;
-        s.ctl->merge = 0;
+        s.ctl->stream_pos = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    if (tid >= (kConsumerWarps + kProducerWarps) * 32) {
+        if (p.l2_prefetch_bytes) {
+            Prefetcher pf(p, s);
+            pf.run(blockIdx.x);
+        }
+        return;
+    }
     if (tid >= kConsumerWarps * 32) {
         if ((tid & 31) == 0) {
             Producer prod(p, s, (tid >> 5) - kConsumerWarps);
@@ -1320,17 +1471,17 @@ __global__ void barrier_kernel(uint32_t *ctr, int rounds, unsigned long long *el
     for (int r = 0; r < rounds; ++r) {
         __syncthreads();
         if (threadIdx.x == 0) {
-            __threadfence();
             red_release_add(ctr, 1u);
             const uint32_t target = n * (uint32_t)(r + 1);
             unsigned long long ts = global_timer();
-            while (ld_acquire(ctr) < target) {
+            while (ld_relaxed(ctr) < target) {
                 if (global_timer() - ts > timeout_ns) {
                     atomicOr(status, kDevTimeout);
                     abort_flag = 1;
                     break;
                 }
             }
+            fence_acquire_gpu();
         }
         __syncthreads();
         if (abort_flag) return;

@@ -112,12 +112,13 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     if (splits < 1 || splits > 4096) return fail(TILES_ERR_INVALID_ARG, "kv_splits");
     G_.kv_splits = splits;
 
-    // the split merge keeps 2 * G * S + G floats in the per-warp state area
-    int merge_need = (2 * G * splits + G) * 4;
-    int attn_need = attn_vec_bytes(G, G_.d);
-    int wstate_off = G * G_.d * 4 + 2 * G_.d * 2 + kConsumerWarps * 32 * G * 4;
-    if (wstate_off + merge_need > attn_need) attn_need = wstate_off + merge_need;
-    int vec = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, attn_need});
+    // the O-proj prologue merges the split partials into the input vector, a
+    // group of q heads at a time: 2 S + 1 floats of scratch per head, after it
+    const int per_head = (2 * splits + 1) * 4;
+    G_.merge_off = round_up(2 * G_.qd, 16);
+    G_.merge_heads = std::max(1, std::min(G_.nq, 16384 / per_head));
+    int vec = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, attn_vec_bytes(G, G_.d),
+                        G_.merge_off + G_.merge_heads * per_head});
     // residual rows of an O-proj / down tile follow (a tile has at most H rows)
     G_.res_off = round_up(vec, 16);
     G_.vec_bytes = round_up(G_.res_off + 2 * G_.H, 128);
@@ -286,11 +287,9 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
             prev[phi] = p;
             if (!phase_tasks[phi].empty()) p = phi;
         }
-        // signals per step: one per task, except the attention phase, which the
-        // merging tile of each KV head signals once (n_kv per step)
+        // signals per step: one per task
         auto per_step = [&](int phi) -> uint32_t {
-            if (phi < 0) return 0;
-            return phase_op[phi] == TILES_OP_ATTN ? (uint32_t)g.nkv : (uint32_t)phase_tasks[phi].size();
+            return phi < 0 ? 0u : (uint32_t)phase_tasks[phi].size();
         };
         for (int phi = 0; phi < PPS; ++phi) {
             int pp = prev[phi];
@@ -352,7 +351,6 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
     std::vector<std::vector<std::pair<uint32_t, uint32_t>>> cover(PPS);
     std::vector<int> phase_op(PPS, 0);
     std::vector<std::vector<int>> sig_by_phase(PPS, std::vector<int>(s.n_counters, 0));
-    std::vector<int> attn_sig(PPS, -1);
     for (int c = 0; c < N; ++c) {
         int last_phi = -1;
         for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i) {
@@ -374,14 +372,7 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
             }
             if (t.signal_ctr != TILES_NO_COUNTER) {
                 if (t.signal_ctr >= s.n_counters) return fail("signal counter out of range");
-                if (t.op == TILES_OP_ATTN && s.scheduler == TILES_SCHED_COUNTERS) {
-                    // counted once per phase below: n_kv merges per step
-                    int &seen = attn_sig[phi];
-                    if (seen == -1) seen = t.signal_ctr;
-                    else if (seen != (int)t.signal_ctr) return fail("attention tiles signal different counters");
-                } else {
-                    sig_by_phase[phi][t.signal_ctr] += 1;
-                }
+                sig_by_phase[phi][t.signal_ctr] += 1;
             }
             if (t.wait_ctr != TILES_NO_COUNTER && t.wait_ctr >= s.n_counters)
                 return fail("wait counter out of range");
@@ -411,8 +402,6 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
             return TILES_ERR_PLAN_INVALID;
         }
     }
-    for (int phi = 0; phi < PPS; ++phi)
-        if (attn_sig[phi] >= 0) sig_by_phase[phi][attn_sig[phi]] += g.nkv;
     // signals per step on each counter; per CTA, the counter its last task of each phase signals
     std::vector<long long> per_step(s.n_counters, 0);
     for (int phi = 0; phi < PPS; ++phi)

@@ -149,6 +149,7 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
     // L2 lookahead is off unless asked for: on GB300 it competes with the ring
     // copies for the TMA unit and measured slower at every distance tried
     p.l2_prefetch_bytes = o.l2_prefetch_kb > 0 ? (unsigned long long)o.l2_prefetch_kb * 1024ull : 0ull;
+    p.l2_prefetch_ns_per_4k = o.l2_prefetch_gbs > 0 ? (4096ull + (unsigned)o.l2_prefetch_gbs - 1) / (unsigned)o.l2_prefetch_gbs : 0ull;
     p.ring_off = kCtlBytes;
     p.vec_off = kCtlBytes + g.ring_slots * g.slot_bytes;
     p.res_off = g.res_off;
@@ -221,20 +222,16 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
     // scratch
     if ((e = dalloc(plan, &p.qkv, (size_t)g.qkv_rows * 4)) != cudaSuccess) return fail(e);
     if ((e = dalloc(plan, &p.partials, (size_t)g.nq * g.kv_splits * (kPartialPad + g.d) * 4)) != cudaSuccess) return fail(e);
-    if ((e = dalloc(plan, &p.o, (size_t)g.qd * 2)) != cudaSuccess) return fail(e);
     if ((e = dalloc(plan, &p.x, (size_t)g.H * 2)) != cudaSuccess) return fail(e);
     if ((e = dalloc(plan, &p.a, (size_t)g.F * 2)) != cudaSuccess) return fail(e);
-    // one memset per launch clears: argmax keys | phase counters | split arrivals
+    // one memset per launch clears: argmax keys | phase counters
     const size_t ctr_bytes = (size_t)plan->sched.n_counters * kCounterStride * 4;
-    const size_t arrive_bytes = (size_t)g.L * g.nkv * kCounterStride * 4;
-    plan->sync_bytes = kMaxStepsPerLaunch * 8 + ctr_bytes + arrive_bytes;
+    plan->sync_bytes = kMaxStepsPerLaunch * 8 + ctr_bytes;
     uint8_t *sync;
     if ((e = dalloc(plan, &sync, plan->sync_bytes)) != cudaSuccess) return fail(e);
     plan->d_keys = reinterpret_cast<unsigned long long *>(sync);
     p.keys = plan->d_keys;
     p.counters = reinterpret_cast<uint32_t *>(sync + kMaxStepsPerLaunch * 8);
-    p.attn_arrive = reinterpret_cast<uint32_t *>(sync + kMaxStepsPerLaunch * 8 + ctr_bytes);
-    p.attn_head_signals = plan->sched.scheduler == TILES_SCHED_COUNTERS ? 1 : 0;
     if ((e = dalloc(plan, &p.status, 16)) != cudaSuccess) return fail(e);
     if ((e = cudaMemset(p.status, 0, 16)) != cudaSuccess) return fail(e);
     if ((e = dalloc(plan, &plan->d_prompt_stage, (size_t)g.max_pos * 4)) != cudaSuccess) return fail(e);
@@ -478,11 +475,10 @@ extern "C" tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache,
     if (n_new > 0 && !out_tokens) return TILES_ERR_INVALID_ARG;
     if (!aligned16(k_cache) || !aligned16(v_cache)) return TILES_ERR_INVALID_ARG;
     const Geom &g = plan->sched.geom;
-    // layout in the array: sync block (zeroed per launch) | qkv | partials | o | x | a
+    // layout in the array: sync block (zeroed per launch) | qkv | partials | x | a
     const size_t off_qkv = align256(plan->sync_bytes);
     const size_t off_part = off_qkv + align256((size_t)g.qkv_rows * 4);
-    const size_t off_o = off_part + align256((size_t)g.nq * g.kv_splits * (kPartialPad + g.d) * 4);
-    const size_t off_x = off_o + align256((size_t)g.qd * 2);
+    const size_t off_x = off_part + align256((size_t)g.nq * g.kv_splits * (kPartialPad + g.d) * 4);
     const size_t off_a = off_x + align256((size_t)g.H * 2);
     const size_t need = off_a + align256((size_t)g.F * 2);
     if (need > kNoAllocScratchBytes) return TILES_ERR_CAPACITY;
@@ -493,14 +489,11 @@ extern "C" tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache,
     if (st != TILES_OK) return st;
     unsigned char *base = nullptr;
     if ((st = noalloc_scratch(plan->device, &base)) != TILES_OK) return st;
-    const size_t ctr_bytes = (size_t)plan->sched.n_counters * kCounterStride * 4;
     KernelParams p = plan->base;
     p.keys = reinterpret_cast<unsigned long long *>(base);
     p.counters = reinterpret_cast<uint32_t *>(base + kMaxStepsPerLaunch * 8);
-    p.attn_arrive = reinterpret_cast<uint32_t *>(base + kMaxStepsPerLaunch * 8 + ctr_bytes);
     p.qkv = reinterpret_cast<float *>(base + off_qkv);
     p.partials = reinterpret_cast<float *>(base + off_part);
-    p.o = reinterpret_cast<uint16_t *>(base + off_o);
     p.x = reinterpret_cast<uint16_t *>(base + off_x);
     p.a = reinterpret_cast<uint16_t *>(base + off_a);
     p.k_cache = reinterpret_cast<uint16_t *>(k_cache);

@@ -19,7 +19,8 @@ namespace tiles {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kProducerWarps = 2;  // lane 0 of each issues the copies of every other ring slot
-constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
+constexpr int kPrefetchWarps = 1;
+constexpr int kThreads = (kConsumerWarps + kProducerWarps + kPrefetchWarps) * 32;
 constexpr int kMaxRowsPerChunk = 8;                   // GEMV rows a warp handles per chunk
 constexpr int kMaxSlots = 32;
 constexpr int kSmemLimit = 232448;                    // 227 KB dynamic shared memory per CTA
@@ -40,6 +41,8 @@ struct Geom {
     int rpc_qkv, rpc_o, rpc_gateup, rpc_down, rpc_lm;
     int vec_bytes;  // shared-memory region for the input vector / attention scratch
     int res_off;    // in the vec region: residual rows of an O-proj / down tile
+    int merge_off;    // in the vec region: split-merge scratch of the O-proj prologue
+    int merge_heads;  // q heads that prologue merges per pass (2 S + 1 floats each)
     int smem_bytes;
 };
 
@@ -175,12 +178,9 @@ struct KernelParams {
     // caches and scratch
     uint16_t *k_cache, *v_cache;
     float *qkv, *partials;
-    uint16_t *o, *x, *a;
+    uint16_t *x, *a;
     unsigned long long *keys;
     uint32_t *counters, *status;
-    // per (layer, kv head) arrivals of split tiles; the last one merges the splits
-    uint32_t *attn_arrive;
-    int attn_head_signals;  // 1: the merging tile signals the attention counter (counter chains)
     // run
     const int32_t *prompt;
     int n_prompt, step0, pos0, n_steps;
@@ -188,6 +188,7 @@ struct KernelParams {
     float *out_logits;
     unsigned long long timeout_ns;
     unsigned long long l2_prefetch_bytes;  // L2 lookahead of the weight stream per CTA (0: off)
+    unsigned long long l2_prefetch_ns_per_4k;  // pacing of the prefetch warp (0: unpaced)
     int vec_off, ring_off, res_off;
     // optional per-task timeline: [cta][step < trace_steps][task][kTraceWords]
     unsigned long long *trace;
