@@ -10,7 +10,7 @@ kernel); each call rewrites positions 1023..1086, so repeats are identical and
 are checked bit for bit.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
-                  [--scheduler counters|waves] [--impl ours|reference] [--tokens T]
+                  [--scheduler counters|waves|flags|all] [--impl ours|reference] [--tokens T]
 
 With N > 1 (launched by torchrun) every rank runs an independent replica: a
 batch-1 decode has no exchange step to shard (replicas only). `--impl
@@ -35,6 +35,9 @@ sys.path.insert(0, ROOT)
 METRIC = "batch-1 decode tok/s on 1 GB300; % of HBM roofline (weight+KV bytes/token)"
 UNIT = "tok/s"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "megakernel_traffic.json")
+
+
+SCHEDULERS = {"counters": 1, "waves": 0, "flags": 2}   # tiles_plan_opts.scheduler values
 
 
 def log(*a):
@@ -267,10 +270,10 @@ def run_ours(args):
 
     bytes_per_token = cfg.algorithmic_bytes_per_token()
     results = {}
-    scheds = ["counters", "waves"] if args.scheduler == "both" else [args.scheduler]
+    scheds = list(SCHEDULERS) if args.scheduler == "all" else [args.scheduler]
     for sname in scheds:
         plan = tsp.Plan(tsp.ModelDesc.from_config(cfg), dw,
-                        tsp.make_opts(scheduler=tsp.SCHED_COUNTERS if sname == "counters" else tsp.SCHED_WAVES))
+                        tsp.make_opts(scheduler=SCHEDULERS[sname]))
         info = plan.info()
         toks = torch.zeros(cfg.n_new, dtype=torch.int32, device="cuda")
         ref_toks = None
@@ -381,7 +384,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="llama1b")
-    ap.add_argument("--scheduler", default="both", choices=["counters", "waves", "both"])
+    ap.add_argument("--scheduler", default="all", choices=["counters", "waves", "flags", "all"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=2,
                     help="oracle decode tokens per timed step (CPU arms)")

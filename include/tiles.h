@@ -87,14 +87,24 @@ typedef struct {
     const tiles_layer_weights *layers;
 } tiles_weights;
 
-enum { TILES_SCHED_WAVES = 0, TILES_SCHED_COUNTERS = 1 };
+/* How tiles wait for their inputs.
+ *  WAVES: every phase ends in a grid barrier (a counter all CTAs arrive on).
+ *  COUNTERS: a tile waits on the dependency counter of the phase it reads,
+ *    which every tile of that phase increments once done.
+ *  FLAGS: activations carry their own readiness. Each word of the residual
+ *    stream, the SwiGLU output and the Q/K/V projection holds the value and
+ *    the tag of the (step, layer, phase) that wrote it, and a tile polls the
+ *    words it reads until they carry the tag it expects. The split-KV partials
+ *    and the sampled token still go through counters.
+ * All three compute bit-identical results. */
+enum { TILES_SCHED_WAVES = 0, TILES_SCHED_COUNTERS = 1, TILES_SCHED_FLAGS = 2 };
 
 /* Planner options; pass NULL to tiles_plan_create for the defaults (shown). */
 typedef struct {
-    int32_t scheduler;    /* TILES_SCHED_COUNTERS (default) or TILES_SCHED_WAVES        */
+    int32_t scheduler;    /* TILES_SCHED_FLAGS (default), _COUNTERS or _WAVES            */
     int32_t n_ctas;       /* 0 = one worker CTA per SM                                  */
-    int32_t slot_bytes;   /* 0 = auto (32 KB or the longest row): ring slot bytes, mult. of 1024 */
-    int32_t ring_slots;   /* 0 = as many as fit in shared memory                         */
+    int32_t slot_bytes;   /* 0 = auto (16 KB or the longest row): ring slot bytes, mult. of 1024 */
+    int32_t ring_slots;   /* 0 = one per consumer warp (8), fewer if they do not fit     */
     int32_t kv_splits;    /* 0 = auto: split-KV ranges per KV head                       */
     int32_t timeout_ms;   /* bound on every in-kernel wait; 0 = 2000 ms                  */
     int32_t l2_prefetch_kb; /* L2 prefetch warp: weight bytes it may run ahead of the ring, KB per CTA; <= 0 = off */

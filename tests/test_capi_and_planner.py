@@ -47,7 +47,7 @@ def _sched(name="llama1b", n=152, **opts):
 
 
 @pytest.mark.parametrize("name", list(S.CONFIGS))
-@pytest.mark.parametrize("scheduler", [0, 1])
+@pytest.mark.parametrize("scheduler", [0, 1, 2])
 def test_schedules_validate_and_balance(name, scheduler):
     cfg = S.CONFIGS[name]
     s = _sched(name, scheduler=scheduler)
@@ -73,7 +73,7 @@ def test_weight_rows_balanced_to_one_row_per_phase():
 
 
 def _mutate_and_expect(mutator, expect):
-    s = _sched("tiny", n=16)
+    s = _sched("tiny", n=16, scheduler=1)   # the counters schedule: every tile waits
     tasks, off = s.tasks()
     mutator(tasks, off)
     st, why = s.validate()
@@ -106,6 +106,53 @@ def test_rejects_wait_on_a_later_phase():
         t = tasks[off[2] + 1]
         t.wait_ctr = (t.signal_ctr + 1) % 13     # a counter signalled after this phase
     _mutate_and_expect(m, "wait")
+
+
+def test_flags_schedule_waits_only_where_inputs_are_untagged():
+    s = _sched("llama1b", scheduler=2)
+    tasks, off = s.tasks()
+    NO = 0xFFFF
+    for c in range(len(off) - 1):
+        for i in range(off[c], off[c + 1]):
+            t = tasks[i]
+            waits = t.op == 4 or (t.op == 1 and t.layer == 0)      # O-proj; first Q/K/V of a step
+            assert (t.wait_ctr != NO) == waits, (t.op, t.layer)
+            assert (t.signal_ctr != NO) == (t.op in (2, 7))          # attention and LM head signal
+
+
+def _mutate_flags_and_expect(mutator, expect):
+    s = _sched("tiny", n=16, scheduler=2)
+    tasks, off = s.tasks()
+    mutator(tasks, off)
+    st, why = s.validate()
+    assert st == -3, f"mutation accepted ({why})"
+    assert expect in why, why
+
+
+def test_flags_rejects_an_o_projection_that_does_not_wait():
+    def m(tasks, off):
+        for i in range(len(tasks)):
+            if tasks[i].op == 4:
+                tasks[i].wait_ctr = 0xFFFF
+                return
+    _mutate_flags_and_expect(m, "without a wait")
+
+
+def test_flags_rejects_an_attention_tile_that_does_not_signal():
+    def m(tasks, off):
+        for i in range(len(tasks)):
+            if tasks[i].op == 2:
+                tasks[i].signal_ctr = 0xFFFF
+                return
+    _mutate_flags_and_expect(m, "wait")
+
+
+def test_flags_rejects_a_layer_whose_attention_is_not_linked_to_the_next_step():
+    def m(tasks, off):
+        for i in range(len(tasks)):                          # no LM-head tile signals
+            if tasks[i].op == 7:
+                tasks[i].signal_ctr = 0xFFFF
+    _mutate_flags_and_expect(m, "")
 
 
 def test_rejects_out_of_range_layer_and_op():

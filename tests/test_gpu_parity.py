@@ -39,7 +39,7 @@ def tiny(tsp):
     return cfg, w, k, v, prompt, ref, rk, rv
 
 
-@pytest.mark.parametrize("scheduler", [0, 1], ids=["waves", "counters"])
+@pytest.mark.parametrize("scheduler", [0, 1, 2], ids=["waves", "counters", "flags"])
 def test_tiny_prompt_then_decode_matches_oracle(tsp, tiny, scheduler):
     cfg, w, k, v, prompt, ref, rk, rv = tiny
     plan = _plan(tsp, cfg, w, scheduler=scheduler)
@@ -66,7 +66,7 @@ def test_tiny_prompt_then_decode_matches_oracle(tsp, tiny, scheduler):
 def test_tiny_bitwise_reproducible_across_runs_and_schedulers(tsp, tiny):
     cfg, w, k, v, prompt, ref, *_ = tiny
     outs = []
-    for sched in (0, 1, 1, 0):
+    for sched in (0, 1, 2, 1, 2, 0):
         plan = _plan(tsp, cfg, w, scheduler=sched)
         outs.append(gpu_run(plan, cfg, k, v, prompt, 0, cfg.n_new))
         plan.close()
@@ -112,7 +112,7 @@ VARIANTS = {
 
 
 @pytest.mark.parametrize("name", list(VARIANTS))
-@pytest.mark.parametrize("scheduler", [0, 1], ids=["waves", "counters"])
+@pytest.mark.parametrize("scheduler", [0, 1, 2], ids=["waves", "counters", "flags"])
 def test_variants_match_oracle(tsp, name, scheduler):
     cfg = VARIANTS[name]
     w, k, v, prompt = inputs(cfg)

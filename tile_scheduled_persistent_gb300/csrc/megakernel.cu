@@ -114,6 +114,28 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
     return v;
 }
 __device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void st_relaxed_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4(const uint32_t *p) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
     uint32_t old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -251,6 +273,46 @@ __device__ __forceinline__ Smem smem_layout(uint8_t *base, const KernelParams &p
 }
 
 __device__ __forceinline__ bool failed(const KernelParams &p) { return ld_volatile(p.status) != 0; }
+
+// ------------------------------------------------------------------ tagged activations
+// Activation words carry the tag of the phase that wrote them:
+// 1 + 4 (step L + layer) + kind, with kind 0 for the Q/K/V rows, 1 for x after
+// the O-projection, 2 for the SwiGLU output a, 3 for x after the down
+// projection. The step is the launch's own (< 64), so within a launch no tag
+// repeats (at most 256 L < 2^16), and every launch starts from zeroed words,
+// so 0 never matches and nothing of an earlier launch reads as ready.
+enum { kTagQKV = 0, kTagXAttn = 1, kTagA = 2, kTagXFfn = 3 };
+__device__ __forceinline__ uint32_t act_tag(const KernelParams &p, int step, int layer, int kind) {
+    return 1u + 4u * ((uint32_t)step * (uint32_t)p.g.L + (uint32_t)layer) + (uint32_t)kind;
+}
+
+// Bounded polling of tagged words, like every other wait: the global timer
+// limits it, and a failure elsewhere ends it.
+struct Poll {
+    unsigned long long t0 = 0;
+    uint32_t spins = 0;
+    // false: stop polling (timeout recorded in the status word, or the run is aborting)
+    __device__ bool again(const KernelParams &p) {
+        if (t0 == 0) t0 = global_timer();
+        if ((++spins & 31u) == 0) {
+            if (failed(p)) return false;
+            if (global_timer() - t0 > p.timeout_ns) {
+                atomicOr(p.status, kDevTimeout);
+                return false;
+            }
+        }
+        return true;
+    }
+};
+
+__device__ __forceinline__ bool tags_ok4(const uint4 &w, uint32_t tag) {
+    return ((w.x >> 16) == tag) & ((w.y >> 16) == tag) & ((w.z >> 16) == tag) & ((w.w >> 16) == tag);
+}
+// the bf16 halves of 8 tagged words, packed as 8 consecutive bf16
+__device__ __forceinline__ uint4 untag8(const uint4 &lo, const uint4 &hi) {
+    return make_uint4(__byte_perm(lo.x, lo.y, 0x5410), __byte_perm(lo.z, lo.w, 0x5410),
+                      __byte_perm(hi.x, hi.y, 0x5410), __byte_perm(hi.z, hi.w, 0x5410));
+}
 
 __device__ __forceinline__ unsigned long long *trace_rec(const KernelParams &p, int cta, int step,
                                                          int task) {
@@ -697,9 +759,10 @@ struct Consumer {
     }
 
     // ---------------------------------------------------------- prologues
-    // vec <- bf16(rmsnorm(src) * gain), src bf16 [n <= 8192]; sum of squares in a
-    // fixed order, so every CTA computes the same scale. One pass over src: each
-    // thread keeps its (at most four) 16-byte pieces in registers.
+    // vec <- bf16(rmsnorm(src) * gain), src bf16 [n <= 8192] in global memory,
+    // or (src null) already in vec; sum of squares in a fixed order, so every
+    // CTA computes the same scale. One pass over src: each thread keeps its (at
+    // most four) 16-byte pieces in registers.
     __device__ void rmsnorm_to_vec(const uint16_t *src, const uint16_t *gain, int n) {
         constexpr int kMaxU = 4;
         const int nu4 = n >> 3;
@@ -709,7 +772,7 @@ struct Consumer {
         for (int k = 0; k < kMaxU; ++k) {
             const int c = tid + k * kConsumerWarps * 32;
             if (c < nu4) {
-                v[k] = __ldcg(reinterpret_cast<const uint4 *>(src) + c);
+                v[k] = src ? __ldcg(reinterpret_cast<const uint4 *>(src) + c) : reinterpret_cast<const uint4 *>(s.vec)[c];
                 float f[8];
                 unpack8(v[k], f);
 #pragma unroll
@@ -744,38 +807,85 @@ struct Consumer {
         }
     }
 
-    // residual rows [begin, end) of `base` into shared memory, for the epilogue
-    __device__ void load_residual(const uint16_t *base, uint32_t begin, uint32_t end) {
+    // residual rows [begin, end) into shared memory, for the epilogue: of the
+    // embedding row (first layer), else of the tagged x words carrying `tag`
+    __device__ void load_residual(const uint16_t *embed_row, uint32_t tag, uint32_t begin, uint32_t end) {
         uint16_t *res = reinterpret_cast<uint16_t *>(s.vec + p.res_off);
-        for (uint32_t r = begin + tid; r < end; r += kConsumerWarps * 32) res[r - begin] = __ldcg(&base[r]);
+        for (uint32_t r = begin + tid; r < end; r += kConsumerWarps * 32) {
+            if (embed_row) {
+                res[r - begin] = __ldcg(&embed_row[r]);
+                continue;
+            }
+            uint32_t w = ld_relaxed_u32(p.xw + r);
+            Poll pl;
+            while ((w >> 16) != tag) {
+                if (bad || !pl.again(p)) {
+                    bad = true;
+                    break;
+                }
+                w = ld_relaxed_u32(p.xw + r);
+            }
+            res[r - begin] = (uint16_t)(w & 0xFFFFu);
+        }
     }
 
-    __device__ void copy_to_vec(const uint16_t *src, int n) {
-        const int nu4 = n >> 3;
+    __device__ uint32_t tag(int layer, int kind) const { return act_tag(p, step, layer, kind); }
+
+    // vec[0, n) (bf16) <- the tagged words src[0, n), n a multiple of 8, each
+    // polled until it carries `tg`. First pass: four 8-word pieces per thread
+    // in flight, the ready ones stored; then the stale ones are polled.
+    __device__ void gather_tagged(const uint32_t *src, int n, uint32_t tg) {
+        constexpr int B = 4;
+        const int n8 = n >> 3;
         uint4 *dst = reinterpret_cast<uint4 *>(s.vec);
-        for (int c = tid; c < nu4; c += kConsumerWarps * 32)
-            dst[c] = __ldcg(reinterpret_cast<const uint4 *>(src) + c);
+        for (int c0 = tid; c0 < n8; c0 += B * kConsumerWarps * 32) {
+            uint32_t stale = 0;
+#pragma unroll
+            for (int k = 0; k < B; ++k) {
+                const int c = c0 + k * kConsumerWarps * 32;
+                if (c < n8) {
+                    const uint4 lo = ld_relaxed_v4(src + 8 * c), hi = ld_relaxed_v4(src + 8 * c + 4);
+                    if (tags_ok4(lo, tg) && tags_ok4(hi, tg)) dst[c] = untag8(lo, hi);
+                    else stale |= 1u << k;
+                }
+            }
+            for (int k = 0; stale != 0; ++k, stale >>= 1) {
+                if (!(stale & 1u)) continue;
+                const int c = c0 + k * kConsumerWarps * 32;
+                Poll pl;
+                uint4 lo, hi;
+                do {
+                    if (bad || !pl.again(p)) {
+                        bad = true;
+                        break;
+                    }
+                    lo = ld_relaxed_v4(src + 8 * c);
+                    hi = ld_relaxed_v4(src + 8 * c + 4);
+                } while (!(tags_ok4(lo, tg) && tags_ok4(hi, tg)));
+                if (!bad) dst[c] = untag8(lo, hi);
+            }
+        }
     }
 
-    // ---------------------------------------------------------- GEMV tasks
     // One output row of a GEMV task, from its MATS dot products: the fused
     // epilogue of the op (residual add, SwiGLU, logits store).
     template <int MATS>
     __device__ void emit_row(int op, const tiles_task &t, uint32_t row, const float (&v)[MATS]) {
         switch (op) {
             case TILES_OP_QKV:
-                __stcg(&p.qkv[row], v[0]);
+                st_relaxed_u64(p.qkvw + row, ((unsigned long long)tag(t.layer, kTagQKV) << 32) | __float_as_uint(v[0]));
                 break;
             case TILES_OP_OPROJ:
             case TILES_OP_DOWN: {  // residual rows were loaded in the prologue
                 const uint16_t xb = reinterpret_cast<const uint16_t *>(s.vec + p.res_off)[row - t.begin];
-                __stcg(&p.x[row], f2bf(__fadd_rn(bf2f(xb), v[0])));
+                const uint32_t tg = tag(t.layer, op == TILES_OP_OPROJ ? kTagXAttn : kTagXFfn);
+                st_relaxed_u32(p.xw + row, (tg << 16) | f2bf(__fadd_rn(bf2f(xb), v[0])));
                 break;
             }
             case TILES_OP_GATEUP: {
                 const float gt = v[0];
                 const float silu = __fdiv_rn(gt, __fadd_rn(1.0f, expf(-gt)));
-                __stcg(&p.a[row], f2bf(__fmul_rn(silu, v[MATS - 1])));
+                st_relaxed_u32(p.aw + row, (tag(t.layer, kTagA) << 16) | f2bf(__fmul_rn(silu, v[MATS - 1])));
                 break;
             }
             case TILES_OP_LMHEAD:
@@ -864,8 +974,24 @@ struct Consumer {
             const int row0 = is_q ? (h * g.G + hh) * D
                                   : (is_k ? g.qd + h * D : g.qd + g.kvd + h * D);
             float v[E];
+            {
+                const uint32_t tg = tag(cur_layer, kTagQKV);
+                unsigned long long w[E];
 #pragma unroll
-            for (int e = 0; e < E; ++e) v[e] = __ldcg(&p.qkv[row0 + lane + 32 * e]);
+                for (int e = 0; e < E; ++e) w[e] = ld_relaxed_u64(p.qkvw + row0 + lane + 32 * e);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    Poll pl;
+                    while ((uint32_t)(w[e] >> 32) != tg) {
+                        if (bad || !pl.again(p)) {
+                            bad = true;
+                            break;
+                        }
+                        w[e] = ld_relaxed_u64(p.qkvw + row0 + lane + 32 * e);
+                    }
+                    v[e] = __uint_as_float((uint32_t)w[e]);
+                }
+            }
             if (!is_q && !is_k) {
 #pragma unroll
                 for (int e = 0; e < E; ++e) a.vnew[lane + 32 * e] = f2bf(v[e]);
@@ -1195,34 +1321,41 @@ struct Consumer {
     // no tile waits on another tile's merge. Per group of heads: split maxima
     // and sums to shared memory, one thread per head for the weights, then
     // every output element with its S independent loads.
-    // The same merge with S known at compile time: a thread takes 4 dims of
-    // one head and issues all its loads (S maxima, S sums, S 16-byte pieces of
-    // o) at once, so the whole prologue costs about one L2 round trip per
-    // group of outputs instead of one per split batch.
-    template <int S>
-    __device__ void merge_to_vec_fixed() {
+    // The same merge for S <= SMAX splits: a thread takes 4 dims of one head
+    // and issues all its loads (S maxima, S sums, S 16-byte pieces of o) at
+    // once, so the prologue costs about one L2 round trip per group of outputs
+    // instead of one per split batch. Splits S..SMAX-1 enter as m = -inf, l = 0,
+    // o = 0: their weight is exactly 0 and every sum is unchanged, bit for bit.
+    template <int SMAX>
+    __device__ void merge_to_vec_upto(int S) {
         const Geom &g = p.g;
         const int D = g.d, q4 = D / 4, n = g.nq * q4;
         uint16_t *out = reinterpret_cast<uint16_t *>(s.vec);
         for (int idx = tid; idx < n; idx += kConsumerWarps * 32) {
             const int i = idx / q4, k = idx % q4;
             const float *hb = p.partials + (size_t)i * S * (kPartialPad + D);
-            float mc[S], lc[S];
-            float4 oc[S];
+            float mc[SMAX], lc[SMAX];
+            float4 oc[SMAX];
 #pragma unroll
-            for (int c = 0; c < S; ++c) {
-                const float *pc = hb + (size_t)c * (kPartialPad + D);
-                mc[c] = __ldcg(pc);
-                lc[c] = __ldcg(pc + 1);
-                oc[c] = __ldcg(reinterpret_cast<const float4 *>(pc + kPartialPad) + k);
+            for (int c = 0; c < SMAX; ++c) {
+                if (c < S) {
+                    const float *pc = hb + (size_t)c * (kPartialPad + D);
+                    mc[c] = __ldcg(pc);
+                    lc[c] = __ldcg(pc + 1);
+                    oc[c] = __ldcg(reinterpret_cast<const float4 *>(pc + kPartialPad) + k);
+                } else {
+                    mc[c] = -INFINITY;
+                    lc[c] = 0.f;
+                    oc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
             float M = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < S; ++c) M = fmaxf(M, mc[c]);
+            for (int c = 0; c < SMAX; ++c) M = fmaxf(M, mc[c]);
             float L = 0.f;
             float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < S; ++c) {
+            for (int c = 0; c < SMAX; ++c) {
                 const float w = mc[c] == -INFINITY ? 0.f : expf(mc[c] - M);
                 L = fmaf(w, lc[c], L);
                 O.x = fmaf(w, oc[c].x, O.x);
@@ -1237,15 +1370,14 @@ struct Consumer {
     }
 
     __device__ void merge_to_vec() {
-        switch (p.g.kv_splits) {  // the split counts the default plans pick
-            case 8: merge_to_vec_fixed<8>(); return;
-            case 9: merge_to_vec_fixed<9>(); return;
-            case 17: merge_to_vec_fixed<17>(); return;
-            case 19: merge_to_vec_fixed<19>(); return;
-            default: break;
-        }
+        const int S = p.g.kv_splits;
+        if (S <= 8) return merge_to_vec_upto<8>(S);
+        if (S <= 12) return merge_to_vec_upto<12>(S);
+        if (S <= 16) return merge_to_vec_upto<16>(S);
+        if (S <= 20) return merge_to_vec_upto<20>(S);
+        // more splits: the same merge through shared memory, a group of heads at a time
         const Geom &g = p.g;
-        const int D = g.d, S = g.kv_splits;
+        const int D = g.d;
         float *ms = reinterpret_cast<float *>(s.vec + g.merge_off);
         uint16_t *out = reinterpret_cast<uint16_t *>(s.vec);
         for (int h0 = 0; h0 < g.nq; h0 += g.merge_heads) {
@@ -1331,7 +1463,11 @@ struct Consumer {
                 // ---- work
                 switch (t.op) {
                     case TILES_OP_QKV:
-                        rmsnorm_to_vec(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : p.x,
+                        if (t.layer > 0) {
+                            gather_tagged(p.xw, g.H, tag(t.layer - 1, kTagXFfn));
+                            consumer_sync();
+                        }
+                        rmsnorm_to_vec(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : nullptr,
                                        p.layers[t.layer].attn_norm, g.H);
                         consumer_sync();
                         gemv_task<1>(t);
@@ -1341,23 +1477,28 @@ struct Consumer {
                         break;
                     case TILES_OP_OPROJ:
                         merge_to_vec();
-                        load_residual(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : p.x, t.begin, t.end);
+                        load_residual(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : nullptr,
+                                      t.layer == 0 ? 0u : tag(t.layer - 1, kTagXFfn), t.begin, t.end);
                         consumer_sync();
                         gemv_task<1>(t);
                         break;
                     case TILES_OP_GATEUP:
-                        rmsnorm_to_vec(p.x, p.layers[t.layer].ffn_norm, g.H);
+                        gather_tagged(p.xw, g.H, tag(t.layer, kTagXAttn));
+                        consumer_sync();
+                        rmsnorm_to_vec(nullptr, p.layers[t.layer].ffn_norm, g.H);
                         consumer_sync();
                         gemv_task<2>(t);
                         break;
                     case TILES_OP_DOWN:
-                        copy_to_vec(p.a, g.F);
-                        load_residual(p.x, t.begin, t.end);
+                        gather_tagged(p.aw, g.F, tag(t.layer, kTagA));
+                        load_residual(nullptr, tag(t.layer, kTagXAttn), t.begin, t.end);
                         consumer_sync();
                         gemv_task<1>(t);
                         break;
                     case TILES_OP_LMHEAD:
-                        rmsnorm_to_vec(p.x, p.final_norm, g.H);
+                        gather_tagged(p.xw, g.H, tag(g.L - 1, kTagXFfn));
+                        consumer_sync();
+                        rmsnorm_to_vec(nullptr, p.final_norm, g.H);
                         consumer_sync();
                         gemv_task<1>(t);
                         break;

@@ -24,7 +24,7 @@ namespace tiles {
 tiles_plan_opts default_opts() {
     tiles_plan_opts o;
     std::memset(&o, 0, sizeof(o));
-    o.scheduler = TILES_SCHED_COUNTERS;
+    o.scheduler = TILES_SCHED_FLAGS;
     return o;
 }
 
@@ -68,8 +68,11 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
         return fail(TILES_ERR_UNSUPPORTED, "dimension too large");
     if (n_ctas < 1 || n_ctas > 4096) return fail(TILES_ERR_INVALID_ARG, "n_ctas");
     if (o.flags != 0) return fail(TILES_ERR_INVALID_ARG, "flags must be 0");
-    if (o.scheduler != TILES_SCHED_WAVES && o.scheduler != TILES_SCHED_COUNTERS)
+    if (o.scheduler != TILES_SCHED_WAVES && o.scheduler != TILES_SCHED_COUNTERS &&
+        o.scheduler != TILES_SCHED_FLAGS)
         return fail(TILES_ERR_INVALID_ARG, "scheduler");
+    // 16-bit activation tags: 1 + 4 * (64 steps * layers) must stay below 2^16
+    if (d.n_layers > 255) return fail(TILES_ERR_UNSUPPORTED, "more than 255 layers");
 
     Geom &G_ = *g;
     std::memset(&G_, 0, sizeof(G_));
@@ -86,13 +89,14 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     G_.kvd = d.n_kv_heads * d.head_dim;
     G_.qkv_rows = G_.qd + 2 * G_.kvd;
 
-    // slot: large enough for one row of every GEMV (two for gate/up). A bulk
-    // copy costs about the same TMA time whatever its size up to tens of KB
-    // (measured on GB300: two issuing lanes reach ~45 GB/s per SM with 16 KB
-    // copies and ~85 GB/s with 32 KB ones), so the default is 32 KB or the
-    // largest row, whichever is bigger.
+    // slot: large enough for one row of every GEMV (two for gate/up). Each
+    // slot has one owning consumer warp, so the default ring is one slot per
+    // warp of 16 KB (or the largest row): a chunk holds its slot while one warp
+    // reduces it, and smaller chunks turn the ring over faster. Measured on
+    // GB300 for the Llama-1B shape: 8 x 16 KB beat 6 x 32 KB by 6 % and
+    // 12 x 16 KB (uneven ownership) by 2 %.
     int need = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, 2 * 2 * G_.H});
-    int slot = o.slot_bytes > 0 ? o.slot_bytes : round_up(std::max(need, 32768), 1024);
+    int slot = o.slot_bytes > 0 ? o.slot_bytes : round_up(std::max(need, 16384), 1024);
     if (slot % 1024 || slot < need) return fail(TILES_ERR_INVALID_ARG, "slot_bytes too small or not a multiple of 1024");
     G_.slot_bytes = slot;
     auto rpc = [&](int in, int mats) {
@@ -108,7 +112,12 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     if (kb < 1) return fail(TILES_ERR_UNSUPPORTED, "slot too small for one KV position");
     G_.kv_block = kb;
     int nb_max = ceil_div(G_.max_pos, kb);
-    int splits = o.kv_splits > 0 ? o.kv_splits : std::max(1, std::min(nb_max, n_ctas / G_.nkv));
+    // default: about two KV blocks per split at the longest context, at most one
+    // split per CTA and KV head. Every O-projection tile merges all S partials
+    // of every head, so more splits than that cost more in the merge than they
+    // save in the attention tiles (Llama-1B shape at 1,087 positions, 64-position
+    // blocks: S = 9 ran about 3 % faster than S = 6, 8 or 17).
+    int splits = o.kv_splits > 0 ? o.kv_splits : std::max(1, std::min(ceil_div(nb_max, 2), n_ctas / G_.nkv));
     if (splits < 1 || splits > 4096) return fail(TILES_ERR_INVALID_ARG, "kv_splits");
     G_.kv_splits = splits;
 
@@ -123,7 +132,7 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     G_.res_off = round_up(vec, 16);
     G_.vec_bytes = round_up(G_.res_off + 2 * G_.H, 128);
     int avail = smem_limit - kCtlBytes - G_.vec_bytes;
-    int slots = o.ring_slots > 0 ? o.ring_slots : std::min(kMaxSlots, avail / slot);
+    int slots = o.ring_slots > 0 ? o.ring_slots : std::min(kConsumerWarps, avail / slot);
     if (slots < 2 || slots > kMaxSlots) return fail(TILES_ERR_UNSUPPORTED, "ring needs 2..32 slots");
     G_.ring_slots = slots;
     G_.smem_bytes = kCtlBytes + slots * slot + G_.vec_bytes;
@@ -305,6 +314,19 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
                 t.wait_ctr = (uint16_t)pp;
                 t.wait_mul = npp;
                 t.wait_add = pp < phi ? npp : 0;  // same step, or the step before
+                if (o.scheduler == TILES_SCHED_FLAGS) {
+                    // tagged inputs need no counter: only the O-projection (reads
+                    // the split partials) and the first Q/K/V tile of a step (reads
+                    // the sampled token) wait, and only their producers signal
+                    const int op = phase_op[phi];
+                    const bool waits = op == TILES_OP_OPROJ || (op == TILES_OP_QKV && phase_layer[phi] == 0);
+                    const bool signals = op == TILES_OP_ATTN || op == TILES_OP_LMHEAD;
+                    if (!waits) {
+                        t.wait_ctr = TILES_NO_COUNTER;
+                        t.wait_mul = t.wait_add = 0;
+                    }
+                    if (!signals) t.signal_ctr = TILES_NO_COUNTER;
+                }
                 per_cta[a.cta].push_back(t);
             }
         }
@@ -422,7 +444,14 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
             const tiles_task &t = s.tasks[i];
             int kind = t.op == TILES_OP_SYNC ? t.phase_kind : phase_of_op(t.op);
             int phi = phase_index(g, kind == 6 ? 0 : t.layer, kind);
-            if (t.wait_ctr == TILES_NO_COUNTER) return fail("task without a wait");
+            if (t.wait_ctr == TILES_NO_COUNTER) {
+                // only tiles whose inputs are all tagged words may skip the counters
+                const bool tagged_inputs = t.op == TILES_OP_ATTN || t.op == TILES_OP_GATEUP ||
+                                           t.op == TILES_OP_DOWN || t.op == TILES_OP_LMHEAD ||
+                                           (t.op == TILES_OP_QKV && t.layer > 0);
+                if (s.scheduler != TILES_SCHED_FLAGS || !tagged_inputs) return fail("task without a wait");
+                continue;
+            }
             int ctr = t.wait_ctr;
             long long before = 0;
             for (int q = 0; q < phi; ++q) before += sig_by_phase[q][ctr];
@@ -447,6 +476,26 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
     }
     if (s.final_ctr < 0 || s.final_ctr >= s.n_counters || (long long)s.final_mul != per_step[s.final_ctr])
         return fail("final wait");
+    if (s.scheduler == TILES_SCHED_FLAGS) {
+        // The K/V written by an attention tile is read by TMA in later steps.
+        // Its only ordering is a chain of counters: attention -> (acquired by
+        // the O-projection tiles) -> LM-head signal -> first tile of the next
+        // step. So in every layer some CTA must both wait for the attention
+        // counter (an O-projection tile) and signal the LM-head counter.
+        std::vector<char> lm(N, 0);
+        for (int c = 0; c < N; ++c)
+            for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i)
+                if (s.tasks[i].op == TILES_OP_LMHEAD && s.tasks[i].signal_ctr != TILES_NO_COUNTER) lm[c] = 1;
+        for (int l = 0; l < g.L; ++l) {
+            bool linked = false;
+            for (int c = 0; c < N && !linked; ++c)
+                for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i) {
+                    const tiles_task &t = s.tasks[i];
+                    if (t.op == TILES_OP_OPROJ && t.layer == l && t.wait_ctr != TILES_NO_COUNTER && lm[c]) linked = true;
+                }
+            if (!linked) return fail("no CTA links a layer's attention to the next step");
+        }
+    }
     return TILES_OK;
 }
 

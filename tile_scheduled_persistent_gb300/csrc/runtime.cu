@@ -52,6 +52,33 @@ cudaError_t dalloc(tiles_plan_s *p, T **ptr, size_t bytes) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+size_t align256(size_t v) { return (v + 255u) & ~(size_t)255u; }
+
+// The block of device memory every launch starts by zeroing:
+// argmax keys [64] | phase counters | x words [H] | a words [F] | Q/K/V words [rows].
+struct SyncLayout {
+    size_t ctr, xw, aw, qkvw, bytes;
+};
+SyncLayout sync_layout(const tiles_schedule_s &s) {
+    const Geom &g = s.geom;
+    SyncLayout l;
+    l.ctr = (size_t)kMaxStepsPerLaunch * 8;
+    l.xw = align256(l.ctr + (size_t)s.n_counters * kCounterStride * 4);
+    l.aw = align256(l.xw + (size_t)g.H * 4);
+    l.qkvw = align256(l.aw + (size_t)g.F * 4);
+    l.bytes = align256(l.qkvw + (size_t)g.qkv_rows * 8);
+    return l;
+}
+size_t sync_block_bytes(const tiles_schedule_s &s) { return sync_layout(s).bytes; }
+void place_sync_block(const tiles_schedule_s &s, uint8_t *base, KernelParams *p) {
+    const SyncLayout l = sync_layout(s);
+    p->keys = reinterpret_cast<unsigned long long *>(base);
+    p->counters = reinterpret_cast<uint32_t *>(base + l.ctr);
+    p->xw = reinterpret_cast<uint32_t *>(base + l.xw);
+    p->aw = reinterpret_cast<uint32_t *>(base + l.aw);
+    p->qkvw = reinterpret_cast<unsigned long long *>(base + l.qkvw);
+}
+
 // RoPE inverse frequencies theta^(-2j/d) in FP64, with the published llama3
 // rule when enabled: wavelength 2 pi / w below orig/high keeps w, above
 // orig/low divides it by the factor, between the two blends linearly in
@@ -220,18 +247,15 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
         p.rope_sin = ds;
     }
     // scratch
-    if ((e = dalloc(plan, &p.qkv, (size_t)g.qkv_rows * 4)) != cudaSuccess) return fail(e);
     if ((e = dalloc(plan, &p.partials, (size_t)g.nq * g.kv_splits * (kPartialPad + g.d) * 4)) != cudaSuccess) return fail(e);
-    if ((e = dalloc(plan, &p.x, (size_t)g.H * 2)) != cudaSuccess) return fail(e);
-    if ((e = dalloc(plan, &p.a, (size_t)g.F * 2)) != cudaSuccess) return fail(e);
-    // one memset per launch clears: argmax keys | phase counters
-    const size_t ctr_bytes = (size_t)plan->sched.n_counters * kCounterStride * 4;
-    plan->sync_bytes = kMaxStepsPerLaunch * 8 + ctr_bytes;
+    // one memset per launch clears: argmax keys | phase counters | tagged activations
+    // (tag 0 is never written, so nothing of an earlier launch reads as ready)
+    plan->sync_bytes = sync_block_bytes(plan->sched);
     uint8_t *sync;
     if ((e = dalloc(plan, &sync, plan->sync_bytes)) != cudaSuccess) return fail(e);
     plan->d_keys = reinterpret_cast<unsigned long long *>(sync);
     p.keys = plan->d_keys;
-    p.counters = reinterpret_cast<uint32_t *>(sync + kMaxStepsPerLaunch * 8);
+    place_sync_block(plan->sched, sync, &p);
     if ((e = dalloc(plan, &p.status, 16)) != cudaSuccess) return fail(e);
     if ((e = cudaMemset(p.status, 0, 16)) != cudaSuccess) return fail(e);
     if ((e = dalloc(plan, &plan->d_prompt_stage, (size_t)g.max_pos * 4)) != cudaSuccess) return fail(e);
@@ -449,7 +473,6 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[kNoAllocMaxDevices];  // device address of g_noalloc_scratch, per device
 
-size_t align256(size_t v) { return (v + 255u) & ~(size_t)255u; }
 
 // Device address of the array on `dev` (current device); looked up once per device.
 tiles_status_t noalloc_scratch(int dev, unsigned char **out) {
@@ -475,12 +498,9 @@ extern "C" tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache,
     if (n_new > 0 && !out_tokens) return TILES_ERR_INVALID_ARG;
     if (!aligned16(k_cache) || !aligned16(v_cache)) return TILES_ERR_INVALID_ARG;
     const Geom &g = plan->sched.geom;
-    // layout in the array: sync block (zeroed per launch) | qkv | partials | x | a
-    const size_t off_qkv = align256(plan->sync_bytes);
-    const size_t off_part = off_qkv + align256((size_t)g.qkv_rows * 4);
-    const size_t off_x = off_part + align256((size_t)g.nq * g.kv_splits * (kPartialPad + g.d) * 4);
-    const size_t off_a = off_x + align256((size_t)g.H * 2);
-    const size_t need = off_a + align256((size_t)g.F * 2);
+    // layout in the array: sync block (zeroed per launch) | split partials
+    const size_t off_part = align256(plan->sync_bytes);
+    const size_t need = off_part + align256((size_t)g.nq * g.kv_splits * (kPartialPad + g.d) * 4);
     if (need > kNoAllocScratchBytes) return TILES_ERR_CAPACITY;
     const long long steps = (long long)n_prompt - 1 + n_new;
     if (steps == 0) return TILES_OK;
@@ -490,12 +510,8 @@ extern "C" tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache,
     unsigned char *base = nullptr;
     if ((st = noalloc_scratch(plan->device, &base)) != TILES_OK) return st;
     KernelParams p = plan->base;
-    p.keys = reinterpret_cast<unsigned long long *>(base);
-    p.counters = reinterpret_cast<uint32_t *>(base + kMaxStepsPerLaunch * 8);
-    p.qkv = reinterpret_cast<float *>(base + off_qkv);
+    place_sync_block(plan->sched, base, &p);
     p.partials = reinterpret_cast<float *>(base + off_part);
-    p.x = reinterpret_cast<uint16_t *>(base + off_x);
-    p.a = reinterpret_cast<uint16_t *>(base + off_a);
     p.k_cache = reinterpret_cast<uint16_t *>(k_cache);
     p.v_cache = reinterpret_cast<uint16_t *>(v_cache);
     p.prompt = prompt;

@@ -177,8 +177,11 @@ struct KernelParams {
     const float *rope_cos, *rope_sin;  // [max_pos][d/2]
     // caches and scratch
     uint16_t *k_cache, *v_cache;
-    float *qkv, *partials;
-    uint16_t *x, *a;
+    float *partials;
+    // tagged activations: (tag << 16) | bf16 for the residual stream x [H] and
+    // the SwiGLU output a [F]; (tag << 32) | f32 bits for the Q/K/V rows
+    uint32_t *xw, *aw;
+    unsigned long long *qkvw;
     unsigned long long *keys;
     uint32_t *counters, *status;
     // run
