@@ -91,11 +91,12 @@ typedef struct {
  *  WAVES: every phase ends in a grid barrier (a counter all CTAs arrive on).
  *  COUNTERS: a tile waits on the dependency counter of the phase it reads,
  *    which every tile of that phase increments once done.
- *  FLAGS: activations carry their own readiness. Each word of the residual
- *    stream, the SwiGLU output and the Q/K/V projection holds the value and
- *    the tag of the (step, layer, phase) that wrote it, and a tile polls the
- *    words it reads until they carry the tag it expects. The split-KV partials
- *    and the sampled token still go through counters.
+ *  FLAGS (default): activations carry their own readiness. Each word of the
+ *    residual stream, the Q/K/V projection, the split-KV partials, the
+ *    attention output and the SwiGLU output holds the value and the tag of
+ *    the (step, layer, phase) that wrote it, and a tile polls the words it
+ *    reads until they carry the tag it expects. Only the sampled token still
+ *    goes through a counter (the LM-head tiles signal it).
  * All three compute bit-identical results. */
 enum { TILES_SCHED_WAVES = 0, TILES_SCHED_COUNTERS = 1, TILES_SCHED_FLAGS = 2 };
 
@@ -224,8 +225,9 @@ tiles_status_t tiles_plan_get_info(tiles_plan_t plan, tiles_plan_info *info);
 
 enum {
     TILES_OP_QKV = 1,      /* RMSNorm prologue, rows of [Wq; Wk; Wv] -> FP32 q,k,v        */
-    TILES_OP_ATTN = 2,     /* q/k norm + RoPE + KV write, split-KV partials (item = kv head * splits + split) */
-    TILES_OP_COMBINE = 3,  /* merge split partials of q heads [begin, end) -> bf16 o      */
+    TILES_OP_ATTN = 2,     /* q/k norm + RoPE + KV write, split-KV partial, then the merge of
+                              1/S of the kv head's outputs (item = kv head * splits + split) */
+    TILES_OP_COMBINE = 3,  /* unused: the attention tiles merge the splits themselves     */
     TILES_OP_OPROJ = 4,    /* rows of Wo, residual add                                    */
     TILES_OP_GATEUP = 5,   /* RMSNorm prologue, rows of Wg and Wu, SwiGLU epilogue        */
     TILES_OP_DOWN = 6,     /* rows of Wd, residual add                                    */

@@ -115,9 +115,9 @@ def test_flags_schedule_waits_only_where_inputs_are_untagged():
     for c in range(len(off) - 1):
         for i in range(off[c], off[c + 1]):
             t = tasks[i]
-            waits = t.op == 4 or (t.op == 1 and t.layer == 0)      # O-proj; first Q/K/V of a step
+            waits = t.op == 1 and t.layer == 0                      # first Q/K/V of a step
             assert (t.wait_ctr != NO) == waits, (t.op, t.layer)
-            assert (t.signal_ctr != NO) == (t.op in (2, 7))          # attention and LM head signal
+            assert (t.signal_ctr != NO) == (t.op == 7)               # the LM head signals
 
 
 def _mutate_flags_and_expect(mutator, expect):
@@ -129,27 +129,21 @@ def _mutate_flags_and_expect(mutator, expect):
     assert expect in why, why
 
 
-def test_flags_rejects_an_o_projection_that_does_not_wait():
+def test_flags_rejects_a_first_qkv_tile_that_does_not_wait():
     def m(tasks, off):
         for i in range(len(tasks)):
-            if tasks[i].op == 4:
+            if tasks[i].op == 1 and tasks[i].layer == 0:
                 tasks[i].wait_ctr = 0xFFFF
                 return
     _mutate_flags_and_expect(m, "without a wait")
 
 
-def test_flags_rejects_an_attention_tile_that_does_not_signal():
+def test_flags_rejects_an_attention_cta_that_does_not_signal_the_lm_head():
+    # the LM-head release of the same CTA is what orders its K/V writes
     def m(tasks, off):
-        for i in range(len(tasks)):
-            if tasks[i].op == 2:
-                tasks[i].signal_ctr = 0xFFFF
-                return
-    _mutate_flags_and_expect(m, "wait")
-
-
-def test_flags_rejects_a_layer_whose_attention_is_not_linked_to_the_next_step():
-    def m(tasks, off):
-        for i in range(len(tasks)):                          # no LM-head tile signals
+        c = next(c for c in range(len(off) - 1)
+                 if any(tasks[i].op == 2 for i in range(off[c], off[c + 1])))
+        for i in range(off[c], off[c + 1]):
             if tasks[i].op == 7:
                 tasks[i].signal_ctr = 0xFFFF
     _mutate_flags_and_expect(m, "")

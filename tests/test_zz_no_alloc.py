@@ -63,12 +63,14 @@ def test_noalloc_matches_regular_decode_twice(tsp, name):
 
 
 def test_noalloc_rejects_a_plan_that_does_not_fit(tsp):
-    """4096 KV splits need ~4 MiB of split partials: more than the fixed array."""
+    """16 q heads of 128 dims in 64 KV splits need 1.06 MB of split partials
+    (64-bit words), more than the fixed 1 MiB array."""
     import torch
-    cfg = S.CONFIGS["tiny"]
+    from dataclasses import replace
+    cfg = replace(S.CONFIGS["tiny"], name="wide", n_q_heads=16, head_dim=128)
     w, k, v, prompt = inputs(cfg, n_pos=0)
     plan = tsp.Plan(tsp.ModelDesc.from_config(cfg), tsp.upload_weights(w),
-                    tsp.make_opts(kv_splits=4096))
+                    tsp.make_opts(kv_splits=64))
     kc, vc = tsp.to_device_bf16(k), tsp.to_device_bf16(v)
     out = torch.zeros(4, dtype=torch.int32, device="cuda")
     with pytest.raises(tsp.TilesError) as e:

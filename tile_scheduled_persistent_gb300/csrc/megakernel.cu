@@ -276,14 +276,15 @@ __device__ __forceinline__ bool failed(const KernelParams &p) { return ld_volati
 
 // ------------------------------------------------------------------ tagged activations
 // Activation words carry the tag of the phase that wrote them:
-// 1 + 4 (step L + layer) + kind, with kind 0 for the Q/K/V rows, 1 for x after
+// 1 + 6 (step L + layer) + kind, with kind 0 for the Q/K/V rows, 1 for x after
 // the O-projection, 2 for the SwiGLU output a, 3 for x after the down
-// projection. The step is the launch's own (< 64), so within a launch no tag
-// repeats (at most 256 L < 2^16), and every launch starts from zeroed words,
-// so 0 never matches and nothing of an earlier launch reads as ready.
-enum { kTagQKV = 0, kTagXAttn = 1, kTagA = 2, kTagXFfn = 3 };
+// projection, 4 for the split partials, 5 for the merged attention output o.
+// The step is the launch's own (< 64), so within a launch no tag repeats (at
+// most 384 L < 2^16), and every launch starts from zeroed words, so 0 never
+// matches and nothing of an earlier launch reads as ready.
+enum { kTagQKV = 0, kTagXAttn = 1, kTagA = 2, kTagXFfn = 3, kTagPart = 4, kTagO = 5 };
 __device__ __forceinline__ uint32_t act_tag(const KernelParams &p, int step, int layer, int kind) {
-    return 1u + 4u * ((uint32_t)step * (uint32_t)p.g.L + (uint32_t)layer) + (uint32_t)kind;
+    return 1u + 6u * ((uint32_t)step * (uint32_t)p.g.L + (uint32_t)layer) + (uint32_t)kind;
 }
 
 // Bounded polling of tagged words, like every other wait: the global timer
@@ -1302,117 +1303,74 @@ struct Consumer {
                         O = fmaf(sc, st[kPartialPad + dd], O);
                     }
                 }
-                float *dst = p.partials + ((size_t)(h * G + i) * g.kv_splits + c) * (kPartialPad + D);
+                unsigned long long *dst = p.partw + ((size_t)(h * G + i) * g.kv_splits + c) * (2 + D);
+                const unsigned long long tg = (unsigned long long)tag(cur_layer, kTagPart) << 32;
                 if (dd == 0) {
-                    __stcg(&dst[0], M);
-                    __stcg(&dst[1], L);
+                    st_relaxed_u64(&dst[0], tg | __float_as_uint(M));
+                    st_relaxed_u64(&dst[1], tg | __float_as_uint(L));
                 }
-                __stcg(&dst[kPartialPad + dd], O);
+                st_relaxed_u64(&dst[2 + dd], tg | __float_as_uint(O));
             }
             // wstate is reused by the next item; leave together on any failure
             if (consumer_sync_or(bad)) return;
         }
-    }
-
-    // O-proj prologue: vec <- bf16 attention output of every q head, merged
-    // from the S split partials in split order:
-    //   M = max_c m_c, w_c = e^(m_c - M), o = sum_c w_c o_c / sum_c w_c l_c.
-    // Every O-proj tile merges all heads itself, straight from the partials, so
-    // no tile waits on another tile's merge. Per group of heads: split maxima
-    // and sums to shared memory, one thread per head for the weights, then
-    // every output element with its S independent loads.
-    // The same merge for S <= SMAX splits: a thread takes 4 dims of one head
-    // and issues all its loads (S maxima, S sums, S 16-byte pieces of o) at
-    // once, so the prologue costs about one L2 round trip per group of outputs
-    // instead of one per split batch. Splits S..SMAX-1 enter as m = -inf, l = 0,
-    // o = 0: their weight is exactly 0 and every sum is unchanged, bit for bit.
-    template <int SMAX>
-    __device__ void merge_to_vec_upto(int S) {
-        const Geom &g = p.g;
-        const int D = g.d, q4 = D / 4, n = g.nq * q4;
-        uint16_t *out = reinterpret_cast<uint16_t *>(s.vec);
-        for (int idx = tid; idx < n; idx += kConsumerWarps * 32) {
-            const int i = idx / q4, k = idx % q4;
-            const float *hb = p.partials + (size_t)i * S * (kPartialPad + D);
-            float mc[SMAX], lc[SMAX];
-            float4 oc[SMAX];
-#pragma unroll
-            for (int c = 0; c < SMAX; ++c) {
-                if (c < S) {
-                    const float *pc = hb + (size_t)c * (kPartialPad + D);
-                    mc[c] = __ldcg(pc);
-                    lc[c] = __ldcg(pc + 1);
-                    oc[c] = __ldcg(reinterpret_cast<const float4 *>(pc + kPartialPad) + k);
-                } else {
-                    mc[c] = -INFINITY;
-                    lc[c] = 0.f;
-                    oc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-            float M = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < SMAX; ++c) M = fmaxf(M, mc[c]);
-            float L = 0.f;
-            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int c = 0; c < SMAX; ++c) {
-                const float w = mc[c] == -INFINITY ? 0.f : expf(mc[c] - M);
-                L = fmaf(w, lc[c], L);
-                O.x = fmaf(w, oc[c].x, O.x);
-                O.y = fmaf(w, oc[c].y, O.y);
-                O.z = fmaf(w, oc[c].z, O.z);
-                O.w = fmaf(w, oc[c].w, O.w);
-            }
-            const uint32_t lo = (uint32_t)f2bf(__fdiv_rn(O.x, L)) | ((uint32_t)f2bf(__fdiv_rn(O.y, L)) << 16);
-            const uint32_t hi = (uint32_t)f2bf(__fdiv_rn(O.z, L)) | ((uint32_t)f2bf(__fdiv_rn(O.w, L)) << 16);
-            reinterpret_cast<uint2 *>(out + (size_t)i * D)[k] = make_uint2(lo, hi);
+        // Every partial of this task is out; now merge. (A merge polls the other
+        // splits of its head, so no merge may come before a partial of the same
+        // task: a CTA holding two splits of one head would wait on itself.)
+        for (uint32_t it = t.begin; it < t.end; ++it) {
+            merge_slice<D, G>((int)(it / (uint32_t)g.kv_splits), (int)(it % (uint32_t)g.kv_splits));
+            if (consumer_sync_or(bad)) return;
         }
     }
 
-    __device__ void merge_to_vec() {
-        const int S = p.g.kv_splits;
-        if (S <= 8) return merge_to_vec_upto<8>(S);
-        if (S <= 12) return merge_to_vec_upto<12>(S);
-        if (S <= 16) return merge_to_vec_upto<16>(S);
-        if (S <= 20) return merge_to_vec_upto<20>(S);
-        // more splits: the same merge through shared memory, a group of heads at a time
+    // Slice c of KV head h's merged attention output: elements [e0, e1) of its
+    // G d outputs, S-th of them per split, from the S partials in split order:
+    //   M = max_c m_c, w_c = e^(m_c - M), o = sum_c w_c o_c / sum_c w_c l_c.
+    // One thread per (element, split) pair polls that pair's tagged m, l and o
+    // into shared memory; then one thread per element merges and writes the
+    // tagged bf16 output, which the O-projection tiles gather.
+    template <int D, int G>
+    __device__ void merge_slice(int h, int c) {
         const Geom &g = p.g;
-        const int D = g.d;
-        float *ms = reinterpret_cast<float *>(s.vec + g.merge_off);
-        uint16_t *out = reinterpret_cast<uint16_t *>(s.vec);
-        for (int h0 = 0; h0 < g.nq; h0 += g.merge_heads) {
-            const int nh = g.nq - h0 < g.merge_heads ? g.nq - h0 : g.merge_heads;
-            float *ls = ms + (size_t)nh * S;   // [nh][S] split sums
-            float *Ls = ls + (size_t)nh * S;   // [nh] merged sums
-            const float *base = p.partials + (size_t)h0 * S * (kPartialPad + D);
-            if (h0 > 0) consumer_sync();       // the previous group is done with the scratch
-            for (int idx = tid; idx < nh * S; idx += kConsumerWarps * 32) {
-                ms[idx] = __ldcg(&base[(size_t)idx * (kPartialPad + D)]);
-                ls[idx] = __ldcg(&base[(size_t)idx * (kPartialPad + D) + 1]);
-            }
-            consumer_sync();
-            for (int i = tid; i < nh; i += kConsumerWarps * 32) {
-                float M = -INFINITY;
-                for (int c = 0; c < S; ++c) M = fmaxf(M, ms[i * S + c]);
-                float L = 0.f;
-                for (int c = 0; c < S; ++c) {
-                    const float mc = ms[i * S + c];
-                    const float w = mc == -INFINITY ? 0.f : expf(mc - M);
-                    ms[i * S + c] = w;
-                    L = fmaf(w, ls[i * S + c], L);
+        const int S = g.kv_splits, n = G * D, per = (n + S - 1) / S;
+        const int e0 = c * per, e1 = e0 + per < n ? e0 + per : n;
+        if (e0 >= e1) return;
+        const int ne = e1 - e0;
+        float *st = reinterpret_cast<float *>(s.vec);  // [ne][S][3]: m, l, o
+        const uint32_t tg = tag(cur_layer, kTagPart);
+        for (int q = tid; q < ne * S; q += kConsumerWarps * 32) {
+            const int e = e0 + q / S, cc = q % S;
+            const unsigned long long *pw = p.partw + ((size_t)(h * G + e / D) * S + cc) * (2 + D);
+            unsigned long long wm = ld_relaxed_u64(pw), wl = ld_relaxed_u64(pw + 1),
+                               wo = ld_relaxed_u64(pw + 2 + e % D);
+            Poll pl;
+            while ((uint32_t)(wm >> 32) != tg || (uint32_t)(wl >> 32) != tg || (uint32_t)(wo >> 32) != tg) {
+                if (bad || !pl.again(p)) {
+                    bad = true;
+                    break;
                 }
-                Ls[i] = L;
+                wm = ld_relaxed_u64(pw);
+                wl = ld_relaxed_u64(pw + 1);
+                wo = ld_relaxed_u64(pw + 2 + e % D);
             }
-            consumer_sync();
-            for (int idx = tid; idx < nh * D; idx += kConsumerWarps * 32) {
-                const int i = idx / D, dd = idx % D;
-                const float *pc = base + (size_t)i * S * (kPartialPad + D) + kPartialPad + dd;
-                const float *wi = ms + (size_t)i * S;
-                float O = 0.f;
-#pragma unroll 4
-                for (int c = 0; c < S; ++c) O = fmaf(wi[c], __ldcg(&pc[(size_t)c * (kPartialPad + D)]), O);
-                out[(size_t)(h0 + i) * D + dd] = f2bf(__fdiv_rn(O, Ls[i]));
+            st[q * 3 + 0] = __uint_as_float((uint32_t)wm);
+            st[q * 3 + 1] = __uint_as_float((uint32_t)wl);
+            st[q * 3 + 2] = __uint_as_float((uint32_t)wo);
+        }
+        consumer_sync();
+        const uint32_t to = tag(cur_layer, kTagO) << 16;
+        for (int q = tid; q < ne; q += kConsumerWarps * 32) {
+            const float *sq = st + (size_t)q * S * 3;
+            float M = -INFINITY;
+            for (int cc = 0; cc < S; ++cc) M = fmaxf(M, sq[cc * 3]);
+            float L = 0.f, O = 0.f;
+            for (int cc = 0; cc < S; ++cc) {
+                const float mc = sq[cc * 3];
+                const float w = mc == -INFINITY ? 0.f : expf(mc - M);
+                L = fmaf(w, sq[cc * 3 + 1], L);
+                O = fmaf(w, sq[cc * 3 + 2], O);
             }
+            st_relaxed_u32(p.ow + (size_t)h * n + e0 + q, to | f2bf(__fdiv_rn(O, L)));
         }
     }
 
@@ -1476,7 +1434,7 @@ struct Consumer {
                         attn_dispatch(t);
                         break;
                     case TILES_OP_OPROJ:
-                        merge_to_vec();
+                        gather_tagged(p.ow, g.qd, tag(t.layer, kTagO));
                         load_residual(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : nullptr,
                                       t.layer == 0 ? 0u : tag(t.layer - 1, kTagXFfn), t.begin, t.end);
                         consumer_sync();

@@ -71,8 +71,8 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     if (o.scheduler != TILES_SCHED_WAVES && o.scheduler != TILES_SCHED_COUNTERS &&
         o.scheduler != TILES_SCHED_FLAGS)
         return fail(TILES_ERR_INVALID_ARG, "scheduler");
-    // 16-bit activation tags: 1 + 4 * (64 steps * layers) must stay below 2^16
-    if (d.n_layers > 255) return fail(TILES_ERR_UNSUPPORTED, "more than 255 layers");
+    // 16-bit activation tags: 1 + 6 * (64 steps * layers) must stay below 2^16
+    if (d.n_layers > 170) return fail(TILES_ERR_UNSUPPORTED, "more than 170 layers");
 
     Geom &G_ = *g;
     std::memset(&G_, 0, sizeof(G_));
@@ -112,22 +112,18 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     if (kb < 1) return fail(TILES_ERR_UNSUPPORTED, "slot too small for one KV position");
     G_.kv_block = kb;
     int nb_max = ceil_div(G_.max_pos, kb);
-    // default: about two KV blocks per split at the longest context, at most one
-    // split per CTA and KV head. Every O-projection tile merges all S partials
-    // of every head, so more splits than that cost more in the merge than they
-    // save in the attention tiles (Llama-1B shape at 1,087 positions, 64-position
-    // blocks: S = 9 ran about 3 % faster than S = 6, 8 or 17).
-    int splits = o.kv_splits > 0 ? o.kv_splits : std::max(1, std::min(ceil_div(nb_max, 2), n_ctas / G_.nkv));
-    if (splits < 1 || splits > 4096) return fail(TILES_ERR_INVALID_ARG, "kv_splits");
+    // default: one KV block per split at the longest context, at most one split
+    // per CTA and KV head. Each attention tile merges a 1/S slice of its head,
+    // so the merge shrinks as S grows (Llama-1B shape at 1,087 positions,
+    // 64-position blocks: S = 17 ran 3 % faster than S = 9 and 6 % faster than 6).
+    int splits = o.kv_splits > 0 ? o.kv_splits : std::max(1, std::min(nb_max, n_ctas / G_.nkv));
+    if (splits < 1 || splits > 256) return fail(TILES_ERR_INVALID_ARG, "kv_splits");
     G_.kv_splits = splits;
 
-    // the O-proj prologue merges the split partials into the input vector, a
-    // group of q heads at a time: 2 S + 1 floats of scratch per head, after it
-    const int per_head = (2 * splits + 1) * 4;
-    G_.merge_off = round_up(2 * G_.qd, 16);
-    G_.merge_heads = std::max(1, std::min(G_.nq, 16384 / per_head));
-    int vec = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, attn_vec_bytes(G, G_.d),
-                        G_.merge_off + G_.merge_heads * per_head});
+    // an attention tile merges a 1/S slice of its KV head's G d outputs,
+    // staging (m, l, o) of every (output, split) pair: 3 floats each
+    const int merge_pairs = ceil_div(G * G_.d, splits) * splits;
+    int vec = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, attn_vec_bytes(G, G_.d), merge_pairs * 12});
     // residual rows of an O-proj / down tile follow (a tile has at most H rows)
     G_.res_off = round_up(vec, 16);
     G_.vec_bytes = round_up(G_.res_off + 2 * G_.H, 128);
@@ -315,12 +311,11 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
                 t.wait_mul = npp;
                 t.wait_add = pp < phi ? npp : 0;  // same step, or the step before
                 if (o.scheduler == TILES_SCHED_FLAGS) {
-                    // tagged inputs need no counter: only the O-projection (reads
-                    // the split partials) and the first Q/K/V tile of a step (reads
-                    // the sampled token) wait, and only their producers signal
+                    // tagged inputs need no counter: only the first Q/K/V tile of a
+                    // step (reads the sampled token) waits, and only the LM head signals
                     const int op = phase_op[phi];
-                    const bool waits = op == TILES_OP_OPROJ || (op == TILES_OP_QKV && phase_layer[phi] == 0);
-                    const bool signals = op == TILES_OP_ATTN || op == TILES_OP_LMHEAD;
+                    const bool waits = op == TILES_OP_QKV && phase_layer[phi] == 0;
+                    const bool signals = op == TILES_OP_LMHEAD;
                     if (!waits) {
                         t.wait_ctr = TILES_NO_COUNTER;
                         t.wait_mul = t.wait_add = 0;
@@ -446,9 +441,9 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
             int phi = phase_index(g, kind == 6 ? 0 : t.layer, kind);
             if (t.wait_ctr == TILES_NO_COUNTER) {
                 // only tiles whose inputs are all tagged words may skip the counters
-                const bool tagged_inputs = t.op == TILES_OP_ATTN || t.op == TILES_OP_GATEUP ||
-                                           t.op == TILES_OP_DOWN || t.op == TILES_OP_LMHEAD ||
-                                           (t.op == TILES_OP_QKV && t.layer > 0);
+                const bool tagged_inputs = t.op == TILES_OP_ATTN || t.op == TILES_OP_OPROJ ||
+                                           t.op == TILES_OP_GATEUP || t.op == TILES_OP_DOWN ||
+                                           t.op == TILES_OP_LMHEAD || (t.op == TILES_OP_QKV && t.layer > 0);
                 if (s.scheduler != TILES_SCHED_FLAGS || !tagged_inputs) return fail("task without a wait");
                 continue;
             }
@@ -477,23 +472,18 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
     if (s.final_ctr < 0 || s.final_ctr >= s.n_counters || (long long)s.final_mul != per_step[s.final_ctr])
         return fail("final wait");
     if (s.scheduler == TILES_SCHED_FLAGS) {
-        // The K/V written by an attention tile is read by TMA in later steps.
-        // Its only ordering is a chain of counters: attention -> (acquired by
-        // the O-projection tiles) -> LM-head signal -> first tile of the next
-        // step. So in every layer some CTA must both wait for the attention
-        // counter (an O-projection tile) and signal the LM-head counter.
-        std::vector<char> lm(N, 0);
-        for (int c = 0; c < N; ++c)
-            for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i)
-                if (s.tasks[i].op == TILES_OP_LMHEAD && s.tasks[i].signal_ctr != TILES_NO_COUNTER) lm[c] = 1;
-        for (int l = 0; l < g.L; ++l) {
-            bool linked = false;
-            for (int c = 0; c < N && !linked; ++c)
-                for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i) {
-                    const tiles_task &t = s.tasks[i];
-                    if (t.op == TILES_OP_OPROJ && t.layer == l && t.wait_ctr != TILES_NO_COUNTER && lm[c]) linked = true;
-                }
-            if (!linked) return fail("no CTA links a layer's attention to the next step");
+        // The K/V an attention tile writes is read by TMA in later steps, and
+        // its only ordering is a release by the same CTA: its LM-head tile's
+        // signal, which the first tile of the next step acquires. So every CTA
+        // with attention work must also signal the LM-head counter.
+        for (int c = 0; c < N; ++c) {
+            bool attn = false, lm = false;
+            for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i) {
+                const tiles_task &t = s.tasks[i];
+                attn |= t.op == TILES_OP_ATTN;
+                lm |= t.op == TILES_OP_LMHEAD && t.signal_ctr != TILES_NO_COUNTER;
+            }
+            if (attn && !lm) return fail("an attention CTA does not signal the LM head (K/V ordering)");
         }
     }
     return TILES_OK;

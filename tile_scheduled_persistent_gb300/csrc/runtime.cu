@@ -54,10 +54,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t align256(size_t v) { return (v + 255u) & ~(size_t)255u; }
 
-// The block of device memory every launch starts by zeroing:
-// argmax keys [64] | phase counters | x words [H] | a words [F] | Q/K/V words [rows].
+// The block of device memory every launch starts by zeroing: argmax keys [64] |
+// phase counters | x words [H] | a words [F] | o words [nq d] | Q/K/V words
+// [rows] | split partial words [nq][S][2 + d].
 struct SyncLayout {
-    size_t ctr, xw, aw, qkvw, bytes;
+    size_t ctr, xw, aw, ow, qkvw, partw, bytes;
 };
 SyncLayout sync_layout(const tiles_schedule_s &s) {
     const Geom &g = s.geom;
@@ -65,8 +66,10 @@ SyncLayout sync_layout(const tiles_schedule_s &s) {
     l.ctr = (size_t)kMaxStepsPerLaunch * 8;
     l.xw = align256(l.ctr + (size_t)s.n_counters * kCounterStride * 4);
     l.aw = align256(l.xw + (size_t)g.H * 4);
-    l.qkvw = align256(l.aw + (size_t)g.F * 4);
-    l.bytes = align256(l.qkvw + (size_t)g.qkv_rows * 8);
+    l.ow = align256(l.aw + (size_t)g.F * 4);
+    l.qkvw = align256(l.ow + (size_t)g.qd * 4);
+    l.partw = align256(l.qkvw + (size_t)g.qkv_rows * 8);
+    l.bytes = align256(l.partw + (size_t)g.nq * g.kv_splits * (2 + g.d) * 8);
     return l;
 }
 size_t sync_block_bytes(const tiles_schedule_s &s) { return sync_layout(s).bytes; }
@@ -76,7 +79,9 @@ void place_sync_block(const tiles_schedule_s &s, uint8_t *base, KernelParams *p)
     p->counters = reinterpret_cast<uint32_t *>(base + l.ctr);
     p->xw = reinterpret_cast<uint32_t *>(base + l.xw);
     p->aw = reinterpret_cast<uint32_t *>(base + l.aw);
+    p->ow = reinterpret_cast<uint32_t *>(base + l.ow);
     p->qkvw = reinterpret_cast<unsigned long long *>(base + l.qkvw);
+    p->partw = reinterpret_cast<unsigned long long *>(base + l.partw);
 }
 
 // RoPE inverse frequencies theta^(-2j/d) in FP64, with the published llama3
@@ -247,7 +252,6 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
         p.rope_sin = ds;
     }
     // scratch
-    if ((e = dalloc(plan, &p.partials, (size_t)g.nq * g.kv_splits * (kPartialPad + g.d) * 4)) != cudaSuccess) return fail(e);
     // one memset per launch clears: argmax keys | phase counters | tagged activations
     // (tag 0 is never written, so nothing of an earlier launch reads as ready)
     plan->sync_bytes = sync_block_bytes(plan->sched);
@@ -498,9 +502,9 @@ extern "C" tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache,
     if (n_new > 0 && !out_tokens) return TILES_ERR_INVALID_ARG;
     if (!aligned16(k_cache) || !aligned16(v_cache)) return TILES_ERR_INVALID_ARG;
     const Geom &g = plan->sched.geom;
-    // layout in the array: sync block (zeroed per launch) | split partials
-    const size_t off_part = align256(plan->sync_bytes);
-    const size_t need = off_part + align256((size_t)g.nq * g.kv_splits * (kPartialPad + g.d) * 4);
+    // the array holds the sync block (zeroed per launch): keys, counters and
+    // every tagged activation
+    const size_t need = plan->sync_bytes;
     if (need > kNoAllocScratchBytes) return TILES_ERR_CAPACITY;
     const long long steps = (long long)n_prompt - 1 + n_new;
     if (steps == 0) return TILES_OK;
@@ -511,7 +515,6 @@ extern "C" tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache,
     if ((st = noalloc_scratch(plan->device, &base)) != TILES_OK) return st;
     KernelParams p = plan->base;
     place_sync_block(plan->sched, base, &p);
-    p.partials = reinterpret_cast<float *>(base + off_part);
     p.k_cache = reinterpret_cast<uint16_t *>(k_cache);
     p.v_cache = reinterpret_cast<uint16_t *>(v_cache);
     p.prompt = prompt;

@@ -41,8 +41,6 @@ struct Geom {
     int rpc_qkv, rpc_o, rpc_gateup, rpc_down, rpc_lm;
     int vec_bytes;  // shared-memory region for the input vector / attention scratch
     int res_off;    // in the vec region: residual rows of an O-proj / down tile
-    int merge_off;    // in the vec region: split-merge scratch of the O-proj prologue
-    int merge_heads;  // q heads that prologue merges per pass (2 S + 1 floats each)
     int smem_bytes;
 };
 
@@ -73,7 +71,7 @@ TILES_HD int op_extent(const Geom &g, int op) {
     switch (op) {
         case TILES_OP_QKV: return g.qkv_rows;
         case TILES_OP_ATTN: return g.nkv * g.kv_splits;
-        case TILES_OP_COMBINE: return 0;  // merged into the attention phase (last split merges)
+        case TILES_OP_COMBINE: return 0;  // merged into the attention tiles (each merges 1/S)
         case TILES_OP_OPROJ: return g.H;
         case TILES_OP_GATEUP: return g.F;
         case TILES_OP_DOWN: return g.H;
@@ -177,11 +175,12 @@ struct KernelParams {
     const float *rope_cos, *rope_sin;  // [max_pos][d/2]
     // caches and scratch
     uint16_t *k_cache, *v_cache;
-    float *partials;
-    // tagged activations: (tag << 16) | bf16 for the residual stream x [H] and
-    // the SwiGLU output a [F]; (tag << 32) | f32 bits for the Q/K/V rows
-    uint32_t *xw, *aw;
-    unsigned long long *qkvw;
+    // tagged activations: (tag << 16) | bf16 for the residual stream x [H],
+    // the SwiGLU output a [F] and the attention output o [nq d];
+    // (tag << 32) | f32 bits for the Q/K/V rows and the split partials
+    // [nq][S][2 + d] (m, l, o of each q head and split)
+    uint32_t *xw, *aw, *ow;
+    unsigned long long *qkvw, *partw;
     unsigned long long *keys;
     uint32_t *counters, *status;
     // run
