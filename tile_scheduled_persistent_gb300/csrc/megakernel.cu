@@ -549,14 +549,19 @@ struct Producer {
 };
 
 // ------------------------------------------------------------------ L2 prefetch warp
-// Keeps HBM streaming while the ring is full and the consumers wait on a
-// dependency. The warp walks this CTA's tasks in the producers' order and
-// prefetches into L2, one 128-byte line per lane, the weight rows of each GEMV
-// tile and the cached K/V of each attention tile, at most l2_prefetch_bytes of
-// weights ahead of what the producers have handed to the ring. Issue is paced
-// (a token bucket in global-timer nanoseconds) so the warp does not queue more
-// requests than this SM's share of HBM bandwidth drains. It never makes the
-// kernel wait: when the producers finish or anything fails, it stops.
+// Warms L2 with the loads of the dependency chain. While the weight stream
+// saturates HBM, a copy the ring issues waits behind every copy in flight on
+// the GPU (the rings alone hold about 3 us of HBM traffic), and on the chain
+// Q/K/V -> attention -> O-projection that wait is pure latency. So the warp
+// walks this CTA's tasks in the producers' order and prefetches into L2, one
+// 128-byte line per lane, only the weight rows of the Q/K/V and O-projection
+// tiles and the cached K/V of the attention tiles, once the producers are
+// within l2_prefetch_bytes of weights of them: about one FFN phase ahead, so
+// they are in L2 when the ring asks. Gate/up, down and LM-head rows are left
+// to the ring (prefetching them too only adds DRAM traffic and congestion).
+// Issue may be paced (a token bucket in global-timer nanoseconds). The warp
+// never makes the kernel wait: when the producers finish or anything fails,
+// it stops.
 struct Prefetcher {
     const KernelParams &p;
     Smem &s;
@@ -607,6 +612,10 @@ struct Prefetcher {
                 if (op_is_gemv(t.op)) {
                     const unsigned long long rb = (unsigned long long)op_in_dim(g, t.op) * 2u * op_mats(t.op);
                     const unsigned long long bytes = (unsigned long long)(t.end - t.begin) * rb;
+                    if (t.op != TILES_OP_QKV && t.op != TILES_OP_OPROJ) {
+                        pos += bytes;  // streaming tiles: left to the ring
+                        continue;
+                    }
                     const unsigned long long sp = ld_volatile_u64(&s.ctl->stream_pos);
                     if (sp == ~0ull) return;
                     // skip what the producers already handed to the ring
