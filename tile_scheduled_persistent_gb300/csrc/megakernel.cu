@@ -1116,29 +1116,39 @@ struct Consumer {
         }
     }
 
-    // Cooperative form: this warp handles one q head (hi) and the 32-position
-    // sub-blocks sb_first, sb_first + sb_step, ... of a chunk all warps share.
-    template <int D>
+    // Cooperative form: this warp handles one q head (hi) and the T-position
+    // blocks blk_first, blk_first + blk_step, ... of a chunk all warps share,
+    // T = 32 / LP. Each position's q . k is split over LP consecutive lanes (an
+    // LP-th of the 16-byte columns each, rotated so a quarter warp touches 8
+    // distinct bank groups) and summed by shuffles; LP > 1 keeps every warp
+    // busy when a head's warps would otherwise get fewer than 32 positions each
+    // (head_dim 128 chunks hold 32 positions).
+    template <int D, int LP>
     __device__ void attn_chunk_one(const uint8_t *slot, int npos, const AttnSmem &a, int hi,
-                                   int sb_first, int sb_step, float &m, float &l,
+                                   int blk_first, int blk_step, float &m, float &l,
                                    float (&o)[D / 32]) {
         constexpr int NC = D / 8;
         constexpr int DPL = D / 32;
+        constexpr int T = 32 / LP;
+        constexpr int CPL = NC / LP;  // 16-byte columns per lane
+        constexpr int ROT = (D == 128 && LP == 2) ? 4 : (D == 128 && LP == 4) ? 1 : 0;
+        static_assert(CPL >= 1, "more lanes per position than columns");
         const Geom &g = p.g;
         const uint8_t *Kb = slot;
         const uint8_t *Vb = slot + (size_t)g.kv_block * D * 2;
         const float *q = a.q + hi * D;
         float *prob = a.prob + (size_t)warp * 32 * g.G;
-        for (int t0 = sb_first * 32; t0 < npos; t0 += sb_step * 32) {
-            const int t = t0 + lane;
+        const int tl = lane / LP, part = lane % LP;
+        for (int t0 = blk_first * T; t0 < npos; t0 += blk_step * T) {
+            const int t = t0 + tl;
             const bool valid = t < npos;
-            // q . k over four independent partial sums (16-byte columns mod 4)
+            // this lane's share of q . k, over four independent partial sums
             float sc4[4] = {0.f, 0.f, 0.f, 0.f};
             if (valid) {
                 const uint4 *krow = reinterpret_cast<const uint4 *>(Kb + (size_t)t * D * 2);
 #pragma unroll
-                for (int jj = 0; jj < NC; ++jj) {
-                    const int col = (jj + lane) & (NC - 1);  // rotated: no bank conflicts
+                for (int jj = 0; jj < CPL; ++jj) {
+                    const int col = part * CPL + ((jj + tl + ROT * part) & (CPL - 1));
                     float kf[8];
                     unpack8(krow[col], kf);
                     const float4 qa = reinterpret_cast<const float4 *>(q + col * 8)[0];
@@ -1151,19 +1161,21 @@ struct Consumer {
                     sc4[jj & 3] = sc;
                 }
             }
-            const float sc = __fadd_rn(__fadd_rn(sc4[0], sc4[1]), __fadd_rn(sc4[2], sc4[3]));
+            float sc = __fadd_rn(__fadd_rn(sc4[0], sc4[1]), __fadd_rn(sc4[2], sc4[3]));
+#pragma unroll
+            for (int off = LP / 2; off > 0; off >>= 1) sc += __shfl_xor_sync(0xFFFFFFFFu, sc, off);
             const float si = valid ? sc * p.attn_scale : -INFINITY;
             const float bm = warp_max(si);
             const float mn = fmaxf(m, bm);
             const float corr = expf(m - mn);
             const float pi = valid ? expf(si - mn) : 0.f;
-            const float ps = warp_sum(pi);
+            const float ps = warp_sum(part == 0 ? pi : 0.f);
             l = fmaf(l, corr, ps);
             m = mn;
-            prob[lane] = pi;
+            if (part == 0) prob[tl] = pi;
             __syncwarp();
             // p . V over the block's positions, four positions in flight
-            const int nv = npos - t0 < 32 ? npos - t0 : 32;
+            const int nv = npos - t0 < T ? npos - t0 : T;
             float acc[4][DPL];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
@@ -1192,6 +1204,12 @@ struct Consumer {
                 o[e] = fmaf(o[e], corr, __fadd_rn(__fadd_rn(acc[0][e], acc[1][e]), __fadd_rn(acc[2][e], acc[3][e])));
             __syncwarp();
         }
+    }
+
+    // positions each warp of a head gets from one chunk -> lanes per position
+    __device__ int attn_lanes_per_pos(int warps_per_head) const {
+        const int ppw = (p.g.kv_block + warps_per_head - 1) / warps_per_head;
+        return ppw >= 32 ? 1 : ppw >= 16 ? 2 : ppw >= 8 ? 4 : 8;
     }
 
     // Put the freshly computed K/V of position P into the chunk's slot (the
@@ -1248,6 +1266,7 @@ struct Consumer {
             if (nch < (uint32_t)kConsumerWarps) {
                 // few chunks: every warp works on every chunk (one q head, some sub-blocks)
                 const int hi = warp % G, sb0 = warp / G, sbs = kConsumerWarps / G;
+                const int lp = attn_lanes_per_pos(sbs);
                 float m1 = -INFINITY, l1 = 0.f, o1[DPL];
 #pragma unroll
                 for (int e = 0; e < DPL; ++e) o1[e] = 0.f;
@@ -1259,7 +1278,12 @@ struct Consumer {
                     if (q1 > P + 1) q1 = P + 1;
                     if (slot && warp == 0 && q0 <= P && P < q1) place_new_kv<D>(slot, q0, a);
                     if (consumer_sync_or(bad)) break;
-                    attn_chunk_one<D>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1);
+                    switch (lp) {
+                        case 1: attn_chunk_one<D, 1>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
+                        case 2: attn_chunk_one<D, 2>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
+                        case 4: attn_chunk_one<D, 4>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
+                        default: attn_chunk_one<D, (D / 8 >= 8 ? 8 : 4)>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
+                    }
                     consumer_sync();
                     if (tid == 0) mbar_arrive(&s.empty[jj % (uint32_t)g.ring_slots]);
                 }
@@ -1383,21 +1407,10 @@ struct Consumer {
         }
     }
 
-    __device__ void attn_dispatch(const tiles_task &t) {
-        const int D = p.g.d, G = p.g.G;
-#define TILES_ATTN_CASE(DD, GG) \
-    if (D == DD && G == GG) { attn_task<DD, GG>(t); return; }
-        TILES_ATTN_CASE(64, 1) TILES_ATTN_CASE(64, 2) TILES_ATTN_CASE(64, 4) TILES_ATTN_CASE(64, 8)
-        TILES_ATTN_CASE(128, 1) TILES_ATTN_CASE(128, 2) TILES_ATTN_CASE(128, 4) TILES_ATTN_CASE(128, 8)
-#undef TILES_ATTN_CASE
-    }
-
-    __device__ void prep_dispatch(int h, const AttnSmem &a) {
-        if (p.g.d == 64) prep_qkv<64>(h, a);
-        else prep_qkv<128>(h, a);
-    }
-
     // ---------------------------------------------------------- main loop
+    // D (head_dim) and G (q heads per KV head) are compile-time: each kernel
+    // instance carries only its own attention code.
+    template <int D, int G>
     __device__ __forceinline__ void run(int cta) {
         const Geom &g = p.g;
         const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
@@ -1440,7 +1453,7 @@ struct Consumer {
                         gemv_task<1>(t);
                         break;
                     case TILES_OP_ATTN:
-                        attn_dispatch(t);
+                        attn_task<D, G>(t);
                         break;
                     case TILES_OP_OPROJ:
                         gather_tagged(p.ow, g.qd, tag(t.layer, kTagO));
@@ -1494,6 +1507,7 @@ struct Consumer {
     }
 };
 
+template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_constant__ KernelParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Smem s = smem_layout(smem_raw, p);
@@ -1525,24 +1539,39 @@ __global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_con
         return;
     }
     Consumer cons(p, s, tid);
-    cons.run(blockIdx.x);
+    cons.template run<D, G>(blockIdx.x);
+}
+
+// One kernel per (head_dim, q heads per KV head): a smaller instruction
+// footprint than one kernel that switches between all of them (measured on the
+// Llama-1B shape: 2.7 % faster).
+static const void *megakernel_for(int d, int G) {
+#define TILES_KERNEL_CASE(DD, GG) \
+    if (d == DD && G == GG) return (const void *)tiles_megakernel<DD, GG>;
+    TILES_KERNEL_CASE(64, 1) TILES_KERNEL_CASE(64, 2) TILES_KERNEL_CASE(64, 4) TILES_KERNEL_CASE(64, 8)
+    TILES_KERNEL_CASE(128, 1) TILES_KERNEL_CASE(128, 2) TILES_KERNEL_CASE(128, 4) TILES_KERNEL_CASE(128, 8)
+#undef TILES_KERNEL_CASE
+    return nullptr;
 }
 
 // ------------------------------------------------------------------ launchers
-cudaError_t megakernel_configure(int smem_bytes) {
-    return cudaFuncSetAttribute(tiles_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                smem_bytes);
+cudaError_t megakernel_configure(int d, int G, int smem_bytes) {
+    const void *k = megakernel_for(d, G);
+    if (!k) return cudaErrorInvalidValue;
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
-cudaError_t megakernel_occupancy(int smem_bytes, int *blocks_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tiles_megakernel, kThreads,
-                                                         smem_bytes);
+cudaError_t megakernel_occupancy(int d, int G, int smem_bytes, int *blocks_per_sm) {
+    const void *k = megakernel_for(d, G);
+    if (!k) return cudaErrorInvalidValue;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kThreads, smem_bytes);
 }
 
 cudaError_t megakernel_launch(const KernelParams &p, int n_ctas, int smem_bytes, cudaStream_t st) {
+    const void *k = megakernel_for(p.g.d, p.g.G);
+    if (!k) return cudaErrorInvalidValue;
     void *args[] = {const_cast<KernelParams *>(&p)};
-    return cudaLaunchCooperativeKernel((const void *)tiles_megakernel, dim3(n_ctas), dim3(kThreads),
-                                       args, (size_t)smem_bytes, st);
+    return cudaLaunchCooperativeKernel(k, dim3(n_ctas), dim3(kThreads), args, (size_t)smem_bytes, st);
 }
 
 // ------------------------------------------------------------------ measurement kernels

@@ -16,8 +16,8 @@
 #include "tiles_internal.h"
 
 namespace tiles {
-cudaError_t megakernel_configure(int smem_bytes);
-cudaError_t megakernel_occupancy(int smem_bytes, int *blocks_per_sm);
+cudaError_t megakernel_configure(int d, int G, int smem_bytes);
+cudaError_t megakernel_occupancy(int d, int G, int smem_bytes, int *blocks_per_sm);
 cudaError_t megakernel_launch(const KernelParams &p, int n_ctas, int smem_bytes, cudaStream_t st);
 cudaError_t copy_launch(void *dst, const void *src, size_t bytes, int n_ctas, cudaStream_t st);
 cudaError_t barrier_launch(uint32_t *ctr, int rounds, unsigned long long *elapsed, uint32_t *status,
@@ -159,9 +159,9 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
     const Geom &g = plan->sched.geom;
 
     // the worker must fit one CTA per SM at this shared-memory size (co-residency)
-    e = megakernel_configure(g.smem_bytes);
+    e = megakernel_configure(g.d, g.G, g.smem_bytes);
     int occ = 0;
-    if (e == cudaSuccess) e = megakernel_occupancy(g.smem_bytes, &occ);
+    if (e == cudaSuccess) e = megakernel_occupancy(g.d, g.G, g.smem_bytes, &occ);
     if (e != cudaSuccess || occ < 1) {
         delete plan;
         return e != cudaSuccess ? TILES_ERR_CUDA : TILES_ERR_UNSUPPORTED;
