@@ -169,18 +169,44 @@ std::vector<Assign> assign_rows(int R, long long row_bytes, int N, std::vector<l
 
 // Single items (attention splits, combine heads) to the least-loaded CTAs,
 // consecutive items merged when they land on the same CTA.
+// Attention items -> CTAs: every CTA gets at most one contiguous range of
+// items (so one attention task per layer). An attention task computes all its
+// partials before merging, and a merge waits for every split of its head: a
+// CTA holding two separate tasks would compute the second task's partials
+// only after the first task's merge, delaying every merge of that head (or,
+// with two splits of one head, waiting on itself until the timeout). The
+// least-loaded CTAs so far take the items: with no more items than CTAs one
+// each, the heaviest item to the least-loaded CTA; otherwise contiguous ranges,
+// the first n_items mod N of them one item longer.
 std::vector<Assign> assign_items(int n_items, const std::vector<long long> &item_bytes, int N,
                                  std::vector<long long> &cum) {
+    std::vector<int> order(N);
+    for (int c = 0; c < N; ++c) order[c] = c;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cum[a] < cum[b]; });
+    if (n_items <= N) {
+        std::vector<int> items(n_items);
+        for (int i = 0; i < n_items; ++i) items[i] = i;
+        std::stable_sort(items.begin(), items.end(),
+                         [&](int a, int b) { return item_bytes[a] > item_bytes[b]; });
+        std::vector<Assign> out;
+        for (int k = 0; k < n_items; ++k) {
+            out.push_back({order[k], (uint32_t)items[k], (uint32_t)items[k] + 1});
+            cum[order[k]] += item_bytes[items[k]];
+        }
+        std::sort(out.begin(), out.end(), [](const Assign &x, const Assign &y) { return x.begin < y.begin; });
+        return out;
+    }
+    const int takers = N;
+    std::vector<int> ctas(order.begin(), order.begin() + takers);
+    std::sort(ctas.begin(), ctas.end());  // ranges in CTA order
     std::vector<Assign> out;
-    for (int it = 0; it < n_items; ++it) {
-        int best = 0;
-        for (int c = 1; c < N; ++c)
-            if (cum[c] < cum[best]) best = c;
-        cum[best] += item_bytes[it];
-        if (!out.empty() && out.back().cta == best && out.back().end == (uint32_t)it)
-            out.back().end += 1;
-        else
-            out.push_back({best, (uint32_t)it, (uint32_t)it + 1});
+    int it = 0;
+    for (int k = 0; k < takers; ++k) {
+        const int n = n_items / takers + (k < n_items % takers ? 1 : 0);
+        Assign a{ctas[k], (uint32_t)it, (uint32_t)(it + n)};
+        for (int i = it; i < it + n; ++i) cum[ctas[k]] += item_bytes[i];
+        it += n;
+        out.push_back(a);
     }
     return out;
 }
@@ -393,6 +419,15 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
             }
             if (t.wait_ctr != TILES_NO_COUNTER && t.wait_ctr >= s.n_counters)
                 return fail("wait counter out of range");
+        }
+    }
+    for (int c = 0; c < N; ++c) {
+        std::vector<char> seen(g.L, 0);
+        for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i) {
+            const tiles_task &t = s.tasks[i];
+            if (t.op != TILES_OP_ATTN) continue;
+            if (seen[t.layer]) return fail("two attention tasks of one layer on one CTA (merge order)");
+            seen[t.layer] = 1;
         }
     }
     for (int phi = 0; phi < PPS; ++phi) {
