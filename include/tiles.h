@@ -110,8 +110,15 @@ typedef struct {
     int32_t timeout_ms;   /* bound on every in-kernel wait; 0 = 2000 ms                  */
     int32_t l2_prefetch_kb; /* L2 prefetch warp: weight bytes it may run ahead of the ring, KB per CTA; <= 0 = off */
     int32_t l2_prefetch_gbs; /* its issue rate per CTA, GB/s (token bucket); <= 0 = unpaced */
-    uint32_t flags;       /* reserved, must be 0                                         */
+    uint32_t flags;       /* TILES_FLAG_* bits; 0 for normal use                         */
 } tiles_plan_opts;
+
+/* TILES_FLAG_INJECT_STALL is a test hook for failure detection. After the
+ * schedule is validated, the first tile of CTA 0 is made to wait for a
+ * counter value no launch reaches. Every bounded wait of the launch then runs
+ * out: the launch ends with TILES_ERR_TIMEOUT in the status word (read with
+ * tiles_status) after about timeout_ms, and nothing faults. */
+enum { TILES_FLAG_INJECT_STALL = 1u };
 
 typedef struct tiles_plan_s *tiles_plan_t;
 

@@ -185,6 +185,10 @@ def test_rejects_bad_options():
               tsp.make_opts(ring_slots=1)):
         with pytest.raises(tsp.TilesError):
             tsp.Schedule(d, 16, o)
+    with pytest.raises(tsp.TilesError):                      # unknown flag bits
+        tsp.Schedule(d, 16, tsp.make_opts(flags=2))
+    st, why = tsp.Schedule(d, 16, tsp.make_opts(flags=tsp.FLAG_INJECT_STALL)).validate()
+    assert st == 0, why                                      # the hook acts only at upload
 
 
 def test_waves_have_one_arrival_per_cta_and_phase():

@@ -200,6 +200,30 @@ def test_errors_are_reported_not_faulted(tsp, tiny):
     plan.close()
 
 
+@pytest.mark.parametrize("scheduler", [0, 1, 2], ids=["waves", "counters", "flags"])
+def test_a_wait_that_runs_out_is_reported_and_the_context_stays_usable(tsp, tiny, scheduler):
+    """Failure detection without a fault: CTA 0's first wait gets a target no
+    launch reaches (host-side injection), so every bounded wait of the launch
+    runs out; the status word says TIMEOUT, and a normal plan still decodes
+    correctly on the same context."""
+    import time
+    import torch
+    cfg, w, k, v, prompt, *_ = tiny
+    bad = _plan(tsp, cfg, w, scheduler=scheduler, timeout_ms=50, flags=tsp.FLAG_INJECT_STALL)
+    kc, vc = tsp.to_device_bf16(k), tsp.to_device_bf16(v)
+    out = torch.zeros(4, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    bad.decode(kc, vc, torch.from_numpy(np.asarray(prompt[:2], np.int32)).cuda(), 0, 4, out)
+    assert bad.status() == -7                                # TILES_ERR_TIMEOUT
+    assert time.time() - t0 < 30                             # bounded: ends by itself
+    bad.close()
+    good = _plan(tsp, cfg, w, scheduler=scheduler)
+    toks, logits, *_ = gpu_run(good, cfg, k, v, prompt[:4], 0, 2)
+    ref, *_ = oracle_run(cfg, w, k, v, prompt[:4], 0, 2)
+    assert_parity(toks, logits, ref, "after a timed-out launch")
+    good.close()
+
+
 def test_host_buffer_entry_point(tsp, tiny):
     cfg, w, k, v, prompt, ref, *_ = tiny
     plan = _plan(tsp, cfg, w)

@@ -18,6 +18,7 @@ STATUS_NAMES = {0: "TILES_OK", -1: "TILES_ERR_INVALID_ARG", -2: "TILES_ERR_UNSUP
                 -5: "TILES_ERR_CAPACITY", -6: "TILES_ERR_CUDA", -7: "TILES_ERR_TIMEOUT",
                 -8: "TILES_ERR_DEVICE_BOUNDS"}
 SCHED_WAVES, SCHED_COUNTERS, SCHED_FLAGS = 0, 1, 2
+FLAG_INJECT_STALL = 1  # test hook: CTA 0's first wait is never met (the launch times out)
 OPS = {1: "QKV", 2: "ATTN", 3: "COMBINE", 4: "OPROJ", 5: "GATEUP", 6: "DOWN", 7: "LMHEAD",
        8: "SYNC"}
 NO_COUNTER = 0xFFFF
@@ -160,10 +161,10 @@ def _check(status: int, what: str):
 
 
 def make_opts(scheduler=SCHED_FLAGS, n_ctas=0, slot_bytes=0, ring_slots=0, kv_splits=0,
-              timeout_ms=0, l2_prefetch_kb=0, l2_prefetch_gbs=0) -> PlanOpts:
+              timeout_ms=0, l2_prefetch_kb=0, l2_prefetch_gbs=0, flags=0) -> PlanOpts:
     return PlanOpts(scheduler=scheduler, n_ctas=n_ctas, slot_bytes=slot_bytes,
                     ring_slots=ring_slots, kv_splits=kv_splits, timeout_ms=timeout_ms,
-                    l2_prefetch_kb=l2_prefetch_kb, l2_prefetch_gbs=l2_prefetch_gbs, flags=0)
+                    l2_prefetch_kb=l2_prefetch_kb, l2_prefetch_gbs=l2_prefetch_gbs, flags=flags)
 
 
 # ------------------------------------------------------------------ schedule (host only)

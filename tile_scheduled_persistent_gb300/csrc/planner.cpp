@@ -67,7 +67,7 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     if ((long long)d.n_q_heads * d.head_dim > 65536 || d.hidden > 65536 || d.ffn > 65536)
         return fail(TILES_ERR_UNSUPPORTED, "dimension too large");
     if (n_ctas < 1 || n_ctas > 4096) return fail(TILES_ERR_INVALID_ARG, "n_ctas");
-    if (o.flags != 0) return fail(TILES_ERR_INVALID_ARG, "flags must be 0");
+    if (o.flags & ~(uint32_t)TILES_FLAG_INJECT_STALL) return fail(TILES_ERR_INVALID_ARG, "unknown flag bits");
     if (o.scheduler != TILES_SCHED_WAVES && o.scheduler != TILES_SCHED_COUNTERS &&
         o.scheduler != TILES_SCHED_FLAGS)
         return fail(TILES_ERR_INVALID_ARG, "scheduler");

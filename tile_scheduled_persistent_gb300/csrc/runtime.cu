@@ -220,8 +220,15 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
         lp[l].wqkv = qkv;
         lp[l].wgu = gu;
     }
-    e = cudaMemcpy(d_tasks, plan->sched.tasks.data(), plan->sched.tasks.size() * sizeof(tiles_task),
-                   cudaMemcpyHostToDevice);
+    {
+        // the validated table, or (test hook) with CTA 0's first wait on a target
+        // no launch reaches (counters stay far below 2^30)
+        std::vector<tiles_task> up = plan->sched.tasks;
+        if ((o.flags & TILES_FLAG_INJECT_STALL) && !up.empty() && plan->sched.offsets[1] > 0 &&
+            up[0].wait_ctr != TILES_NO_COUNTER)
+            up[0].wait_add += 0x40000000u;
+        e = cudaMemcpy(d_tasks, up.data(), up.size() * sizeof(tiles_task), cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess)
         e = cudaMemcpy(d_off, plan->sched.offsets.data(), plan->sched.offsets.size() * sizeof(int32_t),
                        cudaMemcpyHostToDevice);
