@@ -43,6 +43,14 @@ class OrcLayer(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in _SLOTS]
 
 
+_QSLOTS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
+class OrcQLayer(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _QSLOTS] + \
+               [(n, ctypes.c_void_p) for n in ("sq", "sk", "sv", "so", "s_gate", "s_up", "s_down")]
+
+
 def _build_one(path, extra, force):
     if not force and os.path.exists(path) and os.path.getmtime(path) >= os.path.getmtime(_SRC):
         return path
@@ -79,8 +87,11 @@ def lib(variant: str = "seq"):
             L.orc_gemv.argtypes = [vp, i32, i32, vp, vp]
             L.orc_attention.argtypes = [vp, vp, vp, i32, i32, f32, vp]
             L.orc_attention_split.argtypes = [vp, vp, vp, i32, i32, f32, i32, vp, vp]
+            L.orc_quantize_rows.argtypes = [vp, i32, i32, vp, vp]
+            L.orc_gemv_q8.argtypes = [vp, vp, i32, i32, vp, vp]
             L.orc_decode.argtypes = [ctypes.POINTER(OrcModel), ctypes.POINTER(OrcLayer), vp, vp,
-                                     vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32]
+                                     vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32,
+                                     ctypes.POINTER(OrcQLayer), vp, vp]
             L.orc_decode.restype = i32
             _libs[variant] = L
     return _libs[variant]
@@ -155,6 +166,39 @@ def gemv(W_bf16, x) -> np.ndarray:
     return y
 
 
+def quantize_rows(W_bf16):
+    """Weight-only INT8 of a [rows][cols] BF16 matrix: (codes int8 [rows][cols],
+    scales float32 [rows]), scale = row absmax / 127, codes rounded to nearest
+    even and clamped to +-127."""
+    W = _c(W_bf16, np.uint16)
+    Q = np.empty(W.shape, np.int8)
+    sc = np.empty(W.shape[0], np.float32)
+    lib().orc_quantize_rows(W.ctypes.data, W.shape[0], W.shape[1], Q.ctypes.data, sc.ctypes.data)
+    return Q, sc
+
+
+def gemv_q8(Q, scale, x) -> np.ndarray:
+    Q = _c(Q, np.int8)
+    sc = _c(scale, np.float32)
+    x = _c(x, np.float32)
+    y = np.empty(Q.shape[0], np.float32)
+    lib().orc_gemv_q8(Q.ctypes.data, sc.ctypes.data, Q.shape[0], Q.shape[1], x.ctypes.data,
+                      y.ctypes.data)
+    return y
+
+
+class QuantWeights:
+    """INT8 copies of every GEMV matrix of a model (``quantize_model``)."""
+    def __init__(self, layers, lm):
+        self.layers = layers      # per layer: {slot: (codes, scales)}
+        self.lm = lm              # (codes, scales) of the tied LM head
+
+
+def quantize_model(weights) -> QuantWeights:
+    layers = [{slot: quantize_rows(w[slot]) for slot in _QSLOTS} for w in weights.layers]
+    return QuantWeights(layers, quantize_rows(weights.embed))
+
+
 def attention(q, K_bf16, V_bf16, scale: float) -> np.ndarray:
     q = _c(q, np.float32)
     K = _c(K_bf16, np.uint16)
@@ -186,10 +230,12 @@ class DecodeResult:
 
 def decode(cfg, weights, k_cache, v_cache, prompt, start_pos: int, n_new: int,
            force_tokens=None, want_logits: bool = True, n_threads: int = 0,
-           variant: str = "seq") -> DecodeResult:
+           variant: str = "seq", qweights: QuantWeights | None = None) -> DecodeResult:
     """Run the oracle. ``weights`` is a ``synthetic.ModelWeights``; ``k_cache`` and
     ``v_cache`` are [L][n_kv][max_pos][d] uint16 arrays updated in place.
-    ``variant="alt"`` runs the build with the other GEMV summation order."""
+    ``variant="alt"`` runs the build with the other GEMV summation order.
+    With ``qweights`` (``quantize_model(weights)``) every GEMV uses the INT8
+    weights; the embedding lookup stays BF16."""
     prompt = _c(prompt, np.int32)
     n_prompt = prompt.size
     steps = n_prompt - 1 + n_new
@@ -213,10 +259,19 @@ def decode(cfg, weights, k_cache, v_cache, prompt, start_pos: int, n_new: int,
     gaps = np.empty(max(steps, 1), np.float32)
     force = None if force_tokens is None else _c(force_tokens, np.int32)
     m = model_struct(cfg)
+    qlayers, lm_q, lm_s = None, None, None
+    if qweights is not None:
+        qlayers = (OrcQLayer * cfg.n_layers)()
+        for l, ql in enumerate(qweights.layers):
+            for slot, sname in zip(_QSLOTS, ("sq", "sk", "sv", "so", "s_gate", "s_up", "s_down")):
+                codes, sc = ql[slot]
+                setattr(qlayers[l], slot, codes.ctypes.data)
+                setattr(qlayers[l], sname, sc.ctypes.data)
+        lm_q, lm_s = qweights.lm[0].ctypes.data, qweights.lm[1].ctypes.data
     rc = lib(variant).orc_decode(ctypes.byref(m), layers, embed.ctypes.data, fnorm.ctypes.data,
                           k_cache.ctypes.data, v_cache.ctypes.data, prompt.ctypes.data, n_prompt,
                           start_pos, n_new, _ptr(force), out_tokens.ctypes.data, _ptr(logits),
-                          gaps.ctypes.data, n_threads)
+                          gaps.ctypes.data, n_threads, qlayers, lm_q, lm_s)
     if rc != 0:
         raise ValueError(f"orc_decode rejected its arguments (rc={rc})")
     return DecodeResult(out_tokens[:n_new], logits, gaps[:steps])

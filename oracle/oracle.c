@@ -57,6 +57,13 @@ typedef struct {
         *w_up, *w_down;
 } orc_layer;
 
+/* Weight-only INT8 copies of one layer's matrices (codes [rows][cols] and one
+ * FP32 scale per output row), made by orc_quantize_rows. */
+typedef struct {
+    const int8_t *wq, *wk, *wv, *wo, *w_gate, *w_up, *w_down;
+    const float *sq, *sk, *sv, *so, *s_gate, *s_up, *s_down;
+} orc_qlayer;
+
 /* ------------------------------------------------------------------ bf16 */
 
 /* float -> bfloat16 bits, round to nearest, ties to even; NaN stays NaN. */
@@ -178,6 +185,52 @@ void orc_gemv(const uint16_t *W, int rows, int cols, const float *x, float *y) {
     }
 }
 
+/* ------------------------------------------------------------------ INT8 weights */
+
+/* Weight-only INT8 with one FP32 scale per output row ("History and roadmap",
+ * "Milestones": weight-only INT8 linear layers; the pages give no scheme, so
+ * the plainest one): scale_r = max_j |W_rj| / 127, q_rj = round(W_rj / scale_r)
+ * to nearest, ties to even, clamped to [-127, 127]; an all-zero row gets scale
+ * 0 and codes 0. Everything in FP32 (W is BF16, exact in FP32). */
+void orc_quantize_rows(const uint16_t *W, int rows, int cols, int8_t *Q, float *scale) {
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        const uint16_t *w = W + (int64_t)r * cols;
+        float amax = 0.0f;
+        for (int j = 0; j < cols; ++j) {
+            const float a = fabsf(orc_f32_from_bf16(w[j]));
+            if (a > amax) amax = a;
+        }
+        const float s = amax / 127.0f;
+        scale[r] = s;
+        for (int j = 0; j < cols; ++j) {
+            float qf = s > 0.0f ? rintf(orc_f32_from_bf16(w[j]) / s) : 0.0f;
+            if (qf > 127.0f) qf = 127.0f;
+            if (qf < -127.0f) qf = -127.0f;
+            Q[(int64_t)r * cols + j] = (int8_t)qf;
+        }
+    }
+}
+
+/* y[r] = scale[r] * sum_j Q[r][j] x[j]: the products are exact in FP32 (an
+ * 8-bit code times a BF16 value), summed left to right (or, in the
+ * ORC_ALT_SUM_ORDER build, in eight interleaved partial sums), then scaled. */
+void orc_gemv_q8(const int8_t *Q, const float *scale, int rows, int cols, const float *x, float *y) {
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        const int8_t *q = Q + (int64_t)r * cols;
+#ifdef ORC_ALT_SUM_ORDER
+        float pa[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int j = 0; j < cols; ++j) pa[j & 7] += (float)q[j] * x[j];
+        const float acc = ((pa[0] + pa[1]) + (pa[2] + pa[3])) + ((pa[4] + pa[5]) + (pa[6] + pa[7]));
+#else
+        float acc = 0.0f;
+        for (int j = 0; j < cols; ++j) acc += (float)q[j] * x[j];
+#endif
+        y[r] = scale[r] * acc;
+    }
+}
+
 /* ------------------------------------------------------------------ attention */
 
 /* One query head over positions 0..n-1 of one KV head ([n][d] bf16 rows):
@@ -268,13 +321,16 @@ static float silu(float z) { return z / (1.0f + expf(-z)); }
  * a diagnostic). Steps s >= n_prompt - 1 write out_tokens[s - n_prompt + 1].
  * Caches are [L][n_kv][max_pos][d] bf16, read at positions 0..P and written
  * at P. out_logits ([steps][vocab]) and out_gap ([steps], top-1 minus top-2
- * logit) may be NULL. Returns 0, or -1 on bad arguments.
+ * logit) may be NULL. With qlayers (and lm_q, lm_s for the tied LM head) the
+ * GEMVs use those INT8 weights (orc_gemv_q8); the embedding lookup stays BF16.
+ * Returns 0, or -1 on bad arguments.
  */
 int orc_decode(const orc_model *m, const orc_layer *layers, const uint16_t *embed,
                const uint16_t *final_norm, uint16_t *k_cache, uint16_t *v_cache,
                const int32_t *prompt, int n_prompt, int start_pos, int n_new,
                const int32_t *force_tokens, int32_t *out_tokens, float *out_logits,
-               float *out_gap, int n_threads) {
+               float *out_gap, int n_threads, const orc_qlayer *qlayers,
+               const int8_t *lm_q, const float *lm_s) {
     if (!m || !layers || !embed || !final_norm || !k_cache || !v_cache || !prompt ||
         n_prompt < 1 || n_new < 0 || start_pos < 0)
         return -1;
@@ -321,9 +377,16 @@ int orc_decode(const orc_model *m, const orc_layer *layers, const uint16_t *embe
 
             orc_rmsnorm(x, w->attn_norm, H, m->rms_eps, h);
             round_vec(h, H);
-            orc_gemv(w->wq, qd, H, h, q);
-            orc_gemv(w->wk, kvd, H, h, k);
-            orc_gemv(w->wv, kvd, H, h, v);
+            const orc_qlayer *qw = qlayers ? &qlayers[l] : NULL;
+            if (qw) {
+                orc_gemv_q8(qw->wq, qw->sq, qd, H, h, q);
+                orc_gemv_q8(qw->wk, qw->sk, kvd, H, h, k);
+                orc_gemv_q8(qw->wv, qw->sv, kvd, H, h, v);
+            } else {
+                orc_gemv(w->wq, qd, H, h, q);
+                orc_gemv(w->wk, kvd, H, h, k);
+                orc_gemv(w->wv, kvd, H, h, v);
+            }
             for (int i = 0; i < nq; ++i) {
                 if (m->qk_norm) {
                     orc_rmsnorm(q + i * d, w->q_norm, d, m->rms_eps, tmp);
@@ -353,22 +416,30 @@ int orc_decode(const orc_model *m, const orc_layer *layers, const uint16_t *embe
                               Vl + (int64_t)gi * m->max_pos * d, P + 1, d, scale, o + i * d);
             }
             round_vec(o, qd);
-            orc_gemv(w->wo, H, qd, o, y);
+            if (qw) orc_gemv_q8(qw->wo, qw->so, H, qd, o, y);
+            else orc_gemv(w->wo, H, qd, o, y);
             for (int i = 0; i < H; ++i) x[i] = orc_f32_from_bf16(orc_bf16_from_f32(x[i] + y[i]));
 
             orc_rmsnorm(x, w->ffn_norm, H, m->rms_eps, h);
             round_vec(h, H);
-            orc_gemv(w->w_gate, F, H, h, g);
-            orc_gemv(w->w_up, F, H, h, u);
+            if (qw) {
+                orc_gemv_q8(qw->w_gate, qw->s_gate, F, H, h, g);
+                orc_gemv_q8(qw->w_up, qw->s_up, F, H, h, u);
+            } else {
+                orc_gemv(w->w_gate, F, H, h, g);
+                orc_gemv(w->w_up, F, H, h, u);
+            }
             for (int i = 0; i < F; ++i) a[i] = silu(g[i]) * u[i];
             round_vec(a, F);
-            orc_gemv(w->w_down, H, F, a, y);
+            if (qw) orc_gemv_q8(qw->w_down, qw->s_down, H, F, a, y);
+            else orc_gemv(w->w_down, H, F, a, y);
             for (int i = 0; i < H; ++i) x[i] = orc_f32_from_bf16(orc_bf16_from_f32(x[i] + y[i]));
         }
 
         orc_rmsnorm(x, final_norm, H, m->rms_eps, h);
         round_vec(h, H);
-        orc_gemv(embed, V, H, h, logits);
+        if (lm_q) orc_gemv_q8(lm_q, lm_s, V, H, h, logits);
+        else orc_gemv(embed, V, H, h, logits);
         int best = 0;
         for (int r = 1; r < V; ++r)
             if (logits[r] > logits[best]) best = r;

@@ -373,3 +373,96 @@ def test_alternative_sum_order_build_is_the_same_function():
     b = O.decode(cfg, w, k.copy(), v.copy(), p, 0, 4, variant="alt")
     assert np.abs(a.logits - b.logits).max() < 1e-2      # well inside 3e-2 at two layers
     del ctypes
+
+
+# ----------------------------------------------------------------- INT8 weights
+def _bf16_exact(vals):
+    """float values that are exact in BF16 (checked), as BF16 bit patterns"""
+    b = O.bf16_from_f32(np.asarray(vals, np.float32))
+    assert np.array_equal(O.f32_from_bf16(b).ravel(), np.asarray(vals, np.float32).ravel())
+    return b.reshape(np.shape(vals))
+
+
+def test_quantize_power_of_two_scale_gives_exact_codes():
+    """Row absmax 127/128 makes the scale exactly 2^-7, so every code is the
+    value times 128. A divisor of 128 instead of 127, a dropped sign or a
+    per-matrix instead of per-row scale fails it."""
+    W = _bf16_exact(np.array([[127, -127, 64, 1, 0], [0, 0, 127, -2, 3]], np.float32) / 128)
+    Q, s = O.quantize_rows(W)
+    assert np.array_equal(Q, [[127, -127, 64, 1, 0], [0, 0, 127, -2, 3]])
+    assert np.array_equal(s, np.array([2.0 ** -7, 2.0 ** -7], np.float32))
+
+
+def test_quantize_ties_round_to_even():
+    """Codes 2.5 and -2.5 go to 2 and -2, 3.5 to 4: round half to even (half
+    away from zero would give 3, -3, 4)."""
+    W = _bf16_exact(np.array([[127, 2.5, -2.5, 3.5]], np.float32) / 128)
+    Q, _ = O.quantize_rows(W)
+    assert np.array_equal(Q, [[127, 2, -2, 4]])
+
+
+def test_quantize_zero_row_and_gemv_of_it():
+    W = np.zeros((2, 8), np.uint16)
+    W[1, 3] = 0x3F80                                   # 1.0
+    Q, s = O.quantize_rows(W)
+    assert s[0] == 0 and not Q[0].any()
+    assert Q[1, 3] == 127 and s[1] == np.float32(1.0) / np.float32(127.0)
+    y = O.gemv_q8(Q, s, np.arange(8, dtype=np.float32))
+    assert y[0] == 0.0
+
+
+def test_quantize_error_within_half_a_step_and_absmax_maps_to_127():
+    """On a random matrix: |w - q s| <= s/2 plus the FP32 rounding of w / s
+    (half an ulp of a quotient below 128: 128 * 2^-24 steps), and every row's
+    largest magnitude gets code +-127. A wrong scale or rounding rule misses
+    by a whole step."""
+    rng = np.random.default_rng(31)
+    W = O.bf16_from_f32(rng.normal(0, 0.02, (64, 257)).astype(np.float32)).reshape(64, 257)
+    Q, s = O.quantize_rows(W)
+    w = O.f32_from_bf16(W).reshape(64, 257).astype(np.float64)
+    err = np.abs(w - Q.astype(np.float64) * s[:, None].astype(np.float64))
+    assert (err <= s[:, None].astype(np.float64) * (0.5 + 128 * 2.0 ** -24)).all()
+    assert (np.abs(Q).max(axis=1) == 127).all()
+    assert (np.abs(Q[np.arange(64), np.abs(w).argmax(axis=1)]) == 127).all()
+
+
+def test_gemv_q8_matches_fp64_of_codes_times_scale():
+    """y = scale * (codes . x): against FP64 on a non-square matrix (a
+    transposed operand or a scale from the wrong row fails)."""
+    rng = np.random.default_rng(32)
+    W = O.bf16_from_f32(rng.normal(0, 0.02, (37, 300)).astype(np.float32)).reshape(37, 300)
+    Q, s = O.quantize_rows(W)
+    x = O.f32_from_bf16(O.bf16_from_f32(rng.normal(0, 1, 300).astype(np.float32)))
+    y = O.gemv_q8(Q, s, x)
+    ref = s.astype(np.float64) * (Q.astype(np.float64) @ x.astype(np.float64))
+    bound = 300 * 2.0 ** -23 * s.astype(np.float64) * (np.abs(Q).astype(np.float64) @ np.abs(x))
+    assert (np.abs(y - ref) <= bound + 1e-12).all()
+
+
+def test_decoder_int8_equals_bf16_when_weights_lie_on_the_int8_grid(tiny_cfg):
+    """Every weight row (and the tied embedding) is q * 2^-12 with integer
+    |q| <= 127 and one entry at +-127: quantizing gives back q with scale
+    exactly 2^-12, and scaling by a power of two commutes with rounding, so
+    the INT8 decode must equal the BF16 decode bit for bit. A mis-wired code
+    matrix or scale anywhere in the decoder fails it."""
+    cfg = tiny_cfg
+    rng = np.random.default_rng(33)
+    w = S.model_weights(cfg)
+
+    def grid(shape):
+        q = rng.integers(-127, 128, size=shape).astype(np.float32)
+        q[:, 0] = np.where(rng.random(shape[0]) < 0.5, 127, -127)   # absmax 127 in every row
+        return _bf16_exact(q * np.float32(2.0 ** -12))
+
+    for lw in w.layers:
+        for slot in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down"):
+            lw[slot] = grid(lw[slot].shape)
+    w.embed = grid(w.embed.shape)
+    qw = O.quantize_model(w)
+    assert all((sc == np.float32(2.0 ** -12)).all() for ql in qw.layers for _, sc in ql.values())
+    k, v = S.kv_prefill(cfg, n_pos=0)
+    p = S.prompt(cfg)[:6]
+    a = O.decode(cfg, w, k.copy(), v.copy(), p, 0, 5)
+    b = O.decode(cfg, w, k.copy(), v.copy(), p, 0, 5, qweights=qw)
+    assert np.array_equal(a.tokens, b.tokens)
+    assert np.array_equal(a.logits.view(np.uint32), b.logits.view(np.uint32))
