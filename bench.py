@@ -94,7 +94,7 @@ def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tile_scheduled_persistent_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".h", ".cpp")):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(f.read())
     return h.hexdigest()[:16]

@@ -100,6 +100,16 @@ typedef struct {
  * All three compute bit-identical results. */
 enum { TILES_SCHED_WAVES = 0, TILES_SCHED_COUNTERS = 1, TILES_SCHED_FLAGS = 2 };
 
+/* Weights the GEMV tiles stream. BF16: the caller's matrices (Q/K/V and
+ * gate/up repacked by the plan). INT8 ("History and roadmap", "Milestones":
+ * weight-only INT8 linear layers): at plan creation every GEMV matrix, the
+ * tied LM head included, is quantized per output row with
+ * tiles_quantize_rows_int8 into plan-owned codes and FP32 scales, and a GEMV
+ * row becomes scale * sum(code * x). Activations, norms, the KV cache and the
+ * embedding lookup stay BF16. INT8 needs hidden, ffn and n_q_heads * head_dim
+ * to be multiples of 16. */
+enum { TILES_WEIGHTS_BF16 = 0, TILES_WEIGHTS_INT8 = 1 };
+
 /* Planner options; pass NULL to tiles_plan_create for the defaults (shown). */
 typedef struct {
     int32_t scheduler;    /* TILES_SCHED_FLAGS (default), _COUNTERS or _WAVES            */
@@ -110,6 +120,7 @@ typedef struct {
     int32_t timeout_ms;   /* bound on every in-kernel wait; 0 = 2000 ms                  */
     int32_t l2_prefetch_kb; /* L2 prefetch warp: weight bytes it may run ahead of the ring, KB per CTA; <= 0 = off */
     int32_t l2_prefetch_gbs; /* its issue rate per CTA, GB/s (token bucket); <= 0 = unpaced */
+    int32_t weight_format; /* TILES_WEIGHTS_BF16 (default) or TILES_WEIGHTS_INT8           */
     uint32_t flags;       /* TILES_FLAG_* bits; 0 for normal use                         */
 } tiles_plan_opts;
 
@@ -279,6 +290,17 @@ tiles_status_t tiles_schedule_tasks(tiles_schedule_t sched, tiles_task **tasks,
 tiles_status_t tiles_schedule_cta_bytes(tiles_schedule_t sched, int32_t pos, int64_t *bytes);
 
 void tiles_schedule_destroy(tiles_schedule_t sched);
+
+/* Weight-only INT8 quantization of a row-major [rows][cols] BF16 matrix (device
+ * pointers), one output row per CTA, asynchronous on stream: scales[r] =
+ * max_j |w_rj| / 127 and codes[r][j] = w_rj / scales[r] rounded to nearest
+ * even and clamped to [-127, 127], in FP32 (an all-zero row gets scale 0 and
+ * codes 0). The same kernel quantizes a plan's weights when weight_format is
+ * TILES_WEIGHTS_INT8. codes: rows * cols int8; scales: rows floats; both
+ * caller-owned. TILES_ERR_INVALID_ARG on a null pointer (rows > 0), rows < 0
+ * or cols < 1; TILES_ERR_CUDA if the launch fails. */
+tiles_status_t tiles_quantize_rows_int8(const void *w_bf16, int32_t rows, int32_t cols, void *codes,
+                                        float *scales, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* Measurement helpers.                                                       */

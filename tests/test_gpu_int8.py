@@ -1,0 +1,134 @@
+"""Weight-only INT8 GEMV tiles against the INT8 oracle, through the C ABI.
+
+The plan quantizes every GEMV matrix per output row on the device
+(tiles_quantize_rows_int8). Its codes and scales must equal the oracle's
+quantizer bit for bit, because a code is an integer decided in FP32 on both
+sides. The decoder is then held to the same bars as the BF16 path: strict
+tolerance where the depth allows it, the measured noise floor at full depth.
+"""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as S
+from gpu_helpers import assert_parity, gpu_run, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tsp():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import tile_scheduled_persistent_gb300 as t
+    t.build()
+    return t
+
+
+def _plan(tsp, cfg, w, **opts):
+    return tsp.Plan(tsp.ModelDesc.from_config(cfg), tsp.upload_weights(w),
+                    tsp.make_opts(weight_format=tsp.WEIGHTS_INT8, **opts))
+
+
+def _oracle_q8(cfg, w, qw, k, v, prompt, start_pos, n_new, force=None, variant="seq"):
+    return oracle.decode(cfg, w, k.copy(), v.copy(), prompt, start_pos, n_new,
+                         force_tokens=force, qweights=qw, variant=variant)
+
+
+@pytest.mark.parametrize("shape", [(7, 256), (64, 2048), (3, 8192), (128256, 64)])
+def test_device_quantization_equals_oracle_bit_for_bit(tsp, shape):
+    import torch
+    rng = np.random.default_rng(shape[0] * 7 + shape[1])
+    W = oracle.bf16_from_f32(rng.normal(0, 0.02, shape).astype(np.float32)).reshape(shape)
+    W[0] = 0                                              # an all-zero row
+    if shape[1] >= 4:                                     # ties: codes 2.5 and -2.5 (scale 2^-7)
+        W[-1, :4] = oracle.bf16_from_f32(np.array([127, 2.5, -2.5, 3.5], np.float32) / 128)
+        W[-1, 4:] = 0
+    Wd = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
+    codes, scales = tsp.quantize_rows_int8(Wd)
+    torch.cuda.synchronize()
+    Q, s = oracle.quantize_rows(W)
+    assert np.array_equal(codes.cpu().numpy(), Q)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
+def test_tiny_int8_matches_int8_oracle_and_is_bitwise_across_schedulers(tsp):
+    cfg = S.CONFIGS["tiny"]
+    w, k, v, prompt = inputs(cfg, n_pos=0)
+    qw = oracle.quantize_model(w)
+    ref = _oracle_q8(cfg, w, qw, k, v, prompt, 0, cfg.n_new)
+    outs = []
+    for sched in (2, 1, 0):
+        plan = _plan(tsp, cfg, w, scheduler=sched)
+        outs.append(gpu_run(plan, cfg, k, v, prompt, 0, cfg.n_new))
+        plan.close()
+    assert_parity(outs[0][0], outs[0][1], ref, "tiny int8")
+    for o in outs[1:]:
+        assert np.array_equal(o[0], outs[0][0])
+        assert np.array_equal(o[1].view(np.uint32), outs[0][1].view(np.uint32))
+
+
+VARIANTS = {
+    "d128_g8_qknorm": replace(S.CONFIGS["tiny"], name="v1", head_dim=128, n_q_heads=8,
+                              n_kv_heads=1, qk_norm=True, rope_theta=1e6, rms_eps=1e-6),
+    "g2_cache": replace(S.CONFIGS["tiny"], name="v3", start_pos=150, n_prompt=3, n_new=20,
+                        max_pos=200),
+}
+
+
+@pytest.mark.parametrize("name", list(VARIANTS))
+def test_int8_variants_match_int8_oracle(tsp, name):
+    cfg = VARIANTS[name]
+    w, k, v, prompt = inputs(cfg)
+    prompt = prompt[: cfg.n_prompt]
+    ref = _oracle_q8(cfg, w, oracle.quantize_model(w), k, v, prompt, cfg.start_pos, cfg.n_new)
+    plan = _plan(tsp, cfg, w)
+    toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, cfg.n_new)
+    assert_parity(toks, logits, ref, name + " int8")
+    plan.close()
+
+
+def test_int8_rejects_rows_not_a_multiple_of_16(tsp):
+    cfg = replace(S.CONFIGS["tiny"], hidden=264, ffn=776, vocab=1000)
+    d = tsp.ModelDesc.from_config(cfg)
+    with pytest.raises(tsp.TilesError) as e:
+        tsp.Schedule(d, 16, tsp.make_opts(weight_format=tsp.WEIGHTS_INT8))
+    assert e.value.status == -2
+
+
+@pytest.mark.parametrize("name", ["llama1b", "qwen3_0_6b"])
+def test_int8_full_width_one_layer_slice_strict_tolerance(tsp, name):
+    cfg = replace(S.CONFIGS[name], n_layers=1)
+    n_new = 8
+    w, k, v, prompt = inputs(cfg)
+    ref = _oracle_q8(cfg, w, oracle.quantize_model(w), k, v, prompt, cfg.start_pos, n_new)
+    plan = _plan(tsp, cfg, w)
+    toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, n_new)
+    assert_parity(toks, logits, ref, name + " int8 one layer")
+    plan.close()
+
+
+def test_int8_full_depth_within_noise_floor(tsp):
+    """Llama-1B shape at full depth, every logit of 32 steps, teacher-forced:
+    the same noise-floor bar as the BF16 path, against the INT8 oracle and its
+    other-summation-order build."""
+    cfg = S.CONFIGS["llama1b"]
+    n_new = 32
+    w, k, v, prompt = inputs(cfg)
+    qw = oracle.quantize_model(w)
+    plan = _plan(tsp, cfg, w)
+    toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, n_new)
+    plan.close()
+    force = toks[:-1]
+    ref = _oracle_q8(cfg, w, qw, k, v, prompt, cfg.start_pos, n_new, force=force)
+    alt = _oracle_q8(cfg, w, qw, k, v, prompt, cfg.start_pos, n_new, force=force, variant="alt")
+    noise = np.abs(alt.logits - ref.logits).max(axis=1)
+    err = np.abs(logits - ref.logits)
+    bound = 3e-2 + 1e-2 * np.abs(ref.logits) + 1.5 * noise[:, None]
+    assert not np.isnan(logits).any()
+    assert (err <= bound).all(), (f"{int((err > bound).sum())} logits beyond the noise floor; "
+                                  f"max err {err.max():.3e}, max noise {noise.max():.3e}")
+    assert err.mean() <= 2.0 * np.abs(alt.logits - ref.logits).mean() + 1e-3

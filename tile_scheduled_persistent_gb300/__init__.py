@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "TILES_OK", -1: "TILES_ERR_INVALID_ARG", -2: "TILES_ERR_UNSUP
                 -8: "TILES_ERR_DEVICE_BOUNDS"}
 SCHED_WAVES, SCHED_COUNTERS, SCHED_FLAGS = 0, 1, 2
 FLAG_INJECT_STALL = 1  # test hook: CTA 0's first wait is never met (the launch times out)
+WEIGHTS_BF16, WEIGHTS_INT8 = 0, 1
 OPS = {1: "QKV", 2: "ATTN", 3: "COMBINE", 4: "OPROJ", 5: "GATEUP", 6: "DOWN", 7: "LMHEAD",
        8: "SYNC"}
 NO_COUNTER = 0xFFFF
@@ -66,7 +67,7 @@ class Weights(ctypes.Structure):
 class PlanOpts(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("scheduler", "n_ctas", "slot_bytes", "ring_slots", "kv_splits", "timeout_ms",
-                 "l2_prefetch_kb", "l2_prefetch_gbs")] + \
+                 "l2_prefetch_kb", "l2_prefetch_gbs", "weight_format")] + \
                [("flags", ctypes.c_uint32)]
 
 
@@ -96,7 +97,7 @@ EXPORTS = ("tiles_plan_create", "tiles_plan_destroy", "tiles_decode", "tiles_dec
            "tiles_status", "tiles_status_string", "tiles_plan_get_info", "tiles_schedule_build",
            "tiles_schedule_validate", "tiles_schedule_tasks", "tiles_schedule_cta_bytes",
            "tiles_schedule_destroy", "tiles_copy_bw", "tiles_barrier_cost", "tiles_plan_set_trace",
-           "tiles_decode_noalloc")
+           "tiles_decode_noalloc", "tiles_quantize_rows_int8")
 
 _lib_handle = None
 
@@ -144,6 +145,8 @@ def _lib():
         L.tiles_schedule_destroy.restype = None
         L.tiles_copy_bw.argtypes = [vp, vp, ctypes.c_size_t, i32, vp]
         L.tiles_copy_bw.restype = st
+        L.tiles_quantize_rows_int8.argtypes = [vp, i32, i32, vp, vp, vp]
+        L.tiles_quantize_rows_int8.restype = st
         L.tiles_barrier_cost.argtypes = [i32, i32, ctypes.POINTER(ctypes.c_double)]
         L.tiles_barrier_cost.restype = st
         _lib_handle = L
@@ -161,10 +164,12 @@ def _check(status: int, what: str):
 
 
 def make_opts(scheduler=SCHED_FLAGS, n_ctas=0, slot_bytes=0, ring_slots=0, kv_splits=0,
-              timeout_ms=0, l2_prefetch_kb=0, l2_prefetch_gbs=0, flags=0) -> PlanOpts:
+              timeout_ms=0, l2_prefetch_kb=0, l2_prefetch_gbs=0, flags=0,
+              weight_format=0) -> PlanOpts:
     return PlanOpts(scheduler=scheduler, n_ctas=n_ctas, slot_bytes=slot_bytes,
                     ring_slots=ring_slots, kv_splits=kv_splits, timeout_ms=timeout_ms,
-                    l2_prefetch_kb=l2_prefetch_kb, l2_prefetch_gbs=l2_prefetch_gbs, flags=flags)
+                    l2_prefetch_kb=l2_prefetch_kb, l2_prefetch_gbs=l2_prefetch_gbs, flags=flags,
+                    weight_format=weight_format)
 
 
 # ------------------------------------------------------------------ schedule (host only)
@@ -309,6 +314,19 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+def quantize_rows_int8(w_bf16, stream=None):
+    """Weight-only INT8 of a [rows][cols] BF16 CUDA tensor on the device (the
+    kernel plans use): (codes int8 [rows][cols], scales float32 [rows])."""
+    import torch
+    assert w_bf16.is_cuda and w_bf16.dtype == torch.bfloat16 and w_bf16.dim() == 2
+    w = w_bf16.contiguous()
+    codes = torch.empty(w.shape, dtype=torch.int8, device=w.device)
+    scales = torch.empty(w.shape[0], dtype=torch.float32, device=w.device)
+    _check(_lib().tiles_quantize_rows_int8(_ptr(w), w.shape[0], w.shape[1], _ptr(codes), _ptr(scales),
+                                           _stream_ptr(stream)), "tiles_quantize_rows_int8")
+    return codes, scales
 
 
 def copy_bw(dst, src, n_ctas: int = 0, stream=None) -> None:

@@ -1,6 +1,6 @@
 """Builds libtiles.so (the CUDA library behind include/tiles.h) in place.
 
-nvcc for the two CUDA translation units (sm_103a only), g++ for the host
+nvcc for the CUDA translation units (sm_103a only), g++ for the host
 planner, compiled in parallel, linked with the static CUDA runtime.
 """
 from __future__ import annotations
@@ -15,8 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libtiles.so")
 BUILD = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["megakernel.cu", "runtime.cu", "planner.cpp"]
-HEADERS = ["tiles_internal.h"]
+SOURCES = ["megakernel.cu", "kernels_bf16.cu", "kernels_int8.cu", "runtime.cu", "planner.cpp"]
+HEADERS = ["tiles_internal.h", "megakernel.cuh"]
 
 
 def _nvcc() -> str:

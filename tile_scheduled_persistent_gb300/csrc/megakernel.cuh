@@ -1,0 +1,1621 @@
+// The persistent decode kernel for sm_103a.
+//
+// One CTA per SM runs its static task list once per step, for up to 64 steps
+// per cooperative launch ("Tiles: Scheduling LLM Decoding as a Graph of
+// Tiles", intro and "What the code contains": a fixed worker per SM executes a
+// planned schedule, greedy selection inside the kernel, up to 64 tokens per
+// launch). Each CTA has
+//   - one producer warp: a single lane walks the same task list as the
+//     consumers and streams every tile's weight rows (or K/V positions) into a
+//     shared-memory ring with cp.async.bulk (TMA) copies, completing on per-slot
+//     mbarriers. Weights never depend on activations, so the stream runs ahead
+//     across phase boundaries and keeps HBM busy while the consumers wait
+//     (the megakernel paragraph of the same page: load the next weights while
+//     the current work finishes).
+//   - eight consumer warps: chunk j of the CTA's stream goes to ring slot
+//     j % slots, and each slot has one owning warp, (j % slots) % 8. GEMV chunks: 16-byte bf16 loads from shared memory,
+//     FP32 FMA, warp-shuffle reductions. Attention chunks: split-KV online
+//     softmax over up to kv_block positions per chunk.
+// Phases are ordered by counters in global memory (one grid barrier per phase
+// in the wave schedule, or per-phase dependency counters): release-add after a
+// task, acquire-spin before one. Every spin is bounded by the global timer;
+// on expiry the CTA records an error in the status word, drains its copies in
+// flight and returns, and every other CTA leaves at its next wait.
+//
+// Fused work (same page, intro: norms and activations fold into the tiles
+// next to them; "History and roadmap", "M8 so far": q/k norm + RoPE + KV
+// write, residual + RMSNorm and SwiGLU-in-GEMV fusions):
+//   QKV tiles     RMSNorm of the residual in the prologue
+//   ATTN tiles    per-head q/k RMSNorm, RoPE, KV write at the new position
+//   O / DOWN      residual add in the epilogue
+//   GATE/UP       RMSNorm prologue, SwiGLU epilogue
+//   LM head       final RMSNorm prologue, argmax epilogue (packed 64-bit
+//                 atomicMax: ordered logit bits high, inverted row low, so the
+//                 lowest row wins ties)
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tiles_internal.h"
+
+namespace tiles {
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         unsigned long long policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_nohint(void *dst, const void *src, uint32_t bytes,
+                                                uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *src) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+}
+__device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"((uint32_t)__cvta_generic_to_shared(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_volatile_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.volatile.shared.u64 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(p)), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void st_relaxed_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4(const uint32_t *p) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_volatile(const uint32_t *p) {
+    return *(const volatile uint32_t *)p;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_release_cta(int *p, int v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_cta(const int *p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// Consumer barrier that also ORs a flag over all consumer threads: every thread
+// gets the same answer, so leaving on it keeps the barrier sequence aligned.
+__device__ __forceinline__ bool consumer_sync_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kConsumerWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
+// ------------------------------------------------------------------ numerics
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// float -> bfloat16, round to nearest even (finite inputs; NaN kept as NaN)
+__device__ __forceinline__ uint16_t f2bf(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+__device__ __forceinline__ float round_bf(float f) { return bf2f(f2bf(f)); }
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+    f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
+    f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
+}
+
+__device__ __forceinline__ float dot8(const uint4 &w, const float (&x)[8], float acc) {
+    acc = fmaf(bf_lo(w.x), x[0], acc); acc = fmaf(bf_hi(w.x), x[1], acc);
+    acc = fmaf(bf_lo(w.y), x[2], acc); acc = fmaf(bf_hi(w.y), x[3], acc);
+    acc = fmaf(bf_lo(w.z), x[4], acc); acc = fmaf(bf_hi(w.z), x[5], acc);
+    acc = fmaf(bf_lo(w.w), x[6], acc); acc = fmaf(bf_hi(w.w), x[7], acc);
+    return acc;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+// order-preserving key of (logit, row): bigger logit first, lower row on ties
+__device__ __forceinline__ unsigned long long argmax_key(float f, uint32_t row) {
+    uint32_t u = __float_as_uint(f);
+    uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - row);
+}
+__device__ __forceinline__ int key_row(unsigned long long k) {
+    return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+}
+
+// ------------------------------------------------------------------ shared state
+struct Ctl {
+    int unused;
+    int token;
+    int step_ready;  // consumers passed the first wait of this step (KV of earlier steps visible)
+    float red[kConsumerWarps];
+    unsigned long long warp_key[kConsumerWarps];
+    unsigned long long stream_pos;  // weight bytes the producers have handed to the ring
+};
+
+static_assert(2 * kMaxSlots * 8 + sizeof(Ctl) <= (size_t)kCtlBytes, "control block overflows its region");
+
+struct Smem {
+    uint64_t *full, *empty;
+    Ctl *ctl;
+    uint8_t *ring;
+    uint8_t *vec;
+};
+
+__device__ __forceinline__ Smem smem_layout(uint8_t *base, const KernelParams &p) {
+    Smem s;
+    s.full = reinterpret_cast<uint64_t *>(base);
+    s.empty = s.full + kMaxSlots;
+    s.ctl = reinterpret_cast<Ctl *>(base + 2 * kMaxSlots * 8);
+    s.ring = base + p.ring_off;
+    s.vec = base + p.vec_off;
+    return s;
+}
+
+__device__ __forceinline__ bool failed(const KernelParams &p) { return ld_volatile(p.status) != 0; }
+
+// ------------------------------------------------------------------ tagged activations
+// Activation words carry the tag of the phase that wrote them:
+// 1 + 6 (step L + layer) + kind, with kind 0 for the Q/K/V rows, 1 for x after
+// the O-projection, 2 for the SwiGLU output a, 3 for x after the down
+// projection, 4 for the split partials, 5 for the merged attention output o.
+// The step is the launch's own (< 64), so within a launch no tag repeats (at
+// most 384 L < 2^16), and every launch starts from zeroed words, so 0 never
+// matches and nothing of an earlier launch reads as ready.
+enum { kTagQKV = 0, kTagXAttn = 1, kTagA = 2, kTagXFfn = 3, kTagPart = 4, kTagO = 5 };
+__device__ __forceinline__ uint32_t act_tag(const KernelParams &p, int step, int layer, int kind) {
+    return 1u + 6u * ((uint32_t)step * (uint32_t)p.g.L + (uint32_t)layer) + (uint32_t)kind;
+}
+
+// Bounded polling of tagged words, like every other wait: the global timer
+// limits it, and a failure elsewhere ends it.
+struct Poll {
+    unsigned long long t0 = 0;
+    uint32_t spins = 0;
+    // false: stop polling (timeout recorded in the status word, or the run is aborting)
+    __device__ bool again(const KernelParams &p) {
+        if (t0 == 0) t0 = global_timer();
+        if ((++spins & 31u) == 0) {
+            if (failed(p)) return false;
+            if (global_timer() - t0 > p.timeout_ns) {
+                atomicOr(p.status, kDevTimeout);
+                return false;
+            }
+        }
+        return true;
+    }
+};
+
+__device__ __forceinline__ bool tags_ok4(const uint4 &w, uint32_t tag) {
+    return ((w.x >> 16) == tag) & ((w.y >> 16) == tag) & ((w.z >> 16) == tag) & ((w.w >> 16) == tag);
+}
+// the bf16 halves of 8 tagged words, packed as 8 consecutive bf16
+__device__ __forceinline__ uint4 untag8(const uint4 &lo, const uint4 &hi) {
+    return make_uint4(__byte_perm(lo.x, lo.y, 0x5410), __byte_perm(lo.z, lo.w, 0x5410),
+                      __byte_perm(hi.x, hi.y, 0x5410), __byte_perm(hi.z, hi.w, 0x5410));
+}
+
+__device__ __forceinline__ unsigned long long *trace_rec(const KernelParams &p, int cta, int step,
+                                                         int task) {
+    if (!p.trace || step >= p.trace_steps) return nullptr;
+    return p.trace + (((size_t)cta * p.trace_steps + step) * p.trace_tasks + task) * kTraceWords;
+}
+
+// Bounded spin until counter >= target. false when the run is aborting.
+// Acquire side of a dependency counter: relaxed polls, one acquire fence once
+// the target is seen (the signal side is a release reduction after a CTA
+// barrier, which orders every thread's writes of the tile before it).
+static __device__ bool wait_counter(const KernelParams &p, const uint32_t *ctr, uint32_t target) {
+    if (ld_relaxed(ctr) >= target) {
+        fence_acquire_gpu();
+        return true;
+    }
+    unsigned long long t0 = global_timer();
+    for (uint32_t spin = 1;; ++spin) {
+        if (ld_relaxed(ctr) >= target) {
+            fence_acquire_gpu();
+            return true;
+        }
+        if ((spin & 31u) == 0) {
+            if (failed(p)) return false;
+            if (global_timer() - t0 > p.timeout_ns) {
+                atomicOr(p.status, kDevTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded mbarrier wait. false on timeout or when the run is aborting.
+static __device__ bool wait_mbar(const KernelParams &p, uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0 = global_timer();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 15u) == 0) {
+            if (failed(p)) return false;
+            if (global_timer() - t0 > p.timeout_ns) {
+                atomicOr(p.status, kDevTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ producer
+struct Producer {
+    const KernelParams &p;
+    Smem &s;
+    uint32_t j = 0;  // chunks issued
+    bool ok = true;
+    unsigned long long pol_weights;  // L2 evict-first: weights are streamed once per step
+    unsigned long long stall = 0;    // ns spent waiting for a free slot (traced runs)
+    bool tracing = false;
+    int pid = 0;                     // this producer issues chunks of slots with slot % 2 == pid
+
+    __device__ Producer(const KernelParams &p_, Smem &s_, int pid_) : p(p_), s(s_), pid(pid_) {
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_weights));
+    }
+
+    // Weight rows [r0, ...) of a GEMV tile (BF16 or INT8 codes): where they
+    // start in HBM. A gate/up row is the pair of packed rows (gate, up).
+    __device__ const uint8_t *gemv_src(int op, int layer, uint32_t r0) const {
+        const LayerPtrs &lw = p.layers[layer];
+        const size_t rb = (size_t)op_in_dim(p.g, op) * p.g.wbytes * op_mats(op);
+        switch (op) {
+            case TILES_OP_QKV: return lw.qkv + r0 * rb;
+            case TILES_OP_OPROJ: return lw.o + r0 * rb;
+            case TILES_OP_GATEUP: return lw.gu + r0 * rb;
+            case TILES_OP_DOWN: return lw.down + r0 * rb;
+            default: return p.lm + r0 * rb;
+        }
+    }
+
+    unsigned long long stream_bytes = 0;  // weight bytes of every chunk passed so far
+
+    // Chunk j's slot belongs to this producer?
+    __device__ bool owns(uint32_t jj) const {
+        return (int)((jj % (uint32_t)p.g.ring_slots) % kProducerWarps) == pid;
+    }
+
+    // Reserve the next slot: wait until its previous chunk was consumed.
+    __device__ uint8_t *acquire(uint64_t **bar) {
+        const uint32_t ns = (uint32_t)p.g.ring_slots;
+        uint32_t slot = j % ns;
+        if (j >= ns) {
+            unsigned long long t0 = tracing ? global_timer() : 0;
+            const uint32_t par = ((j / ns) - 1u) & 1u;
+            if (!wait_mbar(p, &s.empty[slot], par)) {
+                ok = false;
+                return nullptr;
+            }
+            if (tracing) stall += global_timer() - t0;
+        }
+        *bar = &s.full[slot];
+        return s.ring + (size_t)slot * p.g.slot_bytes;
+    }
+
+    __device__ void gemv_chunk(int op, int layer, uint32_t r0, uint32_t nr) {
+        stream_bytes += (unsigned long long)nr * op_in_dim(p.g, op) * p.g.wbytes * op_mats(op);
+        if (pid == 0) st_volatile_u64(&s.ctl->stream_pos, stream_bytes);
+        if (!owns(j)) {
+            ++j;
+            return;
+        }
+        uint64_t *bar;
+        uint8_t *dst = acquire(&bar);
+        if (!dst) return;
+        // the chunk's rows are contiguous (Q/K/V and gate/up are plan-packed): one copy
+        const uint32_t bytes = nr * (uint32_t)op_in_dim(p.g, op) * (uint32_t)p.g.wbytes * (uint32_t)op_mats(op);
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(dst, gemv_src(op, layer, r0), bytes, bar, pol_weights);
+        ++j;
+    }
+
+    // K and V of positions [p0, p1) (all < P) of kv head `h`, layer `layer`.
+    __device__ void kv_chunk(int layer, int h, int p0, int p1) {
+        if (!owns(j)) {
+            ++j;
+            return;
+        }
+        uint64_t *bar;
+        uint8_t *dst = acquire(&bar);
+        if (!dst) return;
+        const Geom &g = p.g;
+        const int n = p1 > p0 ? p1 - p0 : 0;
+        const uint32_t bytes = (uint32_t)n * g.d * 2u;
+        mbar_expect_tx(bar, 2u * bytes);
+        if (n > 0) {
+            size_t off = ((size_t)(layer * g.nkv + h) * g.max_pos + p0) * g.d;
+            bulk_g2s_nohint(dst, p.k_cache + off, bytes, bar);
+            bulk_g2s_nohint(dst + (size_t)g.kv_block * g.d * 2, p.v_cache + off, bytes, bar);
+        }
+        ++j;
+    }
+
+    // K/V of positions written by step st-1 may be read only after this CTA's
+    // consumers acquired the end of step st-1 (they publish that in step_ready).
+    int ready = 0;
+    __device__ bool kv_ready(int st) {
+        if (ready >= st) return true;
+        unsigned long long t0 = global_timer();
+        for (uint32_t spin = 0;; ++spin) {
+            ready = ld_acquire_cta(&s.ctl->step_ready);
+            if (ready >= st) break;
+            if ((spin & 15u) == 15u) {
+                if (failed(p)) return false;
+                if (global_timer() - t0 > p.timeout_ns) {
+                    atomicOr(p.status, kDevTimeout);
+                    return false;
+                }
+            }
+        }
+        // generic-proxy K/V writes of earlier steps, then async-proxy reads
+        fence_proxy_async_global();
+        return true;
+    }
+
+    __device__ __forceinline__ void run(int cta) {
+        const Geom &g = p.g;
+        const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
+        fence_proxy_async_global();
+        for (int st = 0; st < p.n_steps && ok; ++st) {
+            const int P = p.pos0 + st;
+            for (int ti = t0; ti < t1 && ok; ++ti) {
+                const tiles_task t = p.tasks[ti];
+                unsigned long long *tr = pid == 0 ? trace_rec(p, cta, st, ti - t0) : nullptr;
+                tracing = tr != nullptr;
+                stall = 0;
+                if (tr) tr[kTrProdFirst] = global_timer();
+                if (op_is_gemv(t.op)) {
+                    const uint32_t rpc = (uint32_t)op_rows_per_chunk(g, t.op);
+                    for (uint32_t r = t.begin; r < t.end && ok; r += rpc) {
+                        uint32_t nr = t.end - r < rpc ? t.end - r : rpc;
+                        gemv_chunk(t.op, t.layer, r, nr);
+                    }
+                } else if (t.op == TILES_OP_ATTN) {
+                    if (!kv_ready(st)) { ok = false; break; }
+                    for (uint32_t it = t.begin; it < t.end && ok; ++it) {
+                        const int h = (int)(it / (uint32_t)g.kv_splits);
+                        const int c = (int)(it % (uint32_t)g.kv_splits);
+                        int b0, b1;
+                        attn_split_blocks(g, P + 1, c, &b0, &b1);
+                        for (int b = b0; b < b1 && ok; ++b) {
+                            int q0 = b * g.kv_block, q1 = q0 + g.kv_block;
+                            if (q1 > P) q1 = P;  // position P itself is computed in this step
+                            kv_chunk(t.layer, h, q0, q1);
+                        }
+                    }
+                }
+                if (tr) {
+                    tr[kTrProdLast] = global_timer();
+                    tr[kTrProdStall] = stall;
+                    tr[kTrOpInfo] = (unsigned long long)t.op | ((unsigned long long)t.layer << 8) |
+                                    ((unsigned long long)task_chunks(g, t, P) << 32);
+                }
+            }
+        }
+        if (pid == 0) st_volatile_u64(&s.ctl->stream_pos, ~0ull);  // releases the prefetch warp
+        // drain: wait for every copy still in flight so no bulk copy outlives the CTA
+        const uint32_t ns = (uint32_t)g.ring_slots;
+        uint32_t first = j > ns ? j - ns : 0;
+        for (uint32_t k = first; k < j; ++k) {
+            if (!owns(k)) continue;
+            unsigned long long t0n = global_timer();
+            while (!mbar_try_wait(&s.full[k % ns], (k / ns) & 1u)) {
+                if (global_timer() - t0n > p.timeout_ns) break;
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------ L2 prefetch warp
+// Warms L2 with the loads of the dependency chain. While the weight stream
+// saturates HBM, a copy the ring issues waits behind every copy in flight on
+// the GPU (the rings alone hold about 3 us of HBM traffic), and on the chain
+// Q/K/V -> attention -> O-projection that wait is pure latency. So the warp
+// walks this CTA's tasks in the producers' order and prefetches into L2, one
+// 128-byte line per lane, only the weight rows of the Q/K/V and O-projection
+// tiles and the cached K/V of the attention tiles, once the producers are
+// within l2_prefetch_bytes of weights of them: about one FFN phase ahead, so
+// they are in L2 when the ring asks. Gate/up, down and LM-head rows are left
+// to the ring (prefetching them too only adds DRAM traffic and congestion).
+// Issue may be paced (a token bucket in global-timer nanoseconds). The warp
+// never makes the kernel wait: when the producers finish or anything fails,
+// it stops.
+struct Prefetcher {
+    const KernelParams &p;
+    Smem &s;
+    const int lane;
+    unsigned long long next_ns = 0;
+
+    __device__ Prefetcher(const KernelParams &p_, Smem &s_) : p(p_), s(s_), lane(threadIdx.x & 31) {}
+
+    // false: stop prefetching (failure, or the producers stopped moving)
+    __device__ bool wait_window(unsigned long long pos) {
+        if (pos < ld_volatile_u64(&s.ctl->stream_pos) + p.l2_prefetch_bytes) return true;
+        const unsigned long long t0 = global_timer();
+        for (uint32_t spin = 1;; ++spin) {
+            __nanosleep(64);
+            const unsigned long long sp = ld_volatile_u64(&s.ctl->stream_pos);
+            if (sp == ~0ull) return false;
+            if (pos < sp + p.l2_prefetch_bytes) return true;
+            if ((spin & 63u) == 0 && (failed(p) || global_timer() - t0 > p.timeout_ns)) return false;
+        }
+    }
+
+    // lines [a, a + bytes) of one range, 4 KB per warp instruction
+    __device__ bool range(const uint8_t *a, unsigned long long bytes, unsigned long long pos) {
+        for (unsigned long long off = 0; off < bytes; off += 4096) {
+            if (!wait_window(pos + off)) return false;
+            if (p.l2_prefetch_ns_per_4k) {
+                unsigned long long now = global_timer();
+                const unsigned long long floor = now > 8ull * p.l2_prefetch_ns_per_4k ? now - 8ull * p.l2_prefetch_ns_per_4k : 0ull;
+                if (next_ns < floor) next_ns = floor;  // at most 32 KB of burst credit
+                while (now < next_ns) now = global_timer();
+                next_ns += p.l2_prefetch_ns_per_4k;
+            }
+            const unsigned long long o = off + (unsigned long long)lane * 128u;
+            if (o < bytes) prefetch_l2(a + o);
+        }
+        return true;
+    }
+
+    __device__ void run(int cta) {
+        const Geom &g = p.g;
+        const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
+        unsigned long long pos = 0;  // weight bytes of the tasks walked so far
+        for (int st = 0; st < p.n_steps; ++st) {
+            const int P = p.pos0 + st;
+            for (int ti = t0; ti < t1; ++ti) {
+                const tiles_task t = p.tasks[ti];
+                if (failed(p)) return;
+                if (op_is_gemv(t.op)) {
+                    const unsigned long long rb = (unsigned long long)op_in_dim(g, t.op) * g.wbytes * op_mats(t.op);
+                    const unsigned long long bytes = (unsigned long long)(t.end - t.begin) * rb;
+                    if (t.op != TILES_OP_QKV && t.op != TILES_OP_OPROJ) {
+                        pos += bytes;  // streaming tiles: left to the ring
+                        continue;
+                    }
+                    const unsigned long long sp = ld_volatile_u64(&s.ctl->stream_pos);
+                    if (sp == ~0ull) return;
+                    // skip what the producers already handed to the ring
+                    unsigned long long skip = sp > pos ? (sp - pos) & ~4095ull : 0ull;
+                    if (skip < bytes) {
+                        const LayerPtrs &lw = p.layers[t.layer];
+                        const uint8_t *a = (t.op == TILES_OP_QKV ? lw.qkv : lw.o) + (size_t)t.begin * rb;
+                        if (!range(a + skip, bytes - skip, pos + skip)) return;
+                    }
+                    pos += bytes;
+                } else if (t.op == TILES_OP_ATTN) {
+                    // cached positions only: position P is written in this step
+                    for (uint32_t it = t.begin; it < t.end; ++it) {
+                        const int h = (int)(it / (uint32_t)g.kv_splits);
+                        int b0, b1;
+                        attn_split_blocks(g, P + 1, (int)(it % (uint32_t)g.kv_splits), &b0, &b1);
+                        int q0 = b0 * g.kv_block, q1 = b1 * g.kv_block;
+                        if (q1 > P) q1 = P;
+                        if (q1 <= q0) continue;
+                        const size_t off = ((size_t)(t.layer * g.nkv + h) * g.max_pos + q0) * g.d;
+                        const unsigned long long n = (unsigned long long)(q1 - q0) * g.d * 2u;
+                        if (!range(reinterpret_cast<const uint8_t *>(p.k_cache + off), n, pos)) return;
+                        if (!range(reinterpret_cast<const uint8_t *>(p.v_cache + off), n, pos)) return;
+                    }
+                }
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------ GEMV rows
+// NR rows (x MATS matrices) of one chunk against the input vector in shared
+// memory: lane c reads 16-byte columns c, c+32, ... of every row, FP32 FMA,
+// then an xor-shuffle reduction; lane r returns row r's sums. The row count is
+// a compile-time constant so no predicated-off rows are issued.
+template <int MATS, int NR>
+__device__ __forceinline__ void gemv_rows(const uint8_t *slot, const uint4 *vec, int nu4,
+                                          size_t row_bytes, int rpc, float (&res)[MATS]) {
+    const int lane = threadIdx.x & 31;
+    float acc[NR][MATS];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int m = 0; m < MATS; ++m) acc[r][m] = 0.f;
+    for (int c = lane; c < nu4; c += 32) {
+        float xf[8];
+        unpack8(vec[c], xf);
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int m = 0; m < MATS; ++m) {
+                // MATS == 2: gate row r at 2r, up row r at 2r + 1 (packed layout)
+                const uint4 w = reinterpret_cast<const uint4 *>(slot + ((size_t)r * MATS + m) * row_bytes)[c];
+                acc[r][m] = dot8(w, xf, acc[r][m]);
+            }
+    }
+#pragma unroll
+    for (int m = 0; m < MATS; ++m) res[m] = 0.f;
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int m = 0; m < MATS; ++m) {
+            const float v = warp_sum(acc[r][m]);
+            if (lane == r) res[m] = v;
+        }
+}
+
+template <int MATS>
+__device__ __forceinline__ void gemv_rows_n(uint32_t nr, const uint8_t *slot, const uint4 *vec, int nu4,
+                                            size_t row_bytes, int rpc, float (&res)[MATS]) {
+    switch (nr) {
+        case 1: gemv_rows<MATS, 1>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 2: gemv_rows<MATS, 2>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 3: gemv_rows<MATS, 3>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 4: gemv_rows<MATS, 4>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 5: gemv_rows<MATS, 5>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 6: gemv_rows<MATS, 6>(slot, vec, nu4, row_bytes, rpc, res); break;
+        case 7: gemv_rows<MATS, 7>(slot, vec, nu4, row_bytes, rpc, res); break;
+        default: gemv_rows<MATS, 8>(slot, vec, nu4, row_bytes, rpc, res); break;
+    }
+}
+
+// ------------------------------------------------------------------ INT8 GEMV rows
+// Four INT8 codes of a word to exact floats: with the sign bit of each byte
+// flipped (u = q + 128), the byte placed under the exponent of 2^23 is the
+// float 2^23 + u, and subtracting 2^23 + 128 leaves q (both steps exact).
+__device__ __forceinline__ void q8_word(uint32_t w, float (&f)[4]) {
+    const uint32_t u = w ^ 0x80808080u;
+    f[0] = __fsub_rn(__int_as_float(__byte_perm(u, 0x4B000000u, 0x7540)), 8388736.0f);
+    f[1] = __fsub_rn(__int_as_float(__byte_perm(u, 0x4B000000u, 0x7541)), 8388736.0f);
+    f[2] = __fsub_rn(__int_as_float(__byte_perm(u, 0x4B000000u, 0x7542)), 8388736.0f);
+    f[3] = __fsub_rn(__int_as_float(__byte_perm(u, 0x4B000000u, 0x7543)), 8388736.0f);
+}
+
+// 16 codes times 16 inputs, accumulated in FP32 (each product is exact)
+__device__ __forceinline__ float dot16_q8(const uint4 &w, const float (&x)[16], float acc) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float f[4];
+        q8_word(ws[k], f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc = fmaf(f[i], x[4 * k + i], acc);
+    }
+    return acc;
+}
+
+// The INT8 form of gemv_rows: lane c reads the 16-code pieces c, c+32, ... of
+// every row (16 bytes each) and the 16 matching BF16 inputs; lane r returns
+// row r's unscaled sums (the epilogue applies the row scale).
+template <int MATS, int NR>
+__device__ __forceinline__ void gemv_rows_q8(const uint8_t *slot, const uint4 *vec, int n16,
+                                             size_t row_bytes, float (&res)[MATS]) {
+    const int lane = threadIdx.x & 31;
+    float acc[NR][MATS];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int m = 0; m < MATS; ++m) acc[r][m] = 0.f;
+    for (int c = lane; c < n16; c += 32) {
+        float xf[16];
+        {
+            float a[8], b[8];
+            unpack8(vec[2 * c], a);
+            unpack8(vec[2 * c + 1], b);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                xf[e] = a[e];
+                xf[8 + e] = b[e];
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int m = 0; m < MATS; ++m) {
+                const uint4 w = reinterpret_cast<const uint4 *>(slot + ((size_t)r * MATS + m) * row_bytes)[c];
+                acc[r][m] = dot16_q8(w, xf, acc[r][m]);
+            }
+    }
+#pragma unroll
+    for (int m = 0; m < MATS; ++m) res[m] = 0.f;
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int m = 0; m < MATS; ++m) {
+            const float v = warp_sum(acc[r][m]);
+            if (lane == r) res[m] = v;
+        }
+}
+
+template <int MATS>
+__device__ __forceinline__ void gemv_rows_q8_n(uint32_t nr, const uint8_t *slot, const uint4 *vec, int n16,
+                                               size_t row_bytes, float (&res)[MATS]) {
+    switch (nr) {
+        case 1: gemv_rows_q8<MATS, 1>(slot, vec, n16, row_bytes, res); break;
+        case 2: gemv_rows_q8<MATS, 2>(slot, vec, n16, row_bytes, res); break;
+        case 3: gemv_rows_q8<MATS, 3>(slot, vec, n16, row_bytes, res); break;
+        case 4: gemv_rows_q8<MATS, 4>(slot, vec, n16, row_bytes, res); break;
+        case 5: gemv_rows_q8<MATS, 5>(slot, vec, n16, row_bytes, res); break;
+        case 6: gemv_rows_q8<MATS, 6>(slot, vec, n16, row_bytes, res); break;
+        case 7: gemv_rows_q8<MATS, 7>(slot, vec, n16, row_bytes, res); break;
+        default: gemv_rows_q8<MATS, 8>(slot, vec, n16, row_bytes, res); break;
+    }
+}
+
+// this lane's DPL elements (2 or 4 consecutive dims) of one bf16 V row
+template <int DPL>
+__device__ __forceinline__ void v_piece(const uint8_t *vrow, float (&vf)[DPL]) {
+    const int lane = threadIdx.x & 31;
+    if constexpr (DPL == 2) {
+        const uint32_t w = reinterpret_cast<const uint32_t *>(vrow)[lane];
+        vf[0] = bf_lo(w);
+        vf[1] = bf_hi(w);
+    } else {
+        const uint2 w = reinterpret_cast<const uint2 *>(vrow)[lane];
+        vf[0] = bf_lo(w.x);
+        vf[1] = bf_hi(w.x);
+        vf[2] = bf_lo(w.y);
+        vf[3] = bf_hi(w.y);
+    }
+}
+
+// ------------------------------------------------------------------ consumers
+struct Consumer {
+    const KernelParams &p;
+    Smem &s;
+    const int tid, warp, lane;
+    uint32_t j = 0;  // chunks consumed by the CTA (all warps keep the same count)
+    int step = 0, P = 0;
+    bool bad = false;  // this thread saw a timeout, an abort or a bad index
+
+    __device__ Consumer(const KernelParams &p_, Smem &s_, int tid_)
+        : p(p_), s(s_), tid(tid_), warp(tid_ >> 5), lane(tid_ & 31) {}
+
+    // Chunk k lives in ring slot k % slots and is consumed by the warp that owns
+    // that slot, (k % slots) % 8. One owner per slot means a warp only waits on
+    // a slot after it released the slot's previous chunk itself, so the
+    // mbarrier parity can never alias a chunk two ring laps ahead.
+    __device__ bool mine(uint32_t k) const {
+        return (int)((k % (uint32_t)p.g.ring_slots) % kConsumerWarps) == warp;
+    }
+
+    // slot of CTA chunk k, after its data landed; nullptr when aborting
+    __device__ uint8_t *wait_chunk(uint32_t k) {
+        const uint32_t ns = (uint32_t)p.g.ring_slots;
+        uint32_t slot = k % ns;
+        const bool ok = wait_mbar(p, &s.full[slot], (k / ns) & 1u);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {  // warp-uniform decision
+            bad = true;
+            return nullptr;
+        }
+        return s.ring + (size_t)slot * p.g.slot_bytes;
+    }
+    __device__ void release_chunk(uint32_t k) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.empty[k % (uint32_t)p.g.ring_slots]);
+    }
+
+    __device__ int token_of_step(int st) {
+        const int sg = p.step0 + st;
+        int tok;
+        if (sg < p.n_prompt) tok = p.prompt[sg];
+        else if (st > 0) tok = key_row(__ldcg(&p.keys[st - 1]));
+        else tok = __ldcg(&p.out_tokens[sg - p.n_prompt]);
+        return tok;
+    }
+
+    // ---------------------------------------------------------- prologues
+    // vec <- bf16(rmsnorm(src) * gain), src bf16 [n <= 8192] in global memory,
+    // or (src null) already in vec; sum of squares in a fixed order, so every
+    // CTA computes the same scale. One pass over src: each thread keeps its (at
+    // most four) 16-byte pieces in registers.
+    __device__ void rmsnorm_to_vec(const uint16_t *src, const uint16_t *gain, int n) {
+        constexpr int kMaxU = 4;
+        const int nu4 = n >> 3;
+        uint4 v[kMaxU];
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxU; ++k) {
+            const int c = tid + k * kConsumerWarps * 32;
+            if (c < nu4) {
+                v[k] = src ? __ldcg(reinterpret_cast<const uint4 *>(src) + c) : reinterpret_cast<const uint4 *>(s.vec)[c];
+                float f[8];
+                unpack8(v[k], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+            }
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) s.ctl->red[warp] = ss;
+        consumer_sync();
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) tot += s.ctl->red[w];
+        const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)n), p.eps)));
+        uint4 *dst = reinterpret_cast<uint4 *>(s.vec);
+#pragma unroll
+        for (int k = 0; k < kMaxU; ++k) {
+            const int c = tid + k * kConsumerWarps * 32;
+            if (c < nu4) {
+                const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gain) + c);
+                float f[8], gf[8];
+                unpack8(v[k], f);
+                unpack8(gv, gf);
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint16_t lo = f2bf(__fmul_rn(__fmul_rn(f[2 * e], r), gf[2 * e]));
+                    const uint16_t hi = f2bf(__fmul_rn(__fmul_rn(f[2 * e + 1], r), gf[2 * e + 1]));
+                    o[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                }
+                dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+
+    // residual rows [begin, end) into shared memory, for the epilogue: of the
+    // embedding row (first layer), else of the tagged x words carrying `tag`
+    __device__ void load_residual(const uint16_t *embed_row, uint32_t tag, uint32_t begin, uint32_t end) {
+        uint16_t *res = reinterpret_cast<uint16_t *>(s.vec + p.res_off);
+        for (uint32_t r = begin + tid; r < end; r += kConsumerWarps * 32) {
+            if (embed_row) {
+                res[r - begin] = __ldcg(&embed_row[r]);
+                continue;
+            }
+            uint32_t w = ld_relaxed_u32(p.xw + r);
+            Poll pl;
+            while ((w >> 16) != tag) {
+                if (bad || !pl.again(p)) {
+                    bad = true;
+                    break;
+                }
+                w = ld_relaxed_u32(p.xw + r);
+            }
+            res[r - begin] = (uint16_t)(w & 0xFFFFu);
+        }
+    }
+
+    __device__ uint32_t tag(int layer, int kind) const { return act_tag(p, step, layer, kind); }
+
+    // vec[0, n) (bf16) <- the tagged words src[0, n), n a multiple of 8, each
+    // polled until it carries `tg`. First pass: four 8-word pieces per thread
+    // in flight, the ready ones stored; then the stale ones are polled.
+    __device__ void gather_tagged(const uint32_t *src, int n, uint32_t tg) {
+        constexpr int B = 4;
+        const int n8 = n >> 3;
+        uint4 *dst = reinterpret_cast<uint4 *>(s.vec);
+        for (int c0 = tid; c0 < n8; c0 += B * kConsumerWarps * 32) {
+            uint32_t stale = 0;
+#pragma unroll
+            for (int k = 0; k < B; ++k) {
+                const int c = c0 + k * kConsumerWarps * 32;
+                if (c < n8) {
+                    const uint4 lo = ld_relaxed_v4(src + 8 * c), hi = ld_relaxed_v4(src + 8 * c + 4);
+                    if (tags_ok4(lo, tg) && tags_ok4(hi, tg)) dst[c] = untag8(lo, hi);
+                    else stale |= 1u << k;
+                }
+            }
+            for (int k = 0; stale != 0; ++k, stale >>= 1) {
+                if (!(stale & 1u)) continue;
+                const int c = c0 + k * kConsumerWarps * 32;
+                Poll pl;
+                uint4 lo, hi;
+                do {
+                    if (bad || !pl.again(p)) {
+                        bad = true;
+                        break;
+                    }
+                    lo = ld_relaxed_v4(src + 8 * c);
+                    hi = ld_relaxed_v4(src + 8 * c + 4);
+                } while (!(tags_ok4(lo, tg) && tags_ok4(hi, tg)));
+                if (!bad) dst[c] = untag8(lo, hi);
+            }
+        }
+    }
+
+    // One output row of a GEMV task, from its MATS dot products: the fused
+    // epilogue of the op (residual add, SwiGLU, logits store).
+    template <int MATS>
+    __device__ void emit_row(int op, const tiles_task &t, uint32_t row, const float (&v)[MATS]) {
+        switch (op) {
+            case TILES_OP_QKV:
+                st_relaxed_u64(p.qkvw + row, ((unsigned long long)tag(t.layer, kTagQKV) << 32) | __float_as_uint(v[0]));
+                break;
+            case TILES_OP_OPROJ:
+            case TILES_OP_DOWN: {  // residual rows were loaded in the prologue
+                const uint16_t xb = reinterpret_cast<const uint16_t *>(s.vec + p.res_off)[row - t.begin];
+                const uint32_t tg = tag(t.layer, op == TILES_OP_OPROJ ? kTagXAttn : kTagXFfn);
+                st_relaxed_u32(p.xw + row, (tg << 16) | f2bf(__fadd_rn(bf2f(xb), v[0])));
+                break;
+            }
+            case TILES_OP_GATEUP: {
+                const float gt = v[0];
+                const float silu = __fdiv_rn(gt, __fadd_rn(1.0f, expf(-gt)));
+                st_relaxed_u32(p.aw + row, (tag(t.layer, kTagA) << 16) | f2bf(__fmul_rn(silu, v[MATS - 1])));
+                break;
+            }
+            case TILES_OP_LMHEAD:
+                if (p.out_logits) __stcg(&p.out_logits[(size_t)(p.step0 + step) * p.g.V + row], v[0]);
+                break;
+        }
+    }
+
+    // Chunk k goes to the warp that owns its slot, which reduces it alone; the
+    // warps work on different chunks at once.
+    template <int MATS, bool Q8>
+    __device__ void gemv_task(const tiles_task &t) {
+        const Geom &g = p.g;
+        const int op = t.op;
+        const int in = op_in_dim(g, op);
+        const int nu4 = in >> 3;
+        const float *scale = nullptr;  // INT8: one FP32 scale per streamed row
+        if constexpr (Q8) {
+            const LayerPtrs &lw = p.layers[t.layer];
+            scale = op == TILES_OP_QKV ? lw.s_qkv : op == TILES_OP_OPROJ ? lw.s_o
+                  : op == TILES_OP_GATEUP ? lw.s_gu : op == TILES_OP_DOWN ? lw.s_down : p.lm_s;
+        }
+        const uint32_t rpc = (uint32_t)op_rows_per_chunk(g, op);
+        const uint32_t nchunks = (t.end - t.begin + rpc - 1) / rpc;
+        const uint4 *vec = reinterpret_cast<const uint4 *>(s.vec);
+        unsigned long long best = 0;
+        for (uint32_t k = 0; k < nchunks; ++k) {
+            const uint32_t jj = j + k;
+            if (!mine(jj)) continue;
+            const uint32_t r0 = t.begin + k * rpc;
+            const uint32_t nr = t.end - r0 < rpc ? t.end - r0 : rpc;
+            const uint8_t *slot = wait_chunk(jj);
+            if (!slot) break;
+            float mine[MATS];
+            if constexpr (Q8) {
+                gemv_rows_q8_n<MATS>(nr, slot, vec, in >> 4, (size_t)in, mine);
+            } else {
+                gemv_rows_n<MATS>(nr, slot, vec, nu4, (size_t)in * 2, (int)rpc, mine);
+            }
+            release_chunk(jj);
+            if constexpr (Q8) {
+                if ((uint32_t)lane < nr) {
+                    const uint32_t row = r0 + lane;
+#pragma unroll
+                    for (int m = 0; m < MATS; ++m)  // gate/up: packed rows 2 row, 2 row + 1
+                        mine[m] = __fmul_rn(mine[m], __ldg(scale + (MATS == 2 ? 2 * row + m : row)));
+                }
+            }
+            if ((uint32_t)lane < nr) emit_row<MATS>(op, t, r0 + lane, mine);
+            if (op == TILES_OP_LMHEAD) {
+                unsigned long long key = (uint32_t)lane < nr ? argmax_key(mine[0], r0 + lane) : 0ull;
+                key = warp_max_u64(key);
+                best = key > best ? key : best;
+            }
+        }
+        j += nchunks;
+        if (op == TILES_OP_LMHEAD) {
+            if (lane == 0) s.ctl->warp_key[warp] = best;
+            consumer_sync();
+            if (tid == 0) {
+                unsigned long long b = 0;
+                for (int w = 0; w < kConsumerWarps; ++w) b = s.ctl->warp_key[w] > b ? s.ctl->warp_key[w] : b;
+                atomicMax(&p.keys[step], b);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------- attention
+    // Layout of the vec region during attention tasks.
+    struct AttnSmem {
+        float *q;          // [G][d] f32 (bf16-valued)
+        uint16_t *knew;    // [d]
+        uint16_t *vnew;    // [d]
+        float *prob;       // [warps][32][G]
+        float *wstate;     // [warps][G][4 + d]
+    };
+    __device__ AttnSmem attn_smem() const {
+        const Geom &g = p.g;
+        AttnSmem a;
+        uint8_t *b = s.vec;
+        a.q = reinterpret_cast<float *>(b);
+        b += (size_t)g.G * g.d * 4;
+        a.knew = reinterpret_cast<uint16_t *>(b);
+        b += (size_t)g.d * 2;
+        a.vnew = reinterpret_cast<uint16_t *>(b);
+        b += (size_t)g.d * 2;
+        a.prob = reinterpret_cast<float *>(b);
+        b += (size_t)kConsumerWarps * 32 * g.G * 4;
+        a.wstate = reinterpret_cast<float *>(b);
+        return a;
+    }
+
+    // q heads of kv head h (and k, v of head h): optional RMSNorm over the head,
+    // RoPE at position P, rounding to bf16. One warp per head.
+    template <int D>
+    __device__ void prep_qkv(int h, const AttnSmem &a) {
+        const Geom &g = p.g;
+        const LayerPtrs &lw = p.layers[cur_layer];
+        const float *cs = p.rope_cos + (size_t)P * (D / 2);
+        const float *sn = p.rope_sin + (size_t)P * (D / 2);
+        constexpr int E = D / 32;  // elements per lane: lane, lane+32, ...
+        for (int hh = warp; hh < g.G + 2; hh += kConsumerWarps) {
+            const bool is_q = hh < g.G, is_k = hh == g.G;
+            const int row0 = is_q ? (h * g.G + hh) * D
+                                  : (is_k ? g.qd + h * D : g.qd + g.kvd + h * D);
+            float v[E];
+            {
+                const uint32_t tg = tag(cur_layer, kTagQKV);
+                unsigned long long w[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) w[e] = ld_relaxed_u64(p.qkvw + row0 + lane + 32 * e);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    Poll pl;
+                    while ((uint32_t)(w[e] >> 32) != tg) {
+                        if (bad || !pl.again(p)) {
+                            bad = true;
+                            break;
+                        }
+                        w[e] = ld_relaxed_u64(p.qkvw + row0 + lane + 32 * e);
+                    }
+                    v[e] = __uint_as_float((uint32_t)w[e]);
+                }
+            }
+            if (!is_q && !is_k) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) a.vnew[lane + 32 * e] = f2bf(v[e]);
+                continue;
+            }
+            if (p.qk_norm) {
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
+                ss = warp_sum(ss);
+                const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)D), p.eps)));
+                const uint16_t *gn = is_q ? lw.q_norm : lw.k_norm;
+#pragma unroll
+                for (int e = 0; e < E; ++e) v[e] = __fmul_rn(__fmul_rn(v[e], r), bf2f(gn[lane + 32 * e]));
+            }
+            // rotate-half: element j pairs with j + D/2 (both held by this lane)
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) {
+                const int jx = lane + 32 * e;
+                const float c = cs[jx], sv = sn[jx];
+                const float x0 = v[e], x1 = v[e + E / 2];
+                v[e] = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sv));
+                v[e + E / 2] = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, sv));
+            }
+            if (is_q) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) a.q[hh * D + lane + 32 * e] = round_bf(v[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) a.knew[lane + 32 * e] = f2bf(v[e]);
+            }
+        }
+    }
+
+    int cur_layer = 0;
+
+    // one chunk of positions [q0, q0 + npos) for the G q heads of one kv head
+    template <int D, int G>
+    __device__ void attn_chunk(const uint8_t *slot, int npos, const AttnSmem &a, float (&m)[G],
+                               float (&l)[G], float (&o)[G][D / 32]) {
+        constexpr int NC = D / 8;   // 16-byte columns per row
+        constexpr int DPL = D / 32; // dims per lane in the PV product
+        const Geom &g = p.g;
+        const uint8_t *Kb = slot;
+        const uint8_t *Vb = slot + (size_t)g.kv_block * D * 2;
+        float *prob = a.prob + (size_t)warp * 32 * G;
+        for (int t0 = 0; t0 < npos; t0 += 32) {
+            const int t = t0 + lane;
+            const bool valid = t < npos;
+            float sc[G];
+#pragma unroll
+            for (int i = 0; i < G; ++i) sc[i] = 0.f;
+            if (valid) {
+                const uint4 *krow = reinterpret_cast<const uint4 *>(Kb + (size_t)t * D * 2);
+#pragma unroll
+                for (int jj = 0; jj < NC; ++jj) {
+                    const int col = (jj + lane) & (NC - 1);  // rotated: no bank conflicts
+                    float kf[8];
+                    unpack8(krow[col], kf);
+#pragma unroll
+                    for (int i = 0; i < G; ++i) {
+                        const float4 qa = reinterpret_cast<const float4 *>(a.q + i * D + col * 8)[0];
+                        const float4 qb = reinterpret_cast<const float4 *>(a.q + i * D + col * 8)[1];
+                        float acc = sc[i];
+                        acc = fmaf(kf[0], qa.x, acc); acc = fmaf(kf[1], qa.y, acc);
+                        acc = fmaf(kf[2], qa.z, acc); acc = fmaf(kf[3], qa.w, acc);
+                        acc = fmaf(kf[4], qb.x, acc); acc = fmaf(kf[5], qb.y, acc);
+                        acc = fmaf(kf[6], qb.z, acc); acc = fmaf(kf[7], qb.w, acc);
+                        sc[i] = acc;
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+                const float si = valid ? sc[i] * p.attn_scale : -INFINITY;
+                const float bm = warp_max(si);
+                const float mn = fmaxf(m[i], bm);
+                const float corr = expf(m[i] - mn);
+                const float pi = valid ? expf(si - mn) : 0.f;
+                const float ps = warp_sum(pi);
+                l[i] = fmaf(l[i], corr, ps);
+                m[i] = mn;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o[i][e] *= corr;
+                prob[lane * G + i] = pi;
+            }
+            __syncwarp();
+            const int nv = npos - t0 < 32 ? npos - t0 : 32;
+            for (int tt = 0; tt < nv; ++tt) {
+                float pv[G];
+#pragma unroll
+                for (int i = 0; i < G; ++i) pv[i] = prob[tt * G + i];
+                const uint8_t *vrow = Vb + (size_t)(t0 + tt) * D * 2;
+                float vf[DPL];
+                if (DPL == 2) {
+                    const uint32_t w = reinterpret_cast<const uint32_t *>(vrow)[lane];
+                    vf[0] = bf_lo(w);
+                    vf[1] = bf_hi(w);
+                } else {
+                    const uint2 w = reinterpret_cast<const uint2 *>(vrow)[lane];
+                    vf[0] = bf_lo(w.x);
+                    vf[1] = bf_hi(w.x);
+                    vf[DPL > 2 ? 2 : 0] = bf_lo(w.y);
+                    vf[DPL > 3 ? 3 : 1] = bf_hi(w.y);
+                }
+#pragma unroll
+                for (int i = 0; i < G; ++i)
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) o[i][e] = fmaf(pv[i], vf[e], o[i][e]);
+            }
+            __syncwarp();
+        }
+    }
+
+    // Cooperative form: this warp handles one q head (hi) and the T-position
+    // blocks blk_first, blk_first + blk_step, ... of a chunk all warps share,
+    // T = 32 / LP. Each position's q . k is split over LP consecutive lanes (an
+    // LP-th of the 16-byte columns each, rotated so a quarter warp touches 8
+    // distinct bank groups) and summed by shuffles; LP > 1 keeps every warp
+    // busy when a head's warps would otherwise get fewer than 32 positions each
+    // (head_dim 128 chunks hold 32 positions).
+    template <int D, int LP>
+    __device__ void attn_chunk_one(const uint8_t *slot, int npos, const AttnSmem &a, int hi,
+                                   int blk_first, int blk_step, float &m, float &l,
+                                   float (&o)[D / 32]) {
+        constexpr int NC = D / 8;
+        constexpr int DPL = D / 32;
+        constexpr int T = 32 / LP;
+        constexpr int CPL = NC / LP;  // 16-byte columns per lane
+        constexpr int ROT = (D == 128 && LP == 2) ? 4 : (D == 128 && LP == 4) ? 1 : 0;
+        static_assert(CPL >= 1, "more lanes per position than columns");
+        const Geom &g = p.g;
+        const uint8_t *Kb = slot;
+        const uint8_t *Vb = slot + (size_t)g.kv_block * D * 2;
+        const float *q = a.q + hi * D;
+        float *prob = a.prob + (size_t)warp * 32 * g.G;
+        const int tl = lane / LP, part = lane % LP;
+        for (int t0 = blk_first * T; t0 < npos; t0 += blk_step * T) {
+            const int t = t0 + tl;
+            const bool valid = t < npos;
+            // this lane's share of q . k, over four independent partial sums
+            float sc4[4] = {0.f, 0.f, 0.f, 0.f};
+            if (valid) {
+                const uint4 *krow = reinterpret_cast<const uint4 *>(Kb + (size_t)t * D * 2);
+#pragma unroll
+                for (int jj = 0; jj < CPL; ++jj) {
+                    const int col = part * CPL + ((jj + tl + ROT * part) & (CPL - 1));
+                    float kf[8];
+                    unpack8(krow[col], kf);
+                    const float4 qa = reinterpret_cast<const float4 *>(q + col * 8)[0];
+                    const float4 qb = reinterpret_cast<const float4 *>(q + col * 8)[1];
+                    float sc = sc4[jj & 3];
+                    sc = fmaf(kf[0], qa.x, sc); sc = fmaf(kf[1], qa.y, sc);
+                    sc = fmaf(kf[2], qa.z, sc); sc = fmaf(kf[3], qa.w, sc);
+                    sc = fmaf(kf[4], qb.x, sc); sc = fmaf(kf[5], qb.y, sc);
+                    sc = fmaf(kf[6], qb.z, sc); sc = fmaf(kf[7], qb.w, sc);
+                    sc4[jj & 3] = sc;
+                }
+            }
+            float sc = __fadd_rn(__fadd_rn(sc4[0], sc4[1]), __fadd_rn(sc4[2], sc4[3]));
+#pragma unroll
+            for (int off = LP / 2; off > 0; off >>= 1) sc += __shfl_xor_sync(0xFFFFFFFFu, sc, off);
+            const float si = valid ? sc * p.attn_scale : -INFINITY;
+            const float bm = warp_max(si);
+            const float mn = fmaxf(m, bm);
+            const float corr = expf(m - mn);
+            const float pi = valid ? expf(si - mn) : 0.f;
+            const float ps = warp_sum(part == 0 ? pi : 0.f);
+            l = fmaf(l, corr, ps);
+            m = mn;
+            if (part == 0) prob[tl] = pi;
+            __syncwarp();
+            // p . V over the block's positions, four positions in flight
+            const int nv = npos - t0 < T ? npos - t0 : T;
+            float acc[4][DPL];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[u][e] = 0.f;
+            int tt = 0;
+            for (; tt + 4 <= nv; tt += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float vf[DPL];
+                    v_piece<DPL>(Vb + (size_t)(t0 + tt + u) * D * 2, vf);
+                    const float pv = prob[tt + u];
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) acc[u][e] = fmaf(pv, vf[e], acc[u][e]);
+                }
+            }
+            for (; tt < nv; ++tt) {
+                float vf[DPL];
+                v_piece<DPL>(Vb + (size_t)(t0 + tt) * D * 2, vf);
+                const float pv = prob[tt];
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[0][e] = fmaf(pv, vf[e], acc[0][e]);
+            }
+#pragma unroll
+            for (int e = 0; e < DPL; ++e)
+                o[e] = fmaf(o[e], corr, __fadd_rn(__fadd_rn(acc[0][e], acc[1][e]), __fadd_rn(acc[2][e], acc[3][e])));
+            __syncwarp();
+        }
+    }
+
+    // positions each warp of a head gets from one chunk -> lanes per position
+    __device__ int attn_lanes_per_pos(int warps_per_head) const {
+        const int ppw = (p.g.kv_block + warps_per_head - 1) / warps_per_head;
+        return ppw >= 32 ? 1 : ppw >= 16 ? 2 : ppw >= 8 ? 4 : 8;
+    }
+
+    // Put the freshly computed K/V of position P into the chunk's slot (the
+    // producer loaded only positions < P), then order these generic writes
+    // before the async-proxy copy that will later refill the slot.
+    template <int D>
+    __device__ void place_new_kv(uint8_t *slot, int q0, const AttnSmem &a) {
+        const Geom &g = p.g;
+        uint16_t *kd = reinterpret_cast<uint16_t *>(slot + (size_t)(P - q0) * D * 2);
+        uint16_t *vd = reinterpret_cast<uint16_t *>(slot + (size_t)g.kv_block * D * 2 + (size_t)(P - q0) * D * 2);
+        for (int e = lane; e < D; e += 32) {
+            kd[e] = a.knew[e];
+            vd[e] = a.vnew[e];
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+    template <int D, int G>
+    __device__ void attn_task(const tiles_task &t) {
+        const Geom &g = p.g;
+        const AttnSmem a = attn_smem();
+        constexpr int DPL = D / 32;
+        int prepared = -1;
+        for (uint32_t it = t.begin; it < t.end; ++it) {
+            const int h = (int)(it / (uint32_t)g.kv_splits);
+            const int c = (int)(it % (uint32_t)g.kv_splits);
+            if (h != prepared) {
+                consumer_sync();  // previous item finished reading q / knew / vnew
+                prep_qkv<D>(h, a);
+                consumer_sync();
+                prepared = h;
+            }
+            int b0, b1;
+            attn_split_blocks(g, P + 1, c, &b0, &b1);
+            const int pb = P / g.kv_block;
+            const bool has_new = pb >= b0 && pb < b1;
+            if (has_new && tid < D) {
+                // the one tile whose range holds position P writes the new K/V
+                const size_t off = ((size_t)(cur_layer * g.nkv + h) * g.max_pos + P) * D + tid;
+                p.k_cache[off] = a.knew[tid];
+                p.v_cache[off] = a.vnew[tid];
+                fence_proxy_async_global();
+            }
+            float m[G], l[G], o[G][DPL];
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+                m[i] = -INFINITY;
+                l[i] = 0.f;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
+            }
+            const uint32_t nch = (uint32_t)(b1 - b0);
+            if (nch < (uint32_t)kConsumerWarps) {
+                // few chunks: every warp works on every chunk (one q head, some sub-blocks)
+                const int hi = warp % G, sb0 = warp / G, sbs = kConsumerWarps / G;
+                const int lp = attn_lanes_per_pos(sbs);
+                float m1 = -INFINITY, l1 = 0.f, o1[DPL];
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o1[e] = 0.f;
+                for (uint32_t k = 0; k < nch; ++k) {
+                    const uint32_t jj = j + k;
+                    uint8_t *slot = wait_chunk(jj);
+                    const int q0 = (b0 + (int)k) * g.kv_block;
+                    int q1 = q0 + g.kv_block;
+                    if (q1 > P + 1) q1 = P + 1;
+                    if (slot && warp == 0 && q0 <= P && P < q1) place_new_kv<D>(slot, q0, a);
+                    if (consumer_sync_or(bad)) break;
+                    switch (lp) {
+                        case 1: attn_chunk_one<D, 1>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
+                        case 2: attn_chunk_one<D, 2>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
+                        case 4: attn_chunk_one<D, 4>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
+                        default: attn_chunk_one<D, (D / 8 >= 8 ? 8 : 4)>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
+                    }
+                    consumer_sync();
+                    if (tid == 0) mbar_arrive(&s.empty[jj % (uint32_t)g.ring_slots]);
+                }
+#pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    m[i] = i == hi ? m1 : -INFINITY;
+                    l[i] = i == hi ? l1 : 0.f;
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) o[i][e] = i == hi ? o1[e] : 0.f;
+                }
+            } else {
+                // many chunks: each chunk goes to its slot's owner warp, all q heads
+                for (uint32_t k = 0; k < nch; ++k) {
+                    const uint32_t jj = j + k;
+                    if (!mine(jj)) continue;
+                    uint8_t *slot = wait_chunk(jj);
+                    if (!slot) break;
+                    const int q0 = (b0 + (int)k) * g.kv_block;
+                    int q1 = q0 + g.kv_block;
+                    if (q1 > P + 1) q1 = P + 1;
+                    if (q0 <= P && P < q1) place_new_kv<D>(slot, q0, a);
+                    attn_chunk<D, G>(slot, q1 - q0, a, m, l, o);
+                    release_chunk(jj);
+                }
+            }
+            j += nch;
+            // per-warp states -> shared memory -> one partial for (q heads, split c)
+            float *ws = a.wstate + (size_t)warp * G * (kPartialPad + D);
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+                if (lane == 0) {
+                    ws[i * (kPartialPad + D) + 0] = m[i];
+                    ws[i * (kPartialPad + D) + 1] = l[i];
+                }
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) ws[i * (kPartialPad + D) + kPartialPad + lane * DPL + e] = o[i][e];
+            }
+            consumer_sync();
+            for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
+                const int i = idx / D, dd = idx % D;
+                float M = -INFINITY;
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    M = fmaxf(M, a.wstate[((size_t)w * G + i) * (kPartialPad + D)]);
+                float L = 0.f, O = 0.f;
+                if (M != -INFINITY) {
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        const float *st = a.wstate + ((size_t)w * G + i) * (kPartialPad + D);
+                        const float sc = expf(st[0] - M);
+                        L = fmaf(sc, st[1], L);
+                        O = fmaf(sc, st[kPartialPad + dd], O);
+                    }
+                }
+                unsigned long long *dst = p.partw + ((size_t)(h * G + i) * g.kv_splits + c) * (2 + D);
+                const unsigned long long tg = (unsigned long long)tag(cur_layer, kTagPart) << 32;
+                if (dd == 0) {
+                    st_relaxed_u64(&dst[0], tg | __float_as_uint(M));
+                    st_relaxed_u64(&dst[1], tg | __float_as_uint(L));
+                }
+                st_relaxed_u64(&dst[2 + dd], tg | __float_as_uint(O));
+            }
+            // wstate is reused by the next item; leave together on any failure
+            if (consumer_sync_or(bad)) return;
+        }
+        // Every partial of this task is out; now merge. (A merge polls the other
+        // splits of its head, so no merge may come before a partial of the same
+        // task: a CTA holding two splits of one head would wait on itself.)
+        for (uint32_t it = t.begin; it < t.end; ++it) {
+            merge_slice<D, G>((int)(it / (uint32_t)g.kv_splits), (int)(it % (uint32_t)g.kv_splits));
+            if (consumer_sync_or(bad)) return;
+        }
+    }
+
+    // Slice c of KV head h's merged attention output: elements [e0, e1) of its
+    // G d outputs, S-th of them per split, from the S partials in split order:
+    //   M = max_c m_c, w_c = e^(m_c - M), o = sum_c w_c o_c / sum_c w_c l_c.
+    // One thread per (element, split) pair polls that pair's tagged m, l and o
+    // into shared memory; then one thread per element merges and writes the
+    // tagged bf16 output, which the O-projection tiles gather.
+    template <int D, int G>
+    __device__ void merge_slice(int h, int c) {
+        const Geom &g = p.g;
+        const int S = g.kv_splits, n = G * D, per = (n + S - 1) / S;
+        const int e0 = c * per, e1 = e0 + per < n ? e0 + per : n;
+        if (e0 >= e1) return;
+        const int ne = e1 - e0;
+        float *st = reinterpret_cast<float *>(s.vec);  // [ne][S][3]: m, l, o
+        const uint32_t tg = tag(cur_layer, kTagPart);
+        for (int q = tid; q < ne * S; q += kConsumerWarps * 32) {
+            const int e = e0 + q / S, cc = q % S;
+            const unsigned long long *pw = p.partw + ((size_t)(h * G + e / D) * S + cc) * (2 + D);
+            unsigned long long wm = ld_relaxed_u64(pw), wl = ld_relaxed_u64(pw + 1),
+                               wo = ld_relaxed_u64(pw + 2 + e % D);
+            Poll pl;
+            while ((uint32_t)(wm >> 32) != tg || (uint32_t)(wl >> 32) != tg || (uint32_t)(wo >> 32) != tg) {
+                if (bad || !pl.again(p)) {
+                    bad = true;
+                    break;
+                }
+                wm = ld_relaxed_u64(pw);
+                wl = ld_relaxed_u64(pw + 1);
+                wo = ld_relaxed_u64(pw + 2 + e % D);
+            }
+            st[q * 3 + 0] = __uint_as_float((uint32_t)wm);
+            st[q * 3 + 1] = __uint_as_float((uint32_t)wl);
+            st[q * 3 + 2] = __uint_as_float((uint32_t)wo);
+        }
+        consumer_sync();
+        const uint32_t to = tag(cur_layer, kTagO) << 16;
+        for (int q = tid; q < ne; q += kConsumerWarps * 32) {
+            const float *sq = st + (size_t)q * S * 3;
+            float M = -INFINITY;
+            for (int cc = 0; cc < S; ++cc) M = fmaxf(M, sq[cc * 3]);
+            float L = 0.f, O = 0.f;
+            for (int cc = 0; cc < S; ++cc) {
+                const float mc = sq[cc * 3];
+                const float w = mc == -INFINITY ? 0.f : expf(mc - M);
+                L = fmaf(w, sq[cc * 3 + 1], L);
+                O = fmaf(w, sq[cc * 3 + 2], O);
+            }
+            st_relaxed_u32(p.ow + (size_t)h * n + e0 + q, to | f2bf(__fdiv_rn(O, L)));
+        }
+    }
+
+    // ---------------------------------------------------------- main loop
+    // D (head_dim), G (q heads per KV head) and the weight format (Q8: INT8
+    // codes) are compile-time: each kernel instance carries only its own code.
+    template <int D, int G, bool Q8>
+    __device__ __forceinline__ void run(int cta) {
+        const Geom &g = p.g;
+        const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
+        for (step = 0; step < p.n_steps; ++step) {
+            P = p.pos0 + step;
+            for (int ti = t0; ti < t1; ++ti) {
+                const tiles_task t = p.tasks[ti];
+                cur_layer = t.layer;
+                // ---- wait for the inputs
+                unsigned long long *tr = tid == 0 ? trace_rec(p, cta, step, ti - t0) : nullptr;
+                if (tr) tr[kTrWaitStart] = global_timer();
+                if (tid == 0) {
+                    const uint32_t target = t.wait_mul * (uint32_t)step + t.wait_add;
+                    if (t.wait_ctr != TILES_NO_COUNTER &&
+                        !wait_counter(p, p.counters + (size_t)t.wait_ctr * kCounterStride, target))
+                        bad = true;
+                    if (ti == t0 && !bad) st_release_cta(&s.ctl->step_ready, step);
+                    if (!bad && (t.op == TILES_OP_QKV || t.op == TILES_OP_OPROJ) && t.layer == 0) {
+                        int tok = token_of_step(step);
+                        if (tok < 0 || tok >= g.V) {
+                            atomicOr(p.status, kDevBounds);
+                            bad = true;
+                            tok = 0;
+                        }
+                        s.ctl->token = tok;
+                    }
+                }
+                if (consumer_sync_or(bad)) return;
+                if (tr) tr[kTrWaitEnd] = global_timer();
+                // ---- work
+                switch (t.op) {
+                    case TILES_OP_QKV:
+                        if (t.layer > 0) {
+                            gather_tagged(p.xw, g.H, tag(t.layer - 1, kTagXFfn));
+                            consumer_sync();
+                        }
+                        rmsnorm_to_vec(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : nullptr,
+                                       p.layers[t.layer].attn_norm, g.H);
+                        consumer_sync();
+                        gemv_task<1, Q8>(t);
+                        break;
+                    case TILES_OP_ATTN:
+                        attn_task<D, G>(t);
+                        break;
+                    case TILES_OP_OPROJ:
+                        gather_tagged(p.ow, g.qd, tag(t.layer, kTagO));
+                        load_residual(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : nullptr,
+                                      t.layer == 0 ? 0u : tag(t.layer - 1, kTagXFfn), t.begin, t.end);
+                        consumer_sync();
+                        gemv_task<1, Q8>(t);
+                        break;
+                    case TILES_OP_GATEUP:
+                        gather_tagged(p.xw, g.H, tag(t.layer, kTagXAttn));
+                        consumer_sync();
+                        rmsnorm_to_vec(nullptr, p.layers[t.layer].ffn_norm, g.H);
+                        consumer_sync();
+                        gemv_task<2, Q8>(t);
+                        break;
+                    case TILES_OP_DOWN:
+                        gather_tagged(p.aw, g.F, tag(t.layer, kTagA));
+                        load_residual(nullptr, tag(t.layer, kTagXAttn), t.begin, t.end);
+                        consumer_sync();
+                        gemv_task<1, Q8>(t);
+                        break;
+                    case TILES_OP_LMHEAD:
+                        gather_tagged(p.xw, g.H, tag(g.L - 1, kTagXFfn));
+                        consumer_sync();
+                        rmsnorm_to_vec(nullptr, p.final_norm, g.H);
+                        consumer_sync();
+                        gemv_task<1, Q8>(t);
+                        break;
+                    default:
+                        break;
+                }
+                // ---- publish
+                if (consumer_sync_or(bad)) return;
+                if (tr) tr[kTrTaskEnd] = global_timer();
+                if (tid == 0 && t.signal_ctr != TILES_NO_COUNTER) {
+                    red_release_add(p.counters + (size_t)t.signal_ctr * kCounterStride, 1u);
+                }
+            }
+        }
+        // the chosen tokens of this launch
+        if (cta == 0 && tid == 0) {
+            const uint32_t target = p.final_mul * (uint32_t)p.n_steps;
+            if (wait_counter(p, p.counters + (size_t)p.final_ctr * kCounterStride, target)) {
+                for (int st = 0; st < p.n_steps; ++st) {
+                    const int sg = p.step0 + st;
+                    if (sg >= p.n_prompt - 1)
+                        p.out_tokens[sg - (p.n_prompt - 1)] = key_row(__ldcg(&p.keys[st]));
+                }
+            }
+        }
+    }
+};
+
+template <int D, int G, bool Q8>
+__global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_constant__ KernelParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    Smem s = smem_layout(smem_raw, p);
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int i = 0; i < p.g.ring_slots; ++i) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], 1);
+        }
+        s.ctl->unused = 0;
+        s.ctl->token = 0;
+        s.ctl->step_ready = 0;
+        s.ctl->stream_pos = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid >= (kConsumerWarps + kProducerWarps) * 32) {
+        if (p.l2_prefetch_bytes) {
+            Prefetcher pf(p, s);
+            pf.run(blockIdx.x);
+        }
+        return;
+    }
+    if (tid >= kConsumerWarps * 32) {
+        if ((tid & 31) == 0) {
+            Producer prod(p, s, (tid >> 5) - kConsumerWarps);
+            prod.run(blockIdx.x);
+        }
+        return;
+    }
+    Consumer cons(p, s, tid);
+    cons.template run<D, G, Q8>(blockIdx.x);
+}
+
+}  // namespace tiles

@@ -88,6 +88,12 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     G_.qd = d.n_q_heads * d.head_dim;
     G_.kvd = d.n_kv_heads * d.head_dim;
     G_.qkv_rows = G_.qd + 2 * G_.kvd;
+    if (o.weight_format != TILES_WEIGHTS_BF16 && o.weight_format != TILES_WEIGHTS_INT8)
+        return fail(TILES_ERR_INVALID_ARG, "weight_format");
+    G_.wbytes = o.weight_format == TILES_WEIGHTS_INT8 ? 1 : 2;
+    // INT8 rows are reduced in 16-code pieces (and copied in 16-byte units)
+    if (G_.wbytes == 1 && (G_.H % 16 || G_.F % 16 || G_.qd % 16))
+        return fail(TILES_ERR_UNSUPPORTED, "INT8 weights need hidden, ffn and q width multiples of 16");
 
     // slot: large enough for one row of every GEMV (two for gate/up). Each
     // slot has one owning consumer warp, so the default ring is one slot per
@@ -95,12 +101,13 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     // reduces it, and smaller chunks turn the ring over faster. Measured on
     // GB300 for the Llama-1B shape: 8 x 16 KB beat 6 x 32 KB by 6 % and
     // 12 x 16 KB (uneven ownership) by 2 %.
-    int need = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, 2 * 2 * G_.H});
+    const int wb = G_.wbytes;
+    int need = std::max({wb * G_.H, wb * G_.qd, wb * G_.F, 2 * wb * G_.H});
     int slot = o.slot_bytes > 0 ? o.slot_bytes : round_up(std::max(need, 16384), 1024);
     if (slot % 1024 || slot < need) return fail(TILES_ERR_INVALID_ARG, "slot_bytes too small or not a multiple of 1024");
     G_.slot_bytes = slot;
     auto rpc = [&](int in, int mats) {
-        return std::min(kMaxRowsPerChunk, slot / (in * 2 * mats));
+        return std::min(kMaxRowsPerChunk, slot / (in * G_.wbytes * mats));
     };
     G_.rpc_qkv = rpc(G_.H, 1);
     G_.rpc_o = rpc(G_.qd, 1);
@@ -241,7 +248,7 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
             phase_layer[phi] = l < g.L ? l : 0;
             if (op_is_gemv(op)) {
                 phase_tasks[phi] = assign_rows(op_extent(g, op),
-                                               (long long)op_in_dim(g, op) * 2 * op_mats(op), N,
+                                               (long long)op_in_dim(g, op) * g.wbytes * op_mats(op), N,
                                                cum);
             } else if (op == TILES_OP_ATTN) {
                 int n = op_extent(g, op);
@@ -378,12 +385,12 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
     // geometry: every copy is a whole number of 16-byte units into 128-byte aligned slots
     if (g.slot_bytes % 1024 || g.ring_slots < 2 || g.ring_slots > kMaxSlots)
         return fail("ring geometry");
-    if ((2 * g.H) % 16 || (2 * g.F) % 16 || (2 * g.qd) % 16 || (2 * g.d) % 16)
+    if ((g.wbytes * g.H) % 16 || (g.wbytes * g.F) % 16 || (g.wbytes * g.qd) % 16 || (2 * g.d) % 16)
         return fail("row bytes not a multiple of 16");
     for (int op = TILES_OP_QKV; op <= TILES_OP_LMHEAD; ++op) {
         if (!op_is_gemv(op)) continue;
         int r = op_rows_per_chunk(g, op);
-        if (r < 1 || (long long)r * op_in_dim(g, op) * 2 * op_mats(op) > g.slot_bytes)
+        if (r < 1 || (long long)r * op_in_dim(g, op) * g.wbytes * op_mats(op) > g.slot_bytes)
             return fail("rows per chunk do not fit a slot");
     }
     if (g.kv_block < 1 || 2LL * g.kv_block * g.d * 2 > g.slot_bytes) return fail("kv block");

@@ -16,8 +16,10 @@
 #include "tiles_internal.h"
 
 namespace tiles {
-cudaError_t megakernel_configure(int d, int G, int smem_bytes);
-cudaError_t megakernel_occupancy(int d, int G, int smem_bytes, int *blocks_per_sm);
+cudaError_t megakernel_configure(int d, int G, int wbytes, int smem_bytes);
+cudaError_t megakernel_occupancy(int d, int G, int wbytes, int smem_bytes, int *blocks_per_sm);
+cudaError_t quantize_rows_launch(const void *src, int rows, int cols, void *dst, float *scale,
+                                 int row_step, int row0, cudaStream_t st);
 cudaError_t megakernel_launch(const KernelParams &p, int n_ctas, int smem_bytes, cudaStream_t st);
 cudaError_t copy_launch(void *dst, const void *src, size_t bytes, int n_ctas, cudaStream_t st);
 cudaError_t barrier_launch(uint32_t *ctr, int rounds, unsigned long long *elapsed, uint32_t *status,
@@ -159,9 +161,9 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
     const Geom &g = plan->sched.geom;
 
     // the worker must fit one CTA per SM at this shared-memory size (co-residency)
-    e = megakernel_configure(g.d, g.G, g.smem_bytes);
+    e = megakernel_configure(g.d, g.G, g.wbytes, g.smem_bytes);
     int occ = 0;
-    if (e == cudaSuccess) e = megakernel_occupancy(g.d, g.G, g.smem_bytes, &occ);
+    if (e == cudaSuccess) e = megakernel_occupancy(g.d, g.G, g.wbytes, g.smem_bytes, &occ);
     if (e != cudaSuccess || occ < 1) {
         delete plan;
         return e != cudaSuccess ? TILES_ERR_CUDA : TILES_ERR_UNSUPPORTED;
@@ -196,29 +198,76 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
     if ((e = dalloc(plan, &d_off, plan->sched.offsets.size() * sizeof(int32_t))) != cudaSuccess) return fail(e);
     if ((e = dalloc(plan, &d_layers, (size_t)g.L * sizeof(LayerPtrs))) != cudaSuccess) return fail(e);
     std::vector<LayerPtrs> lp(g.L);
+    const size_t H2 = (size_t)g.H * 2;
     for (int l = 0; l < g.L; ++l) {
         const tiles_layer_weights &lw = w->layers[l];
-        lp[l] = LayerPtrs{(const uint16_t *)lw.attn_norm, (const uint16_t *)lw.wq, (const uint16_t *)lw.wk,
-                          (const uint16_t *)lw.wv,        (const uint16_t *)lw.q_norm, (const uint16_t *)lw.k_norm,
-                          (const uint16_t *)lw.wo,        (const uint16_t *)lw.ffn_norm, (const uint16_t *)lw.w_gate,
-                          (const uint16_t *)lw.w_up,      (const uint16_t *)lw.w_down, nullptr, nullptr};
-        // packed copies ("TilePlan ... packs the weights"): [Wq; Wk; Wv] contiguous,
-        // and Wg / Wu interleaved by row, so each ring chunk is one bulk copy
-        const size_t H2 = (size_t)g.H * 2;
-        uint16_t *qkv, *gu;
-        if ((e = dalloc(plan, &qkv, (size_t)g.qkv_rows * H2)) != cudaSuccess) return fail(e);
-        if ((e = dalloc(plan, &gu, (size_t)g.F * 2 * H2)) != cudaSuccess) return fail(e);
-        uint8_t *q8 = reinterpret_cast<uint8_t *>(qkv);
-        if ((e = cudaMemcpy(q8, lw.wq, (size_t)g.qd * H2, cudaMemcpyDeviceToDevice)) != cudaSuccess ||
-            (e = cudaMemcpy(q8 + (size_t)g.qd * H2, lw.wk, (size_t)g.kvd * H2, cudaMemcpyDeviceToDevice)) != cudaSuccess ||
-            (e = cudaMemcpy(q8 + (size_t)(g.qd + g.kvd) * H2, lw.wv, (size_t)g.kvd * H2, cudaMemcpyDeviceToDevice)) !=
-                cudaSuccess ||
-            (e = cudaMemcpy2D(gu, 2 * H2, lw.w_gate, H2, H2, g.F, cudaMemcpyDeviceToDevice)) != cudaSuccess ||
-            (e = cudaMemcpy2D(reinterpret_cast<uint8_t *>(gu) + H2, 2 * H2, lw.w_up, H2, H2, g.F,
-                              cudaMemcpyDeviceToDevice)) != cudaSuccess)
+        LayerPtrs &L = lp[l];
+        L.attn_norm = (const uint16_t *)lw.attn_norm;
+        L.q_norm = (const uint16_t *)lw.q_norm;
+        L.k_norm = (const uint16_t *)lw.k_norm;
+        L.ffn_norm = (const uint16_t *)lw.ffn_norm;
+        L.s_qkv = L.s_o = L.s_gu = L.s_down = nullptr;
+        if (g.wbytes == 2) {
+            // packed BF16 copies ("TilePlan ... packs the weights"): [Wq; Wk; Wv]
+            // contiguous, and Wg / Wu interleaved by row, so each ring chunk is one bulk copy
+            uint8_t *qkv, *gu;
+            if ((e = dalloc(plan, &qkv, (size_t)g.qkv_rows * H2)) != cudaSuccess) return fail(e);
+            if ((e = dalloc(plan, &gu, (size_t)g.F * 2 * H2)) != cudaSuccess) return fail(e);
+            if ((e = cudaMemcpy(qkv, lw.wq, (size_t)g.qd * H2, cudaMemcpyDeviceToDevice)) != cudaSuccess ||
+                (e = cudaMemcpy(qkv + (size_t)g.qd * H2, lw.wk, (size_t)g.kvd * H2, cudaMemcpyDeviceToDevice)) != cudaSuccess ||
+                (e = cudaMemcpy(qkv + (size_t)(g.qd + g.kvd) * H2, lw.wv, (size_t)g.kvd * H2, cudaMemcpyDeviceToDevice)) !=
+                    cudaSuccess ||
+                (e = cudaMemcpy2D(gu, 2 * H2, lw.w_gate, H2, H2, g.F, cudaMemcpyDeviceToDevice)) != cudaSuccess ||
+                (e = cudaMemcpy2D(gu + H2, 2 * H2, lw.w_up, H2, H2, g.F, cudaMemcpyDeviceToDevice)) != cudaSuccess)
+                return fail(e);
+            L.qkv = qkv;
+            L.gu = gu;
+            L.o = (const uint8_t *)lw.wo;
+            L.down = (const uint8_t *)lw.w_down;
+        } else {
+            // INT8 codes and per-row scales, quantized straight into the packed layouts
+            uint8_t *qkv, *o, *gu, *down;
+            float *sqkv, *so, *sgu, *sdown;
+            if ((e = dalloc(plan, &qkv, (size_t)g.qkv_rows * g.H)) != cudaSuccess ||
+                (e = dalloc(plan, &o, (size_t)g.H * g.qd)) != cudaSuccess ||
+                (e = dalloc(plan, &gu, (size_t)2 * g.F * g.H)) != cudaSuccess ||
+                (e = dalloc(plan, &down, (size_t)g.H * g.F)) != cudaSuccess ||
+                (e = dalloc(plan, &sqkv, (size_t)g.qkv_rows * 4)) != cudaSuccess ||
+                (e = dalloc(plan, &so, (size_t)g.H * 4)) != cudaSuccess ||
+                (e = dalloc(plan, &sgu, (size_t)2 * g.F * 4)) != cudaSuccess ||
+                (e = dalloc(plan, &sdown, (size_t)g.H * 4)) != cudaSuccess)
+                return fail(e);
+            if ((e = quantize_rows_launch(lw.wq, g.qd, g.H, qkv, sqkv, 1, 0, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.wk, g.kvd, g.H, qkv, sqkv, 1, g.qd, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.wv, g.kvd, g.H, qkv, sqkv, 1, g.qd + g.kvd, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.wo, g.H, g.qd, o, so, 1, 0, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.w_gate, g.F, g.H, gu, sgu, 2, 0, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.w_up, g.F, g.H, gu, sgu, 2, 1, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.w_down, g.H, g.F, down, sdown, 1, 0, 0)) != cudaSuccess)
+                return fail(e);
+            L.qkv = qkv;
+            L.o = o;
+            L.gu = gu;
+            L.down = down;
+            L.s_qkv = sqkv;
+            L.s_o = so;
+            L.s_gu = sgu;
+            L.s_down = sdown;
+        }
+    }
+    // the LM head streams the tied embedding, or its INT8 codes
+    p.lm = (const uint8_t *)w->embed;
+    p.lm_s = nullptr;
+    if (g.wbytes == 1) {
+        uint8_t *lm;
+        float *lms;
+        if ((e = dalloc(plan, &lm, (size_t)g.V * g.H)) != cudaSuccess ||
+            (e = dalloc(plan, &lms, (size_t)g.V * 4)) != cudaSuccess ||
+            (e = quantize_rows_launch(w->embed, g.V, g.H, lm, lms, 1, 0, 0)) != cudaSuccess ||
+            (e = cudaDeviceSynchronize()) != cudaSuccess)
             return fail(e);
-        lp[l].wqkv = qkv;
-        lp[l].wgu = gu;
+        p.lm = lm;
+        p.lm_s = lms;
     }
     {
         // the validated table, or (test hook) with CTA 0's first wait on a target
@@ -418,6 +467,14 @@ tiles_status_t tiles_decode_host(tiles_plan_t plan, void *k_cache, void *v_cache
                     cudaSuccess)
         return TILES_ERR_CUDA;
     return tiles_status(plan, stream);
+}
+
+tiles_status_t tiles_quantize_rows_int8(const void *w_bf16, int32_t rows, int32_t cols, void *codes,
+                                        float *scales, void *stream) {
+    if (rows < 0 || cols < 1 || (rows > 0 && (!w_bf16 || !codes || !scales))) return TILES_ERR_INVALID_ARG;
+    const cudaError_t e = quantize_rows_launch(w_bf16, rows, cols, codes, scales, 1, 0,
+                                               reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TILES_OK : TILES_ERR_CUDA;
 }
 
 tiles_status_t tiles_copy_bw(void *dst, const void *src, size_t bytes, int32_t n_ctas, void *stream) {

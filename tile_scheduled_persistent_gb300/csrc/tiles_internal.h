@@ -39,6 +39,7 @@ struct Geom {
     int L, H, nq, nkv, d, F, V, max_pos, G, qd, kvd, qkv_rows;
     int slot_bytes, ring_slots, kv_splits, kv_block;
     int rpc_qkv, rpc_o, rpc_gateup, rpc_down, rpc_lm;
+    int wbytes;     // bytes per streamed weight: 2 (BF16) or 1 (INT8 codes)
     int vec_bytes;  // shared-memory region for the input vector / attention scratch
     int res_off;    // in the vec region: residual rows of an O-proj / down tile
     int smem_bytes;
@@ -135,7 +136,7 @@ TILES_HD int task_chunks(const Geom &g, const tiles_task &t, int P) {
 // Bytes a task streams from HBM at position P (weights, or K/V of positions < P).
 TILES_HD long long task_bytes(const Geom &g, const tiles_task &t, int P) {
     if (op_is_gemv(t.op))
-        return (long long)(t.end - t.begin) * op_in_dim(g, t.op) * 2 * op_mats(t.op);
+        return (long long)(t.end - t.begin) * op_in_dim(g, t.op) * g.wbytes * op_mats(t.op);
     if (t.op == TILES_OP_ATTN) {
         long long n = 0;
         for (uint32_t it = t.begin; it < t.end; ++it) {
@@ -150,14 +151,16 @@ TILES_HD long long task_bytes(const Geom &g, const tiles_task &t, int P) {
     return 0;
 }
 
-// Device copy of one layer's weight pointers.
-// wqkv and wgu are the plan's packed copies: [Wq; Wk; Wv] as one [qd + 2 kvd][H]
-// matrix, and Wg / Wu interleaved by row ([F][2][H]: gate row r, then up row
-// r), so every ring chunk of those tiles is a single contiguous bulk copy.
+// Device copy of one layer's pointers. The streamed weights are rows of
+// g.wbytes-byte elements: qkv = [Wq; Wk; Wv] as one [qd + 2 kvd][H] matrix and
+// gu = Wg / Wu interleaved by row ([F][2][H]: gate row r, then up row r), both
+// plan-packed so every ring chunk of those tiles is one contiguous bulk copy;
+// o = Wo [H][qd], down = Wd [H][F]. With INT8 weights every streamed row has
+// an FP32 scale (s_gu in the interleaved row order); with BF16 they are null.
 struct LayerPtrs {
-    const uint16_t *attn_norm, *wq, *wk, *wv, *q_norm, *k_norm, *wo, *ffn_norm, *w_gate, *w_up,
-        *w_down;
-    const uint16_t *wqkv, *wgu;
+    const uint16_t *attn_norm, *q_norm, *k_norm, *ffn_norm;
+    const uint8_t *qkv, *o, *gu, *down;
+    const float *s_qkv, *s_o, *s_gu, *s_down;
 };
 
 struct KernelParams {
@@ -171,7 +174,9 @@ struct KernelParams {
     uint32_t final_mul;
     // weights
     const LayerPtrs *layers;
-    const uint16_t *embed, *final_norm;
+    const uint16_t *embed, *final_norm;   // BF16 embedding table (the lookup) and final gain
+    const uint8_t *lm;                    // LM-head rows as streamed: the embedding, or its INT8 codes
+    const float *lm_s;                    // INT8: their scales (null for BF16)
     const float *rope_cos, *rope_sin;  // [max_pos][d/2]
     // caches and scratch
     uint16_t *k_cache, *v_cache;
