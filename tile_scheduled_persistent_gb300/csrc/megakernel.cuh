@@ -682,26 +682,53 @@ __device__ __forceinline__ void gemv_rows_n(uint32_t nr, const uint8_t *slot, co
 }
 
 // ------------------------------------------------------------------ INT8 GEMV rows
-// Four INT8 codes of a word to exact floats: with the sign bit of each byte
-// flipped (u = q + 128), the byte placed under the exponent of 2^23 is the
-// float 2^23 + u, and subtracting 2^23 + 128 leaves q (both steps exact).
-__device__ __forceinline__ void q8_word(uint32_t w, float (&f)[4]) {
-    const uint32_t u = w ^ 0x80808080u;
-    f[0] = __fsub_rn(__int_as_float(__byte_perm(u, 0x4B000000u, 0x7540)), 8388736.0f);
-    f[1] = __fsub_rn(__int_as_float(__byte_perm(u, 0x4B000000u, 0x7541)), 8388736.0f);
-    f[2] = __fsub_rn(__int_as_float(__byte_perm(u, 0x4B000000u, 0x7542)), 8388736.0f);
-    f[3] = __fsub_rn(__int_as_float(__byte_perm(u, 0x4B000000u, 0x7543)), 8388736.0f);
+// Two FP32 lanes in one 64-bit register (low word first), for the paired
+// FP32 instructions of sm_100 and later (one issue does two adds or FMAs).
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_pack_bits(uint32_t lo, uint32_t hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ float f2_sum(unsigned long long v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return __fadd_rn(lo, hi);
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
 }
 
-// 16 codes times 16 inputs, accumulated in FP32 (each product is exact)
-__device__ __forceinline__ float dot16_q8(const uint4 &w, const float (&x)[16], float acc) {
+// Four INT8 codes of a word to exact floats, as two pairs: with the sign bit
+// of each byte flipped (u = q + 128), the byte placed under the exponent of
+// 2^23 is the float 2^23 + u, and subtracting 2^23 + 128 leaves q (both steps
+// exact). Then 16 codes times 16 inputs (8 pairs), accumulated in FP32 on two
+// lanes (even and odd elements); each product is exact.
+__device__ __forceinline__ unsigned long long dot16_q8(const uint4 &w, const unsigned long long (&x)[8],
+                                                       unsigned long long acc) {
+    const unsigned long long bias = f2_pack(8388736.0f, 8388736.0f);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        float f[4];
-        q8_word(ws[k], f);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc = fmaf(f[i], x[4 * k + i], acc);
+        const uint32_t u = ws[k] ^ 0x80808080u;
+        const unsigned long long f01 =
+            f2_sub(f2_pack_bits(__byte_perm(u, 0x4B000000u, 0x7540), __byte_perm(u, 0x4B000000u, 0x7541)), bias);
+        const unsigned long long f23 =
+            f2_sub(f2_pack_bits(__byte_perm(u, 0x4B000000u, 0x7542), __byte_perm(u, 0x4B000000u, 0x7543)), bias);
+        acc = f2_fma(f01, x[2 * k], acc);
+        acc = f2_fma(f23, x[2 * k + 1], acc);
     }
     return acc;
 }
@@ -713,29 +740,25 @@ template <int MATS, int NR>
 __device__ __forceinline__ void gemv_rows_q8(const uint8_t *slot, const uint4 *vec, int n16,
                                              size_t row_bytes, float (&res)[MATS]) {
     const int lane = threadIdx.x & 31;
-    float acc[NR][MATS];
+    unsigned long long acc[NR][MATS];
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int m = 0; m < MATS; ++m) acc[r][m] = 0.f;
+        for (int m = 0; m < MATS; ++m) acc[r][m] = 0ull;
     for (int c = lane; c < n16; c += 32) {
-        float xf[16];
+        unsigned long long xp[8];
         {
-            float a[8], b[8];
-            unpack8(vec[2 * c], a);
-            unpack8(vec[2 * c + 1], b);
+            const uint4 a = vec[2 * c], b = vec[2 * c + 1];
+            const uint32_t xs[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                xf[e] = a[e];
-                xf[8 + e] = b[e];
-            }
+            for (int e = 0; e < 8; ++e) xp[e] = f2_pack(bf_lo(xs[e]), bf_hi(xs[e]));
         }
 #pragma unroll
         for (int r = 0; r < NR; ++r)
 #pragma unroll
             for (int m = 0; m < MATS; ++m) {
                 const uint4 w = reinterpret_cast<const uint4 *>(slot + ((size_t)r * MATS + m) * row_bytes)[c];
-                acc[r][m] = dot16_q8(w, xf, acc[r][m]);
+                acc[r][m] = dot16_q8(w, xp, acc[r][m]);
             }
     }
 #pragma unroll
@@ -744,7 +767,7 @@ __device__ __forceinline__ void gemv_rows_q8(const uint8_t *slot, const uint4 *v
     for (int r = 0; r < NR; ++r)
 #pragma unroll
         for (int m = 0; m < MATS; ++m) {
-            const float v = warp_sum(acc[r][m]);
+            const float v = warp_sum(f2_sum(acc[r][m]));
             if (lane == r) res[m] = v;
         }
 }
