@@ -72,14 +72,20 @@ def whole_job_rate(units_per_rank, seconds, device="cpu"):
     return units_per_rank * ws / slowest, slowest
 
 
-def workload_config(cfg):
+def workload_config(cfg, int8=False):
     return {"workload": f"{cfg.name}: {cfg.n_layers} layers, hidden {cfg.hidden}, "
                         f"{cfg.n_q_heads}/{cfg.n_kv_heads} heads x {cfg.head_dim}, ffn {cfg.ffn}, "
                         f"vocab {cfg.vocab}, {cfg.start_pos} cached positions, "
                         f"{cfg.n_new} greedy tokens per step",
+            "weights": WEIGHT_DESC[int8],
             "tokens_per_step": cfg.n_new, "cached_positions": cfg.start_pos,
-            "bytes_per_token": int(round(cfg.algorithmic_bytes_per_token())),
-            "l2": "inputs larger than L2 (every token streams all weights, >1 GB)"}
+            "bytes_per_token": int(round(cfg.algorithmic_bytes_per_token(int8))),
+            "l2": "inputs larger than L2 (every token streams all weights, >0.5 GB)"}
+
+
+WEIGHT_DESC = {False: "bf16",
+               True: "int8 codes with one fp32 scale per output row (GEMV matrices and LM head)"}
+DTYPE = {False: "bf16", True: "int8 weights x bf16 activations, fp32 accumulate"}
 
 
 def measured_peaks():
@@ -175,13 +181,23 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------- CPU oracle arm
-def oracle_sample(cfg, w, k, v, prompt, n_tokens):
-    """Time the oracle on n_tokens decode steps of the workload (all host cores)."""
+def oracle_sample(cfg, w, k, v, prompt, n_tokens, qweights=None):
+    """Time the oracle on n_tokens decode steps of the workload (all host cores);
+    with qweights, its weight-only INT8 form."""
     import oracle
     kk, vv = k.copy(), v.copy()
     t0 = time.perf_counter()
-    oracle.decode(cfg, w, kk, vv, prompt, cfg.start_pos, n_tokens, want_logits=False)
+    oracle.decode(cfg, w, kk, vv, prompt, cfg.start_pos, n_tokens, want_logits=False,
+                  qweights=qweights)
     return time.perf_counter() - t0
+
+
+def oracle_qweights(w, int8):
+    """The oracle's INT8 weights (quantized once, outside any timed region), or None."""
+    if not int8:
+        return None
+    import oracle
+    return oracle.quantize_model(w)
 
 
 def run_reference(args):
@@ -194,10 +210,12 @@ def run_reference(args):
     w = S.model_weights(cfg)
     k, v = S.kv_prefill(cfg)
     prompt = S.prompt(cfg)
+    int8 = args.weights == "int8"
+    qw = oracle_qweights(w, int8)
     n_tok = args.ref_tokens
     for _ in range(args.warmup):
-        oracle_sample(cfg, w, k, v, prompt, n_tok)
-    times = [oracle_sample(cfg, w, k, v, prompt, n_tok) for _ in range(args.steps)]
+        oracle_sample(cfg, w, k, v, prompt, n_tok, qw)
+    times = [oracle_sample(cfg, w, k, v, prompt, n_tok, qw) for _ in range(args.steps)]
     tot = sum(times)
     value = n_tok * args.steps / tot
     cores = os.cpu_count()
@@ -205,8 +223,8 @@ def run_reference(args):
               f"(of {cfg.n_new}), OpenMP over output rows and heads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": workload_config(cfg),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE[int8],
+            "data": "synthetic", "config": workload_config(cfg, int8),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -268,12 +286,14 @@ def run_ours(args):
     except tsp.TilesError:
         barrier_ns = None
 
-    bytes_per_token = cfg.algorithmic_bytes_per_token()
+    int8 = args.weights == "int8"
+    bytes_per_token = cfg.algorithmic_bytes_per_token(int8)
     results = {}
     scheds = list(SCHEDULERS) if args.scheduler == "all" else [args.scheduler]
     for sname in scheds:
         plan = tsp.Plan(tsp.ModelDesc.from_config(cfg), dw,
-                        tsp.make_opts(scheduler=SCHEDULERS[sname]))
+                        tsp.make_opts(scheduler=SCHEDULERS[sname],
+                                      weight_format=tsp.WEIGHTS_INT8 if int8 else tsp.WEIGHTS_BF16))
         info = plan.info()
         toks = torch.zeros(cfg.n_new, dtype=torch.int32, device="cuda")
         ref_toks = None
@@ -321,7 +341,7 @@ def run_ours(args):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
     else:
         peak, peak_src = 6800.0, "fallback 6.8 TB/s"
-    traffic = recorded_traffic(cfg.name, cfg.n_new)
+    traffic = recorded_traffic(cfg.name + ("_int8" if int8 else ""), cfg.n_new)
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     plan = r["plan"]
@@ -339,20 +359,21 @@ def run_ours(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         n_tok = args.ref_tokens
-        secs = oracle_sample(cfg, w, k_np, v_np, prompt_np, n_tok)
+        secs = oracle_sample(cfg, w, k_np, v_np, prompt_np, n_tok, oracle_qweights(w, int8))
         cpu = {"value": n_tok / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"first {n_tok} of the {cfg.n_new} decode tokens from position "
-                         f"{cfg.start_pos}, OpenMP over output rows and heads on all host cores"}
+                         f"{cfg.start_pos}, OpenMP over output rows and heads on all host cores"
+                         + (", the oracle's weight-only INT8 path" if int8 else "")}
 
     if rank == 0:
-        conf = workload_config(cfg)
+        conf = workload_config(cfg, int8)
         conf.update({"scheduler": chosen, "ctas": r["info"]["n_ctas"],
                      "ring": f"{r['info']['ring_slots']} x {r['info']['slot_bytes']} B",
                      "kv_splits": r["info"]["kv_splits"], "parallelism": f"replicas x{ws}"})
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1000 * total_s / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "scaling": "weak", "vs_baseline": None, "dtype": DTYPE[int8], "data": "synthetic",
                 "config": conf,
                 "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak,
                              "unit": "GB/s", "frac": achieved_gbs / peak,
@@ -389,6 +410,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=2,
                     help="oracle decode tokens per timed step (CPU arms)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "int8"],
+                    help="weight format of the plan (int8: weight-only, per-row scales)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="decode tokens per step (default: the workload's 64); a smaller "
                          "launch of the same kernel, for profiler captures")

@@ -162,22 +162,28 @@ class ModelConfig:
     def kv_dim(self) -> int:
         return self.n_kv_heads * self.head_dim
 
-    def weight_bytes(self) -> int:
-        """BF16 bytes of every weight once (tied embedding counted once, as the LM head)."""
+    def weight_bytes(self, int8: bool = False) -> int:
+        """Bytes of every weight once (tied embedding counted once, as the LM head):
+        BF16, or with the GEMV matrices and the LM head as INT8 codes plus one FP32
+        scale per row (norm weights stay BF16)."""
         H, F = self.hidden, self.ffn
-        per_layer = (self.q_dim + 2 * self.kv_dim) * H + H * self.q_dim + 3 * F * H + 2 * H
-        if self.qk_norm:
-            per_layer += 2 * self.head_dim
-        return 2 * (self.n_layers * per_layer + self.vocab * H + H)
+        qkv_rows = self.q_dim + 2 * self.kv_dim
+        matrix = qkv_rows * H + H * self.q_dim + 3 * F * H        # weights per layer
+        rows = qkv_rows + H + 2 * F + H                            # output rows per layer
+        norms = 2 * H + (2 * self.head_dim if self.qk_norm else 0)
+        if not int8:
+            return 2 * (self.n_layers * (matrix + norms) + self.vocab * H + H)
+        return (self.n_layers * (matrix + 4 * rows + 2 * norms)
+                + self.vocab * H + 4 * self.vocab + 2 * H)
 
-    def algorithmic_bytes_per_token(self) -> float:
+    def algorithmic_bytes_per_token(self, int8: bool = False) -> float:
         """Weights once + one embedding row + K/V of positions 0..P read + new K/V write,
         averaged over the run's decode positions."""
         kv_pos_bytes = 2 * 2 * self.n_layers * self.kv_dim      # K and V, one position, all layers
         p0 = self.start_pos
         steps = self.n_steps
         avg_read_pos = p0 + (steps - 1) / 2.0 + 1.0              # positions 0..P inclusive
-        return (self.weight_bytes() + 2 * self.hidden
+        return (self.weight_bytes(int8) + 2 * self.hidden
                 + kv_pos_bytes * avg_read_pos + kv_pos_bytes)
 
     def with_workload(self, **kw) -> "ModelConfig":

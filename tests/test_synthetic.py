@@ -55,3 +55,21 @@ def test_config_byte_counts():
     assert c.weight_bytes() == 2 * (16 * (3072 * 2048 + 2048 * 2048 + 3 * 8192 * 2048 + 2 * 2048)
                                     + 128256 * 2048 + 2048)
     assert abs(c.algorithmic_bytes_per_token() - 2.5063e9) < 1e6
+
+
+def test_config_byte_counts_equal_the_arrays_they_count():
+    """weight_bytes counts what the arrays hold: every BF16 weight once, or the
+    INT8 codes and FP32 row scales of the oracle's quantized model plus the
+    BF16 norm weights."""
+    import oracle
+    for cfg in (S.CONFIGS["tiny"], S.CONFIGS["tiny"].with_workload(qk_norm=True)):
+        w = S.model_weights(cfg)
+        arrays = [w.embed, w.final_norm] + [a for lw in w.layers for a in lw.values() if a is not None]
+        assert cfg.weight_bytes() == sum(a.nbytes for a in arrays)
+        qw = oracle.quantize_model(w)
+        norms = [lw[n] for lw in w.layers for n in ("attn_norm", "ffn_norm", "q_norm", "k_norm")
+                 if lw[n] is not None]
+        q_bytes = (sum(c.nbytes + s.nbytes for ql in qw.layers for c, s in ql.values())
+                   + qw.lm[0].nbytes + qw.lm[1].nbytes + w.final_norm.nbytes
+                   + sum(a.nbytes for a in norms))
+        assert cfg.weight_bytes(int8=True) == q_bytes

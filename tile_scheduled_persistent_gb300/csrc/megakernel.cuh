@@ -1008,6 +1008,13 @@ struct Consumer {
             if (!mine(jj)) continue;
             const uint32_t r0 = t.begin + k * rpc;
             const uint32_t nr = t.end - r0 < rpc ? t.end - r0 : rpc;
+            float sc[MATS];  // INT8: the row scales load while the chunk arrives
+            if constexpr (Q8) {
+                const uint32_t row = r0 + ((uint32_t)lane < nr ? lane : 0);
+#pragma unroll
+                for (int m = 0; m < MATS; ++m)  // gate/up: packed rows 2 row, 2 row + 1
+                    sc[m] = __ldg(scale + (MATS == 2 ? 2 * row + m : row));
+            }
             const uint8_t *slot = wait_chunk(jj);
             if (!slot) break;
             float mine[MATS];
@@ -1018,12 +1025,8 @@ struct Consumer {
             }
             release_chunk(jj);
             if constexpr (Q8) {
-                if ((uint32_t)lane < nr) {
-                    const uint32_t row = r0 + lane;
 #pragma unroll
-                    for (int m = 0; m < MATS; ++m)  // gate/up: packed rows 2 row, 2 row + 1
-                        mine[m] = __fmul_rn(mine[m], __ldg(scale + (MATS == 2 ? 2 * row + m : row)));
-                }
+                for (int m = 0; m < MATS; ++m) mine[m] = __fmul_rn(mine[m], sc[m]);
             }
             if ((uint32_t)lane < nr) emit_row<MATS>(op, t, r0 + lane, mine);
             if (op == TILES_OP_LMHEAD) {

@@ -106,14 +106,24 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     int slot = o.slot_bytes > 0 ? o.slot_bytes : round_up(std::max(need, 16384), 1024);
     if (slot % 1024 || slot < need) return fail(TILES_ERR_INVALID_ARG, "slot_bytes too small or not a multiple of 1024");
     G_.slot_bytes = slot;
-    auto rpc = [&](int in, int mats) {
-        return std::min(kMaxRowsPerChunk, slot / (in * G_.wbytes * mats));
+    // Rows per chunk: as many as fill a slot. INT8 layer GEMVs are capped so
+    // that a CTA's share of rows splits into at least one chunk per consumer
+    // warp: a 16 KB INT8 chunk holds twice the weights of a BF16 one, and in
+    // the short, latency-bound layer phases one warp's chunk arithmetic sets
+    // the pace (GB300: Llama-1B shape 1547 -> 1682 tok/s, Qwen3-0.6B shape
+    // 1049 -> 1273; the same cap on BF16 measured neutral, so BF16 keeps full
+    // chunks). The LM head streams far more rows than warps and stays full.
+    auto rpc = [&](int in, int mats, int rows) {
+        const int full = std::min(kMaxRowsPerChunk, slot / (in * G_.wbytes * mats));
+        if (G_.wbytes != 1 || rows <= 0) return full;
+        const int per_cta = ceil_div(rows, n_ctas);
+        return std::max(1, std::min(full, ceil_div(per_cta, kConsumerWarps)));
     };
-    G_.rpc_qkv = rpc(G_.H, 1);
-    G_.rpc_o = rpc(G_.qd, 1);
-    G_.rpc_gateup = rpc(G_.H, 2);
-    G_.rpc_down = rpc(G_.F, 1);
-    G_.rpc_lm = rpc(G_.H, 1);
+    G_.rpc_qkv = rpc(G_.H, 1, G_.qkv_rows);
+    G_.rpc_o = rpc(G_.qd, 1, G_.H);
+    G_.rpc_gateup = rpc(G_.H, 2, G_.F);
+    G_.rpc_down = rpc(G_.F, 1, G_.H);
+    G_.rpc_lm = rpc(G_.H, 1, 0);
     int kb = slot / (2 * G_.d * 2);
     kb = kb >= 32 ? kb / 32 * 32 : kb;
     if (kb < 1) return fail(TILES_ERR_UNSUPPORTED, "slot too small for one KV position");
