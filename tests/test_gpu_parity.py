@@ -124,6 +124,48 @@ def test_variants_match_oracle(tsp, name, scheduler):
     plan.close()
 
 
+# ------------------------------------------------------------------ tensor-core attention
+# An attention item whose KV split spans at least 8 chunks takes the tensor-
+# core path (swizzled TMA tiles, m16n8k16 MMAs); fewer, the shared-chunk path.
+# With 2 splits these contexts give splits of 7 to 9 chunks, so layers mix
+# both paths, and the last block runs past max_pos in "d64_g2" (the tiled copy
+# fills those rows with zeros).
+MMA = {
+    "d64_g2": replace(S.CONFIGS["tiny"], name="m1", start_pos=955, n_prompt=2, n_new=24, max_pos=1000),
+    "d64_g1": replace(S.CONFIGS["tiny"], name="m2", n_q_heads=2, n_kv_heads=2, start_pos=1010,
+                      n_prompt=2, n_new=12, max_pos=1030),
+    "d128_g8_qknorm": replace(VARIANTS["d128_g8_qknorm"], name="m3", start_pos=490, n_prompt=2,
+                              n_new=24, max_pos=520),
+    "d128_g2_qknorm": replace(VARIANTS["d128_g8_qknorm"], name="m4", n_q_heads=4, n_kv_heads=2,
+                              start_pos=500, n_prompt=2, n_new=16, max_pos=530),
+}
+
+
+@pytest.mark.parametrize("name", list(MMA))
+def test_tensor_core_attention_matches_oracle(tsp, name):
+    """Every head shape on the tensor-core attention path, against the oracle.
+    Cache rows not yet written hold NaN: the kernel copies whole blocks, so
+    those rows reach shared memory and must never count as data."""
+    cfg = MMA[name]
+    w, k, v, prompt = inputs(cfg)
+    prompt = prompt[: cfg.n_prompt]
+    k[:, :, cfg.start_pos:, :] = 0x7FC0       # BF16 NaN
+    v[:, :, cfg.start_pos:, :] = 0x7FC0
+    ref, kref, vref = oracle_run(cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new)
+    plan = _plan(tsp, cfg, w, kv_splits=2)
+    toks, logits, kc, vc = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, cfg.n_new)
+    plan.close()
+    assert not np.isnan(logits).any()
+    assert_parity(toks, logits, ref, name + " tensor-core attention")
+    # the cache: rows written in the run close to the oracle's, the NaN rows after untouched
+    end = cfg.start_pos + cfg.n_prompt - 1 + cfg.n_new
+    for got, want in ((kc, kref), (vc, vref)):
+        np.testing.assert_allclose(S.bf16_to_f32(got[:, :, :end]).astype(np.float64),
+                                   S.bf16_to_f32(want[:, :, :end]).astype(np.float64),
+                                   atol=2e-2, rtol=2e-2)
+        assert (got[:, :, end:] == 0x7FC0).all()
+
+
 def test_few_ctas_and_small_ring(tsp):
     """A plan on 7 CTAs with a 2-slot ring and 3 KV splits still matches."""
     cfg = VARIANTS["g2_cache"]

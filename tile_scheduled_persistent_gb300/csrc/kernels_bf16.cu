@@ -1,13 +1,14 @@
 // Kernel instances with BF16 weights: one per (head_dim, q heads per KV head),
 // a smaller instruction footprint than one kernel that switches between them
-// (measured on the Llama-1B shape: 2.7 % faster).
+// (measured on the Llama-1B shape: 2.7 % faster). These leave out the
+// tensor-core attention path, which only long-context plans use.
 #include "megakernel.cuh"
 
 namespace tiles {
 
 const void *megakernel_bf16(int d, int G) {
 #define TILES_KERNEL_CASE(DD, GG) \
-    if (d == DD && G == GG) return (const void *)tiles_megakernel<DD, GG, false>;
+    if (d == DD && G == GG) return (const void *)tiles_megakernel<DD, GG, false, false>;
     TILES_KERNEL_CASE(64, 1) TILES_KERNEL_CASE(64, 2) TILES_KERNEL_CASE(64, 4) TILES_KERNEL_CASE(64, 8)
     TILES_KERNEL_CASE(128, 1) TILES_KERNEL_CASE(128, 2) TILES_KERNEL_CASE(128, 4) TILES_KERNEL_CASE(128, 8)
 #undef TILES_KERNEL_CASE

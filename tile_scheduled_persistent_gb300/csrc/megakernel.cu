@@ -5,28 +5,31 @@
 
 namespace tiles {
 
-const void *megakernel_bf16(int d, int G);  // kernels_bf16.cu
-const void *megakernel_int8(int d, int G);  // kernels_int8.cu
+const void *megakernel_bf16(int d, int G);      // kernels_bf16.cu
+const void *megakernel_bf16_mma(int d, int G);  // kernels_bf16_mma.cu
+const void *megakernel_int8(int d, int G);      // kernels_int8.cu
+const void *megakernel_int8_mma(int d, int G);  // kernels_int8_mma.cu
 
-static const void *megakernel_for(int d, int G, int wbytes) {
-    return wbytes == 1 ? megakernel_int8(d, G) : megakernel_bf16(d, G);
+static const void *megakernel_for(int d, int G, int wbytes, int mma) {
+    if (wbytes == 1) return mma ? megakernel_int8_mma(d, G) : megakernel_int8(d, G);
+    return mma ? megakernel_bf16_mma(d, G) : megakernel_bf16(d, G);
 }
 
 // ------------------------------------------------------------------ launchers
-cudaError_t megakernel_configure(int d, int G, int wbytes, int smem_bytes) {
-    const void *k = megakernel_for(d, G, wbytes);
+cudaError_t megakernel_configure(int d, int G, int wbytes, int mma, int smem_bytes) {
+    const void *k = megakernel_for(d, G, wbytes, mma);
     if (!k) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
-cudaError_t megakernel_occupancy(int d, int G, int wbytes, int smem_bytes, int *blocks_per_sm) {
-    const void *k = megakernel_for(d, G, wbytes);
+cudaError_t megakernel_occupancy(int d, int G, int wbytes, int mma, int smem_bytes, int *blocks_per_sm) {
+    const void *k = megakernel_for(d, G, wbytes, mma);
     if (!k) return cudaErrorInvalidValue;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kThreads, smem_bytes);
 }
 
 cudaError_t megakernel_launch(const KernelParams &p, int n_ctas, int smem_bytes, cudaStream_t st) {
-    const void *k = megakernel_for(p.g.d, p.g.G, p.g.wbytes);
+    const void *k = megakernel_for(p.g.d, p.g.G, p.g.wbytes, p.g.attn_mma);
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {const_cast<KernelParams *>(&p)};
     return cudaLaunchCooperativeKernel(k, dim3(n_ctas), dim3(kThreads), args, (size_t)smem_bytes, st);

@@ -89,6 +89,57 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// One box of a 3-D tiled tensor map (coordinates innermost first) into shared
+// memory, completing on an mbarrier. `map` is the address of a tensor map in
+// kernel-parameter space; the innermost coordinate is a multiple of 64
+// elements (128 bytes), as the tiled copy requires 16-byte alignment there.
+__device__ __forceinline__ void tensor_g2s_3d(void *dst, const TensorMap *map, int x, int y, int z,
+                                              uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Tensor-core helpers of the attention tiles: four 8x8 BF16 matrices from
+// shared memory (lanes 8i..8i+7 give the row addresses of matrix i), plain or
+// transposed, and one m16n8k16 BF16 MMA with FP32 accumulation.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+// c += A B for A 16x16 and B 16x8 when only rows 0..7 of A are nonzero:
+// a0 = (row g, k 2t..2t+1) and a2 = (row g, k 2t+8..2t+9) for lane (g, t) =
+// (lane / 4, lane % 4), b0 = (k 2t..2t+1, n g), b1 = (k 2t+8..2t+9, n g), and
+// the accumulator of row g, columns 2t and 2t+1, in c0, c1 (rows 8..15 of
+// the result are zero and are not kept).
+__device__ __forceinline__ void mma_rows8(float &c0, float &c1, uint32_t a0, uint32_t a2, uint32_t b0,
+                                          uint32_t b1) {
+    asm volatile("{\n\t.reg .f32 z2, z3;\n\t"
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, z2, z3}, {%2, %6, %3, %6}, {%4, %5},"
+        " {%0, %1, %7, %7};\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "r"(a0), "r"(a2), "r"(b0), "r"(b1), "r"(0u), "f"(0.f));
+}
+
+// Byte offset of 16-byte unit u (elements 8u..8u+7) of row r in a chunk region
+// written by the tiled copy with the 128-byte swizzle: boxes of kvb rows x 128
+// bytes one after another (unit u lives in box u / 8), and inside each
+// 1024-byte-aligned group of 8 rows the unit index is XORed with the row
+// index mod 8.
+__device__ __forceinline__ uint32_t swz_off(int kvb, int r, int u) {
+    return ((uint32_t)(u >> 3) * (uint32_t)kvb + (uint32_t)r) * 128u + ((uint32_t)((u & 7) ^ (r & 7)) << 4);
+}
+
 __device__ __forceinline__ void bulk_g2s_nohint(void *dst, const void *src, uint32_t bytes,
                                                 uint64_t *bar) {
     asm volatile(
@@ -455,6 +506,36 @@ struct Producer {
         ++j;
     }
 
+    // The whole block of kv_block positions from q0 (a multiple of kv_block)
+    // of kv head `h`, as swizzled tiles of the K and V tensor maps: one box
+    // per 64 dims, K boxes then V boxes. Rows past max_pos arrive as zeros;
+    // rows from position P on are overwritten or zeroed by the consumer.
+    __device__ void kv_chunk_tensor(int layer, int h, int q0) {
+        if (!owns(j)) {
+            ++j;
+            return;
+        }
+        uint64_t *bar;
+        uint8_t *dst = acquire(&bar);
+        if (!dst) return;
+        // the swizzle pattern assumes 1024-byte aligned boxes; never issue otherwise
+        if (smem_u32(dst) & 1023u) {
+            atomicOr(p.status, kDevBounds);
+            ok = false;
+            return;
+        }
+        const Geom &g = p.g;
+        const int nb = g.d / 64;
+        const uint32_t box = (uint32_t)g.kv_block * 128u;
+        mbar_expect_tx(bar, 2u * (uint32_t)nb * box);
+        const int z = layer * g.nkv + h;
+        for (int i = 0; i < nb; ++i) {
+            tensor_g2s_3d(dst + (size_t)i * box, &p.kv_map[0], 64 * i, q0, z, bar);
+            tensor_g2s_3d(dst + (size_t)(nb + i) * box, &p.kv_map[1], 64 * i, q0, z, bar);
+        }
+        ++j;
+    }
+
     // K/V of positions written by step st-1 may be read only after this CTA's
     // consumers acquired the end of step st-1 (they publish that in step_ready).
     int ready = 0;
@@ -477,6 +558,7 @@ struct Producer {
         return true;
     }
 
+    template <bool MMA>
     __device__ __forceinline__ void run(int cta) {
         const Geom &g = p.g;
         const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
@@ -502,10 +584,14 @@ struct Producer {
                         const int c = (int)(it % (uint32_t)g.kv_splits);
                         int b0, b1;
                         attn_split_blocks(g, P + 1, c, &b0, &b1);
+                        const bool mma = MMA && attn_uses_mma(g, b1 - b0);
                         for (int b = b0; b < b1 && ok; ++b) {
                             int q0 = b * g.kv_block, q1 = q0 + g.kv_block;
                             if (q1 > P) q1 = P;  // position P itself is computed in this step
-                            kv_chunk(t.layer, h, q0, q1);
+                            if (mma)
+                                kv_chunk_tensor(t.layer, h, q0);
+                            else
+                                kv_chunk(t.layer, h, q0, q1);
                         }
                     }
                 }
@@ -1055,6 +1141,7 @@ struct Consumer {
         uint16_t *vnew;    // [d]
         float *prob;       // [warps][32][G]
         float *wstate;     // [warps][G][4 + d]
+        uint16_t *qh;      // [G][d + 8] bf16 q (rows padded: conflict-free MMA fragment loads)
     };
     __device__ AttnSmem attn_smem() const {
         const Geom &g = p.g;
@@ -1069,12 +1156,14 @@ struct Consumer {
         a.prob = reinterpret_cast<float *>(b);
         b += (size_t)kConsumerWarps * 32 * g.G * 4;
         a.wstate = reinterpret_cast<float *>(b);
+        b += (size_t)kConsumerWarps * g.G * (kPartialPad + g.d) * 4;
+        a.qh = reinterpret_cast<uint16_t *>(b);
         return a;
     }
 
     // q heads of kv head h (and k, v of head h): optional RMSNorm over the head,
     // RoPE at position P, rounding to bf16. One warp per head.
-    template <int D>
+    template <int D, bool MMA>
     __device__ void prep_qkv(int h, const AttnSmem &a) {
         const Geom &g = p.g;
         const LayerPtrs &lw = p.layers[cur_layer];
@@ -1130,7 +1219,11 @@ struct Consumer {
             }
             if (is_q) {
 #pragma unroll
-                for (int e = 0; e < E; ++e) a.q[hh * D + lane + 32 * e] = round_bf(v[e]);
+                for (int e = 0; e < E; ++e) {
+                    const uint16_t qb = f2bf(v[e]);
+                    a.q[hh * D + lane + 32 * e] = bf2f(qb);
+                    if (MMA) a.qh[hh * (D + 8) + lane + 32 * e] = qb;  // tensor-core form
+                }
             } else {
 #pragma unroll
                 for (int e = 0; e < E; ++e) a.knew[lane + 32 * e] = f2bf(v[e]);
@@ -1140,81 +1233,94 @@ struct Consumer {
 
     int cur_layer = 0;
 
-    // one chunk of positions [q0, q0 + npos) for the G q heads of one kv head
+    // One chunk of positions [q0, q0 + npos) for the G q heads of one kv head,
+    // on the tensor cores (the chunk arrived as swizzled K and V tiles). The
+    // q heads are rows 0..G-1 of the m16n8k16 A operand (rows G..15 zero);
+    // lane (g, t) = (lane / 4, lane % 4) holds row g. Per round of 2048 / D
+    // positions (few enough registers that the rest of the kernel's state
+    // stays mostly in registers):
+    //   s = q K^T (FP32, exact BF16 products), masked past npos, times d^-1/2;
+    //   online softmax per row: m' = max(m, max s), c = e^(m - m'),
+    //   p = e^(s - m'), l' = c l + sum p, o' = c o;
+    //   o' += p V, with p split into a BF16 high part and a BF16 remainder
+    //   (two MMAs), so the weights keep ~16 bits.
+    // o[j] holds row g's accumulators of output dims 8j + 2t and 8j + 2t + 1.
     template <int D, int G>
-    __device__ void attn_chunk(const uint8_t *slot, int npos, const AttnSmem &a, float (&m)[G],
-                               float (&l)[G], float (&o)[G][D / 32]) {
-        constexpr int NC = D / 8;   // 16-byte columns per row
-        constexpr int DPL = D / 32; // dims per lane in the PV product
-        const Geom &g = p.g;
-        const uint8_t *Kb = slot;
-        const uint8_t *Vb = slot + (size_t)g.kv_block * D * 2;
-        float *prob = a.prob + (size_t)warp * 32 * G;
-        for (int t0 = 0; t0 < npos; t0 += 32) {
-            const int t = t0 + lane;
-            const bool valid = t < npos;
-            float sc[G];
+    __device__ __forceinline__ void attn_chunk_mma(const uint8_t *slot, int npos, const uint32_t *qrow, bool qrow_ok,
+                                                   float &m, float &l, float (&o)[D / 8][2]) {
+        constexpr int SUB = 2048 / D;  // positions per round
+        constexpr int NT = SUB / 8;    // score n-tiles of 8 positions
+        constexpr int KS = D / 16;     // k-steps of the scores
+        constexpr int PS = SUB / 16;   // k-steps of p V
+        constexpr int NJ = D / 8;      // output n-tiles of 8 dims
+        const int kvb = p.g.kv_block;
+        const uint32_t kb = smem_u32(slot), vb = kb + (uint32_t)kvb * D * 2;
+        const int t4 = lane & 3;
+        const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix and row this lane points at
+        for (int p0 = 0; p0 < npos; p0 += SUB) {
+            float sc[NT][2];
 #pragma unroll
-            for (int i = 0; i < G; ++i) sc[i] = 0.f;
-            if (valid) {
-                const uint4 *krow = reinterpret_cast<const uint4 *>(Kb + (size_t)t * D * 2);
+            for (int jn = 0; jn < NT; ++jn) {
+                float c0 = 0.f, c1 = 0.f;
 #pragma unroll
-                for (int jj = 0; jj < NC; ++jj) {
-                    const int col = (jj + lane) & (NC - 1);  // rotated: no bank conflicts
-                    float kf[8];
-                    unpack8(krow[col], kf);
-#pragma unroll
-                    for (int i = 0; i < G; ++i) {
-                        const float4 qa = reinterpret_cast<const float4 *>(a.q + i * D + col * 8)[0];
-                        const float4 qb = reinterpret_cast<const float4 *>(a.q + i * D + col * 8)[1];
-                        float acc = sc[i];
-                        acc = fmaf(kf[0], qa.x, acc); acc = fmaf(kf[1], qa.y, acc);
-                        acc = fmaf(kf[2], qa.z, acc); acc = fmaf(kf[3], qa.w, acc);
-                        acc = fmaf(kf[4], qb.x, acc); acc = fmaf(kf[5], qb.y, acc);
-                        acc = fmaf(kf[6], qb.z, acc); acc = fmaf(kf[7], qb.w, acc);
-                        sc[i] = acc;
-                    }
+                for (int ks = 0; ks < KS; ks += 2) {
+                    // units 2ks .. 2ks + 3 of positions p0 + 8jn ..: b0, b1 of k-steps ks and ks + 1
+                    uint32_t b[4];
+                    ldsm_x4(kb + swz_off(kvb, p0 + 8 * jn + ri, 2 * ks + mi), b);
+                    // A fragments of q from shared memory (rows >= G are zero)
+                    const uint32_t qa0 = qrow_ok ? qrow[8 * ks] : 0u, qa1 = qrow_ok ? qrow[8 * ks + 4] : 0u;
+                    const uint32_t qb0 = qrow_ok ? qrow[8 * ks + 8] : 0u, qb1 = qrow_ok ? qrow[8 * ks + 12] : 0u;
+                    mma_rows8(c0, c1, qa0, qa1, b[0], b[1]);
+                    mma_rows8(c0, c1, qb0, qb1, b[2], b[3]);
                 }
+                sc[jn][0] = c0;
+                sc[jn][1] = c1;
             }
+            float mx = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < G; ++i) {
-                const float si = valid ? sc[i] * p.attn_scale : -INFINITY;
-                const float bm = warp_max(si);
-                const float mn = fmaxf(m[i], bm);
-                const float corr = expf(m[i] - mn);
-                const float pi = valid ? expf(si - mn) : 0.f;
-                const float ps = warp_sum(pi);
-                l[i] = fmaf(l[i], corr, ps);
-                m[i] = mn;
+            for (int jn = 0; jn < NT; ++jn)
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) o[i][e] *= corr;
-                prob[lane * G + i] = pi;
-            }
-            __syncwarp();
-            const int nv = npos - t0 < 32 ? npos - t0 : 32;
-            for (int tt = 0; tt < nv; ++tt) {
-                float pv[G];
-#pragma unroll
-                for (int i = 0; i < G; ++i) pv[i] = prob[tt * G + i];
-                const uint8_t *vrow = Vb + (size_t)(t0 + tt) * D * 2;
-                float vf[DPL];
-                if (DPL == 2) {
-                    const uint32_t w = reinterpret_cast<const uint32_t *>(vrow)[lane];
-                    vf[0] = bf_lo(w);
-                    vf[1] = bf_hi(w);
-                } else {
-                    const uint2 w = reinterpret_cast<const uint2 *>(vrow)[lane];
-                    vf[0] = bf_lo(w.x);
-                    vf[1] = bf_hi(w.x);
-                    vf[DPL > 2 ? 2 : 0] = bf_lo(w.y);
-                    vf[DPL > 3 ? 3 : 1] = bf_hi(w.y);
+                for (int e = 0; e < 2; ++e) {
+                    const int pos = p0 + 8 * jn + 2 * t4 + e;
+                    sc[jn][e] = pos < npos ? sc[jn][e] * p.attn_scale : -INFINITY;
+                    mx = fmaxf(mx, sc[jn][e]);
                 }
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+            const float mn = fmaxf(m, mx);
+            const float corr = expf(m - mn);
+            float ls = 0.f;
+            uint32_t ahi[PS][2], alo[PS][2];
 #pragma unroll
-                for (int i = 0; i < G; ++i)
-#pragma unroll
-                    for (int e = 0; e < DPL; ++e) o[i][e] = fmaf(pv[i], vf[e], o[i][e]);
+            for (int jn = 0; jn < NT; ++jn) {
+                const float p0f = expf(sc[jn][0] - mn), p1f = expf(sc[jn][1] - mn);
+                ls += p0f + p1f;
+                const uint16_t h0 = f2bf(p0f), h1 = f2bf(p1f);
+                const uint16_t r0 = f2bf(__fsub_rn(p0f, bf2f(h0))), r1 = f2bf(__fsub_rn(p1f, bf2f(h1)));
+                ahi[jn / 2][jn & 1] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+                alo[jn / 2][jn & 1] = (uint32_t)r0 | ((uint32_t)r1 << 16);
             }
-            __syncwarp();
+            ls += __shfl_xor_sync(0xFFFFFFFFu, ls, 1);
+            ls += __shfl_xor_sync(0xFFFFFFFFu, ls, 2);
+            l = fmaf(l, corr, ls);
+            m = mn;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                o[j][0] *= corr;
+                o[j][1] *= corr;
+            }
+#pragma unroll
+            for (int ps = 0; ps < PS; ++ps)
+#pragma unroll
+                for (int j = 0; j < NJ; j += 2) {
+                    // positions p0 + 16ps (+8), dims 8j and 8j + 8, transposed: b0, b1 of n-tiles j, j + 1
+                    uint32_t b[4];
+                    ldsm_x4_t(vb + swz_off(kvb, p0 + 16 * ps + 8 * (mi & 1) + ri, j + (mi >> 1)), b);
+                    mma_rows8(o[j][0], o[j][1], ahi[ps][0], ahi[ps][1], b[0], b[1]);
+                    mma_rows8(o[j][0], o[j][1], alo[ps][0], alo[ps][1], b[0], b[1]);
+                    mma_rows8(o[j + 1][0], o[j + 1][1], ahi[ps][0], ahi[ps][1], b[2], b[3]);
+                    mma_rows8(o[j + 1][0], o[j + 1][1], alo[ps][0], alo[ps][1], b[2], b[3]);
+                }
         }
     }
 
@@ -1330,7 +1436,30 @@ struct Consumer {
         __syncwarp();
     }
 
-    template <int D, int G>
+    // The swizzled form: row r = P - q0 of the chunk gets the new K and V, and
+    // the V rows after it (stale cache memory, which may hold any bits) become
+    // zeros, so the masked positions add exact zeros to p V.
+    template <int D>
+    __device__ __forceinline__ void place_new_kv_swz(uint8_t *slot, int q0) {
+        const int kvb = p.g.kv_block;
+        const AttnSmem a = attn_smem();
+        const int r = P - q0;
+        uint8_t *vs = slot + (size_t)kvb * D * 2;
+        for (int e = lane; e < D; e += 32) {
+            const uint32_t off = swz_off(kvb, r, e >> 3) + (uint32_t)(e & 7) * 2u;
+            *reinterpret_cast<uint16_t *>(slot + off) = a.knew[e];
+            *reinterpret_cast<uint16_t *>(vs + off) = a.vnew[e];
+        }
+        const int nz = (kvb - r - 1) * (D / 8);  // 16-byte units of the rows after r
+        for (int i = lane; i < nz; i += 32) {
+            const int rr = r + 1 + i / (D / 8), u = i % (D / 8);
+            *reinterpret_cast<uint4 *>(vs + swz_off(kvb, rr, u)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+    template <int D, int G, bool MMA>
     __device__ void attn_task(const tiles_task &t) {
         const Geom &g = p.g;
         const AttnSmem a = attn_smem();
@@ -1341,7 +1470,7 @@ struct Consumer {
             const int c = (int)(it % (uint32_t)g.kv_splits);
             if (h != prepared) {
                 consumer_sync();  // previous item finished reading q / knew / vnew
-                prep_qkv<D>(h, a);
+                prep_qkv<D, MMA>(h, a);
                 consumer_sync();
                 prepared = h;
             }
@@ -1365,7 +1494,7 @@ struct Consumer {
                 for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
             }
             const uint32_t nch = (uint32_t)(b1 - b0);
-            if (nch < (uint32_t)kConsumerWarps) {
+            if (!(MMA && attn_uses_mma(g, (int)nch))) {
                 // few chunks: every warp works on every chunk (one q head, some sub-blocks)
                 const int hi = warp % G, sb0 = warp / G, sbs = kConsumerWarps / G;
                 const int lp = attn_lanes_per_pos(sbs);
@@ -1396,8 +1525,26 @@ struct Consumer {
 #pragma unroll
                     for (int e = 0; e < DPL; ++e) o[i][e] = i == hi ? o1[e] : 0.f;
                 }
+                // per-warp states -> shared memory
+                float *ws = a.wstate + (size_t)warp * G * (kPartialPad + D);
+#pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    if (lane == 0) {
+                        ws[i * (kPartialPad + D) + 0] = m[i];
+                        ws[i * (kPartialPad + D) + 1] = l[i];
+                    }
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e)
+                        ws[i * (kPartialPad + D) + kPartialPad + lane * DPL + e] = o[i][e];
+                }
             } else {
-                // many chunks: each chunk goes to its slot's owner warp, all q heads
+                // many chunks: each chunk goes to its slot's owner warp, all q heads, tensor cores
+                const int g8 = lane >> 2, t4 = lane & 3;
+                // q head g8 as BF16 pairs (dims 2t4 + 16ks (+8) in word t4 + 8ks (+4))
+                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.qh + (size_t)(g8 < G ? g8 : 0) * (D + 8)) + t4;
+                float mm = -INFINITY, ll = 0.f, oo[D / 8][2];
+#pragma unroll
+                for (int jd = 0; jd < D / 8; ++jd) oo[jd][0] = oo[jd][1] = 0.f;
                 for (uint32_t k = 0; k < nch; ++k) {
                     const uint32_t jj = j + k;
                     if (!mine(jj)) continue;
@@ -1406,23 +1553,27 @@ struct Consumer {
                     const int q0 = (b0 + (int)k) * g.kv_block;
                     int q1 = q0 + g.kv_block;
                     if (q1 > P + 1) q1 = P + 1;
-                    if (q0 <= P && P < q1) place_new_kv<D>(slot, q0, a);
-                    attn_chunk<D, G>(slot, q1 - q0, a, m, l, o);
+                    if (q0 <= P && P < q1) place_new_kv_swz<D>(slot, q0);
+                    attn_chunk_mma<D, G>(slot, q1 - q0, qrow, g8 < G, mm, ll, oo);
                     release_chunk(jj);
+                }
+                // per-warp states -> shared memory (row g8 = q head g8)
+                float *ws = a.wstate + (size_t)warp * G * (kPartialPad + D);
+                if (g8 < G) {
+                    float *w = ws + (size_t)g8 * (kPartialPad + D);
+                    if (t4 == 0) {
+                        w[0] = mm;
+                        w[1] = ll;
+                    }
+#pragma unroll
+                    for (int jd = 0; jd < D / 8; ++jd) {
+                        w[kPartialPad + 8 * jd + 2 * t4] = oo[jd][0];
+                        w[kPartialPad + 8 * jd + 2 * t4 + 1] = oo[jd][1];
+                    }
                 }
             }
             j += nch;
-            // per-warp states -> shared memory -> one partial for (q heads, split c)
-            float *ws = a.wstate + (size_t)warp * G * (kPartialPad + D);
-#pragma unroll
-            for (int i = 0; i < G; ++i) {
-                if (lane == 0) {
-                    ws[i * (kPartialPad + D) + 0] = m[i];
-                    ws[i * (kPartialPad + D) + 1] = l[i];
-                }
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) ws[i * (kPartialPad + D) + kPartialPad + lane * DPL + e] = o[i][e];
-            }
+            // per-warp states -> one partial for (q heads, split c)
             consumer_sync();
             for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
                 const int i = idx / D, dd = idx % D;
@@ -1512,7 +1663,7 @@ struct Consumer {
     // ---------------------------------------------------------- main loop
     // D (head_dim), G (q heads per KV head) and the weight format (Q8: INT8
     // codes) are compile-time: each kernel instance carries only its own code.
-    template <int D, int G, bool Q8>
+    template <int D, int G, bool Q8, bool MMA>
     __device__ __forceinline__ void run(int cta) {
         const Geom &g = p.g;
         const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
@@ -1555,7 +1706,7 @@ struct Consumer {
                         gemv_task<1, Q8>(t);
                         break;
                     case TILES_OP_ATTN:
-                        attn_task<D, G>(t);
+                        attn_task<D, G, MMA>(t);
                         break;
                     case TILES_OP_OPROJ:
                         gather_tagged(p.ow, g.qd, tag(t.layer, kTagO));
@@ -1609,7 +1760,7 @@ struct Consumer {
     }
 };
 
-template <int D, int G, bool Q8>
+template <int D, int G, bool Q8, bool MMA>
 __global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_constant__ KernelParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Smem s = smem_layout(smem_raw, p);
@@ -1636,12 +1787,12 @@ __global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_con
     if (tid >= kConsumerWarps * 32) {
         if ((tid & 31) == 0) {
             Producer prod(p, s, (tid >> 5) - kConsumerWarps);
-            prod.run(blockIdx.x);
+            prod.template run<MMA>(blockIdx.x);
         }
         return;
     }
     Consumer cons(p, s, tid);
-    cons.template run<D, G, Q8>(blockIdx.x);
+    cons.template run<D, G, Q8, MMA>(blockIdx.x);
 }
 
 }  // namespace tiles

@@ -36,7 +36,7 @@ static int round_up(int v, int m) { return (v + m - 1) / m * m; }
 // per-warp probabilities [32][G] f32, per-warp states [G][4 + d] f32.
 static int attn_vec_bytes(int G, int d) {
     return G * d * 4 + 2 * d * 2 + kConsumerWarps * 32 * G * 4 +
-           kConsumerWarps * G * (kPartialPad + d) * 4;
+           kConsumerWarps * G * (kPartialPad + d) * 4 + G * (d + 8) * 2;
 }
 
 tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o, int n_ctas,
@@ -126,6 +126,7 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     G_.rpc_lm = rpc(G_.H, 1, 0);
     int kb = slot / (2 * G_.d * 2);
     kb = kb >= 32 ? kb / 32 * 32 : kb;
+    kb = std::min(kb, 256);  // a chunk's positions are one TMA box (at most 256 rows)
     if (kb < 1) return fail(TILES_ERR_UNSUPPORTED, "slot too small for one KV position");
     G_.kv_block = kb;
     int nb_max = ceil_div(G_.max_pos, kb);
@@ -136,6 +137,11 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     int splits = o.kv_splits > 0 ? o.kv_splits : std::max(1, std::min(nb_max, n_ctas / G_.nkv));
     if (splits < 1 || splits > 256) return fail(TILES_ERR_INVALID_ARG, "kv_splits");
     G_.kv_splits = splits;
+    // the tensor-core attention path (and its kernel instance) only where a
+    // split can hold kConsumerWarps chunks: short-context plans run kernels
+    // without it, whose registers it would otherwise crowd (measured 2.5 %
+    // on the Llama-1B shape at 1,023 positions)
+    G_.attn_mma = (ceil_div(nb_max, splits) >= kConsumerWarps && kb % (2048 / G_.d) == 0) ? 1 : 0;
 
     // an attention tile merges a 1/S slice of its KV head's G d outputs,
     // staging (m, l, o) of every (output, split) pair: 3 floats each
@@ -403,7 +409,7 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
         if (r < 1 || (long long)r * op_in_dim(g, op) * g.wbytes * op_mats(op) > g.slot_bytes)
             return fail("rows per chunk do not fit a slot");
     }
-    if (g.kv_block < 1 || 2LL * g.kv_block * g.d * 2 > g.slot_bytes) return fail("kv block");
+    if (g.kv_block < 1 || g.kv_block > 256 || 2LL * g.kv_block * g.d * 2 > g.slot_bytes) return fail("kv block");
     if (g.smem_bytes > kSmemLimit) return fail("shared memory");
     if (s.n_counters < 1 || s.n_counters > 0xFFFE) return fail("counter count");
 

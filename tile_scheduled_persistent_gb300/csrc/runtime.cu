@@ -4,6 +4,8 @@
 // "Tiles: Scheduling LLM Decoding as a Graph of Tiles", "What the code
 // contains": the runtime re-validates a plan, checks it was made for this
 // worker binary and GPU, and runs up to 64 tokens per cooperative launch.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -16,8 +18,8 @@
 #include "tiles_internal.h"
 
 namespace tiles {
-cudaError_t megakernel_configure(int d, int G, int wbytes, int smem_bytes);
-cudaError_t megakernel_occupancy(int d, int G, int wbytes, int smem_bytes, int *blocks_per_sm);
+cudaError_t megakernel_configure(int d, int G, int wbytes, int mma, int smem_bytes);
+cudaError_t megakernel_occupancy(int d, int G, int wbytes, int mma, int smem_bytes, int *blocks_per_sm);
 cudaError_t quantize_rows_launch(const void *src, int rows, int cols, void *dst, float *scale,
                                  int row_step, int row0, cudaStream_t st);
 cudaError_t megakernel_launch(const KernelParams &p, int n_ctas, int smem_bytes, cudaStream_t st);
@@ -27,6 +29,9 @@ cudaError_t barrier_launch(uint32_t *ctr, int rounds, unsigned long long *elapse
 }  // namespace tiles
 
 using namespace tiles;
+
+static_assert(sizeof(CUtensorMap) == sizeof(TensorMap) && alignof(CUtensorMap) <= alignof(TensorMap),
+              "TensorMap must hold a CUtensorMap");
 
 struct tiles_plan_s {
     tiles_schedule_s sched;
@@ -161,9 +166,9 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
     const Geom &g = plan->sched.geom;
 
     // the worker must fit one CTA per SM at this shared-memory size (co-residency)
-    e = megakernel_configure(g.d, g.G, g.wbytes, g.smem_bytes);
+    e = megakernel_configure(g.d, g.G, g.wbytes, g.attn_mma, g.smem_bytes);
     int occ = 0;
-    if (e == cudaSuccess) e = megakernel_occupancy(g.d, g.G, g.wbytes, g.smem_bytes, &occ);
+    if (e == cudaSuccess) e = megakernel_occupancy(g.d, g.G, g.wbytes, g.attn_mma, g.smem_bytes, &occ);
     if (e != cudaSuccess || occ < 1) {
         delete plan;
         return e != cudaSuccess ? TILES_ERR_CUDA : TILES_ERR_UNSUPPORTED;
@@ -384,6 +389,44 @@ static tiles_status_t check_device(tiles_plan_t plan) {
     return TILES_OK;
 }
 
+// cuTensorMapEncodeTiled, through the runtime's driver entry point (the
+// library links only the static CUDA runtime)
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// TMA descriptors of this call's K and V caches: [L n_kv][max_pos][d] BF16,
+// boxes of kv_block positions x 64 dims (a 128-dim head takes two boxes per
+// chunk), 128-byte swizzle so the tensor-core fragment loads of the attention
+// tiles are free of bank conflicts; positions past max_pos read as zero.
+static tiles_status_t encode_kv_maps(const Geom &g, void *k_cache, void *v_cache, KernelParams *p) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return TILES_ERR_CUDA;
+    const cuuint64_t dims[3] = {(cuuint64_t)g.d, (cuuint64_t)g.max_pos, (cuuint64_t)g.L * (cuuint64_t)g.nkv};
+    const cuuint64_t strides[2] = {(cuuint64_t)g.d * 2, (cuuint64_t)g.max_pos * (cuuint64_t)g.d * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)g.kv_block, 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    void *ptrs[2] = {k_cache, v_cache};
+    for (int i = 0; i < 2; ++i) {
+        CUtensorMap m;
+        if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptrs[i], dims, strides, box, elem_strides,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TILES_ERR_CUDA;
+        std::memcpy(&p->kv_map[i], &m, sizeof m);
+    }
+    return TILES_OK;
+}
+
 tiles_status_t tiles_decode(tiles_plan_t plan, void *k_cache, void *v_cache, const int32_t *prompt,
                             int32_t n_prompt, int32_t start_pos, int32_t n_new, void *stream,
                             int32_t *out_tokens, float *out_logits) {
@@ -401,6 +444,7 @@ tiles_status_t tiles_decode(tiles_plan_t plan, void *k_cache, void *v_cache, con
     KernelParams p = plan->base;
     p.k_cache = reinterpret_cast<uint16_t *>(k_cache);
     p.v_cache = reinterpret_cast<uint16_t *>(v_cache);
+    if ((st = encode_kv_maps(g, k_cache, v_cache, &p)) != TILES_OK) return st;
     p.prompt = prompt;
     p.n_prompt = n_prompt;
     p.out_tokens = out_tokens;
@@ -581,6 +625,7 @@ extern "C" tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache,
     place_sync_block(plan->sched, base, &p);
     p.k_cache = reinterpret_cast<uint16_t *>(k_cache);
     p.v_cache = reinterpret_cast<uint16_t *>(v_cache);
+    if ((st = encode_kv_maps(g, k_cache, v_cache, &p)) != TILES_OK) return st;
     p.prompt = prompt;
     p.n_prompt = n_prompt;
     p.out_tokens = out_tokens;

@@ -43,6 +43,8 @@ struct Geom {
     int vec_bytes;  // shared-memory region for the input vector / attention scratch
     int res_off;    // in the vec region: residual rows of an O-proj / down tile
     int smem_bytes;
+    int attn_mma;   // 1: some attention split can reach kConsumerWarps chunks, and the
+                    // kernel instance carries the tensor-core attention path
 };
 
 TILES_HD int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -163,6 +165,12 @@ struct LayerPtrs {
     const float *s_qkv, *s_o, *s_gu, *s_down;
 };
 
+// An opaque CUDA tensor map (CUtensorMap: 128 bytes, 128-byte aligned),
+// declared here so the host planner compiles without the driver headers.
+struct alignas(128) TensorMap {
+    uint64_t opaque[16];
+};
+
 struct KernelParams {
     Geom g;
     float eps, attn_scale;
@@ -200,10 +208,25 @@ struct KernelParams {
     // optional per-task timeline: [cta][step < trace_steps][task][kTraceWords]
     unsigned long long *trace;
     int trace_steps, trace_tasks;
+    // TMA descriptors of the K and V caches as [L * n_kv][max_pos][d] BF16,
+    // boxes of kv_block positions x 64 dims, 128-byte swizzle (written per
+    // decode call; the kernel takes their addresses in parameter space)
+    TensorMap kv_map[2];
 };
 
 // trace record words
 constexpr int kTraceWords = 8;
+
+// When an attention item streams at least this many KV chunks (and the plan's
+// kernel instance carries the path), every chunk goes to its slot's owner
+// warp, arrives as a 128-byte-swizzled TMA tile and is reduced on the tensor
+// cores; otherwise all warps share each chunk (linear copies). Producer and
+// consumers decide with the same rule.
+// (The tensor-core form takes 2048 / d positions per round: 32 at d = 64,
+// 16 at d = 128, so kv_block must be a multiple of that.)
+TILES_HD bool attn_uses_mma(const Geom &g, int n_chunks) {
+    return g.attn_mma && n_chunks >= kConsumerWarps && g.kv_block % (2048 / g.d) == 0;
+}
 enum { kTrWaitStart = 0, kTrWaitEnd, kTrTaskEnd, kTrProdFirst, kTrProdLast, kTrProdStall,
        kTrOpInfo };
 
