@@ -91,6 +91,26 @@ def test_int8_variants_match_int8_oracle(tsp, name):
     plan.close()
 
 
+# long contexts: the kernel instances with the tensor-core attention path
+MMA = {
+    "d64_g2": replace(S.CONFIGS["tiny"], name="m1", start_pos=955, n_prompt=2, n_new=24, max_pos=1000),
+    "d128_g8_qknorm": replace(VARIANTS["d128_g8_qknorm"], name="m3", start_pos=490, n_prompt=2,
+                              n_new=24, max_pos=520),
+}
+
+
+@pytest.mark.parametrize("name", list(MMA))
+def test_int8_with_tensor_core_attention_matches_int8_oracle(tsp, name):
+    cfg = MMA[name]
+    w, k, v, prompt = inputs(cfg)
+    prompt = prompt[: cfg.n_prompt]
+    ref = _oracle_q8(cfg, w, oracle.quantize_model(w), k, v, prompt, cfg.start_pos, cfg.n_new)
+    plan = _plan(tsp, cfg, w, kv_splits=2)
+    toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, cfg.n_new)
+    assert_parity(toks, logits, ref, name + " int8, tensor-core attention")
+    plan.close()
+
+
 def test_int8_rejects_rows_not_a_multiple_of_16(tsp):
     cfg = replace(S.CONFIGS["tiny"], hidden=264, ffn=776, vocab=1000)
     d = tsp.ModelDesc.from_config(cfg)
@@ -99,7 +119,7 @@ def test_int8_rejects_rows_not_a_multiple_of_16(tsp):
     assert e.value.status == -2
 
 
-@pytest.mark.parametrize("name", ["llama1b", "qwen3_0_6b"])
+@pytest.mark.parametrize("name", ["llama1b", "qwen3_0_6b", "llama1b_long"])
 def test_int8_full_width_one_layer_slice_strict_tolerance(tsp, name):
     cfg = replace(S.CONFIGS[name], n_layers=1)
     n_new = 8
