@@ -228,10 +228,16 @@ const char *tiles_status_string(tiles_status_t status);
  * Errors: INVALID_ARG. */
 tiles_status_t tiles_plan_set_trace(tiles_plan_t plan, void *trace, int32_t steps);
 
-/* Facts about a built plan, for reports and tests. */
+/* Facts about a built plan (or a host-only schedule), for reports and tests. */
 typedef struct {
     int32_t n_ctas, threads_per_cta, smem_bytes, slot_bytes, ring_slots, kv_splits;
     int32_t scheduler, n_tasks, n_counters, phases_per_step, max_tasks_per_cta;
+    int32_t kv_block;           /* positions per KV chunk                                    */
+    int32_t attn_tensor_cores;  /* 1: attention splits of >= 8 chunks run on the tensor
+                                   cores (swizzled TMA tiles, m16n8k16 MMAs)                 */
+    int32_t rows_per_chunk[5];  /* GEMV rows per ring chunk: Q/K/V, O, gate/up (pairs),
+                                   down, LM head                                             */
+    int32_t weight_format;      /* TILES_WEIGHTS_BF16 or TILES_WEIGHTS_INT8                   */
     int64_t weight_bytes_per_token;     /* every weight byte the kernel streams per step */
     int64_t max_cta_bytes, min_cta_bytes; /* per-step streamed weight bytes, busiest/idlest CTA */
 } tiles_plan_info;
@@ -288,6 +294,10 @@ tiles_status_t tiles_schedule_tasks(tiles_schedule_t sched, tiles_task **tasks,
 
 /* Per-CTA weight+KV bytes streamed in one step at context position `pos`. */
 tiles_status_t tiles_schedule_cta_bytes(tiles_schedule_t sched, int32_t pos, int64_t *bytes);
+
+/* The facts tiles_plan_get_info reports, for a schedule built on the host
+ * (no GPU involved). Errors: INVALID_ARG on a null argument. */
+tiles_status_t tiles_schedule_get_info(tiles_schedule_t sched, tiles_plan_info *info);
 
 void tiles_schedule_destroy(tiles_schedule_t sched);
 

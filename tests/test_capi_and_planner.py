@@ -201,3 +201,55 @@ def test_waves_have_one_arrival_per_cta_and_phase():
             key = (c, t.phase_kind, t.layer)
             per[key] = per.get(key, 0) + (t.signal_ctr != tsp.NO_COUNTER)
     assert set(per.values()) == {1}
+
+
+# ------------------------------------------------------------------ chunk geometry
+def _ceil(a, b):
+    return -(-a // b)
+
+
+def test_int8_layer_chunks_give_every_consumer_warp_work():
+    """INT8 layer GEMVs: rows per chunk = min(what fills a slot (at most 8),
+    ceil(ceil(rows / CTAs) / 8)); the LM head and BF16 keep full chunks."""
+    for name in ("llama1b", "qwen3_0_6b", "qwen3_4b"):
+        cfg = S.CONFIGS[name]
+        H, F, qkv = cfg.hidden, cfg.ffn, cfg.q_dim + 2 * cfg.kv_dim
+        bi, qi = _sched(name).info(), _sched(name, weight_format=tsp.WEIGHTS_INT8).info()
+        b, q = bi["rows_per_chunk"], qi["rows_per_chunk"]
+        # a slot holds 16 KB or the longest row (Qwen3-4B BF16: one 9,728-wide down row)
+        slot = {2: bi["slot_bytes"], 1: qi["slot_bytes"]}
+        full = lambda width, mats, wb: min(8, slot[wb] // (width * wb * mats))
+        assert b == {"qkv": full(H, 1, 2), "o": full(cfg.q_dim, 1, 2), "gateup": full(H, 2, 2),
+                     "down": full(F, 1, 2), "lm": full(H, 1, 2)}
+        cap = lambda rows: _ceil(_ceil(rows, 152), 8)
+        assert q == {"qkv": max(1, min(full(H, 1, 1), cap(qkv))),
+                     "o": max(1, min(full(cfg.q_dim, 1, 1), cap(H))),
+                     "gateup": max(1, min(full(H, 2, 1), cap(F))),
+                     "down": max(1, min(full(F, 1, 1), cap(H))),
+                     "lm": full(H, 1, 1)}
+    # worked by hand for the Llama-1B shape: 3072 Q/K/V rows -> 21 per CTA -> 3 per chunk
+    assert _sched("llama1b", weight_format=tsp.WEIGHTS_INT8).info()["rows_per_chunk"] == \
+        {"qkv": 3, "o": 2, "gateup": 4, "down": 2, "lm": 8}
+
+
+def test_tensor_core_attention_only_where_a_split_can_reach_eight_chunks():
+    """1,088 positions in 64-position blocks over 17 splits: at most 1 chunk per
+    split (no tensor-core path); 32,832 positions over 19 splits: up to 28."""
+    short, long_ = _sched("llama1b").info(), _sched("llama1b_long").info()
+    assert (short["kv_block"], short["kv_splits"], short["attn_tensor_cores"]) == (64, 17, 0)
+    assert (long_["kv_block"], long_["kv_splits"], long_["attn_tensor_cores"]) == (64, 19, 1)
+    # fewer splits turn it on for a short context too: 17 blocks over 2 splits -> 9 chunks
+    assert _sched("llama1b", kv_splits=2).info()["attn_tensor_cores"] == 1
+    assert _sched("llama1b", kv_splits=3).info()["attn_tensor_cores"] == 0      # 6 chunks
+    # head_dim 128: 32-position blocks
+    assert _sched("qwen3_4b").info()["kv_block"] == 32
+
+
+def test_kv_block_is_capped_at_one_tma_box():
+    """A 64 KB slot holds 256 positions of K and V at d = 64; 96 KB would hold
+    384, more than a tensor-map box (256 rows): the chunk stays at 256."""
+    d = tsp.ModelDesc.from_config(S.CONFIGS["tiny"])
+    for slot, want in ((65536, 256), (98304, 256), (32768, 128)):
+        s = tsp.Schedule(d, 16, tsp.make_opts(slot_bytes=slot, ring_slots=2))
+        assert s.info()["kv_block"] == want
+        assert s.validate()[0] == 0

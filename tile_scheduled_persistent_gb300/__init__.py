@@ -75,12 +75,15 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("n_ctas", "threads_per_cta", "smem_bytes", "slot_bytes", "ring_slots",
                  "kv_splits", "scheduler", "n_tasks", "n_counters", "phases_per_step",
-                 "max_tasks_per_cta")] + \
+                 "max_tasks_per_cta", "kv_block", "attn_tensor_cores")] + \
+               [("rows_per_chunk", ctypes.c_int32 * 5), ("weight_format", ctypes.c_int32)] + \
                [(n, ctypes.c_int64) for n in
                 ("weight_bytes_per_token", "max_cta_bytes", "min_cta_bytes")]
 
     def as_dict(self):
-        return {n: getattr(self, n) for n, _ in self._fields_}
+        d = {n: getattr(self, n) for n, _ in self._fields_}
+        d["rows_per_chunk"] = dict(zip(("qkv", "o", "gateup", "down", "lm"), self.rows_per_chunk))
+        return d
 
 
 class Task(ctypes.Structure):
@@ -97,7 +100,7 @@ EXPORTS = ("tiles_plan_create", "tiles_plan_destroy", "tiles_decode", "tiles_dec
            "tiles_status", "tiles_status_string", "tiles_plan_get_info", "tiles_schedule_build",
            "tiles_schedule_validate", "tiles_schedule_tasks", "tiles_schedule_cta_bytes",
            "tiles_schedule_destroy", "tiles_copy_bw", "tiles_barrier_cost", "tiles_plan_set_trace",
-           "tiles_decode_noalloc", "tiles_quantize_rows_int8")
+           "tiles_decode_noalloc", "tiles_quantize_rows_int8", "tiles_schedule_get_info")
 
 _lib_handle = None
 
@@ -141,6 +144,8 @@ def _lib():
         L.tiles_schedule_tasks.restype = st
         L.tiles_schedule_cta_bytes.argtypes = [vp, i32, ctypes.POINTER(i64)]
         L.tiles_schedule_cta_bytes.restype = st
+        L.tiles_schedule_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+        L.tiles_schedule_get_info.restype = st
         L.tiles_schedule_destroy.argtypes = [vp]
         L.tiles_schedule_destroy.restype = None
         L.tiles_copy_bw.argtypes = [vp, vp, ctypes.c_size_t, i32, vp]
@@ -199,6 +204,12 @@ class Schedule:
                                            ctypes.byref(off), ctypes.byref(nc)), "tiles_schedule_tasks")
         arr = ctypes.cast(tp, ctypes.POINTER(Task * n.value)).contents
         return arr, [off[i] for i in range(nc.value + 1)]
+
+    def info(self) -> dict:
+        """The facts a plan made from this schedule would report (no GPU)."""
+        inf = PlanInfo()
+        _check(_lib().tiles_schedule_get_info(self._h, ctypes.byref(inf)), "tiles_schedule_get_info")
+        return inf.as_dict()
 
     def cta_bytes(self, pos: int):
         n = self.tasks()[1]

@@ -600,6 +600,47 @@ tiles_status_t tiles_schedule_cta_bytes(tiles_schedule_t sched, int32_t pos, int
     return TILES_OK;
 }
 
+tiles_status_t tiles_schedule_get_info(tiles_schedule_t sched, tiles_plan_info *info) {
+    if (!sched || !info) return TILES_ERR_INVALID_ARG;
+    const tiles_schedule_s &s = *sched;
+    const Geom &g = s.geom;
+    std::memset(info, 0, sizeof(*info));
+    info->n_ctas = s.n_ctas;
+    info->threads_per_cta = kThreads;
+    info->smem_bytes = g.smem_bytes;
+    info->slot_bytes = g.slot_bytes;
+    info->ring_slots = g.ring_slots;
+    info->kv_splits = g.kv_splits;
+    info->scheduler = s.scheduler;
+    info->n_tasks = (int32_t)s.tasks.size();
+    info->n_counters = s.n_counters;
+    info->phases_per_step = phases_per_step(g);
+    int mt = 0;
+    for (int c = 0; c < s.n_ctas; ++c) mt = std::max(mt, s.offsets[c + 1] - s.offsets[c]);
+    info->max_tasks_per_cta = mt;
+    info->kv_block = g.kv_block;
+    info->attn_tensor_cores = g.attn_mma;
+    info->rows_per_chunk[0] = g.rpc_qkv;
+    info->rows_per_chunk[1] = g.rpc_o;
+    info->rows_per_chunk[2] = g.rpc_gateup;
+    info->rows_per_chunk[3] = g.rpc_down;
+    info->rows_per_chunk[4] = g.rpc_lm;
+    info->weight_format = g.wbytes == 1 ? TILES_WEIGHTS_INT8 : TILES_WEIGHTS_BF16;
+    long long tot = 0, mx = 0, mn = -1;
+    for (int c = 0; c < s.n_ctas; ++c) {
+        long long b = 0;
+        for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i)
+            if (op_is_gemv(s.tasks[i].op)) b += task_bytes(g, s.tasks[i], 0);
+        tot += b;
+        mx = b > mx ? b : mx;
+        mn = (mn < 0 || b < mn) ? b : mn;
+    }
+    info->weight_bytes_per_token = tot;
+    info->max_cta_bytes = mx;
+    info->min_cta_bytes = mn;
+    return TILES_OK;
+}
+
 void tiles_schedule_destroy(tiles_schedule_t sched) { delete sched; }
 
 const char *tiles_status_string(tiles_status_t st) {

@@ -347,36 +347,8 @@ tiles_status_t tiles_plan_set_trace(tiles_plan_t plan, void *trace, int32_t step
 }
 
 tiles_status_t tiles_plan_get_info(tiles_plan_t plan, tiles_plan_info *info) {
-    if (!plan || !info) return TILES_ERR_INVALID_ARG;
-    const tiles_schedule_s &s = plan->sched;
-    const Geom &g = s.geom;
-    std::memset(info, 0, sizeof(*info));
-    info->n_ctas = s.n_ctas;
-    info->threads_per_cta = kThreads;
-    info->smem_bytes = g.smem_bytes;
-    info->slot_bytes = g.slot_bytes;
-    info->ring_slots = g.ring_slots;
-    info->kv_splits = g.kv_splits;
-    info->scheduler = s.scheduler;
-    info->n_tasks = (int32_t)s.tasks.size();
-    info->n_counters = s.n_counters;
-    info->phases_per_step = phases_per_step(g);
-    int mt = 0;
-    for (int c = 0; c < s.n_ctas; ++c) mt = std::max(mt, s.offsets[c + 1] - s.offsets[c]);
-    info->max_tasks_per_cta = mt;
-    long long tot = 0, mx = 0, mn = -1;
-    for (int c = 0; c < s.n_ctas; ++c) {
-        long long b = 0;
-        for (int i = s.offsets[c]; i < s.offsets[c + 1]; ++i)
-            if (op_is_gemv(s.tasks[i].op)) b += task_bytes(g, s.tasks[i], 0);
-        tot += b;
-        mx = b > mx ? b : mx;
-        mn = (mn < 0 || b < mn) ? b : mn;
-    }
-    info->weight_bytes_per_token = tot;
-    info->max_cta_bytes = mx;
-    info->min_cta_bytes = mn;
-    return TILES_OK;
+    if (!plan) return TILES_ERR_INVALID_ARG;
+    return tiles_schedule_get_info(&plan->sched, info);
 }
 
 static tiles_status_t check_device(tiles_plan_t plan) {
