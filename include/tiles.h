@@ -306,7 +306,8 @@ void tiles_schedule_destroy(tiles_schedule_t sched);
  * max_j |w_rj| / 127 and codes[r][j] = w_rj / scales[r] rounded to nearest
  * even and clamped to [-127, 127], in FP32 (an all-zero row gets scale 0 and
  * codes 0). The same kernel quantizes a plan's weights when weight_format is
- * TILES_WEIGHTS_INT8. codes: rows * cols int8; scales: rows floats; both
+ * TILES_WEIGHTS_INT8 (the plan keeps each code as the byte q + 128, which its
+ * GEMV converts without a sign flip). codes: rows * cols int8; scales: rows floats; both
  * caller-owned. TILES_ERR_INVALID_ARG on a null pointer (rows > 0), rows < 0
  * or cols < 1; TILES_ERR_CUDA if the launch fails. */
 tiles_status_t tiles_quantize_rows_int8(const void *w_bf16, int32_t rows, int32_t cols, void *codes,

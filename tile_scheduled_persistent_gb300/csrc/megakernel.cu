@@ -41,11 +41,13 @@ cudaError_t megakernel_launch(const KernelParams &p, int n_ctas, int smem_bytes,
 // none): scale = max |w| / 127 and code = w / scale rounded to nearest even,
 // clamped to +-127, all in FP32 (an all-zero row: scale 0, codes 0). One CTA
 // per row. Source row r goes to destination row r * row_step + row0 (codes
-// and scale), which writes the plan's packed layouts directly.
+// and scale), which writes the plan's packed layouts directly. With offset
+// 128 a code is stored as the byte q + 128 (the plan's form: the GEMV then
+// needs no sign flip); with 0, as the int8 q.
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t *__restrict__ src, int rows,
-                                                            int cols, int8_t *__restrict__ dst,
+                                                            int cols, uint8_t *__restrict__ dst,
                                                             float *__restrict__ scale, int row_step,
-                                                            int row0) {
+                                                            int row0, int offset) {
     const int r = blockIdx.x;
     if (r >= rows) return;
     const uint16_t *w = src + (size_t)r * cols;
@@ -60,19 +62,20 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t *__re
     const float sc = __fdiv_rn(amax, 127.0f);
     const size_t orow = (size_t)r * row_step + row0;
     if (threadIdx.x == 0) scale[orow] = sc;
-    int8_t *q = dst + orow * cols;
+    uint8_t *q = dst + orow * cols;
     for (int j = threadIdx.x; j < cols; j += blockDim.x) {
         float qf = sc > 0.f ? rintf(__fdiv_rn(bf2f(w[j]), sc)) : 0.f;
         qf = fminf(fmaxf(qf, -127.f), 127.f);
-        q[j] = (int8_t)qf;
+        q[j] = (uint8_t)((int)qf + offset);
     }
 }
 
 cudaError_t quantize_rows_launch(const void *src, int rows, int cols, void *dst, float *scale,
-                                 int row_step, int row0, cudaStream_t st) {
+                                 int row_step, int row0, int offset, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
     quantize_rows_kernel<<<rows, 256, 0, st>>>(reinterpret_cast<const uint16_t *>(src), rows, cols,
-                                               reinterpret_cast<int8_t *>(dst), scale, row_step, row0);
+                                               reinterpret_cast<uint8_t *>(dst), scale, row_step, row0,
+                                               offset);
     return cudaGetLastError();
 }
 

@@ -797,8 +797,8 @@ __device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsig
     return d;
 }
 
-// Four INT8 codes of a word to exact floats, as two pairs: with the sign bit
-// of each byte flipped (u = q + 128), the byte placed under the exponent of
+// Four INT8 codes of a word to exact floats, as two pairs: the plan stores
+// each code q as the byte u = q + 128, the byte placed under the exponent of
 // 2^23 is the float 2^23 + u, and subtracting 2^23 + 128 leaves q (both steps
 // exact). Then 16 codes times 16 inputs (8 pairs), accumulated in FP32 on two
 // lanes (even and odd elements); each product is exact.
@@ -808,7 +808,7 @@ __device__ __forceinline__ unsigned long long dot16_q8(const uint4 &w, const uns
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const uint32_t u = ws[k] ^ 0x80808080u;
+        const uint32_t u = ws[k];
         const unsigned long long f01 =
             f2_sub(f2_pack_bits(__byte_perm(u, 0x4B000000u, 0x7540), __byte_perm(u, 0x4B000000u, 0x7541)), bias);
         const unsigned long long f23 =

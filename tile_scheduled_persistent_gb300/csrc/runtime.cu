@@ -21,7 +21,7 @@ namespace tiles {
 cudaError_t megakernel_configure(int d, int G, int wbytes, int mma, int smem_bytes);
 cudaError_t megakernel_occupancy(int d, int G, int wbytes, int mma, int smem_bytes, int *blocks_per_sm);
 cudaError_t quantize_rows_launch(const void *src, int rows, int cols, void *dst, float *scale,
-                                 int row_step, int row0, cudaStream_t st);
+                                 int row_step, int row0, int offset, cudaStream_t st);
 cudaError_t megakernel_launch(const KernelParams &p, int n_ctas, int smem_bytes, cudaStream_t st);
 cudaError_t copy_launch(void *dst, const void *src, size_t bytes, int n_ctas, cudaStream_t st);
 cudaError_t barrier_launch(uint32_t *ctr, int rounds, unsigned long long *elapsed, uint32_t *status,
@@ -242,13 +242,13 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
                 (e = dalloc(plan, &sgu, (size_t)2 * g.F * 4)) != cudaSuccess ||
                 (e = dalloc(plan, &sdown, (size_t)g.H * 4)) != cudaSuccess)
                 return fail(e);
-            if ((e = quantize_rows_launch(lw.wq, g.qd, g.H, qkv, sqkv, 1, 0, 0)) != cudaSuccess ||
-                (e = quantize_rows_launch(lw.wk, g.kvd, g.H, qkv, sqkv, 1, g.qd, 0)) != cudaSuccess ||
-                (e = quantize_rows_launch(lw.wv, g.kvd, g.H, qkv, sqkv, 1, g.qd + g.kvd, 0)) != cudaSuccess ||
-                (e = quantize_rows_launch(lw.wo, g.H, g.qd, o, so, 1, 0, 0)) != cudaSuccess ||
-                (e = quantize_rows_launch(lw.w_gate, g.F, g.H, gu, sgu, 2, 0, 0)) != cudaSuccess ||
-                (e = quantize_rows_launch(lw.w_up, g.F, g.H, gu, sgu, 2, 1, 0)) != cudaSuccess ||
-                (e = quantize_rows_launch(lw.w_down, g.H, g.F, down, sdown, 1, 0, 0)) != cudaSuccess)
+            if ((e = quantize_rows_launch(lw.wq, g.qd, g.H, qkv, sqkv, 1, 0, kCodeOffset, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.wk, g.kvd, g.H, qkv, sqkv, 1, g.qd, kCodeOffset, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.wv, g.kvd, g.H, qkv, sqkv, 1, g.qd + g.kvd, kCodeOffset, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.wo, g.H, g.qd, o, so, 1, 0, kCodeOffset, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.w_gate, g.F, g.H, gu, sgu, 2, 0, kCodeOffset, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.w_up, g.F, g.H, gu, sgu, 2, 1, kCodeOffset, 0)) != cudaSuccess ||
+                (e = quantize_rows_launch(lw.w_down, g.H, g.F, down, sdown, 1, 0, kCodeOffset, 0)) != cudaSuccess)
                 return fail(e);
             L.qkv = qkv;
             L.o = o;
@@ -268,7 +268,7 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
         float *lms;
         if ((e = dalloc(plan, &lm, (size_t)g.V * g.H)) != cudaSuccess ||
             (e = dalloc(plan, &lms, (size_t)g.V * 4)) != cudaSuccess ||
-            (e = quantize_rows_launch(w->embed, g.V, g.H, lm, lms, 1, 0, 0)) != cudaSuccess ||
+            (e = quantize_rows_launch(w->embed, g.V, g.H, lm, lms, 1, 0, kCodeOffset, 0)) != cudaSuccess ||
             (e = cudaDeviceSynchronize()) != cudaSuccess)
             return fail(e);
         p.lm = lm;
@@ -488,7 +488,7 @@ tiles_status_t tiles_decode_host(tiles_plan_t plan, void *k_cache, void *v_cache
 tiles_status_t tiles_quantize_rows_int8(const void *w_bf16, int32_t rows, int32_t cols, void *codes,
                                         float *scales, void *stream) {
     if (rows < 0 || cols < 1 || (rows > 0 && (!w_bf16 || !codes || !scales))) return TILES_ERR_INVALID_ARG;
-    const cudaError_t e = quantize_rows_launch(w_bf16, rows, cols, codes, scales, 1, 0,
+    const cudaError_t e = quantize_rows_launch(w_bf16, rows, cols, codes, scales, 1, 0, 0,
                                                reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TILES_OK : TILES_ERR_CUDA;
 }

@@ -27,6 +27,7 @@ constexpr int kSmemLimit = 232448;                    // 227 KB dynamic shared m
 constexpr int kCtlBytes = 1024;                       // mbarriers + control block
 constexpr int kPhaseKinds = 6;                        // QKV, ATTN, COMBINE, O, GATEUP, DOWN
 constexpr int kMaxStepsPerLaunch = 64;
+constexpr int kCodeOffset = 128;                      // a plan stores INT8 code q as the byte q + 128
 constexpr int kCounterStride = 32;                    // u32 words: one 128-byte line per counter
 constexpr int kPartialPad = 4;                        // (m, l, -, -) ahead of o[d] in a partial
 
