@@ -46,6 +46,10 @@ class OrcLayer(ctypes.Structure):
 _QSLOTS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
 
 
+class OrcKV8(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("kq", "vq", "ks", "vs", "mu")]
+
+
 class OrcQLayer(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in _QSLOTS] + \
                [(n, ctypes.c_void_p) for n in ("sq", "sk", "sv", "so", "s_gate", "s_up", "s_down")]
@@ -89,9 +93,14 @@ def lib(variant: str = "seq"):
             L.orc_attention_split.argtypes = [vp, vp, vp, i32, i32, f32, i32, vp, vp]
             L.orc_quantize_rows.argtypes = [vp, i32, i32, vp, vp]
             L.orc_gemv_q8.argtypes = [vp, vp, i32, i32, vp, vp]
+            L.orc_kv8_quantize_row.argtypes = [vp, i32, vp, vp]
+            L.orc_kv8_key_mean.argtypes = [vp, i32, i32, vp]
+            L.orc_kv8_from_bf16.argtypes = [ctypes.POINTER(OrcModel), vp, vp, i32,
+                                            ctypes.POINTER(OrcKV8)]
+            L.orc_attention_kv8.argtypes = [vp, vp, vp, vp, vp, i32, i32, f32, vp]
             L.orc_decode.argtypes = [ctypes.POINTER(OrcModel), ctypes.POINTER(OrcLayer), vp, vp,
                                      vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32,
-                                     ctypes.POINTER(OrcQLayer), vp, vp]
+                                     ctypes.POINTER(OrcQLayer), vp, vp, ctypes.POINTER(OrcKV8)]
             L.orc_decode.restype = i32
             _libs[variant] = L
     return _libs[variant]
@@ -220,22 +229,79 @@ def attention_split(q, K_bf16, V_bf16, scale: float, bounds) -> np.ndarray:
     return out
 
 
+# ------------------------------------------------------------- INT8 KV cache
+def kv8_quantize_row(x):
+    """One cached row to INT8: (codes int8[d], FP32 scale), absmax / 127, ties to even."""
+    x = _c(x, np.float32)
+    c = np.empty(x.size, np.int8)
+    s = np.zeros(1, np.float32)
+    lib().orc_kv8_quantize_row(x.ctypes.data, x.size, c.ctypes.data, s.ctypes.data)
+    return c, s[0]
+
+
+def kv8_key_mean(K_bf16):
+    """Per-channel mean of [n][d] BF16 keys (the key shift mu), FP32."""
+    K = _c(K_bf16, np.uint16)
+    mu = np.empty(K.shape[1], np.float32)
+    lib().orc_kv8_key_mean(K.ctypes.data, K.shape[0], K.shape[1], mu.ctypes.data)
+    return mu
+
+
+def attention_kv8(q, Kq, Ks, Vq, Vs, scale: float) -> np.ndarray:
+    q = _c(q, np.float32)
+    Kq, Vq = _c(Kq, np.int8), _c(Vq, np.int8)
+    Ks, Vs = _c(Ks, np.float32), _c(Vs, np.float32)
+    out = np.empty(q.size, np.float32)
+    lib().orc_attention_kv8(q.ctypes.data, Kq.ctypes.data, Ks.ctypes.data, Vq.ctypes.data,
+                            Vs.ctypes.data, Kq.shape[0], q.size, scale, out.ctypes.data)
+    return out
+
+
+class KV8Cache:
+    """The INT8 form of a [L][n_kv][max_pos][d] cache pair: codes kq, vq, FP32
+    scales ks, vs ([L][n_kv][max_pos]) and key shifts mu ([L][n_kv][d])."""
+    def __init__(self, cfg):
+        shape = (cfg.n_layers, cfg.n_kv_heads, cfg.max_pos, cfg.head_dim)
+        self.kq = np.zeros(shape, np.int8)
+        self.vq = np.zeros(shape, np.int8)
+        self.ks = np.zeros(shape[:3], np.float32)
+        self.vs = np.zeros(shape[:3], np.float32)
+        self.mu = np.zeros((cfg.n_layers, cfg.n_kv_heads, cfg.head_dim), np.float32)
+
+    def struct(self):
+        return OrcKV8(*(a.ctypes.data for a in (self.kq, self.vq, self.ks, self.vs, self.mu)))
+
+
+def kv8_from_bf16(cfg, k_cache, v_cache, n_pos: int) -> KV8Cache:
+    """INT8 cache of the prefilled positions 0..n_pos-1 (key shifts from them)."""
+    kv = KV8Cache(cfg)
+    st = kv.struct()
+    m = model_struct(cfg)
+    lib().orc_kv8_from_bf16(ctypes.byref(m), _c(k_cache, np.uint16).ctypes.data,
+                            _c(v_cache, np.uint16).ctypes.data, n_pos, ctypes.byref(st))
+    return kv
+
+
 # ------------------------------------------------------------- whole decoder
 class DecodeResult:
-    def __init__(self, tokens, logits, gaps):
+    def __init__(self, tokens, logits, gaps, kv8=None):
         self.tokens = tokens
         self.logits = logits
         self.gaps = gaps
+        self.kv8 = kv8
 
 
 def decode(cfg, weights, k_cache, v_cache, prompt, start_pos: int, n_new: int,
            force_tokens=None, want_logits: bool = True, n_threads: int = 0,
-           variant: str = "seq", qweights: QuantWeights | None = None) -> DecodeResult:
+           variant: str = "seq", qweights: QuantWeights | None = None,
+           kv_int8: bool = False) -> DecodeResult:
     """Run the oracle. ``weights`` is a ``synthetic.ModelWeights``; ``k_cache`` and
     ``v_cache`` are [L][n_kv][max_pos][d] uint16 arrays updated in place.
     ``variant="alt"`` runs the build with the other GEMV summation order.
     With ``qweights`` (``quantize_model(weights)``) every GEMV uses the INT8
-    weights; the embedding lookup stays BF16."""
+    weights; the embedding lookup stays BF16. With ``kv_int8`` attention reads
+    an INT8 KV cache with smoothed keys, built from the prefilled positions
+    (``kv8_from_bf16``) and extended every step; it is returned as ``.kv8``."""
     prompt = _c(prompt, np.int32)
     n_prompt = prompt.size
     steps = n_prompt - 1 + n_new
@@ -268,10 +334,13 @@ def decode(cfg, weights, k_cache, v_cache, prompt, start_pos: int, n_new: int,
                 setattr(qlayers[l], slot, codes.ctypes.data)
                 setattr(qlayers[l], sname, sc.ctypes.data)
         lm_q, lm_s = qweights.lm[0].ctypes.data, qweights.lm[1].ctypes.data
+    kv8 = kv8_from_bf16(cfg, k_cache, v_cache, start_pos) if kv_int8 else None
+    kv8_st = kv8.struct() if kv8 is not None else None
     rc = lib(variant).orc_decode(ctypes.byref(m), layers, embed.ctypes.data, fnorm.ctypes.data,
                           k_cache.ctypes.data, v_cache.ctypes.data, prompt.ctypes.data, n_prompt,
                           start_pos, n_new, _ptr(force), out_tokens.ctypes.data, _ptr(logits),
-                          gaps.ctypes.data, n_threads, qlayers, lm_q, lm_s)
+                          gaps.ctypes.data, n_threads, qlayers, lm_q, lm_s,
+                          ctypes.byref(kv8_st) if kv8_st is not None else None)
     if rc != 0:
         raise ValueError(f"orc_decode rejected its arguments (rc={rc})")
-    return DecodeResult(out_tokens[:n_new], logits, gaps[:steps])
+    return DecodeResult(out_tokens[:n_new], logits, gaps[:steps], kv8)

@@ -261,6 +261,102 @@ void orc_attention(const float *q, const uint16_t *K, const uint16_t *V, int n, 
     free(s);
 }
 
+/* ------------------------------------------------------------------ INT8 KV cache */
+
+/* INT8 KV cache with smoothed keys ("History and roadmap": the M8 log's INT8
+ * KV cache with smoothed keys, and "Tried and not kept": INT8 tensor cores for
+ * Q K^T were dropped because quantizing the queries undid what key smoothing
+ * gained, so queries stay unquantized). The pages give no scheme; the plainest
+ * one is taken:
+ *   - mu[h][j], the key shift of KV head h: the mean over the prefilled
+ *     positions 0..n-1 of the BF16 keys of channel j (FP32; 0 when n = 0);
+ *   - every cached row x (a key minus mu, or a value) gets one FP32 scale
+ *     s = max_j |x_j| / 127 and codes c_j = x_j / s rounded to nearest, ties
+ *     to even, clamped to [-127, 127] (an all-zero row: s = 0, codes 0);
+ *   - attention reads K_t = s_t c_t and V_t likewise. The shift is not added
+ *     back: it adds q . mu to every score of a query, and a softmax does not
+ *     change when every score moves by the same amount.                    */
+void orc_kv8_quantize_row(const float *x, int d, int8_t *c, float *s_out) {
+    float amax = 0.0f;
+    for (int j = 0; j < d; ++j) {
+        const float a = fabsf(x[j]);
+        if (a > amax) amax = a;
+    }
+    const float s = amax / 127.0f;
+    *s_out = s;
+    for (int j = 0; j < d; ++j) {
+        float qf = s > 0.0f ? rintf(x[j] / s) : 0.0f;
+        if (qf > 127.0f) qf = 127.0f;
+        if (qf < -127.0f) qf = -127.0f;
+        c[j] = (int8_t)qf;
+    }
+}
+
+/* mu[j] = (sum_t K[t][j]) / n over n bf16 rows of d (FP64 sum, FP32 result). */
+void orc_kv8_key_mean(const uint16_t *K, int n, int d, float *mu) {
+    for (int j = 0; j < d; ++j) {
+        double acc = 0.0;
+        for (int t = 0; t < n; ++t) acc += (double)orc_f32_from_bf16(K[(int64_t)t * d + j]);
+        mu[j] = n > 0 ? (float)(acc / n) : 0.0f;
+    }
+}
+
+/* The INT8 form of a [L][n_kv][max_pos][d] cache pair: codes kq, vq (same
+ * shape), scales ks, vs ([L][n_kv][max_pos]) and key shifts mu ([L][n_kv][d]). */
+typedef struct {
+    int8_t *kq, *vq;
+    float *ks, *vs, *mu;
+} orc_kv8;
+
+/* Fills kv8 from the BF16 caches for positions 0..n_pos-1 (the prefill):
+ * mu from those keys, then every row quantized as above. */
+void orc_kv8_from_bf16(const orc_model *m, const uint16_t *k_cache, const uint16_t *v_cache, int n_pos,
+                       orc_kv8 *kv8) {
+    const int d = m->head_dim, heads = m->n_layers * m->n_kv_heads;
+    float *row = (float *)malloc(sizeof(float) * d);
+    for (int hh = 0; hh < heads; ++hh) {
+        const int64_t base = (int64_t)hh * m->max_pos;
+        float *mu = kv8->mu + (int64_t)hh * d;
+        orc_kv8_key_mean(k_cache + base * d, n_pos, d, mu);
+        for (int t = 0; t < n_pos; ++t) {
+            const int64_t r = base + t;
+            for (int j = 0; j < d; ++j) row[j] = orc_f32_from_bf16(k_cache[r * d + j]) - mu[j];
+            orc_kv8_quantize_row(row, d, kv8->kq + r * d, kv8->ks + r);
+            for (int j = 0; j < d; ++j) row[j] = orc_f32_from_bf16(v_cache[r * d + j]);
+            orc_kv8_quantize_row(row, d, kv8->vq + r * d, kv8->vs + r);
+        }
+    }
+    free(row);
+}
+
+/* orc_attention over the INT8 rows: s_t = (q . (ks_t Kq_t)) * scale, then the
+ * same softmax and sum_t p_t (vs_t Vq_t). Dequantized values are formed in
+ * FP32 (a code times a scale, one rounding), the sums left to right. */
+void orc_attention_kv8(const float *q, const int8_t *Kq, const float *Ks, const int8_t *Vq,
+                       const float *Vs, int n, int d, float scale, float *out) {
+    float *s = (float *)malloc(sizeof(float) * (n > 0 ? n : 1));
+    float mx = -INFINITY;
+    for (int t = 0; t < n; ++t) {
+        const int8_t *k = Kq + (int64_t)t * d;
+        float dot = 0.0f;
+        for (int j = 0; j < d; ++j) dot += q[j] * (Ks[t] * (float)k[j]);
+        s[t] = dot * scale;
+        if (s[t] > mx) mx = s[t];
+    }
+    float l = 0.0f;
+    for (int t = 0; t < n; ++t) {
+        s[t] = expf(s[t] - mx);
+        l += s[t];
+    }
+    for (int j = 0; j < d; ++j) out[j] = 0.0f;
+    for (int t = 0; t < n; ++t) {
+        const float p = s[t] / l;
+        const int8_t *v = Vq + (int64_t)t * d;
+        for (int j = 0; j < d; ++j) out[j] += p * (Vs[t] * (float)v[j]);
+    }
+    free(s);
+}
+
 /* Split-KV form of the same quantity (test helper, used to pin the reading that
  * split partials plus a separate combine equal the unsplit softmax; "History
  * and roadmap", M5 split-KV decode kernels and "Tried and not kept": separate
@@ -323,14 +419,16 @@ static float silu(float z) { return z / (1.0f + expf(-z)); }
  * at P. out_logits ([steps][vocab]) and out_gap ([steps], top-1 minus top-2
  * logit) may be NULL. With qlayers (and lm_q, lm_s for the tied LM head) the
  * GEMVs use those INT8 weights (orc_gemv_q8); the embedding lookup stays BF16.
- * Returns 0, or -1 on bad arguments.
+ * With kv8 (filled for the prefill by orc_kv8_from_bf16), every new K/V row is
+ * also quantized into it and attention reads the INT8 cache (orc_attention_kv8);
+ * the BF16 caches are still written. Returns 0, or -1 on bad arguments.
  */
 int orc_decode(const orc_model *m, const orc_layer *layers, const uint16_t *embed,
                const uint16_t *final_norm, uint16_t *k_cache, uint16_t *v_cache,
                const int32_t *prompt, int n_prompt, int start_pos, int n_new,
                const int32_t *force_tokens, int32_t *out_tokens, float *out_logits,
                float *out_gap, int n_threads, const orc_qlayer *qlayers,
-               const int8_t *lm_q, const float *lm_s) {
+               const int8_t *lm_q, const float *lm_s, orc_kv8 *kv8) {
     if (!m || !layers || !embed || !final_norm || !k_cache || !v_cache || !prompt ||
         n_prompt < 1 || n_new < 0 || start_pos < 0)
         return -1;
@@ -408,12 +506,30 @@ int orc_decode(const orc_model *m, const orc_layer *layers, const uint16_t *embe
                     Kl[off] = orc_bf16_from_f32(k[i * d + j]);
                     Vl[off] = orc_bf16_from_f32(v[i * d + j]);
                 }
+            if (kv8) {
+                /* the new row, as cached (R(k) - mu, R(v)), into the INT8 cache */
+                for (int i = 0; i < nkv; ++i) {
+                    const int64_t r = ((int64_t)l * nkv + i) * m->max_pos + P;  /* row in kv8 */
+                    const int64_t off = ((int64_t)i * m->max_pos + P) * d;      /* row in Kl, Vl */
+                    const float *mu = kv8->mu + ((int64_t)l * nkv + i) * d;
+                    for (int j = 0; j < d; ++j) tmp[j] = orc_f32_from_bf16(Kl[off + j]) - mu[j];
+                    orc_kv8_quantize_row(tmp, d, kv8->kq + r * d, kv8->ks + r);
+                    for (int j = 0; j < d; ++j) tmp[j] = orc_f32_from_bf16(Vl[off + j]);
+                    orc_kv8_quantize_row(tmp, d, kv8->vq + r * d, kv8->vs + r);
+                }
+            }
             /* q head i reads KV head floor(i / G); positions 0..P inclusive */
 #pragma omp parallel for schedule(static)
             for (int i = 0; i < nq; ++i) {
                 int gi = i / G;
-                orc_attention(q + i * d, Kl + (int64_t)gi * m->max_pos * d,
-                              Vl + (int64_t)gi * m->max_pos * d, P + 1, d, scale, o + i * d);
+                if (kv8) {
+                    const int64_t r0 = ((int64_t)l * nkv + gi) * m->max_pos;
+                    orc_attention_kv8(q + i * d, kv8->kq + r0 * d, kv8->ks + r0, kv8->vq + r0 * d,
+                                      kv8->vs + r0, P + 1, d, scale, o + i * d);
+                } else {
+                    orc_attention(q + i * d, Kl + (int64_t)gi * m->max_pos * d,
+                                  Vl + (int64_t)gi * m->max_pos * d, P + 1, d, scale, o + i * d);
+                }
             }
             round_vec(o, qd);
             if (qw) orc_gemv_q8(qw->wo, qw->so, H, qd, o, y);

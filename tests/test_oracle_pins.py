@@ -466,3 +466,116 @@ def test_decoder_int8_equals_bf16_when_weights_lie_on_the_int8_grid(tiny_cfg):
     b = O.decode(cfg, w, k.copy(), v.copy(), p, 0, 5, qweights=qw)
     assert np.array_equal(a.tokens, b.tokens)
     assert np.array_equal(a.logits.view(np.uint32), b.logits.view(np.uint32))
+
+
+# ------------------------------------------------------------------ INT8 KV cache
+def test_kv8_row_quantizer_scale_ties_and_zero_row():
+    """A row with absmax 127/128 has scale exactly 2^-7: codes are value * 128,
+    ties to even (2.5 -> 2, -2.5 -> -2, 3.5 -> 4); an all-zero row gets scale 0."""
+    c, s = O.kv8_quantize_row(np.array([127, -127, 2.5, -2.5, 3.5, 0, 64], np.float32) / 128)
+    assert s == np.float32(2.0 ** -7)
+    assert np.array_equal(c, [127, -127, 2, -2, 4, 0, 64])
+    c, s = O.kv8_quantize_row(np.zeros(8, np.float32))
+    assert s == 0 and not c.any()
+
+
+def test_kv8_key_mean_closed_form():
+    K = _bf16_exact(np.array([[1, 2, -8], [3, 6, 0], [5, 10, 2]], np.float32))
+    assert np.array_equal(O.kv8_key_mean(K), np.array([3, 6, -2], np.float32))
+    assert not O.kv8_key_mean(K[:0]).any()                 # no prefill: no shift
+
+
+def test_kv8_attention_matches_fp64_of_codes_times_scales():
+    """Scores from ks_t Kq_t, weights from vs_t Vq_t, softmax in FP64 on the
+    same dequantized rows (a swapped K/V scale, a transposed code matrix or a
+    missing 1/sqrt(d) fails)."""
+    rng = np.random.default_rng(41)
+    n, d = 300, 64
+    Kq = rng.integers(-127, 128, (n, d)).astype(np.int8)
+    Vq = rng.integers(-127, 128, (n, d)).astype(np.int8)
+    Ks = rng.uniform(0.005, 0.05, n).astype(np.float32)
+    Vs = rng.uniform(0.005, 0.05, n).astype(np.float32)
+    q = rng.normal(0, 1, d).astype(np.float32)
+    out = O.attention_kv8(q, Kq, Ks, Vq, Vs, 1 / np.sqrt(d))
+    K = Ks[:, None].astype(np.float64) * Kq
+    V = Vs[:, None].astype(np.float64) * Vq
+    sc = K @ q.astype(np.float64) / np.sqrt(d)
+    p = np.exp(sc - sc.max())
+    ref = (p / p.sum()) @ V
+    assert np.allclose(out, ref, rtol=1e-4, atol=1e-5 * np.abs(ref).max())
+
+
+def test_kv8_smoothing_removes_the_channel_offset_from_the_codes(tiny_cfg):
+    """Keys = a per-channel offset mu + deviations on the grid s * code with
+    zero mean per channel. The prefill conversion finds mu,
+    quantizes only the deviations (exactly), and since a softmax ignores the
+    q . mu added to every score, INT8 attention equals FP64 attention over the
+    original keys. Quantizing the keys without the shift loses the deviations
+    under a scale set by the offset, and fails by orders of magnitude."""
+    cfg = tiny_cfg.with_workload(max_pos=64)
+    rng = np.random.default_rng(42)
+    n, d = 32, cfg.head_dim
+    # offsets: integers in [-16, 16]; deviations: k / 4 with |k| <= 127 and
+    # |k| = 127 in column 0 of every row (so every scale is exactly 1/4); keys
+    # below 64 in magnitude on a 1/4 grid are exact in BF16
+    mu = rng.integers(-16, 17, d).astype(np.float32)
+    kdev = rng.integers(-127, 128, (n // 2, d)).astype(np.float32)
+    kdev[:, 0] = 127
+    dev = np.concatenate([kdev, -kdev]) * np.float32(0.25)               # zero mean per channel
+    keys = _bf16_exact(mu[None, :] + dev)
+    shape = (cfg.n_layers, cfg.n_kv_heads, cfg.max_pos, d)
+    k = np.zeros(shape, np.uint16)
+    v = np.zeros(shape, np.uint16)
+    k[0, 0, :n] = keys
+    vq = rng.integers(-127, 128, (n, d)).astype(np.float32)
+    vq[:, 1] = 127                                        # every V scale exactly 2^-7 too
+    v[0, 0, :n] = _bf16_exact(vq * np.float32(2.0 ** -7))
+    kv = O.kv8_from_bf16(cfg, k, v, n)
+    assert np.array_equal(kv.mu[0, 0], mu)
+    deq = kv.ks[0, 0, :n, None].astype(np.float64) * kv.kq[0, 0, :n]
+    assert np.array_equal(deq, dev.astype(np.float64))                   # deviations exact
+    q = rng.normal(0, 0.05, d).astype(np.float32)      # scores of order 1: FP32 error ~1e-7
+    out = O.attention_kv8(q, kv.kq[0, 0, :n], kv.ks[0, 0, :n], kv.vq[0, 0, :n], kv.vs[0, 0, :n],
+                          1 / np.sqrt(d))
+    K = O.f32_from_bf16(keys).reshape(n, d).astype(np.float64)
+    V = O.f32_from_bf16(v[0, 0, :n]).reshape(n, d).astype(np.float64)
+    sc = K @ q.astype(np.float64) / np.sqrt(d)
+    p = np.exp(sc - sc.max())
+    ref = (p / p.sum()) @ V
+    err = np.abs(out - ref).max()
+    assert err < 1e-5
+    # without the shift: codes of the raw keys
+    raw = [O.kv8_quantize_row(O.f32_from_bf16(r)) for r in keys]
+    Kq0 = np.stack([c for c, _ in raw]); Ks0 = np.array([s for _, s in raw], np.float32)
+    out0 = O.attention_kv8(q, Kq0, Ks0, kv.vq[0, 0, :n], kv.vs[0, 0, :n], 1 / np.sqrt(d))
+    assert np.abs(out0 - ref).max() > 100 * max(err, 1e-7)
+
+
+def test_kv8_decode_writes_each_new_row_with_the_prefill_shift(tiny_cfg):
+    """Decoding with the INT8 cache: every row written during the run is the
+    INT8 form of (the BF16 row the run cached) - mu, with mu from the prefill;
+    the prefill rows are converted the same way; and the logits stay close to
+    the BF16-cache decode (INT8 with about 8 bits per entry)."""
+    cfg = tiny_cfg.with_workload(max_pos=96)
+    w = S.model_weights(cfg)
+    n0 = 40
+    k, v = S.kv_prefill(cfg, n_pos=n0)
+    p = S.prompt(cfg)[:3]
+    kb, vb = k.copy(), v.copy()
+    ref = O.decode(cfg, w, kb, vb, p, n0, 6)
+    k8, v8 = k.copy(), v.copy()
+    r8 = O.decode(cfg, w, k8, v8, p, n0, 6, kv_int8=True)
+    kv = r8.kv8
+    end = n0 + p.size - 1 + 6
+    for l in range(cfg.n_layers):
+        for h in range(cfg.n_kv_heads):
+            mu = kv.mu[l, h]
+            assert np.array_equal(mu, O.kv8_key_mean(k[l, h, :n0]))
+            for t in (0, n0 - 1, n0, end - 1):
+                c, s = O.kv8_quantize_row(O.f32_from_bf16(k8[l, h, t]) - mu)
+                assert np.array_equal(kv.kq[l, h, t], c) and kv.ks[l, h, t] == s
+                c, s = O.kv8_quantize_row(O.f32_from_bf16(v8[l, h, t]))
+                assert np.array_equal(kv.vq[l, h, t], c) and kv.vs[l, h, t] == s
+    assert not kv.kq[:, :, end:].any() and not kv.ks[:, :, end:].any()
+    assert np.abs(r8.logits - ref.logits).max() < 0.1 * np.abs(ref.logits).max()
+    assert np.abs(r8.logits - ref.logits).max() > 0                       # it is a different cache
