@@ -344,3 +344,34 @@ def decode(cfg, weights, k_cache, v_cache, prompt, start_pos: int, n_new: int,
     if rc != 0:
         raise ValueError(f"orc_decode rejected its arguments (rc={rc})")
     return DecodeResult(out_tokens[:n_new], logits, gaps[:steps], kv8)
+
+
+# ------------------------------------------------------------- multi-token verify
+class VerifyResult:
+    def __init__(self, n_accepted, tokens, argmax, logits):
+        self.n_accepted = n_accepted   # drafts accepted
+        self.tokens = tokens           # emitted: the accepted drafts, then one model token
+        self.argmax = argmax           # the model's token after each of the k + 1 inputs
+        self.logits = logits           # [k + 1][vocab]
+
+
+def verify(cfg, weights, k_cache, v_cache, last_token: int, start_pos: int, drafts,
+           qweights: QuantWeights | None = None) -> VerifyResult:
+    """One verify step over k draft tokens ("History and roadmap": 16-token
+    verify steps on the split-KV decode kernels; the drafts' source is out of
+    scope). The inputs last_token, d_1..d_k take positions start_pos ..
+    start_pos + k (their K/V rows are written). a_i is the greedy token after
+    input i. The step accepts the longest prefix with d_{i+1} = a_i, n drafts,
+    and emits d_1..d_n, then a_n. Rows past start_pos + n are left as written
+    and are stale; the caller's next step starts at start_pos + n + 1.
+    Greedy decoding from the same state emits the same tokens."""
+    drafts = [int(t) for t in drafts]
+    inputs = np.array([int(last_token)] + drafts, np.int32)
+    r = decode(cfg, weights, k_cache, v_cache, inputs, start_pos, 1, qweights=qweights)
+    argmax = r.logits.argmax(axis=1).astype(np.int32)          # lowest index on ties
+    n = 0
+    while n < len(drafts) and drafts[n] == argmax[n]:
+        n += 1
+    tokens = np.array(drafts[:n] + [int(argmax[n])], np.int32)
+    return VerifyResult(n, tokens, argmax, r.logits)
+

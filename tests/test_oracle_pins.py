@@ -579,3 +579,62 @@ def test_kv8_decode_writes_each_new_row_with_the_prefill_shift(tiny_cfg):
     assert not kv.kq[:, :, end:].any() and not kv.ks[:, :, end:].any()
     assert np.abs(r8.logits - ref.logits).max() < 0.1 * np.abs(ref.logits).max()
     assert np.abs(r8.logits - ref.logits).max() > 0                       # it is a different cache
+
+
+# ------------------------------------------------------------------ multi-token verify
+@pytest.fixture(scope="module")
+def lively_model():
+    """The tiny shape with its weights scaled by 8, so greedy decoding does not
+    repeat one token (needed to see which draft each model token is compared
+    with), and a 20-position prefill."""
+    cfg = S.CONFIGS["tiny"]
+    w = S.model_weights(cfg)
+
+    def scale(a):
+        f = O.f32_from_bf16(a).reshape(a.shape) * np.float32(8)
+        return O.bf16_from_f32(f.astype(np.float32)).reshape(a.shape)
+
+    for lw in w.layers:
+        for slot in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down"):
+            lw[slot] = scale(lw[slot])
+    w.embed = scale(w.embed)
+    k, v = S.kv_prefill(cfg, n_pos=20)
+    greedy = O.decode(cfg, w, k.copy(), v.copy(), np.array([5], np.int32), 20, 24).tokens
+    assert len(set(greedy.tolist())) > 16
+    return cfg, w, k, v, greedy
+
+
+def test_verify_accepts_right_drafts_and_stops_at_the_first_wrong_one(lively_model):
+    """Drafts equal to greedy's: all k accepted, k + 1 tokens out. A wrong
+    draft at index j: j accepted, and the token after them is greedy's. An
+    off-by-one comparing a_i with d_i instead of d_{i+1} accepts nothing here."""
+    cfg, w, k, v, g = lively_model
+    r = O.verify(cfg, w, k.copy(), v.copy(), 5, 20, g[:6])
+    assert r.n_accepted == 6 and np.array_equal(r.tokens, g[:7])
+    for j in (0, 3):
+        d = g[:6].copy()
+        d[j] = (d[j] + 1) % cfg.vocab
+        r = O.verify(cfg, w, k.copy(), v.copy(), 5, 20, d)
+        assert r.n_accepted == j and np.array_equal(r.tokens, g[:j + 1])
+        assert np.array_equal(r.argmax[:j + 1], g[:j + 1])
+
+
+def test_verify_loop_emits_exactly_the_greedy_tokens(lively_model):
+    """Speculative greedy decoding is lossless: verify steps over drafts that
+    are right for a random number of tokens and then wrong, each step starting
+    where the last one's accepted prefix ended (its stale rows overwritten),
+    emit greedy decoding's tokens."""
+    cfg, w, k, v, g = lively_model
+    rng = np.random.default_rng(43)
+    kk, vv = k.copy(), v.copy()
+    out, pos, last = [], 20, 5
+    while len(out) < 20:
+        i = len(out)
+        good = int(rng.integers(0, 5))
+        drafts = list(g[i:i + good]) + [int(rng.integers(0, cfg.vocab)) for _ in range(3)]
+        r = O.verify(cfg, w, kk, vv, last, pos, drafts)
+        assert r.n_accepted >= min(good, len(g) - i)
+        out += r.tokens.tolist()
+        pos += r.n_accepted + 1
+        last = int(r.tokens[-1])
+    assert out[:20] == g[:20].tolist()
