@@ -181,14 +181,14 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------- CPU oracle arm
-def oracle_sample(cfg, w, k, v, prompt, n_tokens, qweights=None):
-    """Time the oracle on n_tokens decode steps of the workload (all host cores);
-    with qweights, its weight-only INT8 form."""
+def oracle_sample(cfg, w, k, v, prompt, n_tokens, qweights=None, n_threads=0):
+    """Time the oracle on n_tokens decode steps of the workload (all host cores,
+    or n_threads); with qweights, its weight-only INT8 form."""
     import oracle
     kk, vv = k.copy(), v.copy()
     t0 = time.perf_counter()
     oracle.decode(cfg, w, kk, vv, prompt, cfg.start_pos, n_tokens, want_logits=False,
-                  qweights=qweights)
+                  qweights=qweights, n_threads=n_threads)
     return time.perf_counter() - t0
 
 
@@ -359,11 +359,18 @@ def run_ours(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         n_tok = args.ref_tokens
-        secs = oracle_sample(cfg, w, k_np, v_np, prompt_np, n_tok, oracle_qweights(w, int8))
+        qw = oracle_qweights(w, int8)
+        secs = oracle_sample(cfg, w, k_np, v_np, prompt_np, n_tok, qw)
         cpu = {"value": n_tok / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"first {n_tok} of the {cfg.n_new} decode tokens from position "
                          f"{cfg.start_pos}, OpenMP over output rows and heads on all host cores"
                          + (", the oracle's weight-only INT8 path" if int8 else "")}
+        try:  # the same oracle on one thread, one token (information only)
+            secs1 = oracle_sample(cfg, w, k_np, v_np, prompt_np, 1, qw, n_threads=1)
+            cpu["single_thread"] = {"value": 1 / secs1, "unit": UNIT, "cores": 1,
+                                    "sample": f"first decode token from position {cfg.start_pos}"}
+        except Exception as e:  # never let the information line cost the measurement
+            cpu["single_thread"] = {"error": str(e)[:200]}
 
     if rank == 0:
         conf = workload_config(cfg, int8)
@@ -388,6 +395,9 @@ def run_ours(args):
                 "clocks": r["clocks"],
                 "bitwise_repeat": r["bitwise"],
                 "us_per_token": 1e6 * launch_s / cfg.n_new,
+                "launch_us": {"mean": 1e6 * launch_s,
+                              "median": 1e6 * statistics.median(r["per_launch"]),
+                              "min": 1e6 * min(r["per_launch"])},
                 "grid_barrier_ns": barrier_ns,
                 "schedulers": {s: {"tok_s": args.steps * cfg.n_new * ws / slowest[s],
                                    "bitwise_repeat": results[s]["bitwise"]} for s in results}}
