@@ -198,8 +198,11 @@ tiles_status_t tiles_decode_host(tiles_plan_t plan, void *k_cache, void *v_cache
  *     library until the process exits. A plan whose working memory does not
  *     fit (q/k/v, split partials, attention output, residual, FFN activation,
  *     argmax keys and counters) is rejected with TILES_ERR_CAPACITY.
- *   - The first call on a device looks up the array's device address once;
- *     make that first call before any stream capture.
+ *   - The first call on a device looks up the array's device address once
+ *     and keeps it for the life of the process: make that first call before
+ *     any stream capture, and make every call in the device's primary context
+ *     (the runtime's default; after cudaDeviceReset or under another current
+ *     context the kept address would not point at the array).
  *   - Every call on a device shares the one array and finds it as the previous
  *     call left it; the call clears what must start at zero. Calls whose work
  *     overlaps on the GPU (other streams, other plans) race on it: keep them
@@ -220,12 +223,19 @@ const char *tiles_status_string(tiles_status_t status);
 
 /* Diagnostics: makes later tiles_decode calls on this plan record a per-task
  * timeline of their first `steps` steps into `trace` (device memory, caller
- * owned, at least n_ctas * steps * max_tasks_per_cta * 8 uint64 words, see
- * tiles_plan_info.max_tasks_per_cta). Word layout per task record: consumer
- * wait start, inputs ready, task end, producer first issue, producer last
- * issue, producer ns stalled on a full ring, op | layer << 8 | chunks << 32.
- * Times are %globaltimer nanoseconds. trace == NULL or steps == 0 turns it off.
- * Errors: INVALID_ARG. */
+ * owned, at least n_ctas * steps * max_tasks_per_cta * 16 uint64 words, see
+ * tiles_plan_info.max_tasks_per_cta). Word layout per task record:
+ *    0 consumer wait start        1 inputs ready (after the counter wait)
+ *    2 task end                   3 producer: first chunk of the task
+ *    4 producer: last chunk       5 producer ns stalled on a full ring
+ *    6 op | layer << 8 | chunks << 32
+ *    7 prologue end (input vector gathered and normalised; attention: the
+ *      first head's q/k/v ready)
+ *    8 first chunk in shared memory
+ *    9 attention: split partials written   10 attention: merge inputs in
+ *   11..15 zero
+ * Times are %globaltimer nanoseconds; a word a task does not use stays 0.
+ * trace == NULL or steps == 0 turns it off. Errors: INVALID_ARG. */
 tiles_status_t tiles_plan_set_trace(tiles_plan_t plan, void *trace, int32_t steps);
 
 /* Facts about a built plan (or a host-only schedule), for reports and tests. */

@@ -72,37 +72,41 @@ def build(force: bool = False) -> str:
     return _build_one(_LIB_PATH, [], force)
 
 
+def load_library(path: str):
+    """Loads an oracle build at `path` with the argument types of every entry point."""
+    L = ctypes.CDLL(path)
+    vp, i32, f32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int64
+    L.orc_bf16_from_f32.argtypes = [f32]
+    L.orc_bf16_from_f32.restype = ctypes.c_uint16
+    L.orc_f32_from_bf16.argtypes = [ctypes.c_uint16]
+    L.orc_f32_from_bf16.restype = f32
+    L.orc_bf16_round_array.argtypes = [vp, vp, i64]
+    L.orc_rmsnorm.argtypes = [vp, vp, i32, f32, vp]
+    L.orc_rope_inv_freq.argtypes = [ctypes.POINTER(OrcModel), vp]
+    L.orc_rope_cos_sin.argtypes = [ctypes.POINTER(OrcModel), i32, vp, vp]
+    L.orc_rope_apply.argtypes = [vp, i32, vp, vp]
+    L.orc_gemv.argtypes = [vp, i32, i32, vp, vp]
+    L.orc_attention.argtypes = [vp, vp, vp, i32, i32, f32, vp]
+    L.orc_attention_split.argtypes = [vp, vp, vp, i32, i32, f32, i32, vp, vp]
+    L.orc_quantize_rows.argtypes = [vp, i32, i32, vp, vp]
+    L.orc_gemv_q8.argtypes = [vp, vp, i32, i32, vp, vp]
+    L.orc_kv8_quantize_row.argtypes = [vp, i32, vp, vp]
+    L.orc_kv8_key_mean.argtypes = [vp, i32, i32, vp]
+    L.orc_kv8_from_bf16.argtypes = [ctypes.POINTER(OrcModel), vp, vp, i32, ctypes.POINTER(OrcKV8)]
+    L.orc_attention_kv8.argtypes = [vp, vp, vp, vp, vp, i32, i32, f32, vp]
+    L.orc_decode.argtypes = [ctypes.POINTER(OrcModel), ctypes.POINTER(OrcLayer), vp, vp,
+                             vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32,
+                             ctypes.POINTER(OrcQLayer), vp, vp, ctypes.POINTER(OrcKV8)]
+    L.orc_decode.restype = i32
+    return L
+
+
 def lib(variant: str = "seq"):
     """The oracle library; variant "alt" is the build with the other GEMV summation order."""
     with _lock:
         if variant not in _libs:
             build()
-            L = ctypes.CDLL(_ALT_LIB_PATH if variant == "alt" else _LIB_PATH)
-            vp, i32, f32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int64
-            L.orc_bf16_from_f32.argtypes = [f32]
-            L.orc_bf16_from_f32.restype = ctypes.c_uint16
-            L.orc_f32_from_bf16.argtypes = [ctypes.c_uint16]
-            L.orc_f32_from_bf16.restype = f32
-            L.orc_bf16_round_array.argtypes = [vp, vp, i64]
-            L.orc_rmsnorm.argtypes = [vp, vp, i32, f32, vp]
-            L.orc_rope_inv_freq.argtypes = [ctypes.POINTER(OrcModel), vp]
-            L.orc_rope_cos_sin.argtypes = [ctypes.POINTER(OrcModel), i32, vp, vp]
-            L.orc_rope_apply.argtypes = [vp, i32, vp, vp]
-            L.orc_gemv.argtypes = [vp, i32, i32, vp, vp]
-            L.orc_attention.argtypes = [vp, vp, vp, i32, i32, f32, vp]
-            L.orc_attention_split.argtypes = [vp, vp, vp, i32, i32, f32, i32, vp, vp]
-            L.orc_quantize_rows.argtypes = [vp, i32, i32, vp, vp]
-            L.orc_gemv_q8.argtypes = [vp, vp, i32, i32, vp, vp]
-            L.orc_kv8_quantize_row.argtypes = [vp, i32, vp, vp]
-            L.orc_kv8_key_mean.argtypes = [vp, i32, i32, vp]
-            L.orc_kv8_from_bf16.argtypes = [ctypes.POINTER(OrcModel), vp, vp, i32,
-                                            ctypes.POINTER(OrcKV8)]
-            L.orc_attention_kv8.argtypes = [vp, vp, vp, vp, vp, i32, i32, f32, vp]
-            L.orc_decode.argtypes = [ctypes.POINTER(OrcModel), ctypes.POINTER(OrcLayer), vp, vp,
-                                     vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32,
-                                     ctypes.POINTER(OrcQLayer), vp, vp, ctypes.POINTER(OrcKV8)]
-            L.orc_decode.restype = i32
-            _libs[variant] = L
+            _libs[variant] = load_library(_ALT_LIB_PATH if variant == "alt" else _LIB_PATH)
     return _libs[variant]
 
 

@@ -17,12 +17,16 @@ and describes the five decoder shapes and workloads used throughout:
 Tiles", intro, and "History and roadmap", "Where it stands" table).
 
 It holds none of the decoding arithmetic: no norm, GEMV, RoPE, attention or
-activation rounding lives here. Weights are N(0, 0.02) bf16, norm gains 1.0,
-KV-cache prefill N(0, 1) bf16, token ids uniform. Tensor ids (the `tid` of the
-generator) are fixed:
+activation rounding lives here. Weights are N(0, 0.02) bf16, norm gains 1.0
+(the workloads' setting) or, with ``gain_sigma`` > 0, seeded 1 + N(0, gain_sigma)
+bf16 gains, a different vector per norm (the parity tests' setting: a kernel that
+dropped or swapped a gain would then disagree with the oracle). KV-cache prefill
+N(0, 1) bf16, token ids uniform. Tensor ids (the `tid` of the generator) are
+fixed:
 
-  weights (seed 0): embed 0; layer l matrix m -> 16 + 16*l + m with
-      m = 1 wq, 2 wk, 3 wv, 6 wo, 8 w_gate, 9 w_up, 10 w_down
+  weights (seed 0): embed 0; final_norm gain 1; layer l slot m -> 16 + 16*l + m
+      with m = 0 attn_norm, 1 wq, 2 wk, 3 wv, 4 q_norm, 5 k_norm, 6 wo,
+      7 ffn_norm, 8 w_gate, 9 w_up, 10 w_down
   kv prefill (seed 1): layer l keys 2*l, values 2*l + 1; element index
       (head * n_pos + pos) * head_dim + j
   tokens (seed 2): prompt 0
@@ -83,6 +87,7 @@ def _load():
             lib.synth_kv_prefill_bf16.argtypes = [u64, u64, i32, i32, i32, i32, dbl, vp]
             lib.synth_tokens.argtypes = [u64, u64, i64, i64, vp]
             lib.synth_fill_bf16.argtypes = [vp, i64, ctypes.c_uint16]
+            lib.synth_gain_bf16.argtypes = [u64, u64, i64, dbl, vp]
             _lib = lib
     return _lib
 
@@ -120,6 +125,13 @@ def ones_bf16(n: int) -> np.ndarray:
     return np.full(n, BF16_ONE, dtype=np.uint16)
 
 
+def gain_bf16(seed: int, tid: int, n: int, sigma: float) -> np.ndarray:
+    """Norm gains 1 + sigma * N(0, 1) as bf16 bit patterns (element c of tensor tid)."""
+    out = np.empty(n, dtype=np.uint16)
+    _load().synth_gain_bf16(seed, tid, n, sigma, out.ctypes.data)
+    return out
+
+
 def bf16_to_f32(a: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns to float32 (a bit shift)."""
     return (a.astype(np.uint32) << 16).view(np.float32)
@@ -144,6 +156,7 @@ class ModelConfig:
     rs_low: float = 1.0
     rs_high: float = 4.0
     rs_orig_max: int = 8192
+    gain_sigma: float = 0.0             # 0: every norm gain 1.0; else 1 + N(0, gain_sigma)
     # workload
     n_prompt: int = 1
     start_pos: int = 1023
@@ -222,15 +235,21 @@ def _tid(layer: int, slot: str) -> int:
 def layer_weights(cfg: ModelConfig, l: int, seed: int = SEED_WEIGHTS) -> dict:
     H, F, d = cfg.hidden, cfg.ffn, cfg.head_dim
     s = WEIGHT_SIGMA
+
+    def gain(slot, n):
+        if cfg.gain_sigma > 0:
+            return gain_bf16(seed, _tid(l, slot), n, cfg.gain_sigma)
+        return ones_bf16(n)
+
     w = {
-        "attn_norm": ones_bf16(H),
+        "attn_norm": gain("attn_norm", H),
         "wq": normal_bf16(seed, _tid(l, "wq"), (cfg.q_dim, H), s),
         "wk": normal_bf16(seed, _tid(l, "wk"), (cfg.kv_dim, H), s),
         "wv": normal_bf16(seed, _tid(l, "wv"), (cfg.kv_dim, H), s),
-        "q_norm": ones_bf16(d) if cfg.qk_norm else None,
-        "k_norm": ones_bf16(d) if cfg.qk_norm else None,
+        "q_norm": gain("q_norm", d) if cfg.qk_norm else None,
+        "k_norm": gain("k_norm", d) if cfg.qk_norm else None,
         "wo": normal_bf16(seed, _tid(l, "wo"), (H, cfg.q_dim), s),
-        "ffn_norm": ones_bf16(H),
+        "ffn_norm": gain("ffn_norm", H),
         "w_gate": normal_bf16(seed, _tid(l, "w_gate"), (F, H), s),
         "w_up": normal_bf16(seed, _tid(l, "w_up"), (F, H), s),
         "w_down": normal_bf16(seed, _tid(l, "w_down"), (H, F), s),
@@ -240,7 +259,9 @@ def layer_weights(cfg: ModelConfig, l: int, seed: int = SEED_WEIGHTS) -> dict:
 
 def model_weights(cfg: ModelConfig, seed: int = SEED_WEIGHTS) -> ModelWeights:
     embed = normal_bf16(seed, 0, (cfg.vocab, cfg.hidden), WEIGHT_SIGMA)
-    mw = ModelWeights(embed=embed, final_norm=ones_bf16(cfg.hidden))
+    fnorm = (gain_bf16(seed, 1, cfg.hidden, cfg.gain_sigma) if cfg.gain_sigma > 0
+             else ones_bf16(cfg.hidden))
+    mw = ModelWeights(embed=embed, final_norm=fnorm)
     mw.layers = [layer_weights(cfg, l, seed) for l in range(cfg.n_layers)]
     return mw
 

@@ -21,6 +21,7 @@
  *                       n[2j+1] = sqrt(-2 ln u(2j)) * sin(2 pi u(2j+1))
  *   bf16 value        sigma * n  -> nearest float -> bfloat16 by
  *                     round-to-nearest-even on the upper 16 bits
+ *   gain value        1 + sigma * n -> nearest float -> bfloat16 (same rounding)
  *   token id          r(c) mod n_vocab
  *
  * Every element depends only on (seed, tid, element index), so a tensor can
@@ -117,6 +118,13 @@ void synth_kv_prefill_bf16(uint64_t seed, uint64_t tid, int n_heads, int max_pos
 /* Uniform token ids in [0, n_vocab): element c of tensor (seed, tid). */
 void synth_tokens(uint64_t seed, uint64_t tid, int64_t n, int64_t n_vocab, int32_t *out) {
     for (int64_t c = 0; c < n; ++c) out[c] = (int32_t)(synth_raw(seed, tid, (uint64_t)c) % (uint64_t)n_vocab);
+}
+
+/* Norm gains 1 + sigma * n as bfloat16 bits, n the standard normal element c of
+ * tensor (seed, tid): the seeded non-unit gains of the parity tests. */
+void synth_gain_bf16(uint64_t seed, uint64_t tid, int64_t n, double sigma, uint16_t *out) {
+    uint64_t key = sm_key(seed, tid);
+    for (int64_t k = 0; k < n; ++k) out[k] = f32_to_bf16_bits((float)(1.0 + sigma * sm_normal(key, k)));
 }
 
 /* Fill with a constant bfloat16 bit pattern (used for norm gains = 1.0). */

@@ -12,6 +12,17 @@ import synthetic as S
 ATOL = 3e-2
 RTOL = 1e-2
 
+# Parity cases run with seeded non-unit norm gains (1 + N(0, GAINS), a different
+# vector per norm), so a kernel that dropped, swapped or misplaced a gain, or
+# applied the q/k norm after RoPE, disagrees with the oracle. The workload
+# configurations themselves keep the 1.0 gains they are defined with.
+GAINS = 0.25
+
+
+def with_gains(cfg):
+    from dataclasses import replace
+    return replace(cfg, gain_sigma=GAINS)
+
 
 def inputs(cfg, n_pos=None):
     w = S.model_weights(cfg)
@@ -60,16 +71,59 @@ def gpu_run(plan, cfg, k, v, prompt, start_pos, n_new, want_logits=True, split_a
             vc.view(torch.int16).cpu().numpy().view(np.uint16))
 
 
-def assert_parity(g_tokens, g_logits, ref, what=""):
-    """Greedy tokens exact; logits within tolerance, with diagnostics on failure."""
-    if g_logits is not None:
-        err = np.abs(g_logits - ref.logits)
-        bound = ATOL + RTOL * np.abs(ref.logits)
-        bad = err > bound
-        assert not np.isnan(g_logits).any(), f"{what}: NaN logits"
-        assert not bad.any(), (f"{what}: {int(bad.sum())} logits out of tolerance, max err "
-                               f"{float(err.max()):.3e}")
-    if not np.array_equal(g_tokens, ref.tokens):
-        i = int(np.nonzero(g_tokens != ref.tokens)[0][0])
-        raise AssertionError(f"{what}: token mismatch at output {i}: gpu {g_tokens[i]} oracle "
-                             f"{ref.tokens[i]}; oracle top-2 gaps {ref.gaps.tolist()}")
+def check_parity(g_tokens, g_logits, cfg, w, k, v, prompt, start_pos, n_new, what="",
+                 qweights=None, envelope=False):
+    """Element-by-element parity of a GPU decode with the oracle.
+
+    The oracle is run on the GPU's own token history (teacher forcing), so every
+    step compares the two on the same inputs. Up to the first step where the
+    oracle would choose another token, that history is the oracle's own
+    free-running one (causality), so this also checks that the two free-running
+    streams agree up to there. A step where the oracle's choice differs from the
+    GPU's is allowed only at a near-tie: the oracle's top-2 gap below tau, the
+    largest logit deviation of the oracle built with another FP32 summation
+    order (an equally valid implementation) at that step. Logits must lie within
+    |gpu - oracle| <= ATOL + RTOL |oracle| at every step; with ``envelope``
+    (deep models, where summation order alone moves logits past that bound)
+    within that plus 1.5 tau, with the mean error within twice the reordered
+    oracle's mean deviation. Returns the facts for the report."""
+    prompt = np.asarray(prompt, np.int32)
+    n_prompt = prompt.size
+    steps = n_prompt - 1 + n_new
+    g_tokens = np.asarray(g_tokens)
+    force = g_tokens[:-1] if n_new > 1 else None
+    kk, vv = k.copy(), v.copy()
+    ref = oracle.decode(cfg, w, kk, vv, prompt, start_pos, n_new, force_tokens=force, qweights=qweights)
+    assert g_logits is not None and g_logits.shape == ref.logits.shape
+    assert not np.isnan(g_logits).any(), f"{what}: NaN logits"
+    out_steps = np.arange(n_prompt - 1, steps)
+    choice = ref.logits[out_steps].argmax(axis=1)               # lowest index on ties
+    differ = np.nonzero(choice != g_tokens)[0]
+    tau = None
+    if envelope or len(differ):
+        alt = oracle.decode(cfg, w, k.copy(), v.copy(), prompt, start_pos, n_new, force_tokens=force,
+                            qweights=qweights, variant="alt")
+        dev = np.abs(alt.logits - ref.logits)
+        tau = dev.max(axis=1)
+    err = np.abs(g_logits - ref.logits)
+    bound = ATOL + RTOL * np.abs(ref.logits)
+    if envelope:
+        bound = bound + 1.5 * tau[:, None]
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {int(bad.sum())} logits out of tolerance, max err "
+                           f"{float(err.max()):.3e}" + (f", max tau {float(tau.max()):.3e}" if envelope else ""))
+    if envelope:
+        assert err.mean() <= 2.0 * dev.mean() + 1e-3, (f"{what}: mean error {err.mean():.3e} above twice "
+                                                       f"the reordered oracle's {dev.mean():.3e}")
+    for i in differ:
+        s = n_prompt - 1 + i
+        assert ref.gaps[s] < tau[s], (f"{what}: token differs at output {i} where the oracle's top-2 "
+                                      f"gap {ref.gaps[s]:.4f} is not below tau {tau[s]:.4f}")
+    first = int(differ[0]) if len(differ) else None
+    facts = {"what": what, "first_difference": first, "steps": n_new,
+             "gap_at_first": None if first is None else float(ref.gaps[n_prompt - 1 + first]),
+             "tau_at_first": None if first is None else float(tau[n_prompt - 1 + first]),
+             "n_differ": int(len(differ)), "max_err": float(err.max()),
+             "frac_within_strict": float(np.mean(err <= ATOL + RTOL * np.abs(ref.logits)))}
+    print(facts)
+    return facts, ref, kk, vv

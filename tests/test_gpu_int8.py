@@ -3,8 +3,9 @@
 The plan quantizes every GEMV matrix per output row on the device
 (tiles_quantize_rows_int8). Its codes and scales must equal the oracle's
 quantizer bit for bit, because a code is an integer decided in FP32 on both
-sides. The decoder is then held to the same bars as the BF16 path: strict
-tolerance where the depth allows it, the measured noise floor at full depth.
+sides. The decoder is then held to the same bars as the BF16 path
+(gpu_helpers.check_parity): strict tolerance where the depth allows it, the
+measured envelope at full depth, tokens identical up to the first near-tie.
 """
 from dataclasses import replace
 
@@ -13,7 +14,7 @@ import pytest
 
 import oracle
 import synthetic as S
-from gpu_helpers import assert_parity, gpu_run, inputs
+from gpu_helpers import GAINS, check_parity, gpu_run, inputs, with_gains
 
 pytestmark = pytest.mark.gpu
 
@@ -56,16 +57,15 @@ def test_device_quantization_equals_oracle_bit_for_bit(tsp, shape):
 
 
 def test_tiny_int8_matches_int8_oracle_and_is_bitwise_across_schedulers(tsp):
-    cfg = S.CONFIGS["tiny"]
+    cfg = with_gains(S.CONFIGS["tiny"])
     w, k, v, prompt = inputs(cfg, n_pos=0)
     qw = oracle.quantize_model(w)
-    ref = _oracle_q8(cfg, w, qw, k, v, prompt, 0, cfg.n_new)
     outs = []
     for sched in (2, 1, 0):
         plan = _plan(tsp, cfg, w, scheduler=sched)
         outs.append(gpu_run(plan, cfg, k, v, prompt, 0, cfg.n_new))
         plan.close()
-    assert_parity(outs[0][0], outs[0][1], ref, "tiny int8")
+    check_parity(outs[0][0], outs[0][1], cfg, w, k, v, prompt, 0, cfg.n_new, "tiny int8", qweights=qw)
     for o in outs[1:]:
         assert np.array_equal(o[0], outs[0][0])
         assert np.array_equal(o[1].view(np.uint32), outs[0][1].view(np.uint32))
@@ -73,9 +73,10 @@ def test_tiny_int8_matches_int8_oracle_and_is_bitwise_across_schedulers(tsp):
 
 VARIANTS = {
     "d128_g8_qknorm": replace(S.CONFIGS["tiny"], name="v1", head_dim=128, n_q_heads=8,
-                              n_kv_heads=1, qk_norm=True, rope_theta=1e6, rms_eps=1e-6),
+                              n_kv_heads=1, qk_norm=True, rope_theta=1e6, rms_eps=1e-6,
+                              gain_sigma=GAINS),
     "g2_cache": replace(S.CONFIGS["tiny"], name="v3", start_pos=150, n_prompt=3, n_new=20,
-                        max_pos=200),
+                        max_pos=200, gain_sigma=GAINS),
 }
 
 
@@ -84,16 +85,17 @@ def test_int8_variants_match_int8_oracle(tsp, name):
     cfg = VARIANTS[name]
     w, k, v, prompt = inputs(cfg)
     prompt = prompt[: cfg.n_prompt]
-    ref = _oracle_q8(cfg, w, oracle.quantize_model(w), k, v, prompt, cfg.start_pos, cfg.n_new)
     plan = _plan(tsp, cfg, w)
     toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, cfg.n_new)
-    assert_parity(toks, logits, ref, name + " int8")
+    check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new, name + " int8",
+                 qweights=oracle.quantize_model(w))
     plan.close()
 
 
 # long contexts: the kernel instances with the tensor-core attention path
 MMA = {
-    "d64_g2": replace(S.CONFIGS["tiny"], name="m1", start_pos=955, n_prompt=2, n_new=24, max_pos=1000),
+    "d64_g2": replace(S.CONFIGS["tiny"], name="m1", start_pos=955, n_prompt=2, n_new=24, max_pos=1000,
+                      gain_sigma=GAINS),
     "d128_g8_qknorm": replace(VARIANTS["d128_g8_qknorm"], name="m3", start_pos=490, n_prompt=2,
                               n_new=24, max_pos=520),
 }
@@ -104,10 +106,10 @@ def test_int8_with_tensor_core_attention_matches_int8_oracle(tsp, name):
     cfg = MMA[name]
     w, k, v, prompt = inputs(cfg)
     prompt = prompt[: cfg.n_prompt]
-    ref = _oracle_q8(cfg, w, oracle.quantize_model(w), k, v, prompt, cfg.start_pos, cfg.n_new)
     plan = _plan(tsp, cfg, w, kv_splits=2)
     toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, cfg.n_new)
-    assert_parity(toks, logits, ref, name + " int8, tensor-core attention")
+    check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new,
+                 name + " int8, tensor-core attention", qweights=oracle.quantize_model(w))
     plan.close()
 
 
@@ -121,20 +123,19 @@ def test_int8_rejects_rows_not_a_multiple_of_16(tsp):
 
 @pytest.mark.parametrize("name", ["llama1b", "qwen3_0_6b", "llama1b_long"])
 def test_int8_full_width_one_layer_slice_strict_tolerance(tsp, name):
-    cfg = replace(S.CONFIGS[name], n_layers=1)
+    cfg = replace(S.CONFIGS[name], n_layers=1, gain_sigma=GAINS)
     n_new = 8
     w, k, v, prompt = inputs(cfg)
-    ref = _oracle_q8(cfg, w, oracle.quantize_model(w), k, v, prompt, cfg.start_pos, n_new)
     plan = _plan(tsp, cfg, w)
     toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, n_new)
-    assert_parity(toks, logits, ref, name + " int8 one layer")
+    check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, n_new, name + " int8 one layer",
+                 qweights=oracle.quantize_model(w))
     plan.close()
 
 
-def test_int8_full_depth_within_noise_floor(tsp):
-    """Llama-1B shape at full depth, every logit of 32 steps, teacher-forced:
-    the same noise-floor bar as the BF16 path, against the INT8 oracle and its
-    other-summation-order build."""
+def test_int8_full_depth_free_running_matches_int8_oracle_up_to_first_near_tie(tsp):
+    """Llama-1B shape at full depth, 32 free-running steps: the same bar as the
+    BF16 path, against the INT8 oracle and its reordered-summation build."""
     cfg = S.CONFIGS["llama1b"]
     n_new = 32
     w, k, v, prompt = inputs(cfg)
@@ -142,13 +143,8 @@ def test_int8_full_depth_within_noise_floor(tsp):
     plan = _plan(tsp, cfg, w)
     toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, n_new)
     plan.close()
-    force = toks[:-1]
-    ref = _oracle_q8(cfg, w, qw, k, v, prompt, cfg.start_pos, n_new, force=force)
-    alt = _oracle_q8(cfg, w, qw, k, v, prompt, cfg.start_pos, n_new, force=force, variant="alt")
-    noise = np.abs(alt.logits - ref.logits).max(axis=1)
-    err = np.abs(logits - ref.logits)
-    bound = 3e-2 + 1e-2 * np.abs(ref.logits) + 1.5 * noise[:, None]
-    assert not np.isnan(logits).any()
-    assert (err <= bound).all(), (f"{int((err > bound).sum())} logits beyond the noise floor; "
-                                  f"max err {err.max():.3e}, max noise {noise.max():.3e}")
-    assert err.mean() <= 2.0 * np.abs(alt.logits - ref.logits).mean() + 1e-3
+    facts, ref, *_ = check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, n_new,
+                                  "llama1b int8 full depth", qweights=qw, envelope=True)
+    free = _oracle_q8(cfg, w, qw, k, v, prompt, cfg.start_pos, n_new)
+    d = n_new if facts["first_difference"] is None else facts["first_difference"]
+    assert np.array_equal(free.tokens[:d], toks[:d])

@@ -1,8 +1,11 @@
 """GPU parity: the persistent kernel against the CPU oracle, through the C ABI.
 
-Greedy tokens must be identical; logits within |err| <= 3e-2 + 1e-2 |oracle|;
-every run bit-identical to every other run, across both schedulers, across a
-run split into two calls, and across launches of at most 64 steps.
+Every logit within |err| <= 3e-2 + 1e-2 |oracle| of the oracle run on the same
+token history; greedy tokens identical, except at a step whose oracle top-2 gap
+is below the measured FP32-reordering deviation (a near-tie, see
+gpu_helpers.check_parity); norm gains seeded non-unit; every run bit-identical
+to every other run, across the schedulers, across a run split into two calls,
+and across launches of at most 64 steps.
 """
 from dataclasses import replace
 
@@ -10,7 +13,7 @@ import numpy as np
 import pytest
 
 import synthetic as S
-from gpu_helpers import assert_parity, gpu_run, inputs, oracle_run
+from gpu_helpers import GAINS, check_parity, gpu_run, inputs, with_gains
 
 pytestmark = pytest.mark.gpu
 
@@ -33,18 +36,17 @@ def _plan(tsp, cfg, w, **opts):
 # ------------------------------------------------------------------ tiny: full coverage
 @pytest.fixture(scope="module")
 def tiny(tsp):
-    cfg = S.CONFIGS["tiny"]
+    cfg = with_gains(S.CONFIGS["tiny"])
     w, k, v, prompt = inputs(cfg, n_pos=0)
-    ref, rk, rv = oracle_run(cfg, w, k, v, prompt, 0, cfg.n_new)
-    return cfg, w, k, v, prompt, ref, rk, rv
+    return cfg, w, k, v, prompt
 
 
 @pytest.mark.parametrize("scheduler", [0, 1, 2], ids=["waves", "counters", "flags"])
 def test_tiny_prompt_then_decode_matches_oracle(tsp, tiny, scheduler):
-    cfg, w, k, v, prompt, ref, rk, rv = tiny
+    cfg, w, k, v, prompt = tiny
     plan = _plan(tsp, cfg, w, scheduler=scheduler)
     toks, logits, kc, vc = gpu_run(plan, cfg, k, v, prompt, 0, cfg.n_new)
-    assert_parity(toks, logits, ref, "tiny")
+    _, _, rk, rv = check_parity(toks, logits, cfg, w, k, v, prompt, 0, cfg.n_new, "tiny")
     # the cache the GPU wrote: every position of the run, close to the oracle's
     n = prompt.size - 1 + cfg.n_new
     gk = S.bf16_to_f32(kc[:, :, :n]).astype(np.float64)
@@ -64,7 +66,7 @@ def test_tiny_prompt_then_decode_matches_oracle(tsp, tiny, scheduler):
 
 
 def test_tiny_bitwise_reproducible_across_runs_and_schedulers(tsp, tiny):
-    cfg, w, k, v, prompt, ref, *_ = tiny
+    cfg, w, k, v, prompt = tiny
     outs = []
     for sched in (0, 1, 2, 1, 2, 0):
         plan = _plan(tsp, cfg, w, scheduler=sched)
@@ -77,7 +79,7 @@ def test_tiny_bitwise_reproducible_across_runs_and_schedulers(tsp, tiny):
 
 
 def test_tiny_split_run_equals_one_run_bitwise(tsp, tiny):
-    cfg, w, k, v, prompt, ref, *_ = tiny
+    cfg, w, k, v, prompt = tiny
     plan = _plan(tsp, cfg, w)
     one = gpu_run(plan, cfg, k, v, prompt, 0, cfg.n_new)
     two = gpu_run(plan, cfg, k, v, prompt, 0, cfg.n_new, split_at=prompt.size + 5)
@@ -87,13 +89,12 @@ def test_tiny_split_run_equals_one_run_bitwise(tsp, tiny):
 
 
 def test_tiny_more_than_64_steps_uses_several_launches(tsp):
-    cfg = S.CONFIGS["tiny"]
+    cfg = with_gains(S.CONFIGS["tiny"])
     w, k, v, prompt = inputs(cfg, n_pos=0)
     n_new = 70                                  # 31 + 70 = 101 steps -> 2 launches
-    ref, *_ = oracle_run(cfg, w, k, v, prompt, 0, n_new)
     plan = _plan(tsp, cfg, w)
     toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, 0, n_new)
-    assert_parity(toks, logits, ref, "tiny 101 steps")
+    check_parity(toks, logits, cfg, w, k, v, prompt, 0, n_new, "tiny 101 steps")
     plan.close()
 
 
@@ -101,13 +102,14 @@ def test_tiny_more_than_64_steps_uses_several_launches(tsp):
 VARIANTS = {
     # head_dim 128, GQA group 8, q/k norm: the Qwen3 attention path
     "d128_g8_qknorm": replace(S.CONFIGS["tiny"], name="v1", head_dim=128, n_q_heads=8,
-                              n_kv_heads=1, qk_norm=True, rope_theta=1e6, rms_eps=1e-6),
+                              n_kv_heads=1, qk_norm=True, rope_theta=1e6, rms_eps=1e-6,
+                              gain_sigma=GAINS),
     # no GQA sharing, llama3 RoPE scaling, ragged rows (hidden not a multiple of 256)
     "g1_llama3": replace(S.CONFIGS["tiny"], name="v2", n_q_heads=2, n_kv_heads=2, hidden=264,
-                         ffn=776, vocab=1000, rope_scaling=True, rope_theta=5e5),
+                         ffn=776, vocab=1000, rope_scaling=True, rope_theta=5e5, gain_sigma=GAINS),
     # head_dim 64, group 2, cached positions crossing several KV blocks
     "g2_cache": replace(S.CONFIGS["tiny"], name="v3", start_pos=150, n_prompt=3, n_new=20,
-                        max_pos=200),
+                        max_pos=200, gain_sigma=GAINS),
 }
 
 
@@ -117,10 +119,9 @@ def test_variants_match_oracle(tsp, name, scheduler):
     cfg = VARIANTS[name]
     w, k, v, prompt = inputs(cfg)
     prompt = prompt[: cfg.n_prompt]
-    ref, *_ = oracle_run(cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new)
     plan = _plan(tsp, cfg, w, scheduler=scheduler)
     toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, cfg.n_new)
-    assert_parity(toks, logits, ref, name)
+    check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new, name)
     plan.close()
 
 
@@ -131,9 +132,10 @@ def test_variants_match_oracle(tsp, name, scheduler):
 # both paths, and the last block runs past max_pos in "d64_g2" (the tiled copy
 # fills those rows with zeros).
 MMA = {
-    "d64_g2": replace(S.CONFIGS["tiny"], name="m1", start_pos=955, n_prompt=2, n_new=24, max_pos=1000),
+    "d64_g2": replace(S.CONFIGS["tiny"], name="m1", start_pos=955, n_prompt=2, n_new=24, max_pos=1000,
+                      gain_sigma=GAINS),
     "d64_g1": replace(S.CONFIGS["tiny"], name="m2", n_q_heads=2, n_kv_heads=2, start_pos=1010,
-                      n_prompt=2, n_new=12, max_pos=1030),
+                      n_prompt=2, n_new=12, max_pos=1030, gain_sigma=GAINS),
     "d128_g8_qknorm": replace(VARIANTS["d128_g8_qknorm"], name="m3", start_pos=490, n_prompt=2,
                               n_new=24, max_pos=520),
     "d128_g2_qknorm": replace(VARIANTS["d128_g8_qknorm"], name="m4", n_q_heads=4, n_kv_heads=2,
@@ -151,12 +153,12 @@ def test_tensor_core_attention_matches_oracle(tsp, name):
     prompt = prompt[: cfg.n_prompt]
     k[:, :, cfg.start_pos:, :] = 0x7FC0       # BF16 NaN
     v[:, :, cfg.start_pos:, :] = 0x7FC0
-    ref, kref, vref = oracle_run(cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new)
     plan = _plan(tsp, cfg, w, kv_splits=2)
     toks, logits, kc, vc = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, cfg.n_new)
     plan.close()
     assert not np.isnan(logits).any()
-    assert_parity(toks, logits, ref, name + " tensor-core attention")
+    _, _, kref, vref = check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new,
+                                    name + " tensor-core attention")
     # the cache: rows written in the run close to the oracle's, the NaN rows after untouched
     end = cfg.start_pos + cfg.n_prompt - 1 + cfg.n_new
     for got, want in ((kc, kref), (vc, vref)):
@@ -171,10 +173,9 @@ def test_few_ctas_and_small_ring(tsp):
     cfg = VARIANTS["g2_cache"]
     w, k, v, prompt = inputs(cfg)
     prompt = prompt[: cfg.n_prompt]
-    ref, *_ = oracle_run(cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new)
     plan = _plan(tsp, cfg, w, n_ctas=7, ring_slots=2, kv_splits=3)
     toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, cfg.n_new)
-    assert_parity(toks, logits, ref, "7 CTAs")
+    check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new, "7 CTAs")
     plan.close()
 
 
@@ -183,7 +184,7 @@ def test_few_ctas_and_small_ring(tsp):
 def test_l2_prefetch_warp_leaves_results_bit_identical(tsp, name, gbs):
     """The L2 prefetch warp only warms the cache: tokens, logits and the cache
     it writes are bit-identical with and without it, paced or not."""
-    cfg = S.CONFIGS["tiny"] if name == "tiny" else VARIANTS[name]
+    cfg = with_gains(S.CONFIGS["tiny"]) if name == "tiny" else VARIANTS[name]
     w, k, v, prompt = inputs(cfg)
     prompt = prompt[: cfg.n_prompt]
     outs = []
@@ -199,7 +200,7 @@ def test_l2_prefetch_warp_leaves_results_bit_identical(tsp, name, gbs):
 # ------------------------------------------------------------------ edge cases
 def test_edges_empty_and_single_step(tsp, tiny):
     import torch
-    cfg, w, k, v, prompt, *_ = tiny
+    cfg, w, k, v, prompt = tiny
     plan = _plan(tsp, cfg, w)
     kc = tsp.to_device_bf16(k)
     vc = tsp.to_device_bf16(v)
@@ -208,21 +209,19 @@ def test_edges_empty_and_single_step(tsp, tiny):
     plan.decode(kc, vc, p1, 0, 0, out)                    # zero steps: nothing happens
     plan.check()
     assert int(out[0]) == -1 and not kc.view(torch.int16).any()
-    ref, *_ = oracle_run(cfg, w, k, v, np.array([5], np.int32), 0, 1)
     toks, logits, *_ = gpu_run(plan, cfg, k, v, np.array([5], np.int32), 0, 1)
-    assert_parity(toks, logits, ref, "one step")
+    check_parity(toks, logits, cfg, w, k, v, np.array([5], np.int32), 0, 1, "one step")
     # last position of the cache
-    ref, *_ = oracle_run(cfg, w, *S.kv_prefill(cfg, n_pos=cfg.max_pos - 1),
-                         np.array([9], np.int32), cfg.max_pos - 1, 1)
-    toks, logits, *_ = gpu_run(plan, cfg, *S.kv_prefill(cfg, n_pos=cfg.max_pos - 1),
-                               np.array([9], np.int32), cfg.max_pos - 1, 1)
-    assert_parity(toks, logits, ref, "last cache position")
+    kl, vl = S.kv_prefill(cfg, n_pos=cfg.max_pos - 1)
+    toks, logits, *_ = gpu_run(plan, cfg, kl, vl, np.array([9], np.int32), cfg.max_pos - 1, 1)
+    check_parity(toks, logits, cfg, w, kl, vl, np.array([9], np.int32), cfg.max_pos - 1, 1,
+                 "last cache position")
     plan.close()
 
 
 def test_errors_are_reported_not_faulted(tsp, tiny):
     import torch
-    cfg, w, k, v, prompt, *_ = tiny
+    cfg, w, k, v, prompt = tiny
     plan = _plan(tsp, cfg, w)
     kc = tsp.to_device_bf16(k)
     vc = tsp.to_device_bf16(v)
@@ -237,8 +236,7 @@ def test_errors_are_reported_not_faulted(tsp, tiny):
     assert plan.status() == 0                                # status word was cleared
     # the context is still usable
     toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt[:4], 0, 2)
-    ref, *_ = oracle_run(cfg, w, k, v, prompt[:4], 0, 2)
-    assert_parity(toks, logits, ref, "after error")
+    check_parity(toks, logits, cfg, w, k, v, prompt[:4], 0, 2, "after error")
     plan.close()
 
 
@@ -250,7 +248,7 @@ def test_a_wait_that_runs_out_is_reported_and_the_context_stays_usable(tsp, tiny
     correctly on the same context."""
     import time
     import torch
-    cfg, w, k, v, prompt, *_ = tiny
+    cfg, w, k, v, prompt = tiny
     bad = _plan(tsp, cfg, w, scheduler=scheduler, timeout_ms=50, flags=tsp.FLAG_INJECT_STALL)
     kc, vc = tsp.to_device_bf16(k), tsp.to_device_bf16(v)
     out = torch.zeros(4, dtype=torch.int32, device="cuda")
@@ -261,33 +259,32 @@ def test_a_wait_that_runs_out_is_reported_and_the_context_stays_usable(tsp, tiny
     bad.close()
     good = _plan(tsp, cfg, w, scheduler=scheduler)
     toks, logits, *_ = gpu_run(good, cfg, k, v, prompt[:4], 0, 2)
-    ref, *_ = oracle_run(cfg, w, k, v, prompt[:4], 0, 2)
-    assert_parity(toks, logits, ref, "after a timed-out launch")
+    check_parity(toks, logits, cfg, w, k, v, prompt[:4], 0, 2, "after a timed-out launch")
     good.close()
 
 
 def test_host_buffer_entry_point(tsp, tiny):
-    cfg, w, k, v, prompt, ref, *_ = tiny
+    cfg, w, k, v, prompt = tiny
     plan = _plan(tsp, cfg, w)
     kc = tsp.to_device_bf16(k)
     vc = tsp.to_device_bf16(v)
     toks = np.zeros(cfg.n_new, np.int32)
     logits = np.zeros((prompt.size - 1 + cfg.n_new, cfg.vocab), np.float32)
     plan.decode_host(kc, vc, prompt.astype(np.int32), 0, cfg.n_new, toks, logits)
-    assert_parity(toks, logits, ref, "host buffers")
+    check_parity(toks, logits, cfg, w, k, v, prompt, 0, cfg.n_new, "host buffers")
     plan.close()
 
 
 # ------------------------------------------------------------------ full-size shapes
-# Deep random-weight decoders amplify any change of FP32 summation order: the
-# oracle built with another (equally valid) GEMV order moves its own logits by
-# 0.06-0.09 and changes greedy tokens at near-ties over 64 steps of the
-# Llama-1B shape. The benchmark spec's tolerance therefore holds at shallow depth
-# (checked on one-layer slices of every full-width shape, below), and at full
-# depth the GPU is held to the measured noise floor: teacher-forced on its own
-# tokens, each logit within 3e-2 + 1e-2|oracle| + 1.5 x the oracle-vs-oracle
-# deviation of that step, each token the oracle's argmax or within twice that
-# deviation of it.
+# One-layer slices of every full-width shape hold the benchmark spec's tolerance
+# (tokens, and every logit within 3e-2 + 1e-2 |oracle|). At full depth a deep
+# random-weight decoder amplifies any change of FP32 summation order: the
+# oracle built with another, equally valid GEMV order moves its own logits by
+# 0.05-0.15 per step, past that bound for thousands of logits, and the GPU's
+# deviation is the same size. So the full-depth runs are held to the measured
+# envelope (bound + 1.5 tau per step, mean error within twice the reordered
+# oracle's), and their free-running token streams to the oracle's up to the
+# first near-tie.
 SLICES = ["llama1b", "qwen3_0_6b", "qwen3_4b", "llama1b_long"]
 
 
@@ -295,13 +292,12 @@ SLICES = ["llama1b", "qwen3_0_6b", "qwen3_4b", "llama1b_long"]
 def test_full_width_one_layer_slice_strict_tolerance(tsp, name):
     """Full width (hidden, heads, FFN, vocab, cached positions) at one layer:
     greedy tokens exact and every logit within the benchmark spec's tolerance."""
-    cfg = replace(S.CONFIGS[name], n_layers=1)
+    cfg = replace(S.CONFIGS[name], n_layers=1, gain_sigma=GAINS)
     n_new = 8
     w, k, v, prompt = inputs(cfg)
-    ref, *_ = oracle_run(cfg, w, k, v, prompt, cfg.start_pos, n_new)
     plan = _plan(tsp, cfg, w)
     toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, n_new)
-    assert_parity(toks, logits, ref, name + " one layer")
+    check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, n_new, name + " one layer")
     plan.close()
 
 
@@ -309,9 +305,13 @@ FULL = [("llama1b", 64), ("qwen3_0_6b", 64), ("qwen3_4b", 16), ("llama1b_long", 
 
 
 @pytest.mark.parametrize("name,n_new", FULL, ids=[f[0] for f in FULL])
-def test_full_depth_within_noise_floor(tsp, name, n_new):
+def test_full_depth_free_running_matches_oracle_up_to_first_near_tie(tsp, name, n_new):
     """The workload shapes at full size, in the launch configuration the
-    benchmark times, every logit of every step, teacher-forced."""
+    benchmark times: the GPU and the oracle both decode freely; their token
+    streams must be identical up to the first step where the oracle's top-2
+    gap is below the measured reordering deviation tau (checked on the
+    free-running oracle itself), and every logit up to there, and after it on
+    the GPU's own history, within the envelope. Bit-reproducible across runs."""
     import oracle
     cfg = S.CONFIGS[name]
     w, k, v, prompt = inputs(cfg)
@@ -321,22 +321,13 @@ def test_full_depth_within_noise_floor(tsp, name, n_new):
     plan.close()
     assert np.array_equal(again[0], toks)                         # bit-reproducible
     assert np.array_equal(again[1].view(np.uint32), logits.view(np.uint32))
-    force = toks[:-1]
-    ref, *_ = oracle_run(cfg, w, k, v, prompt, cfg.start_pos, n_new, force=force)
-    alt = oracle.decode(cfg, w, k.copy(), v.copy(), prompt, cfg.start_pos, n_new,
-                        force_tokens=force, variant="alt")
-    noise = np.abs(alt.logits - ref.logits).max(axis=1)          # per step
-    err = np.abs(logits - ref.logits)
-    bound = 3e-2 + 1e-2 * np.abs(ref.logits) + 1.5 * noise[:, None]
-    assert not np.isnan(logits).any()
-    assert (err <= bound).all(), (f"{name}: {int((err > bound).sum())} logits beyond the noise "
-                                  f"floor; max err {err.max():.3e}, max noise {noise.max():.3e}")
-    assert err.mean() <= 2.0 * np.abs(alt.logits - ref.logits).mean() + 1e-3
-    steps = prompt.size - 1 + n_new
-    out_steps = np.arange(prompt.size - 1, steps)
-    top = ref.logits[out_steps].max(axis=1)
-    chosen = ref.logits[out_steps, toks]
-    assert (chosen >= top - 2 * noise[out_steps]).all(), "a GPU token outside the noise band"
-    exact = float(np.mean(ref.logits[out_steps].argmax(axis=1) == toks))
-    print(f"{name}: argmax agreement {exact:.3f}, max|dlogit| {err.max():.3e}, "
-          f"oracle-vs-oracle {noise.max():.3e}")
+    facts, ref, *_ = check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, n_new,
+                                  name + " full depth", envelope=True)
+    # the free-running oracle: its stream is the GPU's up to the first difference
+    free = oracle.decode(cfg, w, k.copy(), v.copy(), prompt, cfg.start_pos, n_new)
+    d = n_new if facts["first_difference"] is None else facts["first_difference"]
+    s_d = prompt.size - 1 + min(d, n_new - 1)                    # the step that emits output d
+    assert np.array_equal(free.tokens[:d], toks[:d])
+    assert np.array_equal(free.logits[:s_d + 1].view(np.uint32), ref.logits[:s_d + 1].view(np.uint32))
+    if d < n_new:
+        assert free.tokens[d] != toks[d]

@@ -638,3 +638,192 @@ def test_verify_loop_emits_exactly_the_greedy_tokens(lively_model):
         pos += r.n_accepted + 1
         last = int(r.tokens[-1])
     assert out[:20] == g[:20].tolist()
+
+
+# ----------------------------------------------------------------- decoder wiring
+# The closed forms below read logits[j] = hf[j] for j < H: the tied embedding's
+# rows 0..H-1 are the unit vectors e_j, so the LM head hands back the final
+# normed vector itself, and every gain, rotation and softmax weight upstream is
+# visible in it. The input token's own row is a seeded N(0, 1) vector.
+def _rb(a):
+    """FP32 -> BF16 round to nearest even, back as float64 (the R() of the definition)."""
+    return O.f32_from_bf16(O.bf16_from_f32(np.asarray(a, np.float32))).astype(np.float64)
+
+
+def _pow2_gain(n, shift):
+    """Gains 2^((i + shift) mod 5 - 2) in {1/4 .. 4}: exact in BF16, and two
+    vectors differ in every element unless their shifts agree mod 5."""
+    e = (np.arange(n) + shift) % 5 - 2
+    return O.bf16_from_f32((2.0 ** e).astype(np.float32))
+
+
+def _unit_rows_embedding(cfg, tok, rng):
+    H = cfg.hidden
+    E = np.zeros((cfg.vocab, H), np.uint16)
+    E[np.arange(H), np.arange(H)] = 0x3F80                          # e_j, value 1.0
+    E[tok] = O.bf16_from_f32(rng.standard_normal(H).astype(np.float32))
+    return E
+
+
+def _rms(x, eps):
+    return 1.0 / np.sqrt(np.mean(np.asarray(x, np.float64) ** 2) + eps)
+
+
+def test_decoder_norm_gains_route_to_their_own_step_attention_path(tiny_cfg):
+    """Each layer's attn_norm gain scales h, which reaches the residual through
+    v = Wv h (uniform attention: all keys zero), Wo a permutation; the FFN is
+    zero; the final gain scales hf. With distinct power-of-two gains per layer
+    and per norm, a dropped gain, attn_norm and ffn_norm swapped, one layer's
+    gain used for another, or the final gain dropped fails it."""
+    cfg = replace(tiny_cfg, n_layers=2)
+    rng = np.random.default_rng(31)
+    H, d, nkv, G = cfg.hidden, cfg.head_dim, cfg.n_kv_heads, cfg.n_q_heads // cfg.n_kv_heads
+    tok = H + 7
+    w = S.model_weights(cfg)
+    w.embed = _unit_rows_embedding(cfg, tok, rng)
+    w.final_norm = _pow2_gain(H, 3)
+    sel = rng.permutation(H)[: nkv * d]                            # v_g[j] = h[sel[g d + j]]
+    perm = rng.permutation(H)                                      # (Wo o)_j = o[perm[j]]
+    for l, lw in enumerate(w.layers):
+        lw["attn_norm"] = _pow2_gain(H, l)
+        lw["ffn_norm"] = _pow2_gain(H, l + 1)
+        lw["wq"] = np.zeros_like(lw["wq"])
+        lw["wk"] = np.zeros_like(lw["wk"])
+        wv = np.zeros_like(lw["wv"])
+        wv[np.arange(nkv * d), sel] = 0x3F80
+        lw["wv"] = wv
+        wo = np.zeros_like(lw["wo"])
+        wo[np.arange(H), perm] = 0x3F80
+        lw["wo"] = wo
+        for m in ("w_gate", "w_up", "w_down"):
+            lw[m] = np.zeros_like(lw[m])
+    P = 4
+    k = np.zeros((cfg.n_layers, nkv, cfg.max_pos, d), np.uint16)
+    v = np.zeros_like(k)
+    r = O.decode(cfg, w, k, v, np.array([tok], np.int32), P, 1)
+    # closed form: uniform softmax over P + 1 positions, cached values zero
+    p = np.float32(1.0) / np.float32(P + 1)
+    x = O.f32_from_bf16(w.embed[tok]).astype(np.float64)
+    for l in range(cfg.n_layers):
+        g = O.f32_from_bf16(_pow2_gain(H, l)).astype(np.float64)
+        h = _rb(x * _rms(x, cfg.rms_eps) * g)
+        vg = h[sel].reshape(nkv, d)
+        o = np.concatenate([_rb(np.float32(p) * vg[i // G].astype(np.float32)) for i in range(cfg.n_q_heads)])
+        x = _rb(x + o[perm])
+    gF = O.f32_from_bf16(_pow2_gain(H, 3)).astype(np.float64)
+    hf = _rb(x * _rms(x, cfg.rms_eps) * gF)
+    np.testing.assert_allclose(r.logits[0][:H], hf, rtol=2.0 ** -6, atol=1e-6)
+
+
+def test_decoder_norm_gains_route_to_their_own_step_ffn_path(tiny_cfg):
+    """Attention output zero; gate rows 0..H-1 the identity, up 2x the
+    identity, down a permutation: each layer adds R(silu(h2) * 2 h2) permuted,
+    h2 = R(rmsnorm(x) * g_ffn[l]). Distinct power-of-two gains catch a dropped
+    ffn_norm, ffn_norm and attn_norm swapped, or a wrong layer's gain."""
+    cfg = replace(tiny_cfg, n_layers=2)
+    rng = np.random.default_rng(32)
+    H, F = cfg.hidden, cfg.ffn
+    tok = H + 3
+    w = S.model_weights(cfg)
+    w.embed = _unit_rows_embedding(cfg, tok, rng)
+    w.final_norm = _pow2_gain(H, 4)
+    perm = rng.permutation(H)
+    eye_g = np.zeros((F, H), np.uint16)
+    eye_g[np.arange(H), np.arange(H)] = 0x3F80
+    eye_u = np.zeros((F, H), np.uint16)
+    eye_u[np.arange(H), np.arange(H)] = 0x4000                    # 2.0
+    down = np.zeros((H, F), np.uint16)
+    down[np.arange(H), perm] = 0x3F80
+    for l, lw in enumerate(w.layers):
+        lw["attn_norm"] = _pow2_gain(H, l + 2)
+        lw["ffn_norm"] = _pow2_gain(H, l)
+        lw["wo"] = np.zeros_like(lw["wo"])
+        lw["w_gate"], lw["w_up"], lw["w_down"] = eye_g, eye_u, down
+    k, v = S.kv_prefill(cfg, n_pos=3)
+    r = O.decode(cfg, w, k, v, np.array([tok], np.int32), 3, 1)
+    x = O.f32_from_bf16(w.embed[tok]).astype(np.float64)
+    for l in range(cfg.n_layers):
+        g = O.f32_from_bf16(_pow2_gain(H, l)).astype(np.float64)
+        h = _rb(x * _rms(x, cfg.rms_eps) * g)
+        a = _rb(h / (1 + np.exp(-h)) * 2 * h)
+        x = _rb(x + a[perm])
+    gF = O.f32_from_bf16(_pow2_gain(H, 4)).astype(np.float64)
+    hf = _rb(x * _rms(x, cfg.rms_eps) * gF)
+    np.testing.assert_allclose(r.logits[0][:H], hf, rtol=2.0 ** -6, atol=1e-6)
+
+
+def test_decoder_qk_norm_before_rope_and_both_rotated_at_the_position(tiny_cfg):
+    """q/k RMSNorm with distinct per-dimension gains, then RoPE at P, for q and
+    k alike. One hidden unit feeds dimension a of every q head and of KV head
+    0's k, and dimension a + d/2 of KV head 1's k; the cached keys (already
+    rotated) have components on a and a + d/2; cached values are unit vectors,
+    so the output of each q head is its softmax weights. Closed form per score:
+      q' = Q (cos t_a e_a + sin t_a e_{a+d/2}),   Q  = h_m / rms * g_q[a]
+      k0' = K0 (cos t_a e_a + sin t_a e_{a+d/2}), K0 = h_m / rms * g_k[a]
+      k1' = K1 (-sin t_a e_a + cos t_a e_{a+d/2}), K1 = h_m / rms * g_k[a + d/2]
+    (t_a = P w_a), so the new key's score is Q K0 / sqrt(d) for KV head 0 and
+    exactly 0 for KV head 1. Fails if the norm runs after RoPE (then g_q[a+d/2]
+    enters), if q_norm and k_norm are swapped, if k is rotated at another
+    position than q or not at all, or if q is rotated at another position."""
+    cfg = replace(tiny_cfg, n_layers=1, qk_norm=True, rms_eps=1e-6)
+    rng = np.random.default_rng(33)
+    H, d, nkv, G, nq = cfg.hidden, cfg.head_dim, cfg.n_kv_heads, cfg.n_q_heads // cfg.n_kv_heads, cfg.n_q_heads
+    half = d // 2
+    tok, a, P = H + 11, 5, 6
+    w = S.model_weights(cfg)
+    w.embed = _unit_rows_embedding(cfg, tok, rng)
+    x0 = O.f32_from_bf16(w.embed[tok]).astype(np.float64)
+    h = _rb(x0 * _rms(x0, cfg.rms_eps))                            # attn_norm gain 1
+    m = int(np.argmax(np.abs(h)))
+    lw = w.layers[0]
+    gq = np.full(d, 0x3F80, np.uint16)
+    gk = np.full(d, 0x3F80, np.uint16)
+    gq[a], gq[a + half] = O.bf16_from_f32(np.float32(0.5))[0], O.bf16_from_f32(np.float32(2.0))[0]
+    gk[a], gk[a + half] = O.bf16_from_f32(np.float32(0.25))[0], O.bf16_from_f32(np.float32(1.0))[0]
+    gk[0] = O.bf16_from_f32(np.float32(4.0))[0]                     # keeps g_k != g_q elementwise
+    lw["q_norm"], lw["k_norm"] = gq, gk
+    wq = np.zeros_like(lw["wq"])
+    wq[np.arange(nq) * d + a, m] = 0x3F80
+    wk = np.zeros_like(lw["wk"])
+    wk[0 * d + a, m] = 0x3F80
+    wk[1 * d + a + half, m] = 0x3F80
+    lw["wq"], lw["wk"], lw["wv"] = wq, wk, np.zeros_like(lw["wv"])
+    lw["wo"] = np.eye(H, nq * d, dtype=np.uint16) * np.uint16(0x3F80)
+    for mm in ("w_gate", "w_up", "w_down"):
+        lw[mm] = np.zeros_like(lw[mm])
+    k = np.zeros((1, nkv, cfg.max_pos, d), np.uint16)
+    v = np.zeros_like(k)
+    alpha = O.bf16_from_f32((0.5 * np.cos(np.arange(P) * 1.3)).astype(np.float32))
+    beta = O.bf16_from_f32((0.5 * np.sin(np.arange(P) * 0.7 + 0.3)).astype(np.float32))
+    for g in range(nkv):
+        k[0, g, :P, a] = alpha
+        k[0, g, :P, a + half] = beta
+        v[0, g, np.arange(P), np.arange(P)] = 0x3F80                 # V_t = e_t
+    r = O.decode(cfg, w, k, v, np.array([tok], np.int32), P, 1)
+
+    # closed form
+    rms1 = 1.0 / np.sqrt(h[m] ** 2 / d + cfg.rms_eps)               # RMSNorm of h_m e_a over d
+    f = lambda b: float(O.f32_from_bf16(b)[0])
+    Q = h[m] * rms1 * f(gq[a])
+    K0 = h[m] * rms1 * f(gk[a])
+    K1 = h[m] * rms1 * f(gk[a + half])
+    om = cfg.rope_theta ** (-2.0 * a / d)
+    c, s = float(np.float32(np.cos(P * om))), float(np.float32(np.sin(P * om)))
+    q_a, q_b = _rb(Q * c), _rb(Q * s)
+    k_new = {0: (_rb(K0 * c), _rb(K0 * s)), 1: (_rb(-K1 * s), _rb(K1 * c))}
+    al, be = O.f32_from_bf16(alpha).astype(np.float64), O.f32_from_bf16(beta).astype(np.float64)
+    scale = 1.0 / np.sqrt(d)
+    o = np.zeros(nq * d)
+    for i in range(nq):
+        g = i // G
+        sc = np.append((q_a * al + q_b * be) * scale, (q_a * k_new[g][0] + q_b * k_new[g][1]) * scale)
+        pr = np.exp(sc - sc.max())
+        pr /= pr.sum()
+        o[i * d: i * d + P] = pr[:P]                                 # V_P = 0
+    assert abs(q_a * k_new[1][0] + q_b * k_new[1][1]) < 1e-2 * abs(Q * K1)
+    x1 = _rb(x0 + _rb(o))
+    hf = _rb(x1 * _rms(x1, cfg.rms_eps))
+    np.testing.assert_allclose(r.logits[0][:H], hf, rtol=2.0 ** -6, atol=1e-6)
+    # the new rows of the cache are the rotated, normed k (and v = 0)
+    for g in range(nkv):
+        np.testing.assert_allclose(O.f32_from_bf16(k[0, g, P, [a, a + half]]), np.ravel(k_new[g]), rtol=1e-6)

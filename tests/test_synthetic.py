@@ -73,3 +73,26 @@ def test_config_byte_counts_equal_the_arrays_they_count():
                    + qw.lm[0].nbytes + qw.lm[1].nbytes + w.final_norm.nbytes
                    + sum(a.nbytes for a in norms))
         assert cfg.weight_bytes(int8=True) == q_bytes
+
+
+def test_gains_default_to_one_and_are_seeded_distinct_vectors_when_asked():
+    """The workload configs keep every norm gain at 1.0; gain_sigma > 0 gives
+    each norm (per layer and slot, and the final one) its own seeded vector."""
+    base = S.CONFIGS["tiny"].with_workload(qk_norm=True)
+    w = S.model_weights(base)
+    for lw in w.layers:
+        for slot in ("attn_norm", "ffn_norm", "q_norm", "k_norm"):
+            assert (lw[slot] == S.BF16_ONE).all()
+    assert (w.final_norm == S.BF16_ONE).all()
+    g = S.model_weights(base.with_workload(gain_sigma=0.25))
+    vecs = [g.final_norm] + [lw[s] for lw in g.layers
+                             for s in ("attn_norm", "ffn_norm", "q_norm", "k_norm")]
+    f = [S.bf16_to_f32(v).astype(np.float64) for v in vecs]
+    allf = np.concatenate(f)
+    assert abs(allf.mean() - 1.0) < 0.02 and abs(allf.std() - 0.25) < 0.02
+    for i in range(len(f)):
+        for j in range(i + 1, len(f)):
+            n = min(len(f[i]), len(f[j]))
+            assert not np.array_equal(f[i][:n], f[j][:n])
+    # the matrices are the same with or without seeded gains
+    assert np.array_equal(g.layers[1]["wq"], w.layers[1]["wq"]) and np.array_equal(g.embed, w.embed)

@@ -13,8 +13,10 @@ has run every other test before it gets here.
 import numpy as np
 import pytest
 
+from dataclasses import replace
+
 import synthetic as S
-from gpu_helpers import ATOL, RTOL, inputs
+from gpu_helpers import inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -29,36 +31,53 @@ def tsp():
     return t
 
 
-def _run(tsp, plan, cfg, k, v, prompt, use_noalloc):
+def _run(tsp, plan, cfg, k, v, prompt, use_noalloc, n_new=None):
     import torch
+    n_new = cfg.n_new if n_new is None else n_new
     kc = tsp.to_device_bf16(k)
     vc = tsp.to_device_bf16(v)
-    steps = prompt.size - 1 + cfg.n_new
-    toks = torch.full((cfg.n_new,), -1, dtype=torch.int32, device="cuda")
+    steps = prompt.size - 1 + n_new
+    toks = torch.full((n_new,), -1, dtype=torch.int32, device="cuda")
     logits = torch.full((steps, cfg.vocab), float("nan"), dtype=torch.float32, device="cuda")
     dprompt = torch.from_numpy(np.ascontiguousarray(prompt, np.int32)).cuda()
     if use_noalloc:
-        plan.decode_noalloc(kc, vc, dprompt, cfg.start_pos, cfg.n_new, toks, logits)
+        plan.decode_noalloc(kc, vc, dprompt, cfg.start_pos, n_new, toks, logits)
     else:
-        plan.decode(kc, vc, dprompt, cfg.start_pos, cfg.n_new, toks, logits)
+        plan.decode(kc, vc, dprompt, cfg.start_pos, n_new, toks, logits)
     plan.check()
-    return toks.cpu().numpy(), logits.cpu().numpy()
+    return (toks.cpu().numpy(), logits.cpu().numpy(),
+            kc.view(torch.int16).cpu().numpy(), vc.view(torch.int16).cpu().numpy())
 
 
-@pytest.mark.parametrize("name", ["tiny", "g2_cache"])
-def test_noalloc_matches_regular_decode_twice(tsp, name):
-    from dataclasses import replace
-    cfg = S.CONFIGS["tiny"] if name == "tiny" else replace(
-        S.CONFIGS["tiny"], name="v3", start_pos=150, n_prompt=3, n_new=20, max_pos=200)
+CASES = {
+    # prompt then decode, one launch
+    "tiny": (S.CONFIGS["tiny"], None),
+    # cached positions across several KV blocks
+    "g2_cache": (replace(S.CONFIGS["tiny"], name="v3", start_pos=150, n_prompt=3, n_new=20,
+                         max_pos=200), None),
+    # 31 + 80 = 111 steps: two launches in one call, so the array is cleared
+    # again between launches of the same call
+    "tiny_two_launches": (S.CONFIGS["tiny"].with_workload(max_pos=128), 80),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_noalloc_equals_regular_decode_bitwise_twice(tsp, name):
+    """Same kernel, same inputs: tokens, logits and the caches written must be
+    bit-identical to tiles_decode's, on two calls in a row (the second finds
+    the array as the first left it)."""
+    cfg, n_new = CASES[name]
+    cfg = replace(cfg, gain_sigma=0.25)
     w, k, v, prompt = inputs(cfg, n_pos=cfg.start_pos)
     prompt = prompt[: cfg.n_prompt]
     plan = tsp.Plan(tsp.ModelDesc.from_config(cfg), tsp.upload_weights(w))
-    ref_toks, ref_logits = _run(tsp, plan, cfg, k, v, prompt, use_noalloc=False)
+    ref = _run(tsp, plan, cfg, k, v, prompt, use_noalloc=False, n_new=n_new)
+    assert not np.isnan(ref[1]).any()
     for _ in range(2):
-        toks, logits = _run(tsp, plan, cfg, k, v, prompt, use_noalloc=True)
-        assert np.array_equal(toks, ref_toks)
-        assert not np.isnan(logits).any()
-        assert (np.abs(logits - ref_logits) <= ATOL + RTOL * np.abs(ref_logits)).all()
+        got = _run(tsp, plan, cfg, k, v, prompt, use_noalloc=True, n_new=n_new)
+        assert np.array_equal(got[0], ref[0])
+        assert np.array_equal(got[1].view(np.uint32), ref[1].view(np.uint32))
+        assert np.array_equal(got[2], ref[2]) and np.array_equal(got[3], ref[3])
     plan.close()
 
 
@@ -66,7 +85,6 @@ def test_noalloc_rejects_a_plan_that_does_not_fit(tsp):
     """16 q heads of 128 dims in 64 KV splits need 1.06 MB of split partials
     (64-bit words), more than the fixed 1 MiB array."""
     import torch
-    from dataclasses import replace
     cfg = replace(S.CONFIGS["tiny"], name="wide", n_q_heads=16, head_dim=128)
     w, k, v, prompt = inputs(cfg, n_pos=0)
     plan = tsp.Plan(tsp.ModelDesc.from_config(cfg), tsp.upload_weights(w),

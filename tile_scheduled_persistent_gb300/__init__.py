@@ -277,7 +277,7 @@ class Plan:
 
     def set_trace(self, buf, steps: int) -> None:
         """Record a per-task timeline of the first `steps` steps of later decodes into
-        `buf` (int64 CUDA tensor of n_ctas * steps * max_tasks_per_cta * 8 words)."""
+        `buf` (int64 CUDA tensor of n_ctas * steps * max_tasks_per_cta * 16 words)."""
         _check(_lib().tiles_plan_set_trace(self._h, _ptr(buf), steps), "tiles_plan_set_trace")
 
     def decode(self, k_cache, v_cache, prompt, start_pos: int, n_new: int, out_tokens,

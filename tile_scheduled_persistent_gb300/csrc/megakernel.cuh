@@ -604,14 +604,20 @@ struct Producer {
             }
         }
         if (pid == 0) st_volatile_u64(&s.ctl->stream_pos, ~0ull);  // releases the prefetch warp
-        // drain: wait for every copy still in flight so no bulk copy outlives the CTA
+        // drain: wait for every copy still in flight so no bulk copy outlives the
+        // CTA. An issued copy completes on its own (it waits on nothing but
+        // memory), so this wait ends; it is bounded all the same, and running
+        // out is reported like any other timeout.
         const uint32_t ns = (uint32_t)g.ring_slots;
         uint32_t first = j > ns ? j - ns : 0;
         for (uint32_t k = first; k < j; ++k) {
             if (!owns(k)) continue;
             unsigned long long t0n = global_timer();
             while (!mbar_try_wait(&s.full[k % ns], (k / ns) & 1u)) {
-                if (global_timer() - t0n > p.timeout_ns) break;
+                if (global_timer() - t0n > p.timeout_ns) {
+                    atomicOr(p.status, kDevTimeout);
+                    break;
+                }
             }
         }
     }
@@ -1103,6 +1109,7 @@ struct Consumer {
             }
             const uint8_t *slot = wait_chunk(jj);
             if (!slot) break;
+            if (k == 0 && cur_tr && lane == 0) cur_tr[kTrFirstChunk] = global_timer();
             float mine[MATS];
             if constexpr (Q8) {
                 gemv_rows_q8_n<MATS>(nr, slot, vec, in >> 4, (size_t)in, mine);
@@ -1232,6 +1239,7 @@ struct Consumer {
     }
 
     int cur_layer = 0;
+    unsigned long long *cur_tr = nullptr;  // trace record of the running task, or null
 
     // One chunk of positions [q0, q0 + npos) for the G q heads of one kv head,
     // on the tensor cores (the chunk arrived as swizzled K and V tiles). The
@@ -1472,6 +1480,7 @@ struct Consumer {
                 consumer_sync();  // previous item finished reading q / knew / vnew
                 prep_qkv<D, MMA>(h, a);
                 consumer_sync();
+                if (cur_tr && tid == 0 && prepared < 0) cur_tr[kTrPrologue] = global_timer();
                 prepared = h;
             }
             int b0, b1;
@@ -1504,6 +1513,7 @@ struct Consumer {
                 for (uint32_t k = 0; k < nch; ++k) {
                     const uint32_t jj = j + k;
                     uint8_t *slot = wait_chunk(jj);
+                    if (k == 0 && cur_tr && tid == 0 && it == t.begin) cur_tr[kTrFirstChunk] = global_timer();
                     const int q0 = (b0 + (int)k) * g.kv_block;
                     int q1 = q0 + g.kv_block;
                     if (q1 > P + 1) q1 = P + 1;
@@ -1599,6 +1609,7 @@ struct Consumer {
             }
             // wstate is reused by the next item; leave together on any failure
             if (consumer_sync_or(bad)) return;
+            if (cur_tr && tid == 0) cur_tr[kTrPartials] = global_timer();
         }
         // Every partial of this task is out; now merge. (A merge polls the other
         // splits of its head, so no merge may come before a partial of the same
@@ -1644,6 +1655,7 @@ struct Consumer {
             st[q * 3 + 2] = __uint_as_float((uint32_t)wo);
         }
         consumer_sync();
+        if (cur_tr && tid == 0) cur_tr[kTrMergeIn] = global_timer();
         const uint32_t to = tag(cur_layer, kTagO) << 16;
         for (int q = tid; q < ne; q += kConsumerWarps * 32) {
             const float *sq = st + (size_t)q * S * 3;
@@ -1673,7 +1685,8 @@ struct Consumer {
                 const tiles_task t = p.tasks[ti];
                 cur_layer = t.layer;
                 // ---- wait for the inputs
-                unsigned long long *tr = tid == 0 ? trace_rec(p, cta, step, ti - t0) : nullptr;
+                cur_tr = trace_rec(p, cta, step, ti - t0);
+                unsigned long long *tr = tid == 0 ? cur_tr : nullptr;
                 if (tr) tr[kTrWaitStart] = global_timer();
                 if (tid == 0) {
                     const uint32_t target = t.wait_mul * (uint32_t)step + t.wait_add;
@@ -1703,6 +1716,7 @@ struct Consumer {
                         rmsnorm_to_vec(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : nullptr,
                                        p.layers[t.layer].attn_norm, g.H);
                         consumer_sync();
+                        if (tr) tr[kTrPrologue] = global_timer();
                         gemv_task<1, Q8>(t);
                         break;
                     case TILES_OP_ATTN:
@@ -1713,6 +1727,7 @@ struct Consumer {
                         load_residual(t.layer == 0 ? p.embed + (size_t)s.ctl->token * g.H : nullptr,
                                       t.layer == 0 ? 0u : tag(t.layer - 1, kTagXFfn), t.begin, t.end);
                         consumer_sync();
+                        if (tr) tr[kTrPrologue] = global_timer();
                         gemv_task<1, Q8>(t);
                         break;
                     case TILES_OP_GATEUP:
@@ -1720,12 +1735,14 @@ struct Consumer {
                         consumer_sync();
                         rmsnorm_to_vec(nullptr, p.layers[t.layer].ffn_norm, g.H);
                         consumer_sync();
+                        if (tr) tr[kTrPrologue] = global_timer();
                         gemv_task<2, Q8>(t);
                         break;
                     case TILES_OP_DOWN:
                         gather_tagged(p.aw, g.F, tag(t.layer, kTagA));
                         load_residual(nullptr, tag(t.layer, kTagXAttn), t.begin, t.end);
                         consumer_sync();
+                        if (tr) tr[kTrPrologue] = global_timer();
                         gemv_task<1, Q8>(t);
                         break;
                     case TILES_OP_LMHEAD:
@@ -1733,6 +1750,7 @@ struct Consumer {
                         consumer_sync();
                         rmsnorm_to_vec(nullptr, p.final_norm, g.H);
                         consumer_sync();
+                        if (tr) tr[kTrPrologue] = global_timer();
                         gemv_task<1, Q8>(t);
                         break;
                     default:

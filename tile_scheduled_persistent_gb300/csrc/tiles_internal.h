@@ -216,7 +216,7 @@ struct KernelParams {
 };
 
 // trace record words
-constexpr int kTraceWords = 8;
+constexpr int kTraceWords = 16;
 
 // When an attention item streams at least this many KV chunks (and the plan's
 // kernel instance carries the path), every chunk goes to its slot's owner
@@ -229,7 +229,7 @@ TILES_HD bool attn_uses_mma(const Geom &g, int n_chunks) {
     return g.attn_mma && n_chunks >= kConsumerWarps && g.kv_block % (2048 / g.d) == 0;
 }
 enum { kTrWaitStart = 0, kTrWaitEnd, kTrTaskEnd, kTrProdFirst, kTrProdLast, kTrProdStall,
-       kTrOpInfo };
+       kTrOpInfo, kTrPrologue, kTrFirstChunk, kTrPartials, kTrMergeIn };
 
 }  // namespace tiles
 
