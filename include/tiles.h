@@ -255,6 +255,60 @@ typedef struct {
 tiles_status_t tiles_plan_get_info(tiles_plan_t plan, tiles_plan_info *info);
 
 /* ------------------------------------------------------------------------ */
+/* Multi-token passes: verify steps and batched prompt prefill.              */
+
+/* Tokens a single pass of tiles_forward handles; longer inputs run in
+ * consecutive passes, and a verify step takes at most this many inputs. */
+#define TILES_MAX_FORWARD_TOKENS 64
+
+/*
+ * Runs n_tokens input tokens through the model at positions start_pos ..
+ * start_pos + n_tokens - 1 ("Tiles", "Scope and code release": batched
+ * prefill instead of one token per step; "History and roadmap", "M8 so far":
+ * multi-token verify steps), asynchronous on `stream`. The result is what
+ * n_tokens decode steps with those inputs compute: token i attends to every
+ * cached position up to its own (the K/V rows of the earlier tokens of the
+ * call included), and its K/V rows are written into the caches. Each pass of
+ * up to TILES_MAX_FORWARD_TOKENS tokens runs every layer for all of its
+ * tokens at once: the projections as BF16 tensor-core GEMMs with FP32
+ * accumulation, attention as a causal split-KV multi-query kernel, the same
+ * BF16 rounding points as tiles_decode.
+ *
+ *   k_cache, v_cache  device, as for tiles_decode; positions < start_pos filled
+ *   tokens            device, n_tokens ids in [0, vocab)
+ *   out_argmax        device, n_tokens int32: the greedy token after each input
+ *   out_logits        device, [n_tokens][vocab] float32, or NULL
+ *
+ * BF16 plans only (TILES_ERR_UNSUPPORTED for INT8 weights). The first call
+ * allocates the plan's working memory for these passes. An out-of-range
+ * token id is recorded in the status word (tiles_status). Errors:
+ * INVALID_ARG, CAPACITY (start_pos + n_tokens > max_pos), UNSUPPORTED,
+ * DEVICE_MISMATCH, CUDA.
+ */
+tiles_status_t tiles_forward(tiles_plan_t plan, void *k_cache, void *v_cache, const int32_t *tokens,
+                             int32_t n_tokens, int32_t start_pos, void *stream, int32_t *out_argmax,
+                             float *out_logits);
+
+/*
+ * One verify step of greedy speculative decoding ("History and roadmap",
+ * "M8 so far": verify steps on the split-KV decode kernels; draft tokens
+ * handed to the verify step on the device). inputs = the last emitted token
+ * followed by k draft tokens d_1 .. d_k (device, k + 1 ids, k + 1 <=
+ * TILES_MAX_FORWARD_TOKENS), placed at positions start_pos .. start_pos + k.
+ * With a_i the greedy token after input i, the step accepts the longest
+ * prefix with d_{i+1} == a_i (n drafts) and writes d_1 .. d_n, a_n to
+ * out_tokens (device, k + 1 int32; n + 1 of them written) and n to
+ * *out_n_accepted (device). Greedy decoding from the same state emits the
+ * same tokens. K/V rows are written for all k + 1 inputs; rows after
+ * start_pos + n are stale and are overwritten by the next step, which starts
+ * at start_pos + n + 1 with a_n as its last token. out_logits: device
+ * [k + 1][vocab] float32, or NULL. Errors as tiles_forward.
+ */
+tiles_status_t tiles_verify(tiles_plan_t plan, void *k_cache, void *v_cache, const int32_t *inputs, int32_t k,
+                            int32_t start_pos, void *stream, int32_t *out_tokens, int32_t *out_n_accepted,
+                            float *out_logits);
+
+/* ------------------------------------------------------------------------ */
 /* Schedule inspection without a GPU (planner and validator tests).          */
 
 enum {

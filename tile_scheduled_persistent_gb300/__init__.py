@@ -100,7 +100,9 @@ EXPORTS = ("tiles_plan_create", "tiles_plan_destroy", "tiles_decode", "tiles_dec
            "tiles_status", "tiles_status_string", "tiles_plan_get_info", "tiles_schedule_build",
            "tiles_schedule_validate", "tiles_schedule_tasks", "tiles_schedule_cta_bytes",
            "tiles_schedule_destroy", "tiles_copy_bw", "tiles_barrier_cost", "tiles_plan_set_trace",
-           "tiles_decode_noalloc", "tiles_quantize_rows_int8", "tiles_schedule_get_info")
+           "tiles_decode_noalloc", "tiles_quantize_rows_int8", "tiles_schedule_get_info",
+           "tiles_forward", "tiles_verify")
+MAX_FORWARD_TOKENS = 64
 
 _lib_handle = None
 
@@ -125,6 +127,10 @@ def _lib():
         L.tiles_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.tiles_decode_noalloc.restype = st
         L.tiles_decode_host.restype = st
+        L.tiles_forward.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp]
+        L.tiles_forward.restype = st
+        L.tiles_verify.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]
+        L.tiles_verify.restype = st
         L.tiles_status.argtypes = [vp, vp]
         L.tiles_status.restype = st
         L.tiles_status_string.argtypes = [st]
@@ -308,6 +314,25 @@ class Plan:
             out_tokens_np.ctypes.data_as(ctypes.c_void_p),
             None if out_logits_np is None else out_logits_np.ctypes.data_as(ctypes.c_void_p)),
             "tiles_decode_host")
+
+    def forward(self, k_cache, v_cache, tokens, start_pos: int, out_argmax, out_logits=None,
+                stream=None) -> None:
+        """Runs the int32 CUDA tensor `tokens` through the model at positions start_pos..
+        in passes of up to MAX_FORWARD_TOKENS (K/V written); out_argmax int32 [n] gets the
+        greedy token after each input, out_logits float32 [n][vocab] (or None) the logits."""
+        _check(_lib().tiles_forward(self._h, _ptr(k_cache), _ptr(v_cache), _ptr(tokens),
+                                    int(tokens.numel()), start_pos, _stream_ptr(stream),
+                                    _ptr(out_argmax), _ptr(out_logits)), "tiles_forward")
+
+    def verify(self, k_cache, v_cache, inputs, start_pos: int, out_tokens, out_n_accepted,
+               out_logits=None, stream=None) -> None:
+        """One greedy verify step: inputs = [last token, d_1 .. d_k] (int32 CUDA tensor) at
+        positions start_pos..; out_tokens int32 [k + 1] gets the accepted drafts and the
+        model's next token, out_n_accepted int32 [1] the number of accepted drafts."""
+        _check(_lib().tiles_verify(self._h, _ptr(k_cache), _ptr(v_cache), _ptr(inputs),
+                                   int(inputs.numel()) - 1, start_pos, _stream_ptr(stream),
+                                   _ptr(out_tokens), _ptr(out_n_accepted), _ptr(out_logits)),
+               "tiles_verify")
 
     def status(self, stream=None) -> int:
         return _lib().tiles_status(self._h, _stream_ptr(stream))

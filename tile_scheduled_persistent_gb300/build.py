@@ -16,8 +16,8 @@ LIB = os.path.join(HERE, "libtiles.so")
 BUILD = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["megakernel.cu", "kernels_bf16.cu", "kernels_bf16_mma.cu", "kernels_int8.cu", "kernels_int8_mma.cu",
-           "runtime.cu", "planner.cpp"]
-HEADERS = ["tiles_internal.h", "megakernel.cuh"]
+           "runtime.cu", "forward.cu", "planner.cpp"]
+HEADERS = ["tiles_internal.h", "megakernel.cuh", "plan_internal.h"]
 
 
 def _nvcc() -> str:

@@ -33,17 +33,7 @@ using namespace tiles;
 static_assert(sizeof(CUtensorMap) == sizeof(TensorMap) && alignof(CUtensorMap) <= alignof(TensorMap),
               "TensorMap must hold a CUtensorMap");
 
-struct tiles_plan_s {
-    tiles_schedule_s sched;
-    int device = -1, sm_count = 0, cc_major = 0, cc_minor = 0;
-    std::vector<void *> allocs;
-    KernelParams base{};
-    unsigned long long *d_keys = nullptr;  // keys then counters: one memset per launch
-    size_t sync_bytes = 0;
-    int32_t *d_prompt_stage = nullptr, *d_tokens_stage = nullptr;
-    float *d_logits_stage = nullptr;
-    size_t logits_stage_elems = 0;
-};
+#include "plan_internal.h"
 
 namespace {
 
@@ -287,6 +277,7 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
         e = cudaMemcpy(d_off, plan->sched.offsets.data(), plan->sched.offsets.size() * sizeof(int32_t),
                        cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(d_layers, lp.data(), (size_t)g.L * sizeof(LayerPtrs), cudaMemcpyHostToDevice);
+    plan->layers_host = lp;
     if (e != cudaSuccess) return fail(e);
     p.tasks = d_tasks;
     p.offsets = d_off;
@@ -332,6 +323,7 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
 void tiles_plan_destroy(tiles_plan_t plan) {
     if (!plan) return;
     for (void *v : plan->allocs) cudaFree(v);
+    for (void *v : plan->fwd.allocs) cudaFree(v);
     delete plan;
 }
 
@@ -351,7 +343,7 @@ tiles_status_t tiles_plan_get_info(tiles_plan_t plan, tiles_plan_info *info) {
     return tiles_schedule_get_info(&plan->sched, info);
 }
 
-static tiles_status_t check_device(tiles_plan_t plan) {
+tiles_status_t plan_check_device(tiles_plan_t plan) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return TILES_ERR_CUDA;
     if (dev != plan->device) return TILES_ERR_DEVICE_MISMATCH;
@@ -410,7 +402,7 @@ tiles_status_t tiles_decode(tiles_plan_t plan, void *k_cache, void *v_cache, con
     const long long steps = (long long)n_prompt - 1 + n_new;
     if (steps == 0) return TILES_OK;
     if ((long long)start_pos + steps > g.max_pos) return TILES_ERR_CAPACITY;
-    tiles_status_t st = check_device(plan);
+    tiles_status_t st = plan_check_device(plan);
     if (st != TILES_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     KernelParams p = plan->base;
@@ -589,7 +581,7 @@ extern "C" tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache,
     const long long steps = (long long)n_prompt - 1 + n_new;
     if (steps == 0) return TILES_OK;
     if ((long long)start_pos + steps > g.max_pos) return TILES_ERR_CAPACITY;
-    tiles_status_t st = check_device(plan);
+    tiles_status_t st = plan_check_device(plan);
     if (st != TILES_OK) return st;
     unsigned char *base = nullptr;
     if ((st = noalloc_scratch(plan->device, &base)) != TILES_OK) return st;
