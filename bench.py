@@ -11,6 +11,7 @@ are checked bit for bit.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
                   [--scheduler counters|waves|flags|all] [--impl ours|reference] [--tokens T]
+                  [--mode decode|prefill|verify] [--prompt N] [--k K]
 
 With N > 1 (launched by torchrun) every rank runs an independent replica: a
 batch-1 decode has no exchange step to shard (replicas only). `--impl
@@ -96,13 +97,18 @@ def measured_peaks():
         return None
 
 
+# sources the decode kernel's launch depends on (the multi-token pass in
+# forward.cu is a separate set of kernels and does not change its traffic)
+DECODE_SOURCES = ("kernels_bf16.cu", "kernels_bf16_mma.cu", "kernels_int8.cu", "kernels_int8_mma.cu",
+                  "megakernel.cu", "megakernel.cuh", "planner.cpp", "runtime.cu", "tiles_internal.h")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tile_scheduled_persistent_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    for name in DECODE_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -409,6 +415,88 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------------- multi-token arms
+def run_multi(args):
+    """--mode prefill: a prompt of --prompt seeded tokens from an empty cache
+    through tiles_forward (passes of up to 256 tokens); tok/s and the tensor
+    throughput of the weight FLOPs (2 x parameters x tokens) against the
+    measured BF16 peak. --mode verify: one tiles_verify step of --k drafts at
+    the workload's cached positions, the drafts being the decode kernel's own
+    greedy tokens; emitted tokens per second (accepted drafts + 1 per step)."""
+    import numpy as np
+    import torch
+
+    import synthetic as S
+    import tile_scheduled_persistent_gb300 as tsp
+    from dataclasses import replace
+
+    torch.cuda.set_device(0)
+    tsp.build()
+    cfg = S.CONFIGS[args.config]
+    w = S.model_weights(cfg)
+    plan = tsp.Plan(tsp.ModelDesc.from_config(cfg), tsp.upload_weights(w))
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        with ClockSampler(0) as clk:
+            for a, b in ev:
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+        plan.check()
+        ts = [a.elapsed_time(b) / 1e3 for a, b in ev]
+        return statistics.mean(ts), statistics.median(ts), clk.summary()
+
+    peaks = measured_peaks() or {}
+    line = {"n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
+    if args.mode == "prefill":
+        n = args.prompt
+        pc = replace(cfg, start_pos=0, max_pos=max(cfg.max_pos, n + 1))
+        shape = (pc.n_layers, pc.n_kv_heads, pc.max_pos, pc.head_dim)
+        kz = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+        vz = torch.zeros_like(kz)
+        toks = torch.from_numpy(S.tokens(S.SEED_TOKENS, 3, n, cfg.vocab)).cuda()
+        am = torch.zeros(n, dtype=torch.int32, device="cuda")
+        mean_s, med_s, clk = timed(lambda: plan.forward(kz, vz, toks, 0, am))
+        flops = 2.0 * (cfg.weight_bytes() / 2) * n
+        peak = float(peaks.get("bf16_tflops", 1900.0))
+        line.update({"metric": f"prefill tok/s, {n}-token prompt", "value": n / mean_s, "unit": "tok/s",
+                     "ms_per_step": 1e3 * mean_s,
+                     "config": {"workload": f"{cfg.name}: prompt of {n} seeded tokens from an empty cache, "
+                                            f"passes of up to {tsp.MAX_FORWARD_TOKENS} tokens"},
+                     "roofline": {"bound": "tensor", "achieved": flops / mean_s / 1e12, "peak": peak,
+                                  "unit": "TFLOP/s", "frac": flops / mean_s / 1e12 / peak, "traffic": None,
+                                  "note": "weight FLOPs 2 x parameters x tokens; attention not counted"},
+                     "clocks": clk, "gpu_launches": None})
+    else:
+        k, v = S.kv_prefill(cfg)
+        kc, vc = tsp.to_device_bf16(k), tsp.to_device_bf16(v)
+        pr = torch.from_numpy(S.prompt(cfg)).cuda()
+        g = torch.zeros(args.k, dtype=torch.int32, device="cuda")
+        plan.decode(kc, vc, pr, cfg.start_pos, args.k, g)
+        plan.check()
+        inp = torch.cat([pr, g]).to(torch.int32)
+        out = torch.zeros(args.k + 1, dtype=torch.int32, device="cuda")
+        nacc = torch.zeros(1, dtype=torch.int32, device="cuda")
+        mean_s, med_s, clk = timed(lambda: plan.verify(kc, vc, inp, cfg.start_pos, out, nacc))
+        acc = int(nacc.item())
+        line.update({"metric": f"verify-step emitted tok/s, k={args.k} drafts", "value": (acc + 1) / mean_s,
+                     "unit": "tok/s", "ms_per_step": 1e3 * mean_s,
+                     "config": {"workload": f"{cfg.name}: {cfg.start_pos} cached positions, {args.k} drafts "
+                                            f"(the decode kernel's greedy tokens), {acc} accepted"},
+                     "accepted": acc, "clocks": clk, "gpu_launches": None})
+    print(json.dumps(line), flush=True)
+    plan.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -425,7 +513,14 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="decode tokens per step (default: the workload's 64); a smaller "
                          "launch of the same kernel, for profiler captures")
+    ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "verify"],
+                    help="decode (the headline metric), or the multi-token arms")
+    ap.add_argument("--prompt", type=int, default=512, help="prefill: prompt tokens")
+    ap.add_argument("--k", type=int, default=16, help="verify: draft tokens")
     args = ap.parse_args()
+    if args.mode != "decode":
+        args.warmup = max(args.warmup, 3)
+        return run_multi(args)
     if args.warmup < 3 and args.impl == "ours":
         log("warm-up raised to 3 steps")
         args.warmup = 3

@@ -259,7 +259,7 @@ tiles_status_t tiles_plan_get_info(tiles_plan_t plan, tiles_plan_info *info);
 
 /* Tokens a single pass of tiles_forward handles; longer inputs run in
  * consecutive passes, and a verify step takes at most this many inputs. */
-#define TILES_MAX_FORWARD_TOKENS 64
+#define TILES_MAX_FORWARD_TOKENS 256
 
 /*
  * Runs n_tokens input tokens through the model at positions start_pos ..

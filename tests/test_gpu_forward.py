@@ -101,13 +101,14 @@ def test_forward_shapes_match_oracle(tsp, name):
 
 
 def test_forward_of_more_than_one_pass_and_decode_continuation(tsp):
-    """100 inputs run as two passes (64 + 36); then the decode kernel continues
-    from the cache the passes wrote: its tokens and logits match the oracle's
-    continuous run, and the pass's logits the oracle's prompt path."""
+    """300 inputs run as two passes (256 + 44); then the decode kernel
+    continues from the cache the passes wrote: its tokens and logits match
+    the oracle's continuous run, and the pass's logits the oracle's prompt
+    path."""
     import torch
-    cfg = with_gains(S.CONFIGS["tiny"]).with_workload(max_pos=160)
+    cfg = with_gains(S.CONFIGS["tiny"]).with_workload(max_pos=320)
     w, k, v, _ = inputs(cfg, n_pos=0)
-    toks = S.tokens(S.SEED_TOKENS, 9, 100, cfg.vocab)
+    toks = S.tokens(S.SEED_TOKENS, 9, 300, cfg.vocab)
     plan = _plan(tsp, cfg, w)
     am, lg, kc, vc = _forward(tsp, plan, cfg, k, v, toks, 0)
     ref, rk, rv = check_forward(am, lg, cfg, w, k, v, toks, 0, "two passes")
@@ -115,12 +116,12 @@ def test_forward_of_more_than_one_pass_and_decode_continuation(tsp):
     kd, vd = tsp.to_device_bf16(kc), tsp.to_device_bf16(vc)
     out = torch.zeros(12, dtype=torch.int32, device="cuda")
     lgd = torch.zeros((12, cfg.vocab), dtype=torch.float32, device="cuda")
-    plan.decode(kd, vd, torch.tensor([int(toks[-1])], dtype=torch.int32, device="cuda"), 99, 12, out, lgd)
+    plan.decode(kd, vd, torch.tensor([int(toks[-1])], dtype=torch.int32, device="cuda"), 299, 12, out, lgd)
     plan.check()
     plan.close()
-    cont = oracle.decode(cfg, w, rk.copy(), rv.copy(), np.array([toks[-1]], np.int32), 99, 12)
-    # the decode continues from the GPU's own cache; its first step is step 99 of the pass
-    np.testing.assert_allclose(lgd.cpu().numpy()[0], lg[99], atol=3e-2, rtol=1e-2)
+    cont = oracle.decode(cfg, w, rk.copy(), rv.copy(), np.array([toks[-1]], np.int32), 299, 12)
+    # the decode continues from the GPU's own cache; its first step is step 299 of the pass
+    np.testing.assert_allclose(lgd.cpu().numpy()[0], lg[299], atol=3e-2, rtol=1e-2)
     err = np.abs(lgd.cpu().numpy() - cont.logits)
     assert (err <= 3e-2 + 1e-2 * np.abs(cont.logits)).all(), float(err.max())
 

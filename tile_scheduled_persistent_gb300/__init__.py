@@ -102,7 +102,7 @@ EXPORTS = ("tiles_plan_create", "tiles_plan_destroy", "tiles_decode", "tiles_dec
            "tiles_schedule_destroy", "tiles_copy_bw", "tiles_barrier_cost", "tiles_plan_set_trace",
            "tiles_decode_noalloc", "tiles_quantize_rows_int8", "tiles_schedule_get_info",
            "tiles_forward", "tiles_verify")
-MAX_FORWARD_TOKENS = 64
+MAX_FORWARD_TOKENS = 256
 
 _lib_handle = None
 

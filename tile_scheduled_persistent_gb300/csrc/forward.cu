@@ -33,7 +33,7 @@
 namespace tiles {
 namespace fwd {
 
-constexpr int kMaxTokens = 64;  // tokens per pass
+constexpr int kMaxTokens = 256;  // tokens per pass
 constexpr int kBK = 64;         // K elements per pipeline stage
 constexpr int kStages = 4;
 constexpr int kPad = 8;         // bf16 padding per shared-memory row: conflict-free ldmatrix

@@ -7,7 +7,7 @@
 #include "tiles_internal.h"
 
 // Working memory of the multi-token forward pass (tiles_forward,
-// tiles_verify), allocated on first use for up to kMaxForwardTokens tokens
+// tiles_verify), allocated on first use for up to TILES_MAX_FORWARD_TOKENS tokens
 // per pass.
 struct ForwardScratch {
     std::vector<void *> allocs;
