@@ -139,9 +139,11 @@ typedef struct tiles_plan_s *tiles_plan_t;
  * tile graph, assign tiles to CTAs balancing streamed bytes, order them into
  * waves or dependency-counter chains, validate, and allocate the plan's own
  * device tables and scratch. The plan also packs its own copies of
- * [Wq; Wk; Wv] and of Wg/Wu interleaved by row (the kernel streams those);
- * wq/wk/wv/w_gate/w_up are only read during this call, the other weight
- * pointers must stay valid for the plan's lifetime. On success *out owns its
+ * [Wq; Wk; Wv] and of Wg/Wu interleaved by row (the kernel streams those, one
+ * bulk copy per ring chunk); wq/wk/wv/w_gate/w_up are only read during this
+ * call. With TILES_WEIGHTS_INT8 the plan holds codes of every GEMV matrix, so
+ * wo and w_down are only read here too. The embedding and the norm gains (and,
+ * for BF16, wo and w_down) must stay valid for the plan's lifetime. On success *out owns its
  * allocations. Errors: INVALID_ARG, UNSUPPORTED (shape), PLAN_INVALID, CUDA. */
 tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weights *weights,
                                  const tiles_plan_opts *opts, tiles_plan_t *out);

@@ -261,7 +261,8 @@ def test_random_shapes_build_valid_schedules_with_consistent_chunk_geometry():
     CTA count, scheduler, weight format, splits): every schedule the planner
     builds validates, and its chunk geometry follows the rules the kernel
     relies on (rows per chunk >= 1 and within the slot; the INT8 cap; the
-    tensor-core attention flag). Only documented rejections are allowed."""
+    tensor-core attention flag). Vocabularies smaller than the grid are
+    included. Only documented rejections are allowed."""
     from dataclasses import replace
     rng = np.random.default_rng(51)
     built = 0
@@ -284,20 +285,8 @@ def test_random_shapes_build_valid_schedules_with_consistent_chunk_geometry():
             assert e.status in (-1, -2), e.status             # bad option / unsupported shape
             continue
         st, why = sch.validate()
+        assert st == 0, why
         info = sch.info()
-        if st != 0:
-            # the one known gap: under tag-carrying activations an attention CTA
-            # orders its K/V writes through its own LM-head signal, so a vocabulary
-            # with fewer rows than attention items cannot cover them. The
-            # validator rejects that plan (plan creation fails cleanly), and the
-            # counter schedule of the same shape is valid.
-            assert "does not signal the LM head" in why, why
-            assert opts["scheduler"] == tsp.SCHED_FLAGS
-            assert cfg.vocab < cfg.n_kv_heads * info["kv_splits"]
-            alt = tsp.Schedule(tsp.ModelDesc.from_config(cfg), n,
-                               tsp.make_opts(**dict(opts, scheduler=tsp.SCHED_COUNTERS)))
-            assert alt.validate()[0] == 0
-            continue
         wb = 1 if opts["weight_format"] == tsp.WEIGHTS_INT8 else 2
         H, F, qd = cfg.hidden, cfg.ffn, cfg.q_dim
         qkv = qd + 2 * cfg.kv_dim
@@ -318,3 +307,37 @@ def test_random_shapes_build_valid_schedules_with_consistent_chunk_geometry():
         assert info["attn_tensor_cores"] == int(want)
         built += 1
     assert built >= 120
+
+
+def test_small_vocabulary_confines_attention_to_lm_head_ctas():
+    """A vocabulary with fewer rows than CTAs (107 rows on 152 CTAs, more
+    attention items per layer than rows): under tag-carrying activations every
+    CTA with attention work must signal the LM head ("Tiles: Scheduling LLM
+    Decoding as a Graph of Tiles", What the code contains: the schedule is
+    validated before launch). The planner confines every layer's attention
+    items to 107 CTAs, one LM-head row each, and all three schedulers
+    validate. With a vocabulary of at least one row per CTA the attention
+    items are unrestricted."""
+    from dataclasses import replace
+    cfg = replace(S.CONFIGS["tiny"], vocab=107, n_layers=4)
+    for sched in (tsp.SCHED_FLAGS, tsp.SCHED_COUNTERS, tsp.SCHED_WAVES):
+        sch = tsp.Schedule(tsp.ModelDesc.from_config(cfg), 152, tsp.make_opts(scheduler=sched, kv_splits=64))
+        st, why = sch.validate()
+        assert st == 0, why
+        tasks, off = sch.tasks()
+        attn, lm = set(), {}
+        for c in range(152):
+            for i in range(off[c], off[c + 1]):
+                t = tasks[i]
+                if t.op == 2:
+                    attn.add(c)
+                elif t.op == 7:
+                    lm[c] = lm.get(c, 0) + (t.end - t.begin)
+        assert sum(lm.values()) == 107 and len(lm) == 107
+        assert attn <= set(lm), sorted(attn - set(lm))
+        assert len(attn) > 64          # 2 KV heads x 64 splits per layer spread over 107 CTAs
+    big = replace(cfg, vocab=1024)
+    sch = tsp.Schedule(tsp.ModelDesc.from_config(big), 152, tsp.make_opts(kv_splits=64))
+    tasks, off = sch.tasks()
+    attn = {c for c in range(152) for i in range(off[c], off[c + 1]) if tasks[i].op == 2}
+    assert len(attn) == 152

@@ -110,6 +110,9 @@ VARIANTS = {
     # head_dim 64, group 2, cached positions crossing several KV blocks
     "g2_cache": replace(S.CONFIGS["tiny"], name="v3", start_pos=150, n_prompt=3, n_new=20,
                         max_pos=200, gain_sigma=GAINS),
+    # 107 vocabulary rows on the whole grid: fewer LM-head rows than attention
+    # items, so the attention items of every layer sit on the LM-head CTAs
+    "v107_small_vocab": replace(S.CONFIGS["tiny"], name="v4", vocab=107, gain_sigma=GAINS),
 }
 
 
@@ -122,6 +125,29 @@ def test_variants_match_oracle(tsp, name, scheduler):
     plan = _plan(tsp, cfg, w, scheduler=scheduler)
     toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, cfg.n_new)
     check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new, name)
+    plan.close()
+
+
+def test_plan_runs_after_the_packed_weights_are_freed(tsp):
+    """The plan packs its own [Wq; Wk; Wv] and interleaved gate/up: once it
+    exists the caller's wq/wk/wv/w_gate/w_up may go. Drop them, overwrite the
+    freed memory, and decode against the oracle."""
+    import torch
+    cfg = with_gains(S.CONFIGS["tiny"])
+    w, k, v, prompt = inputs(cfg, n_pos=0)
+    dw = tsp.upload_weights(w)
+    plan = tsp.Plan(tsp.ModelDesc.from_config(cfg), dw, tsp.make_opts())
+    shapes = []
+    for lw in dw["layers"]:
+        for f in ("wq", "wk", "wv", "w_gate", "w_up"):
+            shapes.append(lw[f].shape)
+            lw[f] = None
+    torch.cuda.synchronize()
+    # same-sized blocks come back from the allocator's cache: fill them with BF16 NaNs
+    junk = [torch.full(sh, 0x7FC0, dtype=torch.int16, device="cuda") for sh in shapes]
+    toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, 0, cfg.n_new)
+    check_parity(toks, logits, cfg, w, k, v, prompt, 0, cfg.n_new, "packed weights freed")
+    del junk
     plan.close()
 
 

@@ -55,6 +55,11 @@ LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "ffn_no
                 "w_up", "w_down")
 
 
+# Layer tensors a plan reads after tiles_plan_create returns, per weight format.
+_NORMS = ("attn_norm", "q_norm", "k_norm", "ffn_norm")
+_PLAN_READS_LATER = {WEIGHTS_BF16: _NORMS + ("wo", "w_down"), WEIGHTS_INT8: _NORMS}
+
+
 class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in LAYER_FIELDS]
 
@@ -252,11 +257,16 @@ class Plan:
 
     ``weights``: dict with 'embed', 'final_norm' and 'layers' (a list of dicts
     keyed by LAYER_FIELDS) of CUDA tensors holding bf16 bit patterns, row-major
-    [out][in]. The tensors must outlive the plan (the plan keeps references)."""
+    [out][in]. The plan packs its own copies of wq/wk/wv and w_gate/w_up (with
+    INT8 weights, of every GEMV matrix), so it keeps references only to the
+    tensors the kernel still reads: the embedding, the norm gains and, for BF16,
+    wo and w_down. The caller may drop the others once the plan exists."""
 
     def __init__(self, desc: ModelDesc, weights: dict, opts: PlanOpts | None = None):
         self.desc = desc
-        self._keep = weights
+        read_later = _PLAN_READS_LATER[int(opts.weight_format) if opts is not None else WEIGHTS_BF16]
+        self._keep = {"embed": weights["embed"], "final_norm": weights["final_norm"],
+                      "layers": [{f: lw.get(f) for f in read_later} for lw in weights["layers"]]}
         n = desc.n_layers
         self._layers = (LayerWeights * n)()
         for l, lw in enumerate(weights["layers"]):

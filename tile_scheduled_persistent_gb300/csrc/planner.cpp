@@ -201,12 +201,16 @@ std::vector<Assign> assign_rows(int R, long long row_bytes, int N, std::vector<l
 // least-loaded CTAs so far take the items: with no more items than CTAs one
 // each, the heaviest item to the least-loaded CTA; otherwise contiguous ranges,
 // the first n_items mod N of them one item longer.
+// `allowed` (ascending CTA indices) restricts the takers; empty = every CTA.
 std::vector<Assign> assign_items(int n_items, const std::vector<long long> &item_bytes, int N,
-                                 std::vector<long long> &cum) {
-    std::vector<int> order(N);
-    for (int c = 0; c < N; ++c) order[c] = c;
+                                 std::vector<long long> &cum, const std::vector<int> &allowed) {
+    std::vector<int> order = allowed;
+    if (order.empty()) {
+        order.resize(N);
+        for (int c = 0; c < N; ++c) order[c] = c;
+    }
     std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cum[a] < cum[b]; });
-    if (n_items <= N) {
+    if (n_items <= (int)order.size()) {
         std::vector<int> items(n_items);
         for (int i = 0; i < n_items; ++i) items[i] = i;
         std::stable_sort(items.begin(), items.end(),
@@ -219,7 +223,7 @@ std::vector<Assign> assign_items(int n_items, const std::vector<long long> &item
         std::sort(out.begin(), out.end(), [](const Assign &x, const Assign &y) { return x.begin < y.begin; });
         return out;
     }
-    const int takers = N;
+    const int takers = (int)order.size();
     std::vector<int> ctas(order.begin(), order.begin() + takers);
     std::sort(ctas.begin(), ctas.end());  // ranges in CTA order
     std::vector<Assign> out;
@@ -232,6 +236,19 @@ std::vector<Assign> assign_items(int n_items, const std::vector<long long> &item
         out.push_back(a);
     }
     return out;
+}
+
+// CTAs that may hold attention items. Under tag-carrying activations an
+// attention CTA orders its K/V writes before the next step's copies through
+// its own LM-head signal, so it must hold LM-head rows. With at least one
+// vocabulary row per CTA every CTA does (no restriction). With fewer rows the
+// attention items of every layer go to V CTAs spread evenly over the grid,
+// and each of them takes one LM-head row.
+std::vector<int> attention_ctas(const Geom &g, int N) {
+    std::vector<int> a;
+    if (g.V >= N) return a;
+    for (int i = 0; i < g.V; ++i) a.push_back((int)((long long)i * N / g.V));
+    return a;
 }
 
 }  // namespace
@@ -251,6 +268,7 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
     std::vector<std::vector<Assign>> phase_tasks(PPS);
     std::vector<int> phase_op(PPS), phase_layer(PPS);
     std::vector<long long> cum(N, 0);
+    const std::vector<int> attn_ctas = attention_ctas(g, N);
     // attention bytes for balancing: split sizes at the largest position
     for (int l = 0; l <= g.L; ++l) {
         for (int k = 0; k < (l < g.L ? kPhaseKinds : 1); ++k) {
@@ -262,10 +280,15 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
             int op = ops[kind];
             phase_op[phi] = op;
             phase_layer[phi] = l < g.L ? l : 0;
-            if (op_is_gemv(op)) {
-                phase_tasks[phi] = assign_rows(op_extent(g, op),
-                                               (long long)op_in_dim(g, op) * g.wbytes * op_mats(op), N,
-                                               cum);
+            const long long row_bytes = (long long)op_in_dim(g, op) * g.wbytes * op_mats(op);
+            if (op == TILES_OP_LMHEAD && !attn_ctas.empty()) {
+                // one vocabulary row to each attention CTA, in CTA (= row) order
+                for (int i = 0; i < g.V; ++i) {
+                    phase_tasks[phi].push_back({attn_ctas[i], (uint32_t)i, (uint32_t)i + 1});
+                    cum[attn_ctas[i]] += row_bytes;
+                }
+            } else if (op_is_gemv(op)) {
+                phase_tasks[phi] = assign_rows(op_extent(g, op), row_bytes, N, cum);
             } else if (op == TILES_OP_ATTN) {
                 int n = op_extent(g, op);
                 std::vector<long long> b(n);
@@ -276,7 +299,7 @@ tiles_status_t build_schedule(const tiles_model_desc &d, const tiles_plan_opts &
                     t.end = it + 1;
                     b[it] = task_bytes(g, t, g.max_pos - 1);
                 }
-                phase_tasks[phi] = assign_items(n, b, N, cum);
+                phase_tasks[phi] = assign_items(n, b, N, cum, attn_ctas);
             }
             // the combine phase stays empty: the last split tile of each KV head
             // merges the partials inside the attention phase
