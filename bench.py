@@ -73,20 +73,22 @@ def whole_job_rate(units_per_rank, seconds, device="cpu"):
     return units_per_rank * ws / slowest, slowest
 
 
-def workload_config(cfg, int8=False):
+def workload_config(cfg, int8=False, kv8=False):
     return {"workload": f"{cfg.name}: {cfg.n_layers} layers, hidden {cfg.hidden}, "
                         f"{cfg.n_q_heads}/{cfg.n_kv_heads} heads x {cfg.head_dim}, ffn {cfg.ffn}, "
                         f"vocab {cfg.vocab}, {cfg.start_pos} cached positions, "
                         f"{cfg.n_new} greedy tokens per step",
-            "weights": WEIGHT_DESC[int8],
+            "weights": WEIGHT_DESC[int8], "kv_cache": KV_DESC[kv8],
             "tokens_per_step": cfg.n_new, "cached_positions": cfg.start_pos,
-            "bytes_per_token": int(round(cfg.algorithmic_bytes_per_token(int8))),
+            "bytes_per_token": int(round(cfg.algorithmic_bytes_per_token(int8, kv8))),
             "l2": "inputs larger than L2 (every token streams all weights, >0.5 GB)"}
 
 
 WEIGHT_DESC = {False: "bf16",
                True: "int8 codes with one fp32 scale per output row (GEMV matrices and LM head)"}
 DTYPE = {False: "bf16", True: "int8 weights x bf16 activations, fp32 accumulate"}
+KV_DESC = {False: "bf16",
+           True: "int8 codes with one fp32 scale per cached row, keys minus a per-channel mean"}
 
 
 def measured_peaks():
@@ -187,14 +189,15 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------- CPU oracle arm
-def oracle_sample(cfg, w, k, v, prompt, n_tokens, qweights=None, n_threads=0):
+def oracle_sample(cfg, w, k, v, prompt, n_tokens, qweights=None, n_threads=0, kv_int8=False):
     """Time the oracle on n_tokens decode steps of the workload (all host cores,
-    or n_threads); with qweights, its weight-only INT8 form."""
+    or n_threads); with qweights, its weight-only INT8 form; with kv_int8, its
+    INT8 KV cache (built from the prefill inside the call)."""
     import oracle
     kk, vv = k.copy(), v.copy()
     t0 = time.perf_counter()
     oracle.decode(cfg, w, kk, vv, prompt, cfg.start_pos, n_tokens, want_logits=False,
-                  qweights=qweights, n_threads=n_threads)
+                  qweights=qweights, n_threads=n_threads, kv_int8=kv_int8)
     return time.perf_counter() - t0
 
 
@@ -217,11 +220,12 @@ def run_reference(args):
     k, v = S.kv_prefill(cfg)
     prompt = S.prompt(cfg)
     int8 = args.weights == "int8"
+    kv8 = args.kv == "int8"
     qw = oracle_qweights(w, int8)
     n_tok = args.ref_tokens
     for _ in range(args.warmup):
-        oracle_sample(cfg, w, k, v, prompt, n_tok, qw)
-    times = [oracle_sample(cfg, w, k, v, prompt, n_tok, qw) for _ in range(args.steps)]
+        oracle_sample(cfg, w, k, v, prompt, n_tok, qw, kv_int8=kv8)
+    times = [oracle_sample(cfg, w, k, v, prompt, n_tok, qw, kv_int8=kv8) for _ in range(args.steps)]
     tot = sum(times)
     value = n_tok * args.steps / tot
     cores = os.cpu_count()
@@ -230,7 +234,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE[int8],
-            "data": "synthetic", "config": workload_config(cfg, int8),
+            "data": "synthetic", "config": workload_config(cfg, int8, kv8),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -293,13 +297,20 @@ def run_ours(args):
         barrier_ns = None
 
     int8 = args.weights == "int8"
-    bytes_per_token = cfg.algorithmic_bytes_per_token(int8)
+    kv8 = args.kv == "int8"
+    bytes_per_token = cfg.algorithmic_bytes_per_token(int8, kv8)
+    if kv8:
+        # the INT8 cache of the prefill (outside the timed region); decode steps
+        # overwrite positions from start_pos on, like the BF16 cache's
+        cache8 = tsp.KV8Cache(tsp.ModelDesc.from_config(cfg)).from_bf16(kc, vc, cfg.start_pos)
+        kc, vc = cache8.k, cache8.v
     results = {}
     scheds = list(SCHEDULERS) if args.scheduler == "all" else [args.scheduler]
     for sname in scheds:
         plan = tsp.Plan(tsp.ModelDesc.from_config(cfg), dw,
                         tsp.make_opts(scheduler=SCHEDULERS[sname],
-                                      weight_format=tsp.WEIGHTS_INT8 if int8 else tsp.WEIGHTS_BF16))
+                                      weight_format=tsp.WEIGHTS_INT8 if int8 else tsp.WEIGHTS_BF16,
+                                      kv_format=tsp.KV_INT8 if kv8 else tsp.KV_BF16))
         info = plan.info()
         toks = torch.zeros(cfg.n_new, dtype=torch.int32, device="cuda")
         ref_toks = None
@@ -347,7 +358,7 @@ def run_ours(args):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
     else:
         peak, peak_src = 6800.0, "fallback 6.8 TB/s"
-    traffic = recorded_traffic(cfg.name + ("_int8" if int8 else ""), cfg.n_new)
+    traffic = recorded_traffic(cfg.name + ("_int8" if int8 else "") + ("_kv8" if kv8 else ""), cfg.n_new)
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     plan = r["plan"]
@@ -366,20 +377,22 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         n_tok = args.ref_tokens
         qw = oracle_qweights(w, int8)
-        secs = oracle_sample(cfg, w, k_np, v_np, prompt_np, n_tok, qw)
+        secs = oracle_sample(cfg, w, k_np, v_np, prompt_np, n_tok, qw, kv_int8=kv8)
         cpu = {"value": n_tok / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"first {n_tok} of the {cfg.n_new} decode tokens from position "
                          f"{cfg.start_pos}, OpenMP over output rows and heads on all host cores"
-                         + (", the oracle's weight-only INT8 path" if int8 else "")}
+                         + (", the oracle's weight-only INT8 path" if int8 else "")
+                         + (", the oracle's INT8 KV cache (built from the prefill inside the timed call)"
+                            if kv8 else "")}
         try:  # the same oracle on one thread, one token (information only)
-            secs1 = oracle_sample(cfg, w, k_np, v_np, prompt_np, 1, qw, n_threads=1)
+            secs1 = oracle_sample(cfg, w, k_np, v_np, prompt_np, 1, qw, n_threads=1, kv_int8=kv8)
             cpu["single_thread"] = {"value": 1 / secs1, "unit": UNIT, "cores": 1,
                                     "sample": f"first decode token from position {cfg.start_pos}"}
         except Exception as e:  # never let the information line cost the measurement
             cpu["single_thread"] = {"error": str(e)[:200]}
 
     if rank == 0:
-        conf = workload_config(cfg, int8)
+        conf = workload_config(cfg, int8, kv8)
         conf.update({"scheduler": chosen, "ctas": r["info"]["n_ctas"],
                      "ring": f"{r['info']['ring_slots']} x {r['info']['slot_bytes']} B",
                      "kv_splits": r["info"]["kv_splits"], "parallelism": f"replicas x{ws}"})
@@ -510,6 +523,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "int8"],
                     help="weight format of the plan (int8: weight-only, per-row scales)")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"],
+                    help="KV cache format (int8: codes with per-row scales, smoothed keys)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="decode tokens per step (default: the workload's 64); a smaller "
                          "launch of the same kernel, for profiler captures")

@@ -110,6 +110,21 @@ enum { TILES_SCHED_WAVES = 0, TILES_SCHED_COUNTERS = 1, TILES_SCHED_FLAGS = 2 };
  * to be multiples of 16. */
 enum { TILES_WEIGHTS_BF16 = 0, TILES_WEIGHTS_INT8 = 1 };
 
+/* KV cache formats. TILES_KV_BF16: the k_cache / v_cache of the decode calls
+ * are BF16 [L][n_kv][max_pos][head_dim]. TILES_KV_INT8 ("History and
+ * roadmap", "M8 so far": INT8 KV cache with smoothed keys; "Tried and not
+ * kept": queries stay unquantized): each cached row is INT8 codes with one
+ * FP32 scale, and keys are stored minus a per-(layer, KV head) channel mean
+ * mu (the smoothing):
+ *   key row:   x = R(k) - mu;  value row: x = R(v)   (R = the BF16 rounding)
+ *   s = max_j |x_j| / 127,  c_j = x_j / s rounded to nearest even, clamped
+ *   to [-127, 127] (all in FP32; an all-zero row: s = 0, codes 0).
+ * Attention reads K_t = s_t c_t and V_t likewise, and never adds mu back:
+ * it moves every score of a query by q . mu, which the softmax cancels.
+ * mu comes from the prefill (tiles_kv8_from_bf16) and stays fixed while
+ * decoding. See tiles_kv8_layout for the two buffers. */
+enum { TILES_KV_BF16 = 0, TILES_KV_INT8 = 1 };
+
 /* Planner options; pass NULL to tiles_plan_create for the defaults (shown). */
 typedef struct {
     int32_t scheduler;    /* TILES_SCHED_FLAGS (default), _COUNTERS or _WAVES            */
@@ -122,6 +137,7 @@ typedef struct {
     int32_t l2_prefetch_gbs; /* its issue rate per CTA, GB/s (token bucket); <= 0 = unpaced */
     int32_t weight_format; /* TILES_WEIGHTS_BF16 (default) or TILES_WEIGHTS_INT8           */
     uint32_t flags;       /* TILES_FLAG_* bits; 0 for normal use                         */
+    int32_t kv_format;    /* TILES_KV_BF16 (default) or TILES_KV_INT8                     */
 } tiles_plan_opts;
 
 /* TILES_FLAG_INJECT_STALL is a test hook for failure detection. After the
@@ -162,7 +178,10 @@ void tiles_plan_destroy(tiles_plan_t plan);
  * 0..start_pos + s. Steps are split into cooperative launches of <= 64.
  *
  *   k_cache, v_cache  device, [n_layers][n_kv_heads][max_pos][head_dim] bf16,
- *                     positions < start_pos already filled by the caller
+ *                     positions < start_pos already filled by the caller;
+ *                     with kv_format TILES_KV_INT8, the two INT8 cache
+ *                     buffers of tiles_kv8_layout (positions < start_pos
+ *                     filled, e.g. by tiles_kv8_from_bf16)
  *   prompt            device, n_prompt >= 1 token ids in [0, vocab)
  *   out_tokens        device, n_new int32
  *   out_logits        device, [n_prompt - 1 + n_new][vocab] float32, or NULL
@@ -250,6 +269,7 @@ typedef struct {
     int32_t rows_per_chunk[5];  /* GEMV rows per ring chunk: Q/K/V, O, gate/up (pairs),
                                    down, LM head                                             */
     int32_t weight_format;      /* TILES_WEIGHTS_BF16 or TILES_WEIGHTS_INT8                   */
+    int32_t kv_format;          /* TILES_KV_BF16 or TILES_KV_INT8                             */
     int64_t weight_bytes_per_token;     /* every weight byte the kernel streams per step */
     int64_t max_cta_bytes, min_cta_bytes; /* per-step streamed weight bytes, busiest/idlest CTA */
 } tiles_plan_info;
@@ -281,7 +301,7 @@ tiles_status_t tiles_plan_get_info(tiles_plan_t plan, tiles_plan_info *info);
  *   out_argmax        device, n_tokens int32: the greedy token after each input
  *   out_logits        device, [n_tokens][vocab] float32, or NULL
  *
- * BF16 plans only (TILES_ERR_UNSUPPORTED for INT8 weights). The first call
+ * BF16 plans only (TILES_ERR_UNSUPPORTED for INT8 weights or an INT8 KV cache). The first call
  * allocates the plan's working memory for these passes. An out-of-range
  * token id is recorded in the status word (tiles_status). Errors:
  * INVALID_ARG, CAPACITY (start_pos + n_tokens > max_pos), UNSUPPORTED,
@@ -378,6 +398,38 @@ void tiles_schedule_destroy(tiles_schedule_t sched);
  * or cols < 1; TILES_ERR_CUDA if the launch fails. */
 tiles_status_t tiles_quantize_rows_int8(const void *w_bf16, int32_t rows, int32_t cols, void *codes,
                                         float *scales, void *stream);
+
+/* The two caller-owned device buffers of a TILES_KV_INT8 cache (see
+ * TILES_KV_INT8 for the quantities). With Z = n_layers * n_kv_heads, d =
+ * head_dim and MP = max_pos rounded up to a multiple of 16 (position strides
+ * stay multiples of 16 bytes, as the kernel's tiled copies need):
+ *   k buffer: key codes   int8  [Z][MP][d]  at offset 0
+ *             key scales  float [Z][MP]     at k_scale_off
+ *             key shifts  float [Z][d]      at k_mu_off (mu, per channel)
+ *   v buffer: value codes int8  [Z][d][MP]  at offset 0 (transposed: a
+ *                                          head's channel is one row)
+ *             value scales float [Z][MP]    at v_scale_off
+ * Offsets are multiples of 256 bytes; the buffers must be 16-byte aligned.
+ * Positions max_pos..MP-1 are never read as data. Fills *out from desc
+ * alone. Errors: INVALID_ARG (null argument, non-positive dimension). */
+typedef struct {
+    int64_t k_bytes, v_bytes;                 /* sizes of the two buffers          */
+    int64_t k_scale_off, k_mu_off, v_scale_off;
+    int32_t pos_stride;                       /* MP                                */
+} tiles_kv8_layout;
+
+tiles_status_t tiles_kv8_get_layout(const tiles_model_desc *desc, tiles_kv8_layout *out);
+
+/* Builds the INT8 cache of the prefilled positions 0..n_pos-1 from BF16 caches
+ * ([L][n_kv][max_pos][d], device), asynchronous on `stream`: per (layer, KV
+ * head) the key shift mu_j = (sum over t < n_pos of K[t][j]) / n_pos, summed
+ * in FP64 in position order and rounded to FP32 (0 when n_pos = 0), then
+ * every row of positions < n_pos quantized as TILES_KV_INT8 states. Other
+ * positions of k8 / v8 are left as they are. Errors: INVALID_ARG (null
+ * pointer, n_pos outside [0, max_pos], unaligned buffer), UNSUPPORTED
+ * (head_dim not 64 or 128), CUDA. */
+tiles_status_t tiles_kv8_from_bf16(const tiles_model_desc *desc, const void *k_bf16, const void *v_bf16,
+                                   int32_t n_pos, void *k8, void *v8, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* Measurement helpers.                                                       */

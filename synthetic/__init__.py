@@ -189,10 +189,14 @@ class ModelConfig:
         return (self.n_layers * (matrix + 4 * rows + 2 * norms)
                 + self.vocab * H + 4 * self.vocab + 2 * H)
 
-    def algorithmic_bytes_per_token(self, int8: bool = False) -> float:
+    def algorithmic_bytes_per_token(self, int8: bool = False, kv_int8: bool = False) -> float:
         """Weights once + one embedding row + K/V of positions 0..P read + new K/V write,
-        averaged over the run's decode positions."""
-        kv_pos_bytes = 2 * 2 * self.n_layers * self.kv_dim      # K and V, one position, all layers
+        averaged over the run's decode positions. With ``kv_int8`` a cached
+        position is its key and value codes plus their two FP32 scales."""
+        if kv_int8:
+            kv_pos_bytes = self.n_layers * self.n_kv_heads * (2 * self.head_dim + 8)
+        else:
+            kv_pos_bytes = 2 * 2 * self.n_layers * self.kv_dim  # K and V, one position, all layers
         p0 = self.start_pos
         steps = self.n_steps
         avg_read_pos = p0 + (steps - 1) / 2.0 + 1.0              # positions 0..P inclusive

@@ -71,6 +71,24 @@ def gpu_run(plan, cfg, k, v, prompt, start_pos, n_new, want_logits=True, split_a
             vc.view(torch.int16).cpu().numpy().view(np.uint16))
 
 
+def gpu_run_kv8(plan, cfg, k, v, prompt, start_pos, n_new):
+    """Decode with an INT8 KV cache built on the GPU from the BF16 prefill
+    (positions < start_pos). Returns tokens, logits and the cache's parts
+    (KV8Cache.host())."""
+    import torch
+    import tile_scheduled_persistent_gb300 as tsp
+    cache = tsp.KV8Cache(tsp.ModelDesc.from_config(cfg))
+    cache.from_bf16(tsp.to_device_bf16(k), tsp.to_device_bf16(v), start_pos)
+    prompt = np.asarray(prompt, np.int32)
+    steps = prompt.size - 1 + n_new
+    toks = torch.full((max(n_new, 1),), -1, dtype=torch.int32, device="cuda")
+    logits = torch.full((max(steps, 1), cfg.vocab), float("nan"), dtype=torch.float32, device="cuda")
+    plan.decode(cache.k, cache.v, torch.from_numpy(prompt).cuda(), start_pos, n_new, toks, logits)
+    plan.check()
+    torch.cuda.synchronize()
+    return toks.cpu().numpy()[:n_new], logits.cpu().numpy(), cache.host()
+
+
 def near_tie_scale(oracle_logits_step, tau_step, envelope):
     """Below which oracle top-2 gap two greedy choices count as a near-tie: tau
     (the reordered oracle's largest deviation at that step) at full depth; in
@@ -83,7 +101,7 @@ def near_tie_scale(oracle_logits_step, tau_step, envelope):
 
 
 def check_parity(g_tokens, g_logits, cfg, w, k, v, prompt, start_pos, n_new, what="",
-                 qweights=None, envelope=False):
+                 qweights=None, envelope=False, kv_int8=False):
     """Element-by-element parity of a GPU decode with the oracle.
 
     The oracle is run on the GPU's own token history (teacher forcing), so every
@@ -98,14 +116,17 @@ def check_parity(g_tokens, g_logits, cfg, w, k, v, prompt, start_pos, n_new, wha
     |gpu - oracle| <= ATOL + RTOL |oracle| at every step; with ``envelope``
     (deep models, where summation order alone moves logits past that bound)
     within that plus 1.5 tau, with the mean error within twice the reordered
-    oracle's mean deviation. Returns the facts for the report."""
+    oracle's mean deviation. With ``kv_int8`` the oracle attends over its INT8
+    KV cache (built from the prefilled positions, returned as ref.kv8).
+    Returns the facts for the report."""
     prompt = np.asarray(prompt, np.int32)
     n_prompt = prompt.size
     steps = n_prompt - 1 + n_new
     g_tokens = np.asarray(g_tokens)
     force = g_tokens[:-1] if n_new > 1 else None
     kk, vv = k.copy(), v.copy()
-    ref = oracle.decode(cfg, w, kk, vv, prompt, start_pos, n_new, force_tokens=force, qweights=qweights)
+    ref = oracle.decode(cfg, w, kk, vv, prompt, start_pos, n_new, force_tokens=force, qweights=qweights,
+                        kv_int8=kv_int8)
     assert g_logits is not None and g_logits.shape == ref.logits.shape
     assert not np.isnan(g_logits).any(), f"{what}: NaN logits"
     out_steps = np.arange(n_prompt - 1, steps)
@@ -114,7 +135,7 @@ def check_parity(g_tokens, g_logits, cfg, w, k, v, prompt, start_pos, n_new, wha
     tau = None
     if envelope or len(differ):
         alt = oracle.decode(cfg, w, k.copy(), v.copy(), prompt, start_pos, n_new, force_tokens=force,
-                            qweights=qweights, variant="alt")
+                            qweights=qweights, variant="alt", kv_int8=kv_int8)
         dev = np.abs(alt.logits - ref.logits)
         tau = dev.max(axis=1)
     err = np.abs(g_logits - ref.logits)

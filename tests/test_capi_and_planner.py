@@ -341,3 +341,43 @@ def test_small_vocabulary_confines_attention_to_lm_head_ctas():
     tasks, off = sch.tasks()
     attn = {c for c in range(152) for i in range(off[c], off[c + 1]) if tasks[i].op == 2}
     assert len(attn) == 152
+
+
+def test_int8_kv_layout_and_schedule_geometry():
+    """The INT8 KV cache ("History and roadmap", M8: INT8 KV cache with
+    smoothed keys): buffer layout (position stride rounded up to 16, parts at
+    256-byte offsets), the chunk geometry the kernel relies on (8 KB of key
+    codes and 8 KB of value codes per chunk plus their scales, in one slot;
+    every split on the tensor-core form), and the streamed bytes the planner
+    balances: 2 d + 8 bytes per cached position and head instead of 4 d."""
+    from dataclasses import replace
+    for d, nkv, L, mp in ((64, 8, 16, 32832), (128, 8, 28, 1088), (64, 2, 2, 130)):
+        cfg = replace(S.CONFIGS["tiny"], head_dim=d, n_kv_heads=nkv, n_q_heads=nkv * 2, n_layers=L, max_pos=mp)
+        lay = tsp.kv8_layout(tsp.ModelDesc.from_config(cfg))
+        Z, MP = L * nkv, _ceil(mp, 16) * 16
+        assert lay["pos_stride"] == MP
+        assert lay["k_scale_off"] == _ceil(Z * MP * d, 256) * 256
+        assert lay["k_mu_off"] == _ceil(lay["k_scale_off"] + Z * MP * 4, 256) * 256
+        assert lay["k_bytes"] == lay["k_mu_off"] + Z * d * 4
+        assert lay["v_scale_off"] == _ceil(Z * d * MP, 256) * 256
+        assert lay["v_bytes"] == lay["v_scale_off"] + Z * MP * 4
+        sch = tsp.Schedule(tsp.ModelDesc.from_config(cfg), 152, tsp.make_opts(kv_format=tsp.KV_INT8))
+        assert sch.validate()[0] == 0
+        info = sch.info()
+        assert info["kv_format"] == tsp.KV_INT8 and info["attn_tensor_cores"] == 1
+        assert info["kv_block"] == 8192 // d
+        assert info["slot_bytes"] >= 2 * 8192 + 2 * (8192 // d) * 4 and info["slot_bytes"] % 1024 == 0
+    # streamed bytes at a long context: weights the same, K/V at (2d + 8) / 4d
+    cfg = S.CONFIGS["llama1b_long"]
+    desc = tsp.ModelDesc.from_config(cfg)
+    b16 = tsp.Schedule(desc, 152, tsp.make_opts())
+    b8 = tsp.Schedule(desc, 152, tsp.make_opts(kv_format=tsp.KV_INT8))
+    P = cfg.start_pos
+    w = b16.info()["weight_bytes_per_token"]
+    assert b8.info()["weight_bytes_per_token"] == w
+    kv16, kv8 = sum(b16.cta_bytes(P)) - w, sum(b8.cta_bytes(P)) - w
+    per_pos = cfg.n_layers * cfg.n_kv_heads
+    assert kv16 == per_pos * P * 4 * cfg.head_dim
+    assert kv8 == per_pos * P * (2 * cfg.head_dim + 8)
+    with pytest.raises(tsp.TilesError):
+        tsp.Schedule(desc, 152, tsp.make_opts(kv_format=2))

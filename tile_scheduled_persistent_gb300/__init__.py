@@ -20,6 +20,7 @@ STATUS_NAMES = {0: "TILES_OK", -1: "TILES_ERR_INVALID_ARG", -2: "TILES_ERR_UNSUP
 SCHED_WAVES, SCHED_COUNTERS, SCHED_FLAGS = 0, 1, 2
 FLAG_INJECT_STALL = 1  # test hook: CTA 0's first wait is never met (the launch times out)
 WEIGHTS_BF16, WEIGHTS_INT8 = 0, 1
+KV_BF16, KV_INT8 = 0, 1
 OPS = {1: "QKV", 2: "ATTN", 3: "COMBINE", 4: "OPROJ", 5: "GATEUP", 6: "DOWN", 7: "LMHEAD",
        8: "SYNC"}
 NO_COUNTER = 0xFFFF
@@ -73,7 +74,7 @@ class PlanOpts(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("scheduler", "n_ctas", "slot_bytes", "ring_slots", "kv_splits", "timeout_ms",
                  "l2_prefetch_kb", "l2_prefetch_gbs", "weight_format")] + \
-               [("flags", ctypes.c_uint32)]
+               [("flags", ctypes.c_uint32), ("kv_format", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -81,7 +82,8 @@ class PlanInfo(ctypes.Structure):
                 ("n_ctas", "threads_per_cta", "smem_bytes", "slot_bytes", "ring_slots",
                  "kv_splits", "scheduler", "n_tasks", "n_counters", "phases_per_step",
                  "max_tasks_per_cta", "kv_block", "attn_tensor_cores")] + \
-               [("rows_per_chunk", ctypes.c_int32 * 5), ("weight_format", ctypes.c_int32)] + \
+               [("rows_per_chunk", ctypes.c_int32 * 5), ("weight_format", ctypes.c_int32),
+                ("kv_format", ctypes.c_int32)] + \
                [(n, ctypes.c_int64) for n in
                 ("weight_bytes_per_token", "max_cta_bytes", "min_cta_bytes")]
 
@@ -89,6 +91,11 @@ class PlanInfo(ctypes.Structure):
         d = {n: getattr(self, n) for n, _ in self._fields_}
         d["rows_per_chunk"] = dict(zip(("qkv", "o", "gateup", "down", "lm"), self.rows_per_chunk))
         return d
+
+
+class KV8Layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("k_bytes", "v_bytes", "k_scale_off", "k_mu_off", "v_scale_off")] + \
+               [("pos_stride", ctypes.c_int32)]
 
 
 class Task(ctypes.Structure):
@@ -106,7 +113,7 @@ EXPORTS = ("tiles_plan_create", "tiles_plan_destroy", "tiles_decode", "tiles_dec
            "tiles_schedule_validate", "tiles_schedule_tasks", "tiles_schedule_cta_bytes",
            "tiles_schedule_destroy", "tiles_copy_bw", "tiles_barrier_cost", "tiles_plan_set_trace",
            "tiles_decode_noalloc", "tiles_quantize_rows_int8", "tiles_schedule_get_info",
-           "tiles_forward", "tiles_verify")
+           "tiles_forward", "tiles_verify", "tiles_kv8_get_layout", "tiles_kv8_from_bf16")
 MAX_FORWARD_TOKENS = 256
 
 _lib_handle = None
@@ -163,6 +170,10 @@ def _lib():
         L.tiles_copy_bw.restype = st
         L.tiles_quantize_rows_int8.argtypes = [vp, i32, i32, vp, vp, vp]
         L.tiles_quantize_rows_int8.restype = st
+        L.tiles_kv8_get_layout.argtypes = [ctypes.POINTER(ModelDesc), ctypes.POINTER(KV8Layout)]
+        L.tiles_kv8_get_layout.restype = st
+        L.tiles_kv8_from_bf16.argtypes = [ctypes.POINTER(ModelDesc), vp, vp, i32, vp, vp, vp]
+        L.tiles_kv8_from_bf16.restype = st
         L.tiles_barrier_cost.argtypes = [i32, i32, ctypes.POINTER(ctypes.c_double)]
         L.tiles_barrier_cost.restype = st
         _lib_handle = L
@@ -181,11 +192,53 @@ def _check(status: int, what: str):
 
 def make_opts(scheduler=SCHED_FLAGS, n_ctas=0, slot_bytes=0, ring_slots=0, kv_splits=0,
               timeout_ms=0, l2_prefetch_kb=0, l2_prefetch_gbs=0, flags=0,
-              weight_format=0) -> PlanOpts:
+              weight_format=0, kv_format=0) -> PlanOpts:
     return PlanOpts(scheduler=scheduler, n_ctas=n_ctas, slot_bytes=slot_bytes,
                     ring_slots=ring_slots, kv_splits=kv_splits, timeout_ms=timeout_ms,
                     l2_prefetch_kb=l2_prefetch_kb, l2_prefetch_gbs=l2_prefetch_gbs, flags=flags,
-                    weight_format=weight_format)
+                    weight_format=weight_format, kv_format=kv_format)
+
+
+# ------------------------------------------------------------------ INT8 KV cache
+def kv8_layout(desc: ModelDesc) -> dict:
+    """Sizes and offsets of the two buffers of an INT8 KV cache (no GPU)."""
+    lay = KV8Layout()
+    _check(_lib().tiles_kv8_get_layout(ctypes.byref(desc), ctypes.byref(lay)), "tiles_kv8_get_layout")
+    return {n: getattr(lay, n) for n, _ in lay._fields_}
+
+
+class KV8Cache:
+    """The two device buffers of an INT8 KV cache (uint8 CUDA tensors k, v),
+    laid out as tiles_kv8_get_layout states. ``from_bf16`` fills the prefilled
+    positions from BF16 caches; ``host()`` returns the parts as numpy arrays."""
+
+    def __init__(self, desc: ModelDesc, device="cuda"):
+        import torch
+        self.desc = desc
+        self.layout = kv8_layout(desc)
+        self.k = torch.zeros(self.layout["k_bytes"], dtype=torch.uint8, device=device)
+        self.v = torch.zeros(self.layout["v_bytes"], dtype=torch.uint8, device=device)
+
+    def from_bf16(self, k_cache, v_cache, n_pos: int, stream=None) -> "KV8Cache":
+        _check(_lib().tiles_kv8_from_bf16(ctypes.byref(self.desc), _ptr(k_cache), _ptr(v_cache), int(n_pos),
+                                          _ptr(self.k), _ptr(self.v), _stream_ptr(stream)), "tiles_kv8_from_bf16")
+        return self
+
+    def host(self) -> dict:
+        """kq [Z][MP][d] int8, vq [Z][d][MP] int8, ks / vs [Z][MP] float32, mu [Z][d] float32
+        (Z = n_layers * n_kv_heads, MP = pos_stride)."""
+        import numpy as np
+        d, lay = self.desc, self.layout
+        Z, mp, hd = d.n_layers * d.n_kv_heads, lay["pos_stride"], d.head_dim
+        kb, vb = self.k.cpu().numpy(), self.v.cpu().numpy()
+
+        def part(buf, off, n, dt, shape):
+            return np.frombuffer(buf[off:off + n * np.dtype(dt).itemsize].tobytes(), dt).reshape(shape)
+        return {"kq": part(kb, 0, Z * mp * hd, np.int8, (Z, mp, hd)),
+                "ks": part(kb, lay["k_scale_off"], Z * mp, np.float32, (Z, mp)),
+                "mu": part(kb, lay["k_mu_off"], Z * hd, np.float32, (Z, hd)),
+                "vq": part(vb, 0, Z * hd * mp, np.int8, (Z, hd, mp)),
+                "vs": part(vb, lay["v_scale_off"], Z * mp, np.float32, (Z, mp))}
 
 
 # ------------------------------------------------------------------ schedule (host only)

@@ -658,7 +658,7 @@ tiles_status_t forward_check(tiles_plan_t plan, void *k_cache, void *v_cache, in
     if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u)
         return TILES_ERR_INVALID_ARG;
     const Geom &g = plan->sched.geom;
-    if (g.wbytes != 2) return TILES_ERR_UNSUPPORTED;
+    if (g.wbytes != 2 || g.kv8) return TILES_ERR_UNSUPPORTED;  // BF16 weights and cache only
     if ((long long)start_pos + n > g.max_pos) return TILES_ERR_CAPACITY;
     tiles_status_t st = plan_check_device(plan);
     if (st != TILES_OK) return st;

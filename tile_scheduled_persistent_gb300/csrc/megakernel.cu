@@ -9,27 +9,30 @@ const void *megakernel_bf16(int d, int G);      // kernels_bf16.cu
 const void *megakernel_bf16_mma(int d, int G);  // kernels_bf16_mma.cu
 const void *megakernel_int8(int d, int G);      // kernels_int8.cu
 const void *megakernel_int8_mma(int d, int G);  // kernels_int8_mma.cu
+const void *megakernel_bf16_kv8(int d, int G);  // kernels_bf16_kv8.cu
+const void *megakernel_int8_kv8(int d, int G);  // kernels_int8_kv8.cu
 
-static const void *megakernel_for(int d, int G, int wbytes, int mma) {
-    if (wbytes == 1) return mma ? megakernel_int8_mma(d, G) : megakernel_int8(d, G);
-    return mma ? megakernel_bf16_mma(d, G) : megakernel_bf16(d, G);
+// ak: attention kind (attn_kind of the plan's geometry)
+static const void *megakernel_for(int d, int G, int wbytes, int ak) {
+    if (wbytes == 1) return ak == 2 ? megakernel_int8_kv8(d, G) : ak ? megakernel_int8_mma(d, G) : megakernel_int8(d, G);
+    return ak == 2 ? megakernel_bf16_kv8(d, G) : ak ? megakernel_bf16_mma(d, G) : megakernel_bf16(d, G);
 }
 
 // ------------------------------------------------------------------ launchers
-cudaError_t megakernel_configure(int d, int G, int wbytes, int mma, int smem_bytes) {
-    const void *k = megakernel_for(d, G, wbytes, mma);
+cudaError_t megakernel_configure(int d, int G, int wbytes, int ak, int smem_bytes) {
+    const void *k = megakernel_for(d, G, wbytes, ak);
     if (!k) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
-cudaError_t megakernel_occupancy(int d, int G, int wbytes, int mma, int smem_bytes, int *blocks_per_sm) {
-    const void *k = megakernel_for(d, G, wbytes, mma);
+cudaError_t megakernel_occupancy(int d, int G, int wbytes, int ak, int smem_bytes, int *blocks_per_sm) {
+    const void *k = megakernel_for(d, G, wbytes, ak);
     if (!k) return cudaErrorInvalidValue;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kThreads, smem_bytes);
 }
 
 cudaError_t megakernel_launch(const KernelParams &p, int n_ctas, int smem_bytes, cudaStream_t st) {
-    const void *k = megakernel_for(p.g.d, p.g.G, p.g.wbytes, p.g.attn_mma);
+    const void *k = megakernel_for(p.g.d, p.g.G, p.g.wbytes, attn_kind(p.g));
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {const_cast<KernelParams *>(&p)};
     return cudaLaunchCooperativeKernel(k, dim3(n_ctas), dim3(kThreads), args, (size_t)smem_bytes, st);
@@ -76,6 +79,82 @@ cudaError_t quantize_rows_launch(const void *src, int rows, int cols, void *dst,
     quantize_rows_kernel<<<rows, 256, 0, st>>>(reinterpret_cast<const uint16_t *>(src), rows, cols,
                                                reinterpret_cast<uint8_t *>(dst), scale, row_step, row0,
                                                offset);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ INT8 KV cache
+// The INT8 cache of prefilled positions ("History and roadmap", M8: INT8 KV
+// cache with smoothed keys; the plainest scheme, as the pages give none).
+// Key shift of each (layer, KV head): mu_j = sum_t K[t][j] / n in FP64, in
+// position order (one thread per channel), rounded to FP32; 0 when n = 0.
+__global__ void kv8_mean_kernel(const uint16_t *__restrict__ K, int max_pos, int d, int n,
+                                float *__restrict__ mu) {
+    const int z = blockIdx.x, j = threadIdx.x;
+    if (j >= d) return;
+    const uint16_t *k = K + (size_t)z * max_pos * d + j;
+    double acc = 0.0;
+    for (int t = 0; t < n; ++t) acc += (double)bf2f(k[(size_t)t * d]);
+    mu[(size_t)z * d + j] = n > 0 ? (float)(acc / n) : 0.f;
+}
+
+// Rows [t0, t0 + 64) of head z: one warp per row, keys minus mu and values
+// quantized (s = max |x| / 127, codes x / s rounded to nearest even, clamped
+// to +-127, FP32). Key codes go out row by row; value codes are staged and
+// written transposed ([d][MP]) in 64-byte runs.
+template <int D>
+__global__ void __launch_bounds__(256) kv8_quant_kernel(const uint16_t *__restrict__ K, const uint16_t *__restrict__ V,
+                                                        int max_pos, int mp, int n, const float *__restrict__ mu,
+                                                        int8_t *__restrict__ kq, float *__restrict__ ks,
+                                                        int8_t *__restrict__ vq, float *__restrict__ vs) {
+    constexpr int E = D / 32;
+    __shared__ int8_t vt[D][64];
+    const int z = blockIdx.y, t0 = blockIdx.x * 64, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const float *m = mu + (size_t)z * D;
+    for (int tt = w; tt < 64; tt += 8) {
+        const int t = t0 + tt;
+        if (t >= n) break;
+        const size_t row = (size_t)z * max_pos + t;
+        for (int kv = 0; kv < 2; ++kv) {
+            float x[E], amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const int j = lane + 32 * e;
+                x[e] = kv == 0 ? __fsub_rn(bf2f(K[row * D + j]), m[j]) : bf2f(V[row * D + j]);
+                amax = fmaxf(amax, fabsf(x[e]));
+            }
+            amax = warp_max(amax);
+            const float sc = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                float qf = sc > 0.f ? rintf(__fdiv_rn(x[e], sc)) : 0.f;
+                const int8_t c = (int8_t)fminf(fmaxf(qf, -127.f), 127.f);
+                if (kv == 0)
+                    kq[((size_t)z * mp + t) * D + lane + 32 * e] = c;
+                else
+                    vt[lane + 32 * e][tt] = c;
+            }
+            if (lane == 0) (kv == 0 ? ks : vs)[(size_t)z * mp + t] = sc;
+        }
+    }
+    __syncthreads();
+    const int nt = n - t0 < 64 ? n - t0 : 64;
+    for (int i = threadIdx.x; i < D * 64; i += 256) {
+        const int j = i / 64, tt = i % 64;
+        if (tt < nt) vq[((size_t)z * D + j) * mp + t0 + tt] = vt[j][tt];
+    }
+}
+
+cudaError_t kv8_from_bf16_launch(const uint16_t *k, const uint16_t *v, int Z, int max_pos, int mp, int d,
+                                 int n_pos, int8_t *kq, float *ks, float *mu, int8_t *vq, float *vs,
+                                 cudaStream_t st) {
+    kv8_mean_kernel<<<Z, d, 0, st>>>(k, max_pos, d, n_pos, mu);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || n_pos == 0) return e;
+    const dim3 grid((unsigned)((n_pos + 63) / 64), (unsigned)Z);
+    if (d == 64)
+        kv8_quant_kernel<64><<<grid, 256, 0, st>>>(k, v, max_pos, mp, n_pos, mu, kq, ks, vq, vs);
+    else
+        kv8_quant_kernel<128><<<grid, 256, 0, st>>>(k, v, max_pos, mp, n_pos, mu, kq, ks, vq, vs);
     return cudaGetLastError();
 }
 

@@ -102,6 +102,14 @@ __device__ __forceinline__ void tensor_g2s_3d(void *dst, const TensorMap *map, i
         : "memory");
 }
 
+__device__ __forceinline__ void tensor_g2s_2d(void *dst, const TensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Tensor-core helpers of the attention tiles: four 8x8 BF16 matrices from
 // shared memory (lanes 8i..8i+7 give the row addresses of matrix i), plain or
 // transposed, and one m16n8k16 BF16 MMA with FP32 accumulation.
@@ -138,6 +146,29 @@ __device__ __forceinline__ void mma_rows8(float &c0, float &c1, uint32_t a0, uin
 // index mod 8.
 __device__ __forceinline__ uint32_t swz_off(int kvb, int r, int u) {
     return ((uint32_t)(u >> 3) * (uint32_t)kvb + (uint32_t)r) * 128u + ((uint32_t)((u & 7) ^ (r & 7)) << 4);
+}
+
+// Byte offset of 16-byte unit u of row r in an INT8 cache tile written by the
+// tiled copy with rows of RB bytes (64 or 128) and the swizzle of that width:
+// the unit index is XORed with bits 7.. of the row's offset (128-byte rows:
+// r mod 8; 64-byte rows: (r / 2) mod 4). Tiles start 1024-byte aligned.
+template <int RB>
+__device__ __forceinline__ uint32_t swz8_off(int r, int u) {
+    static_assert(RB == 64 || RB == 128, "swizzled rows are 64 or 128 bytes");
+    if (RB == 128) return (uint32_t)r * 128u + ((uint32_t)(u ^ (r & 7)) << 4);
+    return (uint32_t)r * 64u + ((uint32_t)(u ^ ((r >> 1) & 3)) << 4);
+}
+
+// Four INT8 codes (bytes c0..c3 of w) as two BF16 pairs (c0, c1) and (c2, c3),
+// exactly. With the byte 0x43 above it, a byte b is the BF16 number whose
+// exponent carries b's top bit: 128 + (b & 127) when that bit is clear; so
+// (0x43, c & 127) - (0x43, c & 128) is 128 + (c & 127) - 128 = c for c >= 0
+// and 128 + (c + 128) - 256 = c for c < 0. One exact BF16 subtraction per pair.
+__device__ __forceinline__ void codes_bf16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t x0 = __byte_perm(w, 0x43434343u, 0x4140);  // [c0, 0x43, c1, 0x43]
+    const uint32_t x1 = __byte_perm(w, 0x43434343u, 0x4342);  // [c2, 0x43, c3, 0x43]
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(x0 & 0xFF7FFF7Fu), "r"(x0 & 0xFF80FF80u));
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(x1 & 0xFF7FFF7Fu), "r"(x1 & 0xFF80FF80u));
 }
 
 __device__ __forceinline__ void bulk_g2s_nohint(void *dst, const void *src, uint32_t bytes,
@@ -536,6 +567,33 @@ struct Producer {
         ++j;
     }
 
+    // INT8 cache: the kv_block positions from q0 of kv head `h` as four tiles
+    // (key codes [kv_block][d], value codes [d][kv_block], key scales, value
+    // scales). Rows past the tensor arrive as zeros; positions from P on are
+    // stale and are masked or overwritten by the consumer.
+    __device__ void kv_chunk_q8(int layer, int h, int q0) {
+        if (!owns(j)) {
+            ++j;
+            return;
+        }
+        uint64_t *bar;
+        uint8_t *dst = acquire(&bar);
+        if (!dst) return;
+        if (smem_u32(dst) & 1023u) {
+            atomicOr(p.status, kDevBounds);
+            ok = false;
+            return;
+        }
+        const Geom &g = p.g;
+        const int z = layer * g.nkv + h;
+        mbar_expect_tx(bar, (uint32_t)kv8_chunk_bytes(g.d));
+        tensor_g2s_3d(dst, &p.kv_map[0], 0, q0, z, bar);
+        tensor_g2s_3d(dst + 8192, &p.kv_map[1], q0, 0, z, bar);
+        tensor_g2s_2d(dst + 16384, &p.kv_map[2], q0, z, bar);
+        tensor_g2s_2d(dst + 16384 + g.kv_block * 4, &p.kv_map[3], q0, z, bar);
+        ++j;
+    }
+
     // K/V of positions written by step st-1 may be read only after this CTA's
     // consumers acquired the end of step st-1 (they publish that in step_ready).
     int ready = 0;
@@ -558,8 +616,11 @@ struct Producer {
         return true;
     }
 
-    template <bool MMA>
+    // AK: attention kind of the kernel instance (0 shared chunks only, 1 with
+    // the tensor-core form, 2 INT8 cache)
+    template <int AK>
     __device__ __forceinline__ void run(int cta) {
+        constexpr bool MMA = AK >= 1;
         const Geom &g = p.g;
         const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
         fence_proxy_async_global();
@@ -588,7 +649,9 @@ struct Producer {
                         for (int b = b0; b < b1 && ok; ++b) {
                             int q0 = b * g.kv_block, q1 = q0 + g.kv_block;
                             if (q1 > P) q1 = P;  // position P itself is computed in this step
-                            if (mma)
+                            if (AK == 2)
+                                kv_chunk_q8(t.layer, h, q0);
+                            else if (mma)
                                 kv_chunk_tensor(t.layer, h, q0);
                             else
                                 kv_chunk(t.layer, h, q0, q1);
@@ -701,7 +764,7 @@ struct Prefetcher {
                         if (!range(a + skip, bytes - skip, pos + skip)) return;
                     }
                     pos += bytes;
-                } else if (t.op == TILES_OP_ATTN) {
+                } else if (t.op == TILES_OP_ATTN && !g.kv8) {
                     // cached positions only: position P is written in this step
                     for (uint32_t it = t.begin; it < t.end; ++it) {
                         const int h = (int)(it / (uint32_t)g.kv_splits);
@@ -1149,6 +1212,8 @@ struct Consumer {
         float *prob;       // [warps][32][G]
         float *wstate;     // [warps][G][4 + d]
         uint16_t *qh;      // [G][d + 8] bf16 q (rows padded: conflict-free MMA fragment loads)
+        int8_t *k8, *v8;   // INT8 cache: codes of the new key (minus mu) and value rows [d]
+        float *s8;         // and their scales [2]
     };
     __device__ AttnSmem attn_smem() const {
         const Geom &g = p.g;
@@ -1165,13 +1230,37 @@ struct Consumer {
         a.wstate = reinterpret_cast<float *>(b);
         b += (size_t)kConsumerWarps * g.G * (kPartialPad + g.d) * 4;
         a.qh = reinterpret_cast<uint16_t *>(b);
+        b += (size_t)g.G * (g.d + 8) * 2;
+        a.k8 = reinterpret_cast<int8_t *>(b);
+        a.v8 = a.k8 + g.d;
+        a.s8 = reinterpret_cast<float *>(b + 2 * g.d);
         return a;
     }
 
     // q heads of kv head h (and k, v of head h): optional RMSNorm over the head,
     // RoPE at position P, rounding to bf16. One warp per head.
-    template <int D, bool MMA>
+    // One row of the INT8 cache from its FP32 values x (lane holds elements
+    // lane + 32 e): s = max |x| / 127, codes x / s rounded to nearest even and
+    // clamped to +-127, all FP32 (an all-zero row: s = 0, codes 0).
+    template <int E>
+    __device__ __forceinline__ void quantize_row8(const float (&x)[E], int8_t *codes, float *scale) {
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+        amax = warp_max(amax);
+        const float sc = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            float qf = sc > 0.f ? rintf(__fdiv_rn(x[e], sc)) : 0.f;
+            qf = fminf(fmaxf(qf, -127.f), 127.f);
+            codes[lane + 32 * e] = (int8_t)qf;
+        }
+        if (lane == 0) *scale = sc;
+    }
+
+    template <int D, int AK>
     __device__ void prep_qkv(int h, const AttnSmem &a) {
+        constexpr bool MMA = AK >= 1, KV8 = AK == 2;
         const Geom &g = p.g;
         const LayerPtrs &lw = p.layers[cur_layer];
         const float *cs = p.rope_cos + (size_t)P * (D / 2);
@@ -1203,6 +1292,11 @@ struct Consumer {
             if (!is_q && !is_k) {
 #pragma unroll
                 for (int e = 0; e < E; ++e) a.vnew[lane + 32 * e] = f2bf(v[e]);
+                if (KV8) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) v[e] = round_bf(v[e]);
+                    quantize_row8<E>(v, a.v8, &a.s8[1]);
+                }
                 continue;
             }
             if (p.qk_norm) {
@@ -1234,6 +1328,13 @@ struct Consumer {
             } else {
 #pragma unroll
                 for (int e = 0; e < E; ++e) a.knew[lane + 32 * e] = f2bf(v[e]);
+                if (KV8) {
+                    // the cached key is the rounded key minus this head's shift mu
+                    const float *mu = p.mu8 + (size_t)(cur_layer * g.nkv + h) * D;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) v[e] = __fsub_rn(round_bf(v[e]), mu[lane + 32 * e]);
+                    quantize_row8<E>(v, a.k8, &a.s8[0]);
+                }
             }
         }
     }
@@ -1328,6 +1429,122 @@ struct Consumer {
                     mma_rows8(o[j][0], o[j][1], alo[ps][0], alo[ps][1], b[0], b[1]);
                     mma_rows8(o[j + 1][0], o[j + 1][1], ahi[ps][0], ahi[ps][1], b[2], b[3]);
                     mma_rows8(o[j + 1][0], o[j + 1][1], alo[ps][0], alo[ps][1], b[2], b[3]);
+                }
+        }
+    }
+
+    // The INT8-cache form of attn_chunk_mma. The chunk holds key codes
+    // [kvb][D] and value codes transposed [D][kvb] (swizzled tiles), then the
+    // key and value scales. A 32-bit ldmatrix word is four codes: of four
+    // consecutive dims of one position (keys) or four consecutive positions of
+    // one dim (values). They become the B fragment's k slots 2t, 2t+1, 2t+8,
+    // 2t+9, so:
+    //   - q's A fragment takes dims 4t..4t+3 of each 16 in the same slots
+    //     (words 2t and 2t+1 of the k-step: a consistent permutation of the
+    //     summed dims);
+    //   - score n-tile 2i + b (b = 0, 1) holds positions 16 i + 4 (n / 2) +
+    //     2 b + (n & 1) in column n, so that a thread's p values of n-tiles 2i
+    //     and 2i + 1 are exactly the four positions its value word covers.
+    // Key scales multiply the score columns after q . codes; value scales fold
+    // into p (masked positions get exact zeros, so stale codes and scales past
+    // npos never reach the sums); l sums the unscaled p.
+    template <int D, int G>
+    __device__ __forceinline__ void attn_chunk_mma_q8(const uint8_t *slot, int npos, const uint32_t *qrow,
+                                                      bool qrow_ok, float &m, float &l, float (&o)[D / 8][2]) {
+        constexpr int KVB = 8192 / D;  // positions per chunk; also the value tile's row bytes
+        constexpr int SUB = 2048 / D;  // positions per round
+        constexpr int NT = SUB / 8;    // score n-tiles of 8 positions
+        constexpr int PS = SUB / 16;   // k-steps of p V
+        constexpr int NJ = D / 8;      // output n-tiles of 8 dims
+        constexpr int KU = D / 16;     // 16-byte units of a key row
+        const uint32_t kb = smem_u32(slot), vb = kb + 8192u;
+        const float *ksc = reinterpret_cast<const float *>(slot + 16384);
+        const float *vsc = ksc + KVB;
+        const int t4 = lane & 3;
+        const int mi = lane >> 3, ri = lane & 7;
+        for (int p0 = 0; p0 < npos; p0 += SUB) {
+            float sc[NT][2];
+#pragma unroll
+            for (int jn = 0; jn < NT; ++jn) {
+                float c0 = 0.f, c1 = 0.f;
+                const int kr = p0 + 16 * (jn >> 1) + 4 * (ri >> 1) + 2 * (jn & 1) + (ri & 1);
+#pragma unroll
+                for (int u0 = 0; u0 < KU; u0 += 4) {
+                    uint32_t b[4];
+                    ldsm_x4(kb + swz8_off<D>(kr, u0 + mi), b);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int ks = u0 + i;
+                        uint32_t blo, bhi;
+                        codes_bf16x2(b[i], blo, bhi);
+                        const uint32_t qa0 = qrow_ok ? qrow[8 * ks] : 0u, qa2 = qrow_ok ? qrow[8 * ks + 1] : 0u;
+                        mma_rows8(c0, c1, qa0, qa2, blo, bhi);
+                    }
+                }
+                sc[jn][0] = c0;
+                sc[jn][1] = c1;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int ps = 0; ps < PS; ++ps) {
+                const float4 kq = *reinterpret_cast<const float4 *>(ksc + p0 + 16 * ps + 4 * t4);
+                const float ks4[4] = {kq.x, kq.y, kq.z, kq.w};
+#pragma unroll
+                for (int b = 0; b < 2; ++b)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int pos = p0 + 16 * ps + 4 * t4 + 2 * b + e;
+                        float &x = sc[2 * ps + b][e];
+                        x = pos < npos ? (x * ks4[2 * b + e]) * p.attn_scale : -INFINITY;
+                        mx = fmaxf(mx, x);
+                    }
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+            const float mn = fmaxf(m, mx);
+            const float corr = expf(m - mn);
+            float ls = 0.f;
+            uint32_t ahi[PS][2], alo[PS][2];
+#pragma unroll
+            for (int ps = 0; ps < PS; ++ps) {
+                const float4 vq = *reinterpret_cast<const float4 *>(vsc + p0 + 16 * ps + 4 * t4);
+                const float vs4[4] = {vq.x, vq.y, vq.z, vq.w};
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const int pos = p0 + 16 * ps + 4 * t4 + 2 * b;
+                    const float p0f = expf(sc[2 * ps + b][0] - mn), p1f = expf(sc[2 * ps + b][1] - mn);
+                    ls += p0f + p1f;
+                    const float w0 = pos < npos ? p0f * vs4[2 * b] : 0.f;
+                    const float w1 = pos + 1 < npos ? p1f * vs4[2 * b + 1] : 0.f;
+                    const uint16_t h0 = f2bf(w0), h1 = f2bf(w1);
+                    const uint16_t r0 = f2bf(__fsub_rn(w0, bf2f(h0))), r1 = f2bf(__fsub_rn(w1, bf2f(h1)));
+                    ahi[ps][b] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+                    alo[ps][b] = (uint32_t)r0 | ((uint32_t)r1 << 16);
+                }
+            }
+            ls += __shfl_xor_sync(0xFFFFFFFFu, ls, 1);
+            ls += __shfl_xor_sync(0xFFFFFFFFu, ls, 2);
+            l = fmaf(l, corr, ls);
+            m = mn;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                o[j][0] *= corr;
+                o[j][1] *= corr;
+            }
+#pragma unroll
+            for (int ps = 0; ps < PS; ++ps)
+#pragma unroll
+                for (int j = 0; j < NJ; j += 4) {
+                    // dims 8 (j + mi) + ri, positions p0 + 16 ps .. + 15: n-tiles j .. j + 3
+                    uint32_t b[4];
+                    ldsm_x4(vb + swz8_off<KVB>(8 * (j + mi) + ri, (p0 >> 4) + ps), b);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t blo, bhi;
+                        codes_bf16x2(b[i], blo, bhi);
+                        mma_rows8(o[j + i][0], o[j + i][1], ahi[ps][0], ahi[ps][1], blo, bhi);
+                        mma_rows8(o[j + i][0], o[j + i][1], alo[ps][0], alo[ps][1], blo, bhi);
+                    }
                 }
         }
     }
@@ -1467,8 +1684,31 @@ struct Consumer {
         __syncwarp();
     }
 
-    template <int D, int G, bool MMA>
+    // The INT8 form: row r = P - q0 of the chunk gets the new key codes (one
+    // row of the key tile), value codes (one column of the transposed value
+    // tile) and both scales. The other stale rows stay: they are masked.
+    template <int D>
+    __device__ __forceinline__ void place_new_kv_q8(uint8_t *slot, int q0) {
+        constexpr int KVB = 8192 / D;
+        const AttnSmem a = attn_smem();
+        const int r = P - q0;
+        uint8_t *vt = slot + 8192;
+        float *ksc = reinterpret_cast<float *>(slot + 16384);
+        for (int e = lane; e < D; e += 32) {
+            slot[swz8_off<D>(r, e >> 4) + (e & 15)] = (uint8_t)a.k8[e];
+            vt[swz8_off<KVB>(e, r >> 4) + (r & 15)] = (uint8_t)a.v8[e];
+        }
+        if (lane == 0) {
+            ksc[r] = a.s8[0];
+            ksc[KVB + r] = a.s8[1];
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+    template <int D, int G, int AK>
     __device__ void attn_task(const tiles_task &t) {
+        constexpr bool MMA = AK >= 1, KV8 = AK == 2;
         const Geom &g = p.g;
         const AttnSmem a = attn_smem();
         constexpr int DPL = D / 32;
@@ -1478,7 +1718,7 @@ struct Consumer {
             const int c = (int)(it % (uint32_t)g.kv_splits);
             if (h != prepared) {
                 consumer_sync();  // previous item finished reading q / knew / vnew
-                prep_qkv<D, MMA>(h, a);
+                prep_qkv<D, AK>(h, a);
                 consumer_sync();
                 if (cur_tr && tid == 0 && prepared < 0) cur_tr[kTrPrologue] = global_timer();
                 prepared = h;
@@ -1489,9 +1729,19 @@ struct Consumer {
             const bool has_new = pb >= b0 && pb < b1;
             if (has_new && tid < D) {
                 // the one tile whose range holds position P writes the new K/V
-                const size_t off = ((size_t)(cur_layer * g.nkv + h) * g.max_pos + P) * D + tid;
-                p.k_cache[off] = a.knew[tid];
-                p.v_cache[off] = a.vnew[tid];
+                if (KV8) {
+                    const size_t z = (size_t)(cur_layer * g.nkv + h);
+                    p.kq8[(z * g.kv_mp + P) * D + tid] = a.k8[tid];
+                    p.vq8[(z * D + tid) * g.kv_mp + P] = a.v8[tid];
+                    if (tid == 0) {
+                        p.ks8[z * g.kv_mp + P] = a.s8[0];
+                        p.vs8[z * g.kv_mp + P] = a.s8[1];
+                    }
+                } else {
+                    const size_t off = ((size_t)(cur_layer * g.nkv + h) * g.max_pos + P) * D + tid;
+                    p.k_cache[off] = a.knew[tid];
+                    p.v_cache[off] = a.vnew[tid];
+                }
                 fence_proxy_async_global();
             }
             float m[G], l[G], o[G][DPL];
@@ -1503,7 +1753,7 @@ struct Consumer {
                 for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
             }
             const uint32_t nch = (uint32_t)(b1 - b0);
-            if (!(MMA && attn_uses_mma(g, (int)nch))) {
+            if (!KV8 && !(MMA && attn_uses_mma(g, (int)nch))) {
                 // few chunks: every warp works on every chunk (one q head, some sub-blocks)
                 const int hi = warp % G, sb0 = warp / G, sbs = kConsumerWarps / G;
                 const int lp = attn_lanes_per_pos(sbs);
@@ -1551,7 +1801,9 @@ struct Consumer {
                 // many chunks: each chunk goes to its slot's owner warp, all q heads, tensor cores
                 const int g8 = lane >> 2, t4 = lane & 3;
                 // q head g8 as BF16 pairs (dims 2t4 + 16ks (+8) in word t4 + 8ks (+4))
-                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.qh + (size_t)(g8 < G ? g8 : 0) * (D + 8)) + t4;
+                // (the INT8 form reads words 2 t4 and 2 t4 + 1 of each k-step instead)
+                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.qh + (size_t)(g8 < G ? g8 : 0) * (D + 8)) +
+                                       (KV8 ? 2 * t4 : t4);
                 float mm = -INFINITY, ll = 0.f, oo[D / 8][2];
 #pragma unroll
                 for (int jd = 0; jd < D / 8; ++jd) oo[jd][0] = oo[jd][1] = 0.f;
@@ -1563,8 +1815,13 @@ struct Consumer {
                     const int q0 = (b0 + (int)k) * g.kv_block;
                     int q1 = q0 + g.kv_block;
                     if (q1 > P + 1) q1 = P + 1;
-                    if (q0 <= P && P < q1) place_new_kv_swz<D>(slot, q0);
-                    attn_chunk_mma<D, G>(slot, q1 - q0, qrow, g8 < G, mm, ll, oo);
+                    if (KV8) {
+                        if (q0 <= P && P < q1) place_new_kv_q8<D>(slot, q0);
+                        attn_chunk_mma_q8<D, G>(slot, q1 - q0, qrow, g8 < G, mm, ll, oo);
+                    } else {
+                        if (q0 <= P && P < q1) place_new_kv_swz<D>(slot, q0);
+                        attn_chunk_mma<D, G>(slot, q1 - q0, qrow, g8 < G, mm, ll, oo);
+                    }
                     release_chunk(jj);
                 }
                 // per-warp states -> shared memory (row g8 = q head g8)
@@ -1675,7 +1932,7 @@ struct Consumer {
     // ---------------------------------------------------------- main loop
     // D (head_dim), G (q heads per KV head) and the weight format (Q8: INT8
     // codes) are compile-time: each kernel instance carries only its own code.
-    template <int D, int G, bool Q8, bool MMA>
+    template <int D, int G, bool Q8, int AK>
     __device__ __forceinline__ void run(int cta) {
         const Geom &g = p.g;
         const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
@@ -1720,7 +1977,7 @@ struct Consumer {
                         gemv_task<1, Q8>(t);
                         break;
                     case TILES_OP_ATTN:
-                        attn_task<D, G, MMA>(t);
+                        attn_task<D, G, AK>(t);
                         break;
                     case TILES_OP_OPROJ:
                         gather_tagged(p.ow, g.qd, tag(t.layer, kTagO));
@@ -1778,7 +2035,9 @@ struct Consumer {
     }
 };
 
-template <int D, int G, bool Q8, bool MMA>
+// AK, the attention kind: 0 shared chunks only; 1 also the tensor-core form
+// for long splits; 2 INT8 KV cache (tensor-core form only).
+template <int D, int G, bool Q8, int AK>
 __global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_constant__ KernelParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Smem s = smem_layout(smem_raw, p);
@@ -1805,12 +2064,12 @@ __global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_con
     if (tid >= kConsumerWarps * 32) {
         if ((tid & 31) == 0) {
             Producer prod(p, s, (tid >> 5) - kConsumerWarps);
-            prod.template run<MMA>(blockIdx.x);
+            prod.template run<AK>(blockIdx.x);
         }
         return;
     }
     Consumer cons(p, s, tid);
-    cons.template run<D, G, Q8, MMA>(blockIdx.x);
+    cons.template run<D, G, Q8, AK>(blockIdx.x);
 }
 
 }  // namespace tiles

@@ -33,10 +33,12 @@ static bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 static int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
 // Attention scratch in the vec region: q [G][d] f32, new k and v [d] bf16,
-// per-warp probabilities [32][G] f32, per-warp states [G][4 + d] f32.
+// per-warp probabilities [32][G] f32, per-warp states [G][4 + d] f32, q as
+// bf16 [G][d + 8], and the INT8 cache's new key and value codes [d] with
+// their two scales.
 static int attn_vec_bytes(int G, int d) {
     return G * d * 4 + 2 * d * 2 + kConsumerWarps * 32 * G * 4 +
-           kConsumerWarps * G * (kPartialPad + d) * 4 + G * (d + 8) * 2;
+           kConsumerWarps * G * (kPartialPad + d) * 4 + G * (d + 8) * 2 + 2 * d + 8;
 }
 
 tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o, int n_ctas,
@@ -101,8 +103,14 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     // reduces it, and smaller chunks turn the ring over faster. Measured on
     // GB300 for the Llama-1B shape: 8 x 16 KB beat 6 x 32 KB by 6 % and
     // 12 x 16 KB (uneven ownership) by 2 %.
+    if (o.kv_format != TILES_KV_BF16 && o.kv_format != TILES_KV_INT8)
+        return fail(TILES_ERR_INVALID_ARG, "kv_format");
+    G_.kv8 = o.kv_format == TILES_KV_INT8 ? 1 : 0;
+    G_.kv_mp = round_up(G_.max_pos, 16);
     const int wb = G_.wbytes;
-    int need = std::max({wb * G_.H, wb * G_.qd, wb * G_.F, 2 * wb * G_.H});
+    // an INT8 KV chunk (codes of 8 KB of keys and 8 KB of values, and their
+    // scales) fills one slot
+    int need = std::max({wb * G_.H, wb * G_.qd, wb * G_.F, 2 * wb * G_.H, G_.kv8 ? kv8_chunk_bytes(G_.d) : 0});
     int slot = o.slot_bytes > 0 ? o.slot_bytes : round_up(std::max(need, 16384), 1024);
     if (slot % 1024 || slot < need) return fail(TILES_ERR_INVALID_ARG, "slot_bytes too small or not a multiple of 1024");
     G_.slot_bytes = slot;
@@ -127,6 +135,7 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     int kb = slot / (2 * G_.d * 2);
     kb = kb >= 32 ? kb / 32 * 32 : kb;
     kb = std::min(kb, 256);  // a chunk's positions are one TMA box (at most 256 rows)
+    if (G_.kv8) kb = kv8_block(G_.d);
     if (kb < 1) return fail(TILES_ERR_UNSUPPORTED, "slot too small for one KV position");
     G_.kv_block = kb;
     int nb_max = ceil_div(G_.max_pos, kb);
@@ -142,6 +151,7 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     // without it, whose registers it would otherwise crowd (measured 2.5 %
     // on the Llama-1B shape at 1,023 positions)
     G_.attn_mma = (ceil_div(nb_max, splits) >= kConsumerWarps && kb % (2048 / G_.d) == 0) ? 1 : 0;
+    if (G_.kv8) G_.attn_mma = 1;  // the INT8 cache has only the tensor-core form
 
     // an attention tile merges a 1/S slice of its KV head's G d outputs,
     // staging (m, l, o) of every (output, split) pair: 3 floats each
@@ -432,7 +442,10 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
         if (r < 1 || (long long)r * op_in_dim(g, op) * g.wbytes * op_mats(op) > g.slot_bytes)
             return fail("rows per chunk do not fit a slot");
     }
-    if (g.kv_block < 1 || g.kv_block > 256 || 2LL * g.kv_block * g.d * 2 > g.slot_bytes) return fail("kv block");
+    const long long kv_chunk = g.kv8 ? kv8_chunk_bytes(g.d) : 2LL * g.kv_block * g.d * 2;
+    if (g.kv_block < 1 || g.kv_block > 256 || kv_chunk > g.slot_bytes) return fail("kv block");
+    if (g.kv8 && (g.kv_block != kv8_block(g.d) || !g.attn_mma || g.kv_mp % 16 || g.kv_mp < g.max_pos))
+        return fail("INT8 KV chunk geometry");
     if (g.smem_bytes > kSmemLimit) return fail("shared memory");
     if (s.n_counters < 1 || s.n_counters > 0xFFFE) return fail("counter count");
 
@@ -649,6 +662,7 @@ tiles_status_t tiles_schedule_get_info(tiles_schedule_t sched, tiles_plan_info *
     info->rows_per_chunk[3] = g.rpc_down;
     info->rows_per_chunk[4] = g.rpc_lm;
     info->weight_format = g.wbytes == 1 ? TILES_WEIGHTS_INT8 : TILES_WEIGHTS_BF16;
+    info->kv_format = g.kv8 ? TILES_KV_INT8 : TILES_KV_BF16;
     long long tot = 0, mx = 0, mn = -1;
     for (int c = 0; c < s.n_ctas; ++c) {
         long long b = 0;

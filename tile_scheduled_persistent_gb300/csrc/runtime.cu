@@ -18,8 +18,11 @@
 #include "tiles_internal.h"
 
 namespace tiles {
-cudaError_t megakernel_configure(int d, int G, int wbytes, int mma, int smem_bytes);
-cudaError_t megakernel_occupancy(int d, int G, int wbytes, int mma, int smem_bytes, int *blocks_per_sm);
+cudaError_t megakernel_configure(int d, int G, int wbytes, int ak, int smem_bytes);
+cudaError_t megakernel_occupancy(int d, int G, int wbytes, int ak, int smem_bytes, int *blocks_per_sm);
+cudaError_t kv8_from_bf16_launch(const uint16_t *k, const uint16_t *v, int Z, int max_pos, int mp, int d,
+                                 int n_pos, int8_t *kq, float *ks, float *mu, int8_t *vq, float *vs,
+                                 cudaStream_t st);
 cudaError_t quantize_rows_launch(const void *src, int rows, int cols, void *dst, float *scale,
                                  int row_step, int row0, int offset, cudaStream_t st);
 cudaError_t megakernel_launch(const KernelParams &p, int n_ctas, int smem_bytes, cudaStream_t st);
@@ -156,9 +159,9 @@ tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weigh
     const Geom &g = plan->sched.geom;
 
     // the worker must fit one CTA per SM at this shared-memory size (co-residency)
-    e = megakernel_configure(g.d, g.G, g.wbytes, g.attn_mma, g.smem_bytes);
+    e = megakernel_configure(g.d, g.G, g.wbytes, attn_kind(g), g.smem_bytes);
     int occ = 0;
-    if (e == cudaSuccess) e = megakernel_occupancy(g.d, g.G, g.wbytes, g.attn_mma, g.smem_bytes, &occ);
+    if (e == cudaSuccess) e = megakernel_occupancy(g.d, g.G, g.wbytes, attn_kind(g), g.smem_bytes, &occ);
     if (e != cudaSuccess || occ < 1) {
         delete plan;
         return e != cudaSuccess ? TILES_ERR_CUDA : TILES_ERR_UNSUPPORTED;
@@ -391,6 +394,74 @@ static tiles_status_t encode_kv_maps(const Geom &g, void *k_cache, void *v_cache
     return TILES_OK;
 }
 
+// The INT8 cache's two buffers (layout stated with tiles_kv8_layout).
+static void kv8_layout_of(int Z, int max_pos, int d, tiles_kv8_layout *o) {
+    auto up = [](int64_t v) { return (v + 255) / 256 * 256; };
+    const int64_t mp = ((int64_t)max_pos + 15) / 16 * 16;
+    o->pos_stride = (int32_t)mp;
+    o->k_scale_off = up((int64_t)Z * mp * d);
+    o->k_mu_off = up(o->k_scale_off + (int64_t)Z * mp * 4);
+    o->k_bytes = o->k_mu_off + (int64_t)Z * d * 4;
+    o->v_scale_off = up((int64_t)Z * d * mp);
+    o->v_bytes = o->v_scale_off + (int64_t)Z * mp * 4;
+}
+
+// TMA descriptors of an INT8 cache: key codes [Z][MP][d] (box kv_block x d),
+// value codes [Z][d][MP] (box d x kv_block), each swizzled by its row length
+// (64 or 128 bytes) so the fragment loads spread over the banks, and the
+// scales [Z][MP] (box kv_block). Positions past MP read as zero.
+static tiles_status_t encode_kv8_maps(const Geom &g, void *k8, void *v8, KernelParams *p) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return TILES_ERR_CUDA;
+    tiles_kv8_layout lay;
+    kv8_layout_of(g.L * g.nkv, g.max_pos, g.d, &lay);
+    const cuuint64_t Z = (cuuint64_t)g.L * (cuuint64_t)g.nkv, mp = (cuuint64_t)lay.pos_stride, d = (cuuint64_t)g.d;
+    const cuuint32_t kvb = (cuuint32_t)g.kv_block, ones[3] = {1, 1, 1};
+    auto sw = [](cuuint64_t row_bytes) {
+        return row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    };
+    CUtensorMap m[4];
+    {
+        const cuuint64_t dims[3] = {d, mp, Z}, strides[2] = {d, mp * d};
+        const cuuint32_t box[3] = {(cuuint32_t)d, kvb, 1};
+        if (enc(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, k8, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                sw(d), CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TILES_ERR_CUDA;
+    }
+    {
+        const cuuint64_t dims[3] = {mp, d, Z}, strides[2] = {mp, d * mp};
+        const cuuint32_t box[3] = {kvb, (cuuint32_t)d, 1};
+        if (enc(&m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, v8, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                sw(kvb), CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TILES_ERR_CUDA;
+    }
+    void *scales[2] = {static_cast<char *>(k8) + lay.k_scale_off, static_cast<char *>(v8) + lay.v_scale_off};
+    for (int i = 0; i < 2; ++i) {
+        const cuuint64_t dims[2] = {mp, Z}, strides[1] = {mp * 4};
+        const cuuint32_t box[2] = {kvb, 1};
+        if (enc(&m[2 + i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, scales[i], dims, strides, box, ones,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TILES_ERR_CUDA;
+    }
+    std::memcpy(p->kv_map, m, sizeof m);
+    p->k_cache = p->v_cache = nullptr;
+    p->kq8 = static_cast<int8_t *>(k8);
+    p->ks8 = reinterpret_cast<float *>(static_cast<char *>(k8) + lay.k_scale_off);
+    p->mu8 = reinterpret_cast<const float *>(static_cast<char *>(k8) + lay.k_mu_off);
+    p->vq8 = static_cast<int8_t *>(v8);
+    p->vs8 = reinterpret_cast<float *>(static_cast<char *>(v8) + lay.v_scale_off);
+    return TILES_OK;
+}
+
+// The caches of one decode call: pointers and TMA descriptors in p.
+static tiles_status_t bind_caches(const Geom &g, void *k_cache, void *v_cache, KernelParams *p) {
+    if (g.kv8) return encode_kv8_maps(g, k_cache, v_cache, p);
+    p->k_cache = reinterpret_cast<uint16_t *>(k_cache);
+    p->v_cache = reinterpret_cast<uint16_t *>(v_cache);
+    return encode_kv_maps(g, k_cache, v_cache, p);
+}
+
 tiles_status_t tiles_decode(tiles_plan_t plan, void *k_cache, void *v_cache, const int32_t *prompt,
                             int32_t n_prompt, int32_t start_pos, int32_t n_new, void *stream,
                             int32_t *out_tokens, float *out_logits) {
@@ -406,9 +477,7 @@ tiles_status_t tiles_decode(tiles_plan_t plan, void *k_cache, void *v_cache, con
     if (st != TILES_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     KernelParams p = plan->base;
-    p.k_cache = reinterpret_cast<uint16_t *>(k_cache);
-    p.v_cache = reinterpret_cast<uint16_t *>(v_cache);
-    if ((st = encode_kv_maps(g, k_cache, v_cache, &p)) != TILES_OK) return st;
+    if ((st = bind_caches(g, k_cache, v_cache, &p)) != TILES_OK) return st;
     p.prompt = prompt;
     p.n_prompt = n_prompt;
     p.out_tokens = out_tokens;
@@ -482,6 +551,31 @@ tiles_status_t tiles_quantize_rows_int8(const void *w_bf16, int32_t rows, int32_
     if (rows < 0 || cols < 1 || (rows > 0 && (!w_bf16 || !codes || !scales))) return TILES_ERR_INVALID_ARG;
     const cudaError_t e = quantize_rows_launch(w_bf16, rows, cols, codes, scales, 1, 0, 0,
                                                reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TILES_OK : TILES_ERR_CUDA;
+}
+
+tiles_status_t tiles_kv8_get_layout(const tiles_model_desc *desc, tiles_kv8_layout *out) {
+    if (!desc || !out || desc->n_layers < 1 || desc->n_kv_heads < 1 || desc->max_pos < 1 || desc->head_dim < 1)
+        return TILES_ERR_INVALID_ARG;
+    kv8_layout_of(desc->n_layers * desc->n_kv_heads, desc->max_pos, desc->head_dim, out);
+    return TILES_OK;
+}
+
+tiles_status_t tiles_kv8_from_bf16(const tiles_model_desc *desc, const void *k_bf16, const void *v_bf16,
+                                   int32_t n_pos, void *k8, void *v8, void *stream) {
+    if (!desc || !k_bf16 || !v_bf16 || !k8 || !v8 || desc->n_layers < 1 || desc->n_kv_heads < 1 ||
+        desc->max_pos < 1 || n_pos < 0 || n_pos > desc->max_pos || !aligned16(k8) || !aligned16(v8))
+        return TILES_ERR_INVALID_ARG;
+    if (desc->head_dim != 64 && desc->head_dim != 128) return TILES_ERR_UNSUPPORTED;
+    tiles_kv8_layout lay;
+    const int Z = desc->n_layers * desc->n_kv_heads, d = desc->head_dim;
+    kv8_layout_of(Z, desc->max_pos, d, &lay);
+    char *kb = static_cast<char *>(k8), *vb = static_cast<char *>(v8);
+    const cudaError_t e = kv8_from_bf16_launch(
+        static_cast<const uint16_t *>(k_bf16), static_cast<const uint16_t *>(v_bf16), Z, desc->max_pos,
+        lay.pos_stride, d, n_pos, reinterpret_cast<int8_t *>(kb), reinterpret_cast<float *>(kb + lay.k_scale_off),
+        reinterpret_cast<float *>(kb + lay.k_mu_off), reinterpret_cast<int8_t *>(vb),
+        reinterpret_cast<float *>(vb + lay.v_scale_off), reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TILES_OK : TILES_ERR_CUDA;
 }
 
@@ -587,9 +681,7 @@ extern "C" tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache,
     if ((st = noalloc_scratch(plan->device, &base)) != TILES_OK) return st;
     KernelParams p = plan->base;
     place_sync_block(plan->sched, base, &p);
-    p.k_cache = reinterpret_cast<uint16_t *>(k_cache);
-    p.v_cache = reinterpret_cast<uint16_t *>(v_cache);
-    if ((st = encode_kv_maps(g, k_cache, v_cache, &p)) != TILES_OK) return st;
+    if ((st = bind_caches(g, k_cache, v_cache, &p)) != TILES_OK) return st;
     p.prompt = prompt;
     p.n_prompt = n_prompt;
     p.out_tokens = out_tokens;

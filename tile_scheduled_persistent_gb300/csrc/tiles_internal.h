@@ -46,7 +46,15 @@ struct Geom {
     int smem_bytes;
     int attn_mma;   // 1: some attention split can reach kConsumerWarps chunks, and the
                     // kernel instance carries the tensor-core attention path
+    int kv8;        // 1: INT8 KV cache (every attention chunk on the tensor-core path)
+    int kv_mp;      // INT8 cache: position stride (max_pos rounded up to 16)
 };
+
+// INT8 KV chunk: kv_block = 8192 / d positions (128 at d = 64, 64 at d = 128):
+// key codes [kv_block][d], value codes transposed [d][kv_block], then the
+// key and value scales, kv_block floats each.
+TILES_HD int kv8_block(int d) { return 8192 / d; }
+TILES_HD int kv8_chunk_bytes(int d) { return 2 * 8192 + 2 * kv8_block(d) * 4; }
 
 TILES_HD int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -147,7 +155,7 @@ TILES_HD long long task_bytes(const Geom &g, const tiles_task &t, int P) {
             attn_split_blocks(g, P + 1, (int)(it % (uint32_t)g.kv_splits), &b0, &b1);
             int p0 = b0 * g.kv_block, p1 = b1 * g.kv_block;
             if (p1 > P) p1 = P;
-            if (p1 > p0) n += (long long)(p1 - p0) * g.d * 2 * 2;
+            if (p1 > p0) n += (long long)(p1 - p0) * (g.kv8 ? 2 * g.d + 8 : g.d * 2 * 2);
         }
         return n;
     }
@@ -189,6 +197,11 @@ struct KernelParams {
     const float *rope_cos, *rope_sin;  // [max_pos][d/2]
     // caches and scratch
     uint16_t *k_cache, *v_cache;
+    // INT8 KV cache (kv8): key codes [Z][kv_mp][d], value codes [Z][d][kv_mp],
+    // scales [Z][kv_mp], key shifts [Z][d] (Z = L n_kv)
+    int8_t *kq8, *vq8;
+    float *ks8, *vs8;
+    const float *mu8;
     // tagged activations: (tag << 16) | bf16 for the residual stream x [H],
     // the SwiGLU output a [F] and the attention output o [nq d];
     // (tag << 32) | f32 bits for the Q/K/V rows and the split partials
@@ -209,10 +222,13 @@ struct KernelParams {
     // optional per-task timeline: [cta][step < trace_steps][task][kTraceWords]
     unsigned long long *trace;
     int trace_steps, trace_tasks;
-    // TMA descriptors of the K and V caches as [L * n_kv][max_pos][d] BF16,
-    // boxes of kv_block positions x 64 dims, 128-byte swizzle (written per
-    // decode call; the kernel takes their addresses in parameter space)
-    TensorMap kv_map[2];
+    // TMA descriptors (written per decode call; the kernel takes their
+    // addresses in parameter space). BF16 cache: [0] K and [1] V as
+    // [L * n_kv][max_pos][d], boxes of kv_block positions x 64 dims, 128-byte
+    // swizzle. INT8 cache: [0] key codes (box kv_block x d), [1] value codes
+    // (box d x kv_block), both swizzled by their row length (64 or 128
+    // bytes); [2] key and [3] value scales (box kv_block).
+    TensorMap kv_map[4];
 };
 
 // trace record words
@@ -225,9 +241,14 @@ constexpr int kTraceWords = 16;
 // consumers decide with the same rule.
 // (The tensor-core form takes 2048 / d positions per round: 32 at d = 64,
 // 16 at d = 128, so kv_block must be a multiple of that.)
+// An INT8 cache has only the tensor-core form: every chunk of every split.
 TILES_HD bool attn_uses_mma(const Geom &g, int n_chunks) {
-    return g.attn_mma && n_chunks >= kConsumerWarps && g.kv_block % (2048 / g.d) == 0;
+    return g.attn_mma && (g.kv8 || (n_chunks >= kConsumerWarps && g.kv_block % (2048 / g.d) == 0));
 }
+// The kernel instance a plan runs: 0 shared-chunk attention only, 1 with the
+// tensor-core form, 2 INT8 KV cache.
+TILES_HD int attn_kind(const Geom &g) { return g.kv8 ? 2 : g.attn_mma; }
+
 enum { kTrWaitStart = 0, kTrWaitEnd, kTrTaskEnd, kTrProdFirst, kTrProdLast, kTrProdStall,
        kTrOpInfo, kTrPrologue, kTrFirstChunk, kTrPartials, kTrMergeIn };
 
