@@ -16,7 +16,7 @@ LIB = os.path.join(HERE, "libtiles.so")
 BUILD = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["megakernel.cu", "kernels_bf16.cu", "kernels_bf16_mma.cu", "kernels_int8.cu", "kernels_int8_mma.cu",
-           "kernels_bf16_kv8.cu", "kernels_int8_kv8.cu", "runtime.cu", "forward.cu", "planner.cpp"]
+           "kernels_bf16_kv8.cu", "kernels_int8_kv8.cu", "runtime.cu", "forward.cu", "gemm_tc.cu", "planner.cpp"]
 HEADERS = ["tiles_internal.h", "megakernel.cuh", "plan_internal.h"]
 
 

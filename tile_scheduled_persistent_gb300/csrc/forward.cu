@@ -10,11 +10,11 @@
 // 512-token prompt).
 //
 // With T columns every weight row is used T times, so the projections are
-// dense contractions: they run on the tensor cores (m16n8k16 BF16 MMAs with
-// FP32 accumulation; weight and activation tiles staged in shared memory by
-// cp.async in a four-stage pipeline, split along K across CTAs when the
-// output alone would not fill the GPU, and the split partial sums added in a
-// fixed order by the kernel that consumes them). Attention is a causal,
+// dense contractions: they run on the fifth-generation tensor cores
+// (gemm_tc.cu: TMA-staged operands, tcgen05.mma with the accumulator in
+// tensor memory, split along K across CTAs when the output alone would not
+// fill the GPU, and the split partial sums added in a fixed order by the
+// kernel that consumes them). Attention is a causal,
 // split-KV, multi-query kernel on the same MMAs (scores in FP32, the softmax
 // weights split into a BF16 high part and a BF16 remainder for the p V
 // product, as in the decode kernel), followed by an ordered combine. Norms,
@@ -34,20 +34,6 @@ namespace tiles {
 namespace fwd {
 
 constexpr int kMaxTokens = 256;  // tokens per pass
-constexpr int kBK = 64;         // K elements per pipeline stage
-constexpr int kStages = 4;
-constexpr int kPad = 8;         // bf16 padding per shared-memory row: conflict-free ldmatrix
-constexpr int kLds = kBK + kPad;
-
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 // c += A B, A 16x16 (row), B 16x8 (col), BF16 in, FP32 accumulate. Fragments
 // for lane (g, t) = (lane / 4, lane % 4): a = {(g, 2t..2t+1), (g+8, 2t..),
@@ -63,78 +49,6 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
-}
-
-// ------------------------------------------------------------------ GEMM
-// C[z][n][m] = sum over k in split z of W[m][k] X[n][k]: W [M][K] row-major
-// (ldw elements per row), X [T][K] row-major, z = blockIdx.z covering
-// K elements [z kps, (z + 1) kps). 8 warps as (8 / WN) x WN; each warp owns a
-// 16 x 16 block of (m, n), so the CTA tile is (16 * 8 / WN) x (16 * WN).
-template <int WN>
-__global__ void __launch_bounds__(256) gemm_tn_kernel(const uint16_t *__restrict__ W, int ldw,
-                                                      const uint16_t *__restrict__ X, int ldx, int M, int T,
-                                                      int K, int kps, float *__restrict__ C) {
-    constexpr int WM = 8 / WN, BM = 16 * WM, BN = 16 * WN;
-    extern __shared__ __align__(128) uint16_t gsm[];
-    uint16_t *sW = gsm;                          // [kStages][BM][kLds]
-    uint16_t *sX = gsm + kStages * BM * kLds;    // [kStages][BN][kLds]
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wm = warp / WN, wn = warp % WN;
-    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-    const int k0 = blockIdx.z * kps, k1 = min(K, k0 + kps);
-    const int nk = (k1 - k0 + kBK - 1) / kBK;
-    auto load = [&](int stage, int kc) {
-        const int kb = k0 + kc * kBK;
-        for (int i = tid; i < BM * (kBK / 8); i += 256) {
-            const int r = i / (kBK / 8), c = (i % (kBK / 8)) * 8;
-            const int m = m0 + r, k = kb + c;
-            const bool ok = m < M && k < k1;  // K and kps are multiples of 8: a piece is whole or absent
-            cp_async16(sW + (size_t)(stage * BM + r) * kLds + c, ok ? W + (size_t)m * ldw + k : W, ok ? 16 : 0);
-        }
-        for (int i = tid; i < BN * (kBK / 8); i += 256) {
-            const int r = i / (kBK / 8), c = (i % (kBK / 8)) * 8;
-            const int n = n0 + r, k = kb + c;
-            const bool ok = n < T && k < k1;
-            cp_async16(sX + (size_t)(stage * BN + r) * kLds + c, ok ? X + (size_t)n * ldx + k : X, ok ? 16 : 0);
-        }
-    };
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-        if (s < nk) load(s, s);
-        cp_async_commit();
-    }
-    for (int kc = 0; kc < nk; ++kc) {
-        cp_async_wait<kStages - 2>();
-        __syncthreads();  // stage kc landed for every thread; stage kc - 1 is free
-        {
-            const int nx = kc + kStages - 1;
-            if (nx < nk) load(nx % kStages, nx);
-            cp_async_commit();
-        }
-        const int st = kc % kStages;
-        const uint16_t *tw = sW + (size_t)(st * BM + wm * 16) * kLds;
-        const uint16_t *tx = sX + (size_t)(st * BN + wn * 16) * kLds;
-#pragma unroll
-        for (int kk = 0; kk < kBK; kk += 16) {
-            uint32_t a[4], b[4];
-            ldsm_x4(smem_u32(tw + (lane & 15) * kLds + kk + (lane >> 4) * 8), a);
-            ldsm_x4(smem_u32(tx + ((lane & 7) + (lane >> 4) * 8) * kLds + kk + ((lane >> 3) & 1) * 8), b);
-            mma16816(acc[0], a, b[0], b[1]);
-            mma16816(acc[1], a, b[2], b[3]);
-        }
-    }
-    cp_async_wait<0>();
-    float *Cz = C + (size_t)blockIdx.z * T * M;
-    const int g = lane >> 2, t4 = lane & 3;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int m = m0 + wm * 16 + g + (e >> 1) * 8;
-            const int n = n0 + wn * 16 + j * 8 + 2 * t4 + (e & 1);
-            if (m < M && n < T) Cz[(size_t)n * M + m] = acc[j][e];
-        }
 }
 
 // ------------------------------------------------------------------ per-token kernels
@@ -478,44 +392,31 @@ __global__ void accept_kernel(const int32_t *inputs, const int32_t *argmax, int 
 }
 
 // ------------------------------------------------------------------ host side
-struct GemmShape {
-    int wn, bm, bn, mt, nt, sk, kps;
-};
-
-GemmShape gemm_shape(int M, int T, int K, int sms, int max_sk) {
-    GemmShape s;
-    s.wn = T <= 16 ? 1 : (T <= 32 ? 2 : 4);
-    s.bm = 16 * (8 / s.wn);
-    s.bn = 16 * s.wn;
-    s.mt = (M + s.bm - 1) / s.bm;
-    s.nt = (T + s.bn - 1) / s.bn;
-    const int nkc = (K + kBK - 1) / kBK;
-    int sk = std::max(1, std::min(nkc, (2 * sms + s.mt * s.nt - 1) / (s.mt * s.nt)));
-    sk = std::min(sk, max_sk);
-    s.kps = ((nkc + sk - 1) / sk) * kBK;
-    s.sk = (K + s.kps - 1) / s.kps;
-    return s;
+// The 2-D BF16 tensor map of an operand, made once per (base, shape, box).
+const TensorMap *operand_map(ForwardScratch &f, const void *base, int inner, int rows, int ld, int box_rows) {
+    const std::array<uint64_t, 5> key = {(uint64_t)(uintptr_t)base, (uint64_t)inner, (uint64_t)rows,
+                                         (uint64_t)ld, (uint64_t)box_rows};
+    for (auto &e : f.maps)
+        if (e.first == key) return &e.second;
+    if (f.maps.size() >= 4096) f.maps.clear();
+    TensorMap m;
+    if (!encode_bf16_2d(&m, base, (uint64_t)inner, (uint64_t)rows, (uint64_t)ld * 2, 64, (uint32_t)box_rows))
+        return nullptr;
+    f.maps.emplace_back(key, m);
+    return &f.maps.back().second;
 }
 
-size_t gemm_smem(int wn) {
-    const int bm = 16 * (8 / wn), bn = 16 * wn;
-    return (size_t)kStages * (bm + bn) * kLds * 2;
-}
-
-// Launches C = W X^T (split partial sums) and returns the split count.
-cudaError_t gemm(const void *W, int ldw, const uint16_t *X, int ldx, int M, int T, int K, float *C, int sms,
-                 int max_sk, int *sk_out, cudaStream_t st) {
-    const GemmShape s = gemm_shape(M, T, K, sms, max_sk);
-    const dim3 grid(s.mt, s.nt, s.sk);
-    const size_t smem = gemm_smem(s.wn);
-    const uint16_t *w = reinterpret_cast<const uint16_t *>(W);
-    switch (s.wn) {
-        case 1: gemm_tn_kernel<1><<<grid, 256, smem, st>>>(w, ldw, X, ldx, M, T, K, s.kps, C); break;
-        case 2: gemm_tn_kernel<2><<<grid, 256, smem, st>>>(w, ldw, X, ldx, M, T, K, s.kps, C); break;
-        default: gemm_tn_kernel<4><<<grid, 256, smem, st>>>(w, ldw, X, ldx, M, T, K, s.kps, C); break;
-    }
+// Launches C = W X^T (split partial sums) on the tensor cores and returns the
+// split count: W [M][K] (ldw elements per row), X [T][K] (ldx).
+cudaError_t gemm(tiles_plan_s *plan, const void *W, int ldw, const uint16_t *X, int ldx, int M, int T, int K,
+                 float *C, int max_sk, int *sk_out, cudaStream_t st) {
+    const TcShape s = tc_shape(M, T, K, plan->sm_count, max_sk);
+    ForwardScratch &f = plan->fwd;
+    const TensorMap *mw = operand_map(f, W, K, M, ldw, kTcM);
+    const TensorMap *mx = mw ? operand_map(f, X, K, T, ldx, s.n_tile) : nullptr;
+    if (!mw || !mx) return cudaErrorInvalidValue;
     *sk_out = s.sk;
-    return cudaGetLastError();
+    return gemm_tc_launch(*mw, *mx, s, M, T, K, C, plan->base.status, plan->base.timeout_ns, st);
 }
 
 // splits of the attention: about two CTAs per SM over the (query block, KV
@@ -559,7 +460,7 @@ tiles_status_t forward_setup(tiles_plan_s *plan) {
     for (int T = 1; T <= Tm; ++T) {
         const int shapes[4][2] = {{g.qkv_rows, g.H}, {g.H, g.qd}, {2 * g.F, g.H}, {g.H, g.F}};
         for (auto &mk : shapes) {
-            const GemmShape s = gemm_shape(mk[0], T, mk[1], plan->sm_count, 1 << 30);
+            const TcShape s = tc_shape(mk[0], T, mk[1], plan->sm_count, 1 << 30);
             part = std::max(part, (size_t)s.sk * T * mk[0]);
         }
     }
@@ -588,13 +489,7 @@ tiles_status_t forward_setup(tiles_plan_s *plan) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem(d)) != cudaSuccess)
             return TILES_ERR_CUDA;
     }
-    for (int wn : {1, 2, 4}) {
-        const void *k = wn == 1 ? (const void *)gemm_tn_kernel<1>
-                        : wn == 2 ? (const void *)gemm_tn_kernel<2>
-                                  : (const void *)gemm_tn_kernel<4>;
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem(wn)) != cudaSuccess)
-            return TILES_ERR_CUDA;
-    }
+    if (gemm_tc_configure() != cudaSuccess) return TILES_ERR_CUDA;
     f.ready = true;
     return TILES_OK;
 }
@@ -617,7 +512,7 @@ tiles_status_t forward_pass(tiles_plan_s *plan, uint16_t *kc, uint16_t *vc, cons
     const dim3 agrid((T * g.G + 63) / 64, g.nkv, S);
     for (int l = 0; l < g.L; ++l) {
         const LayerPtrs &L = lp[l];
-        if ((e = gemm(L.qkv, g.H, f.h, g.H, g.qkv_rows, T, g.H, f.part, sms, 1 << 30, &sk, st)) != cudaSuccess)
+        if ((e = gemm(plan, L.qkv, g.H, f.h, g.H, g.qkv_rows, T, g.H, f.part, 1 << 30, &sk, st)) != cudaSuccess)
             return TILES_ERR_CUDA;
         const dim3 qgrid(T, g.nq + 2 * g.nkv);
         if (g.d == 64)
@@ -635,20 +530,20 @@ tiles_status_t forward_pass(tiles_plan_s *plan, uint16_t *kc, uint16_t *vc, cons
             attn_mt_kernel<128><<<agrid, 128, attn_smem(128), st>>>(f.q, kc, vc, l, g.nq, g.nkv, g.G, g.max_pos, P0, T, split,
                                                        kp.attn_scale, f.apart, S);
         attn_combine_kernel<<<dim3(T, g.nq), g.d, 0, st>>>(f.apart, S, g.nq, g.d, f.o);
-        if ((e = gemm(L.o, g.qd, f.o, g.qd, g.H, T, g.qd, f.part, sms, 1 << 30, &sk, st)) != cudaSuccess)
+        if ((e = gemm(plan, L.o, g.qd, f.o, g.qd, g.H, T, g.qd, f.part, 1 << 30, &sk, st)) != cudaSuccess)
             return TILES_ERR_CUDA;
         resid_norm_kernel<<<T, 256, 0, st>>>(f.part, sk, T, g.H, f.x, L.ffn_norm, eps, f.h);
-        if ((e = gemm(L.gu, g.H, f.h, g.H, 2 * g.F, T, g.H, f.part, sms, 1 << 30, &sk, st)) != cudaSuccess)
+        if ((e = gemm(plan, L.gu, g.H, f.h, g.H, 2 * g.F, T, g.H, f.part, 1 << 30, &sk, st)) != cudaSuccess)
             return TILES_ERR_CUDA;
         swiglu_kernel<<<std::min(4096, (T * g.F + 255) / 256), 256, 0, st>>>(f.part, sk, T, g.F, f.a);
-        if ((e = gemm(L.down, g.F, f.a, g.F, g.H, T, g.F, f.part, sms, 1 << 30, &sk, st)) != cudaSuccess)
+        if ((e = gemm(plan, L.down, g.F, f.a, g.F, g.H, T, g.F, f.part, 1 << 30, &sk, st)) != cudaSuccess)
             return TILES_ERR_CUDA;
         const uint16_t *next_gain = l + 1 < g.L ? lp[l + 1].attn_norm : kp.final_norm;
         resid_norm_kernel<<<T, 256, 0, st>>>(f.part, sk, T, g.H, f.x, next_gain, eps, f.h);
     }
     // LM head (tied embedding), one split: the partial sums are the logits
     float *lg = logits ? logits : f.logits;
-    if ((e = gemm(kp.embed, g.H, f.h, g.H, g.V, T, g.H, lg, sms, 1, &sk, st)) != cudaSuccess) return TILES_ERR_CUDA;
+    if ((e = gemm(plan, kp.embed, g.H, f.h, g.H, g.V, T, g.H, lg, 1, &sk, st)) != cudaSuccess) return TILES_ERR_CUDA;
     argmax_kernel<<<T, 256, 0, st>>>(lg, g.V, argmax);
     return cudaGetLastError() == cudaSuccess ? TILES_OK : TILES_ERR_CUDA;
 }

@@ -2,9 +2,41 @@
 // runtime and the multi-token forward pass.
 #pragma once
 
+#include <stddef.h>
+
+#include <array>
+#include <utility>
 #include <vector>
 
 #include "tiles_internal.h"
+
+#ifdef __CUDACC__
+#include <cuda_runtime.h>
+namespace tiles {
+namespace fwd {
+// Tensor-core projections of the multi-token pass (gemm_tc.cu): tiles of
+// kTcM weight rows against all T tokens (n_tile = T rounded up to 16), K
+// split into sk ranges of kps elements, `stages` shared-memory stages.
+constexpr int kTcM = 128;
+struct TcShape {
+    int n_tile, mt, sk, kps, stages;
+    size_t smem;
+};
+TcShape tc_shape(int M, int T, int K, int sms, int max_sk);
+cudaError_t gemm_tc_configure();
+cudaError_t gemm_tc_launch(const TensorMap &mw, const TensorMap &mx, const TcShape &s, int M, int T, int K,
+                           float *C, uint32_t *status, unsigned long long timeout_ns, cudaStream_t st);
+}  // namespace fwd
+}  // namespace tiles
+#endif
+
+namespace tiles {
+// A 2-D BF16 tensor map (runtime.cu): `rows` rows of `inner` elements,
+// `row_bytes` apart, boxes of box_inner x box_rows elements, 128-byte swizzle,
+// rows past the end read as zeros. False if the driver refuses it.
+bool encode_bf16_2d(TensorMap *out, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                    uint32_t box_inner, uint32_t box_rows);
+}  // namespace tiles
 
 // Working memory of the multi-token forward pass (tiles_forward,
 // tiles_verify), allocated on first use for up to TILES_MAX_FORWARD_TOKENS tokens
@@ -24,6 +56,8 @@ struct ForwardScratch {
     float *logits = nullptr;      // [T][V] when the caller passes none
     int32_t *argmax = nullptr;    // [T]
     int32_t *tokens = nullptr;    // staging of verify inputs
+    // tensor maps of the projections' operands: (base, inner, rows, row bytes, box rows) -> map
+    std::vector<std::pair<std::array<uint64_t, 5>, tiles::TensorMap>> maps;
 };
 
 struct tiles_plan_s {

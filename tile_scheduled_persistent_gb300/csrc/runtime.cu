@@ -371,6 +371,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+
 // TMA descriptors of this call's K and V caches: [L n_kv][max_pos][d] BF16,
 // boxes of kv_block positions x 64 dims (a 128-dim head takes two boxes per
 // chunk), 128-byte swizzle so the tensor-core fragment loads of the attention
@@ -622,6 +623,24 @@ tiles_status_t tiles_barrier_cost(int32_t n_ctas, int32_t rounds, double *ns_per
 }
 
 }  // extern "C"
+
+namespace tiles {
+bool encode_bf16_2d(TensorMap *out, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                    uint32_t box_inner, uint32_t box_rows) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows}, ones[2] = {1, 1};
+    CUtensorMap m;
+    if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, ones,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::memcpy(out, &m, sizeof m);
+    return true;
+}
+}  // namespace tiles
 
 // ---------------------------------------------------------------------------
 // Decode without any allocation: the per-call working memory of the kernel
