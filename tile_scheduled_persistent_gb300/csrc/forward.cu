@@ -52,17 +52,19 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ per-token kernels
-// Block-wide sum of 256 threads in a fixed order (warp trees, then warps in order).
-__device__ __forceinline__ float block_sum256(float v, float *red) {
+// Block-wide sum of NT threads in a fixed order (warp trees, then warps in order).
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float *red) {
     v = warp_sum(v);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
     float t = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) t += red[w];
+    for (int w = 0; w < NT / 32; ++w) t += red[w];
     __syncthreads();
     return t;
 }
+__device__ __forceinline__ float block_sum256(float v, float *red) { return block_sum<256>(v, red); }
 
 // h[t] = R(rmsnorm(x[t]) * gain), x[t] a bf16 row of n; r = 1 / sqrt(mean(x^2) + eps)
 __device__ __forceinline__ void norm_row(const uint16_t *x, const uint16_t *gain, int n, float eps, uint16_t *h,
@@ -96,35 +98,76 @@ __global__ void __launch_bounds__(256) embed_norm_kernel(const int32_t *tokens, 
     norm_row(xt, gain, H, eps, h + (size_t)t * H, red);
 }
 
-// x[t] = R(x[t] + sum_s part[s][t]) (the split partial sums in order), then
-// h[t] = R(rmsnorm(x[t]) * gain).
-__global__ void __launch_bounds__(256) resid_norm_kernel(const float *part, int sk, int T, int H, uint16_t *x,
-                                                         const uint16_t *gain, float eps, uint16_t *h) {
-    __shared__ float red[8];
-    const int t = blockIdx.x;
-    uint16_t *xt = x + (size_t)t * H;
-    for (int j = threadIdx.x; j < H; j += 256) {
-        float y = 0.f;
-        for (int s = 0; s < sk; ++s) y = __fadd_rn(y, part[((size_t)s * T + t) * H + j]);
-        xt[j] = f2bf(__fadd_rn(bf2f(xt[j]), y));
+// Sum over the sk split partials of 4 consecutive floats at p (split stride
+// zs), in split order, with up to four splits' loads in flight.
+__device__ __forceinline__ float4 split_sum4(const float *__restrict__ p, size_t zs, int sk) {
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [](float4 &a, const float4 &b) {
+        a.x = __fadd_rn(a.x, b.x);
+        a.y = __fadd_rn(a.y, b.y);
+        a.z = __fadd_rn(a.z, b.z);
+        a.w = __fadd_rn(a.w, b.w);
+    };
+    for (int s0 = 0; s0 < sk; s0 += 8) {
+        float4 a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (s0 + i < sk) a[i] = __ldg(reinterpret_cast<const float4 *>(p + (size_t)(s0 + i) * zs));
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (s0 + i < sk) add(y, a[i]);
     }
-    __syncthreads();
-    norm_row(xt, gain, H, eps, h + (size_t)t * H, red);
+    return y;
 }
 
-// a[t][r] = R(silu(g) * u), g and u the split sums of packed rows 2r and 2r + 1.
-__global__ void __launch_bounds__(256) swiglu_kernel(const float *part, int sk, int T, int F, uint16_t *a) {
-    const size_t n = (size_t)T * F;
-    for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
-        const int t = (int)(i / F), r = (int)(i % F);
-        float gt = 0.f, u = 0.f;
-        for (int s = 0; s < sk; ++s) {
-            const float *ps = part + ((size_t)s * T + t) * (2 * (size_t)F);
-            gt = __fadd_rn(gt, ps[2 * r]);
-            u = __fadd_rn(u, ps[2 * r + 1]);
-        }
-        const float silu = __fdiv_rn(gt, __fadd_rn(1.0f, expf(-gt)));
-        a[i] = f2bf(__fmul_rn(silu, u));
+// x[t] = R(x[t] + sum_s part[s][t]) (the split partial sums in order), then
+// h[t] = R(rmsnorm(x[t]) * gain). 512 threads, four elements per thread and
+// step (H is a multiple of 8).
+__global__ void __launch_bounds__(512) resid_norm_kernel(const float *__restrict__ part, int sk, int T, int H,
+                                                         uint16_t *__restrict__ x, const uint16_t *__restrict__ gain,
+                                                         float eps, uint16_t *__restrict__ h) {
+    __shared__ float red[16];
+    const int t = blockIdx.x;
+    uint16_t *xt = x + (size_t)t * H;
+    const float *pt = part + (size_t)t * H;
+    float ss = 0.f;
+    for (int j = threadIdx.x * 4; j < H; j += 2048) {
+        const float4 y = split_sum4(pt + j, (size_t)T * H, sk);
+        const uint2 xv = *reinterpret_cast<const uint2 *>(xt + j);
+        const float r0 = round_bf(__fadd_rn(bf_lo(xv.x), y.x)), r1 = round_bf(__fadd_rn(bf_hi(xv.x), y.y));
+        const float r2 = round_bf(__fadd_rn(bf_lo(xv.y), y.z)), r3 = round_bf(__fadd_rn(bf_hi(xv.y), y.w));
+        *reinterpret_cast<uint2 *>(xt + j) = make_uint2(pack_bf2(r0, r1), pack_bf2(r2, r3));
+        ss = fmaf(r0, r0, ss);
+        ss = fmaf(r1, r1, ss);
+        ss = fmaf(r2, r2, ss);
+        ss = fmaf(r3, r3, ss);
+    }
+    const float tot = block_sum<512>(ss, red);
+    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)H), eps)));
+    uint16_t *ht = h + (size_t)t * H;
+    for (int j = threadIdx.x * 4; j < H; j += 2048) {
+        const uint2 xv = *reinterpret_cast<const uint2 *>(xt + j);
+        const uint2 gv = *reinterpret_cast<const uint2 *>(gain + j);
+        const float h0 = __fmul_rn(__fmul_rn(bf_lo(xv.x), r), bf_lo(gv.x));
+        const float h1 = __fmul_rn(__fmul_rn(bf_hi(xv.x), r), bf_hi(gv.x));
+        const float h2 = __fmul_rn(__fmul_rn(bf_lo(xv.y), r), bf_lo(gv.y));
+        const float h3 = __fmul_rn(__fmul_rn(bf_hi(xv.y), r), bf_hi(gv.y));
+        *reinterpret_cast<uint2 *>(ht + j) = make_uint2(pack_bf2(h0, h1), pack_bf2(h2, h3));
+    }
+}
+
+// a[t][r] = R(silu(g) * u), g and u the split sums of packed rows 2r and 2r + 1;
+// two rows per thread (F is a multiple of 8).
+__global__ void __launch_bounds__(256) swiglu_kernel(const float *__restrict__ part, int sk, int T, int F,
+                                                     uint16_t *__restrict__ a) {
+    const size_t n2 = (size_t)T * F / 2;
+    for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n2; i += (size_t)gridDim.x * 256) {
+        const size_t e = 2 * i;  // output element: token e / F, rows r, r + 1
+        const int t = (int)(e / F), r = (int)(e % F);
+        const float4 y = split_sum4(part + (size_t)t * 2 * F + 2 * (size_t)r, (size_t)T * 2 * F, sk);
+        const float s0 = __fdiv_rn(y.x, __fadd_rn(1.0f, expf(-y.x)));
+        const float s1 = __fdiv_rn(y.z, __fadd_rn(1.0f, expf(-y.z)));
+        *reinterpret_cast<uint32_t *>(a + e) = pack_bf2(__fmul_rn(s0, y.y), __fmul_rn(s1, y.w));
     }
 }
 
@@ -144,12 +187,24 @@ __global__ void __launch_bounds__(32) qkv_post_kernel(const float *part, int sk,
     const int kvh = is_q ? 0 : (is_k ? hh - nq : hh - nq - nkv);
     const int row0 = is_q ? hh * D : (is_k ? nq * D + kvh * D : nq * D + nkv * D + kvh * D);
     float v[E];
+    const float *pt = part + (size_t)t * rows + row0 + lane;
+    const size_t zs = (size_t)T * rows;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-        float y = 0.f;
-        for (int s = 0; s < sk; ++s) y = __fadd_rn(y, part[((size_t)s * T + t) * rows + row0 + lane + 32 * e]);
-        v[e] = y;
+    for (int e = 0; e < E; ++e) v[e] = 0.f;
+    int s = 0;
+    for (; s + 2 <= sk; s += 2) {  // split sums in order, 2 E loads in flight
+        float a0[E], a1[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            a0[e] = __ldg(pt + (size_t)s * zs + 32 * e);
+            a1[e] = __ldg(pt + (size_t)(s + 1) * zs + 32 * e);
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = __fadd_rn(__fadd_rn(v[e], a0[e]), a1[e]);
     }
+    for (; s < sk; ++s)
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = __fadd_rn(v[e], __ldg(pt + (size_t)s * zs + 32 * e));
     const int P = P0 + t;
     const size_t crow = (((size_t)layer * nkv + kvh) * max_pos + P) * D;
     if (!is_q && !is_k) {
@@ -358,13 +413,22 @@ __global__ void attn_combine_kernel(const float *part, int S, int nq, int D, uin
     o[((size_t)t * nq + i) * D + dd] = f2bf(__fdiv_rn(O, L));
 }
 
-// Greedy choice per token: the largest logit, lowest index on ties.
-__global__ void __launch_bounds__(256) argmax_kernel(const float *logits, int V, int32_t *out) {
+// Greedy choice per token: the largest logit, lowest index on ties. Grid
+// (T, kArgBlocks): each block reduces a slice of the row to the packed key
+// (ordered logit, inverted row) and raises keys[t] to it; the last block of
+// the token (a per-token ticket) writes the row and resets keys[t] and the
+// ticket for the next pass. The maximum does not depend on the order of the
+// atomics.
+constexpr int kArgBlocks = 16;
+__global__ void __launch_bounds__(256) argmax_kernel(const float *__restrict__ logits, int V,
+                                                     unsigned long long *keys, uint32_t *tickets, int32_t *out) {
     __shared__ unsigned long long best[8];
     const int t = blockIdx.x;
     const float *lt = logits + (size_t)t * V;
+    const int per = (V + kArgBlocks - 1) / kArgBlocks;
+    const int r0 = blockIdx.y * per, r1 = min(V, r0 + per);
     unsigned long long k = 0;
-    for (int r = threadIdx.x; r < V; r += 256) {
+    for (int r = r0 + threadIdx.x; r < r1; r += 256) {
         const unsigned long long kk = argmax_key(lt[r], (uint32_t)r);
         k = kk > k ? kk : k;
     }
@@ -374,7 +438,15 @@ __global__ void __launch_bounds__(256) argmax_kernel(const float *logits, int V,
     if (threadIdx.x == 0) {
         unsigned long long b = 0;
         for (int w = 0; w < 8; ++w) b = best[w] > b ? best[w] : b;
-        out[t] = key_row(b);
+        atomicMax(&keys[t], b);
+        __threadfence();
+        if (atomicAdd(&tickets[t], 1u) == kArgBlocks - 1) {
+            __threadfence();
+            const unsigned long long m = atomicMax(&keys[t], 0ull);
+            out[t] = key_row(m);
+            keys[t] = 0ull;
+            tickets[t] = 0u;
+        }
     }
 }
 
@@ -480,7 +552,13 @@ tiles_status_t forward_setup(tiles_plan_s *plan) {
         (e = falloc(plan, &f.apart, pairs * g.nq * (2 + g.d) * 4)) != cudaSuccess ||
         (e = falloc(plan, &f.logits, (size_t)Tm * g.V * 4)) != cudaSuccess ||
         (e = falloc(plan, &f.argmax, (size_t)Tm * 4)) != cudaSuccess ||
-        (e = falloc(plan, &f.tokens, (size_t)(Tm + 1) * 4)) != cudaSuccess)
+        (e = falloc(plan, &f.tokens, (size_t)(Tm + 1) * 4)) != cudaSuccess ||
+        (e = falloc(plan, &f.arg_keys, (size_t)Tm * 8)) != cudaSuccess ||
+        (e = falloc(plan, &f.arg_tickets, (size_t)Tm * 4)) != cudaSuccess)
+        return TILES_ERR_CUDA;
+    // the argmax kernel leaves them at zero after every pass
+    if (cudaMemset(f.arg_keys, 0, (size_t)Tm * 8) != cudaSuccess ||
+        cudaMemset(f.arg_tickets, 0, (size_t)Tm * 4) != cudaSuccess)
         return TILES_ERR_CUDA;
     f.part_elems = part;
     f.attn_pairs = pairs;
@@ -532,19 +610,19 @@ tiles_status_t forward_pass(tiles_plan_s *plan, uint16_t *kc, uint16_t *vc, cons
         attn_combine_kernel<<<dim3(T, g.nq), g.d, 0, st>>>(f.apart, S, g.nq, g.d, f.o);
         if ((e = gemm(plan, L.o, g.qd, f.o, g.qd, g.H, T, g.qd, f.part, 1 << 30, &sk, st)) != cudaSuccess)
             return TILES_ERR_CUDA;
-        resid_norm_kernel<<<T, 256, 0, st>>>(f.part, sk, T, g.H, f.x, L.ffn_norm, eps, f.h);
+        resid_norm_kernel<<<T, 512, 0, st>>>(f.part, sk, T, g.H, f.x, L.ffn_norm, eps, f.h);
         if ((e = gemm(plan, L.gu, g.H, f.h, g.H, 2 * g.F, T, g.H, f.part, 1 << 30, &sk, st)) != cudaSuccess)
             return TILES_ERR_CUDA;
-        swiglu_kernel<<<std::min(4096, (T * g.F + 255) / 256), 256, 0, st>>>(f.part, sk, T, g.F, f.a);
+        swiglu_kernel<<<std::min(4096, (T * g.F / 2 + 255) / 256), 256, 0, st>>>(f.part, sk, T, g.F, f.a);
         if ((e = gemm(plan, L.down, g.F, f.a, g.F, g.H, T, g.F, f.part, 1 << 30, &sk, st)) != cudaSuccess)
             return TILES_ERR_CUDA;
         const uint16_t *next_gain = l + 1 < g.L ? lp[l + 1].attn_norm : kp.final_norm;
-        resid_norm_kernel<<<T, 256, 0, st>>>(f.part, sk, T, g.H, f.x, next_gain, eps, f.h);
+        resid_norm_kernel<<<T, 512, 0, st>>>(f.part, sk, T, g.H, f.x, next_gain, eps, f.h);
     }
     // LM head (tied embedding), one split: the partial sums are the logits
     float *lg = logits ? logits : f.logits;
     if ((e = gemm(plan, kp.embed, g.H, f.h, g.H, g.V, T, g.H, lg, 1, &sk, st)) != cudaSuccess) return TILES_ERR_CUDA;
-    argmax_kernel<<<T, 256, 0, st>>>(lg, g.V, argmax);
+    argmax_kernel<<<dim3(T, kArgBlocks), 256, 0, st>>>(lg, g.V, f.arg_keys, f.arg_tickets, argmax);
     return cudaGetLastError() == cudaSuccess ? TILES_OK : TILES_ERR_CUDA;
 }
 

@@ -33,7 +33,7 @@ namespace fwd {
 // kTcM (plan_internal.h): weight rows per CTA, the MMA's M
 constexpr int kTcBK = 64;        // K elements per stage: one 128-byte swizzle row
 constexpr int kTcThreads = 128;
-constexpr int kTcMaxStages = 8;
+constexpr int kTcMaxStages = 12;
 constexpr int kTcABytes = kTcM * kTcBK * 2;  // 16 KB weight slice per stage
 
 struct TcCtl {
@@ -236,7 +236,7 @@ TcShape tc_shape(int M, int T, int K, int sms, int max_sk) {
     s.kps = ((nkc + sk - 1) / sk) * kTcBK;
     s.sk = (K + s.kps - 1) / s.kps;
     const int stage = kTcABytes + s.n_tile * 128;
-    s.stages = std::min(kTcMaxStages, (200 * 1024) / stage);
+    s.stages = std::min(kTcMaxStages, (200 * 1024) / stage);  // 4 stages at 256 tokens, 11 at 16
     // at least 116 KB of shared memory: one CTA per SM, so no CTA ever waits for tensor memory
     s.smem = std::max((size_t)116 * 1024, (size_t)s.stages * stage + sizeof(TcCtl));
     return s;

@@ -56,6 +56,8 @@ struct ForwardScratch {
     float *logits = nullptr;      // [T][V] when the caller passes none
     int32_t *argmax = nullptr;    // [T]
     int32_t *tokens = nullptr;    // staging of verify inputs
+    unsigned long long *arg_keys = nullptr;  // [T] running argmax keys (zero between passes)
+    uint32_t *arg_tickets = nullptr;         // [T] blocks done per token (zero between passes)
     // tensor maps of the projections' operands: (base, inner, rows, row bytes, box rows) -> map
     std::vector<std::pair<std::array<uint64_t, 5>, tiles::TensorMap>> maps;
 };
