@@ -150,7 +150,9 @@ enum { TILES_FLAG_INJECT_STALL = 1u };
 typedef struct tiles_plan_s *tiles_plan_t;
 
 /* Builds, validates and uploads a schedule for `desc` on the current CUDA
- * device. Query the device (SM count, shared memory, cooperative launch,
+ * device ("Tiles: Scheduling LLM Decoding as a Graph of Tiles", intro: the
+ * offline planner; "What the code contains": the schedule is validated before
+ * launch). Query the device (SM count, shared memory, cooperative launch,
  * occupancy of the worker kernel at the chosen shared-memory size), build the
  * tile graph, assign tiles to CTAs balancing streamed bytes, order them into
  * waves or dependency-counter chains, validate, and allocate the plan's own
@@ -164,12 +166,17 @@ typedef struct tiles_plan_s *tiles_plan_t;
 tiles_status_t tiles_plan_create(const tiles_model_desc *desc, const tiles_weights *weights,
                                  const tiles_plan_opts *opts, tiles_plan_t *out);
 
-/* Frees everything the plan allocated. NULL is allowed. The caller must make
- * sure no decode using the plan is still running. */
+/* Frees everything the plan allocated (no counterpart on the pages). NULL is
+ * allowed. The caller must make sure no decode using the plan is still
+ * running. */
 void tiles_plan_destroy(tiles_plan_t plan);
 
 /*
  * Greedy decoding, asynchronous on `stream` (a cudaStream_t, NULL = legacy).
+ * ("Tiles: Scheduling LLM Decoding as a Graph of Tiles", intro and "What the
+ * code contains": one persistent kernel runs the whole schedule for up to 64
+ * tokens per cooperative launch, greedy selection inside the kernel; "Scope
+ * and code release": the prompt goes one token per step.)
  *
  * Runs n_prompt - 1 + n_new steps; step s runs at position start_pos + s. Its
  * input token is prompt[s] when s < n_prompt, else the token chosen at step
@@ -196,7 +203,7 @@ tiles_status_t tiles_decode(tiles_plan_t plan, void *k_cache, void *v_cache,
 
 /*
  * Same as tiles_decode, but prompt, out_tokens and out_logits are HOST
- * buffers: the call copies the prompt in, decodes, copies the results out and
+ * buffers (no counterpart on the pages: the end-to-end measurement): the call copies the prompt in, decodes, copies the results out and
  * synchronises `stream` before returning (so it also reports kernel errors).
  * out_logits may be NULL. Uses the plan's own device staging buffers.
  */
@@ -236,13 +243,14 @@ tiles_status_t tiles_decode_noalloc(tiles_plan_t plan, void *k_cache, void *v_ca
                                     float *out_logits);
 
 /* Synchronises `stream` and reads the plan's device status word, then clears
- * it. Returns TILES_OK, TILES_ERR_TIMEOUT, TILES_ERR_DEVICE_BOUNDS or CUDA. */
+ * it ("Tiles", "What the code contains": the runtime's checks; kernel-side
+ * waits are bounded and report here). Returns TILES_OK, TILES_ERR_TIMEOUT, TILES_ERR_DEVICE_BOUNDS or CUDA. */
 tiles_status_t tiles_status(tiles_plan_t plan, void *stream);
 
-/* Static string naming a status code. Never NULL. */
+/* Static string naming a status code (no counterpart on the pages). Never NULL. */
 const char *tiles_status_string(tiles_status_t status);
 
-/* Diagnostics: makes later tiles_decode calls on this plan record a per-task
+/* Diagnostics (no counterpart on the pages): makes later tiles_decode calls on this plan record a per-task
  * timeline of their first `steps` steps into `trace` (device memory, caller
  * owned, at least n_ctas * steps * max_tasks_per_cta * 16 uint64 words, see
  * tiles_plan_info.max_tasks_per_cta). Word layout per task record:
@@ -259,7 +267,8 @@ const char *tiles_status_string(tiles_status_t status);
  * trace == NULL or steps == 0 turns it off. Errors: INVALID_ARG. */
 tiles_status_t tiles_plan_set_trace(tiles_plan_t plan, void *trace, int32_t steps);
 
-/* Facts about a built plan (or a host-only schedule), for reports and tests. */
+/* Facts about a built plan (or a host-only schedule), for reports and tests
+ * (no counterpart on the pages). */
 typedef struct {
     int32_t n_ctas, threads_per_cta, smem_bytes, slot_bytes, ring_slots, kv_splits;
     int32_t scheduler, n_tasks, n_counters, phases_per_step, max_tasks_per_cta;
@@ -363,28 +372,33 @@ typedef struct {
 typedef struct tiles_schedule_s *tiles_schedule_t;
 
 /* Builds (but does not validate) the schedule the planner would make for
- * n_ctas CTAs, a ring of ring_slots slots of slot_bytes bytes. Host only. */
+ * n_ctas CTAs, a ring of ring_slots slots of slot_bytes bytes. Host only
+ * ("Tiles", intro: the offline planner's assignment and order). */
 tiles_status_t tiles_schedule_build(const tiles_model_desc *desc, const tiles_plan_opts *opts,
                                     int32_t n_ctas, tiles_schedule_t *out);
 
-/* Validates a schedule: every output row / item covered exactly once per step,
+/* Validates a schedule ("Tiles", "What the code contains": the planner and the
+ * runtime validate the schedule): every output row / item covered exactly once per step,
  * indices in range, each wait satisfiable by earlier signals and covering all
  * of them, copy sizes and ring slots 16-byte aligned. Returns TILES_OK or
  * TILES_ERR_PLAN_INVALID; `why` (may be NULL) receives a message. */
 tiles_status_t tiles_schedule_validate(tiles_schedule_t sched, char *why, size_t why_len);
 
-/* Mutable view of the task table: tasks of CTA c are
- * tasks[offsets[c] .. offsets[c+1]). Valid until the schedule is destroyed. */
+/* Mutable view of the task table (fault injection in tests; no counterpart on
+ * the pages): tasks of CTA c are tasks[offsets[c] .. offsets[c+1]). Valid
+ * until the schedule is destroyed. */
 tiles_status_t tiles_schedule_tasks(tiles_schedule_t sched, tiles_task **tasks,
                                     int32_t *n_tasks, const int32_t **offsets, int32_t *n_ctas);
 
-/* Per-CTA weight+KV bytes streamed in one step at context position `pos`. */
+/* Per-CTA weight+KV bytes streamed in one step at context position `pos`
+ * ("Tiles", intro: the planner balances the bytes each worker streams). */
 tiles_status_t tiles_schedule_cta_bytes(tiles_schedule_t sched, int32_t pos, int64_t *bytes);
 
 /* The facts tiles_plan_get_info reports, for a schedule built on the host
  * (no GPU involved). Errors: INVALID_ARG on a null argument. */
 tiles_status_t tiles_schedule_get_info(tiles_schedule_t sched, tiles_plan_info *info);
 
+/* Frees a schedule (no counterpart on the pages). NULL is allowed. */
 void tiles_schedule_destroy(tiles_schedule_t sched);
 
 /* Weight-only INT8 quantization of a row-major [rows][cols] BF16 matrix (device
@@ -399,8 +413,9 @@ void tiles_schedule_destroy(tiles_schedule_t sched);
 tiles_status_t tiles_quantize_rows_int8(const void *w_bf16, int32_t rows, int32_t cols, void *codes,
                                         float *scales, void *stream);
 
-/* The two caller-owned device buffers of a TILES_KV_INT8 cache (see
- * TILES_KV_INT8 for the quantities). With Z = n_layers * n_kv_heads, d =
+/* The two caller-owned device buffers of a TILES_KV_INT8 cache ("History and
+ * roadmap", "M8 so far": INT8 KV cache with smoothed keys; see TILES_KV_INT8
+ * for the quantities). With Z = n_layers * n_kv_heads, d =
  * head_dim and MP = max_pos rounded up to a multiple of 16 (position strides
  * stay multiples of 16 bytes, as the kernel's tiled copies need):
  *   k buffer: key codes   int8  [Z][MP][d]  at offset 0
@@ -421,7 +436,8 @@ typedef struct {
 tiles_status_t tiles_kv8_get_layout(const tiles_model_desc *desc, tiles_kv8_layout *out);
 
 /* Builds the INT8 cache of the prefilled positions 0..n_pos-1 from BF16 caches
- * ([L][n_kv][max_pos][d], device), asynchronous on `stream`: per (layer, KV
+ * ([L][n_kv][max_pos][d], device), asynchronous on `stream` ("History and
+ * roadmap", "M8 so far": smoothed keys; the plainest scheme, the pages give none): per (layer, KV
  * head) the key shift mu_j = (sum over t < n_pos of K[t][j]) / n_pos, summed
  * in FP64 in position order and rounded to FP32 (0 when n_pos = 0), then
  * every row of positions < n_pos quantized as TILES_KV_INT8 states. Other
@@ -436,11 +452,13 @@ tiles_status_t tiles_kv8_from_bf16(const tiles_model_desc *desc, const void *k_b
 
 /* Device-to-device copy of `bytes` (multiple of 16, both pointers 16-byte
  * aligned) by a grid of n_ctas CTAs (0 = 2 per SM), asynchronous on stream.
- * The HBM peak the roofline fraction is taken against. */
+ * The HBM peak the roofline fraction is taken against ("History and roadmap",
+ * "Where it stands": kernels measured against their memory roofline). */
 tiles_status_t tiles_copy_bw(void *dst, const void *src, size_t bytes, int32_t n_ctas,
                              void *stream);
 
-/* Grid-barrier round trip: one cooperative launch of n_ctas CTAs that crosses
+/* Grid-barrier round trip ("Tiles", intro: the cost of a barrier between
+ * waves): one cooperative launch of n_ctas CTAs that crosses
  * `rounds` grid barriers; *ns_per_barrier receives the mean cost measured
  * inside the kernel with the global timer. Synchronous. */
 tiles_status_t tiles_barrier_cost(int32_t n_ctas, int32_t rounds, double *ns_per_barrier);
