@@ -139,6 +139,26 @@ __device__ __forceinline__ void mma_rows8(float &c0, float &c1, uint32_t a0, uin
         : "r"(a0), "r"(a2), "r"(b0), "r"(b1), "r"(0u), "f"(0.f));
 }
 
+// c += A B, A 16x16 and B 16x8 in full: a = {(g, 2t..2t+1), (g+8, 2t..2t+1),
+// (g, 2t+8..2t+9), (g+8, 2t+8..2t+9)}, b = {(k 2t..2t+1, n g), (k 2t+8..2t+9,
+// n g)}, c = {(g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)} for lane (g, t).
+__device__ __forceinline__ void mma_m16n8k16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9},"
+        " {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The transpose of an 8x8 matrix of 16-bit elements held as lane (g, t):
+// row g, columns 2t and 2t+1; returns the same lane's pair of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // Byte offset of 16-byte unit u (elements 8u..8u+7) of row r in a chunk region
 // written by the tiled copy with the 128-byte swizzle: boxes of kvb rows x 128
 // bytes one after another (unit u lives in box u / 8), and inside each
@@ -1343,207 +1363,219 @@ struct Consumer {
     unsigned long long *cur_tr = nullptr;  // trace record of the running task, or null
 
     // One chunk of positions [q0, q0 + npos) for the G q heads of one kv head,
-    // on the tensor cores (the chunk arrived as swizzled K and V tiles). The
-    // q heads are rows 0..G-1 of the m16n8k16 A operand (rows G..15 zero);
-    // lane (g, t) = (lane / 4, lane % 4) holds row g. Per round of 2048 / D
-    // positions (few enough registers that the rest of the kernel's state
-    // stays mostly in registers):
-    //   s = q K^T (FP32, exact BF16 products), masked past npos, times d^-1/2;
-    //   online softmax per row: m' = max(m, max s), c = e^(m - m'),
-    //   p = e^(s - m'), l' = c l + sum p, o' = c o;
-    //   o' += p V, with p split into a BF16 high part and a BF16 remainder
-    //   (two MMAs), so the weights keep ~16 bits.
-    // o[j] holds row g's accumulators of output dims 8j + 2t and 8j + 2t + 1.
+    // on the tensor cores (the chunk arrived as swizzled K and V tiles), with
+    // positions as the 16 rows of the m16n8k16 A operand and the q heads as
+    // the 8 columns of B (columns >= G are zero). A 16-position block takes
+    // d/16 MMAs for s^T = K q^T and 2 d/16 for o^T += V^T p^T: half of what
+    // q heads as A rows take, since G <= 8 rows of 16 would be used there.
+    // Lane (g, t) = (lane / 4, lane % 4) holds the scores of positions g and
+    // g + 8 of each block for heads 2t and 2t + 1, and their running m and l
+    // (l summed over this lane's positions only, reduced over g at the end).
+    // Per round of 2048 / D positions:
+    //   s = K q^T (FP32, exact BF16 products), masked past npos, times d^-1/2;
+    //   m' = max(m, max over positions), c = e^(m - m'), p = e^(s - m'),
+    //   l' = c l + sum p, o' = c o;
+    //   p^T becomes B fragments by one movmatrix.trans per 8 x 8 block, as a
+    //   BF16 high part and a BF16 remainder (two MMAs, ~16 bits kept);
+    //   o^T += V^T p^T with V^T's fragments from transposed ldmatrix of V.
+    // o[mt] holds (dims 16 mt + g and 16 mt + g + 8) x (heads 2t, 2t + 1).
     template <int D, int G>
-    __device__ __forceinline__ void attn_chunk_mma(const uint8_t *slot, int npos, const uint32_t *qrow, bool qrow_ok,
-                                                   float &m, float &l, float (&o)[D / 8][2]) {
+    __device__ __forceinline__ void attn_chunk_mma(const uint8_t *slot, int npos, const uint32_t *qcol, bool qcol_ok,
+                                                   float (&m)[2], float (&l)[2], float (&o)[D / 16][4]) {
         constexpr int SUB = 2048 / D;  // positions per round
-        constexpr int NT = SUB / 8;    // score n-tiles of 8 positions
+        constexpr int NP = SUB / 16;   // 16-position blocks per round
         constexpr int KS = D / 16;     // k-steps of the scores
-        constexpr int PS = SUB / 16;   // k-steps of p V
-        constexpr int NJ = D / 8;      // output n-tiles of 8 dims
+        constexpr int MT = D / 16;     // 16-dim row tiles of o^T
         const int kvb = p.g.kv_block;
         const uint32_t kb = smem_u32(slot), vb = kb + (uint32_t)kvb * D * 2;
-        const int t4 = lane & 3;
+        const int g8 = lane >> 2;
         const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix and row this lane points at
         for (int p0 = 0; p0 < npos; p0 += SUB) {
-            float sc[NT][2];
+            float s[NP][4];
 #pragma unroll
-            for (int jn = 0; jn < NT; ++jn) {
-                float c0 = 0.f, c1 = 0.f;
+            for (int pt = 0; pt < NP; ++pt) {
+                s[pt][0] = s[pt][1] = s[pt][2] = s[pt][3] = 0.f;
 #pragma unroll
-                for (int ks = 0; ks < KS; ks += 2) {
-                    // units 2ks .. 2ks + 3 of positions p0 + 8jn ..: b0, b1 of k-steps ks and ks + 1
-                    uint32_t b[4];
-                    ldsm_x4(kb + swz_off(kvb, p0 + 8 * jn + ri, 2 * ks + mi), b);
-                    // A fragments of q from shared memory (rows >= G are zero)
-                    const uint32_t qa0 = qrow_ok ? qrow[8 * ks] : 0u, qa1 = qrow_ok ? qrow[8 * ks + 4] : 0u;
-                    const uint32_t qb0 = qrow_ok ? qrow[8 * ks + 8] : 0u, qb1 = qrow_ok ? qrow[8 * ks + 12] : 0u;
-                    mma_rows8(c0, c1, qa0, qa1, b[0], b[1]);
-                    mma_rows8(c0, c1, qb0, qb1, b[2], b[3]);
+                for (int ks = 0; ks < KS; ++ks) {
+                    // rows 0-7 / 8-15 of the block, dims 16 ks .. + 7 / + 8 .. + 15
+                    uint32_t a[4];
+                    ldsm_x4(kb + swz_off(kvb, p0 + 16 * pt + 8 * (mi & 1) + ri, 2 * ks + (mi >> 1)), a);
+                    const uint32_t b0 = qcol_ok ? qcol[8 * ks] : 0u, b1 = qcol_ok ? qcol[8 * ks + 4] : 0u;
+                    mma_m16n8k16(s[pt], a[0], a[1], a[2], a[3], b0, b1);
                 }
-                sc[jn][0] = c0;
-                sc[jn][1] = c1;
             }
-            float mx = -INFINITY;
+            float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int jn = 0; jn < NT; ++jn)
+            for (int pt = 0; pt < NP; ++pt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int pos = p0 + 8 * jn + 2 * t4 + e;
-                    sc[jn][e] = pos < npos ? sc[jn][e] * p.attn_scale : -INFINITY;
-                    mx = fmaxf(mx, sc[jn][e]);
+                for (int hr = 0; hr < 2; ++hr) {
+                    const bool ok = p0 + 16 * pt + 8 * hr + g8 < npos;
+                    s[pt][2 * hr] = ok ? s[pt][2 * hr] * p.attn_scale : -INFINITY;
+                    s[pt][2 * hr + 1] = ok ? s[pt][2 * hr + 1] * p.attn_scale : -INFINITY;
+                    mx0 = fmaxf(mx0, s[pt][2 * hr]);
+                    mx1 = fmaxf(mx1, s[pt][2 * hr + 1]);
                 }
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-            const float mn = fmaxf(m, mx);
-            const float corr = expf(m - mn);
-            float ls = 0.f;
-            uint32_t ahi[PS][2], alo[PS][2];
 #pragma unroll
-            for (int jn = 0; jn < NT; ++jn) {
-                const float p0f = expf(sc[jn][0] - mn), p1f = expf(sc[jn][1] - mn);
-                ls += p0f + p1f;
-                const uint16_t h0 = f2bf(p0f), h1 = f2bf(p1f);
-                const uint16_t r0 = f2bf(__fsub_rn(p0f, bf2f(h0))), r1 = f2bf(__fsub_rn(p1f, bf2f(h1)));
-                ahi[jn / 2][jn & 1] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-                alo[jn / 2][jn & 1] = (uint32_t)r0 | ((uint32_t)r1 << 16);
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
             }
-            ls += __shfl_xor_sync(0xFFFFFFFFu, ls, 1);
-            ls += __shfl_xor_sync(0xFFFFFFFFu, ls, 2);
-            l = fmaf(l, corr, ls);
-            m = mn;
+            const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+            const float c0 = expf(m[0] - mn0), c1 = expf(m[1] - mn1);
+            float ls0 = 0.f, ls1 = 0.f;
+            uint32_t bh[NP][2], bl[NP][2];
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                o[j][0] *= corr;
-                o[j][1] *= corr;
+            for (int pt = 0; pt < NP; ++pt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const float pa = expf(s[pt][2 * hr] - mn0), pb = expf(s[pt][2 * hr + 1] - mn1);
+                    ls0 += pa;
+                    ls1 += pb;
+                    const uint16_t ha = f2bf(pa), hb = f2bf(pb);
+                    const uint16_t ra = f2bf(__fsub_rn(pa, bf2f(ha))), rb = f2bf(__fsub_rn(pb, bf2f(hb)));
+                    bh[pt][hr] = movmatrix_t((uint32_t)ha | ((uint32_t)hb << 16));
+                    bl[pt][hr] = movmatrix_t((uint32_t)ra | ((uint32_t)rb << 16));
+                }
+            l[0] = fmaf(l[0], c0, ls0);
+            l[1] = fmaf(l[1], c1, ls1);
+            m[0] = mn0;
+            m[1] = mn1;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                o[mt][0] *= c0;
+                o[mt][1] *= c1;
+                o[mt][2] *= c0;
+                o[mt][3] *= c1;
             }
 #pragma unroll
-            for (int ps = 0; ps < PS; ++ps)
+            for (int pt = 0; pt < NP; ++pt)
 #pragma unroll
-                for (int j = 0; j < NJ; j += 2) {
-                    // positions p0 + 16ps (+8), dims 8j and 8j + 8, transposed: b0, b1 of n-tiles j, j + 1
-                    uint32_t b[4];
-                    ldsm_x4_t(vb + swz_off(kvb, p0 + 16 * ps + 8 * (mi & 1) + ri, j + (mi >> 1)), b);
-                    mma_rows8(o[j][0], o[j][1], ahi[ps][0], ahi[ps][1], b[0], b[1]);
-                    mma_rows8(o[j][0], o[j][1], alo[ps][0], alo[ps][1], b[0], b[1]);
-                    mma_rows8(o[j + 1][0], o[j + 1][1], ahi[ps][0], ahi[ps][1], b[2], b[3]);
-                    mma_rows8(o[j + 1][0], o[j + 1][1], alo[ps][0], alo[ps][1], b[2], b[3]);
+                for (int mt = 0; mt < MT; ++mt) {
+                    // V^T (dims 16 mt.., positions 16 pt..): transposed loads of V blocks
+                    // (positions block mi >> 1, dims block mi & 1)
+                    uint32_t a[4];
+                    ldsm_x4_t(vb + swz_off(kvb, p0 + 16 * pt + 8 * (mi >> 1) + ri, 2 * mt + (mi & 1)), a);
+                    mma_m16n8k16(o[mt], a[0], a[1], a[2], a[3], bh[pt][0], bh[pt][1]);
+                    mma_m16n8k16(o[mt], a[0], a[1], a[2], a[3], bl[pt][0], bl[pt][1]);
                 }
         }
     }
 
-    // The INT8-cache form of attn_chunk_mma. The chunk holds key codes
-    // [kvb][D] and value codes transposed [D][kvb] (swizzled tiles), then the
-    // key and value scales. A 32-bit ldmatrix word is four codes: of four
-    // consecutive dims of one position (keys) or four consecutive positions of
-    // one dim (values). They become the B fragment's k slots 2t, 2t+1, 2t+8,
-    // 2t+9, so:
-    //   - q's A fragment takes dims 4t..4t+3 of each 16 in the same slots
+    // The INT8-cache form of attn_chunk_mma (positions as A rows, q heads as B
+    // columns). The chunk holds key codes [kvb][D] and value codes transposed
+    // [D][kvb] (swizzled tiles), then the key and value scales. A 32-bit
+    // ldmatrix word is four codes: of four consecutive dims of one position
+    // (keys) or four consecutive positions of one dim (values). They become
+    // the A fragment's k slots 2t, 2t+1, 2t+8, 2t+9, so:
+    //   - q's B fragment takes dims 4t..4t+3 of each 16 in the same slots
     //     (words 2t and 2t+1 of the k-step: a consistent permutation of the
     //     summed dims);
-    //   - score n-tile 2i + b (b = 0, 1) holds positions 16 i + 4 (n / 2) +
-    //     2 b + (n & 1) in column n, so that a thread's p values of n-tiles 2i
-    //     and 2i + 1 are exactly the four positions its value word covers.
-    // Key scales multiply the score columns after q . codes; value scales fold
-    // into p (masked positions get exact zeros, so stale codes and scales past
-    // npos never reach the sums); l sums the unscaled p.
+    //   - row r of a 16-position score block is position 4 (r mod 8 / 2) +
+    //     (r & 1) + 2 (r / 8) (the ldmatrix row addresses choose it), so that
+    //     after movmatrix.trans a lane's p fragment covers exactly the four
+    //     positions 4t..4t+3 its value words hold.
+    // Key scales multiply the score rows after the MMA; value scales fold into
+    // p (masked positions get exact zeros, so stale codes and scales past npos
+    // never reach the sums); l sums the unscaled p.
     template <int D, int G>
-    __device__ __forceinline__ void attn_chunk_mma_q8(const uint8_t *slot, int npos, const uint32_t *qrow,
-                                                      bool qrow_ok, float &m, float &l, float (&o)[D / 8][2]) {
+    __device__ __forceinline__ void attn_chunk_mma_q8(const uint8_t *slot, int npos, const uint32_t *qcol,
+                                                      bool qcol_ok, float (&m)[2], float (&l)[2],
+                                                      float (&o)[D / 16][4]) {
         constexpr int KVB = 8192 / D;  // positions per chunk; also the value tile's row bytes
         constexpr int SUB = 2048 / D;  // positions per round
-        constexpr int NT = SUB / 8;    // score n-tiles of 8 positions
-        constexpr int PS = SUB / 16;   // k-steps of p V
-        constexpr int NJ = D / 8;      // output n-tiles of 8 dims
-        constexpr int KU = D / 16;     // 16-byte units of a key row
+        constexpr int NP = SUB / 16;   // 16-position blocks per round
+        constexpr int KU = D / 16;     // 16-byte units of a key row (= k-steps)
+        constexpr int MT = D / 16;     // 16-dim row tiles of o^T
         const uint32_t kb = smem_u32(slot), vb = kb + 8192u;
         const float *ksc = reinterpret_cast<const float *>(slot + 16384);
         const float *vsc = ksc + KVB;
-        const int t4 = lane & 3;
+        const int g8 = lane >> 2;
         const int mi = lane >> 3, ri = lane & 7;
+        const int kr_off = 4 * (ri >> 1) + (ri & 1) + 2 * (mi & 1);  // position of the row this lane addresses
+        const int my_off = 4 * (g8 >> 1) + (g8 & 1);                 // position of this lane's row g (+2: row g + 8)
         for (int p0 = 0; p0 < npos; p0 += SUB) {
-            float sc[NT][2];
+            float s[NP][4];
 #pragma unroll
-            for (int jn = 0; jn < NT; ++jn) {
-                float c0 = 0.f, c1 = 0.f;
-                const int kr = p0 + 16 * (jn >> 1) + 4 * (ri >> 1) + 2 * (jn & 1) + (ri & 1);
+            for (int pt = 0; pt < NP; ++pt) {
+                s[pt][0] = s[pt][1] = s[pt][2] = s[pt][3] = 0.f;
 #pragma unroll
-                for (int u0 = 0; u0 < KU; u0 += 4) {
-                    uint32_t b[4];
-                    ldsm_x4(kb + swz8_off<D>(kr, u0 + mi), b);
+                for (int u0 = 0; u0 < KU; u0 += 2) {
+                    // words: rows 0-7 / 8-15 of the block, units u0 and u0 + 1
+                    uint32_t w[4];
+                    ldsm_x4(kb + swz8_off<D>(p0 + 16 * pt + kr_off, u0 + (mi >> 1)), w);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < 2; ++i) {
                         const int ks = u0 + i;
-                        uint32_t blo, bhi;
-                        codes_bf16x2(b[i], blo, bhi);
-                        const uint32_t qa0 = qrow_ok ? qrow[8 * ks] : 0u, qa2 = qrow_ok ? qrow[8 * ks + 1] : 0u;
-                        mma_rows8(c0, c1, qa0, qa2, blo, bhi);
+                        uint32_t a0, a1, a2, a3;
+                        codes_bf16x2(w[2 * i], a0, a2);
+                        codes_bf16x2(w[2 * i + 1], a1, a3);
+                        const uint32_t b0 = qcol_ok ? qcol[8 * ks] : 0u, b1 = qcol_ok ? qcol[8 * ks + 1] : 0u;
+                        mma_m16n8k16(s[pt], a0, a1, a2, a3, b0, b1);
                     }
                 }
-                sc[jn][0] = c0;
-                sc[jn][1] = c1;
             }
-            float mx = -INFINITY;
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+            float vs[NP][2];
 #pragma unroll
-            for (int ps = 0; ps < PS; ++ps) {
-                const float4 kq = *reinterpret_cast<const float4 *>(ksc + p0 + 16 * ps + 4 * t4);
-                const float ks4[4] = {kq.x, kq.y, kq.z, kq.w};
+            for (int pt = 0; pt < NP; ++pt)
 #pragma unroll
-                for (int b = 0; b < 2; ++b)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int pos = p0 + 16 * ps + 4 * t4 + 2 * b + e;
-                        float &x = sc[2 * ps + b][e];
-                        x = pos < npos ? (x * ks4[2 * b + e]) * p.attn_scale : -INFINITY;
-                        mx = fmaxf(mx, x);
-                    }
-            }
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-            const float mn = fmaxf(m, mx);
-            const float corr = expf(m - mn);
-            float ls = 0.f;
-            uint32_t ahi[PS][2], alo[PS][2];
-#pragma unroll
-            for (int ps = 0; ps < PS; ++ps) {
-                const float4 vq = *reinterpret_cast<const float4 *>(vsc + p0 + 16 * ps + 4 * t4);
-                const float vs4[4] = {vq.x, vq.y, vq.z, vq.w};
-#pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const int pos = p0 + 16 * ps + 4 * t4 + 2 * b;
-                    const float p0f = expf(sc[2 * ps + b][0] - mn), p1f = expf(sc[2 * ps + b][1] - mn);
-                    ls += p0f + p1f;
-                    const float w0 = pos < npos ? p0f * vs4[2 * b] : 0.f;
-                    const float w1 = pos + 1 < npos ? p1f * vs4[2 * b + 1] : 0.f;
-                    const uint16_t h0 = f2bf(w0), h1 = f2bf(w1);
-                    const uint16_t r0 = f2bf(__fsub_rn(w0, bf2f(h0))), r1 = f2bf(__fsub_rn(w1, bf2f(h1)));
-                    ahi[ps][b] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-                    alo[ps][b] = (uint32_t)r0 | ((uint32_t)r1 << 16);
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int pos = p0 + 16 * pt + my_off + 2 * hr;
+                    const bool ok = pos < npos;
+                    const float kscale = ksc[pos];
+                    vs[pt][hr] = ok ? vsc[pos] : 0.f;
+                    s[pt][2 * hr] = ok ? (s[pt][2 * hr] * kscale) * p.attn_scale : -INFINITY;
+                    s[pt][2 * hr + 1] = ok ? (s[pt][2 * hr + 1] * kscale) * p.attn_scale : -INFINITY;
+                    mx0 = fmaxf(mx0, s[pt][2 * hr]);
+                    mx1 = fmaxf(mx1, s[pt][2 * hr + 1]);
                 }
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
             }
-            ls += __shfl_xor_sync(0xFFFFFFFFu, ls, 1);
-            ls += __shfl_xor_sync(0xFFFFFFFFu, ls, 2);
-            l = fmaf(l, corr, ls);
-            m = mn;
+            const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+            const float c0 = expf(m[0] - mn0), c1 = expf(m[1] - mn1);
+            float ls0 = 0.f, ls1 = 0.f;
+            uint32_t bh[NP][2], bl[NP][2];
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                o[j][0] *= corr;
-                o[j][1] *= corr;
+            for (int pt = 0; pt < NP; ++pt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const float pa = expf(s[pt][2 * hr] - mn0), pb = expf(s[pt][2 * hr + 1] - mn1);
+                    ls0 += pa;
+                    ls1 += pb;
+                    const float wa = pa * vs[pt][hr], wb = pb * vs[pt][hr];
+                    const uint16_t ha = f2bf(wa), hb = f2bf(wb);
+                    const uint16_t ra = f2bf(__fsub_rn(wa, bf2f(ha))), rb = f2bf(__fsub_rn(wb, bf2f(hb)));
+                    bh[pt][hr] = movmatrix_t((uint32_t)ha | ((uint32_t)hb << 16));
+                    bl[pt][hr] = movmatrix_t((uint32_t)ra | ((uint32_t)rb << 16));
+                }
+            l[0] = fmaf(l[0], c0, ls0);
+            l[1] = fmaf(l[1], c1, ls1);
+            m[0] = mn0;
+            m[1] = mn1;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                o[mt][0] *= c0;
+                o[mt][1] *= c1;
+                o[mt][2] *= c0;
+                o[mt][3] *= c1;
             }
 #pragma unroll
-            for (int ps = 0; ps < PS; ++ps)
+            for (int pt = 0; pt < NP; ++pt)
 #pragma unroll
-                for (int j = 0; j < NJ; j += 4) {
-                    // dims 8 (j + mi) + ri, positions p0 + 16 ps .. + 15: n-tiles j .. j + 3
-                    uint32_t b[4];
-                    ldsm_x4(vb + swz8_off<KVB>(8 * (j + mi) + ri, (p0 >> 4) + ps), b);
+                for (int mt = 0; mt < MT; mt += 2) {
+                    // words: dims 16 mt + 0..7, + 8..15, 16 (mt + 1) + 0..7, + 8..15; positions 16 pt ..
+                    uint32_t w[4];
+                    ldsm_x4(vb + swz8_off<KVB>(16 * mt + 8 * mi + ri, (p0 >> 4) + pt), w);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t blo, bhi;
-                        codes_bf16x2(b[i], blo, bhi);
-                        mma_rows8(o[j + i][0], o[j + i][1], ahi[ps][0], ahi[ps][1], blo, bhi);
-                        mma_rows8(o[j + i][0], o[j + i][1], alo[ps][0], alo[ps][1], blo, bhi);
+                    for (int i = 0; i < 2; ++i) {
+                        uint32_t a0, a1, a2, a3;
+                        codes_bf16x2(w[2 * i], a0, a2);
+                        codes_bf16x2(w[2 * i + 1], a1, a3);
+                        mma_m16n8k16(o[mt + i], a0, a1, a2, a3, bh[pt][0], bh[pt][1]);
+                        mma_m16n8k16(o[mt + i], a0, a1, a2, a3, bl[pt][0], bl[pt][1]);
                     }
                 }
         }
@@ -1802,11 +1834,11 @@ struct Consumer {
                 const int g8 = lane >> 2, t4 = lane & 3;
                 // q head g8 as BF16 pairs (dims 2t4 + 16ks (+8) in word t4 + 8ks (+4))
                 // (the INT8 form reads words 2 t4 and 2 t4 + 1 of each k-step instead)
-                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.qh + (size_t)(g8 < G ? g8 : 0) * (D + 8)) +
+                const uint32_t *qcol = reinterpret_cast<const uint32_t *>(a.qh + (size_t)(g8 < G ? g8 : 0) * (D + 8)) +
                                        (KV8 ? 2 * t4 : t4);
-                float mm = -INFINITY, ll = 0.f, oo[D / 8][2];
+                float mm[2] = {-INFINITY, -INFINITY}, ll[2] = {0.f, 0.f}, oo[D / 16][4];
 #pragma unroll
-                for (int jd = 0; jd < D / 8; ++jd) oo[jd][0] = oo[jd][1] = 0.f;
+                for (int mt = 0; mt < D / 16; ++mt) oo[mt][0] = oo[mt][1] = oo[mt][2] = oo[mt][3] = 0.f;
                 for (uint32_t k = 0; k < nch; ++k) {
                     const uint32_t jj = j + k;
                     if (!mine(jj)) continue;
@@ -1817,25 +1849,34 @@ struct Consumer {
                     if (q1 > P + 1) q1 = P + 1;
                     if (KV8) {
                         if (q0 <= P && P < q1) place_new_kv_q8<D>(slot, q0);
-                        attn_chunk_mma_q8<D, G>(slot, q1 - q0, qrow, g8 < G, mm, ll, oo);
+                        attn_chunk_mma_q8<D, G>(slot, q1 - q0, qcol, g8 < G, mm, ll, oo);
                     } else {
                         if (q0 <= P && P < q1) place_new_kv_swz<D>(slot, q0);
-                        attn_chunk_mma<D, G>(slot, q1 - q0, qrow, g8 < G, mm, ll, oo);
+                        attn_chunk_mma<D, G>(slot, q1 - q0, qcol, g8 < G, mm, ll, oo);
                     }
                     release_chunk(jj);
                 }
-                // per-warp states -> shared memory (row g8 = q head g8)
+                // per-warp states -> shared memory: l summed over the lanes of a
+                // head (lanes with the same t), then heads 2 t4 and 2 t4 + 1
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    ll[0] += __shfl_xor_sync(0xFFFFFFFFu, ll[0], off);
+                    ll[1] += __shfl_xor_sync(0xFFFFFFFFu, ll[1], off);
+                }
                 float *ws = a.wstate + (size_t)warp * G * (kPartialPad + D);
-                if (g8 < G) {
-                    float *w = ws + (size_t)g8 * (kPartialPad + D);
-                    if (t4 == 0) {
-                        w[0] = mm;
-                        w[1] = ll;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int hh = 2 * t4 + e;
+                    if (hh >= G) continue;
+                    float *w = ws + (size_t)hh * (kPartialPad + D);
+                    if (g8 == 0) {
+                        w[0] = mm[e];
+                        w[1] = ll[e];
                     }
 #pragma unroll
-                    for (int jd = 0; jd < D / 8; ++jd) {
-                        w[kPartialPad + 8 * jd + 2 * t4] = oo[jd][0];
-                        w[kPartialPad + 8 * jd + 2 * t4 + 1] = oo[jd][1];
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        w[kPartialPad + 16 * mt + g8] = oo[mt][e];
+                        w[kPartialPad + 16 * mt + g8 + 8] = oo[mt][2 + e];
                     }
                 }
             }
