@@ -99,10 +99,13 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
 
     // slot: large enough for one row of every GEMV (two for gate/up). Each
     // slot has one owning consumer warp, so the default ring is one slot per
-    // warp of 16 KB (or the largest row): a chunk holds its slot while one warp
-    // reduces it, and smaller chunks turn the ring over faster. Measured on
-    // GB300 for the Llama-1B shape: 8 x 16 KB beat 6 x 32 KB by 6 % and
-    // 12 x 16 KB (uneven ownership) by 2 %.
+    // warp of 16 KB, or of two gate/up row pairs or the largest row if either
+    // is larger: a chunk holds its slot while one warp reduces it, and smaller
+    // chunks turn the ring over faster, but the gate/up stream (the most
+    // bytes) must not be left one pair per chunk. Measured on GB300: Llama-1B
+    // shape, 8 x 16 KB beat 6 x 32 KB by 6 % and 12 x 16 KB (uneven
+    // ownership) by 2 %; Qwen3-4B shape (19 KB down rows, 10 KB gate/up
+    // pairs), 8 x 20 KB slots (two pairs a chunk) beat 8 x 19 KB (one) by 17 %.
     if (o.kv_format != TILES_KV_BF16 && o.kv_format != TILES_KV_INT8)
         return fail(TILES_ERR_INVALID_ARG, "kv_format");
     G_.kv8 = o.kv_format == TILES_KV_INT8 ? 1 : 0;
@@ -111,7 +114,7 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     // an INT8 KV chunk (codes of 8 KB of keys and 8 KB of values, and their
     // scales) fills one slot
     int need = std::max({wb * G_.H, wb * G_.qd, wb * G_.F, 2 * wb * G_.H, G_.kv8 ? kv8_chunk_bytes(G_.d) : 0});
-    int slot = o.slot_bytes > 0 ? o.slot_bytes : round_up(std::max(need, 16384), 1024);
+    int slot = o.slot_bytes > 0 ? o.slot_bytes : round_up(std::max({need, 16384, 4 * wb * G_.H}), 1024);
     if (slot % 1024 || slot < need) return fail(TILES_ERR_INVALID_ARG, "slot_bytes too small or not a multiple of 1024");
     G_.slot_bytes = slot;
     // Rows per chunk: as many as fill a slot. INT8 layer GEMVs are capped so
