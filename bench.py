@@ -102,7 +102,8 @@ def measured_peaks():
 # sources the decode kernel's launch depends on (the multi-token pass in
 # forward.cu is a separate set of kernels and does not change its traffic)
 DECODE_SOURCES = ("kernels_bf16.cu", "kernels_bf16_mma.cu", "kernels_int8.cu", "kernels_int8_mma.cu",
-                  "megakernel.cu", "megakernel.cuh", "planner.cpp", "runtime.cu", "tiles_internal.h")
+                  "kernels_bf16_kv8.cu", "kernels_int8_kv8.cu", "megakernel.cu", "megakernel.cuh",
+                  "planner.cpp", "runtime.cu", "tiles_internal.h")
 
 
 def kernel_source_hash():

@@ -231,7 +231,9 @@ TcShape tc_shape(int M, int T, int K, int sms, int max_sk) {
     s.n_tile = (T + 15) / 16 * 16;
     s.mt = (M + kTcM - 1) / kTcM;
     const int nkc = (K + kTcBK - 1) / kTcBK;
-    int sk = std::max(1, std::min(nkc, (sms + s.mt / 2) / s.mt));
+    // splits: as many as keep the grid within one wave (one CTA per SM: a
+    // second wave of a few CTAs would double the projection's time)
+    int sk = std::max(1, std::min(nkc, sms / s.mt));
     sk = std::max(1, std::min(sk, max_sk));
     s.kps = ((nkc + sk - 1) / sk) * kTcBK;
     s.sk = (K + s.kps - 1) / s.kps;
