@@ -81,6 +81,37 @@ def test_noalloc_equals_regular_decode_bitwise_twice(tsp, name):
     plan.close()
 
 
+def test_noalloc_with_int8_cache_equals_regular_decode_bitwise(tsp):
+    """The INT8 KV cache plan through the allocation-free entry point: tokens,
+    logits and every part of the INT8 cache bit-identical to tiles_decode's."""
+    import torch
+    cfg = replace(S.CONFIGS["tiny"], name="kv8", start_pos=230, n_prompt=2, n_new=40, max_pos=300,
+                  gain_sigma=0.25)
+    w, k, v, prompt = inputs(cfg)
+    prompt = np.ascontiguousarray(prompt[: cfg.n_prompt], np.int32)
+    desc = tsp.ModelDesc.from_config(cfg)
+    plan = tsp.Plan(desc, tsp.upload_weights(w), tsp.make_opts(kv_format=tsp.KV_INT8))
+    outs = []
+    for use_noalloc in (False, True, True):
+        cache = tsp.KV8Cache(desc).from_bf16(tsp.to_device_bf16(k), tsp.to_device_bf16(v), cfg.start_pos)
+        steps = prompt.size - 1 + cfg.n_new
+        toks = torch.full((cfg.n_new,), -1, dtype=torch.int32, device="cuda")
+        logits = torch.full((steps, cfg.vocab), float("nan"), dtype=torch.float32, device="cuda")
+        dprompt = torch.from_numpy(prompt).cuda()
+        fn = plan.decode_noalloc if use_noalloc else plan.decode
+        fn(cache.k, cache.v, dprompt, cfg.start_pos, cfg.n_new, toks, logits)
+        plan.check()
+        outs.append((toks.cpu().numpy(), logits.cpu().numpy(), cache.host()))
+    assert not np.isnan(outs[0][1]).any()
+    for got in outs[1:]:
+        assert np.array_equal(got[0], outs[0][0])
+        assert np.array_equal(got[1].view(np.uint32), outs[0][1].view(np.uint32))
+        for part in ("kq", "vq", "ks", "vs", "mu"):
+            assert np.array_equal(got[2][part], outs[0][2][part])
+    plan.close()
+
+
+
 def test_noalloc_rejects_a_plan_that_does_not_fit(tsp):
     """16 q heads of 128 dims in 64 KV splits need 1.06 MB of split partials
     (64-bit words), more than the fixed 1 MiB array."""
