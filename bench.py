@@ -11,7 +11,14 @@ are checked bit for bit.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
                   [--scheduler counters|waves|flags|all] [--impl ours|reference] [--tokens T]
+                  [--weights bf16|int8] [--kv bf16|int8]
                   [--mode decode|prefill|verify] [--prompt N] [--k K]
+
+--weights int8: weight-only INT8 GEMVs; --kv int8: the INT8 KV cache with
+smoothed keys (built from the BF16 prefill outside the timed region); each
+changes the algorithmic bytes the roofline fraction is taken on. --mode
+prefill / verify time the multi-token pass (tensor roofline on the weight
+FLOPs) and the greedy verify step.
 
 With N > 1 (launched by torchrun) every rank runs an independent replica: a
 batch-1 decode has no exchange step to shard (replicas only). `--impl
@@ -468,6 +475,10 @@ def run_multi(args):
         return statistics.mean(ts), statistics.median(ts), clk.summary()
 
     peaks = measured_peaks() or {}
+    # kernels of one pass: embedding + norm; per layer Q/K/V GEMM, q/k post,
+    # attention, combine, O GEMM, residual norm, gate/up GEMM, SwiGLU, down
+    # GEMM, residual norm; LM-head GEMM and argmax
+    launches_per_pass = 3 + 10 * cfg.n_layers
     line = {"n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
     if args.mode == "prefill":
@@ -488,7 +499,8 @@ def run_multi(args):
                      "roofline": {"bound": "tensor", "achieved": flops / mean_s / 1e12, "peak": peak,
                                   "unit": "TFLOP/s", "frac": flops / mean_s / 1e12 / peak, "traffic": None,
                                   "note": "weight FLOPs 2 x parameters x tokens; attention not counted"},
-                     "clocks": clk, "gpu_launches": None})
+                     "clocks": clk,
+                     "gpu_launches": launches_per_pass * ((n + tsp.MAX_FORWARD_TOKENS - 1) // tsp.MAX_FORWARD_TOKENS)})
     else:
         k, v = S.kv_prefill(cfg)
         kc, vc = tsp.to_device_bf16(k), tsp.to_device_bf16(v)
@@ -505,7 +517,7 @@ def run_multi(args):
                      "unit": "tok/s", "ms_per_step": 1e3 * mean_s,
                      "config": {"workload": f"{cfg.name}: {cfg.start_pos} cached positions, {args.k} drafts "
                                             f"(the decode kernel's greedy tokens), {acc} accepted"},
-                     "accepted": acc, "clocks": clk, "gpu_launches": None})
+                     "accepted": acc, "clocks": clk, "gpu_launches": launches_per_pass + 1})
     print(json.dumps(line), flush=True)
     plan.close()
     return 0
