@@ -542,19 +542,18 @@ tiles_status_t forward_setup(tiles_plan_s *plan) {
     for (int T = 1; T <= Tm; ++T)
         pairs = std::max(pairs, (size_t)T * std::min((g.max_pos + 63) / 64,
                                                      attn_splits_wanted(g, T, plan->sm_count)));
-    cudaError_t e;
-    if ((e = falloc(plan, &f.x, (size_t)Tm * g.H * 2)) != cudaSuccess ||
-        (e = falloc(plan, &f.h, (size_t)Tm * g.H * 2)) != cudaSuccess ||
-        (e = falloc(plan, &f.q, (size_t)Tm * g.qd * 2)) != cudaSuccess ||
-        (e = falloc(plan, &f.o, (size_t)Tm * g.qd * 2)) != cudaSuccess ||
-        (e = falloc(plan, &f.a, (size_t)Tm * g.F * 2)) != cudaSuccess ||
-        (e = falloc(plan, &f.part, part * 4)) != cudaSuccess ||
-        (e = falloc(plan, &f.apart, pairs * g.nq * (2 + g.d) * 4)) != cudaSuccess ||
-        (e = falloc(plan, &f.logits, (size_t)Tm * g.V * 4)) != cudaSuccess ||
-        (e = falloc(plan, &f.argmax, (size_t)Tm * 4)) != cudaSuccess ||
-        (e = falloc(plan, &f.tokens, (size_t)(Tm + 1) * 4)) != cudaSuccess ||
-        (e = falloc(plan, &f.arg_keys, (size_t)Tm * 8)) != cudaSuccess ||
-        (e = falloc(plan, &f.arg_tickets, (size_t)Tm * 4)) != cudaSuccess)
+    if (falloc(plan, &f.x, (size_t)Tm * g.H * 2) != cudaSuccess ||
+        falloc(plan, &f.h, (size_t)Tm * g.H * 2) != cudaSuccess ||
+        falloc(plan, &f.q, (size_t)Tm * g.qd * 2) != cudaSuccess ||
+        falloc(plan, &f.o, (size_t)Tm * g.qd * 2) != cudaSuccess ||
+        falloc(plan, &f.a, (size_t)Tm * g.F * 2) != cudaSuccess ||
+        falloc(plan, &f.part, part * 4) != cudaSuccess ||
+        falloc(plan, &f.apart, pairs * g.nq * (2 + g.d) * 4) != cudaSuccess ||
+        falloc(plan, &f.logits, (size_t)Tm * g.V * 4) != cudaSuccess ||
+        falloc(plan, &f.argmax, (size_t)Tm * 4) != cudaSuccess ||
+        falloc(plan, &f.tokens, (size_t)(Tm + 1) * 4) != cudaSuccess ||
+        falloc(plan, &f.arg_keys, (size_t)Tm * 8) != cudaSuccess ||
+        falloc(plan, &f.arg_tickets, (size_t)Tm * 4) != cudaSuccess)
         return TILES_ERR_CUDA;
     // the argmax kernel leaves them at zero after every pass
     if (cudaMemset(f.arg_keys, 0, (size_t)Tm * 8) != cudaSuccess ||
@@ -581,7 +580,6 @@ tiles_status_t forward_pass(tiles_plan_s *plan, uint16_t *kc, uint16_t *vc, cons
     const int sms = plan->sm_count;
     const float eps = kp.eps;
     std::vector<LayerPtrs> &lp = plan->layers_host;
-    cudaError_t e;
     int sk = 1;
     embed_norm_kernel<<<T, 256, 0, st>>>(tokens, kp.embed, g.V, g.H, lp[0].attn_norm, eps, f.x, f.h, kp.status);
     const int split = attn_split_len(g, P0, T, sms);
@@ -590,7 +588,7 @@ tiles_status_t forward_pass(tiles_plan_s *plan, uint16_t *kc, uint16_t *vc, cons
     const dim3 agrid((T * g.G + 63) / 64, g.nkv, S);
     for (int l = 0; l < g.L; ++l) {
         const LayerPtrs &L = lp[l];
-        if ((e = gemm(plan, L.qkv, g.H, f.h, g.H, g.qkv_rows, T, g.H, f.part, 1 << 30, &sk, st)) != cudaSuccess)
+        if (gemm(plan, L.qkv, g.H, f.h, g.H, g.qkv_rows, T, g.H, f.part, 1 << 30, &sk, st) != cudaSuccess)
             return TILES_ERR_CUDA;
         const dim3 qgrid(T, g.nq + 2 * g.nkv);
         if (g.d == 64)
@@ -608,20 +606,20 @@ tiles_status_t forward_pass(tiles_plan_s *plan, uint16_t *kc, uint16_t *vc, cons
             attn_mt_kernel<128><<<agrid, 128, attn_smem(128), st>>>(f.q, kc, vc, l, g.nq, g.nkv, g.G, g.max_pos, P0, T, split,
                                                        kp.attn_scale, f.apart, S);
         attn_combine_kernel<<<dim3(T, g.nq), g.d, 0, st>>>(f.apart, S, g.nq, g.d, f.o);
-        if ((e = gemm(plan, L.o, g.qd, f.o, g.qd, g.H, T, g.qd, f.part, 1 << 30, &sk, st)) != cudaSuccess)
+        if (gemm(plan, L.o, g.qd, f.o, g.qd, g.H, T, g.qd, f.part, 1 << 30, &sk, st) != cudaSuccess)
             return TILES_ERR_CUDA;
         resid_norm_kernel<<<T, 512, 0, st>>>(f.part, sk, T, g.H, f.x, L.ffn_norm, eps, f.h);
-        if ((e = gemm(plan, L.gu, g.H, f.h, g.H, 2 * g.F, T, g.H, f.part, 1 << 30, &sk, st)) != cudaSuccess)
+        if (gemm(plan, L.gu, g.H, f.h, g.H, 2 * g.F, T, g.H, f.part, 1 << 30, &sk, st) != cudaSuccess)
             return TILES_ERR_CUDA;
         swiglu_kernel<<<std::min(4096, (T * g.F / 2 + 255) / 256), 256, 0, st>>>(f.part, sk, T, g.F, f.a);
-        if ((e = gemm(plan, L.down, g.F, f.a, g.F, g.H, T, g.F, f.part, 1 << 30, &sk, st)) != cudaSuccess)
+        if (gemm(plan, L.down, g.F, f.a, g.F, g.H, T, g.F, f.part, 1 << 30, &sk, st) != cudaSuccess)
             return TILES_ERR_CUDA;
         const uint16_t *next_gain = l + 1 < g.L ? lp[l + 1].attn_norm : kp.final_norm;
         resid_norm_kernel<<<T, 512, 0, st>>>(f.part, sk, T, g.H, f.x, next_gain, eps, f.h);
     }
     // LM head (tied embedding), one split: the partial sums are the logits
     float *lg = logits ? logits : f.logits;
-    if ((e = gemm(plan, kp.embed, g.H, f.h, g.H, g.V, T, g.H, lg, 1, &sk, st)) != cudaSuccess) return TILES_ERR_CUDA;
+    if (gemm(plan, kp.embed, g.H, f.h, g.H, g.V, T, g.H, lg, 1, &sk, st) != cudaSuccess) return TILES_ERR_CUDA;
     argmax_kernel<<<dim3(T, kArgBlocks), 256, 0, st>>>(lg, g.V, f.arg_keys, f.arg_tickets, argmax);
     return cudaGetLastError() == cudaSuccess ? TILES_OK : TILES_ERR_CUDA;
 }
