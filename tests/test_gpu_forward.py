@@ -268,3 +268,23 @@ def test_forward_rejects_int8_plans_and_overflow(tsp):
         plan.forward(kc, vc, toks, cfg.max_pos - 4, am)
     assert e.value.status == -5
     plan.close()
+
+
+@pytest.mark.parametrize("n,start", [(1, 0), (1, 37), (256, 0), (5, 123)], ids=["one_token", "one_token_cached",
+                                                                                "exactly_one_pass", "up_to_max_pos"])
+def test_forward_edge_lengths_match_oracle(tsp, n, start):
+    """A pass of one token (a decode step), of exactly 256 tokens (one full
+    pass), and one that ends on the last cache position (start + n =
+    max_pos): every logit and greedy choice against the oracle's prompt path,
+    the cache written up to the end and nothing past it."""
+    max_pos = 260 if n == 256 else 128
+    cfg = replace(S.CONFIGS["tiny"], name="edge", max_pos=max_pos, start_pos=start, gain_sigma=GAINS)
+    w, k, v, _ = inputs(cfg)
+    toks = S.tokens(S.SEED_TOKENS, 11, n, cfg.vocab)
+    plan = _plan(tsp, cfg, w)
+    am, lg, kc, vc = _forward(tsp, plan, cfg, k, v, toks, start)
+    plan.close()
+    _, kk, vv = check_forward(am, lg, cfg, w, k, v, toks, start, f"edge n={n} start={start}")
+    _cache_close(kc, kk, start + n)
+    _cache_close(vc, vv, start + n)
+    assert not kc[:, :, start + n:].any() and not vc[:, :, start + n:].any()
