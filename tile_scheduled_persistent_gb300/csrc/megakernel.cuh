@@ -1477,13 +1477,15 @@ struct Consumer {
     // Key scales multiply the score rows after the MMA; value scales fold into
     // p (masked positions get exact zeros, so stale codes and scales past npos
     // never reach the sums); l sums the unscaled p.
-    template <int D, int G>
+    // A round is NP 16-position blocks; this warp takes rounds grp0,
+    // grp0 + grp_step, ... of the chunk (all of them when it owns the chunk;
+    // one block in eight when all warps share a chunk of a short split).
+    template <int D, int G, int NP>
     __device__ __forceinline__ void attn_chunk_mma_q8(const uint8_t *slot, int npos, const uint32_t *qcol,
                                                       bool qcol_ok, float (&m)[2], float (&l)[2],
-                                                      float (&o)[D / 16][4]) {
+                                                      float (&o)[D / 16][4], int grp0, int grp_step) {
         constexpr int KVB = 8192 / D;  // positions per chunk; also the value tile's row bytes
-        constexpr int SUB = 2048 / D;  // positions per round
-        constexpr int NP = SUB / 16;   // 16-position blocks per round
+        constexpr int SUB = 16 * NP;   // positions per round
         constexpr int KU = D / 16;     // 16-byte units of a key row (= k-steps)
         constexpr int MT = D / 16;     // 16-dim row tiles of o^T
         const uint32_t kb = smem_u32(slot), vb = kb + 8192u;
@@ -1493,7 +1495,7 @@ struct Consumer {
         const int mi = lane >> 3, ri = lane & 7;
         const int kr_off = 4 * (ri >> 1) + (ri & 1) + 2 * (mi & 1);  // position of the row this lane addresses
         const int my_off = 4 * (g8 >> 1) + (g8 & 1);                 // position of this lane's row g (+2: row g + 8)
-        for (int p0 = 0; p0 < npos; p0 += SUB) {
+        for (int p0 = grp0 * SUB; p0 < npos; p0 += grp_step * SUB) {
             float s[NP][4];
 #pragma unroll
             for (int pt = 0; pt < NP; ++pt) {
@@ -1839,6 +1841,23 @@ struct Consumer {
                 float mm[2] = {-INFINITY, -INFINITY}, ll[2] = {0.f, 0.f}, oo[D / 16][4];
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) oo[mt][0] = oo[mt][1] = oo[mt][2] = oo[mt][3] = 0.f;
+                if (KV8 && nch < (uint32_t)kConsumerWarps) {
+                    // a short split (INT8 cache): every warp works on every chunk,
+                    // one 16-position block in eight each; the chunk is released
+                    // once all warps are done with it
+                    for (uint32_t k = 0; k < nch; ++k) {
+                        const uint32_t jj = j + k;
+                        uint8_t *slot = wait_chunk(jj);
+                        const int q0 = (b0 + (int)k) * g.kv_block;
+                        int q1 = q0 + g.kv_block;
+                        if (q1 > P + 1) q1 = P + 1;
+                        if (slot && warp == 0 && q0 <= P && P < q1) place_new_kv_q8<D>(slot, q0);
+                        if (consumer_sync_or(bad)) break;
+                        attn_chunk_mma_q8<D, G, 1>(slot, q1 - q0, qcol, g8 < G, mm, ll, oo, warp, kConsumerWarps);
+                        consumer_sync();
+                        if (tid == 0) mbar_arrive(&s.empty[jj % (uint32_t)g.ring_slots]);
+                    }
+                } else {
                 for (uint32_t k = 0; k < nch; ++k) {
                     const uint32_t jj = j + k;
                     if (!mine(jj)) continue;
@@ -1849,12 +1868,13 @@ struct Consumer {
                     if (q1 > P + 1) q1 = P + 1;
                     if (KV8) {
                         if (q0 <= P && P < q1) place_new_kv_q8<D>(slot, q0);
-                        attn_chunk_mma_q8<D, G>(slot, q1 - q0, qcol, g8 < G, mm, ll, oo);
+                        attn_chunk_mma_q8<D, G, 2048 / D / 16>(slot, q1 - q0, qcol, g8 < G, mm, ll, oo, 0, 1);
                     } else {
                         if (q0 <= P && P < q1) place_new_kv_swz<D>(slot, q0);
                         attn_chunk_mma<D, G>(slot, q1 - q0, qcol, g8 < G, mm, ll, oo);
                     }
                     release_chunk(jj);
+                }
                 }
                 // per-warp states -> shared memory: l summed over the lanes of a
                 // head (lanes with the same t), then heads 2 t4 and 2 t4 + 1
