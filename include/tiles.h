@@ -129,8 +129,15 @@ enum { TILES_KV_BF16 = 0, TILES_KV_INT8 = 1 };
 typedef struct {
     int32_t scheduler;    /* TILES_SCHED_FLAGS (default), _COUNTERS or _WAVES            */
     int32_t n_ctas;       /* 0 = one worker CTA per SM                                  */
-    int32_t slot_bytes;   /* 0 = auto (16 KB or the longest row): ring slot bytes, mult. of 1024 */
-    int32_t ring_slots;   /* 0 = one per consumer warp (8), fewer if they do not fit     */
+    int32_t slot_bytes;   /* ring slot bytes, a multiple of 1024. 0 = auto: Q/K/V, O and
+                           * KV-block chunks fill 16 KB (or the longest row, or two
+                           * gate/up row pairs, if larger); the slot, which gate/up,
+                           * down and LM-head chunks fill, grows from there to whole
+                           * gate/up pairs while 8 slots fit shared memory and a CTA's
+                           * gate/up rows still make 16 chunks. Nonzero: every chunk
+                           * fills this size.                                         */
+    int32_t ring_slots;   /* 0 = one per consumer warp (8), fewer if they do not fit;
+                           * nonzero also keeps the slot at the 16 KB rule             */
     int32_t kv_splits;    /* 0 = auto: split-KV ranges per KV head                       */
     int32_t timeout_ms;   /* bound on every in-kernel wait; 0 = 2000 ms                  */
     int32_t l2_prefetch_kb; /* L2 prefetch warp: weight bytes it may run ahead of the ring, KB per CTA; <= 0 = off */

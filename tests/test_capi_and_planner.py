@@ -209,28 +209,85 @@ def _ceil(a, b):
     return -(-a // b)
 
 
+def _chain_budget(cfg, wb, kv8=False, slot_bytes=0):
+    """The chunk budget of the chain's GEMVs (Q/K/V, O-projection) and of a BF16
+    KV block: the caller's slot, else 16 KB, four hidden-wide rows or the
+    longest row (two for gate/up), whichever is largest, in whole KB."""
+    if slot_bytes:
+        return slot_bytes
+    H, F, qd, d = cfg.hidden, cfg.ffn, cfg.q_dim, cfg.head_dim
+    need = max(wb * H, wb * qd, wb * F, 2 * wb * H, 2 * 8192 + 2 * (8192 // d) * 4 if kv8 else 0)
+    return _ceil(max(need, 16384, 4 * wb * H), 1024) * 1024
+
+
+def _check_slot_growth(info, cfg, wb, n, chain, grows):
+    """The slot is the chain budget, or, for a default plan (`grows`), the
+    largest whole number k of gate/up pairs above it with eight slots within
+    227 KB of shared memory and k <= ceil(F / CTAs) / 16 (two ring laps)."""
+    slot, pair = info["slot_bytes"], 2 * wb * cfg.hidden
+    rest = info["smem_bytes"] - info["ring_slots"] * slot   # control block + vector area
+    kmax = _ceil(cfg.ffn, n) // 16 if grows else 0
+    fits = [k for k in range(kmax, 0, -1)
+            if _ceil(k * pair, 1024) * 1024 > chain and rest + 8 * _ceil(k * pair, 1024) * 1024 <= 232448]
+    # the loop stops at the first k whose slot is not above the chain budget
+    stop = next((k for k in range(kmax, 0, -1) if _ceil(k * pair, 1024) * 1024 <= chain), 0)
+    fits = [k for k in fits if k > stop]
+    want = _ceil(fits[0] * pair, 1024) * 1024 if fits else chain
+    assert slot == want, (slot, want, chain)
+
+
 def test_int8_layer_chunks_give_every_consumer_warp_work():
-    """INT8 layer GEMVs: rows per chunk = min(what fills a slot (at most 8),
-    ceil(ceil(rows / CTAs) / 8)); the LM head and BF16 keep full chunks."""
+    """INT8 layer GEMVs: rows per chunk = min(what fills the op's budget (at
+    most 8), ceil(ceil(rows / CTAs) / 8)); the LM head and BF16 keep full
+    chunks. Q/K/V and the O-projection fill the chain budget, the rest the
+    slot."""
     for name in ("llama1b", "qwen3_0_6b", "qwen3_4b"):
         cfg = S.CONFIGS[name]
         H, F, qkv = cfg.hidden, cfg.ffn, cfg.q_dim + 2 * cfg.kv_dim
         bi, qi = _sched(name).info(), _sched(name, weight_format=tsp.WEIGHTS_INT8).info()
         b, q = bi["rows_per_chunk"], qi["rows_per_chunk"]
-        # a slot holds 16 KB or the longest row (Qwen3-4B BF16: one 9,728-wide down row)
         slot = {2: bi["slot_bytes"], 1: qi["slot_bytes"]}
+        chain = {2: _chain_budget(cfg, 2), 1: _chain_budget(cfg, 1)}
+        _check_slot_growth(bi, cfg, 2, 152, chain[2], True)
+        _check_slot_growth(qi, cfg, 1, 152, chain[1], True)
         full = lambda width, mats, wb: min(8, slot[wb] // (width * wb * mats))
-        assert b == {"qkv": full(H, 1, 2), "o": full(cfg.q_dim, 1, 2), "gateup": full(H, 2, 2),
+        cfull = lambda width, mats, wb: min(8, chain[wb] // (width * wb * mats))
+        assert b == {"qkv": cfull(H, 1, 2), "o": cfull(cfg.q_dim, 1, 2), "gateup": full(H, 2, 2),
                      "down": full(F, 1, 2), "lm": full(H, 1, 2)}
         cap = lambda rows: _ceil(_ceil(rows, 152), 8)
-        assert q == {"qkv": max(1, min(full(H, 1, 1), cap(qkv))),
-                     "o": max(1, min(full(cfg.q_dim, 1, 1), cap(H))),
+        assert q == {"qkv": max(1, min(cfull(H, 1, 1), cap(qkv))),
+                     "o": max(1, min(cfull(cfg.q_dim, 1, 1), cap(H))),
                      "gateup": max(1, min(full(H, 2, 1), cap(F))),
                      "down": max(1, min(full(F, 1, 1), cap(H))),
                      "lm": full(H, 1, 1)}
     # worked by hand for the Llama-1B shape: 3072 Q/K/V rows -> 21 per CTA -> 3 per chunk
     assert _sched("llama1b", weight_format=tsp.WEIGHTS_INT8).info()["rows_per_chunk"] == \
         {"qkv": 3, "o": 2, "gateup": 4, "down": 2, "lm": 8}
+
+
+def test_default_slot_grows_by_whole_gate_up_pairs():
+    """Worked by hand, 152 CTAs. Llama-1B shape, BF16: 54 gate/up pairs of
+    8 KB per CTA allow at most 3 pairs a chunk (two laps of 8), and 8 x 24 KB
+    fit, so 24 KB slots with 3 pairs, 6 LM-head rows, but Q/K/V and O at the
+    16 KB budget (4 rows) and 64-position KV blocks. Qwen3-0.6B: 21 pairs
+    allow 1 pair (4 KB), under 16 KB: no growth. Qwen3-4B BF16: 64 pairs of
+    10 KB allow 4, but only 2 (20 KB, the budget itself) fit. Qwen3-4B INT8:
+    4 pairs of 5 KB = 20 KB over a 16 KB budget. A slot or ring size given by
+    the caller turns the growth off."""
+    i = _sched("llama1b").info()
+    assert (i["slot_bytes"], i["ring_slots"], i["kv_block"]) == (24576, 8, 64)
+    assert i["rows_per_chunk"] == {"qkv": 4, "o": 4, "gateup": 3, "down": 1, "lm": 6}
+    assert i["smem_bytes"] <= 232448
+    assert _sched("llama1b", kv_format=tsp.KV_INT8).info()["slot_bytes"] == 24576
+    assert _sched("qwen3_0_6b").info()["slot_bytes"] == 16384
+    assert _sched("qwen3_4b").info()["slot_bytes"] == 20480
+    q4 = _sched("qwen3_4b", weight_format=tsp.WEIGHTS_INT8).info()
+    assert q4["slot_bytes"] == 20480 and q4["rows_per_chunk"]["gateup"] == 4
+    assert _sched("llama1b", weight_format=tsp.WEIGHTS_INT8).info()["slot_bytes"] == 16384
+    for opts in (dict(slot_bytes=16384), dict(ring_slots=8)):
+        j = _sched("llama1b", **opts).info()
+        assert j["slot_bytes"] == 16384
+        assert j["rows_per_chunk"] == {"qkv": 4, "o": 4, "gateup": 2, "down": 1, "lm": 4}
 
 
 def test_tensor_core_attention_only_where_a_split_can_reach_eight_chunks():
@@ -291,18 +348,20 @@ def test_random_shapes_build_valid_schedules_with_consistent_chunk_geometry():
         H, F, qd = cfg.hidden, cfg.ffn, cfg.q_dim
         qkv = qd + 2 * cfg.kv_dim
         slot = info["slot_bytes"]
+        chain = _chain_budget(cfg, wb, opts.get("kv_format", 0) == tsp.KV_INT8, opts.get("slot_bytes", 0))
+        _check_slot_growth(info, cfg, wb, n, chain, "slot_bytes" not in opts and "ring_slots" not in opts)
         widths = {"qkv": (H, 1, qkv), "o": (qd, 1, H), "gateup": (H, 2, F), "down": (F, 1, H),
                   "lm": (H, 1, 0)}
         for op, rows in info["rows_per_chunk"].items():
             width, mats, out_rows = widths[op]
-            full = min(8, slot // (width * wb * mats))
+            full = min(8, (chain if op in ("qkv", "o") else slot) // (width * wb * mats))
             assert 1 <= rows <= full and rows * width * wb * mats <= slot
             if wb == 1 and op != "lm":
                 assert rows == max(1, min(full, _ceil(_ceil(out_rows, n), 8)))
             else:
                 assert rows == full
         kvb, S_ = info["kv_block"], info["kv_splits"]
-        assert 1 <= kvb <= 256 and 2 * kvb * d * 2 <= slot
+        assert 1 <= kvb <= 256 and 2 * kvb * d * 2 <= chain
         want = _ceil(_ceil(cfg.max_pos, kvb), S_) >= 8 and kvb % (2048 // d) == 0
         assert info["attn_tensor_cores"] == int(want)
         built += 1

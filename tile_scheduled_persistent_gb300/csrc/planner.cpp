@@ -114,28 +114,27 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     // an INT8 KV chunk (codes of 8 KB of keys and 8 KB of values, and their
     // scales) fills one slot
     int need = std::max({wb * G_.H, wb * G_.qd, wb * G_.F, 2 * wb * G_.H, G_.kv8 ? kv8_chunk_bytes(G_.d) : 0});
-    int slot = o.slot_bytes > 0 ? o.slot_bytes : round_up(std::max({need, 16384, 4 * wb * G_.H}), 1024);
-    if (slot % 1024 || slot < need) return fail(TILES_ERR_INVALID_ARG, "slot_bytes too small or not a multiple of 1024");
-    G_.slot_bytes = slot;
-    // Rows per chunk: as many as fill a slot. INT8 layer GEMVs are capped so
+    // `chain`: the chunk budget of the Q/K/V and O-projection GEMVs and of a
+    // BF16 KV block, whose chunks sit on the layer's dependency chain.
+    const int chain = o.slot_bytes > 0 ? o.slot_bytes : round_up(std::max({need, 16384, 4 * wb * G_.H}), 1024);
+    if (chain % 1024 || chain < need) return fail(TILES_ERR_INVALID_ARG, "slot_bytes too small or not a multiple of 1024");
+    // Rows per chunk: as many as fill the op's budget (`chain` for Q/K/V and
+    // the O-projection, the slot for the rest). INT8 layer GEMVs are capped so
     // that a CTA's share of rows splits into at least one chunk per consumer
     // warp: a 16 KB INT8 chunk holds twice the weights of a BF16 one, and in
     // the short, latency-bound layer phases one warp's chunk arithmetic sets
     // the pace (GB300: Llama-1B shape 1547 -> 1682 tok/s, Qwen3-0.6B shape
     // 1049 -> 1273; the same cap on BF16 measured neutral, so BF16 keeps full
     // chunks). The LM head streams far more rows than warps and stays full.
-    auto rpc = [&](int in, int mats, int rows) {
-        const int full = std::min(kMaxRowsPerChunk, slot / (in * G_.wbytes * mats));
+    auto rpc = [&](int in, int mats, int rows, int budget) {
+        const int full = std::min(kMaxRowsPerChunk, budget / (in * G_.wbytes * mats));
         if (G_.wbytes != 1 || rows <= 0) return full;
         const int per_cta = ceil_div(rows, n_ctas);
         return std::max(1, std::min(full, ceil_div(per_cta, kConsumerWarps)));
     };
-    G_.rpc_qkv = rpc(G_.H, 1, G_.qkv_rows);
-    G_.rpc_o = rpc(G_.qd, 1, G_.H);
-    G_.rpc_gateup = rpc(G_.H, 2, G_.F);
-    G_.rpc_down = rpc(G_.F, 1, G_.H);
-    G_.rpc_lm = rpc(G_.H, 1, 0);
-    int kb = slot / (2 * G_.d * 2);
+    G_.rpc_qkv = rpc(G_.H, 1, G_.qkv_rows, chain);
+    G_.rpc_o = rpc(G_.qd, 1, G_.H, chain);
+    int kb = chain / (2 * G_.d * 2);
     kb = kb >= 32 ? kb / 32 * 32 : kb;
     kb = std::min(kb, 256);  // a chunk's positions are one TMA box (at most 256 rows)
     if (G_.kv8) kb = kv8_block(G_.d);
@@ -163,6 +162,31 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     // residual rows of an O-proj / down tile follow (a tile has at most H rows)
     G_.res_off = round_up(vec, 16);
     G_.vec_bytes = round_up(G_.res_off + 2 * G_.H, 128);
+    int slot = chain;
+    if (o.slot_bytes <= 0 && o.ring_slots <= 0) {
+        // While the chain runs the ring fills with the layer's gate/up rows, and
+        // HBM idles once it is full. So the default slot grows to the largest
+        // whole number of gate/up pairs with which eight slots still fit the
+        // shared memory and a CTA's gate/up share still spans two ring laps;
+        // the chain's GEMVs keep `chain`-sized chunks, since fewer, longer
+        // chunks there lengthen the chain. GB300, Llama-1B shape: 8 x 24 KB
+        // slots (three pairs) 1542 tok/s against 1507-1522 with 16 KB; without
+        // the chain budget 1493; Qwen3-0.6B shape with 24 KB slots (six pairs,
+        // four chunks a CTA) 1281 against 1337-1344.
+        const int pair = 2 * wb * G_.H;
+        for (int k = ceil_div(G_.F, n_ctas) / (2 * kConsumerWarps); k >= 1; --k) {
+            const int cand = round_up(k * pair, 1024);
+            if (cand <= chain) break;
+            if (kCtlBytes + kConsumerWarps * cand + G_.vec_bytes <= smem_limit) {
+                slot = cand;
+                break;
+            }
+        }
+    }
+    G_.slot_bytes = slot;
+    G_.rpc_gateup = rpc(G_.H, 2, G_.F, slot);
+    G_.rpc_down = rpc(G_.F, 1, G_.H, slot);
+    G_.rpc_lm = rpc(G_.H, 1, 0, slot);
     int avail = smem_limit - kCtlBytes - G_.vec_bytes;
     int slots = o.ring_slots > 0 ? o.ring_slots : std::min(kConsumerWarps, avail / slot);
     if (slots < 2 || slots > kMaxSlots) return fail(TILES_ERR_UNSUPPORTED, "ring needs 2..32 slots");
