@@ -279,9 +279,11 @@ tiles_status_t tiles_plan_set_trace(tiles_plan_t plan, void *trace, int32_t step
 typedef struct {
     int32_t n_ctas, threads_per_cta, smem_bytes, slot_bytes, ring_slots, kv_splits;
     int32_t scheduler, n_tasks, n_counters, phases_per_step, max_tasks_per_cta;
-    int32_t kv_block;           /* positions per KV chunk                                    */
-    int32_t attn_tensor_cores;  /* 1: attention splits of >= 8 chunks run on the tensor
-                                   cores (swizzled TMA tiles, m16n8k16 MMAs)                 */
+    int32_t kv_block;           /* positions per KV chunk (a multiple of 16)                 */
+    int32_t attn_tensor_cores;  /* 1: splits of >= 8 chunks give each chunk to one warp (the
+                                   kernel instance carries that form); 0: every split
+                                   shares its chunks across the warps. Either way every
+                                   chunk is a swizzled TMA tile reduced by m16n8k16 MMAs     */
     int32_t rows_per_chunk[5];  /* GEMV rows per ring chunk: Q/K/V, O, gate/up (pairs),
                                    down, LM head                                             */
     int32_t weight_format;      /* TILES_WEIGHTS_BF16 or TILES_WEIGHTS_INT8                   */

@@ -291,8 +291,10 @@ def test_default_slot_grows_by_whole_gate_up_pairs():
 
 
 def test_tensor_core_attention_only_where_a_split_can_reach_eight_chunks():
-    """1,088 positions in 64-position blocks over 17 splits: at most 1 chunk per
-    split (no tensor-core path); 32,832 positions over 19 splits: up to 28."""
+    """The owner form (one warp per chunk) only where a split can reach 8
+    chunks: 1,088 positions in 64-position blocks over 17 splits: at most 1
+    chunk per split (shared chunks); 32,832 positions over 19 splits: up to
+    28."""
     short, long_ = _sched("llama1b").info(), _sched("llama1b_long").info()
     assert (short["kv_block"], short["kv_splits"], short["attn_tensor_cores"]) == (64, 17, 0)
     assert (long_["kv_block"], long_["kv_splits"], long_["attn_tensor_cores"]) == (64, 19, 1)
@@ -361,7 +363,7 @@ def test_random_shapes_build_valid_schedules_with_consistent_chunk_geometry():
             else:
                 assert rows == full
         kvb, S_ = info["kv_block"], info["kv_splits"]
-        assert 1 <= kvb <= 256 and 2 * kvb * d * 2 <= chain
+        assert 16 <= kvb <= 256 and kvb % 16 == 0 and 2 * kvb * d * 2 <= chain
         want = _ceil(_ceil(cfg.max_pos, kvb), S_) >= 8 and kvb % (2048 // d) == 0
         assert info["attn_tensor_cores"] == int(want)
         built += 1

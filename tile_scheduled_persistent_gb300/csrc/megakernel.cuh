@@ -536,27 +536,6 @@ struct Producer {
         ++j;
     }
 
-    // K and V of positions [p0, p1) (all < P) of kv head `h`, layer `layer`.
-    __device__ void kv_chunk(int layer, int h, int p0, int p1) {
-        if (!owns(j)) {
-            ++j;
-            return;
-        }
-        uint64_t *bar;
-        uint8_t *dst = acquire(&bar);
-        if (!dst) return;
-        const Geom &g = p.g;
-        const int n = p1 > p0 ? p1 - p0 : 0;
-        const uint32_t bytes = (uint32_t)n * g.d * 2u;
-        mbar_expect_tx(bar, 2u * bytes);
-        if (n > 0) {
-            size_t off = ((size_t)(layer * g.nkv + h) * g.max_pos + p0) * g.d;
-            bulk_g2s_nohint(dst, p.k_cache + off, bytes, bar);
-            bulk_g2s_nohint(dst + (size_t)g.kv_block * g.d * 2, p.v_cache + off, bytes, bar);
-        }
-        ++j;
-    }
-
     // The whole block of kv_block positions from q0 (a multiple of kv_block)
     // of kv head `h`, as swizzled tiles of the K and V tensor maps: one box
     // per 64 dims, K boxes then V boxes. Rows past max_pos arrive as zeros;
@@ -640,7 +619,6 @@ struct Producer {
     // the tensor-core form, 2 INT8 cache)
     template <int AK>
     __device__ __forceinline__ void run(int cta) {
-        constexpr bool MMA = AK >= 1;
         const Geom &g = p.g;
         const int t0 = p.offsets[cta], t1 = p.offsets[cta + 1];
         fence_proxy_async_global();
@@ -665,16 +643,13 @@ struct Producer {
                         const int c = (int)(it % (uint32_t)g.kv_splits);
                         int b0, b1;
                         attn_split_blocks(g, P + 1, c, &b0, &b1);
-                        const bool mma = MMA && attn_uses_mma(g, b1 - b0);
+                        // whole blocks: positions from P on are overwritten,
+                        // zeroed or masked by the consumer
                         for (int b = b0; b < b1 && ok; ++b) {
-                            int q0 = b * g.kv_block, q1 = q0 + g.kv_block;
-                            if (q1 > P) q1 = P;  // position P itself is computed in this step
                             if (AK == 2)
-                                kv_chunk_q8(t.layer, h, q0);
-                            else if (mma)
-                                kv_chunk_tensor(t.layer, h, q0);
+                                kv_chunk_q8(t.layer, h, b * g.kv_block);
                             else
-                                kv_chunk(t.layer, h, q0, q1);
+                                kv_chunk_tensor(t.layer, h, b * g.kv_block);
                         }
                     }
                 }
@@ -962,23 +937,6 @@ __device__ __forceinline__ void gemv_rows_q8_n(uint32_t nr, const uint8_t *slot,
     }
 }
 
-// this lane's DPL elements (2 or 4 consecutive dims) of one bf16 V row
-template <int DPL>
-__device__ __forceinline__ void v_piece(const uint8_t *vrow, float (&vf)[DPL]) {
-    const int lane = threadIdx.x & 31;
-    if constexpr (DPL == 2) {
-        const uint32_t w = reinterpret_cast<const uint32_t *>(vrow)[lane];
-        vf[0] = bf_lo(w);
-        vf[1] = bf_hi(w);
-    } else {
-        const uint2 w = reinterpret_cast<const uint2 *>(vrow)[lane];
-        vf[0] = bf_lo(w.x);
-        vf[1] = bf_hi(w.x);
-        vf[2] = bf_lo(w.y);
-        vf[3] = bf_hi(w.y);
-    }
-}
-
 // ------------------------------------------------------------------ consumers
 struct Consumer {
     const KernelParams &p;
@@ -1226,10 +1184,8 @@ struct Consumer {
     // ---------------------------------------------------------- attention
     // Layout of the vec region during attention tasks.
     struct AttnSmem {
-        float *q;          // [G][d] f32 (bf16-valued)
         uint16_t *knew;    // [d]
         uint16_t *vnew;    // [d]
-        float *prob;       // [warps][32][G]
         float *wstate;     // [warps][G][4 + d]
         uint16_t *qh;      // [G][d + 8] bf16 q (rows padded: conflict-free MMA fragment loads)
         int8_t *k8, *v8;   // INT8 cache: codes of the new key (minus mu) and value rows [d]
@@ -1239,14 +1195,10 @@ struct Consumer {
         const Geom &g = p.g;
         AttnSmem a;
         uint8_t *b = s.vec;
-        a.q = reinterpret_cast<float *>(b);
-        b += (size_t)g.G * g.d * 4;
         a.knew = reinterpret_cast<uint16_t *>(b);
         b += (size_t)g.d * 2;
         a.vnew = reinterpret_cast<uint16_t *>(b);
         b += (size_t)g.d * 2;
-        a.prob = reinterpret_cast<float *>(b);
-        b += (size_t)kConsumerWarps * 32 * g.G * 4;
         a.wstate = reinterpret_cast<float *>(b);
         b += (size_t)kConsumerWarps * g.G * (kPartialPad + g.d) * 4;
         a.qh = reinterpret_cast<uint16_t *>(b);
@@ -1280,7 +1232,7 @@ struct Consumer {
 
     template <int D, int AK>
     __device__ void prep_qkv(int h, const AttnSmem &a) {
-        constexpr bool MMA = AK >= 1, KV8 = AK == 2;
+        constexpr bool KV8 = AK == 2;
         const Geom &g = p.g;
         const LayerPtrs &lw = p.layers[cur_layer];
         const float *cs = p.rope_cos + (size_t)P * (D / 2);
@@ -1341,9 +1293,7 @@ struct Consumer {
             if (is_q) {
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    const uint16_t qb = f2bf(v[e]);
-                    a.q[hh * D + lane + 32 * e] = bf2f(qb);
-                    if (MMA) a.qh[hh * (D + 8) + lane + 32 * e] = qb;  // tensor-core form
+                    a.qh[hh * (D + 8) + lane + 32 * e] = f2bf(v[e]);
                 }
             } else {
 #pragma unroll
@@ -1371,7 +1321,9 @@ struct Consumer {
     // Lane (g, t) = (lane / 4, lane % 4) holds the scores of positions g and
     // g + 8 of each block for heads 2t and 2t + 1, and their running m and l
     // (l summed over this lane's positions only, reduced over g at the end).
-    // Per round of 2048 / D positions:
+    // A round takes NP blocks from block grp0 on, and the next round starts
+    // grp_step rounds later: (NP, 0, 1) walks the whole chunk (2048 / D
+    // positions a round), (1, w, 8) gives warp w every eighth block. Per round:
     //   s = K q^T (FP32, exact BF16 products), masked past npos, times d^-1/2;
     //   m' = max(m, max over positions), c = e^(m - m'), p = e^(s - m'),
     //   l' = c l + sum p, o' = c o;
@@ -1379,18 +1331,18 @@ struct Consumer {
     //   BF16 high part and a BF16 remainder (two MMAs, ~16 bits kept);
     //   o^T += V^T p^T with V^T's fragments from transposed ldmatrix of V.
     // o[mt] holds (dims 16 mt + g and 16 mt + g + 8) x (heads 2t, 2t + 1).
-    template <int D, int G>
+    template <int D, int G, int NP>
     __device__ __forceinline__ void attn_chunk_mma(const uint8_t *slot, int npos, const uint32_t *qcol, bool qcol_ok,
-                                                   float (&m)[2], float (&l)[2], float (&o)[D / 16][4]) {
-        constexpr int SUB = 2048 / D;  // positions per round
-        constexpr int NP = SUB / 16;   // 16-position blocks per round
+                                                   float (&m)[2], float (&l)[2], float (&o)[D / 16][4], int grp0,
+                                                   int grp_step) {
+        constexpr int SUB = 16 * NP;  // positions per round (NP 16-position blocks)
         constexpr int KS = D / 16;     // k-steps of the scores
         constexpr int MT = D / 16;     // 16-dim row tiles of o^T
         const int kvb = p.g.kv_block;
         const uint32_t kb = smem_u32(slot), vb = kb + (uint32_t)kvb * D * 2;
         const int g8 = lane >> 2;
         const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix and row this lane points at
-        for (int p0 = 0; p0 < npos; p0 += SUB) {
+        for (int p0 = grp0 * SUB; p0 < npos; p0 += grp_step * SUB) {
             float s[NP][4];
 #pragma unroll
             for (int pt = 0; pt < NP; ++pt) {
@@ -1583,118 +1535,6 @@ struct Consumer {
         }
     }
 
-    // Cooperative form: this warp handles one q head (hi) and the T-position
-    // blocks blk_first, blk_first + blk_step, ... of a chunk all warps share,
-    // T = 32 / LP. Each position's q . k is split over LP consecutive lanes (an
-    // LP-th of the 16-byte columns each, rotated so a quarter warp touches 8
-    // distinct bank groups) and summed by shuffles; LP > 1 keeps every warp
-    // busy when a head's warps would otherwise get fewer than 32 positions each
-    // (head_dim 128 chunks hold 32 positions).
-    template <int D, int LP>
-    __device__ void attn_chunk_one(const uint8_t *slot, int npos, const AttnSmem &a, int hi,
-                                   int blk_first, int blk_step, float &m, float &l,
-                                   float (&o)[D / 32]) {
-        constexpr int NC = D / 8;
-        constexpr int DPL = D / 32;
-        constexpr int T = 32 / LP;
-        constexpr int CPL = NC / LP;  // 16-byte columns per lane
-        constexpr int ROT = (D == 128 && LP == 2) ? 4 : (D == 128 && LP == 4) ? 1 : 0;
-        static_assert(CPL >= 1, "more lanes per position than columns");
-        const Geom &g = p.g;
-        const uint8_t *Kb = slot;
-        const uint8_t *Vb = slot + (size_t)g.kv_block * D * 2;
-        const float *q = a.q + hi * D;
-        float *prob = a.prob + (size_t)warp * 32 * g.G;
-        const int tl = lane / LP, part = lane % LP;
-        for (int t0 = blk_first * T; t0 < npos; t0 += blk_step * T) {
-            const int t = t0 + tl;
-            const bool valid = t < npos;
-            // this lane's share of q . k, over four independent partial sums
-            float sc4[4] = {0.f, 0.f, 0.f, 0.f};
-            if (valid) {
-                const uint4 *krow = reinterpret_cast<const uint4 *>(Kb + (size_t)t * D * 2);
-#pragma unroll
-                for (int jj = 0; jj < CPL; ++jj) {
-                    const int col = part * CPL + ((jj + tl + ROT * part) & (CPL - 1));
-                    float kf[8];
-                    unpack8(krow[col], kf);
-                    const float4 qa = reinterpret_cast<const float4 *>(q + col * 8)[0];
-                    const float4 qb = reinterpret_cast<const float4 *>(q + col * 8)[1];
-                    float sc = sc4[jj & 3];
-                    sc = fmaf(kf[0], qa.x, sc); sc = fmaf(kf[1], qa.y, sc);
-                    sc = fmaf(kf[2], qa.z, sc); sc = fmaf(kf[3], qa.w, sc);
-                    sc = fmaf(kf[4], qb.x, sc); sc = fmaf(kf[5], qb.y, sc);
-                    sc = fmaf(kf[6], qb.z, sc); sc = fmaf(kf[7], qb.w, sc);
-                    sc4[jj & 3] = sc;
-                }
-            }
-            float sc = __fadd_rn(__fadd_rn(sc4[0], sc4[1]), __fadd_rn(sc4[2], sc4[3]));
-#pragma unroll
-            for (int off = LP / 2; off > 0; off >>= 1) sc += __shfl_xor_sync(0xFFFFFFFFu, sc, off);
-            const float si = valid ? sc * p.attn_scale : -INFINITY;
-            const float bm = warp_max(si);
-            const float mn = fmaxf(m, bm);
-            const float corr = expf(m - mn);
-            const float pi = valid ? expf(si - mn) : 0.f;
-            const float ps = warp_sum(part == 0 ? pi : 0.f);
-            l = fmaf(l, corr, ps);
-            m = mn;
-            if (part == 0) prob[tl] = pi;
-            __syncwarp();
-            // p . V over the block's positions, four positions in flight
-            const int nv = npos - t0 < T ? npos - t0 : T;
-            float acc[4][DPL];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) acc[u][e] = 0.f;
-            int tt = 0;
-            for (; tt + 4 <= nv; tt += 4) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float vf[DPL];
-                    v_piece<DPL>(Vb + (size_t)(t0 + tt + u) * D * 2, vf);
-                    const float pv = prob[tt + u];
-#pragma unroll
-                    for (int e = 0; e < DPL; ++e) acc[u][e] = fmaf(pv, vf[e], acc[u][e]);
-                }
-            }
-            for (; tt < nv; ++tt) {
-                float vf[DPL];
-                v_piece<DPL>(Vb + (size_t)(t0 + tt) * D * 2, vf);
-                const float pv = prob[tt];
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) acc[0][e] = fmaf(pv, vf[e], acc[0][e]);
-            }
-#pragma unroll
-            for (int e = 0; e < DPL; ++e)
-                o[e] = fmaf(o[e], corr, __fadd_rn(__fadd_rn(acc[0][e], acc[1][e]), __fadd_rn(acc[2][e], acc[3][e])));
-            __syncwarp();
-        }
-    }
-
-    // positions each warp of a head gets from one chunk -> lanes per position
-    __device__ int attn_lanes_per_pos(int warps_per_head) const {
-        const int ppw = (p.g.kv_block + warps_per_head - 1) / warps_per_head;
-        return ppw >= 32 ? 1 : ppw >= 16 ? 2 : ppw >= 8 ? 4 : 8;
-    }
-
-    // Put the freshly computed K/V of position P into the chunk's slot (the
-    // producer loaded only positions < P), then order these generic writes
-    // before the async-proxy copy that will later refill the slot.
-    template <int D>
-    __device__ void place_new_kv(uint8_t *slot, int q0, const AttnSmem &a) {
-        const Geom &g = p.g;
-        uint16_t *kd = reinterpret_cast<uint16_t *>(slot + (size_t)(P - q0) * D * 2);
-        uint16_t *vd = reinterpret_cast<uint16_t *>(slot + (size_t)g.kv_block * D * 2 + (size_t)(P - q0) * D * 2);
-        for (int e = lane; e < D; e += 32) {
-            kd[e] = a.knew[e];
-            vd[e] = a.vnew[e];
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-    }
-
     // The swizzled form: row r = P - q0 of the chunk gets the new K and V, and
     // the V rows after it (stale cache memory, which may hold any bits) become
     // zeros, so the masked positions add exact zeros to p V.
@@ -1745,7 +1585,6 @@ struct Consumer {
         constexpr bool MMA = AK >= 1, KV8 = AK == 2;
         const Geom &g = p.g;
         const AttnSmem a = attn_smem();
-        constexpr int DPL = D / 32;
         int prepared = -1;
         for (uint32_t it = t.begin; it < t.end; ++it) {
             const int h = (int)(it / (uint32_t)g.kv_splits);
@@ -1778,61 +1617,9 @@ struct Consumer {
                 }
                 fence_proxy_async_global();
             }
-            float m[G], l[G], o[G][DPL];
-#pragma unroll
-            for (int i = 0; i < G; ++i) {
-                m[i] = -INFINITY;
-                l[i] = 0.f;
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
-            }
             const uint32_t nch = (uint32_t)(b1 - b0);
-            if (!KV8 && !(MMA && attn_uses_mma(g, (int)nch))) {
-                // few chunks: every warp works on every chunk (one q head, some sub-blocks)
-                const int hi = warp % G, sb0 = warp / G, sbs = kConsumerWarps / G;
-                const int lp = attn_lanes_per_pos(sbs);
-                float m1 = -INFINITY, l1 = 0.f, o1[DPL];
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) o1[e] = 0.f;
-                for (uint32_t k = 0; k < nch; ++k) {
-                    const uint32_t jj = j + k;
-                    uint8_t *slot = wait_chunk(jj);
-                    if (k == 0 && cur_tr && tid == 0 && it == t.begin) cur_tr[kTrFirstChunk] = global_timer();
-                    const int q0 = (b0 + (int)k) * g.kv_block;
-                    int q1 = q0 + g.kv_block;
-                    if (q1 > P + 1) q1 = P + 1;
-                    if (slot && warp == 0 && q0 <= P && P < q1) place_new_kv<D>(slot, q0, a);
-                    if (consumer_sync_or(bad)) break;
-                    switch (lp) {
-                        case 1: attn_chunk_one<D, 1>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
-                        case 2: attn_chunk_one<D, 2>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
-                        case 4: attn_chunk_one<D, 4>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
-                        default: attn_chunk_one<D, (D / 8 >= 8 ? 8 : 4)>(slot, q1 - q0, a, hi, sb0, sbs, m1, l1, o1); break;
-                    }
-                    consumer_sync();
-                    if (tid == 0) mbar_arrive(&s.empty[jj % (uint32_t)g.ring_slots]);
-                }
-#pragma unroll
-                for (int i = 0; i < G; ++i) {
-                    m[i] = i == hi ? m1 : -INFINITY;
-                    l[i] = i == hi ? l1 : 0.f;
-#pragma unroll
-                    for (int e = 0; e < DPL; ++e) o[i][e] = i == hi ? o1[e] : 0.f;
-                }
-                // per-warp states -> shared memory
-                float *ws = a.wstate + (size_t)warp * G * (kPartialPad + D);
-#pragma unroll
-                for (int i = 0; i < G; ++i) {
-                    if (lane == 0) {
-                        ws[i * (kPartialPad + D) + 0] = m[i];
-                        ws[i * (kPartialPad + D) + 1] = l[i];
-                    }
-#pragma unroll
-                    for (int e = 0; e < DPL; ++e)
-                        ws[i * (kPartialPad + D) + kPartialPad + lane * DPL + e] = o[i][e];
-                }
-            } else {
-                // many chunks: each chunk goes to its slot's owner warp, all q heads, tensor cores
+            {
+                // tensor cores: every q head of the group as a B column
                 const int g8 = lane >> 2, t4 = lane & 3;
                 // q head g8 as BF16 pairs (dims 2t4 + 16ks (+8) in word t4 + 8ks (+4))
                 // (the INT8 form reads words 2 t4 and 2 t4 + 1 of each k-step instead)
@@ -1857,24 +1644,55 @@ struct Consumer {
                         consumer_sync();
                         if (tid == 0) mbar_arrive(&s.empty[jj % (uint32_t)g.ring_slots]);
                     }
-                } else {
-                for (uint32_t k = 0; k < nch; ++k) {
-                    const uint32_t jj = j + k;
-                    if (!mine(jj)) continue;
-                    uint8_t *slot = wait_chunk(jj);
-                    if (!slot) break;
-                    const int q0 = (b0 + (int)k) * g.kv_block;
-                    int q1 = q0 + g.kv_block;
-                    if (q1 > P + 1) q1 = P + 1;
-                    if (KV8) {
-                        if (q0 <= P && P < q1) place_new_kv_q8<D>(slot, q0);
-                        attn_chunk_mma_q8<D, G, 2048 / D / 16>(slot, q1 - q0, qcol, g8 < G, mm, ll, oo, 0, 1);
-                    } else {
-                        if (q0 <= P && P < q1) place_new_kv_swz<D>(slot, q0);
-                        attn_chunk_mma<D, G>(slot, q1 - q0, qcol, g8 < G, mm, ll, oo);
+                } else if (!KV8 && !(MMA && attn_owner(g, (int)nch))) {
+                    // a short split (BF16 cache): all warps work on each group of
+                    // resident chunks (at most a ring's worth), one 16-position
+                    // block per warp and round, the group's blocks numbered across
+                    // its chunks; the group is released once all warps are done
+                    const uint32_t ns = (uint32_t)g.ring_slots;
+                    const int nb = g.kv_block / 16;
+                    for (uint32_t k0 = 0; k0 < nch; k0 += ns) {
+                        const uint32_t kn = nch - k0 < ns ? nch - k0 : ns;
+                        for (uint32_t k = k0; k < k0 + kn; ++k) {
+                            uint8_t *slot = wait_chunk(j + k);
+                            if (k == 0 && cur_tr && tid == 0 && it == t.begin) cur_tr[kTrFirstChunk] = global_timer();
+                            const int q0 = (b0 + (int)k) * g.kv_block;
+                            if (slot && warp == 0 && q0 <= P && P < q0 + g.kv_block) place_new_kv_swz<D>(slot, q0);
+                        }
+                        if (consumer_sync_or(bad)) break;
+                        for (uint32_t k = k0; k < k0 + kn; ++k) {
+                            const uint8_t *slot = s.ring + (size_t)((j + k) % ns) * g.slot_bytes;
+                            const int q0 = (b0 + (int)k) * g.kv_block;
+                            int q1 = q0 + g.kv_block;
+                            if (q1 > P + 1) q1 = P + 1;
+                            // group block (k - k0) nb + b goes to warp (k - k0) nb + b mod 8
+                            const int first = ((warp - (int)(k - k0) * nb) % kConsumerWarps + kConsumerWarps) %
+                                              kConsumerWarps;
+                            attn_chunk_mma<D, G, 1>(slot, q1 - q0, qcol, g8 < G, mm, ll, oo, first, kConsumerWarps);
+                        }
+                        consumer_sync();
+                        if (tid == 0)
+                            for (uint32_t k = k0; k < k0 + kn; ++k) mbar_arrive(&s.empty[(j + k) % ns]);
                     }
-                    release_chunk(jj);
-                }
+                } else if constexpr (MMA) {
+                    // a long split: each chunk to its slot's owner warp
+                    for (uint32_t k = 0; k < nch; ++k) {
+                        const uint32_t jj = j + k;
+                        if (!mine(jj)) continue;
+                        uint8_t *slot = wait_chunk(jj);
+                        if (!slot) break;
+                        const int q0 = (b0 + (int)k) * g.kv_block;
+                        int q1 = q0 + g.kv_block;
+                        if (q1 > P + 1) q1 = P + 1;
+                        if (KV8) {
+                            if (q0 <= P && P < q1) place_new_kv_q8<D>(slot, q0);
+                            attn_chunk_mma_q8<D, G, 2048 / D / 16>(slot, q1 - q0, qcol, g8 < G, mm, ll, oo, 0, 1);
+                        } else {
+                            if (q0 <= P && P < q1) place_new_kv_swz<D>(slot, q0);
+                            attn_chunk_mma<D, G, 2048 / D / 16>(slot, q1 - q0, qcol, g8 < G, mm, ll, oo, 0, 1);
+                        }
+                        release_chunk(jj);
+                    }
                 }
                 // per-warp states -> shared memory: l summed over the lanes of a
                 // head (lanes with the same t), then heads 2 t4 and 2 t4 + 1

@@ -32,13 +32,11 @@ static bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 
 static int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
-// Attention scratch in the vec region: q [G][d] f32, new k and v [d] bf16,
-// per-warp probabilities [32][G] f32, per-warp states [G][4 + d] f32, q as
-// bf16 [G][d + 8], and the INT8 cache's new key and value codes [d] with
-// their two scales.
+// Attention scratch in the vec region: new k and v [d] bf16, per-warp states
+// [G][4 + d] f32, q as bf16 [G][d + 8], and the INT8 cache's new key and
+// value codes [d] with their two scales.
 static int attn_vec_bytes(int G, int d) {
-    return G * d * 4 + 2 * d * 2 + kConsumerWarps * 32 * G * 4 +
-           kConsumerWarps * G * (kPartialPad + d) * 4 + G * (d + 8) * 2 + 2 * d + 8;
+    return 2 * d * 2 + kConsumerWarps * G * (kPartialPad + d) * 4 + G * (d + 8) * 2 + 2 * d + 8;
 }
 
 tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o, int n_ctas,
@@ -134,11 +132,13 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     };
     G_.rpc_qkv = rpc(G_.H, 1, G_.qkv_rows, chain);
     G_.rpc_o = rpc(G_.qd, 1, G_.H, chain);
+    // KV block: whole 16-position MMA blocks (whole 32-position rounds from 32
+    // on), at most one TMA box (256 rows)
     int kb = chain / (2 * G_.d * 2);
-    kb = kb >= 32 ? kb / 32 * 32 : kb;
-    kb = std::min(kb, 256);  // a chunk's positions are one TMA box (at most 256 rows)
+    kb = kb >= 32 ? kb / 32 * 32 : kb / 16 * 16;
+    kb = std::min(kb, 256);
     if (G_.kv8) kb = kv8_block(G_.d);
-    if (kb < 1) return fail(TILES_ERR_UNSUPPORTED, "slot too small for one KV position");
+    if (kb < 16) return fail(TILES_ERR_UNSUPPORTED, "slot too small for 16 KV positions");
     G_.kv_block = kb;
     int nb_max = ceil_div(G_.max_pos, kb);
     // default: one KV block per split at the longest context, at most one split
@@ -148,10 +148,10 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     int splits = o.kv_splits > 0 ? o.kv_splits : std::max(1, std::min(nb_max, n_ctas / G_.nkv));
     if (splits < 1 || splits > 256) return fail(TILES_ERR_INVALID_ARG, "kv_splits");
     G_.kv_splits = splits;
-    // the tensor-core attention path (and its kernel instance) only where a
-    // split can hold kConsumerWarps chunks: short-context plans run kernels
-    // without it, whose registers it would otherwise crowd (measured 2.5 %
-    // on the Llama-1B shape at 1,023 positions)
+    // the tensor-core owner form (and its kernel instance) only where a split
+    // can hold kConsumerWarps chunks: short-context plans run kernels without
+    // it, whose registers it would otherwise crowd (measured 2.5 % on the
+    // Llama-1B shape at 1,023 positions)
     G_.attn_mma = (ceil_div(nb_max, splits) >= kConsumerWarps && kb % (2048 / G_.d) == 0) ? 1 : 0;
     if (G_.kv8) G_.attn_mma = 1;  // the INT8 cache has only the tensor-core form
 
@@ -470,7 +470,8 @@ tiles_status_t validate_schedule(const tiles_schedule_s &s, std::string *why) {
             return fail("rows per chunk do not fit a slot");
     }
     const long long kv_chunk = g.kv8 ? kv8_chunk_bytes(g.d) : 2LL * g.kv_block * g.d * 2;
-    if (g.kv_block < 1 || g.kv_block > 256 || kv_chunk > g.slot_bytes) return fail("kv block");
+    if (g.kv_block < 16 || g.kv_block > 256 || g.kv_block % 16 || kv_chunk > g.slot_bytes) return fail("kv block");
+    if (g.attn_mma && g.kv_block % (2048 / g.d)) return fail("kv block not a whole number of tensor-core rounds");
     if (g.kv8 && (g.kv_block != kv8_block(g.d) || !g.attn_mma || g.kv_mp % 16 || g.kv_mp < g.max_pos))
         return fail("INT8 KV chunk geometry");
     if (g.smem_bytes > kSmemLimit) return fail("shared memory");

@@ -45,7 +45,7 @@ struct Geom {
     int res_off;    // in the vec region: residual rows of an O-proj / down tile
     int smem_bytes;
     int attn_mma;   // 1: some attention split can reach kConsumerWarps chunks, and the
-                    // kernel instance carries the tensor-core attention path
+                    // kernel instance carries the tensor-core owner form for them
     int kv8;        // 1: INT8 KV cache (every attention chunk on the tensor-core path)
     int kv_mp;      // INT8 cache: position stride (max_pos rounded up to 16)
 };
@@ -234,19 +234,16 @@ struct KernelParams {
 // trace record words
 constexpr int kTraceWords = 16;
 
-// When an attention item streams at least this many KV chunks (and the plan's
-// kernel instance carries the path), every chunk goes to its slot's owner
-// warp, arrives as a 128-byte-swizzled TMA tile and is reduced on the tensor
-// cores; otherwise all warps share each chunk (linear copies). Producer and
-// consumers decide with the same rule.
-// (The tensor-core form takes 2048 / d positions per round: 32 at d = 64,
-// 16 at d = 128, so kv_block must be a multiple of that.)
-// An INT8 cache has only the tensor-core form: every chunk of every split.
-TILES_HD bool attn_uses_mma(const Geom &g, int n_chunks) {
-    return g.attn_mma && (g.kv8 || (n_chunks >= kConsumerWarps && g.kv_block % (2048 / g.d) == 0));
-}
-// The kernel instance a plan runs: 0 shared-chunk attention only, 1 with the
-// tensor-core form, 2 INT8 KV cache.
+// Attention chunks arrive as 128-byte-swizzled TMA tiles of whole KV blocks
+// (a multiple of 16 positions) and are reduced on the tensor cores. A split of
+// at least kConsumerWarps chunks gives each chunk to its slot's owner warp, in
+// rounds of 2048 / d positions (32 at d = 64, 16 at d = 128, so the block must
+// be a multiple of that; kernel instances compiled with the owner form only);
+// a shorter split shares its chunks across all warps, one 16-position block
+// per warp and round. Producer and consumers decide with the same rule.
+TILES_HD bool attn_owner(const Geom &g, int n_chunks) { return g.attn_mma && n_chunks >= kConsumerWarps; }
+// The kernel instance a plan runs: 0 shared-chunk attention only, 1 also the
+// owner form for long splits, 2 INT8 KV cache.
 TILES_HD int attn_kind(const Geom &g) { return g.kv8 ? 2 : g.attn_mma; }
 
 enum { kTrWaitStart = 0, kTrWaitEnd, kTrTaskEnd, kTrProdFirst, kTrProdLast, kTrProdStall,
