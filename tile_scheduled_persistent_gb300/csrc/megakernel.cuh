@@ -1719,18 +1719,28 @@ struct Consumer {
                 }
             }
             j += nch;
-            // per-warp states -> one partial for (q heads, split c)
+            // per-warp states -> one partial for (q heads, split c): first each
+            // (head, warp) state's weight e^(m_w - M) into word 2 of the state
+            // (0 for a head no warp saw), then the outputs
+            consumer_sync();
+            if (tid < G * kConsumerWarps) {
+                const int i = tid / kConsumerWarps, w = tid % kConsumerWarps;
+                float M = -INFINITY;
+                for (int v = 0; v < kConsumerWarps; ++v)
+                    M = fmaxf(M, a.wstate[((size_t)v * G + i) * (kPartialPad + D)]);
+                float *st = a.wstate + ((size_t)w * G + i) * (kPartialPad + D);
+                st[2] = M == -INFINITY ? 0.f : expf(st[0] - M);
+                st[3] = M;
+            }
             consumer_sync();
             for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
                 const int i = idx / D, dd = idx % D;
-                float M = -INFINITY;
-                for (int w = 0; w < kConsumerWarps; ++w)
-                    M = fmaxf(M, a.wstate[((size_t)w * G + i) * (kPartialPad + D)]);
+                const float M = a.wstate[(size_t)i * (kPartialPad + D) + 3];
                 float L = 0.f, O = 0.f;
                 if (M != -INFINITY) {
                     for (int w = 0; w < kConsumerWarps; ++w) {
                         const float *st = a.wstate + ((size_t)w * G + i) * (kPartialPad + D);
-                        const float sc = expf(st[0] - M);
+                        const float sc = st[2];
                         L = fmaf(sc, st[1], L);
                         O = fmaf(sc, st[kPartialPad + dd], O);
                     }
@@ -1770,6 +1780,7 @@ struct Consumer {
         if (e0 >= e1) return;
         const int ne = e1 - e0;
         float *st = reinterpret_cast<float *>(s.vec);  // [ne][S][3]: m, l, o
+        float *wt = st + (size_t)ne * S * 3;           // [heads of the slice][S]: e^(m_c - M)
         const uint32_t tg = tag(cur_layer, kTagPart);
         for (int q = tid; q < ne * S; q += kConsumerWarps * 32) {
             const int e = e0 + q / S, cc = q % S;
@@ -1792,15 +1803,26 @@ struct Consumer {
         }
         consumer_sync();
         if (cur_tr && tid == 0) cur_tr[kTrMergeIn] = global_timer();
+        // m and l belong to a (q head, split), so the weights are taken once per
+        // head of the slice, from its first element's staged copies
+        const int hq0 = e0 / D, nhq = (e1 - 1) / D - hq0 + 1;
+        for (int q = tid; q < nhq * S; q += kConsumerWarps * 32) {
+            const int hl = q / S, cc = q % S;
+            const int ef = (hq0 + hl) * D > e0 ? (hq0 + hl) * D : e0;
+            const float *sq = st + (size_t)(ef - e0) * S * 3;
+            float M = -INFINITY;
+            for (int c2 = 0; c2 < S; ++c2) M = fmaxf(M, sq[c2 * 3]);
+            const float mc = sq[cc * 3];
+            wt[q] = mc == -INFINITY ? 0.f : expf(mc - M);
+        }
+        consumer_sync();
         const uint32_t to = tag(cur_layer, kTagO) << 16;
         for (int q = tid; q < ne; q += kConsumerWarps * 32) {
             const float *sq = st + (size_t)q * S * 3;
-            float M = -INFINITY;
-            for (int cc = 0; cc < S; ++cc) M = fmaxf(M, sq[cc * 3]);
+            const float *wq = wt + (size_t)((e0 + q) / D - hq0) * S;
             float L = 0.f, O = 0.f;
             for (int cc = 0; cc < S; ++cc) {
-                const float mc = sq[cc * 3];
-                const float w = mc == -INFINITY ? 0.f : expf(mc - M);
+                const float w = wq[cc];
                 L = fmaf(w, sq[cc * 3 + 1], L);
                 O = fmaf(w, sq[cc * 3 + 2], O);
             }

@@ -156,9 +156,11 @@ tiles_status_t resolve_geom(const tiles_model_desc &d, const tiles_plan_opts &o,
     if (G_.kv8) G_.attn_mma = 1;  // the INT8 cache has only the tensor-core form
 
     // an attention tile merges a 1/S slice of its KV head's G d outputs,
-    // staging (m, l, o) of every (output, split) pair: 3 floats each
-    const int merge_pairs = ceil_div(G * G_.d, splits) * splits;
-    int vec = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, attn_vec_bytes(G, G_.d), merge_pairs * 12});
+    // staging (m, l, o) of every (output, split) pair (3 floats each) and a
+    // weight per (q head of the slice, split)
+    const int per = ceil_div(G * G_.d, splits);
+    const int merge_bytes = per * splits * 12 + (ceil_div(per, G_.d) + 1) * splits * 4;
+    int vec = std::max({2 * G_.H, 2 * G_.qd, 2 * G_.F, attn_vec_bytes(G, G_.d), merge_bytes});
     // residual rows of an O-proj / down tile follow (a tile has at most H rows)
     G_.res_off = round_up(vec, 16);
     G_.vec_bytes = round_up(G_.res_off + 2 * G_.H, 128);
