@@ -16,7 +16,11 @@
 //     the last stage, to the "done" mbarrier;
 //   - all four warps: tensor memory -> registers (tcgen05.ld, warp w owns
 //     rows 32 w .. 32 w + 31) -> C, one token column at a time, so each warp
-//     writes 32 consecutive m of one token.
+//     writes 32 consecutive m of one token. For the gate/up projection with
+//     one split, the epilogue applies the SwiGLU instead: rows come in
+//     (gate, up) pairs, so lane 2i pairs its gate sum with lane 2i + 1's up
+//     sum and writes a[t][m / 2] = R(silu(g) u) in BF16, with the arithmetic
+//     of the separate SwiGLU kernel (the split sum 0 + g first).
 // Every wait is bounded: past the limit the CTA records a timeout in the
 // status word, lets what it issued finish (bounded too), frees its tensor
 // memory and returns.
@@ -102,10 +106,11 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, unsigned
     }
 }
 
+template <bool SWIGLU>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ TensorMap mw, const __grid_constant__ TensorMap mx, int M, int T, int K,
-                   int kps, int n_tile, int stages, float *__restrict__ C, uint32_t *status,
-                   unsigned long long timeout_ns) {
+                   int kps, int n_tile, int stages, float *__restrict__ C, uint16_t *__restrict__ act,
+                   uint32_t *status, unsigned long long timeout_ns) {
     extern __shared__ __align__(1024) uint8_t tsm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t b_bytes = (uint32_t)n_tile * 128u;
@@ -194,10 +199,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = 0.f;  // an empty split adds zeros
             }
+            if constexpr (SWIGLU) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = c0 + j;
-                if (m < M && t < T) Cz[(size_t)t * M + m] = v[j];
+                for (int j = 0; j < 16; ++j) {
+                    const int t = c0 + j;
+                    const float up = __shfl_down_sync(0xFFFFFFFFu, v[j], 1);
+                    if (!(lane & 1) && m < M && t < T) {
+                        const float gt = __fadd_rn(0.f, v[j]), u = __fadd_rn(0.f, up);
+                        const float silu = __fdiv_rn(gt, __fadd_rn(1.0f, expf(-gt)));
+                        act[(size_t)t * (M / 2) + m / 2] = f2bf(__fmul_rn(silu, u));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = c0 + j;
+                    if (m < M && t < T) Cz[(size_t)t * M + m] = v[j];
+                }
             }
         }
     } else if (!ok && tid == 0) {
@@ -245,14 +263,25 @@ TcShape tc_shape(int M, int T, int K, int sms, int max_sk) {
 }
 
 cudaError_t gemm_tc_configure() {
-    return cudaFuncSetAttribute((const void *)gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                200 * 1024 + (int)sizeof(TcCtl) + 1024);
+    const int bytes = 200 * 1024 + (int)sizeof(TcCtl) + 1024;
+    cudaError_t e = cudaFuncSetAttribute((const void *)gemm_tc_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute((const void *)gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 bytes);
+    return e;
 }
 
 cudaError_t gemm_tc_launch(const TensorMap &mw, const TensorMap &mx, const TcShape &s, int M, int T, int K,
-                           float *C, uint32_t *status, unsigned long long timeout_ns, cudaStream_t st) {
-    gemm_tc_kernel<<<dim3(s.mt, 1, s.sk), kTcThreads, s.smem, st>>>(mw, mx, M, T, K, s.kps, s.n_tile, s.stages, C,
-                                                                    status, timeout_ns);
+                           float *C, uint16_t *act, uint32_t *status, unsigned long long timeout_ns,
+                           cudaStream_t st) {
+    if (act && (s.sk != 1 || M % 2)) return cudaErrorInvalidValue;
+    if (act)
+        gemm_tc_kernel<true><<<dim3(s.mt, 1, s.sk), kTcThreads, s.smem, st>>>(mw, mx, M, T, K, s.kps, s.n_tile,
+                                                                              s.stages, C, act, status, timeout_ns);
+    else
+        gemm_tc_kernel<false><<<dim3(s.mt, 1, s.sk), kTcThreads, s.smem, st>>>(mw, mx, M, T, K, s.kps, s.n_tile,
+                                                                               s.stages, C, act, status, timeout_ns);
     return cudaGetLastError();
 }
 

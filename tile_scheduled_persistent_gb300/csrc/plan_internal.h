@@ -24,8 +24,11 @@ struct TcShape {
 };
 TcShape tc_shape(int M, int T, int K, int sms, int max_sk);
 cudaError_t gemm_tc_configure();
+// act: null, or (one split only, M even, rows in gate/up pairs) the SwiGLU
+// output bf16 [T][M / 2] in place of C
 cudaError_t gemm_tc_launch(const TensorMap &mw, const TensorMap &mx, const TcShape &s, int M, int T, int K,
-                           float *C, uint32_t *status, unsigned long long timeout_ns, cudaStream_t st);
+                           float *C, uint16_t *act, uint32_t *status, unsigned long long timeout_ns,
+                           cudaStream_t st);
 }  // namespace fwd
 }  // namespace tiles
 #endif
