@@ -152,10 +152,10 @@ def test_plan_runs_after_the_packed_weights_are_freed(tsp):
 
 
 # ------------------------------------------------------------------ tensor-core attention
-# An attention item whose KV split spans at least 8 chunks takes the tensor-
-# core path (swizzled TMA tiles, m16n8k16 MMAs); fewer, the shared-chunk path.
-# With 2 splits these contexts give splits of 7 to 9 chunks, so layers mix
-# both paths, and the last block runs past max_pos in "d64_g2" (the tiled copy
+# An attention item whose KV split spans at least 8 chunks gives each chunk
+# to one warp; fewer, all warps share each group of chunks (both forms on the
+# tensor cores: swizzled TMA tiles, m16n8k16 MMAs). With 2 splits these
+# contexts give splits of 7 to 9 chunks, so layers mix both forms, and the last block runs past max_pos in "d64_g2" (the tiled copy
 # fills those rows with zeros).
 MMA = {
     "d64_g2": replace(S.CONFIGS["tiny"], name="m1", start_pos=955, n_prompt=2, n_new=24, max_pos=1000,

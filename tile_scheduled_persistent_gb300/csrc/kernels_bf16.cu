@@ -1,7 +1,7 @@
 // Kernel instances with BF16 weights: one per (head_dim, q heads per KV head),
 // a smaller instruction footprint than one kernel that switches between them
 // (measured on the Llama-1B shape: 2.7 % faster). These leave out the
-// tensor-core attention path, which only long-context plans use.
+// one-warp-per-chunk attention form, which only long-context plans use.
 #include "megakernel.cuh"
 
 namespace tiles {

@@ -1,5 +1,6 @@
-// Kernel instances with BF16 weights and the tensor-core attention path, for
-// plans whose attention splits can hold 8 or more KV chunks (long contexts).
+// Kernel instances with BF16 weights and the one-warp-per-chunk attention
+// form, for plans whose attention splits can hold 8 or more KV chunks (long
+// contexts).
 #include "megakernel.cuh"
 
 namespace tiles {

@@ -1,5 +1,5 @@
 // Kernel instances with INT8 weights: one per (head_dim, q heads per KV head),
-// without the tensor-core attention path.
+// without the one-warp-per-chunk attention form.
 #include "megakernel.cuh"
 
 namespace tiles {

@@ -1,5 +1,5 @@
-// Kernel instances with INT8 weights and the tensor-core attention path (long
-// contexts).
+// Kernel instances with INT8 weights and the one-warp-per-chunk attention
+// form (long contexts).
 #include "megakernel.cuh"
 
 namespace tiles {

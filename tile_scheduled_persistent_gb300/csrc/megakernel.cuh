@@ -615,8 +615,8 @@ struct Producer {
         return true;
     }
 
-    // AK: attention kind of the kernel instance (0 shared chunks only, 1 with
-    // the tensor-core form, 2 INT8 cache)
+    // AK: attention kind of the kernel instance (0 shared chunks only, 1 also
+    // one warp per chunk for long splits, 2 INT8 cache)
     template <int AK>
     __device__ __forceinline__ void run(int cta) {
         const Geom &g = p.g;
@@ -1936,8 +1936,8 @@ struct Consumer {
     }
 };
 
-// AK, the attention kind: 0 shared chunks only; 1 also the tensor-core form
-// for long splits; 2 INT8 KV cache (tensor-core form only).
+// AK, the attention kind: 0 shared chunks only; 1 also one warp per chunk for
+// long splits; 2 INT8 KV cache. Every form runs on the tensor cores.
 template <int D, int G, bool Q8, int AK>
 __global__ void __launch_bounds__(kThreads, 1) tiles_megakernel(const __grid_constant__ KernelParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];

@@ -243,7 +243,7 @@ constexpr int kTraceWords = 16;
 // per warp and round. Producer and consumers decide with the same rule.
 TILES_HD bool attn_owner(const Geom &g, int n_chunks) { return g.attn_mma && n_chunks >= kConsumerWarps; }
 // The kernel instance a plan runs: 0 shared-chunk attention only, 1 also the
-// owner form for long splits, 2 INT8 KV cache.
+// one-warp-per-chunk form for long splits, 2 INT8 KV cache.
 TILES_HD int attn_kind(const Geom &g) { return g.kv8 ? 2 : g.attn_mma; }
 
 enum { kTrWaitStart = 0, kTrWaitEnd, kTrTaskEnd, kTrProdFirst, kTrProdLast, kTrProdStall,
