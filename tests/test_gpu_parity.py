@@ -194,14 +194,24 @@ def test_tensor_core_attention_matches_oracle(tsp, name):
         assert (got[:, :, end:] == 0x7FC0).all()
 
 
-def test_few_ctas_and_small_ring(tsp):
-    """A plan on 7 CTAs with a 2-slot ring and 3 KV splits still matches."""
+@pytest.mark.parametrize("case", ["splits3", "one_split_groups", "one_split_owner"])
+def test_few_ctas_and_small_ring(tsp, case):
+    """A plan on 7 CTAs with a 2-slot ring still matches:
+    - 3 KV splits (one chunk each);
+    - one split of 3 chunks: the shared attention form takes them in groups
+      of the ring's 2 slots (2, then 1);
+    - one split of 9-10 chunks at 520+ positions: the one-warp-per-chunk form,
+      with only warps 0 and 1 owning slots."""
     cfg = VARIANTS["g2_cache"]
+    if case == "one_split_owner":
+        cfg = replace(cfg, name="v3o", start_pos=520, max_pos=600)
     w, k, v, prompt = inputs(cfg)
     prompt = prompt[: cfg.n_prompt]
-    plan = _plan(tsp, cfg, w, n_ctas=7, ring_slots=2, kv_splits=3)
+    plan = _plan(tsp, cfg, w, n_ctas=7, ring_slots=2, kv_splits=3 if case == "splits3" else 1)
+    info = plan.info()
+    assert info["attn_tensor_cores"] == (1 if case == "one_split_owner" else 0)
     toks, logits, *_ = gpu_run(plan, cfg, k, v, prompt, cfg.start_pos, cfg.n_new)
-    check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new, "7 CTAs")
+    check_parity(toks, logits, cfg, w, k, v, prompt, cfg.start_pos, cfg.n_new, f"7 CTAs, {case}")
     plan.close()
 
 
