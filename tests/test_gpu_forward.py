@@ -235,14 +235,16 @@ def test_verify_loop_emits_the_greedy_tokens(tsp, lively):
     print({"verify loop agrees with greedy for": d})
 
 
-@pytest.mark.parametrize("name,n", [("llama1b", 64), ("qwen3_0_6b", 40), ("llama1b", 512), ("llama1b", 17)],
-                         ids=["llama1b_64", "qwen3_0_6b_40", "llama1b_512", "llama1b_17"])
+@pytest.mark.parametrize("name,n", [("llama1b", 64), ("qwen3_0_6b", 40), ("llama1b", 512), ("llama1b", 17),
+                                    ("qwen3_4b", 17)],
+                         ids=["llama1b_64", "qwen3_0_6b_40", "llama1b_512", "llama1b_17", "qwen3_4b_17"])
 def test_forward_full_width_one_layer_slice(tsp, name, n):
     """Full width (hidden, heads, FFN, vocab) at one layer: a pass of n tokens
     after the workload's cached positions (a 512-token prompt from position 0
     for the third case), every logit within the strict tolerance. 17 tokens
-    of the Llama-1B shape take the SwiGLU in the gate/up projection's
-    epilogue (one split, a short pass); the others the separate kernel."""
+    of the Llama-1B and Qwen3-4B shapes (head_dim 64 and 128, q/k norm in
+    the second) take the SwiGLU in the gate/up projection's epilogue (one
+    split, a short pass); the others the separate kernel."""
     base = replace(S.CONFIGS[name], n_layers=1, gain_sigma=GAINS)
     cfg = base if n < 512 else base.with_workload(start_pos=0, max_pos=520)
     w, k, v, _ = inputs(cfg)
